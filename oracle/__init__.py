@@ -1,0 +1,274 @@
+"""Oracle for fixed-codebook lossless coding of e4m3 byte tensors.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
+package.  It wraps ``ecc_oracle.c`` -- a plain, bit-serial C implementation
+that shares no code with the CUDA library -- with NumPy marshalling, and adds
+the few float64 figures that are one-liners on top of it.
+
+Every function cites the page passage it follows (see the header of
+``ecc_oracle.c`` for the page list and for the readings taken where the pages
+are silent).
+
+Parity status: the QLC tables, Huffman lengths, canonical codes, codec and
+figures are pinned by the tests in ``tests/test_oracle_pins.py``.  The
+container layout (chunk padding, offsets, sub-block bit counts) is this
+library's own format: the pages fix nothing about it, so beyond round-trip
+and bit-count invariants it is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ecc_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libecc_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ARG, CAPACITY, CORRUPT, CODEBOOK = 0, 1, 2, 3, 4
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: oracle status {code}")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, libm)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ct.CDLL(build())
+        P = ct.c_void_p
+        U64, U32, I32 = ct.c_uint64, ct.c_uint32, ct.c_int
+        sig = {
+            "eo_histogram": (None, [P, U64, P]),
+            "eo_rank": (None, [P, P, P]),
+            "eo_qlc_layout": (I32, [P, P, P]),
+            "eo_qlc_codebook": (I32, [P, P, P, P, P]),
+            "eo_qlc_search": (I32, [P, I32, I32, I32, P, P]),
+            "eo_huffman_lengths": (I32, [P, P]),
+            "eo_canonical_codes": (I32, [P, P]),
+            "eo_encode": (I32, [P, U64, P, P, U32, U32, P, U64, P, P, P]),
+            "eo_decode_qlc": (I32, [P, U64, P, P, U64, U32, U32, P, P, P]),
+            "eo_decode_huffman": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
+            "eo_entropy_bits": (ct.c_double, [P]),
+            "eo_kl_bits": (ct.c_double, [P, P]),
+            "eo_code_bits": (U64, [P, P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ct.c_void_p)
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _u64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint64)
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise OracleError(code, what)
+
+
+# ---------------------------------------------------------------- statistics
+
+def histogram(x) -> np.ndarray:
+    """count[b] = number of bytes equal to b (Single-Stage Huffman,
+    Methodology step 1)."""
+    x = _u8(x)
+    out = np.zeros(256, np.uint64)
+    _load().eo_histogram(_p(x), x.size, _p(out))
+    return out
+
+
+def fixed_codebook_weights(counts) -> np.ndarray:
+    """Weights of the single-stage codebook: the pooled counts of the warm-up
+    batches plus a pseudocount of one per byte.  With equal-size batches the
+    pooled counts are the average PMF times the total (Single-Stage Huffman,
+    TL;DR and Methodology step 2); the pseudocount gives every byte a code."""
+    w = np.ones(256, np.uint64)
+    for c in counts:
+        w += _u64(c)
+    return w
+
+
+# ---------------------------------------------------------------- QLC
+
+def rank(count):
+    """(rank, by_rank): bytes sorted by count descending, ties by byte value
+    (Quad Length Codes, section 2, LUT paragraph)."""
+    count = _u64(count)
+    r = np.zeros(256, np.uint8)
+    br = np.zeros(256, np.uint8)
+    _load().eo_rank(_p(count), _p(r), _p(br))
+    return r, br
+
+
+BASE_WIDTHS = (3, 3, 3, 3, 3, 4, 5, 8)
+
+
+def qlc_layout(width):
+    """(start, size, covered) of the 8 areas filled in rank order."""
+    w = _u8(width)
+    start = np.zeros(8, np.int32)
+    size = np.zeros(8, np.int32)
+    covered = _load().eo_qlc_layout(_p(w), _p(start), _p(size))
+    return start, size, covered
+
+
+def qlc_codebook(count, width=BASE_WIDTHS) -> dict:
+    """Per-byte QLC code (len, code) plus by_rank, for the given widths."""
+    count = _u64(count)
+    w = _u8(width)
+    ln = np.zeros(256, np.uint8)
+    code = np.zeros(256, np.uint64)
+    br = np.zeros(256, np.uint8)
+    _check(_load().eo_qlc_codebook(_p(count), _p(w), _p(ln), _p(code), _p(br)), "qlc_codebook")
+    return {"family": "qlc", "width": w.copy(), "len": ln, "code": code, "by_rank": br}
+
+
+def qlc_search(count, max_distinct=4, require_full=False, nondecreasing_only=True):
+    """Adapted-QLC widths by exhaustive search; returns (width, cost_bits)."""
+    count = _u64(count)
+    w = np.zeros(8, np.uint8)
+    cost = np.zeros(1, np.uint64)
+    _check(_load().eo_qlc_search(_p(count), int(max_distinct), int(bool(require_full)),
+                                 int(bool(nondecreasing_only)), _p(w), _p(cost)), "qlc_search")
+    return w, int(cost[0])
+
+
+# ---------------------------------------------------------------- Huffman
+
+def huffman_lengths(weight) -> np.ndarray:
+    weight = _u64(weight)
+    ln = np.zeros(256, np.uint8)
+    _check(_load().eo_huffman_lengths(_p(weight), _p(ln)), "huffman_lengths")
+    return ln
+
+
+def canonical_codes(length) -> np.ndarray:
+    ln = _u8(length)
+    code = np.zeros(256, np.uint64)
+    _check(_load().eo_canonical_codes(_p(ln), _p(code)), "canonical_codes")
+    return code
+
+
+def huffman_codebook(weight) -> dict:
+    """Canonical Huffman code of a weight vector (Single-Stage Huffman,
+    Methodology step 3)."""
+    ln = huffman_lengths(weight)
+    return {"family": "huffman", "len": ln, "code": canonical_codes(ln)}
+
+
+# ---------------------------------------------------------------- codec
+
+def max_encoded_bytes(n: int, C: int, max_len: int) -> int:
+    """Upper bound of the container payload: every symbol at max_len bits,
+    each chunk padded to 16 bytes."""
+    full, tail = divmod(n, C)
+    per = lambda L: (L * max_len + 7) // 8 // 1
+    tot = full * ((per(C) + 15) // 16 * 16)
+    if tail:
+        tot += (per(tail) + 15) // 16 * 16
+    return tot
+
+
+def encode(x, cb: dict, C: int, S: int, cap: int | None = None) -> dict:
+    """Bit-serial encode into the chunked container."""
+    x = _u8(x)
+    n = x.size
+    ln = _u8(cb["len"])
+    code = _u64(cb["code"])
+    if cap is None:
+        cap = max_encoded_bytes(n, C, int(ln.max()) if n else 1)
+    out = np.zeros(max(cap, 1), np.uint8)
+    n_chunks = -(-n // C)
+    chunk_off = np.zeros(n_chunks + 1, np.uint64)
+    sub_bits = np.zeros(max(-(-n // S), 1), np.uint16)
+    total = np.zeros(1, np.uint64)
+    _check(_load().eo_encode(_p(x), n, _p(ln), _p(code), C, S, _p(out), cap,
+                             _p(chunk_off), _p(sub_bits), _p(total)), "encode")
+    used = int(chunk_off[-1])
+    return {"payload": out[:used].copy(), "chunk_off": chunk_off,
+            "sub_bits": sub_bits[:-(-n // S)].copy(), "total_bits": int(total[0]),
+            "n": n, "C": C, "S": S}
+
+
+def decode(enc: dict, cb: dict) -> np.ndarray:
+    """Bit-serial decode of a container produced by encode()."""
+    payload = _u8(enc["payload"])
+    n, C, S = enc["n"], enc["C"], enc["S"]
+    chunk_off = _u64(enc["chunk_off"])
+    sub_bits = np.ascontiguousarray(enc["sub_bits"], dtype=np.uint16)
+    if sub_bits.size == 0:
+        sub_bits = np.zeros(1, np.uint16)
+    out = np.zeros(max(n, 1), np.uint8)
+    buf = payload if payload.size else np.zeros(1, np.uint8)
+    lib = _load()
+    if cb["family"] == "qlc":
+        rc = lib.eo_decode_qlc(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
+                               _p(_u8(cb["width"])), _p(_u8(cb["by_rank"])), _p(out))
+    else:
+        rc = lib.eo_decode_huffman(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
+                                   _p(_u8(cb["len"])), _p(out))
+    _check(rc, "decode")
+    return out[:n]
+
+
+# ---------------------------------------------------------------- figures
+
+def entropy_bits(count) -> float:
+    """Shannon entropy H = -sum p log2 p, bits per symbol."""
+    return float(_load().eo_entropy_bits(_p(_u64(count))))
+
+
+def kl_bits(p_count, q_count) -> float:
+    """D(P || Q) in bits (Single-Stage Huffman, Figure 3)."""
+    return float(_load().eo_kl_bits(_p(_u64(p_count)), _p(_u64(q_count))))
+
+
+def code_bits(count, length) -> int:
+    """Total payload bits sum(count x length) of a codebook on a histogram."""
+    v = int(_load().eo_code_bits(_p(_u64(count)), _p(_u8(length))))
+    if v == (1 << 64) - 1:
+        raise OracleError(CODEBOOK, "code_bits: a counted byte has no code")
+    return v
+
+
+def compressibility(bits: int, n: int) -> float:
+    """1 - mean code length / 8: the fraction of the 8-bit container saved
+    (the pages quote it in percent, e.g. 15.9% for FFN1 Huffman)."""
+    return 1.0 - bits / (8.0 * n)
+
+
+def shannon_compressibility(count) -> float:
+    return 1.0 - entropy_bits(count) / 8.0

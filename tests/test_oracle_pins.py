@@ -1,0 +1,377 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test ties an oracle function to something the pages print, to a closed
+form, to a textbook result, to an exhaustive search, or to an invariant of
+prefix codes, so that a dropped term, a wrong index or a swapped operand in
+the oracle fails at least one of them.
+"""
+import itertools
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import golden
+from workloads import np_gauss, np_grad, np_zero_spike, qlc_base_tensor
+
+C16K, S256 = 16384, 256
+
+
+def bits_of(code, length):
+    return format(int(code), "b").zfill(int(length)) if length else ""
+
+
+def pack_bits(bitstring):
+    """Pack a '0'/'1' string MSB-first into bytes (test-side helper)."""
+    pad = (-len(bitstring)) % 8
+    s = bitstring + "0" * pad
+    return np.array([int(s[i:i + 8], 2) for i in range(0, len(s), 8)], np.uint8)
+
+
+def prefix_free(codes):
+    """Brute force: no codeword is a prefix of another."""
+    for a, b in itertools.permutations(codes, 2):
+        if b.startswith(a):
+            return False
+    return True
+
+
+def kraft(lengths):
+    return sum(Fraction(1, 2 ** int(L)) for L in lengths if L > 0)
+
+
+@pytest.fixture(scope="module")
+def gauss_counts():
+    return oracle.histogram(qlc_base_tensor())
+
+
+@pytest.fixture(scope="module")
+def spike_counts():
+    return oracle.histogram(np_zero_spike(1 << 20, (3, 99)))
+
+
+# --------------------------------------------------------------- base QLC
+
+def test_base_layout_matches_page():
+    start, size, covered = oracle.qlc_layout(oracle.BASE_WIDTHS)
+    rows = golden("qlc_base_layout.txt")
+    assert covered == 256
+    for k, (area, nsym, pre, suf, tot) in enumerate(rows):
+        assert int(area) == k + 1
+        assert size[k] == int(nsym)
+        assert oracle.BASE_WIDTHS[k] == int(suf)
+        assert int(pre) + int(suf) == int(tot)
+    cb = oracle.qlc_codebook(np.arange(256)[::-1].astype(np.uint64))
+    lens = sorted(set(cb["len"].tolist()))
+    assert lens == sorted({int(r[4]) for r in rows})
+
+
+def test_base_codes_golden():
+    # counts 256..1 make rank r the byte r, so code(byte r) is code(rank r)
+    cb = oracle.qlc_codebook(np.arange(256, 0, -1).astype(np.uint64))
+    assert (cb["by_rank"] == np.arange(256)).all()
+    for r, word in golden("qlc_base_codes.txt"):
+        r = int(r)
+        assert bits_of(cb["code"][r], cb["len"][r]) == word
+
+
+def test_base_kraft_closed_form():
+    cb = oracle.qlc_codebook(np.ones(256, np.uint64))
+    # 40/64 + 16/128 + 32/256 + 168/2048: prefix-free but not complete
+    assert kraft(cb["len"]) == Fraction(40, 64) + Fraction(16, 128) + Fraction(32, 256) + Fraction(168, 2048)
+    assert float(kraft(cb["len"])) == 0.95703125
+
+
+def test_base_has_four_lengths_and_is_prefix_free(gauss_counts):
+    cb = oracle.qlc_codebook(gauss_counts)
+    assert sorted(set(cb["len"].tolist())) == [6, 7, 8, 11]
+    assert prefix_free([bits_of(c, L) for c, L in zip(cb["code"], cb["len"])])
+
+
+def test_rank_order_and_ties():
+    count = np.zeros(256, np.uint64)
+    count[[200, 3, 77]] = 5          # a three-way tie at the top
+    count[10] = 4
+    r, br = oracle.rank(count)
+    assert list(br[:4]) == [3, 77, 200, 10]
+    assert (r[br] == np.arange(256)).all()
+    # zero-count bytes still get ranks, in byte order
+    rest = [b for b in range(256) if b not in (3, 77, 200, 10)]
+    assert list(br[4:]) == rest
+
+
+def test_qlc_decode_reads_prefix_then_suffix():
+    # hand-assembled stream of ranks 0, 40, 56, 88, 255 under the base code
+    words = {int(r): w for r, w in golden("qlc_base_codes.txt")}
+    ranks = [0, 40, 56, 88, 255]
+    stream = "".join(words[r] for r in ranks)
+    payload = pack_bits(stream)
+    payload = np.concatenate([payload, np.zeros((-payload.size) % 16, np.uint8)])
+    count = np.arange(256, 0, -1).astype(np.uint64)
+    cb = oracle.qlc_codebook(count)
+    enc = {"payload": payload, "chunk_off": np.array([0, payload.size], np.uint64),
+           "sub_bits": np.array([len(stream)], np.uint16), "n": 5, "C": 1024, "S": 64}
+    assert list(oracle.decode(enc, cb)) == ranks
+    # and the oracle's encoder writes the same bits
+    e = oracle.encode(np.array(ranks, np.uint8), cb, 1024, 64)
+    assert (e["payload"] == payload).all()
+    assert e["total_bits"] == len(stream)
+
+
+def test_unused_qlc_suffix_is_corrupt():
+    cb = oracle.qlc_codebook(np.arange(256, 0, -1).astype(np.uint64))
+    # area 8 suffix 168 (first unused one): 111 10101000
+    stream = "11110101000"
+    payload = pack_bits(stream)
+    payload = np.concatenate([payload, np.zeros((-payload.size) % 16, np.uint8)])
+    enc = {"payload": payload, "chunk_off": np.array([0, 16], np.uint64),
+           "sub_bits": np.array([11], np.uint16), "n": 1, "C": 1024, "S": 64}
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.decode(enc, cb)
+    assert ei.value.code == oracle.CORRUPT
+
+
+# --------------------------------------------------------------- Huffman
+
+def test_huffman_textbook_example():
+    rows = golden("huffman_textbook.txt")
+    w = np.zeros(256, np.uint64)
+    want = {}
+    for b, wt, L in rows:
+        w[int(b)] = int(wt)
+        want[int(b)] = int(L)
+    ln = oracle.huffman_lengths(w)
+    for b, L in want.items():
+        assert ln[b] == L
+    assert (ln[6:] == 0).all()
+    assert oracle.code_bits(w, ln) == 224
+
+
+def test_huffman_dyadic_and_uniform():
+    w = np.zeros(256, np.uint64)
+    w[:5] = [8, 4, 2, 1, 1]                    # p = 1/2, 1/4, 1/8, 1/16, 1/16
+    assert list(oracle.huffman_lengths(w)[:5]) == [1, 2, 3, 4, 4]
+    for k in range(1, 9):                      # 2^k equal weights -> all length k
+        w = np.zeros(256, np.uint64)
+        w[: 2 ** k] = 7
+        ln = oracle.huffman_lengths(w)
+        assert (ln[: 2 ** k] == k).all() and (ln[2 ** k:] == 0).all()
+
+
+def test_huffman_single_and_absent_symbols():
+    w = np.zeros(256, np.uint64)
+    w[42] = 1000
+    ln = oracle.huffman_lengths(w)
+    assert ln[42] == 1 and ln.sum() == 1
+    cb = oracle.huffman_codebook(w)
+    x = np.full(3000, 42, np.uint8)
+    e = oracle.encode(x, cb, 1024, 64)
+    assert e["total_bits"] == 3000
+    assert (oracle.decode(e, cb) == x).all()
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.encode(np.array([41], np.uint8), cb, 1024, 64)
+    assert ei.value.code == oracle.CODEBOOK
+
+
+def _brute_force_min_cost(weights):
+    """Minimum of sum(w*l) over all length vectors with Kraft sum <= 1, i.e.
+    over all prefix codes (Kraft-McMillan)."""
+    n = len(weights)
+    w = np.array(weights, np.int64)
+    best = None
+    grid = np.array(list(itertools.product(range(1, n), repeat=n)), np.int64)
+    kr = (2.0 ** (-grid)).sum(axis=1)
+    ok = kr <= 1.0 + 1e-12
+    costs = (grid[ok] * w).sum(axis=1)
+    best = int(costs.min())
+    return best
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 6, 7])
+def test_huffman_optimal_against_brute_force(n):
+    g = np.random.default_rng(100 + n)
+    for trial in range(4):
+        wts = g.integers(1, 50, n)
+        w = np.zeros(256, np.uint64)
+        syms = g.choice(256, n, replace=False)
+        w[syms] = wts
+        ln = oracle.huffman_lengths(w)
+        assert oracle.code_bits(w, ln) == _brute_force_min_cost(list(wts))
+
+
+def test_huffman_kraft_canonical_and_entropy_bounds(gauss_counts, spike_counts):
+    for count in (gauss_counts, spike_counts, np.arange(1, 257).astype(np.uint64)):
+        cb = oracle.huffman_codebook(count)
+        ln, code = cb["len"], cb["code"]
+        assert kraft(ln) == 1                                  # complete code
+        words = [bits_of(c, L) for c, L in zip(code, ln) if L]
+        assert prefix_free(words)
+        # canonical: ordering by (length, byte) equals ordering of the
+        # left-aligned code values, and equal-length codes are consecutive
+        order = sorted((int(ln[b]), b) for b in range(256) if ln[b])
+        vals = [int(code[b]) << (64 - int(ln[b])) for _, b in order]
+        assert vals == sorted(vals)
+        for (l1, b1), (l2, b2) in zip(order, order[1:]):
+            if l1 == l2:
+                assert int(code[b2]) == int(code[b1]) + 1
+        # source coding theorem: H <= mean length < H + 1
+        n = int(count.sum())
+        H = oracle.entropy_bits(count)
+        mean = oracle.code_bits(count, ln) / n
+        assert H <= mean + 1e-12 and mean < H + 1
+
+
+def test_mean_length_is_entropy_plus_kl(spike_counts):
+    # For a complete code, sum p*l = H(P) + D(P || 2^-l): ties code bits,
+    # entropy and KL together exactly.
+    cb = oracle.huffman_codebook(spike_counts)
+    ln = cb["len"].astype(np.int64)
+    q = np.where(ln > 0, 2 ** (ln.max() - ln), 0).astype(np.uint64)
+    n = int(spike_counts.sum())
+    lhs = oracle.code_bits(spike_counts, cb["len"]) / n
+    rhs = oracle.entropy_bits(spike_counts) + oracle.kl_bits(spike_counts, q)
+    assert abs(lhs - rhs) < 1e-12 * lhs
+
+
+# --------------------------------------------------------------- figures
+
+def test_entropy_and_kl_closed_forms(gauss_counts):
+    assert oracle.entropy_bits(np.full(256, 3, np.uint64)) == pytest.approx(8.0, abs=1e-15)
+    one = np.zeros(256, np.uint64)
+    one[5] = 9
+    assert oracle.entropy_bits(one) == 0.0
+    two = np.zeros(256, np.uint64)
+    two[[1, 2]] = 11
+    assert oracle.entropy_bits(two) == pytest.approx(1.0, abs=1e-15)
+    # D(P || P) = 0; D(P || uniform) = 8 - H(P); Gibbs: D >= 0
+    assert abs(oracle.kl_bits(gauss_counts, gauss_counts)) < 1e-15
+    uni = np.ones(256, np.uint64)
+    assert oracle.kl_bits(gauss_counts, uni) == pytest.approx(8.0 - oracle.entropy_bits(gauss_counts), abs=1e-12)
+    assert oracle.kl_bits(gauss_counts, np.arange(1, 257).astype(np.uint64)) > 0
+    assert oracle.kl_bits(two, one) == float("inf")
+
+
+# --------------------------------------------------------------- adapted QLC
+
+def test_search_space_reduction_matches_all_orderings(spike_counts):
+    # the search keeps only non-decreasing widths; all 9^8 orderings give the
+    # same optimum (exchange argument, checked exhaustively)
+    w, cost = oracle.qlc_search(spike_counts)
+    w_all, cost_all = oracle.qlc_search(spike_counts, nondecreasing_only=False)
+    assert cost == cost_all
+
+
+def test_adapted_qlc_properties(gauss_counts, spike_counts):
+    n = int(spike_counts.sum())
+    base = oracle.qlc_codebook(spike_counts)
+    base_bits = oracle.code_bits(spike_counts, base["len"])
+    w, cost = oracle.qlc_search(spike_counts)
+    cb = oracle.qlc_codebook(spike_counts, w)
+    assert oracle.code_bits(spike_counts, cb["len"]) == cost
+    assert cost <= base_bits                         # base is in the search space
+    assert len(set(cb["len"].tolist())) <= 4         # still four lengths at most
+    assert prefix_free([bits_of(c, L) for c, L in zip(cb["code"], cb["len"])])
+    huff = oracle.huffman_codebook(spike_counts)
+    hbits = oracle.code_bits(spike_counts, huff["len"])
+    # ordering: Shannon >= Huffman >= adapted QLC >= base QLC (compressibility)
+    assert oracle.shannon_compressibility(spike_counts) >= oracle.compressibility(hbits, n)
+    assert hbits <= cost <= base_bits
+    # on the Gaussian law the base layout is already optimal among 4-length codes
+    wg, cg = oracle.qlc_search(gauss_counts)
+    assert cg == oracle.code_bits(gauss_counts, oracle.qlc_codebook(gauss_counts)["len"])
+    # the strict reading (capacity exactly 256) can only be worse
+    ws, cs = oracle.qlc_search(spike_counts, require_full=True)
+    assert sum(2 ** int(b) for b in ws) == 256 and cs >= cost
+
+
+# --------------------------------------------------------------- codec
+
+@pytest.mark.parametrize("C,S", [(1024, 64), (4096, 128), (16384, 256), (65536, 1024)])
+def test_round_trip_and_bit_count(C, S, gauss_counts):
+    x = np_grad(3 * C + 777, (9, C))                 # several chunks + ragged tail
+    count = oracle.histogram(x)
+    for cb in (oracle.qlc_codebook(count),
+               oracle.qlc_codebook(count, oracle.qlc_search(count)[0]),
+               oracle.huffman_codebook(oracle.fixed_codebook_weights([count]))):
+        e = oracle.encode(x, cb, C, S)
+        assert e["total_bits"] == oracle.code_bits(count, cb["len"])
+        assert int(e["sub_bits"].astype(np.int64).sum()) == e["total_bits"]
+        assert (np.diff(e["chunk_off"].astype(np.int64)) % 16 == 0).all()
+        assert (oracle.decode(e, cb) == x).all()
+
+
+def test_edge_sizes():
+    count = np.arange(256, 0, -1).astype(np.uint64)
+    for cb in (oracle.qlc_codebook(count), oracle.huffman_codebook(count)):
+        for n in (0, 1, 63, 64, 65, 1023, 1024, 1025):
+            x = np.random.default_rng(n).integers(0, 256, n).astype(np.uint8)
+            e = oracle.encode(x, cb, 1024, 64)
+            assert len(e["chunk_off"]) == -(-n // 1024) + 1
+            assert (oracle.decode(e, cb) == x).all()
+
+
+def test_long_codes_round_trip():
+    # Fibonacci weights give the deepest Huffman tree: lengths up to 40 bits
+    w = np.zeros(256, np.uint64)
+    a, b = 1, 1
+    for s in range(41):
+        w[s] = a
+        a, b = b, a + b
+    cb = oracle.huffman_codebook(w)
+    assert cb["len"].max() == 40
+    x = np.arange(41, dtype=np.uint8).repeat(3)
+    e = oracle.encode(x, cb, 1024, 64)
+    assert (oracle.decode(e, cb) == x).all()
+
+
+def test_capacity_error():
+    x = np.zeros(5000, np.uint8)
+    cb = oracle.qlc_codebook(np.ones(256, np.uint64))
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.encode(x, cb, 1024, 64, cap=100)
+    assert ei.value.code == oracle.CAPACITY
+
+
+def test_corruption_is_detected_or_changes_output():
+    x = np_gauss(5000, (7, 1), 1.0)[0]
+    count = oracle.histogram(x)
+    for cb in (oracle.qlc_codebook(count), oracle.huffman_codebook(count)):
+        e = oracle.encode(x, cb, 1024, 64)
+        g = np.random.default_rng(5)
+        for _ in range(20):
+            bad = dict(e)
+            bad["payload"] = e["payload"].copy()
+            bad["payload"][g.integers(0, e["payload"].size)] ^= np.uint8(1 << int(g.integers(0, 8)))
+            try:
+                y = oracle.decode(bad, cb)
+            except oracle.OracleError as err:
+                assert err.code == oracle.CORRUPT
+            else:
+                assert not (y == x).all()
+
+
+# --------------------------------------------------------------- planted mistakes
+
+def test_pins_catch_planted_mistakes(spike_counts):
+    """Plant typical slips in oracle outputs and check a pin fails."""
+    cb = oracle.huffman_codebook(spike_counts)
+    ln = cb["len"].copy()
+    # a dropped level (one length one too short) breaks Kraft
+    i = int(np.argmax(ln))
+    ln_bad = ln.copy()
+    ln_bad[i] -= 1
+    assert kraft(ln_bad) > 1
+    # a swapped pair of lengths loses optimality (cost rises)
+    j, k = int(np.argmax(spike_counts)), int(np.argmin(np.where(ln > 0, spike_counts, 2**63)))
+    ln_sw = ln.copy()
+    ln_sw[j], ln_sw[k] = ln[k], ln[j]
+    assert oracle.code_bits(spike_counts, ln_sw) > oracle.code_bits(spike_counts, ln)
+    # an off-by-one in the rank order changes the QLC cost
+    base = oracle.qlc_codebook(spike_counts)
+    r, br = oracle.rank(spike_counts)
+    ln_q = base["len"].copy()
+    a, b = br[39], br[40]                            # last 6-bit rank, first 7-bit rank
+    assert spike_counts[a] > spike_counts[b]
+    ln_q[a], ln_q[b] = ln_q[b], ln_q[a]
+    assert oracle.code_bits(spike_counts, ln_q) > oracle.code_bits(spike_counts, base["len"])
