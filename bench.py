@@ -1,0 +1,538 @@
+#!/usr/bin/env python3
+"""Encode/decode throughput of e4m3 tensors on GB300.
+
+Workload: the gradient-like e4m3 tensor of 2^30 bytes (x = s_b * t_4, block
+scale s_b = 2^U(-4,4) per 4096 elements, E4M3 RNE saturating), coded with the
+two fixed codebooks built once from 8 warm-up tensors of 2^24 bytes of the
+same law (pooled counts; the Huffman weights add one per byte): the
+single-stage canonical Huffman code and the base Quad Length Code, chunks of
+16 KiB.
+
+A step is one pass of the hot path over the tensor: encode and decode with
+each of the two codebooks (histogram and codebook construction belong to the
+warm-up stage of the single-stage method and are timed separately).  `value`
+is e4m3 bytes encoded and decoded per second, device-resident, max over
+ranks.  `e2e` repeats the step through the Python API from pinned host
+memory, with the host-to-device copy of the tensor and the device-to-host
+read of the Huffman payload inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_DEFAULT = 1 << 30
+CHUNK = 16384
+WARM_TENSORS, WARM_BYTES = 8, 1 << 24
+METRIC = "encode/decode GB/s of e4m3 input on 1 GB300, % of HBM roofline; compressibility %"
+WORKLOAD = "gradient-like e4m3 tensor, 2^30 B (s_b * t_4, s_b = 2^U(-4,4) per 4096 elements)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--n", type=int, default=N_DEFAULT, help="tensor bytes (default 2^30)")
+    p.add_argument("--chunk", type=int, default=CHUNK)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------- ranks
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (timing aggregation; no data exchange)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, wall-stamped."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        import datetime as dt
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                ts = dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if not (t0 - 0.15 <= ts <= t1 + 0.15):
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------- peaks / traffic
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lossless_entropy_coding_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    k = rec.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------- oracle baseline
+
+def oracle_round_trip_rate(x_chunks, codebooks, C, S, seconds_target=10.0, threads=None):
+    """Oracle (bit-serial C) encode + decode of independent chunks on host
+    threads; returns (GB/s of input round-tripped per codebook pass, cores,
+    sample description)."""
+    import numpy as np
+    import oracle
+
+    threads = threads or os.cpu_count() or 1
+
+    def work(chunk):
+        for ocb in codebooks:
+            e = oracle.encode(chunk, ocb, C, S)
+            y = oracle.decode(e, ocb)
+            assert (y == chunk).all()
+        return chunk.size * len(codebooks)
+
+    # calibrate on one chunk per thread, then size the sample (the chunks
+    # are cycled) to about seconds_target of wall time on all threads
+    m = min(threads, len(x_chunks))
+    t = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, x_chunks[:m]))
+    per = (time.perf_counter() - t) / m          # wall seconds per chunk
+    k = max(m, int(seconds_target / max(per, 1e-6)))
+    t = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        done = sum(ex.map(work, (x_chunks[i % len(x_chunks)] for i in range(k))))
+    dt = time.perf_counter() - t
+    return done / dt / 1e9, threads, (f"{k} chunks of {C} B cycled from {len(x_chunks)} distinct chunks of the "
+                                      f"workload, encode+decode with {len(codebooks)} codebooks, {dt:.1f} s")
+
+
+def cpu_sample(n_chunks, C, key=(4, 0)):
+    import numpy as np
+    from workloads import np_grad
+    x = np_grad(n_chunks * C, key)
+    return [x[i * C:(i + 1) * C] for i in range(n_chunks)]
+
+
+def host_codebooks(C):
+    """Oracle codebooks from a host-generated warm-up of the same law."""
+    import oracle
+    from workloads import grad_warmup
+    counts = [oracle.histogram(grad_warmup(i, 1 << 22)) for i in range(2)]
+    pooled = oracle.fixed_codebook_weights(counts)
+    return [oracle.huffman_codebook(pooled), oracle.qlc_codebook(pooled)]
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    C = args.chunk
+    S = min(1024, max(64, C // 64))
+    cbs = host_codebooks(C)
+    threads = os.cpu_count() or 1
+    # per-step sample sized so that warm-up + timed steps take ~90 s
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    chunks = cpu_sample(max(threads, 64), C)
+    rate, cores, _ = oracle_round_trip_rate(chunks, cbs, C, S, seconds_target=0.5)
+    per_chunk = C * len(cbs) / (rate * 1e9)      # wall seconds per chunk, all threads busy
+    k = max(threads, int(budget / per_chunk))
+    sample = [chunks[i % len(chunks)] for i in range(k)]
+
+    def step():
+        def work(chunk):
+            import oracle
+            for ocb in cbs:
+                e = oracle.encode(chunk, ocb, C, S)
+                oracle.decode(e, ocb)
+            return chunk.size * len(cbs)
+        with cf.ThreadPoolExecutor(threads) as ex:
+            return sum(ex.map(work, sample))
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += step()
+    dt = time.perf_counter() - t
+    value = done / dt / 1e9
+    desc = (f"{k} chunks of {C} B per step, cycled from {len(chunks)} distinct chunks of the workload, "
+            f"encode+decode with 2 codebooks")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "chunk": C, "subblock": S, "codebooks": ["fixed Huffman", "base QLC"],
+                   "oracle": "bit-serial C, host threads over chunks"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import lossless_entropy_coding_gb300 as ecc
+    from workloads import dev_grad
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+
+    n, C = args.n, args.chunk
+    S = ecc.default_subblock(C)
+    stream = torch.cuda.current_stream()
+
+    # warm-up stage of the single-stage method: pooled histogram -> codebooks
+    pooled = torch.zeros(256, dtype=torch.int64, device=dev)
+    for i in range(WARM_TENSORS):
+        w = dev_grad(WARM_BYTES, (4, 1 + i), device=dev)
+        ecc.e4m3_histogram(w, pooled)
+    torch.cuda.synchronize()
+    pooled_h = pooled.cpu().numpy().view(np.uint64).copy()
+    cbs = {"huffman": ecc.huff_build_canonical(pooled_h + np.uint64(1)),
+           "qlc": ecc.qlc_build_tables(pooled_h)}
+    dcbs = {k: ecc.to_device(v, dev) for k, v in cbs.items()}
+    max_len = {k: int(ecc.codebook_view(v)["max_len"]) for k, v in cbs.items()}
+
+    x = dev_grad(n, (4, rank), device=dev)
+    xcount = ecc.e4m3_histogram(x)
+    torch.cuda.synchronize()
+    xcount_h = xcount.cpu().numpy().view(np.uint64).copy()
+
+    bufs = {}
+    for k in cbs:
+        bufs[k] = {
+            "out": torch.empty(ecc.max_encoded_bytes(n, C, max_len[k]), dtype=torch.uint8, device=dev),
+            "chunk_off": torch.empty(ecc.num_chunks(n, C) + 1, dtype=torch.int64, device=dev),
+            "sub_bits": torch.empty(ecc.num_subblocks(n, S), dtype=torch.int16, device=dev),
+            "total_bits": torch.empty(1, dtype=torch.int64, device=dev),
+            "status": torch.empty(1, dtype=torch.int32, device=dev),
+            "dstatus": torch.empty(1, dtype=torch.int32, device=dev),
+            "ws": torch.empty(ecc.encode_workspace_bytes(n, C), dtype=torch.uint8, device=dev),
+            "y": torch.empty(n, dtype=torch.uint8, device=dev),
+        }
+
+    def encode(k, src):
+        b = bufs[k]
+        return ecc.ecc_encode(src, dcbs[k], C, S, out=b["out"], chunk_off=b["chunk_off"], sub_bits=b["sub_bits"],
+                              total_bits=b["total_bits"], ws=b["ws"], status=b["status"])
+
+    def decode(k, enc):
+        b = bufs[k]
+        return ecc.ecc_decode(enc, dcbs[k], out=b["y"], status=b["dstatus"])
+
+    kinds = ("huffman", "qlc")
+    EV = torch.cuda.Event
+
+    def step(record=None):
+        for k in kinds:
+            if record is not None:
+                record[k][0].append(EV(enable_timing=True))
+                record[k][0][-1].record(stream)
+            enc = encode(k, x)
+            if record is not None:
+                record[k][1].append(EV(enable_timing=True))
+                record[k][1][-1].record(stream)
+            decode(k, enc)
+            if record is not None:
+                record[k][2].append(EV(enable_timing=True))
+                record[k][2][-1].record(stream)
+
+    t_warm = time.time()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    rec = {k: ([], [], []) for k in kinds}
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    e0, e1 = EV(enable_timing=True), EV(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(rec)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_end = time.time()
+    total_ms = e0.elapsed_time(e1)
+    max_ms = max_over_ranks(total_ms, world, dev)
+
+    # correctness of the timed outputs
+    stats = {}
+    for k in kinds:
+        b = bufs[k]
+        ok = int(b["status"].item()) == 0 and int(b["dstatus"].item()) == 0 and torch.equal(b["y"], x)
+        if not ok:
+            raise SystemExit(f"{k}: encode/decode status or round trip failed")
+        enc_ms = [a.elapsed_time(c) for a, c in zip(rec[k][0], rec[k][1])]
+        dec_ms = [a.elapsed_time(c) for a, c in zip(rec[k][1], rec[k][2])]
+        payload = int(b["chunk_off"][-1].item())
+        bits = int(b["total_bits"].item())
+        side = 8 * (ecc.num_chunks(n, C) + 1) + 2 * ecc.num_subblocks(n, S)
+        algo = n + payload + side          # bytes read + written by one encode or one decode
+        stats[k] = {
+            "encode_ms": statistics.mean(enc_ms), "decode_ms": statistics.mean(dec_ms),
+            "encode_gbs": n / statistics.mean(enc_ms) / 1e6, "decode_gbs": n / statistics.mean(dec_ms) / 1e6,
+            "encode_hbm_gbs": algo / statistics.mean(enc_ms) / 1e6,
+            "decode_hbm_gbs": algo / statistics.mean(dec_ms) / 1e6,
+            "algorithmic_bytes": algo, "payload_bytes": payload,
+            "compressibility_pct": 100.0 * (1.0 - bits / (8.0 * n)),
+            "container_compressibility_pct": 100.0 * (1.0 - (payload + side) / n),
+            "max_code_len": max_len[k],
+        }
+    peak, peak_src = hbm_peak()
+    # dominant kernel: largest total device time among the four launches
+    cand = [(stats[k][f"{d}_ms"], k, d) for k in kinds for d in ("encode", "decode")]
+    _, kd, dd = max(cand)
+    achieved = stats[kd][f"{dd}_hbm_gbs"]
+    kname = f"ecc_{dd}_{kd}"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(kname), "kernel": kname, "peak_source": f"{peak_src} (hbm_gbs)"}
+    per_kernel = {f"{d}_{k}": {"achieved_gbs": stats[k][f"{d}_hbm_gbs"],
+                               "frac": stats[k][f"{d}_hbm_gbs"] / peak} for k in kinds for d in ("encode", "decode")}
+
+    clocks_t1 = time.time()
+
+    # end to end through the Python API, pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        xh.copy_(x)
+        xin = torch.empty(n, dtype=torch.uint8, device=dev)
+        payload_h = torch.empty(bufs["huffman"]["out"].numel(), dtype=torch.uint8, pin_memory=True)
+        st_h = torch.empty(4, dtype=torch.int32, pin_memory=True)
+        e2e_steps = max(1, min(args.steps, 20))
+
+        def e2e_step():
+            xin.copy_(xh, non_blocking=True)
+            encs = {}
+            for k in kinds:
+                encs[k] = encode(k, xin)
+                decode(k, encs[k])
+            used = bufs["huffman"]["out"].numel()
+            payload_h[:used].copy_(bufs["huffman"]["out"][:used], non_blocking=True)
+            st_h[0:1].copy_(bufs["huffman"]["status"], non_blocking=True)
+            st_h[1:2].copy_(bufs["qlc"]["status"], non_blocking=True)
+            torch.cuda.synchronize()
+            return used
+
+        for _ in range(2):
+            e2e_step()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        d2h = 0
+        for _ in range(e2e_steps):
+            d2h = e2e_step()
+        dt = max_over_ranks(time.perf_counter() - t, world, dev)
+        e2e = {"value": weak_scaling_value(2.0 * n * e2e_steps, world, dt) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": n, "d2h_bytes_per_step": d2h + 8, "steps": e2e_steps}
+        del xh, payload_h
+
+    # histogram (warm-up stage) and chunk-size sweep: informational timings
+    extra = {}
+    if rank == 0:
+        h0, h1 = EV(enable_timing=True), EV(enable_timing=True)
+        tmp = torch.zeros(256, dtype=torch.int64, device=dev)
+        ecc.e4m3_histogram(x, tmp)
+        h0.record(stream)
+        for _ in range(5):
+            ecc.e4m3_histogram(x, tmp)
+        h1.record(stream)
+        torch.cuda.synchronize()
+        extra["histogram_gbs"] = 5 * n / h0.elapsed_time(h1) / 1e6
+        if not args.no_sweep:
+            sweep = {}
+            for Cs in (4096, 16384, 65536):
+                Ss = ecc.default_subblock(Cs)
+                for k in kinds:
+                    out = torch.empty(ecc.max_encoded_bytes(n, Cs, max_len[k]), dtype=torch.uint8, device=dev)
+                    res = []
+                    for rep in range(4):
+                        a, b2, c2 = EV(enable_timing=True), EV(enable_timing=True), EV(enable_timing=True)
+                        a.record(stream)
+                        enc = ecc.ecc_encode(x, dcbs[k], Cs, Ss, out=out)
+                        b2.record(stream)
+                        y, st = ecc.ecc_decode(enc, dcbs[k], out=bufs[k]["y"])
+                        c2.record(stream)
+                        torch.cuda.synchronize()
+                        if rep:
+                            res.append((a.elapsed_time(b2), b2.elapsed_time(c2)))
+                    assert int(enc.status.item()) == 0 and int(st.item()) == 0 and torch.equal(y, x)
+                    em = statistics.mean(r[0] for r in res)
+                    dm = statistics.mean(r[1] for r in res)
+                    sweep[f"{k}_C{Cs}"] = {"encode_gbs": n / em / 1e6, "decode_gbs": n / dm / 1e6,
+                                           "payload_bytes": int(enc.chunk_off[-1].item())}
+                    del out, enc
+            extra["chunk_sweep"] = sweep
+        import oracle
+        extra["figures"] = {
+            "shannon_compressibility_pct": 100.0 * (1.0 - ecc.entropy_bits(xcount_h) / 8.0),
+            "kl_tensor_vs_warmup_bits": ecc.kl_bits(xcount_h, pooled_h + np.uint64(1)),
+        }
+        del oracle
+
+    clocks.stop()
+    ck = clocks.summary(t_warm, t_end)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        C_ = C
+        cbo = host_codebooks(C_)
+        chunks = cpu_sample(256, C_)
+        rate, cores, desc = oracle_round_trip_rate(chunks, cbo, C_, S, seconds_target=12.0)
+        cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    value = weak_scaling_value(2.0 * n * args.steps, world, max_ms / 1e3) / 1e9
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "bytes": n, "chunk": C, "subblock": S,
+                       "codebooks": ["fixed canonical Huffman (8 x 2^24 B warm-up, +1)", "base QLC (same counts)"],
+                       "step": "encode + decode with each codebook", "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline,
+            "per_kernel_roofline": per_kernel,
+            "results": stats,
+            "clocks": ck,
+            "e2e": e2e,
+            "gpu_launches": args.steps * len(kinds) * 3,
+            "cpu_baseline": cpu,
+            **extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,311 @@
+/*
+ * ecc.h -- C ABI of the GB300 library for lossless fixed-codebook coding of
+ * e4m3 byte tensors.
+ *
+ * Two codebook families, both fixed before the data is seen:
+ *
+ *  - the Quad Length Code (QLC) of "Quad Length Codes for Lossless
+ *    Compression of e4m3" (gist.science summary of arXiv 2602.17849),
+ *    section 2 "Metodologia": the 256 byte values are ranked by decreasing
+ *    probability, the ranks are split into 8 areas named by a 3-bit prefix,
+ *    every area has one fixed suffix width, so there are at most 4 distinct
+ *    code lengths and the decoder learns the length from the first 3 bits;
+ *  - the single-stage canonical Huffman code of "Single-Stage Huffman
+ *    Encoder for ML Compression" (arXiv 2601.10673), abstract and TL;DR: one
+ *    codebook built from the average symbol distribution of earlier batches
+ *    and reused for every later tensor, with no per-tensor frequency
+ *    analysis and no codebook sent with the data.
+ *
+ * Conventions (all entry points):
+ *  - Every function returns an ecc_status.  A host-side return value reports
+ *    argument and launch errors only; errors that depend on the data are
+ *    written by the kernels to a caller-provided device word `status`, which
+ *    the call first sets to ECC_OK.  Read it after the stream has reached the
+ *    end of the call.  The first error written wins.
+ *  - Device buffers are plain device pointers owned by the caller.  Buffers
+ *    that hold bytes (tensor, payload) must start on a 16-byte boundary.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device calls only enqueue work: they never synchronise and,
+ *    apart from the batched calls' one host-to-device copy of their
+ *    descriptors, never copy between host and device.  The library allocates
+ *    no device memory; scratch space is the caller's workspace.
+ *  - Calls keep no state between invocations and may be made from several
+ *    host threads; calls on one stream run in order.
+ *
+ * Container format written by ecc_encode and read by ecc_decode (the pages
+ * fix no format; this one is the library's own):
+ *  - the n input bytes are split into chunks of C symbols (C a power of two,
+ *    1024 <= C <= 65536), chunk c holding symbols [cC, min(n, (c+1)C));
+ *  - a chunk's payload is its codewords in symbol order, each written most
+ *    significant bit first, packed most significant bit first into bytes and
+ *    zero-padded to a multiple of 16 bytes; payloads follow each other;
+ *  - chunk_off has n_chunks + 1 entries: chunk_off[0] = 0 and
+ *    chunk_off[c + 1] = chunk_off[c] + padded payload bytes of chunk c;
+ *  - sub_bits has ceil(n / S) entries: the exact payload bits of the
+ *    symbols [jS, min(n, (j+1)S)) (S a power of two, 64 <= S <= 1024,
+ *    S <= C), which lets a decoder start in the middle of a chunk;
+ *  - total_bits is the sum of all code lengths, i.e. sum over bytes of
+ *    count x length.
+ */
+#ifndef ECC_H
+#define ECC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ecc_status;
+
+enum {
+    ECC_OK = 0,
+    ECC_ERR_ARG = 1,      /* bad size, alignment, null pointer or workspace */
+    ECC_ERR_CAPACITY = 2, /* the payload does not fit in out_cap bytes */
+    ECC_ERR_CORRUPT = 3,  /* stream, offsets or sub-block bits inconsistent */
+    ECC_ERR_CODEBOOK = 4, /* bad codebook, or a byte the codebook does not code */
+    ECC_ERR_TIMEOUT = 5,  /* a bounded device wait ran out (the kernel returned) */
+    ECC_ERR_CUDA = 6      /* a CUDA runtime call failed */
+};
+
+enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2 };
+
+#define ECC_CODEBOOK_MAGIC 0x45434342u /* "ECCB" */
+#define ECC_MAX_CODE_LEN 48            /* longest code the device path accepts */
+#define ECC_PEEK_BITS 12               /* first-level decode table index width */
+
+/*
+ * Codebook: a fixed-size, pointer-free record built on the host by
+ * qlc_build_tables or huff_build_canonical and copied as raw bytes to the
+ * device (cudaMemcpy of ecc_codebook_bytes()).  Serialising it is a memcpy.
+ * Fields marked "derived" are lookup tables the kernels stage in shared
+ * memory; they follow from len/code and are filled by the builders.
+ */
+typedef struct ecc_codebook {
+    uint32_t magic;       /* ECC_CODEBOOK_MAGIC */
+    uint32_t family;      /* ECC_FAMILY_QLC or ECC_FAMILY_HUFFMAN */
+    uint32_t max_len;     /* longest code length in bits */
+    uint32_t min_len;     /* shortest code length in bits */
+    uint32_t n_coded;     /* number of byte values that have a code */
+    uint32_t reserved[3];
+    uint64_t code[256];   /* code of each byte value, right-aligned */
+    uint64_t first[64];   /* Huffman: first canonical code of each length */
+    uint32_t enc[256];    /* derived: (code << 5) | len if len <= 26, else 0 */
+    uint32_t area[8];     /* derived, QLC: per prefix k, start | len << 16 | width << 24 */
+    uint16_t dec[4096];   /* derived: 12-bit peek -> byte | len << 8; 0 = not resolved */
+    uint16_t count[64];   /* Huffman: number of codes of each length */
+    uint16_t index[64];   /* Huffman: position in sorted[] of the first code of each length */
+    uint16_t area_start[8]; /* QLC: first rank of each area */
+    uint16_t area_size[8];  /* QLC: ranks held by each area (0 = empty) */
+    uint8_t width[8];     /* QLC: suffix width of each area, 0..8 */
+    uint8_t len[256];     /* code length of each byte value, 0 = no code */
+    uint8_t rank[256];    /* QLC: rank of each byte value */
+    uint8_t by_rank[256]; /* QLC: byte value holding each rank */
+    uint8_t sorted[256];  /* Huffman: coded byte values sorted by (length, value) */
+} ecc_codebook;
+
+/* Size in bytes of ecc_codebook (what to copy to the device). */
+size_t ecc_codebook_bytes(void);
+
+/* ------------------------------------------------------------------------
+ * Host codebook builders (pure CPU, no CUDA calls)
+ * ---------------------------------------------------------------------- */
+
+/*
+ * qlc_build_tables -- Quad Length Code tables ("Quad Length Codes ...",
+ * section 2: LUT paragraph and area bullets; "Adattabilita" for other widths).
+ *   count[256]  occurrences of each byte value (any scale; only the order
+ *               matters).  Ranks sort by count descending, ties by byte value
+ *               ascending; every byte gets a rank.
+ *   width[8]    suffix width of each area, 0..8; areas are filled with ranks
+ *               in order, area k taking min(2^width[k], ranks left).  The base
+ *               code is {3,3,3,3,3,4,5,8}: areas of 8,8,8,8,8,16,32,168 ranks
+ *               and lengths 6,6,6,6,6,7,8,11.  Rank r in area k gets the code
+ *               (k << width[k]) | (r - start_k), length 3 + width[k].
+ *   out         filled codebook (caller-owned host memory).
+ * Errors: ECC_ERR_ARG if a pointer is NULL, a width exceeds 8, or the areas
+ * hold fewer than 256 ranks.
+ */
+ecc_status qlc_build_tables(const uint64_t count[256], const uint8_t width[8], ecc_codebook *out);
+
+/*
+ * qlc_search_widths -- adapted QLC ("Quad Length Codes ...", section 2
+ * "Adattabilita", section 3 case 2 and section 5 "Future Directions"):
+ * exhaustive search over non-decreasing width vectors (0..8 each) whose
+ * areas hold at least 256 ranks (require_full != 0: exactly 256), whose
+ * non-empty areas use at most max_distinct distinct lengths, minimising
+ * sum(count x length); ties go to the lexicographically smallest vector.
+ *   width_out[8]  best widths; cost_bits (may be NULL) its sum(count x len).
+ * Errors: ECC_ERR_ARG for NULL inputs, max_distinct == 0, or no vector.
+ */
+ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, uint32_t require_full,
+                             uint8_t width_out[8], uint64_t *cost_bits);
+
+/*
+ * huff_build_canonical -- the fixed Huffman codebook of the single-stage
+ * encoder ("Single-Stage Huffman Encoder ...", abstract: codebook built once
+ * from the average probability distribution of earlier batches; euno.news
+ * summary, Methodology step 3).
+ *   weight[256]  integer PMF numerators, e.g. pooled warm-up counts plus one
+ *                per byte; weight 0 = byte absent (gets no code).  The two
+ *                nodes with the smallest (weight, smallest byte below) keys
+ *                merge first, so equal weights resolve deterministically.  A
+ *                lone coded byte gets length 1.  Codes are canonical: sorted
+ *                by (length, byte value), consecutive within a length.
+ *   max_len      longest code accepted, 1..ECC_MAX_CODE_LEN; a longer tree
+ *                is an error, not a silent length limit.
+ *   out          filled codebook (caller-owned host memory).
+ * Errors: ECC_ERR_ARG (NULL, max_len out of range, all weights 0, weights
+ * whose sum overflows 64 bits), ECC_ERR_CODEBOOK (tree deeper than max_len).
+ */
+ecc_status huff_build_canonical(const uint64_t weight[256], uint32_t max_len, ecc_codebook *out);
+
+/* ------------------------------------------------------------------------
+ * Host figures in float64 ("Single-Stage Huffman ...", TL;DR: compressibility
+ * against per-shard Huffman and the Shannon bound; Figure 3: KL divergence
+ * of shard distributions from the average one)
+ * ---------------------------------------------------------------------- */
+
+/* Shannon entropy -sum p log2 p (bits/symbol) of a count vector. */
+double ecc_entropy_bits(const uint64_t count[256]);
+
+/* D(P || Q) in bits of two count vectors; +inf if Q lacks a byte P has. */
+double ecc_kl_bits(const uint64_t p_count[256], const uint64_t q_count[256]);
+
+/* Exact payload bits sum(count x len) of a codebook on a histogram.
+ * Errors: ECC_ERR_CODEBOOK if a counted byte has no code, ECC_ERR_ARG. */
+ecc_status ecc_code_bits(const uint64_t count[256], const ecc_codebook *cb, uint64_t *bits);
+
+/* ------------------------------------------------------------------------
+ * Sizes
+ * ---------------------------------------------------------------------- */
+size_t ecc_num_chunks(size_t n, uint32_t C);     /* ceil(n / C) */
+size_t ecc_num_subblocks(size_t n, uint32_t S);  /* ceil(n / S) */
+/* Payload bytes that always suffice: every symbol at max_len bits, every
+ * chunk padded to 16 bytes. */
+size_t ecc_max_encoded_bytes(size_t n, uint32_t C, uint32_t max_len);
+/* Device workspace ecc_encode needs for n symbols in chunks of C. */
+size_t ecc_encode_workspace_bytes(size_t n, uint32_t C);
+
+/* ------------------------------------------------------------------------
+ * Device calls
+ * ---------------------------------------------------------------------- */
+
+/*
+ * e4m3_histogram -- count of each byte value ("Single-Stage Huffman ...",
+ * euno.news summary, Methodology step 1: record symbol frequencies of
+ * warm-up batches; also the rank input of qlc_build_tables).
+ *   in     device bytes [n] (any alignment);
+ *   count  device uint64[256]; the counts of `in` are ADDED to it, so
+ *          several tensors can be pooled (zero it first for one tensor).
+ * Errors (host): ECC_ERR_ARG for NULL pointers with n > 0, ECC_ERR_CUDA.
+ */
+ecc_status e4m3_histogram(const uint8_t *in, size_t n, uint64_t *count, void *stream);
+
+/*
+ * ecc_encode -- single-stage encode with a fixed codebook ("Quad Length
+ * Codes ...", section 2 "Codifica": the encoder looks the code up in the
+ * LUT; "Single-Stage Huffman ...", Methodology step 4: encode with the
+ * precomputed codebook, no analysis, no codebook transmission).
+ *   in, n        device bytes [n], 16-byte aligned.
+ *   cb           device copy of an ecc_codebook (max_len <= 48).
+ *   C, S         chunk and sub-block sizes (see the container format).
+ *   out, out_cap device payload buffer, 16-byte aligned, out_cap bytes;
+ *                ecc_max_encoded_bytes() always suffices.
+ *   chunk_off    device uint64[ceil(n/C) + 1]; written.
+ *   sub_bits     device uint16[ceil(n/S)]; written.
+ *   total_bits   device uint64[1]; written (sum of all code lengths).
+ *   ws, ws_bytes device workspace of at least ecc_encode_workspace_bytes();
+ *                its contents need not be initialised and are clobbered.
+ *   status       device uint32[1]; set to ECC_OK, then to the first error.
+ * Device errors: ECC_ERR_CODEBOOK (bad magic or a byte without a code),
+ * ECC_ERR_CAPACITY (payload exceeds out_cap; chunk_off still holds the sizes
+ * the payload needs, nothing is written past out_cap), ECC_ERR_TIMEOUT (the
+ * chunk-offset look-back waited more than about a second).
+ * Host errors: ECC_ERR_ARG (sizes, alignment, NULL, small workspace),
+ * ECC_ERR_CUDA.  n = 0 writes chunk_off[0] = 0 and total_bits = 0.
+ */
+ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S,
+                      uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,
+                      uint64_t *total_bits, void *ws, size_t ws_bytes, uint32_t *status, void *stream);
+
+/*
+ * ecc_decode -- chunk-parallel decode ("Quad Length Codes ...", section 2
+ * "Decodifica": read 3 bits -> area -> length, read the suffix, add the
+ * area's offset, a second LUT gives the byte; section 4 items 2-3; Huffman
+ * codes resolve through a 12-bit first-level table and canonical per-length
+ * ranges for longer codes).
+ *   in, in_bytes device payload [in_bytes], 16-byte aligned.
+ *   chunk_off    device uint64[ceil(n/C) + 1] and sub_bits device
+ *                uint16[ceil(n/S)] as written by ecc_encode.
+ *   n, C, S      symbol count and the sizes used at encode time.
+ *   cb           device codebook used at encode time.
+ *   out          device bytes [n], 16-byte aligned; written.
+ *   status       device uint32[1]; set to ECC_OK, then to the first error.
+ * Device errors: ECC_ERR_CORRUPT (offsets out of range, a code the codebook
+ * lacks, a sub-block whose bit count differs from sub_bits, a chunk whose
+ * padded size differs from its offsets); output bytes of a corrupt chunk are
+ * unspecified but nothing is written outside out[0, n).  ECC_ERR_CODEBOOK.
+ */
+ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_off,
+                      const uint16_t *sub_bits, size_t n, uint32_t C, uint32_t S,
+                      const ecc_codebook *cb, uint8_t *out, uint32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Batched calls: many tensors, one kernel launch for encode and one for
+ * decode (each tensor an independent container, each with its own codebook)
+ * ---------------------------------------------------------------------- */
+typedef struct ecc_desc {
+    const uint8_t *in;     /* encode: symbols [n]; decode: payload [in_bytes] */
+    uint8_t *out;          /* encode: payload [out_cap]; decode: symbols [n] */
+    uint64_t n;            /* symbols */
+    uint64_t cap;          /* encode: out_cap; decode: in_bytes */
+    uint64_t *chunk_off;   /* [ceil(n/C) + 1] */
+    uint16_t *sub_bits;    /* [ceil(n/S)] */
+    uint64_t *total_bits;  /* encode: [1], written; decode: ignored (may be NULL) */
+    const ecc_codebook *cb;/* device codebook */
+    uint32_t *status;      /* device word, set to ECC_OK then the first error */
+    uint64_t *t_done_ns;   /* optional device word: %globaltimer (ns) when the
+                              tensor's last chunk finished; NULL = not recorded */
+    uint32_t C, S;         /* container sizes of this tensor */
+} ecc_desc;
+
+/* Workspace the batched calls need for these descriptors (host array). */
+size_t ecc_batched_workspace_bytes(const ecc_desc *descs, uint32_t count);
+
+/*
+ * ecc_encode_batched / ecc_decode_batched -- the calls above over `count`
+ * tensors in one launch.  `descs` is a host array; the call copies it and a
+ * chunk prefix table into `ws` with one asynchronous host-to-device copy,
+ * so `descs` may be reused once the call returns.  Every tensor obeys the
+ * rules of ecc_encode / ecc_decode; its errors go to its own status word.
+ * Optionally `t_start_ns` (device word, may be NULL) receives %globaltimer
+ * at kernel start, for per-tensor latency = t_done_ns - t_start_ns.
+ * Host errors: ECC_ERR_ARG (bad descriptor, small workspace), ECC_ERR_CUDA.
+ */
+ecc_status ecc_encode_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes,
+                              uint64_t *t_start_ns, void *stream);
+ecc_status ecc_decode_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes,
+                              uint64_t *t_start_ns, void *stream);
+
+/*
+ * ecc_selftest_wait -- failure-detection self-test of the bounded wait used
+ * by the encoder's chunk-offset look-back.  Runs the look-back of chunk
+ * `chunk` on the caller's device array flags[chunk + 1] (uint64, zero = not
+ * published) with a time limit of timeout_ns; writes the exclusive prefix it
+ * found to *prefix and ECC_ERR_TIMEOUT to *status if the limit ran out.  A
+ * flags array in which no predecessor is ever published must return
+ * ECC_ERR_TIMEOUT, not hang.  Host errors: ECC_ERR_ARG, ECC_ERR_CUDA.
+ */
+ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate, uint64_t timeout_ns,
+                             uint64_t *prefix, uint32_t *status, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *ecc_status_string(ecc_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ECC_H */

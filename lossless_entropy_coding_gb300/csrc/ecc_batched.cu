@@ -1,0 +1,335 @@
+// ecc_batched.cu -- one-launch encode and decode of many tensors, each with
+// its own codebook and container sizes (the message regime of collective
+// communication: many tensors of very different sizes).  See ecc.h.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "ecc_device.cuh"
+#include "ecc_launch.h"
+
+namespace ecc {
+
+// Workspace layout (all offsets 16-byte aligned):
+//   header | descs[count] | prefix[count + 1] | done[count] | flags[total]
+// prefix[d] = first global work item of tensor d (chunks for encode, groups
+// of `warps` chunks for decode); flags = look-back words (encode only).
+struct BatchHeader {
+    uint32_t ticket;
+    uint32_t count;
+    uint32_t warps;       // decode: chunks per work item
+    uint32_t stage_bytes;
+    uint64_t total_items;
+    uint64_t total_chunks;
+    uint64_t desc_off, prefix_off, done_off, flags_off;
+};
+
+struct BatchLayout {
+    size_t desc_off, prefix_off, done_off, flags_off, bytes;
+};
+
+static size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
+
+static BatchLayout layout_for(uint32_t count, uint64_t total_chunks)
+{
+    BatchLayout L;
+    L.desc_off = up16(sizeof(BatchHeader));
+    L.prefix_off = up16(L.desc_off + (size_t)count * sizeof(ecc_desc));
+    L.done_off = up16(L.prefix_off + ((size_t)count + 1) * sizeof(uint64_t));
+    L.flags_off = up16(L.done_off + (size_t)count * sizeof(uint32_t));
+    L.bytes = up16(L.flags_off + total_chunks * sizeof(uint64_t));
+    return L;
+}
+
+__device__ __forceinline__ uint32_t find_tensor(const uint64_t *prefix, uint32_t count, uint64_t item)
+{
+    // largest d with prefix[d] <= item (prefix is non-decreasing; empty
+    // tensors share a prefix with their successor and are skipped)
+    uint32_t lo = 0, hi = count; // invariant: prefix[lo] <= item < prefix[hi]
+    while (hi - lo > 1) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (prefix[mid] <= item)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+__global__ void batch_prologue_kernel(uint8_t *ws, int encode)
+{
+    BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
+    const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
+    uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
+    uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
+    const uint64_t i0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = i0; i < h->count; i += stride) {
+        const ecc_desc &d = descs[i];
+        *d.status = ECC_OK;
+        done[i] = 0;
+        if (encode) {
+            *d.total_bits = 0;
+            d.chunk_off[0] = 0;
+        }
+        if (d.t_done_ns && d.n == 0)
+            *d.t_done_ns = 0;
+    }
+    if (encode)
+        for (uint64_t i = i0; i < h->total_chunks; i += stride)
+            flags[i] = 0;
+}
+
+__device__ __forceinline__ void stamp_done(const ecc_desc &d, uint32_t *done, uint32_t k, uint64_t n_chunks,
+                                           uint32_t items)
+{
+    if (!d.t_done_ns)
+        return;
+    __threadfence();
+    if (atomicAdd(done + k, items) + items == n_chunks)
+        *d.t_done_ns = globaltimer();
+}
+
+__global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws, uint64_t *t_start)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    EncShared &sh = *reinterpret_cast<EncShared *>(smem);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + enc_shared_bytes());
+    BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
+    const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
+    const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
+    uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
+    uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
+    const uint32_t stage_bytes = h->stage_bytes;
+    if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
+        *t_start = globaltimer();
+    if (threadIdx.x == 0)
+        sh.loaded = nullptr;
+    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
+    for (uint32_t i = threadIdx.x; i < stage_bytes / 16; i += kEncThreads)
+        st4[i] = make_uint4(0, 0, 0, 0);
+    for (;;) {
+        if (threadIdx.x == 0)
+            sh.ticket = atomicAdd(&h->ticket, 1u);
+        __syncthreads();
+        const uint64_t t = sh.ticket;
+        if (t >= h->total_chunks)
+            break;
+        const uint32_t k = find_tensor(prefix, h->count, t);
+        const ecc_desc d = descs[k];
+        const uint64_t c = t - prefix[k];
+        const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
+        if (cb_ok && d.cb != sh.loaded) {
+            load_encode_lut(sh, d.cb);
+            __syncthreads();
+            if (threadIdx.x == 0)
+                sh.loaded = d.cb;
+        }
+        EncJob job{d.in, d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits, d.total_bits,
+                   flags + prefix[k], d.status};
+        if (cb_ok) {
+            encode_chunk(sh, stage, stage_bytes, job, c, kWaitLimitNs);
+        } else if (threadIdx.x < 32) {
+            // keep the tensor's look-back moving; its status says why it is empty
+            bool to;
+            const uint64_t pre = lookback(job.flags, c, 0, kWaitLimitNs, &to);
+            if (threadIdx.x == 0) {
+                set_status(d.status, ECC_ERR_CODEBOOK);
+                d.chunk_off[c + 1] = pre;
+            }
+        }
+        if (threadIdx.x == 0)
+            stamp_done(d, done, k, (d.n + d.C - 1) / d.C, 1);
+        __syncthreads();
+    }
+}
+
+__global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
+    __shared__ const ecc_codebook *loaded;
+    __shared__ uint32_t ticket;
+    BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
+    const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
+    const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
+    uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
+    const uint32_t stage_bytes = h->stage_bytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t warps = h->warps;
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + sizeof(((ecc_codebook *)0)->dec) +
+                                                   (size_t)warp * stage_bytes);
+    if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
+        *t_start = globaltimer();
+    if (threadIdx.x == 0)
+        loaded = nullptr;
+    for (;;) {
+        if (threadIdx.x == 0)
+            ticket = atomicAdd(&h->ticket, 1u);
+        __syncthreads();
+        const uint64_t g = ticket;
+        if (g >= h->total_items)
+            break;
+        const uint32_t k = find_tensor(prefix, h->count, g);
+        const ecc_desc d = descs[k];
+        const uint64_t n_chunks = (d.n + d.C - 1) / d.C;
+        const uint64_t c = (g - prefix[k]) * warps + warp;
+        const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
+        if (cb_ok && d.cb != loaded) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(d.cb->dec);
+            uint4 *dst = reinterpret_cast<uint4 *>(dec);
+            for (int i = threadIdx.x; i < (int)(sizeof(d.cb->dec) / 16); i += blockDim.x)
+                dst[i] = src[i];
+            __syncthreads();
+            if (threadIdx.x == 0)
+                loaded = d.cb;
+        }
+        if (c < n_chunks) {
+            if (cb_ok) {
+                DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
+                if (d.C / d.S >= 64)
+                    decode_chunk<2>(job, dec, stage, stage_bytes, c);
+                else
+                    decode_chunk<1>(job, dec, stage, stage_bytes, c);
+            } else if (lane == 0) {
+                set_status(d.status, ECC_ERR_CODEBOOK);
+            }
+            if (lane == 0)
+                stamp_done(d, done, k, n_chunks, 1);
+        }
+        __syncthreads();
+    }
+}
+
+} // namespace ecc
+
+using namespace ecc;
+
+namespace {
+
+ecc_status check_descs(const ecc_desc *descs, uint32_t count, bool encode, uint64_t *total_chunks, uint32_t *max_C)
+{
+    if (!descs || count == 0)
+        return ECC_ERR_ARG;
+    uint64_t tot = 0;
+    uint32_t mc = 1024;
+    for (uint32_t i = 0; i < count; ++i) {
+        const ecc_desc &d = descs[i];
+        if (!valid_sizes(d.C, d.S) || !d.cb || !d.status || !d.chunk_off)
+            return ECC_ERR_ARG;
+        if (encode && !d.total_bits)
+            return ECC_ERR_ARG;
+        if (d.n && (!d.in || !d.out || !d.sub_bits || !aligned16(d.in) || !aligned16(d.out)))
+            return ECC_ERR_ARG;
+        tot += ecc_num_chunks(d.n, d.C);
+        mc = std::max(mc, d.C);
+    }
+    *total_chunks = tot;
+    *max_C = mc;
+    return ECC_OK;
+}
+
+int decode_warps(uint32_t stage_bytes)
+{
+    const size_t table = sizeof(((ecc_codebook *)0)->dec);
+    int w = (int)std::min<size_t>(kDecMaxWarps, (kMaxDynSmem - table) / stage_bytes);
+    return std::max(w, 1);
+}
+
+ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes, uint64_t *t_start,
+                       void *stream, bool encode)
+{
+    uint64_t total_chunks;
+    uint32_t max_C;
+    ecc_status e = check_descs(descs, count, encode, &total_chunks, &max_C);
+    if (e != ECC_OK)
+        return e;
+    BatchLayout L = layout_for(count, total_chunks);
+    if (!ws || !aligned16(ws) || ws_bytes < L.bytes)
+        return ECC_ERR_ARG;
+    const uint32_t stage = stage_bytes_for(max_C);
+    const int warps = decode_warps(stage);
+    // host image of header | descs | prefix, copied with one async copy
+    std::vector<uint8_t> img(L.done_off, 0);
+    BatchHeader *h = reinterpret_cast<BatchHeader *>(img.data());
+    h->ticket = 0;
+    h->count = count;
+    h->warps = (uint32_t)warps;
+    h->stage_bytes = stage;
+    h->total_chunks = total_chunks;
+    h->desc_off = L.desc_off;
+    h->prefix_off = L.prefix_off;
+    h->done_off = L.done_off;
+    h->flags_off = L.flags_off;
+    std::memcpy(img.data() + L.desc_off, descs, (size_t)count * sizeof(ecc_desc));
+    uint64_t *prefix = reinterpret_cast<uint64_t *>(img.data() + L.prefix_off);
+    uint64_t acc = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+        prefix[i] = acc;
+        const uint64_t nc = ecc_num_chunks(descs[i].n, descs[i].C);
+        acc += encode ? nc : (nc + warps - 1) / warps;
+    }
+    prefix[count] = acc;
+    h->total_items = acc;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return launch_status(cudaErrorUnknown);
+    const int sms = sm_count();
+    if (sms <= 0)
+        return ECC_ERR_CUDA;
+    {
+        const uint64_t work = std::max<uint64_t>(count, encode ? total_chunks : 0);
+        const uint64_t nb = std::max<uint64_t>(1, std::min<uint64_t>((work + 255) / 256, 1024));
+        batch_prologue_kernel<<<(unsigned)nb, 256, 0, st>>>((uint8_t *)ws, encode ? 1 : 0);
+        if ((e = launch_status(cudaGetLastError())) != ECC_OK)
+            return e;
+    }
+    if (acc == 0)
+        return ECC_OK;
+    if (encode) {
+        const size_t smem = enc_shared_bytes() + stage;
+        const int occ = occupancy((const void *)encode_batched_kernel, kEncThreads, smem);
+        if (occ <= 0)
+            return ECC_ERR_CUDA;
+        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, acc);
+        encode_batched_kernel<<<(unsigned)grid, kEncThreads, smem, st>>>((uint8_t *)ws, t_start);
+    } else {
+        const size_t smem = sizeof(((ecc_codebook *)0)->dec) + (size_t)warps * stage;
+        const int occ = occupancy((const void *)decode_batched_kernel, warps * 32, smem);
+        if (occ <= 0)
+            return ECC_ERR_CUDA;
+        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, acc);
+        decode_batched_kernel<<<(unsigned)grid, warps * 32, smem, st>>>((uint8_t *)ws, t_start);
+    }
+    return launch_status(cudaGetLastError());
+}
+
+} // namespace
+
+extern "C" {
+
+size_t ecc_batched_workspace_bytes(const ecc_desc *descs, uint32_t count)
+{
+    if (!descs || !count)
+        return 0;
+    uint64_t tot = 0;
+    for (uint32_t i = 0; i < count; ++i)
+        tot += ecc_num_chunks(descs[i].n, descs[i].C ? descs[i].C : 1);
+    return layout_for(count, tot).bytes;
+}
+
+ecc_status ecc_encode_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes, uint64_t *t_start_ns,
+                              void *stream)
+{
+    return run_batched(descs, count, ws, ws_bytes, t_start_ns, stream, true);
+}
+
+ecc_status ecc_decode_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes, uint64_t *t_start_ns,
+                              void *stream)
+{
+    return run_batched(descs, count, ws, ws_bytes, t_start_ns, stream, false);
+}
+
+} // extern "C"

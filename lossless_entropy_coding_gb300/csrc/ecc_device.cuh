@@ -1,0 +1,719 @@
+// ecc_device.cuh -- device building blocks of the e4m3 entropy coder for
+// sm_103a: the chunk encoder (LUT lookup, scans of code lengths, decoupled
+// look-back for chunk offsets, bit packing) and the warp-per-chunk decoder
+// (first-level peek table, canonical long-code ranges).  Included by the
+// single-tensor and the batched translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ecc.h"
+
+namespace ecc {
+
+// ---------------------------------------------------------------- constants
+constexpr int kEncThreads = 256;
+constexpr int kEncWarps = kEncThreads / 32;
+constexpr int kSymPerThread = 16;                     // one 16-byte load
+constexpr int kTile = kEncThreads * kSymPerThread;    // symbols per tile
+constexpr uint32_t kLutRows = 256;                    // byte values
+constexpr uint64_t kFlagAggregate = 1ull << 62;       // look-back states
+constexpr uint64_t kFlagPrefix = 2ull << 62;
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;      // bounded waits: 1 s
+
+__host__ __device__ constexpr uint32_t pad16(uint32_t b) { return (b + 15u) & ~15u; }
+
+// Worst-case staging bytes for one chunk of C symbols at up to 11 bits
+// (every QLC code fits; longer Huffman chunks take the unstaged path), with
+// a zeroed guard so peeks past a payload's end read zeros.
+__host__ __device__ constexpr uint32_t stage_bytes_for(uint32_t C) { return pad16((C * 11u + 7u) / 8u) + 32u; }
+
+// ---------------------------------------------------------------- memory ops
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream16(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
+
+// byte k (0..3) of x, zero-extended
+__device__ __forceinline__ uint32_t byte_of(uint32_t x, int k) { return __byte_perm(x, 0, 0x4440 | k); }
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t code)
+{
+    if (status)
+        atomicCAS(status, 0u, code);
+}
+
+// ---------------------------------------------------------------- look-back
+// Decoupled look-back over chunk offsets, run by one full warp.  flags[c]
+// holds (state << 62) | value: state 1 = chunk aggregate published, 2 =
+// inclusive prefix published.  Returns the exclusive prefix of chunk c and
+// publishes c's inclusive prefix.  Every wait is bounded: past timeout_ns the
+// warp reports ECC_ERR_TIMEOUT through *timed_out, still publishes (so that
+// successors finish), and the caller writes nothing for the chunk.
+__device__ __forceinline__ uint64_t lookback(uint64_t *flags, uint64_t c, uint64_t aggregate, uint64_t timeout_ns,
+                                             bool *timed_out)
+{
+    const int lane = threadIdx.x & 31;
+    *timed_out = false;
+    if (c == 0) {
+        if (lane == 0)
+            st_relaxed(flags, kFlagPrefix | (aggregate & kValueMask));
+        return 0;
+    }
+    if (lane == 0)
+        st_relaxed(flags + c, kFlagAggregate | (aggregate & kValueMask));
+    uint64_t prefix = 0;
+    int64_t j = (int64_t)c - 1;
+    uint64_t t0 = 0;
+    bool expired = false;
+    for (;;) {
+        const int64_t idx = j - lane;
+        const uint64_t f = idx >= 0 ? ld_relaxed(flags + idx) : kFlagPrefix;
+        const uint32_t state = (uint32_t)(f >> 62);
+        const unsigned pmask = __ballot_sync(~0u, state == 2);
+        const unsigned zmask = __ballot_sync(~0u, state == 0);
+        const int fp = pmask ? __ffs(pmask) - 1 : 32;          // nearest prefix
+        const unsigned need = fp >= 31 ? ~0u : ((2u << fp) - 1u); // lanes 0..fp
+        if (zmask & need) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0)
+                t0 = now;
+            if (__any_sync(~0u, now - t0 > timeout_ns)) {
+                expired = true;
+                break;
+            }
+            __nanosleep(64);
+            continue;
+        }
+        uint64_t v = lane <= fp ? (f & kValueMask) : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            v += __shfl_xor_sync(~0u, v, o);
+        prefix += v;
+        if (fp < 32)
+            break;
+        j -= 32;
+    }
+    if (lane == 0)
+        st_relaxed(flags + c, kFlagPrefix | ((prefix + aggregate) & kValueMask));
+    *timed_out = expired;
+    return prefix;
+}
+
+// ---------------------------------------------------------------- encoder
+// Shared state of one encoder CTA.  lut holds one replica of the 256 encode
+// entries per bank: entry s for lane l is lut[s * 32 + l], so the 32 lanes of
+// a warp always hit 32 different banks whatever bytes they look up.
+struct EncShared {
+    uint32_t lut[kLutRows * 32];
+    uint32_t warp_tot[kEncWarps];
+    uint32_t off[kEncThreads + 4];
+    uint64_t prefix;
+    const ecc_codebook *loaded; // codebook currently in lut
+    uint32_t ticket;
+    uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
+    uint32_t pad[2];
+};
+
+__host__ __device__ constexpr uint32_t enc_shared_bytes() { return (sizeof(EncShared) + 15u) & ~15u; }
+
+struct EncJob {
+    const uint8_t *in;
+    uint64_t n;
+    const ecc_codebook *cb;
+    uint32_t C, S;
+    uint8_t *out;
+    uint64_t out_cap;
+    uint64_t *chunk_off;
+    uint16_t *sub_bits;
+    uint64_t *total_bits;
+    uint64_t *flags;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ void load_encode_lut(EncShared &sh, const ecc_codebook *cb)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int s0 = warp * 32; s0 < (int)kLutRows; s0 += kEncWarps * 32) {
+        const uint32_t mine = cb->enc[s0 + lane];
+#pragma unroll 8
+        for (int t = 0; t < 32; ++t)
+            sh.lut[(s0 + t) * 32 + lane] = __shfl_sync(~0u, mine, t);
+    }
+}
+
+// Load up to 16 input bytes (16-byte aligned when cnt == 16).
+__device__ __forceinline__ uint4 load_symbols(const uint8_t *src, uint32_t cnt)
+{
+    if (cnt == kSymPerThread)
+        return ld_stream16(src);
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < kSymPerThread; ++i)
+        if ((uint32_t)i < cnt)
+            w[i >> 2] |= (uint32_t)src[i] << (8 * (i & 3));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Packing sink: 32-bit words in memory byte order (MSB-first bitstream).
+// Words shared with a neighbouring thread are merged with atomicOr into a
+// zeroed destination; words a thread owns alone are stored.
+struct Packer {
+    uint32_t *dst;
+    uint32_t wi;     // index of the word being filled
+    uint32_t nb;     // pending bits in acc (low bits)
+    bool first;      // the word at wi may hold a predecessor's bits
+    uint64_t acc;
+
+    __device__ __forceinline__ void start(uint32_t *d, uint32_t bitpos)
+    {
+        dst = d;
+        wi = bitpos >> 5;
+        nb = bitpos & 31;   // the predecessor's bits count as zeros here
+        first = nb != 0;
+        acc = 0;
+    }
+    __device__ __forceinline__ void emit_if_full()
+    {
+        if (nb >= 32) {
+            nb -= 32;
+            const uint32_t w = bswap32((uint32_t)(acc >> nb));
+            if (first)
+                atomicOr(dst + wi, w);
+            else
+                dst[wi] = w;
+            first = false;
+            ++wi;
+        }
+    }
+    // append up to 32 bits (len <= 32, nb < 32 on entry)
+    __device__ __forceinline__ void put(uint32_t code, uint32_t len)
+    {
+        acc = (acc << len) | code;
+        nb += len;
+        emit_if_full();
+    }
+    // append up to 48 bits
+    __device__ __forceinline__ void put_long(uint64_t code, uint32_t len)
+    {
+        if (len > 24) {
+            put((uint32_t)(code >> 24), len - 24);
+            put((uint32_t)(code & 0xFFFFFFu), 24);
+        } else {
+            put((uint32_t)code, len);
+        }
+    }
+    __device__ __forceinline__ void finish()
+    {
+        if (nb)
+            atomicOr(dst + wi, bswap32((uint32_t)(acc << (32 - nb))));
+    }
+};
+
+// Encode entries of the 16 symbols held in v.  Returns the bit total; sets
+// *slow if some symbol has no packed entry (a code longer than 26 bits or a
+// byte without code), *bad if some byte has no code at all.
+__device__ __forceinline__ uint32_t lookup16(const EncShared &sh, uint4 v, uint32_t cnt, const ecc_codebook *cb,
+                                             uint32_t e[16], bool *slow, bool *bad)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    uint32_t bits = 0;
+    bool s = false;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t b = byte_of(wv[j >> 2], j & 3);
+        e[j] = sh.lut[b * 32 + lane];
+        bits += e[j] & 31u;
+        s |= (e[j] == 0u) & ((uint32_t)j < cnt);
+    }
+    *slow = s;
+    *bad = false;
+    if (cnt < 16 || s) { // rare: recount exactly
+        bits = 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if ((uint32_t)j >= cnt)
+                continue;
+            if (e[j]) {
+                bits += e[j] & 31u;
+            } else {
+                const uint32_t L = min((uint32_t)cb->len[byte_of(wv[j >> 2], j & 3)], (uint32_t)ECC_MAX_CODE_LEN);
+                *bad |= (L == 0);
+                bits += L;
+            }
+        }
+    }
+    return bits;
+}
+
+__device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], uint4 v, uint32_t cnt, bool slow,
+                                       const ecc_codebook *cb)
+{
+    if (!slow && cnt == 16) {
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            const uint32_t l1 = e[j] & 31u, l2 = e[j + 1] & 31u;
+            const uint32_t pl = l1 + l2;
+            if (pl <= 32) {
+                const uint32_t pc = ((e[j] >> 5) << l2) | (e[j + 1] >> 5);
+                pk.put(pc, pl);
+            } else {
+                pk.put(e[j] >> 5, l1);
+                pk.put(e[j + 1] >> 5, l2);
+            }
+        }
+    } else {
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if ((uint32_t)j >= cnt)
+                continue;
+            if (e[j]) {
+                pk.put(e[j] >> 5, e[j] & 31u);
+            } else {
+                const uint32_t b = byte_of(wv[j >> 2], j & 3);
+                const uint32_t L = min((uint32_t)cb->len[b], (uint32_t)ECC_MAX_CODE_LEN);
+                if (L)
+                    pk.put_long(cb->code[b] & ((1ull << L) - 1), L);
+            }
+        }
+    }
+    pk.finish();
+}
+
+// One tile pass over a chunk: lookups, block scan of bit counts, packing into
+// `sink` (chunk-relative bit offsets).  Writes sub_bits when write_sub.
+// Returns the tile's bit total (uniform across the CTA).
+template <bool kCheckRoom>
+__device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job, uint64_t base, uint32_t L, uint32_t t0,
+                                                uint32_t run, uint32_t *sink, uint32_t sink_bits, bool write_sub,
+                                                bool *bad_out)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t my0 = t0 + (uint32_t)tid * kSymPerThread;
+    const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
+    const uint4 v = cnt ? load_symbols(job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
+    uint32_t e[16];
+    bool slow, bad;
+    const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, &slow, &bad);
+    *bad_out |= bad;
+
+    uint32_t incl = bits;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(~0u, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        sh.warp_tot[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, tile_total = 0;
+#pragma unroll
+    for (int w = 0; w < kEncWarps; ++w) {
+        const uint32_t t = sh.warp_tot[w];
+        before += w < warp ? t : 0u;
+        tile_total += t;
+    }
+    const uint32_t excl = before + incl - bits;
+    if (write_sub) {
+        sh.off[tid] = excl;
+        if (tid == 0)
+            sh.off[kEncThreads] = tile_total;
+    }
+    const uint32_t pos = run + excl;
+    if (cnt) {
+        if (!kCheckRoom || pos + bits <= sink_bits) {
+            Packer pk;
+            pk.start(sink, pos);
+            pack16(pk, e, v, cnt, slow, job.cb);
+        } else {
+            atomicOr(&sh.flags, 1u);
+        }
+    }
+    __syncthreads();
+    if (write_sub && cnt) {
+        const uint32_t tps = job.S / kSymPerThread;
+        if ((uint32_t)tid % tps == 0) {
+            const uint32_t end = min((uint32_t)tid + tps, (uint32_t)kEncThreads);
+            job.sub_bits[(base + my0) / job.S] = (uint16_t)(sh.off[end] - sh.off[tid]);
+        }
+    }
+    return tile_total;
+}
+
+// Encode chunk c of job into its place in job.out.  `stage` is a zeroed
+// shared-memory buffer of stage_bytes; it is zeroed again on return.
+__device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uint32_t stage_bytes, const EncJob &job,
+                                             uint64_t c, uint64_t timeout_ns)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t base = c * job.C;
+    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
+    if (tid == 0)
+        sh.flags = 0;
+    __syncthreads();
+
+    bool bad = false;
+    uint32_t run = 0;
+    for (uint32_t t0 = 0; t0 < L; t0 += kTile)
+        run += encode_tile<true>(sh, job, base, L, t0, run, stage, stage_bytes * 8u, true, &bad);
+    if (bad)
+        set_status(job.status, ECC_ERR_CODEBOOK);
+
+    const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
+    if (warp == 0) {
+        bool to;
+        const uint64_t prefix = lookback(job.flags, c, bytes, timeout_ns, &to);
+        if (lane == 0) {
+            sh.prefix = prefix;
+            if (to) {
+                atomicOr(&sh.flags, 2u);
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            }
+            job.chunk_off[c + 1] = prefix + bytes;
+            if (c == 0)
+                job.chunk_off[0] = 0;
+            atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)run);
+        }
+    }
+    __syncthreads();
+    const uint64_t prefix = sh.prefix;
+    const uint32_t fl = sh.flags;
+    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
+    const uint32_t nvec = (uint32_t)(bytes / 16);
+    const bool fits = prefix + bytes <= job.out_cap;
+    if (!fits && !(fl & 2u) && tid == 0)
+        set_status(job.status, ECC_ERR_CAPACITY);
+    if (!(fl & 1u)) {
+        uint4 *dst = reinterpret_cast<uint4 *>(job.out + prefix);
+        const bool write = fits && !(fl & 2u);
+        for (uint32_t i = tid; i < nvec; i += kEncThreads) {
+            const uint4 w = st4[i];
+            st4[i] = make_uint4(0, 0, 0, 0);
+            if (write)
+                st_stream16(dst + i, w);
+        }
+    } else {
+        // the payload outgrew the staging buffer: re-encode straight into
+        // global memory (zeroed first), then clear the whole stage
+        for (uint32_t i = tid; i < stage_bytes / 16; i += kEncThreads)
+            st4[i] = make_uint4(0, 0, 0, 0);
+        if (fits && !(fl & 2u)) {
+            uint4 *dst = reinterpret_cast<uint4 *>(job.out + prefix);
+            for (uint32_t i = tid; i < nvec; i += kEncThreads)
+                dst[i] = make_uint4(0, 0, 0, 0);
+            __syncthreads();
+            bool bad2 = false;
+            uint32_t run2 = 0;
+            uint32_t *gsink = reinterpret_cast<uint32_t *>(job.out + prefix);
+            for (uint32_t t0 = 0; t0 < L; t0 += kTile)
+                run2 += encode_tile<false>(sh, job, base, L, t0, run2, gsink, 0, false, &bad2);
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- decoder
+// One warp decodes one chunk: lane l runs the sub-blocks l, l + 32, ... of
+// the chunk as independent bit streams, starting at offsets given by a warp
+// scan of sub_bits.  Each step peeks 12 bits and resolves the code through
+// the first-level table; longer Huffman codes fall back to canonical
+// per-length ranges.
+struct DecJob {
+    const uint8_t *in;
+    uint64_t in_bytes;
+    const uint64_t *chunk_off;
+    const uint16_t *sub_bits;
+    uint64_t n;
+    uint32_t C, S;
+    const ecc_codebook *cb;
+    uint8_t *out;
+    uint32_t *status;
+};
+
+// Resolve a code longer than the first-level table from the canonical
+// per-length ranges.  win holds the next 64 stream bits, MSB first.  Returns
+// byte | len << 8, or 0 for a code the codebook lacks.
+static __device__ __noinline__ uint32_t decode_long(uint64_t win, const ecc_codebook *cb)
+{
+    if (cb->family != ECC_FAMILY_HUFFMAN)
+        return 0;
+    const uint32_t maxl = min(cb->max_len, (uint32_t)ECC_MAX_CODE_LEN);
+    for (uint32_t L = ECC_PEEK_BITS + 1; L <= maxl; ++L) {
+        const uint32_t k = cb->count[L];
+        if (!k)
+            continue;
+        const uint64_t v = win >> (64 - L);
+        const uint64_t d = v - cb->first[L];
+        if (d < k) {
+            const uint32_t at = cb->index[L] + (uint32_t)d;
+            return at < 256 ? (uint32_t)cb->sorted[at] | (L << 8) : 0u;
+        }
+    }
+    return 0;
+}
+
+// Bit reader over 32-bit words in memory byte order.  (hi, lo) are the two
+// words at wp-2, wp-1; o is the bit offset into hi.
+template <bool kShared>
+struct Reader {
+    const uint32_t *words;
+    uint32_t wlast; // last readable word index
+    uint32_t wp;
+    uint32_t hi, lo, o;
+
+    __device__ __forceinline__ uint32_t word(uint32_t i) const
+    {
+        const uint32_t k = min(i, wlast);
+        if (kShared)
+            return bswap32(words[k]);
+        return bswap32(__ldg(words + k));
+    }
+    __device__ __forceinline__ void start(const uint32_t *w, uint32_t last, uint32_t bit)
+    {
+        words = w;
+        wlast = last;
+        const uint32_t w0 = bit >> 5;
+        o = bit & 31;
+        hi = word(w0);
+        lo = word(w0 + 1);
+        wp = w0 + 2;
+    }
+    __device__ __forceinline__ uint32_t peek32() const { return __funnelshift_l(lo, hi, o); }
+    __device__ __forceinline__ uint32_t position() const { return (wp - 2) * 32 + o; }
+    __device__ __forceinline__ void refill()
+    {
+        if (o >= 32) {
+            hi = lo;
+            lo = word(wp);
+            ++wp;
+            o -= 32;
+        }
+    }
+    __device__ __forceinline__ uint64_t window64() const
+    {
+        const uint64_t two = ((uint64_t)hi << 32) | lo;
+        const uint64_t w3 = word(wp);
+        return o ? (two << o) | (w3 >> (32 - o)) : two;
+    }
+};
+
+// Decode one symbol; returns the byte, advances the reader, flags bad codes.
+template <bool kShared>
+__device__ __forceinline__ uint32_t decode_symbol(Reader<kShared> &r, const uint16_t *dec, const ecc_codebook *cb,
+                                                  bool &bad)
+{
+    const uint32_t e0 = dec[r.peek32() >> (32 - ECC_PEEK_BITS)];
+    uint32_t e = e0;
+    if (e0 == 0) {
+        e = decode_long(r.window64(), cb);
+        if (e == 0) {
+            bad = true;
+            e = 1u << 8; // consume one bit to keep going (output is flagged)
+        }
+        r.o += e >> 8;
+        while (r.o >= 32)
+            r.refill();
+        return e & 0xFF;
+    }
+    r.o += e >> 8;
+    r.refill();
+    return e & 0xFF;
+}
+
+// Decode the R sub-blocks a lane owns in one group of a chunk.
+template <int R, bool kShared>
+__device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *dec, const uint32_t *words,
+                                             uint32_t wlast, uint64_t base, uint32_t L, uint32_t g0,
+                                             const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
+{
+    const int lane = threadIdx.x & 31;
+    Reader<kShared> rd[R];
+    uint32_t cnt[R], endpos[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t k = g0 + (uint32_t)(r * 32 + lane);
+        const uint32_t s0 = k * job.S;
+        cnt[r] = s0 < L ? min(job.S, L - s0) : 0u;
+        rd[r].start(words, wlast, st[r]);
+        endpos[r] = st[r];
+    }
+    uint32_t steps = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        steps = max(steps, cnt[r]);
+    bool full = true;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        full &= cnt[r] == job.S;
+    // steps differs between lanes only in the tensor's last chunk
+    for (uint32_t i = 0; i < steps; i += 16) {
+        uint32_t w[R][4];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0;
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, job.cb, bad), 0x4321);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        if (i + q * 4 + t < cnt[r])
+                            w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, job.cb, bad), 0x4321);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (i >= cnt[r])
+                continue;
+            const uint32_t k = g0 + (uint32_t)(r * 32 + lane);
+            uint8_t *dst = job.out + base + (uint64_t)k * job.S + i;
+            if (i + 16 <= cnt[r]) {
+                st_stream16(dst, make_uint4(w[r][0], w[r][1], w[r][2], w[r][3]));
+            } else {
+                const uint32_t m = cnt[r] - i;
+                // partial group: bytes sit in the high end of each word
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    if ((uint32_t)t >= m)
+                        continue;
+                    const uint32_t filled = min(4u, m - (uint32_t)(t & ~3)); // bytes pushed into word t/4
+                    const uint32_t sh = 8u * (4u - filled + (uint32_t)(t & 3));
+                    dst[t] = (uint8_t)(w[r][t >> 2] >> sh);
+                }
+            }
+            if (i + 16 >= cnt[r])
+                endpos[r] = rd[r].position();
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (cnt[r] && endpos[r] - st[r] != nb[r])
+            bad = true;
+}
+
+// Decode chunk c with one warp.  stage: this warp's shared buffer of
+// stage_bytes (NULL: read the payload from global memory).
+template <int R>
+__device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *dec, uint32_t *stage,
+                                             uint32_t stage_bytes, uint64_t c)
+{
+    const int lane = threadIdx.x & 31;
+    const uint64_t b0 = job.chunk_off[c], b1 = job.chunk_off[c + 1];
+    const uint64_t base = c * job.C;
+    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
+    const uint32_t nsub = (L + job.S - 1) / job.S;
+    const uint64_t sub0 = base / job.S;
+    if (b1 < b0 || b1 > job.in_bytes || ((b0 | b1) & 15) || (b1 - b0) > (uint64_t)job.C * 8) {
+        if (lane == 0)
+            set_status(job.status, ECC_ERR_CORRUPT);
+        return;
+    }
+    const uint32_t bytes = (uint32_t)(b1 - b0);
+    if (bytes == 0) { // every chunk holds at least one code bit
+        if (lane == 0)
+            set_status(job.status, ECC_ERR_CORRUPT);
+        return;
+    }
+    const bool staged = stage != nullptr && bytes + 16 <= stage_bytes;
+    const uint32_t *words;
+    uint32_t wlast;
+    if (staged) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(job.in + b0);
+        uint4 *dst = reinterpret_cast<uint4 *>(stage);
+        for (uint32_t i = lane; i < bytes / 16; i += 32)
+            dst[i] = ld_stream16(src + i);
+        if (lane == 0)
+            dst[bytes / 16] = make_uint4(0, 0, 0, 0); // guard: peeks past the end read 0
+        __syncwarp();
+        words = stage;
+        wlast = bytes / 4 + 3;
+    } else {
+        words = reinterpret_cast<const uint32_t *>(job.in + b0);
+        wlast = bytes / 4 ? bytes / 4 - 1 : 0;
+    }
+
+    bool bad = false;
+    uint32_t carry = 0;
+    for (uint32_t g0 = 0; g0 < nsub; g0 += 32 * R) {
+        uint32_t st[R], nb[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t k = g0 + (uint32_t)(r * 32 + lane);
+            const uint32_t v = k < nsub ? job.sub_bits[sub0 + k] : 0u;
+            uint32_t incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(~0u, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            st[r] = carry + incl - v;
+            nb[r] = v;
+            carry += __shfl_sync(~0u, incl, 31);
+        }
+        if (staged)
+            decode_group<R, true>(job, dec, words, wlast, base, L, g0, st, nb, bad);
+        else
+            decode_group<R, false>(job, dec, words, wlast, base, L, g0, st, nb, bad);
+    }
+    if (pad16((carry + 7) / 8) != bytes)
+        bad = true;
+    // the padding after the last code must be zero bits
+    if (!bad && lane == 0) {
+        for (uint32_t wi = carry >> 5; wi < bytes / 4; ++wi) {
+            uint32_t w = bswap32(staged ? words[wi] : __ldg(words + wi));
+            if (wi == (carry >> 5))
+                w &= 0xFFFFFFFFu >> (carry & 31);
+            bad |= w != 0;
+        }
+    }
+    if (__any_sync(~0u, bad) && lane == 0)
+        set_status(job.status, ECC_ERR_CORRUPT);
+    __syncwarp();
+}
+
+} // namespace ecc

@@ -1,0 +1,337 @@
+// ecc_kernels.cu -- sm_103a kernels and C-ABI launchers for single tensors:
+// byte histogram, chunk-parallel encode with decoupled look-back, and
+// warp-per-chunk decode.  See include/ecc.h for the contract.
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "ecc_device.cuh"
+#include "ecc_launch.h"
+
+namespace ecc {
+
+// ---------------------------------------------------------------- histogram
+// e4m3_histogram: per-warp sub-histograms in shared memory (privatised bins:
+// lanes of different warps never collide), 16-byte streaming loads, one
+// 64-bit global atomic per non-empty bin per CTA at the end.
+constexpr int kHistThreads = 512;
+constexpr int kHistWarps = kHistThreads / 32;
+
+__global__ void __launch_bounds__(kHistThreads) hist_kernel(const uint8_t *in, uint64_t n, uint64_t head,
+                                                            unsigned long long *count)
+{
+    __shared__ uint32_t h[kHistWarps][256];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int i = tid; i < kHistWarps * 256; i += kHistThreads)
+        (&h[0][0])[i] = 0;
+    __syncthreads();
+    uint32_t *mine = h[warp];
+    // unaligned head and the tail bytes: block 0
+    const uint64_t nvec = (n - head) / 16;
+    const uint64_t tail0 = head + nvec * 16;
+    if (blockIdx.x == 0) {
+        for (uint64_t i = tid; i < head; i += kHistThreads)
+            atomicAdd(&mine[in[i]], 1u);
+        for (uint64_t i = tail0 + tid; i < n; i += kHistThreads)
+            atomicAdd(&mine[in[i]], 1u);
+    }
+    const uint8_t *body = in + head;
+    const uint64_t stride = (uint64_t)gridDim.x * kHistThreads;
+    for (uint64_t i = (uint64_t)blockIdx.x * kHistThreads + tid; i < nvec; i += stride) {
+        const uint4 v = ld_stream16(body + i * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            atomicAdd(&mine[byte_of(w[j >> 2], j & 3)], 1u);
+    }
+    __syncthreads();
+    for (int b = tid; b < 256; b += kHistThreads) {
+        uint32_t s = 0;
+#pragma unroll
+        for (int w = 0; w < kHistWarps; ++w)
+            s += h[w][b];
+        if (s)
+            atomicAdd(count + b, (unsigned long long)s);
+    }
+}
+
+// ---------------------------------------------------------------- encode
+struct EncParams {
+    EncJob job;
+    uint64_t n_chunks;
+    uint32_t *ticket;
+    uint32_t stage_bytes;
+    uint64_t timeout_ns;
+};
+
+// zero the look-back flags, the ticket and the outputs the kernel accumulates
+__global__ void enc_prologue_kernel(uint64_t *flags, uint64_t n_flags, uint32_t *ticket, uint64_t *total_bits,
+                                    uint64_t *chunk_off, uint32_t *status)
+{
+    const uint64_t i0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (uint64_t i = i0; i < n_flags; i += (uint64_t)gridDim.x * blockDim.x)
+        flags[i] = 0;
+    if (i0 == 0) {
+        *ticket = 0;
+        *total_bits = 0;
+        chunk_off[0] = 0;
+        *status = ECC_OK;
+    }
+}
+
+// Persistent CTAs take chunks in ticket order, so a chunk's predecessors have
+// always been claimed by running CTAs when it looks back.
+__global__ void __launch_bounds__(kEncThreads) encode_kernel(EncParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    EncShared &sh = *reinterpret_cast<EncShared *>(smem);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + enc_shared_bytes());
+    if (p.job.cb->magic != ECC_CODEBOOK_MAGIC || p.job.cb->max_len > ECC_MAX_CODE_LEN) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            set_status(p.job.status, ECC_ERR_CODEBOOK);
+        return;
+    }
+    load_encode_lut(sh, p.job.cb);
+    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
+    for (uint32_t i = threadIdx.x; i < p.stage_bytes / 16; i += kEncThreads)
+        st4[i] = make_uint4(0, 0, 0, 0);
+    for (;;) {
+        if (threadIdx.x == 0)
+            sh.ticket = atomicAdd(p.ticket, 1u);
+        __syncthreads();
+        const uint64_t c = sh.ticket;
+        if (c >= p.n_chunks)
+            break;
+        encode_chunk(sh, stage, p.stage_bytes, p.job, c, p.timeout_ns);
+    }
+}
+
+// ---------------------------------------------------------------- decode
+struct DecParams {
+    DecJob job;
+    uint64_t n_chunks;
+    uint32_t stage_bytes;
+};
+
+template <int R>
+__global__ void decode_kernel(DecParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
+    const int warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
+    if (p.job.cb->magic != ECC_CODEBOOK_MAGIC || p.job.cb->max_len > ECC_MAX_CODE_LEN) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            set_status(p.job.status, ECC_ERR_CODEBOOK);
+        return;
+    }
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.job.cb->dec);
+        uint4 *dst = reinterpret_cast<uint4 *>(dec);
+        for (int i = threadIdx.x; i < (int)(sizeof(p.job.cb->dec) / 16); i += blockDim.x)
+            dst[i] = src[i];
+    }
+    __syncthreads();
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + sizeof(((ecc_codebook *)0)->dec) +
+                                                   (size_t)warp * p.stage_bytes);
+    for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += (uint64_t)gridDim.x * warps)
+        decode_chunk<R>(p.job, dec, stage, p.stage_bytes, c);
+}
+
+// ---------------------------------------------------------------- self-test
+__global__ void selftest_wait_kernel(uint64_t *flags, uint64_t chunk, uint64_t aggregate, uint64_t timeout_ns,
+                                     uint64_t *prefix, uint32_t *status)
+{
+    bool to;
+    const uint64_t pre = lookback(flags, chunk, aggregate, timeout_ns, &to);
+    if (threadIdx.x == 0) {
+        *prefix = pre;
+        *status = to ? ECC_ERR_TIMEOUT : ECC_OK;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+struct DevInfo {
+    int sms = 0;
+    std::map<std::pair<const void *, size_t>, int> occ; // (kernel, smem) -> blocks/SM
+};
+
+std::mutex g_mu;
+std::map<int, DevInfo> g_dev;
+
+DevInfo *device_info()
+{
+    int dev;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.sms && cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        d.sms = 0;
+        return nullptr;
+    }
+    return &d;
+}
+
+bool pow2_in(uint64_t v, uint64_t lo, uint64_t hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+} // namespace
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool valid_sizes(uint32_t C, uint32_t S) { return pow2_in(C, 1024, 65536) && pow2_in(S, 64, 1024) && S <= C; }
+
+ecc_status launch_status(cudaError_t e)
+{
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ECC_ERR_CUDA;
+    }
+    return ECC_OK;
+}
+
+int sm_count()
+{
+    DevInfo *d = device_info();
+    return d ? d->sms : 0;
+}
+
+int occupancy(const void *kernel, int threads, size_t smem)
+{
+    DevInfo *d = device_info();
+    if (!d)
+        return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(kernel, smem);
+    auto it = d->occ.find(key);
+    if (it != d->occ.end())
+        return it->second;
+    int nb = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        nb = 0;
+    }
+    d->occ[key] = nb;
+    return nb;
+}
+
+} // namespace ecc
+
+using namespace ecc;
+
+extern "C" {
+
+size_t ecc_encode_workspace_bytes(size_t n, uint32_t C)
+{
+    if (!C)
+        return 0;
+    return 256 + ecc_num_chunks(n, C) * sizeof(uint64_t);
+}
+
+ecc_status e4m3_histogram(const uint8_t *in, size_t n, uint64_t *count, void *stream)
+{
+    if (!count || (n && !in))
+        return ECC_ERR_ARG;
+    if (!n)
+        return ECC_OK;
+    const int sms = sm_count();
+    if (!sms)
+        return ECC_ERR_CUDA;
+    const uint64_t head = std::min<uint64_t>(n, (16 - ((uintptr_t)in & 15)) & 15);
+    const uint64_t nvec = (n - head) / 16;
+    uint64_t blocks = (nvec + kHistThreads - 1) / kHistThreads;
+    const uint64_t cap = (uint64_t)sms * 4;
+    blocks = std::max<uint64_t>(1, std::min(blocks, cap));
+    hist_kernel<<<(unsigned)blocks, kHistThreads, 0, (cudaStream_t)stream>>>(in, n, head,
+                                                                              (unsigned long long *)count);
+    return launch_status(cudaGetLastError());
+}
+
+ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S, uint8_t *out,
+                      size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits, uint64_t *total_bits, void *ws,
+                      size_t ws_bytes, uint32_t *status, void *stream)
+{
+    if (!cb || !chunk_off || !total_bits || !status || !ws || !valid_sizes(C, S))
+        return ECC_ERR_ARG;
+    if (n && (!in || !out || !sub_bits || !aligned16(in) || !aligned16(out)))
+        return ECC_ERR_ARG;
+    if (!aligned16(ws) || ws_bytes < ecc_encode_workspace_bytes(n, C))
+        return ECC_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint64_t n_chunks = ecc_num_chunks(n, C);
+    uint32_t *ticket = (uint32_t *)ws;
+    uint64_t *flags = (uint64_t *)((uint8_t *)ws + 256);
+    {
+        const uint64_t nb = std::max<uint64_t>(1, std::min<uint64_t>((n_chunks + 255) / 256, 1024));
+        enc_prologue_kernel<<<(unsigned)nb, 256, 0, st>>>(flags, n_chunks, ticket, total_bits, chunk_off, status);
+        ecc_status e = launch_status(cudaGetLastError());
+        if (e != ECC_OK || !n)
+            return e;
+    }
+    EncParams p;
+    p.job = EncJob{in, n, cb, C, S, out, out_cap, chunk_off, sub_bits, total_bits, flags, status};
+    p.n_chunks = n_chunks;
+    p.ticket = ticket;
+    p.stage_bytes = stage_bytes_for(C);
+    p.timeout_ns = kWaitLimitNs;
+    const size_t smem = enc_shared_bytes() + p.stage_bytes;
+    const int occ = occupancy((const void *)encode_kernel, kEncThreads, smem);
+    const int sms = sm_count();
+    if (occ <= 0 || sms <= 0)
+        return ECC_ERR_CUDA;
+    const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
+    encode_kernel<<<(unsigned)grid, kEncThreads, smem, st>>>(p);
+    return launch_status(cudaGetLastError());
+}
+
+ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_off, const uint16_t *sub_bits,
+                      size_t n, uint32_t C, uint32_t S, const ecc_codebook *cb, uint8_t *out, uint32_t *status,
+                      void *stream)
+{
+    if (!cb || !status || !chunk_off || !valid_sizes(C, S))
+        return ECC_ERR_ARG;
+    if (n && (!in || !out || !sub_bits || !aligned16(in) || !aligned16(out)))
+        return ECC_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return launch_status(cudaErrorUnknown);
+    if (!n)
+        return ECC_OK;
+    DecParams p;
+    p.job = DecJob{in, in_bytes, chunk_off, sub_bits, n, C, S, cb, out, status};
+    p.n_chunks = ecc_num_chunks(n, C);
+    p.stage_bytes = stage_bytes_for(C);
+    const size_t table = sizeof(((ecc_codebook *)0)->dec);
+    int warps = (int)std::min<size_t>(kDecMaxWarps, (kMaxDynSmem - table) / p.stage_bytes);
+    warps = std::max(warps, 1);
+    const size_t smem = table + (size_t)warps * p.stage_bytes;
+    const bool two = C / S >= 64;
+    const void *kfn = two ? (const void *)decode_kernel<2> : (const void *)decode_kernel<1>;
+    const int occ = occupancy(kfn, warps * 32, smem);
+    const int sms = sm_count();
+    if (occ <= 0 || sms <= 0)
+        return ECC_ERR_CUDA;
+    const uint64_t need = (p.n_chunks + warps - 1) / warps;
+    const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, need);
+    if (two)
+        decode_kernel<2><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    else
+        decode_kernel<1><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    return launch_status(cudaGetLastError());
+}
+
+ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate, uint64_t timeout_ns,
+                             uint64_t *prefix, uint32_t *status, void *stream)
+{
+    if (!flags || !prefix || !status || timeout_ns == 0 || timeout_ns > 10ull * kWaitLimitNs)
+        return ECC_ERR_ARG;
+    selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flags, chunk, aggregate, timeout_ns, prefix, status);
+    return launch_status(cudaGetLastError());
+}
+
+} // extern "C"

@@ -1,0 +1,24 @@
+// ecc_launch.h -- host-side launch helpers shared by the kernel translation
+// units (device properties, occupancy, argument checks).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ecc.h"
+
+namespace ecc {
+
+constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit
+constexpr int kDecMaxWarps = 8;
+
+bool valid_sizes(uint32_t C, uint32_t S);
+bool aligned16(const void *p);
+ecc_status launch_status(cudaError_t e);
+int sm_count();
+// CTAs of `kernel` that fit on one SM (raises the kernel's dynamic shared
+// memory limit on first use on the current device).
+int occupancy(const void *kernel, int threads, size_t smem);
+
+} // namespace ecc

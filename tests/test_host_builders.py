@@ -1,0 +1,154 @@
+"""The library's host side (C ABI, no GPU needed) against the oracle.
+
+The codebook builders, the width search and the figures of the CUDA library
+are independent implementations; here they must agree with the oracle bit
+for bit (tables) or to 1e-9 relative (float64 figures).
+"""
+import ctypes as ct
+import os
+import re
+
+import numpy as np
+import pytest
+
+import lossless_entropy_coding_gb300 as ecc
+import oracle
+from lossless_entropy_coding_gb300 import build as ecc_build
+from workloads import np_gauss, np_grad, np_zero_spike, qlc_base_tensor
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ecc_build.build()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "ecc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert len(names) >= 19
+    lib = ct.CDLL(ecc.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_codebook_layout():
+    assert ecc.codebook_bytes() == ecc.CODEBOOK_DTYPE.itemsize
+
+
+def pmfs():
+    g = np.random.default_rng(7)
+    ties = np.zeros(256, np.uint64)
+    ties[g.choice(256, 40, replace=False)] = 5
+    ties[[0, 255]] = 9
+    return {
+        "gauss": oracle.histogram(qlc_base_tensor()),
+        "spike": oracle.histogram(np_zero_spike(1 << 20, (3, 5))),
+        "grad": oracle.histogram(np_grad(1 << 20, (4, 5))),
+        "uniform": np.full(256, 11, np.uint64),
+        "ties": ties,
+        "random": g.integers(0, 1 << 40, 256).astype(np.uint64),
+        "one": np.eye(256, dtype=np.uint64)[200] * 77,
+    }
+
+
+@pytest.mark.parametrize("name", list(pmfs().keys()))
+def test_qlc_tables_match_oracle(name):
+    count = pmfs()[name]
+    widths = [ecc.BASE_WIDTHS, (0, 1, 1, 4, 4, 4, 4, 8), (8, 0, 0, 0, 0, 0, 0, 0), (2, 2, 4, 4, 5, 5, 6, 7)]
+    for w in widths:
+        cb = ecc.codebook_view(ecc.qlc_build_tables(count, w))
+        ref = oracle.qlc_codebook(count, w)
+        assert cb["magic"] == 0x45434342 and cb["family"] == ecc.FAMILY_QLC
+        assert (cb["len"] == ref["len"]).all()
+        assert (cb["code"] == ref["code"]).all()
+        assert (cb["by_rank"] == ref["by_rank"]).all()
+        r, _ = oracle.rank(count)
+        assert (cb["rank"] == r).all()
+        assert cb["max_len"] == ref["len"].max()
+
+
+@pytest.mark.parametrize("name", ["gauss", "spike", "grad", "ties", "random"])
+@pytest.mark.parametrize("full", [False, True])
+def test_width_search_matches_oracle(name, full):
+    count = pmfs()[name]
+    for md in (2, 3, 4):
+        w, cost = ecc.qlc_search_widths(count, md, full)
+        wr, cr = oracle.qlc_search(count, md, full)
+        assert cost == cr and (w == wr).all()
+
+
+def test_width_search_rejects_impossible():
+    with pytest.raises(ecc.EccError):
+        ecc.qlc_search_widths(np.ones(256, np.uint64), 0)
+
+
+@pytest.mark.parametrize("name", list(pmfs().keys()))
+def test_huffman_matches_oracle(name):
+    weight = pmfs()[name]
+    cb = ecc.codebook_view(ecc.huff_build_canonical(weight))
+    ref = oracle.huffman_codebook(weight)
+    assert cb["family"] == ecc.FAMILY_HUFFMAN
+    assert (cb["len"] == ref["len"]).all()
+    assert (cb["code"] == ref["code"]).all()
+    fixed = oracle.fixed_codebook_weights([weight])
+    cb2 = ecc.codebook_view(ecc.huff_build_canonical(fixed))
+    assert (cb2["len"] == oracle.huffman_lengths(fixed)).all()
+
+
+def test_huffman_length_limit_is_an_error():
+    w = np.zeros(256, np.uint64)
+    a, b = 1, 1
+    for s in range(52):            # Fibonacci weights: depth 50
+        w[s] = a
+        a, b = b, a + b
+    assert oracle.huffman_lengths(w).max() > 48
+    with pytest.raises(ecc.EccError) as ei:
+        ecc.huff_build_canonical(w, 48)
+    assert ei.value.code == ecc.ERR_CODEBOOK
+    with pytest.raises(ecc.EccError):
+        ecc.huff_build_canonical(np.zeros(256, np.uint64))
+
+
+def test_derived_decode_table():
+    # every 12-bit index resolves to the code that prefixes it, or is 0 when
+    # no code of <= 12 bits does
+    for cbb in (ecc.qlc_build_tables(pmfs()["gauss"]), ecc.huff_build_canonical(pmfs()["spike"] + 1)):
+        cb = ecc.codebook_view(cbb)
+        want = np.zeros(4096, np.uint16)
+        for b in range(256):
+            L = int(cb["len"][b])
+            if 0 < L <= 12:
+                lo = int(cb["code"][b]) << (12 - L)
+                want[lo:lo + (1 << (12 - L))] = b | (L << 8)
+        assert (cb["dec"] == want).all()
+        for b in range(256):
+            L = int(cb["len"][b])
+            e = int(cb["enc"][b])
+            assert e == ((int(cb["code"][b]) << 5) | L if 0 < L <= 26 else 0)
+
+
+def test_figures_match_oracle():
+    P = pmfs()
+    for a in ("gauss", "spike", "grad", "random"):
+        h, hr = ecc.entropy_bits(P[a]), oracle.entropy_bits(P[a])
+        assert abs(h - hr) <= 1e-9 * abs(hr)
+        for b in ("gauss", "uniform", "random"):
+            k, kr = ecc.kl_bits(P[a], P[b] + 1), oracle.kl_bits(P[a], P[b] + 1)
+            assert abs(k - kr) <= 1e-9 * max(abs(kr), 1e-300)
+        cb = ecc.qlc_build_tables(P[a])
+        assert ecc.code_bits(P[a], cb) == oracle.code_bits(P[a], oracle.qlc_codebook(P[a])["len"])
+
+
+def test_sizes():
+    for n in (0, 1, 1023, 1024, 1025, 5 * 16384 + 3):
+        for C in (1024, 16384):
+            assert ecc.num_chunks(n, C) == -(-n // C)
+            for L in (11, 48):
+                assert ecc.max_encoded_bytes(n, C, L) == oracle.max_encoded_bytes(n, C, L)
