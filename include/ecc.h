@@ -23,7 +23,8 @@
  *    the call first sets to ECC_OK.  Read it after the stream has reached the
  *    end of the call.  The first error written wins.
  *  - Device buffers are plain device pointers owned by the caller.  Buffers
- *    that hold bytes (tensor, payload) must start on a 16-byte boundary.
+ *    that hold bytes (tensor, payload) and the device codebook must start on
+ *    a 16-byte boundary.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Device calls only enqueue work: they never synchronise and,
  *    apart from the batched calls' one host-to-device copy of their

@@ -217,7 +217,7 @@ ecc_status check_descs(const ecc_desc *descs, uint32_t count, bool encode, uint6
     uint32_t mc = 1024;
     for (uint32_t i = 0; i < count; ++i) {
         const ecc_desc &d = descs[i];
-        if (!valid_sizes(d.C, d.S) || !d.cb || !d.status || !d.chunk_off)
+        if (!valid_sizes(d.C, d.S) || !d.cb || !aligned16(d.cb) || !d.status || !d.chunk_off)
             return ECC_ERR_ARG;
         if (encode && !d.total_bits)
             return ECC_ERR_ARG;

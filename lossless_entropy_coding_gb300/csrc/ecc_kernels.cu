@@ -256,7 +256,7 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
                       size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits, uint64_t *total_bits, void *ws,
                       size_t ws_bytes, uint32_t *status, void *stream)
 {
-    if (!cb || !chunk_off || !total_bits || !status || !ws || !valid_sizes(C, S))
+    if (!cb || !aligned16(cb) || !chunk_off || !total_bits || !status || !ws || !valid_sizes(C, S))
         return ECC_ERR_ARG;
     if (n && (!in || !out || !sub_bits || !aligned16(in) || !aligned16(out)))
         return ECC_ERR_ARG;
@@ -293,7 +293,7 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
                       size_t n, uint32_t C, uint32_t S, const ecc_codebook *cb, uint8_t *out, uint32_t *status,
                       void *stream)
 {
-    if (!cb || !status || !chunk_off || !valid_sizes(C, S))
+    if (!cb || !aligned16(cb) || !status || !chunk_off || !valid_sizes(C, S))
         return ECC_ERR_ARG;
     if (n && (!in || !out || !sub_bits || !aligned16(in) || !aligned16(out)))
         return ECC_ERR_ARG;
