@@ -257,12 +257,14 @@ def test_bounded_wait_times_out():
     torch.cuda.synchronize()
     assert int(status.item()) == ecc.ERR_TIMEOUT
     # with every predecessor published it returns their sum, no timeout
-    flags[:40] = (1 << 62) | 16
-    flags[0] = (2 << 62) | 16
+    def word(state, value):                  # (state << 62) | value as int64
+        return int(np.array([(state << 62) | value], np.uint64).view(np.int64)[0])
+    flags[:40] = word(1, 16)
+    flags[0] = word(2, 16)
     ecc.ecc_selftest_wait(flags, 40, 123, 20_000_000, prefix, status)
     torch.cuda.synchronize()
     assert int(status.item()) == ecc.OK and int(prefix.item()) == 40 * 16
-    assert int(flags[40].item()) == (2 << 62) | (40 * 16 + 123)
+    assert int(flags[40].item()) == word(2, 40 * 16 + 123)
 
 
 def test_host_argument_errors():
