@@ -234,7 +234,7 @@ ecc_status check_descs(const ecc_desc *descs, uint32_t count, bool encode, uint6
 int decode_warps(uint32_t stage_bytes)
 {
     const size_t table = sizeof(((ecc_codebook *)0)->dec);
-    int w = (int)std::min<size_t>(kDecMaxWarps, (kMaxDynSmem - table) / stage_bytes);
+    int w = (int)std::min<size_t>(kDecMaxWarps, (kMaxDynSmem - kStaticSmemReserve - table) / stage_bytes);
     return std::max(w, 1);
 }
 

@@ -211,7 +211,10 @@ int occupancy(const void *kernel, int threads, size_t smem)
     if (it != d->occ.end())
         return it->second;
     int nb = 0;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxDynSmem) != cudaSuccess ||
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || fa.sharedSizeBytes + smem > kMaxDynSmem ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kMaxDynSmem - fa.sharedSizeBytes)) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess) {
         (void)cudaGetLastError();
         nb = 0;

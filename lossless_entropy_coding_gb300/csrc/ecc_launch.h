@@ -10,7 +10,8 @@
 
 namespace ecc {
 
-constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit
+constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit (static + dynamic)
+constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may add on top
 constexpr int kDecMaxWarps = 8;
 
 bool valid_sizes(uint32_t C, uint32_t S);
