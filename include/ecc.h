@@ -302,6 +302,30 @@ ecc_status ecc_decode_batched(const ecc_desc *descs, uint32_t count, void *ws, s
 ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate, uint64_t timeout_ns,
                              uint64_t *prefix, uint32_t *status, void *stream);
 
+/*
+ * ecc_encode_static -- ecc_encode without a workspace argument, for callers
+ * that cannot allocate device memory on their call path: latency-critical
+ * communication code (cudaMalloc can synchronise the whole device) and code
+ * embedded in a framework whose allocator owns all device memory.  The pages
+ * have no counterpart; this is a property of the library, not of the method.
+ *   Arguments, outputs and errors are those of ecc_encode.  The scratch
+ *   space (a ticket and one 64-bit look-back word per chunk) is a file-scope
+ *   device array of ECC_STATIC_MAX_CHUNKS + 32 words (about 512 KiB) that
+ *   every GPU loading the library holds until the process exits; the call
+ *   allocates and frees nothing.  Inputs with more than ECC_STATIC_MAX_CHUNKS
+ *   chunks (n > 65536 * C) are rejected with ECC_ERR_ARG.
+ *   The first call on each device resolves the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  Every call clears the scratch words it uses
+ *   before use, but all calls share the one array: calls that can overlap on
+ *   the GPU (other streams, other host threads) race and must be ordered by
+ *   the caller.
+ */
+#define ECC_STATIC_MAX_CHUNKS 65536u
+ecc_status ecc_encode_static(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S,
+                             uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,
+                             uint64_t *total_bits, uint32_t *status, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *ecc_status_string(ecc_status s);
 

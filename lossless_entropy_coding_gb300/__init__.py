@@ -84,6 +84,7 @@ def _load():
             "ecc_encode_batched": (I32, [P, U32, P, Z, P, P]),
             "ecc_decode_batched": (I32, [P, U32, P, Z, P, P]),
             "ecc_selftest_wait": (I32, [P, U64, U64, U64, P, P, P]),
+            "ecc_encode_static": (I32, [P, Z, P, U32, U32, P, Z, P, P, P, P, P]),
             "ecc_status_string": (ct.c_char_p, [I32]),
         }
         for name, (res, args) in sig.items():
@@ -320,3 +321,32 @@ def ecc_decode_batched(descs, ws, t_start=None, stream=None):
 def ecc_selftest_wait(flags, chunk: int, aggregate: int, timeout_ns: int, prefix, status, stream=None):
     _check(_load().ecc_selftest_wait(_dptr(flags), chunk, aggregate, timeout_ns, _dptr(prefix), _dptr(status),
                                      _stream_ptr(stream)), "ecc_selftest_wait")
+
+
+STATIC_MAX_CHUNKS = 65536
+
+
+def ecc_encode_static(x, dev_cb, C: int = 16384, S: int | None = None, max_len: int = MAX_CODE_LEN, out=None,
+                      chunk_off=None, sub_bits=None, total_bits=None, status=None, stream=None) -> Encoded:
+    """ecc_encode with the library's built-in scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory on
+    their call path).  Calls that may overlap on the GPU must be ordered by
+    the caller: they share the scratch array."""
+    torch = _torch()
+    dev = x.device
+    n = x.numel()
+    S = default_subblock(C) if S is None else S
+    if out is None:
+        out = torch.empty(max(16, max_encoded_bytes(n, C, max_len)), dtype=torch.uint8, device=dev)
+    if chunk_off is None:
+        chunk_off = torch.empty(num_chunks(n, C) + 1, dtype=torch.int64, device=dev)
+    if sub_bits is None:
+        sub_bits = torch.empty(max(1, num_subblocks(n, S)), dtype=torch.int16, device=dev)
+    if total_bits is None:
+        total_bits = torch.empty(1, dtype=torch.int64, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(_load().ecc_encode_static(_dptr(x), n, _dptr(dev_cb), C, S, _dptr(out), out.numel(), _dptr(chunk_off),
+                                     _dptr(sub_bits), _dptr(total_bits), _dptr(status), _stream_ptr(stream)),
+           "ecc_encode_static")
+    return Encoded(out, chunk_off, sub_bits, total_bits, status, n, C, S)

@@ -338,3 +338,64 @@ ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate
 }
 
 } // extern "C"
+
+// ---------------------------------------------------------------- encode without allocation
+// ecc_encode_static: ecc_encode for callers that cannot allocate device
+// memory on their call path.  Its workspace (ticket + one look-back word per
+// chunk) is a file-scope device array instead of a caller buffer.
+namespace ecc {
+
+constexpr uint64_t kStaticMaxChunks = ECC_STATIC_MAX_CHUNKS;
+constexpr uint64_t kStaticScratchWords = 256 / sizeof(uint64_t) + kStaticMaxChunks;
+
+// Held by every GPU that loads the library until the process exits.  Host
+// code must not pass this name to a kernel: on the host it is only a
+// stand-in; the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint64_t g_encode_scratch[kStaticScratchWords];
+
+namespace {
+std::mutex g_scratch_mu;
+std::map<int, void *> g_scratch_addr; // device ordinal -> device address of g_encode_scratch
+
+// Resolve the array's device address once per device, with that device
+// current (the first ecc_encode_static call on a device does this).
+ecc_status static_scratch(void **out)
+{
+    int dev;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return ECC_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    auto it = g_scratch_addr.find(dev);
+    if (it != g_scratch_addr.end()) {
+        *out = it->second;
+        return ECC_OK;
+    }
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_encode_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return ECC_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+    *out = p;
+    return ECC_OK;
+}
+} // namespace
+
+} // namespace ecc
+
+extern "C" ecc_status ecc_encode_static(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S,
+                                        uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,
+                                        uint64_t *total_bits, uint32_t *status, void *stream)
+{
+    if (!valid_sizes(C, S) || ecc_num_chunks(n, C) > ecc::kStaticMaxChunks)
+        return ECC_ERR_ARG;
+    void *scratch = nullptr;
+    const ecc_status e = ecc::static_scratch(&scratch);
+    if (e != ECC_OK)
+        return e;
+    return ecc_encode(in, n, cb, C, S, out, out_cap, chunk_off, sub_bits, total_bits, scratch,
+                      sizeof(ecc::g_encode_scratch), status, stream);
+}
