@@ -21,6 +21,8 @@ struct BatchHeader {
     uint32_t count;
     uint32_t warps;       // decode: chunks per work item
     uint32_t stage_bytes;
+    uint32_t max_C;
+    uint32_t nbuf; // encode: shared input buffers (2 = next chunk prefetched)
     uint64_t total_items;
     uint64_t total_chunks;
     uint64_t desc_off, prefix_off, done_off, flags_off;
@@ -92,64 +94,123 @@ __device__ __forceinline__ void stamp_done(const ecc_desc &d, uint32_t *done, ui
         *d.t_done_ns = globaltimer();
 }
 
+__device__ __forceinline__ EncJob batch_job(const ecc_desc &d, uint64_t *flags, const uint64_t *prefix, uint32_t k)
+{
+    return EncJob{d.in, d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits, d.total_bits,
+                  flags + prefix[k], d.status};
+}
+
 __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws, uint64_t *t_start)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
-    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + enc_shared_bytes());
     BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
     const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
     const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
     uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
     uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
     const uint32_t stage_bytes = h->stage_bytes;
-    if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
+    const uint32_t cmax = h->max_C;
+    uint8_t *inbuf = smem + enc_shared_bytes();
+    const uint32_t nbuf = h->nbuf;
+    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + (size_t)nbuf * cmax);
+    const int tid = threadIdx.x;
+    if (t_start && blockIdx.x == 0 && tid == 0)
         *t_start = globaltimer();
-    if (threadIdx.x == 0)
+    if (tid == 0) {
         sh.loaded = nullptr;
+        mbar_init(&sh.bar[0], 1);
+        mbar_init(&sh.bar[1], 1);
+        fence_mbar_init();
+    }
     uint4 *st4 = reinterpret_cast<uint4 *>(stage);
-    for (uint32_t i = threadIdx.x; i < stage_bytes / 16; i += kEncThreads)
+    for (uint32_t i = tid; i < stage_bytes / 16; i += kEncThreads)
         st4[i] = make_uint4(0, 0, 0, 0);
-    for (;;) {
-        if (threadIdx.x == 0)
-            sh.ticket = atomicAdd(&h->ticket, 1u);
-        __syncthreads();
-        const uint64_t t = sh.ticket;
-        if (t >= h->total_chunks)
-            break;
+    // thread 0 claims chunks one ahead and bulk-copies their input
+    uint32_t pending = 0;
+    auto claim = [&](uint32_t buf) {
+        const uint32_t t = atomicAdd(&h->ticket, 1u);
+        sh.ticket = t;
+        if (t < h->total_chunks) {
+            const uint32_t k = find_tensor(prefix, h->count, t);
+            const ecc_desc &d = descs[k];
+            issue_chunk_input(batch_job(d, flags, prefix, k), t - prefix[k], inbuf + (size_t)buf * cmax,
+                              &sh.bar[buf]);
+            pending |= 1u << buf;
+        }
+    };
+    if (tid == 0)
+        claim(0);
+    __syncthreads();
+    uint64_t t = sh.ticket;
+    uint32_t b = 0, phase = 0;
+    bool staging = true;
+    while (t < h->total_chunks) {
+        __syncthreads(); // every thread has read sh.ticket and sh.loaded
+        if (tid == 0) {
+            if (staging && nbuf == 2)
+                claim(b ^ 1);
+            else if (!staging)
+                sh.ticket = atomicAdd(&h->ticket, 1u);
+        }
         const uint32_t k = find_tensor(prefix, h->count, t);
         const ecc_desc d = descs[k];
         const uint64_t c = t - prefix[k];
+        const EncJob job = batch_job(d, flags, prefix, k);
         const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
         if (cb_ok && d.cb != sh.loaded) {
             load_encode_lut(sh, d.cb);
             __syncthreads();
-            if (threadIdx.x == 0)
+            if (tid == 0)
                 sh.loaded = d.cb;
         }
-        EncJob job{d.in, d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits, d.total_bits,
-                   flags + prefix[k], d.status};
+        bool ok = staging && mbar_wait(&sh.bar[b], (phase >> b) & 1u, kWaitLimitNs);
+        ok = __syncthreads_and(ok) != 0;
+        if (ok) {
+            phase ^= 1u << b;
+            if (tid == 0)
+                pending &= ~(1u << b);
+        } else {
+            if (staging && tid == 0)
+                set_status(d.status, ECC_ERR_TIMEOUT);
+            staging = false;
+        }
         if (cb_ok) {
-            encode_chunk(sh, stage, stage_bytes, job, c, kWaitLimitNs);
-        } else if (threadIdx.x < 32) {
+            if (ok)
+                encode_chunk<true>(sh, stage, stage_bytes, job, inbuf + (size_t)b * cmax, c, kWaitLimitNs);
+            else
+                encode_chunk<false>(sh, stage, stage_bytes, job, nullptr, c, kWaitLimitNs);
+        } else if (tid < 32) {
             // keep the tensor's look-back moving; its status says why it is empty
             bool to;
             const uint64_t pre = lookback(job.flags, c, 0, kWaitLimitNs, &to);
-            if (threadIdx.x == 0) {
+            if (tid == 0) {
                 set_status(d.status, ECC_ERR_CODEBOOK);
                 d.chunk_off[c + 1] = pre;
             }
         }
-        if (threadIdx.x == 0)
+        if (tid == 0) {
             stamp_done(d, done, k, (d.n + d.C - 1) / d.C, 1);
+            if (staging && nbuf == 1)
+                claim(0); // the single buffer is free again
+        }
         __syncthreads();
+        t = sh.ticket;
+        if (nbuf == 2)
+            b ^= 1;
     }
+    if (tid == 0)
+        for (uint32_t q = 0; q < 2; ++q)
+            if (pending & (1u << q))
+                (void)mbar_wait(&sh.bar[q], (phase >> q) & 1u, kWaitLimitNs);
 }
 
 __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
+    LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes);
     __shared__ const ecc_codebook *loaded;
     __shared__ uint32_t ticket;
     BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
@@ -159,12 +220,16 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
     const uint32_t stage_bytes = h->stage_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t warps = h->warps;
-    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + sizeof(((ecc_codebook *)0)->dec) +
-                                                   (size_t)warp * stage_bytes);
     if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
         *t_start = globaltimer();
     if (threadIdx.x == 0)
         loaded = nullptr;
+    if (lane == 0) {
+        mbar_init(&bars[warp], 1);
+        fence_mbar_init();
+    }
+    WarpStage wst{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * stage_bytes), stage_bytes,
+                  &bars[warp], 0};
     for (;;) {
         if (threadIdx.x == 0)
             ticket = atomicAdd(&h->ticket, 1u);
@@ -180,8 +245,9 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
         if (cb_ok && d.cb != loaded) {
             const uint4 *src = reinterpret_cast<const uint4 *>(d.cb->dec);
             uint4 *dst = reinterpret_cast<uint4 *>(dec);
-            for (int i = threadIdx.x; i < (int)(sizeof(d.cb->dec) / 16); i += blockDim.x)
+            for (int i = threadIdx.x; i < (int)(kDecTableBytes / 16); i += blockDim.x)
                 dst[i] = src[i];
+            load_long_table(lt, d.cb);
             __syncthreads();
             if (threadIdx.x == 0)
                 loaded = d.cb;
@@ -190,9 +256,9 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
             if (cb_ok) {
                 DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
                 if (d.C / d.S >= 64)
-                    decode_chunk<2>(job, dec, stage, stage_bytes, c);
+                    decode_chunk<2>(job, dec, lt, wst, c, c + warps, n_chunks);
                 else
-                    decode_chunk<1>(job, dec, stage, stage_bytes, c);
+                    decode_chunk<1>(job, dec, lt, wst, c, c + warps, n_chunks);
             } else if (lane == 0) {
                 set_status(d.status, ECC_ERR_CODEBOOK);
             }
@@ -231,13 +297,6 @@ ecc_status check_descs(const ecc_desc *descs, uint32_t count, bool encode, uint6
     return ECC_OK;
 }
 
-int decode_warps(uint32_t stage_bytes)
-{
-    const size_t table = sizeof(((ecc_codebook *)0)->dec);
-    int w = (int)std::min<size_t>(kDecMaxWarps, (kMaxDynSmem - kStaticSmemReserve - table) / stage_bytes);
-    return std::max(w, 1);
-}
-
 ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes, uint64_t *t_start,
                        void *stream, bool encode)
 {
@@ -258,6 +317,8 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     h->count = count;
     h->warps = (uint32_t)warps;
     h->stage_bytes = stage;
+    h->max_C = max_C;
+    h->nbuf = enc_input_buffers(max_C);
     h->total_chunks = total_chunks;
     h->desc_off = L.desc_off;
     h->prefix_off = L.prefix_off;
@@ -289,14 +350,14 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     if (acc == 0)
         return ECC_OK;
     if (encode) {
-        const size_t smem = enc_shared_bytes() + stage;
+        const size_t smem = enc_shared_bytes() + (size_t)h->nbuf * max_C + stage;
         const int occ = occupancy((const void *)encode_batched_kernel, kEncThreads, smem);
         if (occ <= 0)
             return ECC_ERR_CUDA;
         const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, acc);
         encode_batched_kernel<<<(unsigned)grid, kEncThreads, smem, st>>>((uint8_t *)ws, t_start);
     } else {
-        const size_t smem = sizeof(((ecc_codebook *)0)->dec) + (size_t)warps * stage;
+        const size_t smem = kDecHeadBytes + (size_t)warps * stage;
         const int occ = occupancy((const void *)decode_batched_kernel, warps * 32, smem);
         if (occ <= 0)
             return ECC_ERR_CUDA;

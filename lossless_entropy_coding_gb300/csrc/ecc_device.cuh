@@ -67,6 +67,69 @@ __device__ __forceinline__ void st_stream16(void *p, uint4 v)
 
 __device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
 
+// ---------------------------------------------------------------- bulk copies
+// One-instruction global -> shared copies through the bulk-copy (TMA) engine,
+// completion tracked by an mbarrier transaction count.  Sizes are multiples
+// of 16 bytes, addresses 16-byte aligned.
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// order this thread's earlier generic accesses to shared memory before later
+// bulk-copy writes to it
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false if limit_ns
+// passed first (the copy is then still in flight: wait again before the
+// buffer is reused or the CTA exits).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (globaltimer() - t0 > limit_ns)
+            return false;
+    }
+}
+
 // byte k (0..3) of x, zero-extended
 __device__ __forceinline__ uint32_t byte_of(uint32_t x, int k) { return __byte_perm(x, 0, 0x4440 | k); }
 
@@ -142,6 +205,7 @@ struct EncShared {
     uint32_t warp_tot[kEncWarps];
     uint32_t off[kEncThreads + 4];
     uint64_t prefix;
+    uint64_t bar[2];            // input-buffer mbarriers
     const ecc_codebook *loaded; // codebook currently in lut
     uint32_t ticket;
     uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
@@ -175,11 +239,18 @@ __device__ __forceinline__ void load_encode_lut(EncShared &sh, const ecc_codeboo
     }
 }
 
-// Load up to 16 input bytes (16-byte aligned when cnt == 16).
-__device__ __forceinline__ uint4 load_symbols(const uint8_t *src, uint32_t cnt)
+// Load up to 16 input bytes: a full group from the chunk source (shared
+// stage or global memory, 16-byte aligned), a partial one (the tensor's last
+// bytes) from global memory.
+template <bool kSharedSrc>
+__device__ __forceinline__ uint4 load_symbols(const uint8_t *chunk_src, const uint8_t *global_src, uint32_t cnt)
 {
-    if (cnt == kSymPerThread)
-        return ld_stream16(src);
+    if (cnt == kSymPerThread) {
+        if (kSharedSrc)
+            return *reinterpret_cast<const uint4 *>(chunk_src);
+        return ld_stream16(global_src);
+    }
+    const uint8_t *src = global_src;
     uint32_t w[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < kSymPerThread; ++i)
@@ -318,15 +389,15 @@ __device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], uint4 v
 // One tile pass over a chunk: lookups, block scan of bit counts, packing into
 // `sink` (chunk-relative bit offsets).  Writes sub_bits when write_sub.
 // Returns the tile's bit total (uniform across the CTA).
-template <bool kCheckRoom>
-__device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job, uint64_t base, uint32_t L, uint32_t t0,
-                                                uint32_t run, uint32_t *sink, uint32_t sink_bits, bool write_sub,
-                                                bool *bad_out)
+template <bool kCheckRoom, bool kSharedSrc>
+__device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job, const uint8_t *src, uint64_t base,
+                                                uint32_t L, uint32_t t0, uint32_t run, uint32_t *sink,
+                                                uint32_t sink_bits, bool write_sub, bool *bad_out)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t my0 = t0 + (uint32_t)tid * kSymPerThread;
     const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
-    const uint4 v = cnt ? load_symbols(job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
+    const uint4 v = cnt ? load_symbols<kSharedSrc>(src + my0, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
     uint32_t e[16];
     bool slow, bad;
     const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, &slow, &bad);
@@ -376,10 +447,13 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
     return tile_total;
 }
 
-// Encode chunk c of job into its place in job.out.  `stage` is a zeroed
-// shared-memory buffer of stage_bytes; it is zeroed again on return.
+// Encode chunk c of job into its place in job.out.  src holds the chunk's
+// input (its whole 16-byte groups) in shared memory when kSharedSrc, else
+// src is unused and the input is read from global memory.  `stage` is a
+// zeroed shared-memory buffer of stage_bytes; it is zeroed again on return.
+template <bool kSharedSrc>
 __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uint32_t stage_bytes, const EncJob &job,
-                                             uint64_t c, uint64_t timeout_ns)
+                                             const uint8_t *src, uint64_t c, uint64_t timeout_ns)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint64_t base = c * job.C;
@@ -391,7 +465,7 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
     bool bad = false;
     uint32_t run = 0;
     for (uint32_t t0 = 0; t0 < L; t0 += kTile)
-        run += encode_tile<true>(sh, job, base, L, t0, run, stage, stage_bytes * 8u, true, &bad);
+        run += encode_tile<true, kSharedSrc>(sh, job, src, base, L, t0, run, stage, stage_bytes * 8u, true, &bad);
     if (bad)
         set_status(job.status, ECC_ERR_CODEBOOK);
 
@@ -442,10 +516,24 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
             uint32_t run2 = 0;
             uint32_t *gsink = reinterpret_cast<uint32_t *>(job.out + prefix);
             for (uint32_t t0 = 0; t0 < L; t0 += kTile)
-                run2 += encode_tile<false>(sh, job, base, L, t0, run2, gsink, 0, false, &bad2);
+                run2 += encode_tile<false, kSharedSrc>(sh, job, src, base, L, t0, run2, gsink, 0, false, &bad2);
         }
     }
     __syncthreads();
+}
+
+// Bulk-copy the whole 16-byte groups of chunk c's input into buf (thread 0);
+// completion arrives on bar.  The last chunk's trailing bytes (fewer than
+// 16) are read from global memory by the thread that owns them.
+__device__ __forceinline__ void issue_chunk_input(const EncJob &job, uint64_t c, uint8_t *buf, uint64_t *bar)
+{
+    const uint64_t base = c * job.C;
+    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
+    const uint32_t whole = L & ~15u;
+    fence_proxy_async();
+    mbar_expect_tx(bar, whole);
+    if (whole)
+        bulk_g2s(buf, job.in + base, whole, bar);
 }
 
 // ---------------------------------------------------------------- decoder
@@ -466,23 +554,73 @@ struct DecJob {
     uint32_t *status;
 };
 
-// Resolve a code longer than the first-level table from the canonical
-// per-length ranges.  win holds the next 64 stream bits, MSB first.  Returns
-// byte | len << 8, or 0 for a code the codebook lacks.
-static __device__ __noinline__ uint32_t decode_long(uint64_t win, const ecc_codebook *cb)
+// Canonical ranges of the codes longer than the first-level table, staged in
+// shared memory for the decoder's slow path.  For a length L the L-bit
+// prefix v of the stream is a code of length L exactly when v < first[L] +
+// count[L] and no shorter length matched; the test is monotone in L, so the
+// code length is the number of lengths that fail plus the first length tried.
+struct LongTable {
+    uint64_t lim32[33];    // (first[L] + count[L]) << (32 - L), L <= 32
+    uint64_t first[ECC_MAX_CODE_LEN + 1];
+    uint16_t index[ECC_MAX_CODE_LEN + 1];
+    uint16_t count[ECC_MAX_CODE_LEN + 1];
+    uint8_t sorted[256];
+    uint32_t max_len;
+    uint32_t family;
+};
+
+__device__ __forceinline__ void load_long_table(LongTable &lt, const ecc_codebook *cb)
 {
-    if (cb->family != ECC_FAMILY_HUFFMAN)
-        return 0;
+    const int t = threadIdx.x;
     const uint32_t maxl = min(cb->max_len, (uint32_t)ECC_MAX_CODE_LEN);
-    for (uint32_t L = ECC_PEEK_BITS + 1; L <= maxl; ++L) {
-        const uint32_t k = cb->count[L];
+    for (int L = t; L <= ECC_MAX_CODE_LEN; L += blockDim.x) {
+        const uint64_t f = cb->first[L];
+        const uint32_t k = (uint32_t)L <= maxl ? cb->count[L] : 0u;
+        lt.first[L] = f;
+        lt.index[L] = cb->index[L];
+        lt.count[L] = (uint16_t)k;
+        if (L <= 32)
+            lt.lim32[L] = L == 0 ? 0ull : (f + k) << (32 - L);
+    }
+    for (int i = t; i < 256; i += blockDim.x)
+        lt.sorted[i] = cb->sorted[i];
+    if (t == 0) {
+        lt.max_len = maxl;
+        lt.family = cb->family;
+    }
+}
+
+// Resolve a code longer than the first-level table.  p32 holds the next 32
+// stream bits and win the next 64, MSB first.  Returns byte | len << 8, or 0
+// for a code the codebook lacks.
+static __device__ __noinline__ uint32_t decode_long(uint32_t p32, uint64_t win, const LongTable &lt)
+{
+    if (lt.family != ECC_FAMILY_HUFFMAN)
+        return 0;
+    const uint32_t maxl = lt.max_len;
+    uint32_t L = ECC_PEEK_BITS + 1;
+    if (maxl <= 32) {
+        // count the lengths in (12, maxl) whose range lies below the window
+#pragma unroll
+        for (uint32_t j = ECC_PEEK_BITS + 1; j < 32; ++j)
+            L += (j < maxl) & ((uint64_t)p32 >= lt.lim32[j]);
+        if (L > maxl)
+            return 0;
+        const uint32_t v = p32 >> (32 - L);
+        const uint64_t d = (uint64_t)v - lt.first[L];
+        if (d >= lt.count[L])
+            return 0;
+        const uint32_t at = lt.index[L] + (uint32_t)d;
+        return at < 256 ? (uint32_t)lt.sorted[at] | (L << 8) : 0u;
+    }
+    for (; L <= maxl; ++L) {
+        const uint32_t k = lt.count[L];
         if (!k)
             continue;
-        const uint64_t v = win >> (64 - L);
-        const uint64_t d = v - cb->first[L];
+        const uint64_t d = (win >> (64 - L)) - lt.first[L];
         if (d < k) {
-            const uint32_t at = cb->index[L] + (uint32_t)d;
-            return at < 256 ? (uint32_t)cb->sorted[at] | (L << 8) : 0u;
+            const uint32_t at = lt.index[L] + (uint32_t)d;
+            return at < 256 ? (uint32_t)lt.sorted[at] | (L << 8) : 0u;
         }
     }
     return 0;
@@ -535,13 +673,14 @@ struct Reader {
 
 // Decode one symbol; returns the byte, advances the reader, flags bad codes.
 template <bool kShared>
-__device__ __forceinline__ uint32_t decode_symbol(Reader<kShared> &r, const uint16_t *dec, const ecc_codebook *cb,
+__device__ __forceinline__ uint32_t decode_symbol(Reader<kShared> &r, const uint16_t *dec, const LongTable &lt,
                                                   bool &bad)
 {
-    const uint32_t e0 = dec[r.peek32() >> (32 - ECC_PEEK_BITS)];
+    const uint32_t p = r.peek32();
+    const uint32_t e0 = dec[p >> (32 - ECC_PEEK_BITS)];
     uint32_t e = e0;
     if (e0 == 0) {
-        e = decode_long(r.window64(), cb);
+        e = decode_long(p, r.window64(), lt);
         if (e == 0) {
             bad = true;
             e = 1u << 8; // consume one bit to keep going (output is flagged)
@@ -558,7 +697,8 @@ __device__ __forceinline__ uint32_t decode_symbol(Reader<kShared> &r, const uint
 
 // Decode the R sub-blocks a lane owns in one group of a chunk.
 template <int R, bool kShared>
-__device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *dec, const uint32_t *words,
+__device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *dec, const LongTable &lt,
+                                             const uint32_t *words,
                                              uint32_t wlast, uint64_t base, uint32_t L, uint32_t g0,
                                              const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
 {
@@ -594,7 +734,7 @@ __device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *
                 for (int t = 0; t < 4; ++t)
 #pragma unroll
                     for (int r = 0; r < R; ++r)
-                        w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, job.cb, bad), 0x4321);
+                        w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, lt, bad), 0x4321);
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -603,7 +743,7 @@ __device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *
 #pragma unroll
                     for (int r = 0; r < R; ++r)
                         if (i + q * 4 + t < cnt[r])
-                            w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, job.cb, bad), 0x4321);
+                            w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, lt, bad), 0x4321);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -635,45 +775,80 @@ __device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *
             bad = true;
 }
 
-// Decode chunk c with one warp.  stage: this warp's shared buffer of
-// stage_bytes (NULL: read the payload from global memory).
+constexpr uint32_t kDecTableBytes = sizeof(((ecc_codebook *)0)->dec);
+constexpr uint32_t kLongTableBytes = (sizeof(LongTable) + 15u) & ~15u;
+constexpr uint32_t kDecBarSlots = 16; // one mbarrier per warp
+constexpr uint32_t kDecHeadBytes = kDecTableBytes + kLongTableBytes + kDecBarSlots * 8;
+
+// Per-warp staging state: the chunk buffer, its mbarrier and phase.
+struct WarpStage {
+    uint32_t *buf;
+    uint32_t bytes; // capacity
+    uint64_t *bar;
+    uint32_t phase;
+};
+
+__device__ __forceinline__ bool chunk_range_ok(const DecJob &job, uint64_t c, uint64_t &b0, uint64_t &b1)
+{
+    b0 = job.chunk_off[c];
+    b1 = job.chunk_off[c + 1];
+    return b1 > b0 && b1 <= job.in_bytes && !((b0 | b1) & 15) && (b1 - b0) <= (uint64_t)job.C * 8;
+}
+
+// Decode chunk c with one warp.  The compressed chunk is staged into the
+// warp's shared buffer by one bulk copy (when it fits), while the lanes scan
+// sub_bits; next_c (if valid) is prefetched into L2 for the warp's next call.
 template <int R>
-__device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *dec, uint32_t *stage,
-                                             uint32_t stage_bytes, uint64_t c)
+__device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *dec, const LongTable &lt,
+                                             WarpStage &ws, uint64_t c, uint64_t next_c, uint64_t n_chunks)
 {
     const int lane = threadIdx.x & 31;
-    const uint64_t b0 = job.chunk_off[c], b1 = job.chunk_off[c + 1];
     const uint64_t base = c * job.C;
     const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
     const uint32_t nsub = (L + job.S - 1) / job.S;
     const uint64_t sub0 = base / job.S;
-    if (b1 < b0 || b1 > job.in_bytes || ((b0 | b1) & 15) || (b1 - b0) > (uint64_t)job.C * 8) {
+    uint64_t b0, b1;
+    if (!chunk_range_ok(job, c, b0, b1)) {
         if (lane == 0)
             set_status(job.status, ECC_ERR_CORRUPT);
         return;
     }
     const uint32_t bytes = (uint32_t)(b1 - b0);
-    if (bytes == 0) { // every chunk holds at least one code bit
-        if (lane == 0)
-            set_status(job.status, ECC_ERR_CORRUPT);
-        return;
+    const bool staged = ws.buf != nullptr && bytes + 16 <= ws.bytes;
+    if (staged) {
+        __syncwarp();
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_expect_tx(ws.bar, bytes);
+            bulk_g2s(ws.buf, job.in + b0, bytes, ws.bar);
+        }
     }
-    const bool staged = stage != nullptr && bytes + 16 <= stage_bytes;
+    if (lane == 0 && next_c < n_chunks) {
+        uint64_t n0, n1;
+        if (chunk_range_ok(job, next_c, n0, n1))
+            prefetch_l2(job.in + n0, (uint32_t)(n1 - n0));
+    }
     const uint32_t *words;
     uint32_t wlast;
     if (staged) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(job.in + b0);
-        uint4 *dst = reinterpret_cast<uint4 *>(stage);
-        for (uint32_t i = lane; i < bytes / 16; i += 32)
-            dst[i] = ld_stream16(src + i);
-        if (lane == 0)
-            dst[bytes / 16] = make_uint4(0, 0, 0, 0); // guard: peeks past the end read 0
+        bool ok = __all_sync(~0u, mbar_wait(ws.bar, ws.phase, kWaitLimitNs));
+        if (!ok) // never expected: the copy reads valid memory; wait once more
+            ok = __all_sync(~0u, mbar_wait(ws.bar, ws.phase, kWaitLimitNs));
+        ws.phase ^= 1;
+        if (!ok) {
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            ws.buf = nullptr; // the copy may still land: stop using this buffer
+            return;
+        }
+        if (lane < 4)
+            ws.buf[bytes / 4 + lane] = 0; // guard: peeks past the end read 0
         __syncwarp();
-        words = stage;
+        words = ws.buf;
         wlast = bytes / 4 + 3;
     } else {
         words = reinterpret_cast<const uint32_t *>(job.in + b0);
-        wlast = bytes / 4 ? bytes / 4 - 1 : 0;
+        wlast = bytes / 4 - 1;
     }
 
     bool bad = false;
@@ -696,9 +871,9 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
             carry += __shfl_sync(~0u, incl, 31);
         }
         if (staged)
-            decode_group<R, true>(job, dec, words, wlast, base, L, g0, st, nb, bad);
+            decode_group<R, true>(job, dec, lt, words, wlast, base, L, g0, st, nb, bad);
         else
-            decode_group<R, false>(job, dec, words, wlast, base, L, g0, st, nb, bad);
+            decode_group<R, false>(job, dec, lt, words, wlast, base, L, g0, st, nb, bad);
     }
     if (pad16((carry + 7) / 8) != bytes)
         bad = true;

@@ -64,6 +64,7 @@ struct EncParams {
     uint64_t n_chunks;
     uint32_t *ticket;
     uint32_t stage_bytes;
+    uint32_t nbuf; // shared input buffers of C bytes: 2 = next chunk prefetched
     uint64_t timeout_ns;
 };
 
@@ -83,30 +84,82 @@ __global__ void enc_prologue_kernel(uint64_t *flags, uint64_t n_flags, uint32_t 
 }
 
 // Persistent CTAs take chunks in ticket order, so a chunk's predecessors have
-// always been claimed by running CTAs when it looks back.
+// always been claimed by running CTAs when it looks back.  Each CTA claims
+// its next chunk one chunk ahead and bulk-copies that chunk's input into the
+// second shared buffer while it encodes the current one.
 __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
-    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + enc_shared_bytes());
+    uint8_t *inbuf = smem + enc_shared_bytes();
+    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + (size_t)p.nbuf * p.job.C);
+    const int tid = threadIdx.x;
     if (p.job.cb->magic != ECC_CODEBOOK_MAGIC || p.job.cb->max_len > ECC_MAX_CODE_LEN) {
-        if (threadIdx.x == 0 && blockIdx.x == 0)
+        if (tid == 0 && blockIdx.x == 0)
             set_status(p.job.status, ECC_ERR_CODEBOOK);
         return;
     }
+    if (tid == 0) {
+        mbar_init(&sh.bar[0], 1);
+        mbar_init(&sh.bar[1], 1);
+        fence_mbar_init();
+    }
     load_encode_lut(sh, p.job.cb);
     uint4 *st4 = reinterpret_cast<uint4 *>(stage);
-    for (uint32_t i = threadIdx.x; i < p.stage_bytes / 16; i += kEncThreads)
+    for (uint32_t i = tid; i < p.stage_bytes / 16; i += kEncThreads)
         st4[i] = make_uint4(0, 0, 0, 0);
-    for (;;) {
-        if (threadIdx.x == 0)
-            sh.ticket = atomicAdd(p.ticket, 1u);
-        __syncthreads();
-        const uint64_t c = sh.ticket;
-        if (c >= p.n_chunks)
-            break;
-        encode_chunk(sh, stage, p.stage_bytes, p.job, c, p.timeout_ns);
+    uint32_t pending = 0; // thread 0: buffers with a copy not yet waited for
+    if (tid == 0) {
+        const uint32_t t = atomicAdd(p.ticket, 1u);
+        sh.ticket = t;
+        if (t < p.n_chunks) {
+            issue_chunk_input(p.job, t, inbuf, &sh.bar[0]);
+            pending = 1;
+        }
     }
+    __syncthreads();
+    uint64_t c = sh.ticket;
+    uint32_t b = 0, phase = 0;
+    bool staging = true;
+    while (c < p.n_chunks) {
+        __syncthreads(); // every thread has read sh.ticket
+        if (tid == 0) {
+            const uint32_t t = atomicAdd(p.ticket, 1u);
+            sh.ticket = t;
+            if (t < p.n_chunks && p.nbuf == 2 && staging) {
+                issue_chunk_input(p.job, t, inbuf + (size_t)(b ^ 1) * p.job.C, &sh.bar[b ^ 1]);
+                pending |= 1u << (b ^ 1);
+            }
+        }
+        bool ok = staging && mbar_wait(&sh.bar[b], (phase >> b) & 1u, p.timeout_ns);
+        ok = __syncthreads_and(ok) != 0;
+        if (ok) {
+            phase ^= 1u << b;
+            if (tid == 0)
+                pending &= ~(1u << b);
+            encode_chunk<true>(sh, stage, p.stage_bytes, p.job, inbuf + (size_t)b * p.job.C, c, p.timeout_ns);
+        } else {
+            // the copy did not arrive in time: report it, stop staging, and
+            // read this and later chunks from global memory
+            if (staging && tid == 0)
+                set_status(p.job.status, ECC_ERR_TIMEOUT);
+            staging = false;
+            encode_chunk<false>(sh, stage, p.stage_bytes, p.job, nullptr, c, p.timeout_ns);
+        }
+        const uint64_t nc = sh.ticket;
+        if (p.nbuf == 1 && staging && tid == 0 && nc < p.n_chunks) {
+            issue_chunk_input(p.job, nc, inbuf, &sh.bar[0]);
+            pending |= 1u;
+        }
+        if (p.nbuf == 2)
+            b ^= 1;
+        c = nc;
+    }
+    // never exit with a bulk copy still writing into this CTA's shared memory
+    if (tid == 0)
+        for (uint32_t k = 0; k < 2; ++k)
+            if (pending & (1u << k))
+                (void)mbar_wait(&sh.bar[k], (phase >> k) & 1u, p.timeout_ns);
 }
 
 // ---------------------------------------------------------------- decode
@@ -121,7 +174,9 @@ __global__ void decode_kernel(DecParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
-    const int warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
+    LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = blockDim.x >> 5;
     if (p.job.cb->magic != ECC_CODEBOOK_MAGIC || p.job.cb->max_len > ECC_MAX_CODE_LEN) {
         if (threadIdx.x == 0 && blockIdx.x == 0)
             set_status(p.job.status, ECC_ERR_CODEBOOK);
@@ -130,14 +185,20 @@ __global__ void decode_kernel(DecParams p)
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(p.job.cb->dec);
         uint4 *dst = reinterpret_cast<uint4 *>(dec);
-        for (int i = threadIdx.x; i < (int)(sizeof(p.job.cb->dec) / 16); i += blockDim.x)
+        for (int i = threadIdx.x; i < (int)(kDecTableBytes / 16); i += blockDim.x)
             dst[i] = src[i];
     }
+    load_long_table(lt, p.job.cb);
+    if (lane == 0) {
+        mbar_init(&bars[warp], 1);
+        fence_mbar_init();
+    }
     __syncthreads();
-    uint32_t *stage = reinterpret_cast<uint32_t *>(smem + sizeof(((ecc_codebook *)0)->dec) +
-                                                   (size_t)warp * p.stage_bytes);
-    for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += (uint64_t)gridDim.x * warps)
-        decode_chunk<R>(p.job, dec, stage, p.stage_bytes, c);
+    WarpStage ws{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * p.stage_bytes), p.stage_bytes,
+                 &bars[warp], 0};
+    const uint64_t stride = (uint64_t)gridDim.x * warps;
+    for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += stride)
+        decode_chunk<R>(p.job, dec, lt, ws, c, c + stride, p.n_chunks);
 }
 
 // ---------------------------------------------------------------- self-test
@@ -184,6 +245,20 @@ bool pow2_in(uint64_t v, uint64_t lo, uint64_t hi) { return v >= lo && v <= hi &
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 bool valid_sizes(uint32_t C, uint32_t S) { return pow2_in(C, 1024, 65536) && pow2_in(S, 64, 1024) && S <= C; }
+
+uint32_t enc_input_buffers(uint32_t C)
+{
+    // two CTAs per SM must fit: LUT + two input buffers + output staging
+    const size_t two = enc_shared_bytes() + 2 * (size_t)C + stage_bytes_for(C);
+    return two <= kMaxDynSmem / 2 - kStaticSmemReserve ? 2u : 1u;
+}
+
+int decode_warps(uint32_t stage_bytes)
+{
+    const size_t room = kMaxDynSmem - kStaticSmemReserve - kDecHeadBytes;
+    const int w = (int)std::min<size_t>(kDecMaxWarps, room / stage_bytes);
+    return std::max(w, 1);
+}
 
 ecc_status launch_status(cudaError_t e)
 {
@@ -281,8 +356,9 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     p.n_chunks = n_chunks;
     p.ticket = ticket;
     p.stage_bytes = stage_bytes_for(C);
+    p.nbuf = enc_input_buffers(C);
     p.timeout_ns = kWaitLimitNs;
-    const size_t smem = enc_shared_bytes() + p.stage_bytes;
+    const size_t smem = enc_shared_bytes() + (size_t)p.nbuf * C + p.stage_bytes;
     const int occ = occupancy((const void *)encode_kernel, kEncThreads, smem);
     const int sms = sm_count();
     if (occ <= 0 || sms <= 0)
@@ -309,10 +385,8 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
     p.job = DecJob{in, in_bytes, chunk_off, sub_bits, n, C, S, cb, out, status};
     p.n_chunks = ecc_num_chunks(n, C);
     p.stage_bytes = stage_bytes_for(C);
-    const size_t table = sizeof(((ecc_codebook *)0)->dec);
-    int warps = (int)std::min<size_t>(kDecMaxWarps, (kMaxDynSmem - table) / p.stage_bytes);
-    warps = std::max(warps, 1);
-    const size_t smem = table + (size_t)warps * p.stage_bytes;
+    const int warps = decode_warps(p.stage_bytes);
+    const size_t smem = kDecHeadBytes + (size_t)warps * p.stage_bytes;
     const bool two = C / S >= 64;
     const void *kfn = two ? (const void *)decode_kernel<2> : (const void *)decode_kernel<1>;
     const int occ = occupancy(kfn, warps * 32, smem);

@@ -15,6 +15,10 @@ constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may a
 constexpr int kDecMaxWarps = 8;
 
 bool valid_sizes(uint32_t C, uint32_t S);
+// shared input buffers of the encoder (2 = the next chunk is prefetched)
+uint32_t enc_input_buffers(uint32_t C);
+// warps of a decoder CTA whose per-warp staging buffers hold stage_bytes
+int decode_warps(uint32_t stage_bytes);
 bool aligned16(const void *p);
 ecc_status launch_status(cudaError_t e);
 int sm_count();
