@@ -202,8 +202,7 @@ __device__ __forceinline__ uint64_t lookback(uint64_t *flags, uint64_t c, uint64
 // a warp always hit 32 different banks whatever bytes they look up.
 struct EncShared {
     uint32_t lut[kLutRows * 32];
-    uint32_t warp_tot[kEncWarps];
-    uint32_t off[kEncThreads + 4];
+    uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
     uint64_t prefix;
     uint64_t bar[2];            // input-buffer mbarriers
     const ecc_codebook *loaded; // codebook currently in lut
@@ -260,42 +259,41 @@ __device__ __forceinline__ uint4 load_symbols(const uint8_t *chunk_src, const ui
 }
 
 // Packing sink: 32-bit words in memory byte order (MSB-first bitstream).
-// Words shared with a neighbouring thread are merged with atomicOr into a
-// zeroed destination; words a thread owns alone are stored.
+// A thread's first word may also hold its predecessor's last bits and its
+// last word its successor's first bits: those two are merged with atomicOr
+// into a zeroed destination, the words in between are stored.  The first
+// completed word is kept in a register until the end, so the append itself
+// has no branch.
 struct Packer {
     uint32_t *dst;
-    uint32_t wi;     // index of the word being filled
-    uint32_t nb;     // pending bits in acc (low bits)
-    bool first;      // the word at wi may hold a predecessor's bits
+    uint32_t wi0, wi; // first word, word being filled
+    uint32_t nb;      // pending bits in acc (low bits)
+    uint32_t ne;      // words completed so far
+    uint32_t fw;      // the first completed word
     uint64_t acc;
 
     __device__ __forceinline__ void start(uint32_t *d, uint32_t bitpos)
     {
         dst = d;
-        wi = bitpos >> 5;
-        nb = bitpos & 31;   // the predecessor's bits count as zeros here
-        first = nb != 0;
+        wi0 = wi = bitpos >> 5;
+        nb = bitpos & 31; // the predecessor's bits count as zeros here
+        ne = 0;
+        fw = 0;
         acc = 0;
-    }
-    __device__ __forceinline__ void emit_if_full()
-    {
-        if (nb >= 32) {
-            nb -= 32;
-            const uint32_t w = bswap32((uint32_t)(acc >> nb));
-            if (first)
-                atomicOr(dst + wi, w);
-            else
-                dst[wi] = w;
-            first = false;
-            ++wi;
-        }
     }
     // append up to 32 bits (len <= 32, nb < 32 on entry)
     __device__ __forceinline__ void put(uint32_t code, uint32_t len)
     {
         acc = (acc << len) | code;
         nb += len;
-        emit_if_full();
+        const bool full = nb >= 32;
+        nb -= full ? 32u : 0u;
+        const uint32_t w = bswap32((uint32_t)(acc >> nb));
+        if (full && ne != 0)
+            dst[wi] = w;
+        fw = (full && ne == 0) ? w : fw;
+        wi += full ? 1u : 0u;
+        ne += full ? 1u : 0u;
     }
     // append up to 48 bits
     __device__ __forceinline__ void put_long(uint64_t code, uint32_t len)
@@ -309,6 +307,8 @@ struct Packer {
     }
     __device__ __forceinline__ void finish()
     {
+        if (ne != 0)
+            atomicOr(dst + wi0, fw);
         if (nb)
             atomicOr(dst + wi, bswap32((uint32_t)(acc << (32 - nb))));
     }
@@ -395,6 +395,7 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
                                                 uint32_t sink_bits, bool write_sub, bool *bad_out)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t parity = (t0 / kTile) & 1;
     const uint32_t my0 = t0 + (uint32_t)tid * kSymPerThread;
     const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
     const uint4 v = cnt ? load_symbols<kSharedSrc>(src + my0, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
@@ -411,20 +412,27 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
             incl += y;
     }
     if (lane == 31)
-        sh.warp_tot[warp] = incl;
+        sh.warp_tot[parity][warp] = incl;
     __syncthreads();
     uint32_t before = 0, tile_total = 0;
 #pragma unroll
     for (int w = 0; w < kEncWarps; ++w) {
-        const uint32_t t = sh.warp_tot[w];
+        const uint32_t t = sh.warp_tot[parity][w];
         before += w < warp ? t : 0u;
         tile_total += t;
     }
     const uint32_t excl = before + incl - bits;
     if (write_sub) {
-        sh.off[tid] = excl;
-        if (tid == 0)
-            sh.off[kEncThreads] = tile_total;
+        // bits of each sub-block of S symbols = S/16 consecutive threads
+        const uint32_t tps = job.S / kSymPerThread;
+        uint32_t sb;
+        if (tps <= 32) {
+            sb = __shfl_sync(~0u, incl, lane | (int)(tps - 1)) - (incl - bits);
+        } else { // S = 1024: two whole warps
+            sb = sh.warp_tot[parity][warp] + sh.warp_tot[parity][warp | 1];
+        }
+        if (cnt && ((uint32_t)tid % tps) == 0)
+            job.sub_bits[(base + my0) / job.S] = (uint16_t)sb;
     }
     const uint32_t pos = run + excl;
     if (cnt) {
@@ -434,14 +442,6 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
             pack16(pk, e, v, cnt, slow, job.cb);
         } else {
             atomicOr(&sh.flags, 1u);
-        }
-    }
-    __syncthreads();
-    if (write_sub && cnt) {
-        const uint32_t tps = job.S / kSymPerThread;
-        if ((uint32_t)tid % tps == 0) {
-            const uint32_t end = min((uint32_t)tid + tps, (uint32_t)kEncThreads);
-            job.sub_bits[(base + my0) / job.S] = (uint16_t)(sh.off[end] - sh.off[tid]);
         }
     }
     return tile_total;
@@ -626,153 +626,142 @@ static __device__ __noinline__ uint32_t decode_long(uint32_t p32, uint64_t win, 
     return 0;
 }
 
-// Bit reader over 32-bit words in memory byte order.  (hi, lo) are the two
-// words at wp-2, wp-1; o is the bit offset into hi.
-template <bool kShared>
-struct Reader {
-    const uint32_t *words;
-    uint32_t wlast; // last readable word index
-    uint32_t wp;
-    uint32_t hi, lo, o;
-
-    __device__ __forceinline__ uint32_t word(uint32_t i) const
-    {
-        const uint32_t k = min(i, wlast);
-        if (kShared)
-            return bswap32(words[k]);
-        return bswap32(__ldg(words + k));
-    }
-    __device__ __forceinline__ void start(const uint32_t *w, uint32_t last, uint32_t bit)
-    {
-        words = w;
-        wlast = last;
-        const uint32_t w0 = bit >> 5;
-        o = bit & 31;
-        hi = word(w0);
-        lo = word(w0 + 1);
-        wp = w0 + 2;
-    }
-    __device__ __forceinline__ uint32_t peek32() const { return __funnelshift_l(lo, hi, o); }
-    __device__ __forceinline__ uint32_t position() const { return (wp - 2) * 32 + o; }
-    __device__ __forceinline__ void refill()
-    {
-        if (o >= 32) {
-            hi = lo;
-            lo = word(wp);
-            ++wp;
-            o -= 32;
-        }
-    }
-    __device__ __forceinline__ uint64_t window64() const
-    {
-        const uint64_t two = ((uint64_t)hi << 32) | lo;
-        const uint64_t w3 = word(wp);
-        return o ? (two << o) | (w3 >> (32 - o)) : two;
-    }
+// Bit stream of one sub-block, read from 32-bit words in memory byte order
+// through a sliding window: (hi, lo) are words wp-3 and wp-2, nx (word wp-1)
+// is already loaded, o is the bit offset into hi.  Word reads are clamped to
+// [0, wlast], so a corrupt stream can never read outside its chunk.
+struct Stream {
+    uint32_t hi, lo, nx, o, wp;
 };
 
-// Decode one symbol; returns the byte, advances the reader, flags bad codes.
 template <bool kShared>
-__device__ __forceinline__ uint32_t decode_symbol(Reader<kShared> &r, const uint16_t *dec, const LongTable &lt,
-                                                  bool &bad)
+__device__ __forceinline__ uint32_t load_word(const uint32_t *words, uint32_t i, uint32_t wlast)
 {
-    const uint32_t p = r.peek32();
-    const uint32_t e0 = dec[p >> (32 - ECC_PEEK_BITS)];
-    uint32_t e = e0;
-    if (e0 == 0) {
-        e = decode_long(p, r.window64(), lt);
-        if (e == 0) {
-            bad = true;
-            e = 1u << 8; // consume one bit to keep going (output is flagged)
-        }
-        r.o += e >> 8;
-        while (r.o >= 32)
-            r.refill();
-        return e & 0xFF;
-    }
-    r.o += e >> 8;
-    r.refill();
-    return e & 0xFF;
+    const uint32_t k = min(i, wlast);
+    return bswap32(kShared ? words[k] : __ldg(words + k));
 }
 
-// Decode the R sub-blocks a lane owns in one group of a chunk.
-template <int R, bool kShared>
-__device__ __forceinline__ void decode_group(const DecJob &job, const uint16_t *dec, const LongTable &lt,
-                                             const uint32_t *words,
-                                             uint32_t wlast, uint64_t base, uint32_t L, uint32_t g0,
-                                             const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
+template <bool kShared>
+__device__ __forceinline__ void stream_start(Stream &s, const uint32_t *words, uint32_t wlast, uint32_t bit)
+{
+    const uint32_t w0 = bit >> 5;
+    s.o = bit & 31;
+    s.hi = load_word<kShared>(words, w0, wlast);
+    s.lo = load_word<kShared>(words, w0 + 1, wlast);
+    s.nx = load_word<kShared>(words, w0 + 2, wlast);
+    s.wp = w0 + 3;
+}
+
+__device__ __forceinline__ uint32_t stream_pos(const Stream &s) { return (s.wp - 3) * 32 + s.o; }
+
+// Long or invalid code at the window (hi:lo:nx << o): byte | len << 8, or 0.
+static __device__ __noinline__ uint32_t decode_long_at(uint32_t hi, uint32_t lo, uint32_t nx, uint32_t o,
+                                                       const LongTable &lt)
+{
+    const uint64_t two = ((uint64_t)hi << 32) | lo;
+    const uint64_t win = o ? (two << o) | ((uint64_t)nx >> (32 - o)) : two;
+    return decode_long((uint32_t)(win >> 32), win, lt);
+}
+
+// Decode one symbol: returns byte | len << 8 (byte in the low 8 bits).
+template <bool kShared>
+__device__ __forceinline__ uint32_t step(Stream &s, const uint32_t *words, uint32_t wlast, const uint16_t *dec,
+                                         const LongTable &lt, bool &bad)
+{
+    const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
+    uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
+    if (e == 0) { // rare: a code longer than 12 bits, or an invalid one
+        e = decode_long_at(s.hi, s.lo, s.nx, s.o, lt);
+        if (e == 0) {
+            bad = true;
+            e = 1u << 8; // consume one bit and go on; the chunk is flagged
+        }
+        s.o += e >> 8;
+        while (s.o >= 32) {
+            s.hi = s.lo;
+            s.lo = s.nx;
+            s.nx = load_word<kShared>(words, s.wp, wlast);
+            ++s.wp;
+            s.o -= 32;
+        }
+        return e;
+    }
+    // short code: at most one word to move on, done without a branch
+    s.o += e >> 8;
+    const bool adv = s.o >= 32;
+    s.hi = adv ? s.lo : s.hi;
+    s.lo = adv ? s.nx : s.lo;
+    if (adv) {
+        s.nx = load_word<kShared>(words, s.wp, wlast);
+        ++s.wp;
+    }
+    s.o &= 31;
+    return e;
+}
+
+// Hot loop: R full sub-blocks per lane from a staged chunk, 8 symbols per
+// stream per iteration, output as 16-byte stores every second iteration.
+template <int R>
+__device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint16_t *dec, const LongTable &lt,
+                                                  const uint32_t *words, uint32_t wlast, uint64_t base, uint32_t g0,
+                                                  const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
 {
     const int lane = threadIdx.x & 31;
-    Reader<kShared> rd[R];
-    uint32_t cnt[R], endpos[R];
+    Stream s[R];
+    uint8_t *dst[R];
+    uint32_t q0[R], q1[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const uint32_t k = g0 + (uint32_t)(r * 32 + lane);
-        const uint32_t s0 = k * job.S;
-        cnt[r] = s0 < L ? min(job.S, L - s0) : 0u;
-        rd[r].start(words, wlast, st[r]);
-        endpos[r] = st[r];
+        stream_start<true>(s[r], words, wlast, st[r]);
+        dst[r] = job.out + base + (uint64_t)(g0 + (uint32_t)(r * 32 + lane)) * job.S;
+        q0[r] = q1[r] = 0;
     }
-    uint32_t steps = 0;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        steps = max(steps, cnt[r]);
-    bool full = true;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        full &= cnt[r] == job.S;
-    // steps differs between lanes only in the tensor's last chunk
-    for (uint32_t i = 0; i < steps; i += 16) {
-        uint32_t w[R][4];
+    for (uint32_t i = 0; i < job.S; i += 8) {
+        uint32_t a[R], b[R];
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0;
-        if (full) {
+            a[r] = b[r] = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+        for (int t = 0; t < 4; ++t)
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
+            for (int r = 0; r < R; ++r)
+                a[r] = __byte_perm(a[r], step<true>(s[r], words, wlast, dec, lt, bad), 0x4321);
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, lt, bad), 0x4321);
-        } else {
+        for (int t = 0; t < 4; ++t)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int r = 0; r < R; ++r)
+                b[r] = __byte_perm(b[r], step<true>(s[r], words, wlast, dec, lt, bad), 0x4321);
+        if (i & 8) {
 #pragma unroll
-                for (int t = 0; t < 4; ++t)
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        if (i + q * 4 + t < cnt[r])
-                            w[r][q] = __byte_perm(w[r][q], decode_symbol<kShared>(rd[r], dec, lt, bad), 0x4321);
+            for (int r = 0; r < R; ++r)
+                st_stream16(dst[r] + i - 8, make_uint4(q0[r], q1[r], a[r], b[r]));
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            if (i >= cnt[r])
-                continue;
-            const uint32_t k = g0 + (uint32_t)(r * 32 + lane);
-            uint8_t *dst = job.out + base + (uint64_t)k * job.S + i;
-            if (i + 16 <= cnt[r]) {
-                st_stream16(dst, make_uint4(w[r][0], w[r][1], w[r][2], w[r][3]));
-            } else {
-                const uint32_t m = cnt[r] - i;
-                // partial group: bytes sit in the high end of each word
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    if ((uint32_t)t >= m)
-                        continue;
-                    const uint32_t filled = min(4u, m - (uint32_t)(t & ~3)); // bytes pushed into word t/4
-                    const uint32_t sh = 8u * (4u - filled + (uint32_t)(t & 3));
-                    dst[t] = (uint8_t)(w[r][t >> 2] >> sh);
-                }
-            }
-            if (i + 16 >= cnt[r])
-                endpos[r] = rd[r].position();
+            q0[r] = a[r];
+            q1[r] = b[r];
         }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r)
-        if (cnt[r] && endpos[r] - st[r] != nb[r])
+        if (stream_pos(s[r]) - st[r] != nb[r])
             bad = true;
+}
+
+// Any other sub-block (the tensor's last, partial chunk, or a chunk read
+// straight from global memory): one symbol at a time, byte stores.
+// Returns true if the stream was inconsistent.
+template <bool kShared>
+static __device__ __noinline__ bool decode_stream_generic(const uint32_t *words, uint32_t wlast, uint32_t start,
+                                                          uint32_t cnt, uint32_t expect, uint8_t *dst,
+                                                          const uint16_t *dec, const LongTable &lt)
+{
+    bool bad = false;
+    Stream s;
+    stream_start<kShared>(s, words, wlast, start);
+    for (uint32_t i = 0; i < cnt; ++i)
+        dst[i] = (uint8_t)step<kShared>(s, words, wlast, dec, lt, bad);
+    return bad || stream_pos(s) - start != expect;
 }
 
 constexpr uint32_t kDecTableBytes = sizeof(((ecc_codebook *)0)->dec);
@@ -870,10 +859,20 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
             nb[r] = v;
             carry += __shfl_sync(~0u, incl, 31);
         }
-        if (staged)
-            decode_group<R, true>(job, dec, lt, words, wlast, base, L, g0, st, nb, bad);
-        else
-            decode_group<R, false>(job, dec, lt, words, wlast, base, L, g0, st, nb, bad);
+        if (staged && L == job.C) {
+            decode_group_fast<R>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
+        } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t k = g0 + (uint32_t)(r * 32 + lane);
+                if (k * job.S >= L)
+                    continue;
+                const uint32_t cnt = min(job.S, L - k * job.S);
+                uint8_t *dst = job.out + base + (uint64_t)k * job.S;
+                bad |= staged ? decode_stream_generic<true>(words, wlast, st[r], cnt, nb[r], dst, dec, lt)
+                              : decode_stream_generic<false>(words, wlast, st[r], cnt, nb[r], dst, dec, lt);
+            }
+        }
     }
     if (pad16((carry + 7) / 8) != bytes)
         bad = true;
