@@ -859,7 +859,8 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
             nb[r] = v;
             carry += __shfl_sync(~0u, incl, 31);
         }
-        if (staged && L == job.C) {
+        // the hot loop needs every lane to own R full sub-blocks
+        if (staged && L == job.C && nsub - g0 >= 32u * R) {
             decode_group_fast<R>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
         } else {
 #pragma unroll
