@@ -258,42 +258,49 @@ __device__ __forceinline__ uint4 load_symbols(const uint8_t *chunk_src, const ui
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// x << n with n >= 32 giving 0 (PTX shift semantics)
+__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t n)
+{
+    uint32_t r;
+    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(n));
+    return r;
+}
+
 // Packing sink: 32-bit words in memory byte order (MSB-first bitstream).
 // A thread's first word may also hold its predecessor's last bits and its
-// last word its successor's first bits: those two are merged with atomicOr
-// into a zeroed destination, the words in between are stored.  The first
-// completed word is kept in a register until the end, so the append itself
-// has no branch.
+// last word its successor's first bits; those two are merged with atomicOr
+// into a zeroed destination.  Every word in between belongs to this thread
+// alone and is stored once, when it completes.  The accumulator is kept as
+// two 32-bit halves shifted with funnel shifts.
 struct Packer {
     uint32_t *dst;
     uint32_t wi0, wi; // first word, word being filled
-    uint32_t nb;      // pending bits in acc (low bits)
-    uint32_t ne;      // words completed so far
-    uint32_t fw;      // the first completed word
-    uint64_t acc;
+    uint32_t nb;      // pending bits in (ahi:alo), right-aligned, < 32 between appends
+    uint32_t ahi, alo;
+    uint32_t fw;      // the first word, once completed
 
     __device__ __forceinline__ void start(uint32_t *d, uint32_t bitpos)
     {
         dst = d;
         wi0 = wi = bitpos >> 5;
         nb = bitpos & 31; // the predecessor's bits count as zeros here
-        ne = 0;
+        ahi = alo = 0;
         fw = 0;
-        acc = 0;
     }
-    // append up to 32 bits (len <= 32, nb < 32 on entry)
+    // append up to 32 bits (len <= 32)
     __device__ __forceinline__ void put(uint32_t code, uint32_t len)
     {
-        acc = (acc << len) | code;
+        ahi = __funnelshift_lc(alo, ahi, len);
+        alo = shl_clamp(alo, len) | code;
         nb += len;
         const bool full = nb >= 32;
-        nb -= full ? 32u : 0u;
-        const uint32_t w = bswap32((uint32_t)(acc >> nb));
-        if (full && ne != 0)
+        nb &= 31;
+        const uint32_t w = bswap32(__funnelshift_r(alo, ahi, nb));
+        const bool first = wi == wi0;
+        if (full && !first)
             dst[wi] = w;
-        fw = (full && ne == 0) ? w : fw;
+        fw = (full && first) ? w : fw;
         wi += full ? 1u : 0u;
-        ne += full ? 1u : 0u;
     }
     // append up to 48 bits
     __device__ __forceinline__ void put_long(uint64_t code, uint32_t len)
@@ -307,33 +314,38 @@ struct Packer {
     }
     __device__ __forceinline__ void finish()
     {
-        if (ne != 0)
+        if (wi != wi0)
             atomicOr(dst + wi0, fw);
         if (nb)
-            atomicOr(dst + wi, bswap32((uint32_t)(acc << (32 - nb))));
+            atomicOr(dst + wi, bswap32(shl_clamp(alo, 32 - nb)));
     }
 };
 
-// Encode entries of the 16 symbols held in v.  Returns the bit total; sets
-// *slow if some symbol has no packed entry (a code longer than 26 bits or a
-// byte without code), *bad if some byte has no code at all.
+// Encode entries of the 16 symbols held in v, and the bit lengths of the 8
+// consecutive pairs.  Returns the bit total; sets *slow if some symbol has
+// no packed entry (a code longer than 26 bits or a byte without code) or the
+// group is partial, *bad if some byte has no code at all.
 __device__ __forceinline__ uint32_t lookup16(const EncShared &sh, uint4 v, uint32_t cnt, const ecc_codebook *cb,
-                                             uint32_t e[16], bool *slow, bool *bad)
+                                             uint32_t e[16], uint32_t pl[8], bool *slow, bool *bad)
 {
     const int lane = threadIdx.x & 31;
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    uint32_t bits = 0;
-    bool s = false;
+    const uint32_t *lut = sh.lut + lane;
+    uint32_t emin = ~0u;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const uint32_t b = byte_of(wv[j >> 2], j & 3);
-        e[j] = sh.lut[b * 32 + lane];
-        bits += e[j] & 31u;
-        s |= (e[j] == 0u) & ((uint32_t)j < cnt);
+        e[j] = lut[byte_of(wv[j >> 2], j & 3) * 32];
+        emin = min(emin, e[j]);
     }
-    *slow = s;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        pl[k] = (e[2 * k] & 31u) + (e[2 * k + 1] & 31u);
+        bits += pl[k];
+    }
     *bad = false;
-    if (cnt < 16 || s) { // rare: recount exactly
+    *slow = cnt < 16 || emin == 0;
+    if (*slow) { // rare: recount exactly
         bits = 0;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -351,20 +363,19 @@ __device__ __forceinline__ uint32_t lookup16(const EncShared &sh, uint4 v, uint3
     return bits;
 }
 
-__device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], uint4 v, uint32_t cnt, bool slow,
-                                       const ecc_codebook *cb)
+__device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], const uint32_t pl[8], uint4 v, uint32_t cnt,
+                                       bool slow, const ecc_codebook *cb)
 {
-    if (!slow && cnt == 16) {
+    if (!slow) {
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-            const uint32_t l1 = e[j] & 31u, l2 = e[j + 1] & 31u;
-            const uint32_t pl = l1 + l2;
-            if (pl <= 32) {
-                const uint32_t pc = ((e[j] >> 5) << l2) | (e[j + 1] >> 5);
-                pk.put(pc, pl);
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t e1 = e[2 * k], e2 = e[2 * k + 1];
+            const uint32_t plk = (e1 & 31u) + (e2 & 31u);
+            if (plk <= 32) {
+                pk.put(((e1 >> 5) << (e2 & 31u)) | (e2 >> 5), plk);
             } else {
-                pk.put(e[j] >> 5, l1);
-                pk.put(e[j + 1] >> 5, l2);
+                pk.put(e1 >> 5, e1 & 31u);
+                pk.put(e2 >> 5, e2 & 31u);
             }
         }
     } else {
@@ -386,9 +397,6 @@ __device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], uint4 v
     pk.finish();
 }
 
-// One tile pass over a chunk: lookups, block scan of bit counts, packing into
-// `sink` (chunk-relative bit offsets).  Writes sub_bits when write_sub.
-// Returns the tile's bit total (uniform across the CTA).
 template <bool kCheckRoom, bool kSharedSrc>
 __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job, const uint8_t *src, uint64_t base,
                                                 uint32_t L, uint32_t t0, uint32_t run, uint32_t *sink,
@@ -399,9 +407,9 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
     const uint32_t my0 = t0 + (uint32_t)tid * kSymPerThread;
     const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
     const uint4 v = cnt ? load_symbols<kSharedSrc>(src + my0, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
-    uint32_t e[16];
+    uint32_t e[16], pl[8];
     bool slow, bad;
-    const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, &slow, &bad);
+    const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, pl, &slow, &bad);
     *bad_out |= bad;
 
     uint32_t incl = bits;
@@ -439,7 +447,7 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
         if (!kCheckRoom || pos + bits <= sink_bits) {
             Packer pk;
             pk.start(sink, pos);
-            pack16(pk, e, v, cnt, slow, job.cb);
+            pack16(pk, e, pl, v, cnt, slow, job.cb);
         } else {
             atomicOr(&sh.flags, 1u);
         }
@@ -664,44 +672,52 @@ static __device__ __noinline__ uint32_t decode_long_at(uint32_t hi, uint32_t lo,
 }
 
 // Decode one symbol: returns byte | len << 8 (byte in the low 8 bits).
-template <bool kShared>
+// kLong: the codebook has codes longer than the 12-bit first-level table, so
+// an empty entry sends the lane to the slow path; otherwise an empty entry
+// is an invalid code, recorded in emin (the minimum entry seen) and decoded
+// as a zero-length code -- the sub-block's bit count then fails too.
+template <bool kShared, bool kLong>
 __device__ __forceinline__ uint32_t step(Stream &s, const uint32_t *words, uint32_t wlast, const uint16_t *dec,
-                                         const LongTable &lt, bool &bad)
+                                         const LongTable &lt, bool &bad, uint32_t &emin)
 {
     const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
     uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
-    if (e == 0) { // rare: a code longer than 12 bits, or an invalid one
-        e = decode_long_at(s.hi, s.lo, s.nx, s.o, lt);
-        if (e == 0) {
-            bad = true;
-            e = 1u << 8; // consume one bit and go on; the chunk is flagged
+    if (kLong) {
+        if (e == 0) { // rare: a long or invalid code
+            e = decode_long_at(s.hi, s.lo, s.nx, s.o, lt);
+            if (e == 0) {
+                bad = true;
+                e = 1u << 8; // consume one bit and go on; the chunk is flagged
+            }
+            s.o += e >> 8;
+            while (s.o >= 32) {
+                s.hi = s.lo;
+                s.lo = s.nx;
+                s.nx = load_word<kShared>(words, s.wp, wlast);
+                ++s.wp;
+                s.o -= 32;
+            }
+            return e;
         }
-        s.o += e >> 8;
-        while (s.o >= 32) {
-            s.hi = s.lo;
-            s.lo = s.nx;
-            s.nx = load_word<kShared>(words, s.wp, wlast);
-            ++s.wp;
-            s.o -= 32;
-        }
-        return e;
+    } else {
+        emin = min(emin, e);
     }
-    // short code: at most one word to move on, done without a branch
+    // a code of at most 12 bits moves the window by at most one word; the
+    // word after nx is loaded every step, so no lane ever branches here
     s.o += e >> 8;
     const bool adv = s.o >= 32;
+    const uint32_t w = load_word<kShared>(words, s.wp, wlast);
     s.hi = adv ? s.lo : s.hi;
     s.lo = adv ? s.nx : s.lo;
-    if (adv) {
-        s.nx = load_word<kShared>(words, s.wp, wlast);
-        ++s.wp;
-    }
+    s.nx = adv ? w : s.nx;
+    s.wp += adv ? 1u : 0u;
     s.o &= 31;
     return e;
 }
 
 // Hot loop: R full sub-blocks per lane from a staged chunk, 8 symbols per
 // stream per iteration, output as 16-byte stores every second iteration.
-template <int R>
+template <int R, bool kLong>
 __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint16_t *dec, const LongTable &lt,
                                                   const uint32_t *words, uint32_t wlast, uint64_t base, uint32_t g0,
                                                   const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
@@ -710,6 +726,7 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
     Stream s[R];
     uint8_t *dst[R];
     uint32_t q0[R], q1[R];
+    uint32_t emin = ~0u;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         stream_start<true>(s[r], words, wlast, st[r]);
@@ -725,12 +742,12 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                a[r] = __byte_perm(a[r], step<true>(s[r], words, wlast, dec, lt, bad), 0x4321);
+                a[r] = __byte_perm(a[r], step<true, kLong>(s[r], words, wlast, dec, lt, bad, emin), 0x4321);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                b[r] = __byte_perm(b[r], step<true>(s[r], words, wlast, dec, lt, bad), 0x4321);
+                b[r] = __byte_perm(b[r], step<true, kLong>(s[r], words, wlast, dec, lt, bad, emin), 0x4321);
         if (i & 8) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -742,6 +759,8 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
             q1[r] = b[r];
         }
     }
+    if (emin == 0)
+        bad = true;
 #pragma unroll
     for (int r = 0; r < R; ++r)
         if (stream_pos(s[r]) - st[r] != nb[r])
@@ -757,10 +776,11 @@ static __device__ __noinline__ bool decode_stream_generic(const uint32_t *words,
                                                           const uint16_t *dec, const LongTable &lt)
 {
     bool bad = false;
+    uint32_t emin = ~0u;
     Stream s;
     stream_start<kShared>(s, words, wlast, start);
     for (uint32_t i = 0; i < cnt; ++i)
-        dst[i] = (uint8_t)step<kShared>(s, words, wlast, dec, lt, bad);
+        dst[i] = (uint8_t)step<kShared, true>(s, words, wlast, dec, lt, bad, emin);
     return bad || stream_pos(s) - start != expect;
 }
 
@@ -861,7 +881,10 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
         }
         // the hot loop needs every lane to own R full sub-blocks
         if (staged && L == job.C && nsub - g0 >= 32u * R) {
-            decode_group_fast<R>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
+            if (lt.max_len > ECC_PEEK_BITS)
+                decode_group_fast<R, true>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
+            else
+                decode_group_fast<R, false>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {

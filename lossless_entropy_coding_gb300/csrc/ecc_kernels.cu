@@ -87,7 +87,7 @@ __global__ void enc_prologue_kernel(uint64_t *flags, uint64_t n_flags, uint32_t 
 // always been claimed by running CTAs when it looks back.  Each CTA claims
 // its next chunk one chunk ahead and bulk-copies that chunk's input into the
 // second shared buffer while it encodes the current one.
-__global__ void __launch_bounds__(kEncThreads) encode_kernel(EncParams p)
+__global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(EncParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);

@@ -30,27 +30,46 @@ def u16(t):
     return t.cpu().numpy().view(np.uint16)
 
 
+CANARY = 64
+
+
 def check_against_oracle(x, cbb, ocb, C, S, stream=None):
-    """Encode on the GPU, compare with the oracle, decode, compare."""
+    """Encode on the GPU, compare with the oracle, decode, compare.  Every
+    output buffer is followed by canary bytes that must stay untouched, and
+    payload bytes past the used size must keep their fill value."""
     n = x.size
     xd = torch.from_numpy(x).cuda() if n else torch.empty(0, dtype=torch.uint8, device="cuda")
     dcb = ecc.to_device(cbb)
     view = ecc.codebook_view(cbb)
-    enc = ecc.ecc_encode(xd, dcb, C, S, max_len=int(view["max_len"]), stream=stream)
+    cap = max(16, ecc.max_encoded_bytes(n, C, int(view["max_len"])))
+    nch, nsub = ecc.num_chunks(n, C), -(-n // S)
+    payload = torch.full((cap + CANARY,), 0xEE, dtype=torch.uint8, device="cuda")
+    chunk_off = torch.full((nch + 1 + CANARY,), 0x1234, dtype=torch.int64, device="cuda")
+    sub_bits = torch.full((nsub + CANARY,), 0x5A5A, dtype=torch.int16, device="cuda")
+    enc = ecc.ecc_encode(xd, dcb, C, S, out=payload[:cap], chunk_off=chunk_off[:nch + 1],
+                         sub_bits=sub_bits[:max(nsub, 1)], stream=stream)
     torch.cuda.synchronize()
     assert int(enc.status.item()) == ecc.OK
     ref = oracle.encode(x, ocb, C, S)
     off = u64(enc.chunk_off)
     assert (off == ref["chunk_off"]).all()
     used = int(off[-1])
-    assert (enc.payload[:used].cpu().numpy() == ref["payload"]).all()
-    nsub = -(-n // S)
-    assert (u16(enc.sub_bits)[:nsub] == ref["sub_bits"]).all()
+    pay = payload.cpu().numpy()
+    assert (pay[:used] == ref["payload"]).all()
+    assert (pay[used:] == 0xEE).all(), "encoder wrote past its payload"
+    assert (chunk_off[nch + 1:].cpu().numpy() == 0x1234).all(), "encoder wrote past chunk_off"
+    assert (u16(sub_bits)[:nsub] == ref["sub_bits"]).all()
+    assert (u16(sub_bits)[max(nsub, 1):] == 0x5A5A).all(), "encoder wrote past sub_bits"
     assert int(u64(enc.total_bits)[0]) == ref["total_bits"]
-    out, st = ecc.ecc_decode(enc, dcb, stream=stream)
+    out = torch.full((max(n, 16) + CANARY,), 0xA5, dtype=torch.uint8, device="cuda")
+    _, st = ecc.ecc_decode(enc, dcb, out=out[:max(n, 16)], stream=stream)
     torch.cuda.synchronize()
     assert int(st.item()) == ecc.OK
-    assert (out[:n].cpu().numpy() == x).all()
+    o = out.cpu().numpy()
+    assert (o[:n] == x).all()
+    assert (o[max(n, 16):] == 0xA5).all(), "decoder wrote past its output"
+    if n < 16:
+        assert (o[n:16] == 0xA5).all(), "decoder wrote past n"
     return enc
 
 
