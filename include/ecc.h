@@ -74,7 +74,7 @@ enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2 };
 
 #define ECC_CODEBOOK_MAGIC 0x45434342u /* "ECCB" */
 #define ECC_MAX_CODE_LEN 48            /* longest code the device path accepts */
-#define ECC_PEEK_BITS 12               /* first-level decode table index width */
+#define ECC_PEEK_BITS 14               /* first-level decode table index width */
 
 /*
  * Codebook: a fixed-size, pointer-free record built on the host by
@@ -94,7 +94,7 @@ typedef struct ecc_codebook {
     uint64_t first[64];   /* Huffman: first canonical code of each length */
     uint32_t enc[256];    /* derived: (code << 5) | len if len <= 26, else 0 */
     uint32_t area[8];     /* derived, QLC: per prefix k, start | len << 16 | width << 24 */
-    uint16_t dec[4096];   /* derived: 12-bit peek -> byte | len << 8; 0 = not resolved */
+    uint16_t dec[16384];  /* derived: 14-bit peek -> byte | len << 8; 0 = not resolved */
     uint16_t count[64];   /* Huffman: number of codes of each length */
     uint16_t index[64];   /* Huffman: position in sorted[] of the first code of each length */
     uint16_t area_start[8]; /* QLC: first rank of each area */
@@ -235,7 +235,7 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
  * ecc_decode -- chunk-parallel decode ("Quad Length Codes ...", section 2
  * "Decodifica": read 3 bits -> area -> length, read the suffix, add the
  * area's offset, a second LUT gives the byte; section 4 items 2-3; Huffman
- * codes resolve through a 12-bit first-level table and canonical per-length
+ * codes resolve through a 14-bit first-level table and canonical per-length
  * ranges for longer codes).
  *   in, in_bytes device payload [in_bytes], 16-byte aligned.
  *   chunk_off    device uint64[ceil(n/C) + 1] and sub_bits device

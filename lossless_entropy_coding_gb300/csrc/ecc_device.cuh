@@ -25,10 +25,13 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;      // bounded waits: 1 s
 
 __host__ __device__ constexpr uint32_t pad16(uint32_t b) { return (b + 15u) & ~15u; }
 
+// Zeroed bytes after a staged chunk: the decoder reads ahead into them.
+constexpr uint32_t kStageGuard = 96;
+
 // Worst-case staging bytes for one chunk of C symbols at up to 11 bits
 // (every QLC code fits; longer Huffman chunks take the unstaged path), with
 // a zeroed guard so peeks past a payload's end read zeros.
-__host__ __device__ constexpr uint32_t stage_bytes_for(uint32_t C) { return pad16((C * 11u + 7u) / 8u) + 32u; }
+__host__ __device__ constexpr uint32_t stage_bytes_for(uint32_t C) { return pad16((C * 11u + 7u) / 8u) + kStageGuard; }
 
 // ---------------------------------------------------------------- memory ops
 __device__ __forceinline__ uint64_t ld_relaxed(const uint64_t *p)
@@ -196,6 +199,73 @@ __device__ __forceinline__ uint64_t lookback(uint64_t *flags, uint64_t c, uint64
     return prefix;
 }
 
+// Resolve the exclusive prefix of chunk c (c > 0) whose aggregate was
+// already published, then publish its inclusive prefix.  One full warp.
+__device__ __forceinline__ uint64_t resolve_prefix(uint64_t *flags, uint64_t c, uint64_t aggregate,
+                                                   uint64_t timeout_ns, bool *timed_out)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t prefix = 0;
+    int64_t j = (int64_t)c - 1;
+    uint64_t t0 = 0;
+    bool expired = false;
+    for (;;) {
+        const int64_t idx = j - lane;
+        const uint64_t f = idx >= 0 ? ld_relaxed(flags + idx) : kFlagPrefix;
+        const uint32_t state = (uint32_t)(f >> 62);
+        const unsigned pmask = __ballot_sync(~0u, state == 2);
+        const unsigned zmask = __ballot_sync(~0u, state == 0);
+        const int fp = pmask ? __ffs(pmask) - 1 : 32;
+        const unsigned need = fp >= 31 ? ~0u : ((2u << fp) - 1u);
+        if (zmask & need) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0)
+                t0 = now;
+            if (__any_sync(~0u, now - t0 > timeout_ns)) {
+                expired = true;
+                break;
+            }
+            __nanosleep(32);
+            continue;
+        }
+        uint64_t v = lane <= fp ? (f & kValueMask) : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            v += __shfl_xor_sync(~0u, v, o);
+        prefix += v;
+        if (fp < 32)
+            break;
+        j -= 32;
+    }
+    if (lane == 0)
+        st_relaxed(flags + c, kFlagPrefix | ((prefix + aggregate) & kValueMask));
+    *timed_out = expired;
+    return prefix;
+}
+
+// ---------------------------------------------------------------- named barriers
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t n)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// barrier over n threads that also returns the AND of p over them
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool p)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\tbar.red.and.pred b, %2, %3, a;\n\t"
+                 "selp.u32 %0, 1, 0, b;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)p), "r"(id), "r"(n)
+                 : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- encoder
 // Shared state of one encoder CTA.  lut holds one replica of the 256 encode
 // entries per bank: entry s for lane l is lut[s * 32 + l], so the 32 lanes of
@@ -205,6 +275,10 @@ struct EncShared {
     uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
     uint64_t prefix;
     uint64_t bar[2];            // input-buffer mbarriers
+    uint64_t slot_chunk[2];     // warp-specialised encoder: chunk in each stage slot
+    uint32_t slot_bits[2];      // its payload bits
+    uint32_t slot_flags[2];     // bit 0: staging overflow
+    uint32_t tk[2];             // tickets of the current and the next chunk
     const ecc_codebook *loaded; // codebook currently in lut
     uint32_t ticket;
     uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
@@ -397,10 +471,24 @@ __device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], const u
     pk.finish();
 }
 
-template <bool kCheckRoom, bool kSharedSrc>
+constexpr uint32_t kBarCompute = 1;   // the encoder's compute warps
+constexpr uint32_t kBarFull = 2;      // + slot: stage slot filled (compute -> output warp)
+constexpr uint32_t kBarEmpty = 4;     // + slot: stage slot drained (output warp -> compute)
+constexpr int kEncThreadsWS = kEncThreads + 32;
+
+__device__ __forceinline__ void compute_barrier(bool named)
+{
+    if (named)
+        bar_sync(kBarCompute, kEncThreads);
+    else
+        __syncthreads();
+}
+
+template <bool kCheckRoom, bool kSharedSrc, bool kNamed = false>
 __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job, const uint8_t *src, uint64_t base,
                                                 uint32_t L, uint32_t t0, uint32_t run, uint32_t *sink,
-                                                uint32_t sink_bits, bool write_sub, bool *bad_out)
+                                                uint32_t sink_bits, bool write_sub, bool *bad_out,
+                                                uint32_t *flag_word = nullptr)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t parity = (t0 / kTile) & 1;
@@ -421,7 +509,7 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
     }
     if (lane == 31)
         sh.warp_tot[parity][warp] = incl;
-    __syncthreads();
+    compute_barrier(kNamed);
     uint32_t before = 0, tile_total = 0;
 #pragma unroll
     for (int w = 0; w < kEncWarps; ++w) {
@@ -449,7 +537,7 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
             pk.start(sink, pos);
             pack16(pk, e, pl, v, cnt, slow, job.cb);
         } else {
-            atomicOr(&sh.flags, 1u);
+            atomicOr(flag_word ? flag_word : &sh.flags, 1u);
         }
     }
     return tile_total;
@@ -528,6 +616,42 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
         }
     }
     __syncthreads();
+}
+
+// Re-encode chunk c with one warp straight into global memory at dst (the
+// chunk's place in the output, `words` 32-bit words, zeroed here first):
+// the path for chunks whose payload outgrew the shared staging buffer.
+static __device__ __noinline__ void encode_chunk_warp(const EncShared &sh, const EncJob &job, uint64_t c,
+                                                      uint32_t *dst, uint32_t words)
+{
+    const int lane = threadIdx.x & 31;
+    for (uint32_t i = lane; i < words; i += 32)
+        dst[i] = 0;
+    __syncwarp();
+    const uint64_t base = c * job.C;
+    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
+    uint32_t run = 0;
+    for (uint32_t t0 = 0; t0 < L; t0 += 32 * kSymPerThread) {
+        const uint32_t my0 = t0 + (uint32_t)lane * kSymPerThread;
+        const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
+        const uint4 v = cnt ? load_symbols<false>(nullptr, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
+        uint32_t e[16], pl[8];
+        bool slow, bad;
+        const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, pl, &slow, &bad);
+        uint32_t incl = bits;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(~0u, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        if (cnt) {
+            Packer pk;
+            pk.start(dst, run + incl - bits);
+            pack16(pk, e, pl, v, cnt, slow, job.cb);
+        }
+        run += __shfl_sync(~0u, incl, 31);
+    }
 }
 
 // Bulk-copy the whole 16-byte groups of chunk c's input into buf (thread 0);
@@ -715,39 +839,108 @@ __device__ __forceinline__ uint32_t step(Stream &s, const uint32_t *words, uint3
     return e;
 }
 
+// Stream of the hot loop, reading the staged chunk in shared memory: window
+// (hi, lo) in stream order, the following word nx still in memory byte
+// order, wa the shared-memory address of the word after nx.
+struct FastStream {
+    uint32_t hi, lo, nx, o, wa;
+};
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// v = word at addr for lanes with p set; other lanes keep v (no branch)
+__device__ __forceinline__ void lds_u32_if(uint32_t &v, uint32_t addr, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.shared.u32 %0, [%1];\n\t}"
+                 : "+r"(v)
+                 : "r"(addr), "r"((uint32_t)p));
+}
+
+template <bool kLong>
+__device__ __forceinline__ uint32_t fstep(FastStream &s, const uint16_t *dec, const LongTable &lt, bool &bad,
+                                          uint32_t &emin)
+{
+    const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
+    uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
+    if (kLong) {
+        if (e == 0) { // rare: a long or invalid code
+            e = decode_long_at(s.hi, s.lo, bswap32(s.nx), s.o, lt);
+            if (e == 0) {
+                bad = true;
+                e = 1u << 8;
+            }
+            s.o += e >> 8;
+            while (s.o >= 32) {
+                s.hi = s.lo;
+                s.lo = bswap32(s.nx);
+                s.nx = lds_u32(s.wa);
+                s.wa += 4;
+                s.o -= 32;
+            }
+            return e;
+        }
+    } else {
+        emin = min(emin, e);
+    }
+    s.o += e >> 8;
+    const bool adv = s.o >= 32;
+    s.hi = adv ? s.lo : s.hi;
+    s.lo = adv ? bswap32(s.nx) : s.lo;
+    lds_u32_if(s.nx, s.wa, adv);
+    s.wa += adv ? 4u : 0u;
+    s.o &= 31;
+    return e;
+}
+
 // Hot loop: R full sub-blocks per lane from a staged chunk, 8 symbols per
 // stream per iteration, output as 16-byte stores every second iteration.
+// wmax: the highest word index a stream may reach at an iteration start; a
+// stream moves at most 16 words per iteration, into the zeroed guard.
 template <int R, bool kLong>
 __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint16_t *dec, const LongTable &lt,
-                                                  const uint32_t *words, uint32_t wlast, uint64_t base, uint32_t g0,
+                                                  const uint32_t *words, uint32_t wmax, uint64_t base, uint32_t g0,
                                                   const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
 {
     const int lane = threadIdx.x & 31;
-    Stream s[R];
+    const uint32_t w_base = smem_u32(words);
+    const uint32_t a_max = w_base + wmax * 4;
+    FastStream s[R];
     uint8_t *dst[R];
     uint32_t q0[R], q1[R];
     uint32_t emin = ~0u;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        stream_start<true>(s[r], words, wlast, st[r]);
+        const uint32_t w0 = min(st[r] >> 5, wmax);
+        s[r].o = st[r] & 31;
+        s[r].hi = bswap32(words[w0]);
+        s[r].lo = bswap32(words[w0 + 1]);
+        s[r].nx = words[w0 + 2];
+        s[r].wa = w_base + (w0 + 3) * 4;
         dst[r] = job.out + base + (uint64_t)(g0 + (uint32_t)(r * 32 + lane)) * job.S;
         q0[r] = q1[r] = 0;
     }
     for (uint32_t i = 0; i < job.S; i += 8) {
         uint32_t a[R], b[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+        for (int r = 0; r < R; ++r) {
             a[r] = b[r] = 0;
+            s[r].wa = min(s[r].wa, a_max);
+        }
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                a[r] = __byte_perm(a[r], step<true, kLong>(s[r], words, wlast, dec, lt, bad, emin), 0x4321);
+                a[r] = __byte_perm(a[r], fstep<kLong>(s[r], dec, lt, bad, emin), 0x4321);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                b[r] = __byte_perm(b[r], step<true, kLong>(s[r], words, wlast, dec, lt, bad, emin), 0x4321);
+                b[r] = __byte_perm(b[r], fstep<kLong>(s[r], dec, lt, bad, emin), 0x4321);
         if (i & 8) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -763,7 +956,7 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
         bad = true;
 #pragma unroll
     for (int r = 0; r < R; ++r)
-        if (stream_pos(s[r]) - st[r] != nb[r])
+        if ((s[r].wa - w_base) / 4 * 32 - 96 + s[r].o - st[r] != nb[r]) // position = (word of hi) * 32 + o
             bad = true;
 }
 
@@ -823,7 +1016,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
         return;
     }
     const uint32_t bytes = (uint32_t)(b1 - b0);
-    const bool staged = ws.buf != nullptr && bytes + 16 <= ws.bytes;
+    const bool staged = ws.buf != nullptr && bytes + kStageGuard <= ws.bytes;
     if (staged) {
         __syncwarp();
         if (lane == 0) {
@@ -850,11 +1043,11 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
             ws.buf = nullptr; // the copy may still land: stop using this buffer
             return;
         }
-        if (lane < 4)
-            ws.buf[bytes / 4 + lane] = 0; // guard: peeks past the end read 0
+        if (lane < kStageGuard / 4)
+            ws.buf[bytes / 4 + lane] = 0; // guard: reads past the end see 0
         __syncwarp();
         words = ws.buf;
-        wlast = bytes / 4 + 3;
+        wlast = bytes / 4 + kStageGuard / 4 - 1;
     } else {
         words = reinterpret_cast<const uint32_t *>(job.in + b0);
         wlast = bytes / 4 - 1;
@@ -881,10 +1074,11 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
         }
         // the hot loop needs every lane to own R full sub-blocks
         if (staged && L == job.C && nsub - g0 >= 32u * R) {
+            const uint32_t wmax = bytes / 4 + 4; // + up to 2 words per step x 8 steps < guard
             if (lt.max_len > ECC_PEEK_BITS)
-                decode_group_fast<R, true>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
+                decode_group_fast<R, true>(job, dec, lt, words, wmax, base, g0, st, nb, bad);
             else
-                decode_group_fast<R, false>(job, dec, lt, words, wlast, base, g0, st, nb, bad);
+                decode_group_fast<R, false>(job, dec, lt, words, wmax, base, g0, st, nb, bad);
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {

@@ -117,16 +117,16 @@ def test_huffman_length_limit_is_an_error():
 
 
 def test_derived_decode_table():
-    # every 12-bit index resolves to the code that prefixes it, or is 0 when
-    # no code of <= 12 bits does
+    # every 14-bit index resolves to the code that prefixes it, or is 0 when
+    # no code of <= 14 bits does
     for cbb in (ecc.qlc_build_tables(pmfs()["gauss"]), ecc.huff_build_canonical(pmfs()["spike"] + 1)):
         cb = ecc.codebook_view(cbb)
-        want = np.zeros(4096, np.uint16)
+        want = np.zeros(1 << 14, np.uint16)
         for b in range(256):
             L = int(cb["len"][b])
-            if 0 < L <= 12:
-                lo = int(cb["code"][b]) << (12 - L)
-                want[lo:lo + (1 << (12 - L))] = b | (L << 8)
+            if 0 < L <= 14:
+                lo = int(cb["code"][b]) << (14 - L)
+                want[lo:lo + (1 << (14 - L))] = b | (L << 8)
         assert (cb["dec"] == want).all()
         for b in range(256):
             L = int(cb["len"][b])
