@@ -861,32 +861,14 @@ __device__ __forceinline__ void lds_u32_if(uint32_t &v, uint32_t addr, bool p)
                  : "r"(addr), "r"((uint32_t)p));
 }
 
-template <bool kLong>
-__device__ __forceinline__ uint32_t fstep(FastStream &s, const uint16_t *dec, const LongTable &lt, bool &bad,
-                                          uint32_t &emin)
+// Hot-loop step: codes the 14-bit table resolves.  An empty entry (a longer
+// or an invalid code) has length 0, so the stream stays where it is; emin
+// records it and the caller redoes the iteration with fstep_slow.
+__device__ __forceinline__ uint32_t fstep(FastStream &s, const uint16_t *dec, uint32_t &emin)
 {
     const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
-    uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
-    if (kLong) {
-        if (e == 0) { // rare: a long or invalid code
-            e = decode_long_at(s.hi, s.lo, bswap32(s.nx), s.o, lt);
-            if (e == 0) {
-                bad = true;
-                e = 1u << 8;
-            }
-            s.o += e >> 8;
-            while (s.o >= 32) {
-                s.hi = s.lo;
-                s.lo = bswap32(s.nx);
-                s.nx = lds_u32(s.wa);
-                s.wa += 4;
-                s.o -= 32;
-            }
-            return e;
-        }
-    } else {
-        emin = min(emin, e);
-    }
+    const uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
+    emin = min(emin, e);
     s.o += e >> 8;
     const bool adv = s.o >= 32;
     s.hi = adv ? s.lo : s.hi;
@@ -897,11 +879,37 @@ __device__ __forceinline__ uint32_t fstep(FastStream &s, const uint16_t *dec, co
     return e;
 }
 
+// Any code, long ones through the canonical ranges; invalid codes set bad.
+__device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *dec, const LongTable &lt, bool &bad)
+{
+    const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
+    uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
+    if (e == 0) {
+        e = decode_long_at(s.hi, s.lo, bswap32(s.nx), s.o, lt);
+        if (e == 0) {
+            bad = true;
+            e = 1u << 8; // consume one bit and go on; the chunk is flagged
+        }
+    }
+    s.o += e >> 8;
+    while (s.o >= 32) {
+        s.hi = s.lo;
+        s.lo = bswap32(s.nx);
+        s.nx = lds_u32(s.wa);
+        s.wa += 4;
+        s.o -= 32;
+    }
+    return e;
+}
+
 // Hot loop: R full sub-blocks per lane from a staged chunk, 8 symbols per
 // stream per iteration, output as 16-byte stores every second iteration.
+// The loop body has no branch, so the R streams interleave; a lane that met
+// a code the table cannot resolve redoes the iteration from its saved state
+// with fstep_slow (rare: codes longer than 14 bits, or corrupt data).
 // wmax: the highest word index a stream may reach at an iteration start; a
 // stream moves at most 16 words per iteration, into the zeroed guard.
-template <int R, bool kLong>
+template <int R>
 __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint16_t *dec, const LongTable &lt,
                                                   const uint32_t *words, uint32_t wmax, uint64_t base, uint32_t g0,
                                                   const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
@@ -912,7 +920,6 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
     FastStream s[R];
     uint8_t *dst[R];
     uint32_t q0[R], q1[R];
-    uint32_t emin = ~0u;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const uint32_t w0 = min(st[r] >> 5, wmax);
@@ -925,22 +932,39 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
         q0[r] = q1[r] = 0;
     }
     for (uint32_t i = 0; i < job.S; i += 8) {
+        FastStream s0[R];
         uint32_t a[R], b[R];
+        uint32_t emin = ~0u;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            a[r] = b[r] = 0;
             s[r].wa = min(s[r].wa, a_max);
+            s0[r] = s[r];
+            a[r] = b[r] = 0;
         }
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                a[r] = __byte_perm(a[r], fstep<kLong>(s[r], dec, lt, bad, emin), 0x4321);
+                a[r] = __byte_perm(a[r], fstep(s[r], dec, emin), 0x4321);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                b[r] = __byte_perm(b[r], fstep<kLong>(s[r], dec, lt, bad, emin), 0x4321);
+                b[r] = __byte_perm(b[r], fstep(s[r], dec, emin), 0x4321);
+        if (__any_sync(~0u, emin == 0) && emin == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                s[r] = s0[r];
+                a[r] = b[r] = 0;
+                for (int t = 0; t < 8; ++t) {
+                    const uint32_t e = fstep_slow(s[r], dec, lt, bad);
+                    if (t < 4)
+                        a[r] = __byte_perm(a[r], e, 0x4321);
+                    else
+                        b[r] = __byte_perm(b[r], e, 0x4321);
+                }
+            }
+        }
         if (i & 8) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -952,8 +976,6 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
             q1[r] = b[r];
         }
     }
-    if (emin == 0)
-        bad = true;
 #pragma unroll
     for (int r = 0; r < R; ++r)
         if ((s[r].wa - w_base) / 4 * 32 - 96 + s[r].o - st[r] != nb[r]) // position = (word of hi) * 32 + o
@@ -1075,10 +1097,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
         // the hot loop needs every lane to own R full sub-blocks
         if (staged && L == job.C && nsub - g0 >= 32u * R) {
             const uint32_t wmax = bytes / 4 + 4; // + up to 2 words per step x 8 steps < guard
-            if (lt.max_len > ECC_PEEK_BITS)
-                decode_group_fast<R, true>(job, dec, lt, words, wmax, base, g0, st, nb, bad);
-            else
-                decode_group_fast<R, false>(job, dec, lt, words, wmax, base, g0, st, nb, bad);
+            decode_group_fast<R>(job, dec, lt, words, wmax, base, g0, st, nb, bad);
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {

@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(EncParams p)
 // while the compute warps already encode chunk k + 1 into the other slot.
 // Slots are handed over with named barriers: kBarFull + slot (compute ->
 // output) and kBarEmpty + slot (output -> compute).
-__global__ void __maxnreg__(112) encode_ws_kernel(EncParams p)
+__global__ void __maxnreg__(96) encode_ws_kernel(EncParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
