@@ -49,6 +49,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--n", type=int, default=N_DEFAULT, help="tensor bytes (default 2^30)")
     p.add_argument("--chunk", type=int, default=CHUNK)
+    p.add_argument("--subblock", type=int, default=0, help="sub-block symbols (default: library default for the chunk)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -294,7 +295,7 @@ def run_ours(args):
     clocks.start()
 
     n, C = args.n, args.chunk
-    S = ecc.default_subblock(C)
+    S = args.subblock or ecc.default_subblock(C)
     stream = torch.cuda.current_stream()
 
     # warm-up stage of the single-stage method: pooled histogram -> codebooks

@@ -255,7 +255,10 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
         if (c < n_chunks) {
             if (cb_ok) {
                 DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
-                if (d.C / d.S >= 64)
+                const uint32_t per_lane = (d.C >> (31 - __clz(d.S))) >> 5; // (C/S)/32
+                if (per_lane >= 4)
+                    decode_chunk<4>(job, dec, lt, wst, c, c + warps, n_chunks);
+                else if (per_lane >= 2)
                     decode_chunk<2>(job, dec, lt, wst, c, c + warps, n_chunks);
                 else
                     decode_chunk<1>(job, dec, lt, wst, c, c + warps, n_chunks);

@@ -272,7 +272,7 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool p)
 // a warp always hit 32 different banks whatever bytes they look up.
 struct EncShared {
     uint32_t lut[kLutRows * 32];
-    uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
+    alignas(16) uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
     uint64_t prefix;
     uint64_t bar[2];            // input-buffer mbarriers
     uint64_t slot_chunk[2];     // warp-specialised encoder: chunk in each stage slot
@@ -511,24 +511,28 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
         sh.warp_tot[parity][warp] = incl;
     compute_barrier(kNamed);
     uint32_t before = 0, tile_total = 0;
+    {
+        const uint4 w03 = *reinterpret_cast<const uint4 *>(&sh.warp_tot[parity][0]);
+        const uint4 w47 = *reinterpret_cast<const uint4 *>(&sh.warp_tot[parity][4]);
+        const uint32_t t[8] = {w03.x, w03.y, w03.z, w03.w, w47.x, w47.y, w47.z, w47.w};
 #pragma unroll
-    for (int w = 0; w < kEncWarps; ++w) {
-        const uint32_t t = sh.warp_tot[parity][w];
-        before += w < warp ? t : 0u;
-        tile_total += t;
+        for (int w = 0; w < kEncWarps; ++w) {
+            before += w < warp ? t[w] : 0u;
+            tile_total += t[w];
+        }
     }
     const uint32_t excl = before + incl - bits;
     if (write_sub) {
         // bits of each sub-block of S symbols = S/16 consecutive threads
-        const uint32_t tps = job.S / kSymPerThread;
+        const uint32_t tps = job.S / kSymPerThread; // a power of two, 4..64
         uint32_t sb;
         if (tps <= 32) {
             sb = __shfl_sync(~0u, incl, lane | (int)(tps - 1)) - (incl - bits);
         } else { // S = 1024: two whole warps
             sb = sh.warp_tot[parity][warp] + sh.warp_tot[parity][warp | 1];
         }
-        if (cnt && ((uint32_t)tid % tps) == 0)
-            job.sub_bits[(base + my0) / job.S] = (uint16_t)sb;
+        if (cnt && ((uint32_t)tid & (tps - 1)) == 0)
+            job.sub_bits[(base + my0) >> (31 - __clz(job.S))] = (uint16_t)sb;
     }
     const uint32_t pos = run + excl;
     if (cnt) {
@@ -1029,8 +1033,9 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
     const int lane = threadIdx.x & 31;
     const uint64_t base = c * job.C;
     const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
-    const uint32_t nsub = (L + job.S - 1) / job.S;
-    const uint64_t sub0 = base / job.S;
+    const uint32_t s_shift = 31 - __clz(job.S); // S is a power of two
+    const uint32_t nsub = (L + job.S - 1) >> s_shift;
+    const uint64_t sub0 = base >> s_shift;
     uint64_t b0, b1;
     if (!chunk_range_ok(job, c, b0, b1)) {
         if (lane == 0)

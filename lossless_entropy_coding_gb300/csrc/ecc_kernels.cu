@@ -568,15 +568,20 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
     p.stage_bytes = stage_bytes_for(C);
     const int warps = decode_warps(p.stage_bytes);
     const size_t smem = kDecHeadBytes + (size_t)warps * p.stage_bytes;
-    const bool two = C / S >= 64;
-    const void *kfn = two ? (const void *)decode_kernel<2> : (const void *)decode_kernel<1>;
+    // streams per lane: C/S sub-blocks per chunk over 32 lanes, at most 4
+    const uint32_t per_lane = std::min<uint32_t>(4, std::max<uint32_t>(1, C / S / 32));
+    const void *kfn = per_lane == 4 ? (const void *)decode_kernel<4>
+                      : per_lane == 2 ? (const void *)decode_kernel<2>
+                                      : (const void *)decode_kernel<1>;
     const int occ = occupancy(kfn, warps * 32, smem);
     const int sms = sm_count();
     if (occ <= 0 || sms <= 0)
         return ECC_ERR_CUDA;
     const uint64_t need = (p.n_chunks + warps - 1) / warps;
     const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, need);
-    if (two)
+    if (per_lane == 4)
+        decode_kernel<4><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    else if (per_lane == 2)
         decode_kernel<2><<<(unsigned)grid, warps * 32, smem, st>>>(p);
     else
         decode_kernel<1><<<(unsigned)grid, warps * 32, smem, st>>>(p);
