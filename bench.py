@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--workload", choices=["gradient", "batched"], default="gradient",
+                   help="gradient: the 2^30-byte tensor (default); batched: 4096 tensors in one launch each way")
     return p.parse_args(argv)
 
 
@@ -528,10 +530,126 @@ def run_ours(args):
     return 0
 
 
+def run_batched(args):
+    """4096 tensors (sizes 2^U(12,23) B, laws gauss / gauss-sigma / zero
+    spike, four codebooks), one batched encode and one batched decode launch
+    per step; aggregate GB/s and per-tensor completion latency."""
+    import numpy as np
+    import torch
+
+    import lossless_entropy_coding_gb300 as ecc
+    from workloads import batch_plan, dev_batch_tensor, dev_gauss, dev_zero_spike
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    C = args.chunk
+    S = args.subblock or ecc.default_subblock(C)
+    plan = batch_plan(4096)
+    # four codebooks from warm-up tensors of the laws (device histograms)
+    def counts(x):
+        c = ecc.e4m3_histogram(x)
+        torch.cuda.synchronize()
+        return c.cpu().numpy().view(np.uint64).copy()
+    c1 = counts(dev_gauss(1 << 22, (5, 1001), dev, sigma=1.0)[0])
+    c3 = counts(dev_zero_spike(1 << 22, (5, 1003), dev))
+    c2 = np.zeros(256, np.uint64)
+    for i in range(4):
+        c2 += counts(dev_gauss(1 << 20, (5, 2000 + i), dev)[0])
+    w3, _ = ecc.qlc_search_widths(c3)
+    books = [ecc.qlc_build_tables(c1), ecc.qlc_build_tables(c3, w3),
+             ecc.huff_build_canonical(c2 + np.uint64(1)), ecc.huff_build_canonical(c3 + np.uint64(1))]
+    dcbs = [ecc.to_device(b, dev) for b in books]
+    max_len = [int(ecc.codebook_view(b)["max_len"]) for b in books]
+    total = sum(sz for sz, _, _ in plan)
+    xin = torch.empty(total + 16 * len(plan), dtype=torch.uint8, device=dev)
+    enc_items, dec_items, off = [], [], 0
+    for i, (size, law, tag) in enumerate(plan):
+        x = xin[off:off + size]
+        dev_batch_tensor(size, law, (5, i), device=dev, out=x)
+        off += (size + 15) // 16 * 16
+        cap = ecc.max_encoded_bytes(size, C, max_len[tag])
+        common = {"n": size, "cap": cap, "cb": dcbs[tag], "C": C, "S": S,
+                  "chunk_off": torch.empty(ecc.num_chunks(size, C) + 1, dtype=torch.int64, device=dev),
+                  "sub_bits": torch.empty(ecc.num_subblocks(size, S), dtype=torch.int16, device=dev)}
+        payload = torch.empty(cap, dtype=torch.uint8, device=dev)
+        enc_items.append(dict(common, **{"in": x, "out": payload,
+                                         "total_bits": torch.empty(1, dtype=torch.int64, device=dev),
+                                         "status": torch.empty(1, dtype=torch.int32, device=dev),
+                                         "t_done_ns": torch.empty(1, dtype=torch.int64, device=dev)}))
+        dec_items.append(dict(common, **{"in": payload, "out": torch.empty(size, dtype=torch.uint8, device=dev),
+                                         "total_bits": None,
+                                         "status": torch.empty(1, dtype=torch.int32, device=dev),
+                                         "t_done_ns": torch.empty(1, dtype=torch.int64, device=dev)}))
+    edesc, ddesc = ecc.make_descs(enc_items), ecc.make_descs(dec_items)
+    ws_e = torch.empty(ecc.batched_workspace_bytes(edesc), dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(ecc.batched_workspace_bytes(ddesc), dtype=torch.uint8, device=dev)
+    t_enc = torch.zeros(1, dtype=torch.int64, device=dev)
+    t_dec = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream()
+    EV = torch.cuda.Event
+
+    def step(rec=None):
+        if rec is not None:
+            rec[0].append(EV(enable_timing=True)); rec[0][-1].record(stream)
+        ecc.ecc_encode_batched(edesc, ws_e, t_enc)
+        if rec is not None:
+            rec[1].append(EV(enable_timing=True)); rec[1][-1].record(stream)
+        ecc.ecc_decode_batched(ddesc, ws_d, t_dec)
+        if rec is not None:
+            rec[2].append(EV(enable_timing=True)); rec[2][-1].record(stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_warm = time.time()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rec = ([], [], [])
+    e0, e1 = EV(enable_timing=True), EV(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(rec)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    clocks.stop()
+    ok = all(int(it["status"].item()) == 0 for it in enc_items[:64]) and \
+        torch.equal(torch.cat([it["out"] for it in dec_items[:256]]), torch.cat([it["in"] for it in enc_items[:256]]))
+    st_all = torch.cat([it["status"] for it in enc_items] + [it["status"] for it in dec_items])
+    if not ok or int(st_all.abs().sum().item()) != 0:
+        raise SystemExit("batched encode/decode failed")
+    total_ms = e0.elapsed_time(e1)
+    enc_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(rec[0], rec[1]))
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(rec[1], rec[2]))
+    done_e = (torch.cat([it["t_done_ns"] for it in enc_items]) - t_enc).cpu().numpy() / 1e3
+    done_d = (torch.cat([it["t_done_ns"] for it in dec_items]) - t_dec).cpu().numpy() / 1e3
+    payload = sum(int(it["chunk_off"][-1].item()) for it in enc_items)
+    line = {
+        "metric": METRIC + " (batched messages)", "value": 2.0 * total * args.steps / total_ms / 1e6,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "4096 tensors, sizes 2^U(12,23) B, laws {N(0,1), N(0,sigma), zero spike}, "
+                               "codebooks {base QLC, adapted QLC, 2 fixed Huffman}", "bytes": total, "chunk": C,
+                   "subblock": S, "step": "one batched encode + one batched decode launch"},
+        "encode_gbs": total / enc_ms / 1e6, "decode_gbs": total / dec_ms / 1e6,
+        "compressibility_container_pct": 100.0 * (1 - payload / total),
+        "latency_us": {"encode_p50": float(np.percentile(done_e, 50)), "encode_p99": float(np.percentile(done_e, 99)),
+                       "decode_p50": float(np.percentile(done_d, 50)), "decode_p99": float(np.percentile(done_d, 99))},
+        "clocks": clocks.summary(t_warm, t_end),
+        "gpu_launches": args.steps * 4,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "batched":
+        return run_batched(args)
     return run_ours(args)
 
 

@@ -937,27 +937,33 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
     }
     for (uint32_t i = 0; i < job.S; i += 8) {
         FastStream s0[R];
-        uint32_t a[R], b[R];
-        uint32_t emin = ~0u;
+        uint32_t a[R], b[R], emin[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             s[r].wa = min(s[r].wa, a_max);
             s0[r] = s[r];
             a[r] = b[r] = 0;
+            emin[r] = ~0u;
         }
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                a[r] = __byte_perm(a[r], fstep(s[r], dec, emin), 0x4321);
+                a[r] = __byte_perm(a[r], fstep(s[r], dec, emin[r]), 0x4321);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                b[r] = __byte_perm(b[r], fstep(s[r], dec, emin), 0x4321);
-        if (__any_sync(~0u, emin == 0) && emin == 0) {
+                b[r] = __byte_perm(b[r], fstep(s[r], dec, emin[r]), 0x4321);
+        uint32_t esc = 0; // streams of this lane that met an unresolved code
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            esc |= (emin[r] == 0) ? (1u << r) : 0u;
+        if (__any_sync(~0u, esc != 0)) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
+                if (!(esc & (1u << r)))
+                    continue;
                 s[r] = s0[r];
                 a[r] = b[r] = 0;
                 for (int t = 0; t < 8; ++t) {
