@@ -100,6 +100,17 @@ __device__ __forceinline__ EncJob batch_job(const ecc_desc &d, uint64_t *flags, 
                   flags + prefix[k], d.status};
 }
 
+// Work items are claimed one ahead by thread 0, which also finds the item's
+// tensor (binary search over the prefix table) and copies its descriptor
+// into shared memory, so the other threads never wait on that search.
+struct BatchSlot {
+    ecc_desc d;
+    uint64_t item;   // global work item (ticket)
+    uint32_t tensor; // index of the tensor it belongs to
+    uint32_t pad;
+};
+constexpr uint32_t kBatchSlotBytes = 2 * ((sizeof(BatchSlot) + 15) & ~15u);
+
 __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws, uint64_t *t_start)
 {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -111,8 +122,9 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
     uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
     const uint32_t stage_bytes = h->stage_bytes;
     const uint32_t cmax = h->max_C;
-    uint8_t *inbuf = smem + enc_shared_bytes();
     const uint32_t nbuf = h->nbuf;
+    BatchSlot *slot = reinterpret_cast<BatchSlot *>(smem + enc_shared_bytes());
+    uint8_t *inbuf = smem + enc_shared_bytes() + kBatchSlotBytes;
     uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + (size_t)nbuf * cmax);
     const int tid = threadIdx.x;
     if (t_start && blockIdx.x == 0 && tid == 0)
@@ -126,35 +138,36 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
     uint4 *st4 = reinterpret_cast<uint4 *>(stage);
     for (uint32_t i = tid; i < stage_bytes / 16; i += kEncThreads)
         st4[i] = make_uint4(0, 0, 0, 0);
-    // thread 0 claims chunks one ahead and bulk-copies their input
+    // thread 0: claim the next chunk into slot q (and bulk-copy its input)
     uint32_t pending = 0;
-    auto claim = [&](uint32_t buf) {
+    auto claim = [&](uint32_t q, bool copy) {
         const uint32_t t = atomicAdd(&h->ticket, 1u);
-        sh.ticket = t;
+        slot[q].item = t;
         if (t < h->total_chunks) {
             const uint32_t k = find_tensor(prefix, h->count, t);
-            const ecc_desc &d = descs[k];
-            issue_chunk_input(batch_job(d, flags, prefix, k), t - prefix[k], inbuf + (size_t)buf * cmax,
-                              &sh.bar[buf]);
-            pending |= 1u << buf;
+            slot[q].tensor = k;
+            slot[q].d = descs[k];
+            if (copy) {
+                issue_chunk_input(batch_job(slot[q].d, flags, prefix, k), t - prefix[k],
+                                  inbuf + (size_t)q * cmax, &sh.bar[q]);
+                pending |= 1u << q;
+            }
         }
     };
     if (tid == 0)
-        claim(0);
+        claim(0, true);
     __syncthreads();
-    uint64_t t = sh.ticket;
     uint32_t b = 0, phase = 0;
     bool staging = true;
-    while (t < h->total_chunks) {
-        __syncthreads(); // every thread has read sh.ticket and sh.loaded
-        if (tid == 0) {
-            if (staging && nbuf == 2)
-                claim(b ^ 1);
-            else if (!staging)
-                sh.ticket = atomicAdd(&h->ticket, 1u);
-        }
-        const uint32_t k = find_tensor(prefix, h->count, t);
-        const ecc_desc d = descs[k];
+    for (;;) {
+        const uint64_t t = slot[b].item;
+        if (t >= h->total_chunks)
+            break;
+        const uint32_t k = slot[b].tensor;
+        const ecc_desc d = slot[b].d;
+        __syncthreads(); // every thread has read slot b before it is refilled
+        if (tid == 0 && nbuf == 2)
+            claim(b ^ 1, staging);
         const uint64_t c = t - prefix[k];
         const EncJob job = batch_job(d, flags, prefix, k);
         const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
@@ -164,12 +177,13 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
             if (tid == 0)
                 sh.loaded = d.cb;
         }
-        bool ok = staging && mbar_wait(&sh.bar[b], (phase >> b) & 1u, kWaitLimitNs);
+        const uint32_t ib = nbuf == 2 ? b : 0u;
+        bool ok = staging && mbar_wait(&sh.bar[ib], (phase >> ib) & 1u, kWaitLimitNs);
         ok = __syncthreads_and(ok) != 0;
         if (ok) {
-            phase ^= 1u << b;
+            phase ^= 1u << ib;
             if (tid == 0)
-                pending &= ~(1u << b);
+                pending &= ~(1u << ib);
         } else {
             if (staging && tid == 0)
                 set_status(d.status, ECC_ERR_TIMEOUT);
@@ -177,7 +191,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
         }
         if (cb_ok) {
             if (ok)
-                encode_chunk<true>(sh, stage, stage_bytes, job, inbuf + (size_t)b * cmax, c, kWaitLimitNs);
+                encode_chunk<true>(sh, stage, stage_bytes, job, inbuf + (size_t)ib * cmax, c, kWaitLimitNs);
             else
                 encode_chunk<false>(sh, stage, stage_bytes, job, nullptr, c, kWaitLimitNs);
         } else if (tid < 32) {
@@ -191,11 +205,10 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
         }
         if (tid == 0) {
             stamp_done(d, done, k, (d.n + d.C - 1) / d.C, 1);
-            if (staging && nbuf == 1)
-                claim(0); // the single buffer is free again
+            if (nbuf == 1)
+                claim(0, staging); // the single buffer is free again
         }
         __syncthreads();
-        t = sh.ticket;
         if (nbuf == 2)
             b ^= 1;
     }
@@ -211,8 +224,8 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
     LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes);
+    BatchSlot *slot = reinterpret_cast<BatchSlot *>(smem + kDecHeadBytes);
     __shared__ const ecc_codebook *loaded;
-    __shared__ uint32_t ticket;
     BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
     const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
     const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
@@ -222,23 +235,35 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
     const uint32_t warps = h->warps;
     if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
         *t_start = globaltimer();
-    if (threadIdx.x == 0)
-        loaded = nullptr;
     if (lane == 0) {
         mbar_init(&bars[warp], 1);
         fence_mbar_init();
     }
-    WarpStage wst{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * stage_bytes), stage_bytes,
-                  &bars[warp], 0};
-    for (;;) {
-        if (threadIdx.x == 0)
-            ticket = atomicAdd(&h->ticket, 1u);
-        __syncthreads();
-        const uint64_t g = ticket;
+    auto claim = [&](uint32_t q) {
+        const uint32_t g = atomicAdd(&h->ticket, 1u);
+        slot[q].item = g;
+        if (g < h->total_items) {
+            const uint32_t k = find_tensor(prefix, h->count, g);
+            slot[q].tensor = k;
+            slot[q].d = descs[k];
+        }
+    };
+    if (threadIdx.x == 0) {
+        loaded = nullptr;
+        claim(0);
+    }
+    __syncthreads();
+    WarpStage wst{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + kBatchSlotBytes + (size_t)warp * stage_bytes),
+                  stage_bytes, &bars[warp], 0};
+    for (uint32_t b = 0;; b ^= 1) {
+        const uint64_t g = slot[b].item;
         if (g >= h->total_items)
             break;
-        const uint32_t k = find_tensor(prefix, h->count, g);
-        const ecc_desc d = descs[k];
+        const uint32_t k = slot[b].tensor;
+        const ecc_desc d = slot[b].d;
+        __syncthreads(); // every thread has read slot b
+        if (threadIdx.x == 0)
+            claim(b ^ 1);
         const uint64_t n_chunks = (d.n + d.C - 1) / d.C;
         const uint64_t c = (g - prefix[k]) * warps + warp;
         const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
@@ -312,7 +337,9 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     if (!ws || !aligned16(ws) || ws_bytes < L.bytes)
         return ECC_ERR_ARG;
     const uint32_t stage = stage_bytes_for(max_C);
-    const int warps = decode_warps(stage);
+    int warps = decode_warps(stage);
+    while (warps > 1 && kDecHeadBytes + kBatchSlotBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve)
+        --warps;
     // host image of header | descs | prefix, copied with one async copy
     std::vector<uint8_t> img(L.done_off, 0);
     BatchHeader *h = reinterpret_cast<BatchHeader *>(img.data());
@@ -353,14 +380,14 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     if (acc == 0)
         return ECC_OK;
     if (encode) {
-        const size_t smem = enc_shared_bytes() + (size_t)h->nbuf * max_C + stage;
+        const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)h->nbuf * max_C + stage;
         const int occ = occupancy((const void *)encode_batched_kernel, kEncThreads, smem);
         if (occ <= 0)
             return ECC_ERR_CUDA;
         const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, acc);
         encode_batched_kernel<<<(unsigned)grid, kEncThreads, smem, st>>>((uint8_t *)ws, t_start);
     } else {
-        const size_t smem = kDecHeadBytes + (size_t)warps * stage;
+        const size_t smem = kDecHeadBytes + kBatchSlotBytes + (size_t)warps * stage;
         const int occ = occupancy((const void *)decode_batched_kernel, warps * 32, smem);
         if (occ <= 0)
             return ECC_ERR_CUDA;
