@@ -53,6 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--tensors", type=int, default=4096, help="batched workload: number of tensors")
     p.add_argument("--workload", choices=["gradient", "batched"], default="gradient",
                    help="gradient: the 2^30-byte tensor (default); batched: 4096 tensors in one launch each way")
     return p.parse_args(argv)
@@ -555,7 +556,7 @@ def run_batched(args):
     dev = torch.device("cuda", local)
     C = args.chunk
     S = args.subblock or ecc.default_subblock(C)
-    plan = batch_plan(4096)
+    plan = batch_plan(args.tensors)
     # four codebooks from warm-up tensors of the laws (device histograms)
     def counts(x):
         c = ecc.e4m3_histogram(x)
@@ -640,7 +641,7 @@ def run_batched(args):
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u8", "data": "synthetic",
-        "config": {"workload": "4096 tensors, sizes 2^U(12,23) B, laws {N(0,1), N(0,sigma), zero spike}, "
+        "config": {"workload": f"{len(plan)} tensors, sizes 2^U(12,23) B, laws {{N(0,1), N(0,sigma), zero spike}}, "
                                "codebooks {base QLC, adapted QLC, 2 fixed Huffman}", "bytes": total, "chunk": C,
                    "subblock": S, "step": "one batched encode + one batched decode launch"},
         "encode_gbs": total / enc_ms / 1e6, "decode_gbs": total / dec_ms / 1e6,
