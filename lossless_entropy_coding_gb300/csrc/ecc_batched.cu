@@ -1,10 +1,18 @@
 // ecc_batched.cu -- one-launch encode and decode of many tensors, each with
 // its own codebook and container sizes (the message regime of collective
 // communication: many tensors of very different sizes).  See ecc.h.
+//
+// The host orders the tensors by codebook (stable: equal codebooks keep the
+// caller's order) and lays their chunks end to end in that order.  A
+// prologue kernel writes item[i] = tensor << 32 | chunk for every position,
+// so a kernel finds its work with one load instead of a search, and a CTA
+// reloads its shared code tables only where the codebook changes (a few
+// times per launch) instead of at almost every chunk.
 
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <numeric>
 #include <vector>
 
 #include "ecc_device.cuh"
@@ -13,100 +21,120 @@
 namespace ecc {
 
 // Workspace layout (all offsets 16-byte aligned):
-//   header | descs[count] | prefix[count + 1] | done[count] | flags[total]
-// prefix[d] = first global work item of tensor d (chunks for encode, groups
-// of `warps` chunks for decode); flags = look-back words (encode only).
+//   header | descs[count] | prefix[count + 1] | done[count] | item[n_items] | flags[total_chunks]
+// descs are in workspace order (sorted by codebook); prefix[d] = first item
+// of tensor d; flags = look-back words (encode only).
 struct BatchHeader {
     uint32_t ticket;
     uint32_t count;
-    uint32_t warps;       // decode: chunks per work item
+    uint32_t warps;       // decode: chunks per group (warps per CTA)
     uint32_t stage_bytes;
     uint32_t max_C;
-    uint32_t nbuf; // encode: shared input buffers (2 = next chunk prefetched)
-    uint64_t total_items;
+    uint32_t encode;
+    uint64_t n_items;     // encode: chunks; decode: chunks, each codebook run padded to a multiple of warps
     uint64_t total_chunks;
-    uint64_t desc_off, prefix_off, done_off, flags_off;
+    uint64_t desc_off, prefix_off, done_off, item_off, flags_off;
 };
 
+constexpr uint64_t kNoItem = ~0ull; // item of a padding position
+
 struct BatchLayout {
-    size_t desc_off, prefix_off, done_off, flags_off, bytes;
+    size_t desc_off, prefix_off, done_off, item_off, flags_off, bytes;
 };
 
 static size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
 
-static BatchLayout layout_for(uint32_t count, uint64_t total_chunks)
+static BatchLayout layout_for(uint32_t count, uint64_t n_items, uint64_t flag_words)
 {
     BatchLayout L;
     L.desc_off = up16(sizeof(BatchHeader));
     L.prefix_off = up16(L.desc_off + (size_t)count * sizeof(ecc_desc));
     L.done_off = up16(L.prefix_off + ((size_t)count + 1) * sizeof(uint64_t));
-    L.flags_off = up16(L.done_off + (size_t)count * sizeof(uint32_t));
-    L.bytes = up16(L.flags_off + total_chunks * sizeof(uint64_t));
+    L.item_off = up16(L.done_off + (size_t)count * sizeof(uint32_t));
+    L.flags_off = up16(L.item_off + n_items * sizeof(uint64_t));
+    L.bytes = up16(L.flags_off + flag_words * sizeof(uint64_t));
     return L;
 }
 
-__device__ __forceinline__ uint32_t find_tensor(const uint64_t *prefix, uint32_t count, uint64_t item)
-{
-    // largest d with prefix[d] <= item (prefix is non-decreasing; empty
-    // tensors share a prefix with their successor and are skipped)
-    uint32_t lo = 0, hi = count; // invariant: prefix[lo] <= item < prefix[hi]
-    while (hi - lo > 1) {
-        const uint32_t mid = (lo + hi) >> 1;
-        if (prefix[mid] <= item)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    return lo;
-}
+__device__ __forceinline__ uint64_t chunks_of(const ecc_desc &d) { return (d.n + d.C - 1) >> (31 - __clz(d.C)); }
 
-__global__ void batch_prologue_kernel(uint8_t *ws, int encode)
+__global__ void batch_prologue_kernel(uint8_t *ws)
 {
-    BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
+    const BatchHeader *h = reinterpret_cast<const BatchHeader *>(ws);
     const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
+    const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
     uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
+    uint64_t *item = reinterpret_cast<uint64_t *>(ws + h->item_off);
     uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
+    const uint32_t count = h->count;
     const uint64_t i0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    for (uint64_t i = i0; i < h->count; i += stride) {
+    for (uint64_t i = i0; i < count; i += stride) {
         const ecc_desc &d = descs[i];
         *d.status = ECC_OK;
         done[i] = 0;
-        if (encode) {
+        if (h->encode) {
             *d.total_bits = 0;
             d.chunk_off[0] = 0;
         }
         if (d.t_done_ns && d.n == 0)
             *d.t_done_ns = 0;
     }
-    if (encode)
+    for (uint64_t i = i0; i < h->n_items; i += stride) {
+        // the tensor of position i: largest d with prefix[d] <= i (empty
+        // tensors share their successor's prefix and are passed over)
+        uint32_t lo = 0, hi = count;
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (prefix[mid] <= i)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const uint64_t c = i - prefix[lo];
+        item[i] = c < chunks_of(descs[lo]) ? ((uint64_t)lo << 32 | c) : kNoItem;
+    }
+    if (h->encode)
         for (uint64_t i = i0; i < h->total_chunks; i += stride)
             flags[i] = 0;
 }
 
-__device__ __forceinline__ void stamp_done(const ecc_desc &d, uint32_t *done, uint32_t k, uint64_t n_chunks,
-                                           uint32_t items)
+// ---------------------------------------------------------------- encode
+// Warp-specialised many-tensor encoder: the single-tensor kernel's body with
+// each claimed chunk's job taken from the item map and its descriptor.
+__global__ void __maxnreg__(96) encode_batched_ws_kernel(uint8_t *ws, uint64_t *t_start)
+{
+    BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
+    if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
+        *t_start = globaltimer();
+    EncBatch bt;
+    bt.ticket = &h->ticket;
+    bt.total = h->total_chunks;
+    bt.item = reinterpret_cast<const uint64_t *>(ws + h->item_off);
+    bt.descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
+    bt.flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
+    bt.done = reinterpret_cast<uint32_t *>(ws + h->done_off);
+    const EncJob none{};
+    encode_ws_body<true>(none, 0, nullptr, bt, h->stage_bytes, h->max_C, kWaitLimitNs);
+}
+
+__device__ __forceinline__ void stamp_done(const ecc_desc &d, uint32_t *done, uint32_t k)
 {
     if (!d.t_done_ns)
         return;
     __threadfence();
-    if (atomicAdd(done + k, items) + items == n_chunks)
+    if (atomicAdd(done + k, 1u) + 1u == chunks_of(d))
         *d.t_done_ns = globaltimer();
 }
 
-__device__ __forceinline__ EncJob batch_job(const ecc_desc &d, uint64_t *flags, const uint64_t *prefix, uint32_t k)
-{
-    return EncJob{d.in, d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits, d.total_bits,
-                  flags + prefix[k], d.status};
-}
-
-// Work items are claimed one ahead by thread 0, which also finds the item's
-// tensor (binary search over the prefix table) and copies its descriptor
-// into shared memory, so the other threads never wait on that search.
+// Single-slot many-tensor encoder, for chunk sizes whose two input buffers
+// and two stage slots exceed shared memory (C = 64 KiB).  Thread 0 claims
+// one chunk ahead into a shared slot and bulk-copies its input.
 struct BatchSlot {
     ecc_desc d;
-    uint64_t item;   // global work item (ticket)
-    uint32_t tensor; // index of the tensor it belongs to
+    uint64_t item;   // ticket
+    uint64_t c;      // chunk within its tensor
+    uint32_t tensor;
     uint32_t pad;
 };
 constexpr uint32_t kBatchSlotBytes = 2 * ((sizeof(BatchSlot) + 15) & ~15u);
@@ -117,183 +145,165 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
     BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
     const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
-    const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
+    const uint64_t *item = reinterpret_cast<const uint64_t *>(ws + h->item_off);
     uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
     uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
     const uint32_t stage_bytes = h->stage_bytes;
     const uint32_t cmax = h->max_C;
-    const uint32_t nbuf = h->nbuf;
+    const uint64_t total = h->total_chunks;
     BatchSlot *slot = reinterpret_cast<BatchSlot *>(smem + enc_shared_bytes());
     uint8_t *inbuf = smem + enc_shared_bytes() + kBatchSlotBytes;
-    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + (size_t)nbuf * cmax);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + cmax);
     const int tid = threadIdx.x;
     if (t_start && blockIdx.x == 0 && tid == 0)
         *t_start = globaltimer();
     if (tid == 0) {
-        sh.loaded = nullptr;
         mbar_init(&sh.bar[0], 1);
-        mbar_init(&sh.bar[1], 1);
         fence_mbar_init();
     }
     uint4 *st4 = reinterpret_cast<uint4 *>(stage);
     for (uint32_t i = tid; i < stage_bytes / 16; i += kEncThreads)
         st4[i] = make_uint4(0, 0, 0, 0);
-    // thread 0: claim the next chunk into slot q (and bulk-copy its input)
-    uint32_t pending = 0;
+    auto job_of = [&](const BatchSlot &s) {
+        const ecc_desc &d = s.d;
+        return EncJob{d.in,         d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits,
+                      d.total_bits, flags + (s.item - s.c), d.status};
+    };
+    // thread 0: claim the next chunk into slot q, and bulk-copy its input
+    bool pending = false;
     auto claim = [&](uint32_t q, bool copy) {
         const uint32_t t = atomicAdd(&h->ticket, 1u);
         slot[q].item = t;
-        if (t < h->total_chunks) {
-            const uint32_t k = find_tensor(prefix, h->count, t);
-            slot[q].tensor = k;
-            slot[q].d = descs[k];
+        if (t < total) {
+            const uint64_t m = item[t];
+            slot[q].tensor = (uint32_t)(m >> 32);
+            slot[q].c = m & 0xFFFFFFFFull;
+            slot[q].d = descs[m >> 32];
             if (copy) {
-                issue_chunk_input(batch_job(slot[q].d, flags, prefix, k), t - prefix[k],
-                                  inbuf + (size_t)q * cmax, &sh.bar[q]);
-                pending |= 1u << q;
+                issue_chunk_input(job_of(slot[q]), slot[q].c, inbuf, &sh.bar[0]);
+                pending = true;
             }
         }
     };
     if (tid == 0)
         claim(0, true);
     __syncthreads();
-    uint32_t b = 0, phase = 0;
+    uint32_t phase = 0;
     bool staging = true;
-    for (;;) {
-        const uint64_t t = slot[b].item;
-        if (t >= h->total_chunks)
+    const ecc_codebook *loaded = nullptr;
+    for (uint32_t b = 0;; b ^= 1) {
+        if (slot[b].item >= total)
             break;
-        const uint32_t k = slot[b].tensor;
-        const ecc_desc d = slot[b].d;
-        __syncthreads(); // every thread has read slot b before it is refilled
-        if (tid == 0 && nbuf == 2)
-            claim(b ^ 1, staging);
-        const uint64_t c = t - prefix[k];
-        const EncJob job = batch_job(d, flags, prefix, k);
-        const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
-        if (cb_ok && d.cb != sh.loaded) {
-            load_encode_lut(sh, d.cb);
+        const BatchSlot s = slot[b];
+        const EncJob job = job_of(s);
+        const bool cb_ok = s.d.cb->magic == ECC_CODEBOOK_MAGIC && s.d.cb->max_len <= ECC_MAX_CODE_LEN;
+        if (cb_ok && s.d.cb != loaded) {
+            __syncthreads(); // the previous chunk's lookups are done
+            load_encode_lut(sh, s.d.cb);
+            loaded = s.d.cb;
             __syncthreads();
-            if (tid == 0)
-                sh.loaded = d.cb;
         }
-        const uint32_t ib = nbuf == 2 ? b : 0u;
-        bool ok = staging && mbar_wait(&sh.bar[ib], (phase >> ib) & 1u, kWaitLimitNs);
+        bool ok = staging && mbar_wait(&sh.bar[0], phase, kWaitLimitNs);
         ok = __syncthreads_and(ok) != 0;
         if (ok) {
-            phase ^= 1u << ib;
+            phase ^= 1u;
             if (tid == 0)
-                pending &= ~(1u << ib);
+                pending = false;
         } else {
             if (staging && tid == 0)
-                set_status(d.status, ECC_ERR_TIMEOUT);
+                set_status(job.status, ECC_ERR_TIMEOUT);
             staging = false;
         }
         if (cb_ok) {
             if (ok)
-                encode_chunk<true>(sh, stage, stage_bytes, job, inbuf + (size_t)ib * cmax, c, kWaitLimitNs);
+                encode_chunk<true>(sh, stage, stage_bytes, job, inbuf, s.c, kWaitLimitNs);
             else
-                encode_chunk<false>(sh, stage, stage_bytes, job, nullptr, c, kWaitLimitNs);
+                encode_chunk<false>(sh, stage, stage_bytes, job, nullptr, s.c, kWaitLimitNs);
         } else if (tid < 32) {
             // keep the tensor's look-back moving; its status says why it is empty
             bool to;
-            const uint64_t pre = lookback(job.flags, c, 0, kWaitLimitNs, &to);
+            const uint64_t pre = lookback(job.flags, s.c, 0, kWaitLimitNs, &to);
             if (tid == 0) {
-                set_status(d.status, ECC_ERR_CODEBOOK);
-                d.chunk_off[c + 1] = pre;
+                set_status(job.status, ECC_ERR_CODEBOOK);
+                job.chunk_off[s.c + 1] = pre;
             }
         }
         if (tid == 0) {
-            stamp_done(d, done, k, (d.n + d.C - 1) / d.C, 1);
-            if (nbuf == 1)
-                claim(0, staging); // the single buffer is free again
+            stamp_done(s.d, done, s.tensor);
+            claim(b ^ 1, staging); // the input buffer is free again
         }
         __syncthreads();
-        if (nbuf == 2)
-            b ^= 1;
     }
-    if (tid == 0)
-        for (uint32_t q = 0; q < 2; ++q)
-            if (pending & (1u << q))
-                (void)mbar_wait(&sh.bar[q], (phase >> q) & 1u, kWaitLimitNs);
+    if (tid == 0 && pending)
+        (void)mbar_wait(&sh.bar[0], phase, kWaitLimitNs);
 }
 
+// ---------------------------------------------------------------- decode
+// Groups of `warps` consecutive items; CTA x decodes groups x, x + grid, ...
+// (warp w the group's item w), the schedule of the single-tensor decoder.
+// Codebook runs are padded to whole groups, so a group has one codebook and
+// every warp of a CTA meets the codebook changes at the same groups.
+template <int R>
 __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
     LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes);
-    BatchSlot *slot = reinterpret_cast<BatchSlot *>(smem + kDecHeadBytes);
-    __shared__ const ecc_codebook *loaded;
-    BatchHeader *h = reinterpret_cast<BatchHeader *>(ws);
+    const BatchHeader *h = reinterpret_cast<const BatchHeader *>(ws);
     const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
-    const uint64_t *prefix = reinterpret_cast<const uint64_t *>(ws + h->prefix_off);
+    const uint64_t *item = reinterpret_cast<const uint64_t *>(ws + h->item_off);
     uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
     const uint32_t stage_bytes = h->stage_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t warps = h->warps;
+    const uint32_t W = blockDim.x >> 5;
     if (t_start && blockIdx.x == 0 && threadIdx.x == 0)
         *t_start = globaltimer();
     if (lane == 0) {
         mbar_init(&bars[warp], 1);
         fence_mbar_init();
     }
-    auto claim = [&](uint32_t q) {
-        const uint32_t g = atomicAdd(&h->ticket, 1u);
-        slot[q].item = g;
-        if (g < h->total_items) {
-            const uint32_t k = find_tensor(prefix, h->count, g);
-            slot[q].tensor = k;
-            slot[q].d = descs[k];
-        }
-    };
-    if (threadIdx.x == 0) {
-        loaded = nullptr;
-        claim(0);
-    }
     __syncthreads();
-    WarpStage wst{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + kBatchSlotBytes + (size_t)warp * stage_bytes),
-                  stage_bytes, &bars[warp], 0};
-    for (uint32_t b = 0;; b ^= 1) {
-        const uint64_t g = slot[b].item;
-        if (g >= h->total_items)
-            break;
-        const uint32_t k = slot[b].tensor;
-        const ecc_desc d = slot[b].d;
-        __syncthreads(); // every thread has read slot b
-        if (threadIdx.x == 0)
-            claim(b ^ 1);
-        const uint64_t n_chunks = (d.n + d.C - 1) / d.C;
-        const uint64_t c = (g - prefix[k]) * warps + warp;
-        const bool cb_ok = d.cb->magic == ECC_CODEBOOK_MAGIC && d.cb->max_len <= ECC_MAX_CODE_LEN;
-        if (cb_ok && d.cb != loaded) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(d.cb->dec);
-            uint4 *dst = reinterpret_cast<uint4 *>(dec);
-            for (int i = threadIdx.x; i < (int)(kDecTableBytes / 16); i += blockDim.x)
-                dst[i] = src[i];
-            load_long_table(lt, d.cb);
-            __syncthreads();
-            if (threadIdx.x == 0)
-                loaded = d.cb;
-        }
-        if (c < n_chunks) {
-            if (cb_ok) {
-                DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
-                const uint32_t per_lane = (d.C >> (31 - __clz(d.S))) >> 5; // (C/S)/32
-                if (per_lane >= 4)
-                    decode_chunk<4>(job, dec, lt, wst, c, c + warps, n_chunks);
-                else if (per_lane >= 2)
-                    decode_chunk<2>(job, dec, lt, wst, c, c + warps, n_chunks);
-                else
-                    decode_chunk<1>(job, dec, lt, wst, c, c + warps, n_chunks);
-            } else if (lane == 0) {
-                set_status(d.status, ECC_ERR_CODEBOOK);
+    WarpStage wst{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * stage_bytes), stage_bytes,
+                  &bars[warp], 0};
+    const uint64_t groups = h->n_items / W;
+    const ecc_codebook *loaded = nullptr;
+    bool loaded_ok = false;
+    for (uint64_t g = blockIdx.x; g < groups; g += gridDim.x) {
+        const uint64_t m0 = item[g * W]; // a group never starts on padding
+        const uint64_t m = item[g * W + warp];
+        const ecc_codebook *cb = descs[m0 >> 32].cb;
+        if (cb != loaded) {
+            __syncthreads(); // every warp is done with the previous tables
+            loaded = cb;
+            loaded_ok = cb->magic == ECC_CODEBOOK_MAGIC && cb->max_len <= ECC_MAX_CODE_LEN;
+            if (loaded_ok) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(cb->dec);
+                uint4 *dst = reinterpret_cast<uint4 *>(dec);
+                for (int i = threadIdx.x; i < (int)(kDecTableBytes / 16); i += blockDim.x)
+                    dst[i] = src[i];
+                load_long_table(lt, cb);
             }
-            if (lane == 0)
-                stamp_done(d, done, k, n_chunks, 1);
+            __syncthreads();
         }
-        __syncthreads();
+        if (m == kNoItem)
+            continue;
+        const uint32_t k = (uint32_t)(m >> 32);
+        const uint64_t c = m & 0xFFFFFFFFull;
+        const ecc_desc &d = descs[k];
+        const uint64_t nch = chunks_of(d);
+        if (loaded_ok) {
+            const DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
+            decode_chunk<R>(job, dec, lt, wst, c, nch, nch); // next chunk is another tensor's: no L2 prefetch
+        } else if (lane == 0) {
+            set_status(d.status, ECC_ERR_CODEBOOK);
+        }
+        if (d.t_done_ns) {
+            __threadfence(); // this lane's output stores before the completion count
+            __syncwarp();
+            if (lane == 0 && atomicAdd(done + k, 1u) + 1u == nch)
+                *d.t_done_ns = globaltimer();
+        }
     }
 }
 
@@ -303,67 +313,105 @@ using namespace ecc;
 
 namespace {
 
-ecc_status check_descs(const ecc_desc *descs, uint32_t count, bool encode, uint64_t *total_chunks, uint32_t *max_C)
+constexpr uint64_t kMaxItems = 1ull << 31; // tickets are 32-bit
+
+struct BatchPlan {
+    std::vector<uint32_t> order; // workspace position -> caller's index
+    std::vector<uint64_t> prefix;
+    uint64_t n_items = 0, total_chunks = 0;
+    uint32_t max_C = 1024, warps = 1, stage = 0;
+    int R = 4; // decode: streams per lane, the smallest any tensor allows
+};
+
+uint32_t batch_decode_warps(uint32_t stage)
+{
+    int warps = decode_warps(stage);
+    while (warps > 1 && kDecHeadBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve)
+        --warps;
+    return (uint32_t)warps;
+}
+
+ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool check, BatchPlan *P)
 {
     if (!descs || count == 0)
         return ECC_ERR_ARG;
-    uint64_t tot = 0;
-    uint32_t mc = 1024;
     for (uint32_t i = 0; i < count; ++i) {
         const ecc_desc &d = descs[i];
-        if (!valid_sizes(d.C, d.S) || !d.cb || !aligned16(d.cb) || !d.status || !d.chunk_off)
+        if (check) {
+            if (!valid_sizes(d.C, d.S) || !d.cb || !aligned16(d.cb) || !d.status || !d.chunk_off)
+                return ECC_ERR_ARG;
+            if (encode && !d.total_bits)
+                return ECC_ERR_ARG;
+            if (d.n && (!d.in || !d.out || !d.sub_bits || !aligned16(d.in) || !aligned16(d.out)))
+                return ECC_ERR_ARG;
+        } else if (!valid_sizes(d.C, d.S)) {
+            continue;
+        }
+        const uint64_t nc = ecc_num_chunks(d.n, d.C);
+        if (nc >= kMaxItems)
             return ECC_ERR_ARG;
-        if (encode && !d.total_bits)
-            return ECC_ERR_ARG;
-        if (d.n && (!d.in || !d.out || !d.sub_bits || !aligned16(d.in) || !aligned16(d.out)))
-            return ECC_ERR_ARG;
-        tot += ecc_num_chunks(d.n, d.C);
-        mc = std::max(mc, d.C);
+        P->total_chunks += nc;
+        P->max_C = std::max(P->max_C, d.C);
+        if (d.n)
+            P->R = std::min<int>(P->R, (int)std::max<uint32_t>(1, d.C / d.S / 32));
     }
-    *total_chunks = tot;
-    *max_C = mc;
+    P->stage = stage_bytes_for(P->max_C);
+    P->warps = batch_decode_warps(P->stage);
+    P->R = P->R >= 4 ? 4 : P->R >= 2 ? 2 : 1;
+    P->order.resize(count);
+    std::iota(P->order.begin(), P->order.end(), 0u);
+    std::stable_sort(P->order.begin(), P->order.end(), [&](uint32_t a, uint32_t b) {
+        return reinterpret_cast<uintptr_t>(descs[a].cb) < reinterpret_cast<uintptr_t>(descs[b].cb);
+    });
+    P->prefix.assign((size_t)count + 1, 0);
+    uint64_t acc = 0;
+    for (uint32_t j = 0; j < count; ++j) {
+        const ecc_desc &d = descs[P->order[j]];
+        // decode: pad each codebook run to whole groups
+        if (!encode && j > 0 && d.cb != descs[P->order[j - 1]].cb)
+            acc = (acc + P->warps - 1) / P->warps * P->warps;
+        P->prefix[j] = acc;
+        acc += valid_sizes(d.C, d.S) ? ecc_num_chunks(d.n, d.C) : 0;
+    }
+    if (!encode)
+        acc = (acc + P->warps - 1) / P->warps * P->warps;
+    P->prefix[count] = acc;
+    P->n_items = acc;
+    if (acc >= kMaxItems)
+        return ECC_ERR_ARG;
     return ECC_OK;
 }
 
 ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes, uint64_t *t_start,
                        void *stream, bool encode)
 {
-    uint64_t total_chunks;
-    uint32_t max_C;
-    ecc_status e = check_descs(descs, count, encode, &total_chunks, &max_C);
+    BatchPlan P;
+    ecc_status e = plan_batch(descs, count, encode, true, &P);
     if (e != ECC_OK)
         return e;
-    BatchLayout L = layout_for(count, total_chunks);
+    const BatchLayout L = layout_for(count, P.n_items, encode ? P.total_chunks : 0);
     if (!ws || !aligned16(ws) || ws_bytes < L.bytes)
         return ECC_ERR_ARG;
-    const uint32_t stage = stage_bytes_for(max_C);
-    int warps = decode_warps(stage);
-    while (warps > 1 && kDecHeadBytes + kBatchSlotBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve)
-        --warps;
     // host image of header | descs | prefix, copied with one async copy
     std::vector<uint8_t> img(L.done_off, 0);
     BatchHeader *h = reinterpret_cast<BatchHeader *>(img.data());
     h->ticket = 0;
     h->count = count;
-    h->warps = (uint32_t)warps;
-    h->stage_bytes = stage;
-    h->max_C = max_C;
-    h->nbuf = enc_input_buffers(max_C);
-    h->total_chunks = total_chunks;
+    h->warps = P.warps;
+    h->stage_bytes = P.stage;
+    h->max_C = P.max_C;
+    h->encode = encode ? 1u : 0u;
+    h->n_items = P.n_items;
+    h->total_chunks = P.total_chunks;
     h->desc_off = L.desc_off;
     h->prefix_off = L.prefix_off;
     h->done_off = L.done_off;
+    h->item_off = L.item_off;
     h->flags_off = L.flags_off;
-    std::memcpy(img.data() + L.desc_off, descs, (size_t)count * sizeof(ecc_desc));
-    uint64_t *prefix = reinterpret_cast<uint64_t *>(img.data() + L.prefix_off);
-    uint64_t acc = 0;
-    for (uint32_t i = 0; i < count; ++i) {
-        prefix[i] = acc;
-        const uint64_t nc = ecc_num_chunks(descs[i].n, descs[i].C);
-        acc += encode ? nc : (nc + warps - 1) / warps;
-    }
-    prefix[count] = acc;
-    h->total_items = acc;
+    ecc_desc *sorted = reinterpret_cast<ecc_desc *>(img.data() + L.desc_off);
+    for (uint32_t j = 0; j < count; ++j)
+        sorted[j] = descs[P.order[j]];
+    std::memcpy(img.data() + L.prefix_off, P.prefix.data(), P.prefix.size() * sizeof(uint64_t));
     cudaStream_t st = (cudaStream_t)stream;
     if (cudaMemcpyAsync(ws, img.data(), img.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
         return launch_status(cudaErrorUnknown);
@@ -371,29 +419,47 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     if (sms <= 0)
         return ECC_ERR_CUDA;
     {
-        const uint64_t work = std::max<uint64_t>(count, encode ? total_chunks : 0);
+        const uint64_t work = std::max<uint64_t>(count, P.n_items);
         const uint64_t nb = std::max<uint64_t>(1, std::min<uint64_t>((work + 255) / 256, 1024));
-        batch_prologue_kernel<<<(unsigned)nb, 256, 0, st>>>((uint8_t *)ws, encode ? 1 : 0);
+        batch_prologue_kernel<<<(unsigned)nb, 256, 0, st>>>((uint8_t *)ws);
         if ((e = launch_status(cudaGetLastError())) != ECC_OK)
             return e;
     }
-    if (acc == 0)
+    if (P.n_items == 0)
         return ECC_OK;
     if (encode) {
-        const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)h->nbuf * max_C + stage;
+        const size_t ws_smem = enc_ws_smem_bytes(P.max_C, P.stage);
+        const int occ_ws = ws_smem <= kMaxDynSmem - kStaticSmemReserve
+                               ? occupancy((const void *)encode_batched_ws_kernel, kEncThreadsWS, ws_smem)
+                               : 0;
+        if (occ_ws > 0) {
+            const uint64_t grid = std::min<uint64_t>((uint64_t)occ_ws * sms, P.n_items);
+            encode_batched_ws_kernel<<<(unsigned)grid, kEncThreadsWS, ws_smem, st>>>((uint8_t *)ws, t_start);
+            return launch_status(cudaGetLastError());
+        }
+        const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)P.max_C + P.stage;
         const int occ = occupancy((const void *)encode_batched_kernel, kEncThreads, smem);
         if (occ <= 0)
             return ECC_ERR_CUDA;
-        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, acc);
+        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, P.n_items);
         encode_batched_kernel<<<(unsigned)grid, kEncThreads, smem, st>>>((uint8_t *)ws, t_start);
-    } else {
-        const size_t smem = kDecHeadBytes + kBatchSlotBytes + (size_t)warps * stage;
-        const int occ = occupancy((const void *)decode_batched_kernel, warps * 32, smem);
-        if (occ <= 0)
-            return ECC_ERR_CUDA;
-        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, acc);
-        decode_batched_kernel<<<(unsigned)grid, warps * 32, smem, st>>>((uint8_t *)ws, t_start);
+        return launch_status(cudaGetLastError());
     }
+    const size_t smem = kDecHeadBytes + (size_t)P.warps * P.stage;
+    const void *kfn = P.R == 4 ? (const void *)decode_batched_kernel<4>
+                      : P.R == 2 ? (const void *)decode_batched_kernel<2>
+                                 : (const void *)decode_batched_kernel<1>;
+    const int occ = occupancy(kfn, (int)P.warps * 32, smem);
+    if (occ <= 0)
+        return ECC_ERR_CUDA;
+    const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, P.n_items / P.warps);
+    const unsigned threads = P.warps * 32;
+    if (P.R == 4)
+        decode_batched_kernel<4><<<(unsigned)grid, threads, smem, st>>>((uint8_t *)ws, t_start);
+    else if (P.R == 2)
+        decode_batched_kernel<2><<<(unsigned)grid, threads, smem, st>>>((uint8_t *)ws, t_start);
+    else
+        decode_batched_kernel<1><<<(unsigned)grid, threads, smem, st>>>((uint8_t *)ws, t_start);
     return launch_status(cudaGetLastError());
 }
 
@@ -403,12 +469,12 @@ extern "C" {
 
 size_t ecc_batched_workspace_bytes(const ecc_desc *descs, uint32_t count)
 {
-    if (!descs || !count)
+    // room for both directions: encode needs the look-back words, decode
+    // the padded item map
+    BatchPlan pe, pd;
+    if (plan_batch(descs, count, true, false, &pe) != ECC_OK || plan_batch(descs, count, false, false, &pd) != ECC_OK)
         return 0;
-    uint64_t tot = 0;
-    for (uint32_t i = 0; i < count; ++i)
-        tot += ecc_num_chunks(descs[i].n, descs[i].C ? descs[i].C : 1);
-    return layout_for(count, tot).bytes;
+    return std::max(layout_for(count, pe.n_items, pe.total_chunks).bytes, layout_for(count, pd.n_items, 0).bytes);
 }
 
 ecc_status ecc_encode_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes, uint64_t *t_start_ns,

@@ -267,26 +267,6 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t n, bool p)
 }
 
 // ---------------------------------------------------------------- encoder
-// Shared state of one encoder CTA.  lut holds one replica of the 256 encode
-// entries per bank: entry s for lane l is lut[s * 32 + l], so the 32 lanes of
-// a warp always hit 32 different banks whatever bytes they look up.
-struct EncShared {
-    uint32_t lut[kLutRows * 32];
-    alignas(16) uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
-    uint64_t prefix;
-    uint64_t bar[2];            // input-buffer mbarriers
-    uint64_t slot_chunk[2];     // warp-specialised encoder: chunk in each stage slot
-    uint32_t slot_bits[2];      // its payload bits
-    uint32_t slot_flags[2];     // bit 0: staging overflow
-    uint32_t tk[2];             // tickets of the current and the next chunk
-    const ecc_codebook *loaded; // codebook currently in lut
-    uint32_t ticket;
-    uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
-    uint32_t pad[2];
-};
-
-__host__ __device__ constexpr uint32_t enc_shared_bytes() { return (sizeof(EncShared) + 15u) & ~15u; }
-
 struct EncJob {
     const uint8_t *in;
     uint64_t n;
@@ -300,6 +280,37 @@ struct EncJob {
     uint64_t *flags;
     uint32_t *status;
 };
+
+// One chunk claimed by the warp-specialised encoder.
+struct EncSlot {
+    EncJob job;       // many-tensor kernel: the chunk's tensor (flags already offset to it)
+    uint64_t c;       // chunk index within its tensor
+    uint64_t *t_done; // many-tensor kernel: the tensor's completion stamp (may be null)
+    uint32_t tensor;  // many-tensor kernel: tensor index (completion counters)
+    uint32_t state;   // kSlotEnd: no more work; kSlotChunk; kSlotBadCodebook
+};
+constexpr uint32_t kSlotEnd = 0, kSlotChunk = 1, kSlotBadCodebook = 2;
+constexpr uint32_t kEncSlots = 4; // claimed two chunks ahead: slots k .. k + 2 live at once
+
+// Shared state of one encoder CTA.  lut holds one replica of the 256 encode
+// entries per bank: entry s for lane l is lut[s * 32 + l], so the 32 lanes of
+// a warp always hit 32 different banks whatever bytes they look up.
+struct EncShared {
+    uint32_t lut[kLutRows * 32];
+    alignas(16) uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
+    uint64_t prefix;
+    uint64_t bar[2];            // input-buffer mbarriers
+    uint32_t slot_bits[2];      // warp-specialised encoder: payload bits of the chunk in each stage slot
+    uint32_t slot_flags[2];     // bit 0: staging overflow
+    uint32_t issued[2];         // bulk copies issued into each input buffer
+    uint32_t nostage;           // set once a copy timed out: issue no more copies
+    const ecc_codebook *loaded; // codebook currently in lut
+    uint32_t ticket;
+    uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
+    EncSlot slot[kEncSlots];
+};
+
+__host__ __device__ constexpr uint32_t enc_shared_bytes() { return (sizeof(EncShared) + 15u) & ~15u; }
 
 __device__ __forceinline__ void load_encode_lut(EncShared &sh, const ecc_codebook *cb)
 {
@@ -399,16 +410,18 @@ struct Packer {
 // consecutive pairs.  Returns the bit total; sets *slow if some symbol has
 // no packed entry (a code longer than 26 bits or a byte without code) or the
 // group is partial, *bad if some byte has no code at all.
-__device__ __forceinline__ uint32_t lookup16(const EncShared &sh, uint4 v, uint32_t cnt, const ecc_codebook *cb,
+// lut points at entry 0 of this thread's replica: entry s is lut[s * kStride]
+// (the shared bank-replicated table: sh.lut + lane, stride 32; the codebook's
+// own enc[] in global memory: stride 1).
+template <int kStride>
+__device__ __forceinline__ uint32_t lookup16(const uint32_t *lut, uint4 v, uint32_t cnt, const ecc_codebook *cb,
                                              uint32_t e[16], uint32_t pl[8], bool *slow, bool *bad)
 {
-    const int lane = threadIdx.x & 31;
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    const uint32_t *lut = sh.lut + lane;
     uint32_t emin = ~0u;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        e[j] = lut[byte_of(wv[j >> 2], j & 3) * 32];
+        e[j] = lut[byte_of(wv[j >> 2], j & 3) * kStride];
         emin = min(emin, e[j]);
     }
     uint32_t bits = 0;
@@ -497,7 +510,7 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
     const uint4 v = cnt ? load_symbols<kSharedSrc>(src + my0, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
     uint32_t e[16], pl[8];
     bool slow, bad;
-    const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, pl, &slow, &bad);
+    const uint32_t bits = lookup16<32>(sh.lut + lane, v, cnt, job.cb, e, pl, &slow, &bad);
     *bad_out |= bad;
 
     uint32_t incl = bits;
@@ -625,6 +638,9 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
 // Re-encode chunk c with one warp straight into global memory at dst (the
 // chunk's place in the output, `words` 32-bit words, zeroed here first):
 // the path for chunks whose payload outgrew the shared staging buffer.
+// kGlobalLut: look codes up in the codebook's enc[] in global memory instead
+// of the shared table (which the compute warps may be reloading meanwhile).
+template <bool kGlobalLut>
 static __device__ __noinline__ void encode_chunk_warp(const EncShared &sh, const EncJob &job, uint64_t c,
                                                       uint32_t *dst, uint32_t words)
 {
@@ -641,7 +657,8 @@ static __device__ __noinline__ void encode_chunk_warp(const EncShared &sh, const
         const uint4 v = cnt ? load_symbols<false>(nullptr, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
         uint32_t e[16], pl[8];
         bool slow, bad;
-        const uint32_t bits = lookup16(sh, v, cnt, job.cb, e, pl, &slow, &bad);
+        const uint32_t bits = kGlobalLut ? lookup16<1>(job.cb->enc, v, cnt, job.cb, e, pl, &slow, &bad)
+                                         : lookup16<32>(sh.lut + lane, v, cnt, job.cb, e, pl, &slow, &bad);
         uint32_t incl = bits;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -670,6 +687,251 @@ __device__ __forceinline__ void issue_chunk_input(const EncJob &job, uint64_t c,
     mbar_expect_tx(bar, whole);
     if (whole)
         bulk_g2s(buf, job.in + base, whole, bar);
+}
+
+// ---------------------------------------------------------------- warp-specialised encoder
+// 8 compute warps encode chunk k into stage slot k % 2 and publish its
+// aggregate at once; one output warp resolves the chunk's offset (decoupled
+// look-back), writes the staged payload out and claims chunk k + 2 (ticket,
+// then a bulk copy of its input into the input buffer chunk k has just
+// released), while the compute warps already encode chunk k + 1.  Stage
+// slots are handed over with named barriers: kBarFull + slot (compute ->
+// output) and kBarEmpty + slot (output -> compute).  Claiming in the output
+// warp keeps the ticket's round trip off the compute warps' critical path.
+
+// Source of chunks of the many-tensor encoder: one ticket over the chunks of
+// all tensors (workspace order), item[t] = tensor << 32 | chunk.
+struct EncBatch {
+    uint32_t *ticket;
+    uint64_t total;
+    const uint64_t *item;
+    const ecc_desc *descs;
+    uint64_t *flags; // look-back words, one per ticket
+    uint32_t *done;  // chunks finished, per tensor
+};
+
+__device__ __forceinline__ void claim_single(EncSlot &s, uint32_t *ticket, uint64_t n_chunks)
+{
+    const uint32_t t = atomicAdd(ticket, 1u);
+    s.c = t;
+    s.state = t < n_chunks ? kSlotChunk : kSlotEnd;
+}
+
+__device__ __forceinline__ void claim_batched(EncSlot &s, const EncBatch &bt)
+{
+    const uint32_t t = atomicAdd(bt.ticket, 1u);
+    if (t >= bt.total) {
+        s.state = kSlotEnd;
+        return;
+    }
+    const uint64_t m = bt.item[t];
+    const uint32_t k = (uint32_t)(m >> 32);
+    const uint64_t c = m & 0xFFFFFFFFull;
+    const ecc_desc &d = bt.descs[k];
+    const ecc_codebook *cb = d.cb;
+    s.job = EncJob{d.in,     d.n,        cb,           d.C,  d.S, d.out, d.cap, d.chunk_off, d.sub_bits,
+                   d.total_bits, bt.flags + (t - c), d.status};
+    s.c = c;
+    s.t_done = d.t_done_ns;
+    s.tensor = k;
+    s.state = (cb->magic == ECC_CODEBOOK_MAGIC && cb->max_len <= ECC_MAX_CODE_LEN) ? kSlotChunk : kSlotBadCodebook;
+}
+
+// kBatched: chunks of many tensors from bt (each chunk's job in its slot);
+// else the chunks of `single`, claimed with `ticket`.  Shared memory: EncShared
+// | 2 input buffers of cmax bytes | 2 stage slots of stage_bytes.
+__host__ __device__ constexpr size_t enc_ws_smem_bytes(uint32_t cmax, uint32_t stage_bytes)
+{
+    return enc_shared_bytes() + 2 * (size_t)cmax + 2 * (size_t)stage_bytes;
+}
+
+template <bool kBatched>
+__device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_chunks, uint32_t *ticket,
+                                               const EncBatch &bt, uint32_t stage_bytes, uint32_t cmax,
+                                               uint64_t timeout_ns)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    EncShared &sh = *reinterpret_cast<EncShared *>(smem);
+    uint8_t *inbuf = smem + enc_shared_bytes();
+    uint32_t *stage0 = reinterpret_cast<uint32_t *>(inbuf + 2 * (size_t)cmax);
+    const uint32_t slot_words = stage_bytes / 4;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (!kBatched && (single.cb->magic != ECC_CODEBOOK_MAGIC || single.cb->max_len > ECC_MAX_CODE_LEN)) {
+        if (tid == 0 && blockIdx.x == 0)
+            set_status(single.status, ECC_ERR_CODEBOOK);
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(&sh.bar[0], 1);
+        mbar_init(&sh.bar[1], 1);
+        fence_mbar_init();
+        sh.issued[0] = sh.issued[1] = 0;
+        sh.nostage = 0;
+    }
+    if (!kBatched)
+        load_encode_lut(sh, single.cb);
+    {
+        uint4 *st4 = reinterpret_cast<uint4 *>(stage0);
+        for (uint32_t i = tid; i < 2 * stage_bytes / 16; i += kEncThreadsWS)
+            st4[i] = make_uint4(0, 0, 0, 0);
+    }
+    // one thread: claim the chunk of iteration k into slot k % 4 and, unless
+    // staging was given up, bulk-copy its input into buffer k % 2
+    auto claim = [&](uint32_t k) {
+        EncSlot &s = sh.slot[k % kEncSlots];
+        if (kBatched)
+            claim_batched(s, bt);
+        else
+            claim_single(s, ticket, n_chunks);
+        if (s.state != kSlotEnd && !sh.nostage) {
+            issue_chunk_input(kBatched ? s.job : single, s.c, inbuf + (size_t)(k & 1) * cmax, &sh.bar[k & 1]);
+            ++sh.issued[k & 1];
+        }
+    };
+    if (tid == 0) {
+        claim(0);
+        if (sh.slot[0].state != kSlotEnd)
+            claim(1);
+        else
+            sh.slot[1].state = kSlotEnd;
+    }
+    __syncthreads(); // the last CTA-wide barrier before the warps split
+
+    uint32_t consumed[2] = {0, 0}; // compute warps: copies waited for, per input buffer
+    if (warp == kEncWarps) { // ---------------- output warp
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t b = k & 1;
+            bar_sync(kBarFull + b, kEncThreadsWS);
+            const EncSlot &s = sh.slot[k % kEncSlots];
+            if (s.state == kSlotEnd)
+                break;
+            if (lane == 0) { // chunk k's input buffer is free: claim chunk k + 2 into it
+                if (sh.slot[(k + 1) % kEncSlots].state != kSlotEnd)
+                    claim(k + 2);
+                else
+                    sh.slot[(k + 2) % kEncSlots].state = kSlotEnd;
+            }
+            const EncJob &job = kBatched ? s.job : single;
+            const uint64_t c = s.c;
+            const uint32_t run = sh.slot_bits[b];
+            const uint32_t fl = sh.slot_flags[b];
+            const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
+            bool to = false;
+            const uint64_t prefix = c == 0 ? 0 : resolve_prefix(job.flags, c, bytes, timeout_ns, &to);
+            const bool fits = prefix + bytes <= job.out_cap;
+            if (lane == 0) {
+                job.chunk_off[c + 1] = prefix + bytes;
+                if (c == 0)
+                    job.chunk_off[0] = 0;
+                atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)run);
+                if (to)
+                    set_status(job.status, ECC_ERR_TIMEOUT);
+                else if (!fits)
+                    set_status(job.status, ECC_ERR_CAPACITY);
+            }
+            uint4 *st4 = reinterpret_cast<uint4 *>(stage0 + b * slot_words);
+            const uint32_t nvec = (uint32_t)(bytes / 16);
+            const bool write = fits && !to;
+            if (!(fl & 1u)) {
+                uint4 *dst = reinterpret_cast<uint4 *>(job.out + prefix);
+#pragma unroll 4
+                for (uint32_t i = lane; i < nvec; i += 32) {
+                    const uint4 w = st4[i];
+                    st4[i] = make_uint4(0, 0, 0, 0);
+                    if (write)
+                        st_stream16(dst + i, w);
+                }
+            } else {
+                for (uint32_t i = lane; i < stage_bytes / 16; i += 32)
+                    st4[i] = make_uint4(0, 0, 0, 0);
+                if (write)
+                    encode_chunk_warp<kBatched>(sh, job, c, reinterpret_cast<uint32_t *>(job.out + prefix), nvec * 4);
+            }
+            if (kBatched && s.t_done) {
+                __threadfence(); // this lane's payload stores before the completion count
+                __syncwarp();
+                if (lane == 0) {
+                    const uint64_t nch = (job.n + job.C - 1) >> (31 - __clz(job.C));
+                    if (atomicAdd(bt.done + s.tensor, 1u) + 1u == nch)
+                        *s.t_done = globaltimer();
+                }
+            }
+            bar_arrive(kBarEmpty + b, kEncThreadsWS);
+        }
+    } else { // ---------------- compute warps
+        bool staging = true;
+        const ecc_codebook *loaded = kBatched ? nullptr : single.cb;
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t b = k & 1;
+            if (k >= 2)
+                bar_sync(kBarEmpty + b, kEncThreadsWS);
+            const EncSlot &s = sh.slot[k % kEncSlots];
+            const uint32_t state = s.state;
+            if (state == kSlotEnd) {
+                bar_arrive(kBarFull + b, kEncThreadsWS);
+                if (k >= 1)
+                    bar_sync(kBarEmpty + (b ^ 1), kEncThreadsWS);
+                break;
+            }
+            const EncJob &job = kBatched ? s.job : single;
+            const uint64_t c = s.c;
+            if (tid == 0)
+                sh.slot_flags[b] = 0;
+            if (kBatched && state == kSlotChunk && job.cb != loaded) {
+                // every compute warp is past the last lookup of the previous
+                // chunk (its final tile barrier); the output warp's overflow
+                // path reads the codebook in global memory
+                load_encode_lut(sh, job.cb);
+                loaded = job.cb;
+                bar_sync(kBarCompute, kEncThreads);
+            }
+            bool ok = staging && mbar_wait(&sh.bar[b], consumed[b] & 1u, timeout_ns);
+            ok = bar_red_and(kBarCompute, kEncThreads, ok);
+            if (ok) {
+                ++consumed[b];
+            } else {
+                if (staging && tid == 0) {
+                    set_status(job.status, ECC_ERR_TIMEOUT);
+                    sh.nostage = 1;
+                }
+                staging = false;
+            }
+            uint32_t *stage = stage0 + b * slot_words;
+            const uint64_t base = c * job.C;
+            const uint32_t L = state == kSlotChunk ? (uint32_t)min((uint64_t)job.C, job.n - base) : 0u;
+            const uint8_t *src = inbuf + (size_t)b * cmax;
+            bool bad = state == kSlotBadCodebook;
+            uint32_t run = 0;
+            for (uint32_t t0 = 0; t0 < L; t0 += kTile) {
+                if (ok)
+                    run += encode_tile<true, true, true>(sh, job, src, base, L, t0, run, stage, stage_bytes * 8u, true,
+                                                         &bad, &sh.slot_flags[b]);
+                else
+                    run += encode_tile<true, false, true>(sh, job, nullptr, base, L, t0, run, stage, stage_bytes * 8u,
+                                                          true, &bad, &sh.slot_flags[b]);
+            }
+            if (bad)
+                set_status(job.status, ECC_ERR_CODEBOOK);
+            if (tid == 0) {
+                const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
+                st_relaxed(job.flags + c, (c == 0 ? kFlagPrefix : kFlagAggregate) | (bytes & kValueMask));
+                sh.slot_bits[b] = run;
+            }
+            // each thread's packing writes precede its arrival; the output warp
+            // waits for all 256 arrivals
+            bar_arrive(kBarFull + b, kEncThreadsWS);
+        }
+    }
+    // never exit with a bulk copy still writing into this CTA's shared memory
+    // (only after a timed-out wait can an issued copy be left unconsumed)
+    __syncthreads();
+    if (tid == 0)
+        for (uint32_t q = 0; q < 2; ++q)
+            while (consumed[q] < sh.issued[q]) {
+                if (!mbar_wait(&sh.bar[q], consumed[q] & 1u, timeout_ns))
+                    break;
+                ++consumed[q];
+            }
 }
 
 // ---------------------------------------------------------------- decoder

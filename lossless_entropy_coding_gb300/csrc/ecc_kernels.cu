@@ -162,169 +162,12 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(EncParams p)
                 (void)mbar_wait(&sh.bar[k], (phase >> k) & 1u, p.timeout_ns);
 }
 
-// Warp-specialised encoder: 8 compute warps encode chunk k into stage slot
-// k & 1 and publish its aggregate at once; one output warp resolves the
-// chunk's offset (decoupled look-back) and writes the staged payload out,
-// while the compute warps already encode chunk k + 1 into the other slot.
-// Slots are handed over with named barriers: kBarFull + slot (compute ->
-// output) and kBarEmpty + slot (output -> compute).
+// Warp-specialised encoder over one tensor: see encode_ws_body.  At most 96
+// registers a thread, so that two 288-thread CTAs fit one SM.
 __global__ void __maxnreg__(96) encode_ws_kernel(EncParams p)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    EncShared &sh = *reinterpret_cast<EncShared *>(smem);
-    uint8_t *inbuf = smem + enc_shared_bytes();
-    uint32_t *stage0 = reinterpret_cast<uint32_t *>(inbuf + (size_t)p.nbuf * p.job.C);
-    const uint32_t slot_words = p.stage_bytes / 4;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const EncJob &job = p.job;
-    if (job.cb->magic != ECC_CODEBOOK_MAGIC || job.cb->max_len > ECC_MAX_CODE_LEN) {
-        if (tid == 0 && blockIdx.x == 0)
-            set_status(job.status, ECC_ERR_CODEBOOK);
-        return;
-    }
-    if (tid == 0) {
-        mbar_init(&sh.bar[0], 1);
-        mbar_init(&sh.bar[1], 1);
-        fence_mbar_init();
-    }
-    load_encode_lut(sh, job.cb);
-    {
-        uint4 *st4 = reinterpret_cast<uint4 *>(stage0);
-        for (uint32_t i = tid; i < 2 * p.stage_bytes / 16; i += kEncThreadsWS)
-            st4[i] = make_uint4(0, 0, 0, 0);
-    }
-    uint32_t pending = 0; // thread 0: input buffers with a copy not yet waited for
-    if (tid == 0) {
-        const uint32_t t = atomicAdd(p.ticket, 1u);
-        sh.tk[0] = t;
-        if (t < p.n_chunks) {
-            issue_chunk_input(job, t, inbuf, &sh.bar[0]);
-            pending = 1;
-        }
-    }
-    __syncthreads(); // the last CTA-wide barrier: the warps split below
-
-    if (warp == kEncWarps) { // ---------------- output warp
-        for (uint32_t k = 0;; ++k) {
-            const uint32_t b = k & 1;
-            bar_sync(kBarFull + b, kEncThreadsWS);
-            const uint64_t c = sh.slot_chunk[b];
-            if (c == ~0ull)
-                break;
-            const uint32_t run = sh.slot_bits[b];
-            const uint32_t fl = sh.slot_flags[b];
-            const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
-            bool to = false;
-            const uint64_t prefix = c == 0 ? 0 : resolve_prefix(job.flags, c, bytes, p.timeout_ns, &to);
-            const bool fits = prefix + bytes <= job.out_cap;
-            if (lane == 0) {
-                job.chunk_off[c + 1] = prefix + bytes;
-                if (c == 0)
-                    job.chunk_off[0] = 0;
-                atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)run);
-                if (to)
-                    set_status(job.status, ECC_ERR_TIMEOUT);
-                else if (!fits)
-                    set_status(job.status, ECC_ERR_CAPACITY);
-            }
-            uint4 *st4 = reinterpret_cast<uint4 *>(stage0 + b * slot_words);
-            const uint32_t nvec = (uint32_t)(bytes / 16);
-            const bool write = fits && !to;
-            if (!(fl & 1u)) {
-                uint4 *dst = reinterpret_cast<uint4 *>(job.out + prefix);
-#pragma unroll 4
-                for (uint32_t i = lane; i < nvec; i += 32) {
-                    const uint4 w = st4[i];
-                    st4[i] = make_uint4(0, 0, 0, 0);
-                    if (write)
-                        st_stream16(dst + i, w);
-                }
-            } else {
-                for (uint32_t i = lane; i < p.stage_bytes / 16; i += 32)
-                    st4[i] = make_uint4(0, 0, 0, 0);
-                if (write)
-                    encode_chunk_warp(sh, job, c, reinterpret_cast<uint32_t *>(job.out + prefix), nvec * 4);
-            }
-            bar_arrive(kBarEmpty + b, kEncThreadsWS);
-        }
-        return;
-    }
-
-    // ---------------- compute warps
-    uint32_t phase = 0;
-    bool staging = true;
-    for (uint32_t k = 0;; ++k) {
-        const uint32_t b = k & 1;
-        const uint64_t c = sh.tk[b];
-        if (k >= 2)
-            bar_sync(kBarEmpty + b, kEncThreadsWS);
-        if (c >= p.n_chunks) {
-            if (tid == 0)
-                sh.slot_chunk[b] = ~0ull;
-            bar_arrive(kBarFull + b, kEncThreadsWS);
-            if (k >= 1)
-                bar_sync(kBarEmpty + (b ^ 1), kEncThreadsWS);
-            break;
-        }
-        const uint32_t ib = p.nbuf == 2 ? b : 0u;
-        if (tid == 0) {
-            const uint32_t t = atomicAdd(p.ticket, 1u);
-            sh.tk[b ^ 1] = t;
-            sh.slot_flags[b] = 0;
-            if (t < p.n_chunks && p.nbuf == 2 && staging) {
-                issue_chunk_input(job, t, inbuf + (size_t)(b ^ 1) * job.C, &sh.bar[b ^ 1]);
-                pending |= 1u << (b ^ 1);
-            }
-        }
-        bool ok = staging && mbar_wait(&sh.bar[ib], (phase >> ib) & 1u, p.timeout_ns);
-        ok = bar_red_and(kBarCompute, kEncThreads, ok);
-        if (ok) {
-            phase ^= 1u << ib;
-            if (tid == 0)
-                pending &= ~(1u << ib);
-        } else {
-            if (staging && tid == 0)
-                set_status(job.status, ECC_ERR_TIMEOUT);
-            staging = false;
-        }
-        uint32_t *stage = stage0 + b * slot_words;
-        const uint64_t base = c * job.C;
-        const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
-        const uint8_t *src = inbuf + (size_t)ib * job.C;
-        bool bad = false;
-        uint32_t run = 0;
-        for (uint32_t t0 = 0; t0 < L; t0 += kTile) {
-            if (ok)
-                run += encode_tile<true, true, true>(sh, job, src, base, L, t0, run, stage, p.stage_bytes * 8u, true,
-                                                     &bad, &sh.slot_flags[b]);
-            else
-                run += encode_tile<true, false, true>(sh, job, nullptr, base, L, t0, run, stage, p.stage_bytes * 8u,
-                                                      true, &bad, &sh.slot_flags[b]);
-        }
-        if (bad)
-            set_status(job.status, ECC_ERR_CODEBOOK);
-        if (tid == 0) {
-            const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
-            st_relaxed(job.flags + c, (c == 0 ? kFlagPrefix : kFlagAggregate) | (bytes & kValueMask));
-            sh.slot_chunk[b] = c;
-            sh.slot_bits[b] = run;
-            if (p.nbuf == 1 && staging) {
-                const uint32_t t = sh.tk[b ^ 1];
-                if (t < p.n_chunks) {
-                    issue_chunk_input(job, t, inbuf, &sh.bar[0]);
-                    pending |= 1u;
-                }
-            }
-        }
-        // each thread's packing writes precede its arrival; the output warp
-        // waits for all 256 arrivals
-        bar_arrive(kBarFull + b, kEncThreadsWS);
-    }
-    // never exit with a bulk copy still writing into this CTA's shared memory
-    if (tid == 0)
-        for (uint32_t q = 0; q < 2; ++q)
-            if (pending & (1u << q))
-                (void)mbar_wait(&sh.bar[q], (phase >> q) & 1u, p.timeout_ns);
+    const EncBatch none{};
+    encode_ws_body<false>(p.job, p.n_chunks, p.ticket, none, p.stage_bytes, p.job.C, p.timeout_ns);
 }
 
 // ---------------------------------------------------------------- decode
@@ -525,19 +368,19 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     const int sms = sm_count();
     if (sms <= 0)
         return ECC_ERR_CUDA;
-    // warp-specialised kernel (two stage slots) when it fits, else the
-    // single-slot kernel
-    for (uint32_t nbuf = 2; nbuf >= 1; --nbuf) {
-        const size_t smem = enc_shared_bytes() + (size_t)nbuf * C + 2 * (size_t)p.stage_bytes;
-        if (smem > kMaxDynSmem - kStaticSmemReserve)
-            continue;
-        const int occ = occupancy((const void *)encode_ws_kernel, kEncThreadsWS, smem);
-        if (occ <= 0)
-            continue;
-        p.nbuf = nbuf;
-        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
-        encode_ws_kernel<<<(unsigned)grid, kEncThreadsWS, smem, st>>>(p);
-        return launch_status(cudaGetLastError());
+    // warp-specialised kernel (two input buffers, two stage slots) when it
+    // fits, else the single-slot kernel
+    {
+        const size_t smem = enc_ws_smem_bytes(C, p.stage_bytes);
+        const int occ = smem <= kMaxDynSmem - kStaticSmemReserve
+                            ? occupancy((const void *)encode_ws_kernel, kEncThreadsWS, smem)
+                            : 0;
+        if (occ > 0) {
+            p.nbuf = 2;
+            const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
+            encode_ws_kernel<<<(unsigned)grid, kEncThreadsWS, smem, st>>>(p);
+            return launch_status(cudaGetLastError());
+        }
     }
     p.nbuf = enc_input_buffers(C);
     const size_t smem = enc_shared_bytes() + (size_t)p.nbuf * C + p.stage_bytes;

@@ -76,3 +76,5 @@ def test_generators_are_seeded_and_shaped():
     plan = batch_plan(64)
     assert all(4096 <= s < 8 * 2 ** 20 for s, _, _ in plan)
     assert {law for _, law, _ in plan} <= {0, 1, 2} and {t for _, _, t in plan} <= {0, 1, 2, 3}
+    # each law is coded with a codebook fitted to that law
+    assert all(t in ((0,), (2,), (1, 3))[law] for _, law, t in plan)
