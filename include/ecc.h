@@ -92,7 +92,8 @@ typedef struct ecc_codebook {
     uint32_t reserved[3];
     uint64_t code[256];   /* code of each byte value, right-aligned */
     uint64_t first[64];   /* Huffman: first canonical code of each length */
-    uint32_t enc[256];    /* derived: (code << 5) | len if len <= 26, else 0 */
+    uint32_t enc_code[256]; /* derived: code << (32 - len) (first bit in bit 31) if 1 <= len <= 31, else 0 */
+    uint32_t enc_mul[256];  /* derived: 2^(32 - len) if 1 <= len <= 31, else 0 (the exact path codes it) */
     uint32_t area[8];     /* derived, QLC: per prefix k, start | len << 16 | width << 24 */
     uint16_t dec[16384];  /* derived: 14-bit peek -> byte | len << 8; 0 = not resolved */
     uint16_t count[64];   /* Huffman: number of codes of each length */

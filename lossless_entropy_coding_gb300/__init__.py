@@ -30,7 +30,7 @@ CODEBOOK_DTYPE = np.dtype([
     ("magic", "<u4"), ("family", "<u4"), ("max_len", "<u4"), ("min_len", "<u4"),
     ("n_coded", "<u4"), ("reserved", "<u4", (3,)),
     ("code", "<u8", (256,)), ("first", "<u8", (64,)),
-    ("enc", "<u4", (256,)), ("area", "<u4", (8,)), ("dec", "<u2", (16384,)),
+    ("enc_code", "<u4", (256,)), ("enc_mul", "<u4", (256,)), ("area", "<u4", (8,)), ("dec", "<u2", (16384,)),
     ("count", "<u2", (64,)), ("index", "<u2", (64,)),
     ("area_start", "<u2", (8,)), ("area_size", "<u2", (8,)),
     ("width", "u1", (8,)), ("len", "u1", (256,)), ("rank", "u1", (256,)),

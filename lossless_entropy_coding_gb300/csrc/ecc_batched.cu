@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
     const uint64_t total = h->total_chunks;
     BatchSlot *slot = reinterpret_cast<BatchSlot *>(smem + enc_shared_bytes());
     uint8_t *inbuf = smem + enc_shared_bytes() + kBatchSlotBytes;
-    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + cmax);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + cmax + kStageLead);
     const int tid = threadIdx.x;
     if (t_start && blockIdx.x == 0 && tid == 0)
         *t_start = globaltimer();
@@ -161,8 +161,8 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
         mbar_init(&sh.bar[0], 1);
         fence_mbar_init();
     }
-    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
-    for (uint32_t i = tid; i < stage_bytes / 16; i += kEncThreads)
+    uint4 *st4 = reinterpret_cast<uint4 *>(inbuf + cmax); // the guard word and the stage
+    for (uint32_t i = tid; i < (kStageLead + stage_bytes) / 16; i += kEncThreads)
         st4[i] = make_uint4(0, 0, 0, 0);
     auto job_of = [&](const BatchSlot &s) {
         const ecc_desc &d = s.d;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
         const bool cb_ok = s.d.cb->magic == ECC_CODEBOOK_MAGIC && s.d.cb->max_len <= ECC_MAX_CODE_LEN;
         if (cb_ok && s.d.cb != loaded) {
             __syncthreads(); // the previous chunk's lookups are done
-            load_encode_lut(sh, s.d.cb);
+            load_encode_lut(sh, s.d.cb, kEncThreads);
             loaded = s.d.cb;
             __syncthreads();
         }
@@ -437,7 +437,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
             encode_batched_ws_kernel<<<(unsigned)grid, kEncThreadsWS, ws_smem, st>>>((uint8_t *)ws, t_start);
             return launch_status(cudaGetLastError());
         }
-        const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)P.max_C + P.stage;
+        const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)P.max_C + kStageLead + P.stage;
         const int occ = occupancy((const void *)encode_batched_kernel, kEncThreads, smem);
         if (occ <= 0)
             return ECC_ERR_CUDA;

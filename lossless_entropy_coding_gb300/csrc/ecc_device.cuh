@@ -292,11 +292,14 @@ struct EncSlot {
 constexpr uint32_t kSlotEnd = 0, kSlotChunk = 1, kSlotBadCodebook = 2;
 constexpr uint32_t kEncSlots = 4; // claimed two chunks ahead: slots k .. k + 2 live at once
 
-// Shared state of one encoder CTA.  lut holds one replica of the 256 encode
-// entries per bank: entry s for lane l is lut[s * 32 + l], so the 32 lanes of
-// a warp always hit 32 different banks whatever bytes they look up.
+// Shared state of one encoder CTA.  lut holds 16 replicas of the 256 encode
+// entries {code << (32 - len), 2^(32 - len)}: entry s for lane l is
+// lut[s * 16 + (l & 15)].  A warp's 64-bit loads are served half a warp at a
+// time, and the 16 lanes of each half read 16 different bank pairs whatever
+// bytes they look up.
+constexpr uint32_t kLutReplicas = 16;
 struct EncShared {
-    uint32_t lut[kLutRows * 32];
+    uint2 lut[kLutRows * kLutReplicas];
     alignas(16) uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
     uint64_t prefix;
     uint64_t bar[2];            // input-buffer mbarriers
@@ -312,14 +315,15 @@ struct EncShared {
 
 __host__ __device__ constexpr uint32_t enc_shared_bytes() { return (sizeof(EncShared) + 15u) & ~15u; }
 
-__device__ __forceinline__ void load_encode_lut(EncShared &sh, const ecc_codebook *cb)
+// Fill the shared encode table from the codebook; threads [0, nthreads).
+__device__ __forceinline__ void load_encode_lut(EncShared &sh, const ecc_codebook *cb, uint32_t nthreads)
 {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int s0 = warp * 32; s0 < (int)kLutRows; s0 += kEncWarps * 32) {
-        const uint32_t mine = cb->enc[s0 + lane];
-#pragma unroll 8
-        for (int t = 0; t < 32; ++t)
-            sh.lut[(s0 + t) * 32 + lane] = __shfl_sync(~0u, mine, t);
+    const uint32_t tid = threadIdx.x;
+    if (tid >= nthreads)
+        return;
+    for (uint32_t i = tid; i < kLutRows * kLutReplicas; i += nthreads) {
+        const uint32_t s = i / kLutReplicas;
+        sh.lut[i] = make_uint2(cb->enc_code[s], cb->enc_mul[s]);
     }
 }
 
@@ -351,12 +355,86 @@ __device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t n)
     return r;
 }
 
-// Packing sink: 32-bit words in memory byte order (MSB-first bitstream).
-// A thread's first word may also hold its predecessor's last bits and its
-// last word its successor's first bits; those two are merged with atomicOr
-// into a zeroed destination.  Every word in between belongs to this thread
-// alone and is stored once, when it completes.  The accumulator is kept as
-// two 32-bit halves shifted with funnel shifts.
+// hi32(a * b) + c
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t r;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// ---- fast path: codes as multiplications
+// A code of length l is held as v = code << (32 - l) (first bit in bit 31)
+// with the multiplier q = 2^(32 - l).  Appending code 2 behind code 1 is
+// v1 + hi32(v2 * q1), and the pair's multiplier is hi32(q1 * q2) =
+// 2^(32 - l1 - l2), which is 0 exactly when the pair is longer than 32 bits
+// (or when either entry is 0, a byte the fast path does not code).
+
+// Encode entries of the 16 symbols in `in`, joined in 8 consecutive pairs
+// (v[k], q[k]).  Returns the bit total; *slow when the group is partial or
+// some pair has q == 0 (the exact path must code the group).
+__device__ __forceinline__ uint32_t lookup_pairs(const uint2 *lut, uint4 in, uint32_t cnt, uint32_t v[8],
+                                                 uint32_t q[8], bool *slow)
+{
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t zsum = 0, zor = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint2 e1 = lut[byte_of(w[k >> 1], (2 * k) & 3) * kLutReplicas];
+        const uint2 e2 = lut[byte_of(w[k >> 1], (2 * k + 1) & 3) * kLutReplicas];
+        v[k] = mad_hi(e2.x, e1.y, e1.x);
+        q[k] = __umulhi(e1.y, e2.y);
+        const uint32_t z = __clz(q[k]); // pair length - 1 (32: no fast code)
+        zsum += z;
+        zor |= z;
+    }
+    *slow = cnt < kSymPerThread || (zor & 32u);
+    return zsum + 8;
+}
+
+// Bit sink of the fast path: the partial word cur (its first nb bits used,
+// 1 <= nb <= 32, first bit in bit 31) belongs at *p, and K = 2^(32 - nb).
+// Appending (v, q) of length l: v * K + (cur << 32) holds in its high word
+// cur with v's leading bits behind it and in its low word v's remaining
+// bits; K * q = 2^(64 - nb - l) says whether the word filled up (high word
+// 0) and gives the next K (whichever word is non-zero).  Completed words
+// are merged with atomicOr into a zeroed destination, which also merges the
+// first and last words a thread shares with its neighbours.  A start at a
+// word boundary begins as a full, empty word just before it (for bit 0 of
+// the sink: a zero guard word in front of it, only ever or-ed with 0).
+struct MulPacker {
+    uint32_t *p;
+    uint32_t cur, K;
+
+    __device__ __forceinline__ void start(uint32_t *sink, uint32_t bitpos)
+    {
+        const uint32_t pm1 = bitpos - 1u;
+        p = sink + ((int32_t)pm1 >> 5);
+        K = 1u << (31u - (pm1 & 31u));
+        cur = 0;
+    }
+    __device__ __forceinline__ void put(uint32_t v, uint32_t q)
+    {
+        const uint64_t a = (uint64_t)v * K + ((uint64_t)cur << 32);
+        const uint64_t b = (uint64_t)K * q;
+        const uint32_t ahi = (uint32_t)(a >> 32), alo = (uint32_t)a;
+        const uint32_t bhi = (uint32_t)(b >> 32), blo = (uint32_t)b;
+        const bool full = bhi == 0;
+        if (full)
+            atomicOr(p, bswap32(ahi));
+        cur = full ? alo : ahi;
+        p += full ? 1 : 0;
+        K = bhi + blo;
+    }
+    __device__ __forceinline__ void finish() { atomicOr(p, bswap32(cur)); }
+};
+
+// ---- exact path: any code length up to ECC_MAX_CODE_LEN, codes read from
+// the codebook (global memory).  Packing sink: 32-bit words in memory byte
+// order; a thread's first and last words are merged with atomicOr into a
+// zeroed destination, every word in between belongs to this thread alone
+// and is stored once.  The accumulator is kept as two 32-bit halves
+// shifted with funnel shifts.
 struct Packer {
     uint32_t *dst;
     uint32_t wi0, wi; // first word, word being filled
@@ -406,80 +484,39 @@ struct Packer {
     }
 };
 
-// Encode entries of the 16 symbols held in v, and the bit lengths of the 8
-// consecutive pairs.  Returns the bit total; sets *slow if some symbol has
-// no packed entry (a code longer than 26 bits or a byte without code) or the
-// group is partial, *bad if some byte has no code at all.
-// lut points at entry 0 of this thread's replica: entry s is lut[s * kStride]
-// (the shared bank-replicated table: sh.lut + lane, stride 32; the codebook's
-// own enc[] in global memory: stride 1).
-template <int kStride>
-__device__ __forceinline__ uint32_t lookup16(const uint32_t *lut, uint4 v, uint32_t cnt, const ecc_codebook *cb,
-                                             uint32_t e[16], uint32_t pl[8], bool *slow, bool *bad)
+// Exact bit total of the cnt symbols in `in`; *bad if some byte has no code.
+__device__ __forceinline__ uint32_t exact_bits(uint4 in, uint32_t cnt, const ecc_codebook *cb, bool *bad)
 {
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    uint32_t emin = ~0u;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        e[j] = lut[byte_of(wv[j >> 2], j & 3) * kStride];
-        emin = min(emin, e[j]);
-    }
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
     uint32_t bits = 0;
+    bool nocode = false;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        pl[k] = (e[2 * k] & 31u) + (e[2 * k + 1] & 31u);
-        bits += pl[k];
+    for (int j = 0; j < kSymPerThread; ++j) {
+        if ((uint32_t)j >= cnt)
+            continue;
+        const uint32_t L = min((uint32_t)cb->len[byte_of(w[j >> 2], j & 3)], (uint32_t)ECC_MAX_CODE_LEN);
+        nocode |= L == 0;
+        bits += L;
     }
-    *bad = false;
-    *slow = cnt < 16 || emin == 0;
-    if (*slow) { // rare: recount exactly
-        bits = 0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if ((uint32_t)j >= cnt)
-                continue;
-            if (e[j]) {
-                bits += e[j] & 31u;
-            } else {
-                const uint32_t L = min((uint32_t)cb->len[byte_of(wv[j >> 2], j & 3)], (uint32_t)ECC_MAX_CODE_LEN);
-                *bad |= (L == 0);
-                bits += L;
-            }
-        }
-    }
+    *bad = nocode;
     return bits;
 }
 
-__device__ __forceinline__ void pack16(Packer &pk, const uint32_t e[16], const uint32_t pl[8], uint4 v, uint32_t cnt,
-                                       bool slow, const ecc_codebook *cb)
+// Exact packing of the cnt symbols in `in` at bit `pos` of dst.
+__device__ __forceinline__ void exact_pack(uint32_t *dst, uint32_t pos, uint4 in, uint32_t cnt,
+                                           const ecc_codebook *cb)
 {
-    if (!slow) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t e1 = e[2 * k], e2 = e[2 * k + 1];
-            const uint32_t plk = (e1 & 31u) + (e2 & 31u);
-            if (plk <= 32) {
-                pk.put(((e1 >> 5) << (e2 & 31u)) | (e2 >> 5), plk);
-            } else {
-                pk.put(e1 >> 5, e1 & 31u);
-                pk.put(e2 >> 5, e2 & 31u);
-            }
-        }
-    } else {
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if ((uint32_t)j >= cnt)
-                continue;
-            if (e[j]) {
-                pk.put(e[j] >> 5, e[j] & 31u);
-            } else {
-                const uint32_t b = byte_of(wv[j >> 2], j & 3);
-                const uint32_t L = min((uint32_t)cb->len[b], (uint32_t)ECC_MAX_CODE_LEN);
-                if (L)
-                    pk.put_long(cb->code[b] & ((1ull << L) - 1), L);
-            }
-        }
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    Packer pk;
+    pk.start(dst, pos);
+#pragma unroll 1
+    for (int j = 0; j < kSymPerThread; ++j) {
+        if ((uint32_t)j >= cnt)
+            break;
+        const uint32_t b = byte_of(w[j >> 2], j & 3);
+        const uint32_t L = min((uint32_t)cb->len[b], (uint32_t)ECC_MAX_CODE_LEN);
+        if (L)
+            pk.put_long(cb->code[b] & ((1ull << L) - 1), L);
     }
     pk.finish();
 }
@@ -497,7 +534,17 @@ __device__ __forceinline__ void compute_barrier(bool named)
         __syncthreads();
 }
 
-template <bool kCheckRoom, bool kSharedSrc, bool kNamed = false>
+// Bytes in front of each stage slot: a zero guard word the multiplying
+// packer may or 0 into when a thread starts at bit 0 of the slot.
+constexpr uint32_t kStageLead = 16;
+
+// Encode one tile (kTile symbols from t0) of a chunk of L symbols at bit
+// `run` of sink; returns the tile's bits.  kFast: full groups are coded with
+// the shared table and the multiplying packer (the sink is a shared stage
+// slot with its guard word in front); otherwise every group takes the exact
+// path (any sink).  kCheckRoom: a group that would pass sink_bits is not
+// written and raises bit 0 of *flag_word (or sh.flags).
+template <bool kCheckRoom, bool kSharedSrc, bool kNamed = false, bool kFast = true>
 __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job, const uint8_t *src, uint64_t base,
                                                 uint32_t L, uint32_t t0, uint32_t run, uint32_t *sink,
                                                 uint32_t sink_bits, bool write_sub, bool *bad_out,
@@ -508,9 +555,13 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
     const uint32_t my0 = t0 + (uint32_t)tid * kSymPerThread;
     const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
     const uint4 v = cnt ? load_symbols<kSharedSrc>(src + my0, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
-    uint32_t e[16], pl[8];
-    bool slow, bad;
-    const uint32_t bits = lookup16<32>(sh.lut + lane, v, cnt, job.cb, e, pl, &slow, &bad);
+    uint32_t pv[8], pq[8];
+    bool slow = true, bad = false;
+    uint32_t bits = 0;
+    if (kFast)
+        bits = lookup_pairs(sh.lut + (lane & (kLutReplicas - 1)), v, cnt, pv, pq, &slow);
+    if (slow) // rare: a partial group or a code the fast path leaves out
+        bits = exact_bits(v, cnt, job.cb, &bad);
     *bad_out |= bad;
 
     uint32_t incl = bits;
@@ -550,9 +601,16 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
     const uint32_t pos = run + excl;
     if (cnt) {
         if (!kCheckRoom || pos + bits <= sink_bits) {
-            Packer pk;
-            pk.start(sink, pos);
-            pack16(pk, e, pl, v, cnt, slow, job.cb);
+            if (!slow) {
+                MulPacker pk;
+                pk.start(sink, pos);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    pk.put(pv[k], pq[k]);
+                pk.finish();
+            } else {
+                exact_pack(sink, pos, v, cnt, job.cb);
+            }
         } else {
             atomicOr(flag_word ? flag_word : &sh.flags, 1u);
         }
@@ -629,7 +687,8 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
             uint32_t run2 = 0;
             uint32_t *gsink = reinterpret_cast<uint32_t *>(job.out + prefix);
             for (uint32_t t0 = 0; t0 < L; t0 += kTile)
-                run2 += encode_tile<false, kSharedSrc>(sh, job, src, base, L, t0, run2, gsink, 0, false, &bad2);
+                run2 += encode_tile<false, kSharedSrc, false, false>(sh, job, src, base, L, t0, run2, gsink, 0, false,
+                                                                     &bad2);
         }
     }
     __syncthreads();
@@ -638,11 +697,9 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
 // Re-encode chunk c with one warp straight into global memory at dst (the
 // chunk's place in the output, `words` 32-bit words, zeroed here first):
 // the path for chunks whose payload outgrew the shared staging buffer.
-// kGlobalLut: look codes up in the codebook's enc[] in global memory instead
-// of the shared table (which the compute warps may be reloading meanwhile).
-template <bool kGlobalLut>
-static __device__ __noinline__ void encode_chunk_warp(const EncShared &sh, const EncJob &job, uint64_t c,
-                                                      uint32_t *dst, uint32_t words)
+// Codes come from the codebook in global memory (the exact path), never
+// from the shared table, which the compute warps may be reloading.
+static __device__ __noinline__ void encode_chunk_warp(const EncJob &job, uint64_t c, uint32_t *dst, uint32_t words)
 {
     const int lane = threadIdx.x & 31;
     for (uint32_t i = lane; i < words; i += 32)
@@ -655,10 +712,8 @@ static __device__ __noinline__ void encode_chunk_warp(const EncShared &sh, const
         const uint32_t my0 = t0 + (uint32_t)lane * kSymPerThread;
         const uint32_t cnt = my0 < L ? min((uint32_t)kSymPerThread, L - my0) : 0u;
         const uint4 v = cnt ? load_symbols<false>(nullptr, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
-        uint32_t e[16], pl[8];
-        bool slow, bad;
-        const uint32_t bits = kGlobalLut ? lookup16<1>(job.cb->enc, v, cnt, job.cb, e, pl, &slow, &bad)
-                                         : lookup16<32>(sh.lut + lane, v, cnt, job.cb, e, pl, &slow, &bad);
+        bool bad;
+        const uint32_t bits = exact_bits(v, cnt, job.cb, &bad);
         uint32_t incl = bits;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -666,11 +721,8 @@ static __device__ __noinline__ void encode_chunk_warp(const EncShared &sh, const
             if (lane >= o)
                 incl += y;
         }
-        if (cnt) {
-            Packer pk;
-            pk.start(dst, run + incl - bits);
-            pack16(pk, e, pl, v, cnt, slow, job.cb);
-        }
+        if (cnt)
+            exact_pack(dst, run + incl - bits, v, cnt, job.cb);
         run += __shfl_sync(~0u, incl, 31);
     }
 }
@@ -739,10 +791,10 @@ __device__ __forceinline__ void claim_batched(EncSlot &s, const EncBatch &bt)
 
 // kBatched: chunks of many tensors from bt (each chunk's job in its slot);
 // else the chunks of `single`, claimed with `ticket`.  Shared memory: EncShared
-// | 2 input buffers of cmax bytes | 2 stage slots of stage_bytes.
+// | 2 input buffers of cmax bytes | 2 x (guard | stage slot of stage_bytes).
 __host__ __device__ constexpr size_t enc_ws_smem_bytes(uint32_t cmax, uint32_t stage_bytes)
 {
-    return enc_shared_bytes() + 2 * (size_t)cmax + 2 * (size_t)stage_bytes;
+    return enc_shared_bytes() + 2 * (size_t)cmax + 2 * ((size_t)kStageLead + stage_bytes);
 }
 
 template <bool kBatched>
@@ -753,8 +805,8 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
     uint8_t *inbuf = smem + enc_shared_bytes();
-    uint32_t *stage0 = reinterpret_cast<uint32_t *>(inbuf + 2 * (size_t)cmax);
-    const uint32_t slot_words = stage_bytes / 4;
+    uint32_t *stage0 = reinterpret_cast<uint32_t *>(inbuf + 2 * (size_t)cmax + kStageLead);
+    const uint32_t slot_words = (kStageLead + stage_bytes) / 4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (!kBatched && (single.cb->magic != ECC_CODEBOOK_MAGIC || single.cb->max_len > ECC_MAX_CODE_LEN)) {
         if (tid == 0 && blockIdx.x == 0)
@@ -769,10 +821,10 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
         sh.nostage = 0;
     }
     if (!kBatched)
-        load_encode_lut(sh, single.cb);
+        load_encode_lut(sh, single.cb, kEncThreadsWS);
     {
-        uint4 *st4 = reinterpret_cast<uint4 *>(stage0);
-        for (uint32_t i = tid; i < 2 * stage_bytes / 16; i += kEncThreadsWS)
+        uint4 *st4 = reinterpret_cast<uint4 *>(inbuf + 2 * (size_t)cmax); // both slots with their guards
+        for (uint32_t i = tid; i < 2 * (kStageLead + stage_bytes) / 16; i += kEncThreadsWS)
             st4[i] = make_uint4(0, 0, 0, 0);
     }
     // one thread: claim the chunk of iteration k into slot k % 4 and, unless
@@ -845,7 +897,7 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 for (uint32_t i = lane; i < stage_bytes / 16; i += 32)
                     st4[i] = make_uint4(0, 0, 0, 0);
                 if (write)
-                    encode_chunk_warp<kBatched>(sh, job, c, reinterpret_cast<uint32_t *>(job.out + prefix), nvec * 4);
+                    encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + prefix), nvec * 4);
             }
             if (kBatched && s.t_done) {
                 __threadfence(); // this lane's payload stores before the completion count
@@ -881,7 +933,7 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 // every compute warp is past the last lookup of the previous
                 // chunk (its final tile barrier); the output warp's overflow
                 // path reads the codebook in global memory
-                load_encode_lut(sh, job.cb);
+                load_encode_lut(sh, job.cb, kEncThreads);
                 loaded = job.cb;
                 bar_sync(kBarCompute, kEncThreads);
             }

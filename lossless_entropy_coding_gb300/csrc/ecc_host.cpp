@@ -28,22 +28,27 @@ void clear(ecc_codebook *cb, uint32_t family)
     cb->family = family;
 }
 
-// Fill the derived tables from len[]/code[]: the encode entries and the
-// 12-bit first-level decode table (byte | len << 8 for codes of at most 12
-// bits; entries under a longer code's prefix and unused entries stay 0).
+// Fill the derived tables from len[]/code[]: the encode entries (the code
+// with its first bit in bit 31, and the multiplier 2^(32 - len) that shifts
+// a following code behind it) and the 14-bit first-level decode table
+// (byte | len << 8 for codes of at most 14 bits; entries under a longer
+// code's prefix and unused entries stay 0).
 void fill_derived(ecc_codebook *cb)
 {
     uint32_t mx = 0, mn = 255, nc = 0;
     for (int b = 0; b < 256; ++b) {
         uint32_t L = cb->len[b];
-        if (!L) {
-            cb->enc[b] = 0;
+        cb->enc_code[b] = 0;
+        cb->enc_mul[b] = 0;
+        if (!L)
             continue;
-        }
         ++nc;
         mx = std::max(mx, L);
         mn = std::min(mn, L);
-        cb->enc[b] = (L <= 26) ? (uint32_t)((cb->code[b] << 5) | L) : 0u;
+        if (L <= 31) {
+            cb->enc_code[b] = (uint32_t)(cb->code[b] << (32 - L));
+            cb->enc_mul[b] = 1u << (32 - L);
+        }
         if (L <= (uint32_t)kPeek) {
             uint32_t lo = (uint32_t)cb->code[b] << (kPeek - L);
             uint32_t hi = lo + (1u << (kPeek - L));

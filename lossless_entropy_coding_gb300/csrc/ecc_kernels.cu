@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(EncParams p)
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
     uint8_t *inbuf = smem + enc_shared_bytes();
-    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + (size_t)p.nbuf * p.job.C);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(inbuf + (size_t)p.nbuf * p.job.C + kStageLead);
     const int tid = threadIdx.x;
     if (p.job.cb->magic != ECC_CODEBOOK_MAGIC || p.job.cb->max_len > ECC_MAX_CODE_LEN) {
         if (tid == 0 && blockIdx.x == 0)
@@ -104,9 +104,9 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(EncParams p)
         mbar_init(&sh.bar[1], 1);
         fence_mbar_init();
     }
-    load_encode_lut(sh, p.job.cb);
-    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
-    for (uint32_t i = tid; i < p.stage_bytes / 16; i += kEncThreads)
+    load_encode_lut(sh, p.job.cb, kEncThreads);
+    uint4 *st4 = reinterpret_cast<uint4 *>(inbuf + (size_t)p.nbuf * p.job.C); // the guard word and the stage
+    for (uint32_t i = tid; i < (kStageLead + p.stage_bytes) / 16; i += kEncThreads)
         st4[i] = make_uint4(0, 0, 0, 0);
     uint32_t pending = 0; // thread 0: buffers with a copy not yet waited for
     if (tid == 0) {
@@ -257,7 +257,7 @@ bool valid_sizes(uint32_t C, uint32_t S) { return pow2_in(C, 1024, 65536) && pow
 uint32_t enc_input_buffers(uint32_t C)
 {
     // two CTAs per SM must fit: LUT + two input buffers + output staging
-    const size_t two = enc_shared_bytes() + 2 * (size_t)C + stage_bytes_for(C);
+    const size_t two = enc_shared_bytes() + 2 * (size_t)C + kStageLead + stage_bytes_for(C);
     return two <= kMaxDynSmem / 2 - kStaticSmemReserve ? 2u : 1u;
 }
 
@@ -383,7 +383,7 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
         }
     }
     p.nbuf = enc_input_buffers(C);
-    const size_t smem = enc_shared_bytes() + (size_t)p.nbuf * C + p.stage_bytes;
+    const size_t smem = enc_shared_bytes() + (size_t)p.nbuf * C + kStageLead + p.stage_bytes;
     const int occ = occupancy((const void *)encode_kernel, kEncThreads, smem);
     if (occ <= 0)
         return ECC_ERR_CUDA;

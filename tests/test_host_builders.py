@@ -128,10 +128,16 @@ def test_derived_decode_table():
                 lo = int(cb["code"][b]) << (14 - L)
                 want[lo:lo + (1 << (14 - L))] = b | (L << 8)
         assert (cb["dec"] == want).all()
+        # encode entries: the code with its first bit in bit 31 and the
+        # multiplier 2^(32 - len); both 0 where the exact path codes the byte
         for b in range(256):
             L = int(cb["len"][b])
-            e = int(cb["enc"][b])
-            assert e == ((int(cb["code"][b]) << 5) | L if 0 < L <= 26 else 0)
+            v, q = int(cb["enc_code"][b]), int(cb["enc_mul"][b])
+            if 0 < L <= 31:
+                assert q == 1 << (32 - L) and v == (int(cb["code"][b]) << (32 - L)) & 0xFFFFFFFF
+                assert v >> (32 - L) == int(cb["code"][b])
+            else:
+                assert v == 0 and q == 0
 
 
 def test_figures_match_oracle():
