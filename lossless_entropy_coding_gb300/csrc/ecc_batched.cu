@@ -31,6 +31,8 @@ struct BatchHeader {
     uint32_t stage_bytes;
     uint32_t max_C;
     uint32_t encode;
+    uint32_t ws_slot_bytes; // encode: stage slot of the warp-specialised kernel (largest over the tensors)
+    uint32_t pad;
     uint64_t n_items;     // encode: chunks; decode: chunks, each codebook run padded to a multiple of warps
     uint64_t total_chunks;
     uint64_t desc_off, prefix_off, done_off, item_off, flags_off;
@@ -115,7 +117,7 @@ __global__ void __maxnreg__(96) encode_batched_ws_kernel(uint8_t *ws, uint64_t *
     bt.flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
     bt.done = reinterpret_cast<uint32_t *>(ws + h->done_off);
     const EncJob none{};
-    encode_ws_body<true>(none, 0, nullptr, bt, h->stage_bytes, h->max_C, kWaitLimitNs);
+    encode_ws_body<true>(none, 0, nullptr, bt, h->ws_slot_bytes, h->max_C, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void stamp_done(const ecc_desc &d, uint32_t *done, uint32_t k)
@@ -319,7 +321,7 @@ struct BatchPlan {
     std::vector<uint32_t> order; // workspace position -> caller's index
     std::vector<uint64_t> prefix;
     uint64_t n_items = 0, total_chunks = 0;
-    uint32_t max_C = 1024, warps = 1, stage = 0;
+    uint32_t max_C = 1024, warps = 1, stage = 0, ws_slot = 0;
     int R = 4; // decode: streams per lane, the smallest any tensor allows
 };
 
@@ -352,6 +354,7 @@ ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool c
             return ECC_ERR_ARG;
         P->total_chunks += nc;
         P->max_C = std::max(P->max_C, d.C);
+        P->ws_slot = std::max(P->ws_slot, enc_ws_slot_bytes(d.C, d.S));
         if (d.n)
             P->R = std::min<int>(P->R, (int)std::max<uint32_t>(1, d.C / d.S / 32));
     }
@@ -401,6 +404,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     h->stage_bytes = P.stage;
     h->max_C = P.max_C;
     h->encode = encode ? 1u : 0u;
+    h->ws_slot_bytes = P.ws_slot;
     h->n_items = P.n_items;
     h->total_chunks = P.total_chunks;
     h->desc_off = L.desc_off;
@@ -428,7 +432,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     if (P.n_items == 0)
         return ECC_OK;
     if (encode) {
-        const size_t ws_smem = enc_ws_smem_bytes(P.max_C, P.stage);
+        const size_t ws_smem = enc_ws_smem_bytes(P.max_C, P.ws_slot);
         const int occ_ws = ws_smem <= kMaxDynSmem - kStaticSmemReserve
                                ? occupancy((const void *)encode_batched_ws_kernel, kEncThreadsWS, ws_smem)
                                : 0;

@@ -69,6 +69,7 @@ __device__ __forceinline__ void st_stream16(void *p, uint4 v)
 }
 
 __device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
+__device__ __forceinline__ uint4 bswap4(uint4 v) { return make_uint4(bswap32(v.x), bswap32(v.y), bswap32(v.z), bswap32(v.w)); }
 
 // ---------------------------------------------------------------- bulk copies
 // One-instruction global -> shared copies through the bulk-copy (TMA) engine,
@@ -288,6 +289,8 @@ struct EncSlot {
     uint64_t *t_done; // many-tensor kernel: the tensor's completion stamp (may be null)
     uint32_t tensor;  // many-tensor kernel: tensor index (completion counters)
     uint32_t state;   // kSlotEnd: no more work; kSlotChunk; kSlotBadCodebook
+    uint32_t staged;  // its input was bulk-copied into input buffer k % 2
+    uint32_t parity;  // phase parity of that copy on the buffer's mbarrier
 };
 constexpr uint32_t kSlotEnd = 0, kSlotChunk = 1, kSlotBadCodebook = 2;
 constexpr uint32_t kEncSlots = 4; // claimed two chunks ahead: slots k .. k + 2 live at once
@@ -311,6 +314,9 @@ struct EncShared {
     uint32_t ticket;
     uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
     EncSlot slot[kEncSlots];
+    uint32_t seg_bits[2][kEncWarps]; // warp-segmented encoder: payload bits of each warp's segment, per slot
+    uint64_t out_prefix[2];          // byte offset of the slot's chunk in the output (resolved look-back)
+    uint32_t out_copy[2];            // 1: the compute warps copy the slot out to the output
 };
 
 __host__ __device__ constexpr uint32_t enc_shared_bytes() { return (sizeof(EncShared) + 15u) & ~15u; }
@@ -392,49 +398,95 @@ __device__ __forceinline__ uint32_t lookup_pairs(const uint2 *lut, uint4 in, uin
     return zsum + 8;
 }
 
-// Bit sink of the fast path: the partial word cur (its first nb bits used,
-// 1 <= nb <= 32, first bit in bit 31) belongs at *p, and K = 2^(32 - nb).
-// Appending (v, q) of length l: v * K + (cur << 32) holds in its high word
-// cur with v's leading bits behind it and in its low word v's remaining
-// bits; K * q = 2^(64 - nb - l) says whether the word filled up (high word
-// 0) and gives the next K (whichever word is non-zero).  Completed words
-// are merged with atomicOr into a zeroed destination, which also merges the
+// Predicated or-reduction into a shared word (addr: shared-window address):
+// done when `gate` is 0.  Written as one predicated instruction so that no
+// branch surrounds it.
+__device__ __forceinline__ void red_or_shared_if_zero(uint32_t addr, uint32_t v, uint32_t gate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %2, 0;\n\t@p red.shared.or.b32 [%0], %1;\n\t}" ::"r"(addr),
+                 "r"(v), "r"(gate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void red_or_shared(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.shared.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// predicated 32-bit shared store (addr: shared-window address)
+__device__ __forceinline__ void st_shared_if(uint32_t addr, uint32_t v, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.b32 [%0], %1;\n\t}" ::"r"(addr),
+                 "r"(v), "r"((uint32_t)p)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4_zero(uint32_t addr)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Bit sink of the fast path, a shared stage of 32-bit words in register
+// order (bit 31 of a word is its first bit; whoever copies the stage out
+// swaps the bytes).  The partial word cur (its first nb bits used,
+// 1 <= nb <= 32, first bit in bit 31) belongs at shared address a, and
+// K = 2^(32 - nb).  Appending (v, q) of length l: v * K + (cur << 32) holds
+// in its high word cur with v's leading bits behind it and in its low word
+// v's remaining bits; K * q = 2^(64 - nb - l) says whether the word filled
+// up (high word 0) and gives the next K (whichever word is non-zero).
+// Completed words are or-ed into the zeroed stage, which also merges the
 // first and last words a thread shares with its neighbours.  A start at a
 // word boundary begins as a full, empty word just before it (for bit 0 of
-// the sink: a zero guard word in front of it, only ever or-ed with 0).
+// the stage: a zero guard word in front of it, only ever or-ed with 0).
 struct MulPacker {
-    uint32_t *p;
+    uint32_t a;
     uint32_t cur, K;
 
-    __device__ __forceinline__ void start(uint32_t *sink, uint32_t bitpos)
+    __device__ __forceinline__ void start(uint32_t sink_addr, uint32_t bitpos)
     {
         const uint32_t pm1 = bitpos - 1u;
-        p = sink + ((int32_t)pm1 >> 5);
+        a = sink_addr + (uint32_t)(((int32_t)pm1 >> 5) * 4);
         K = 1u << (31u - (pm1 & 31u));
         cur = 0;
     }
     __device__ __forceinline__ void put(uint32_t v, uint32_t q)
     {
-        const uint64_t a = (uint64_t)v * K + ((uint64_t)cur << 32);
-        const uint64_t b = (uint64_t)K * q;
-        const uint32_t ahi = (uint32_t)(a >> 32), alo = (uint32_t)a;
-        const uint32_t bhi = (uint32_t)(b >> 32), blo = (uint32_t)b;
-        const bool full = bhi == 0;
-        if (full)
-            atomicOr(p, bswap32(ahi));
-        cur = full ? alo : ahi;
-        p += full ? 1 : 0;
-        K = bhi + blo;
+        const uint64_t x = (uint64_t)v * K + ((uint64_t)cur << 32);
+        const uint64_t y = (uint64_t)K * q;
+        const uint32_t xhi = (uint32_t)(x >> 32), xlo = (uint32_t)x;
+        const uint32_t yhi = (uint32_t)(y >> 32), ylo = (uint32_t)y;
+        red_or_shared_if_zero(a, xhi, yhi);
+        const bool full = yhi == 0;
+        cur = full ? xlo : xhi;
+        a += full ? 4u : 0u;
+        K = yhi + ylo;
     }
-    __device__ __forceinline__ void finish() { atomicOr(p, bswap32(cur)); }
+    __device__ __forceinline__ void finish() { red_or_shared(a, cur); }
 };
 
 // ---- exact path: any code length up to ECC_MAX_CODE_LEN, codes read from
-// the codebook (global memory).  Packing sink: 32-bit words in memory byte
-// order; a thread's first and last words are merged with atomicOr into a
-// zeroed destination, every word in between belongs to this thread alone
-// and is stored once.  The accumulator is kept as two 32-bit halves
-// shifted with funnel shifts.
+// the codebook (global memory).  Packing sink: 32-bit words, in memory byte
+// order when kSwap (a final destination), else in register order (a shared
+// stage, swapped when copied out); a thread's first and last words are
+// merged with atomicOr into a zeroed destination, every word in between
+// belongs to this thread alone and is stored once.  The accumulator is kept
+// as two 32-bit halves shifted with funnel shifts.
+template <bool kSwap>
 struct Packer {
     uint32_t *dst;
     uint32_t wi0, wi; // first word, word being filled
@@ -458,7 +510,8 @@ struct Packer {
         nb += len;
         const bool full = nb >= 32;
         nb &= 31;
-        const uint32_t w = bswap32(__funnelshift_r(alo, ahi, nb));
+        const uint32_t w0 = __funnelshift_r(alo, ahi, nb);
+        const uint32_t w = kSwap ? bswap32(w0) : w0;
         const bool first = wi == wi0;
         if (full && !first)
             dst[wi] = w;
@@ -480,7 +533,7 @@ struct Packer {
         if (wi != wi0)
             atomicOr(dst + wi0, fw);
         if (nb)
-            atomicOr(dst + wi, bswap32(shl_clamp(alo, 32 - nb)));
+            atomicOr(dst + wi, kSwap ? bswap32(shl_clamp(alo, 32 - nb)) : shl_clamp(alo, 32 - nb));
     }
 };
 
@@ -503,11 +556,12 @@ __device__ __forceinline__ uint32_t exact_bits(uint4 in, uint32_t cnt, const ecc
 }
 
 // Exact packing of the cnt symbols in `in` at bit `pos` of dst.
+template <bool kSwap>
 __device__ __forceinline__ void exact_pack(uint32_t *dst, uint32_t pos, uint4 in, uint32_t cnt,
                                            const ecc_codebook *cb)
 {
     const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    Packer pk;
+    Packer<kSwap> pk;
     pk.start(dst, pos);
 #pragma unroll 1
     for (int j = 0; j < kSymPerThread; ++j) {
@@ -523,7 +577,6 @@ __device__ __forceinline__ void exact_pack(uint32_t *dst, uint32_t pos, uint4 in
 
 constexpr uint32_t kBarCompute = 1;   // the encoder's compute warps
 constexpr uint32_t kBarFull = 2;      // + slot: stage slot filled (compute -> output warp)
-constexpr uint32_t kBarEmpty = 4;     // + slot: stage slot drained (output warp -> compute)
 constexpr int kEncThreadsWS = kEncThreads + 32;
 
 __device__ __forceinline__ void compute_barrier(bool named)
@@ -603,13 +656,13 @@ __device__ __forceinline__ uint32_t encode_tile(EncShared &sh, const EncJob &job
         if (!kCheckRoom || pos + bits <= sink_bits) {
             if (!slow) {
                 MulPacker pk;
-                pk.start(sink, pos);
+                pk.start(smem_u32(sink), pos);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     pk.put(pv[k], pq[k]);
                 pk.finish();
             } else {
-                exact_pack(sink, pos, v, cnt, job.cb);
+                exact_pack<!kFast>(sink, pos, v, cnt, job.cb);
             }
         } else {
             atomicOr(flag_word ? flag_word : &sh.flags, 1u);
@@ -671,7 +724,7 @@ __device__ __forceinline__ void encode_chunk(EncShared &sh, uint32_t *stage, uin
             const uint4 w = st4[i];
             st4[i] = make_uint4(0, 0, 0, 0);
             if (write)
-                st_stream16(dst + i, w);
+                st_stream16(dst + i, bswap4(w));
         }
     } else {
         // the payload outgrew the staging buffer: re-encode straight into
@@ -722,7 +775,7 @@ static __device__ __noinline__ void encode_chunk_warp(const EncJob &job, uint64_
                 incl += y;
         }
         if (cnt)
-            exact_pack(dst, run + incl - bits, v, cnt, job.cb);
+            exact_pack<true>(dst, run + incl - bits, v, cnt, job.cb);
         run += __shfl_sync(~0u, incl, 31);
     }
 }
@@ -741,15 +794,309 @@ __device__ __forceinline__ void issue_chunk_input(const EncJob &job, uint64_t c,
         bulk_g2s(buf, job.in + base, whole, bar);
 }
 
+// ---------------------------------------------------------------- warp-segmented encoder
+// Each compute warp codes one contiguous segment of a chunk into a region of
+// its own in a shared stage slot, in rounds of 32 lanes x 16 symbols: a warp
+// scan of the lanes' bit counts places every lane, so no CTA-wide barrier
+// is needed until the chunk ends.  A segment is at least 512 symbols (one
+// full round) and at least one sub-block, so sub-blocks never straddle
+// warps.  Regions hold 32-bit words in register order (bit 31 first).  Once
+// the chunk's offset in the output is known each compute warp copies its
+// region out, shifted to where its segment starts in the chunk's bitstream
+// (the stream is the segments' bits end to end).
+
+constexpr uint32_t kRoundSyms = 32 * kSymPerThread; // 512
+
+__host__ __device__ constexpr uint32_t seg_symbols(uint32_t C, uint32_t S)
+{
+    return (C / kEncWarps > S ? C / kEncWarps : S) > kRoundSyms ? (C / kEncWarps > S ? C / kEncWarps : S)
+                                                                  : kRoundSyms;
+}
+// a region: room for the segment at up to 11 bits a symbol, plus one zero
+// word of slack that the out-copy may read past the payload
+__host__ __device__ constexpr uint32_t region_cap_bytes(uint32_t seg) { return pad16((seg * 11u + 7u) / 8u); }
+__host__ __device__ constexpr uint32_t region_bytes(uint32_t seg) { return region_cap_bytes(seg) + 16u; }
+__host__ __device__ constexpr uint32_t enc_ws_slot_bytes(uint32_t C, uint32_t S)
+{
+    return (C / seg_symbols(C, S)) * region_bytes(seg_symbols(C, S));
+}
+
+// Fast-path sink for one lane's group: the multiplying packer with plain
+// stores.  State: the partial word cur (its first nb bits used, 1 <= nb <=
+// 32) at word index a of the region, K = 2^(32 - nb).  A group that starts
+// at a word boundary takes its first pair as the initial partial word, so
+// no lane ever writes a word before the one holding its first bit.  A
+// completed word is stored whole, the predecessor's bits in it as zeros:
+// the lane that ends in a word merges its partial word into it afterwards
+// (or-reduction after a warp barrier), which also covers a word completed
+// by the next lane.
+struct SegPacker {
+    uint32_t addr, cur, K; // addr: shared-window address of the word holding cur
+
+    // one append's tail: store w at addr when gate == 0 (the word filled up),
+    // then take xlo (the code's remaining bits) as the partial word and move
+    // to the next word; else w stays the partial word
+    __device__ __forceinline__ void tail(uint32_t w, uint32_t xlo, uint32_t gate)
+    {
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %4, 0;\n\t@p st.shared.b32 [%0], %2;\n\t"
+                     "selp.b32 %1, %3, %2, p;\n\t@p add.u32 %0, %0, 4;\n\t}"
+                     : "+r"(addr), "=r"(cur)
+                     : "r"(w), "r"(xlo), "r"(gate)
+                     : "memory");
+    }
+    // pairs (v[k], q[k]) of one group at bit pos of the region (word base
+    // `region`, shared-window address); c0 = the bits already in the word
+    // holding pos (merged there by an earlier round, else 0)
+    __device__ __forceinline__ void pack(uint32_t region, uint32_t pos, uint32_t c0, const uint32_t v[8],
+                                         const uint32_t q[8])
+    {
+        const uint32_t nb0 = pos & 31u;
+        addr = region + (pos >> 5) * 4u;
+        {   // first pair: a normal append unless the group starts a word
+            const uint32_t K0 = 1u << ((32u - nb0) & 31u); // nb0 = 0: unused
+            const uint64_t x = (uint64_t)v[0] * K0;
+            const uint64_t y = (uint64_t)K0 * q[0];
+            const uint32_t yhi = (uint32_t)(y >> 32), ylo = (uint32_t)y;
+            tail((uint32_t)(x >> 32) | c0, (uint32_t)x, nb0 ? yhi : 1u);
+            cur = nb0 ? cur : v[0];
+            K = nb0 ? yhi + ylo : q[0];
+        }
+#pragma unroll
+        for (int k = 1; k < 8; ++k) {
+            const uint64_t x = (uint64_t)v[k] * K;
+            const uint64_t y = (uint64_t)K * q[k];
+            const uint32_t yhi = (uint32_t)(y >> 32), ylo = (uint32_t)y;
+            tail((uint32_t)(x >> 32) | cur, (uint32_t)x, yhi);
+            K = yhi + ylo;
+        }
+    }
+};
+
+// Exact-path sink for one lane's group (rare: partial groups, long codes):
+// same protocol as SegPacker, codes read from the codebook.  Returns the
+// final partial word (first bit in bit 31), its word index and its bit count
+// (0: the group ended on a word boundary).
+struct PackEnd {
+    uint32_t word, wa, nb;
+};
+static __device__ __noinline__ PackEnd seg_exact_pack(uint32_t *region, uint32_t pos, uint32_t c0, uint4 in,
+                                                      uint32_t cnt, const ecc_codebook *cb)
+{
+    const uint32_t w4[4] = {in.x, in.y, in.z, in.w};
+    uint32_t wi = pos >> 5, nb = pos & 31u;
+    uint32_t alo = nb ? c0 >> (32u - nb) : 0u, ahi = 0;
+    auto put = [&](uint32_t code, uint32_t len) { // len <= 32
+        ahi = __funnelshift_lc(alo, ahi, len);
+        alo = shl_clamp(alo, len) | code;
+        nb += len;
+        if (nb >= 32) {
+            nb -= 32;
+            region[wi++] = __funnelshift_r(alo, ahi, nb);
+        }
+    };
+    for (uint32_t j = 0; j < cnt; ++j) {
+        const uint32_t b = byte_of(w4[j >> 2], j & 3);
+        const uint32_t L = min((uint32_t)cb->len[b], (uint32_t)ECC_MAX_CODE_LEN);
+        if (!L)
+            continue;
+        const uint64_t code = cb->code[b] & ((1ull << L) - 1);
+        if (L > 24) {
+            put((uint32_t)(code >> 24), L - 24);
+            put((uint32_t)(code & 0xFFFFFFu), 24);
+        } else {
+            put((uint32_t)code, L);
+        }
+    }
+    return PackEnd{nb ? shl_clamp(alo, 32u - nb) : 0u, wi, nb};
+}
+
+// Code the rounds of one warp's segment [s0, s1) of chunk symbols (s1 > s0)
+// into its region (shared-window address `region`, cap_bits of room).
+// src: the chunk's staged input (kSharedSrc) else unused; the tensor's bytes
+// come from job.in + base.  Writes the segment's sub-block bit counts.
+// Returns the segment's bit total; raises bit 0 of *flag_word (and writes
+// nothing more) if the segment outgrows its region; *bad if some byte has no
+// code.
+template <bool kSharedSrc>
+__device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &job, const uint8_t *src,
+                                                   uint64_t base, uint32_t s0, uint32_t s1, uint32_t region,
+                                                   uint32_t cap_bits, uint32_t *flag_word, bool *bad)
+{
+    const int lane = threadIdx.x & 31;
+    const uint2 *lut = sh.lut + (lane & (kLutReplicas - 1));
+    const uint32_t s_shift = 31 - __clz(job.S);
+    const uint32_t tps = job.S / kSymPerThread; // lanes per sub-block (64 for S = 1024: two rounds)
+    uint16_t *sub = job.sub_bits + (base >> s_shift);
+    uint32_t run = 0, half = 0;
+    bool room = true;
+    for (uint32_t r0 = s0; r0 < s1; r0 += kRoundSyms) {
+        const bool full_round = r0 + kRoundSyms <= s1; // the same for every lane
+        const uint32_t my0 = r0 + (uint32_t)lane * kSymPerThread;
+        const uint32_t cnt = full_round ? kSymPerThread : my0 < s1 ? min((uint32_t)kSymPerThread, s1 - my0) : 0u;
+        uint4 in = make_uint4(0, 0, 0, 0);
+        if (full_round)
+            in = load_symbols<kSharedSrc>(src + my0, job.in + base + my0, kSymPerThread);
+        else if (cnt)
+            in = load_symbols<kSharedSrc>(src + my0, job.in + base + my0, cnt);
+        uint32_t pv[8], pq[8];
+        bool slow;
+        uint32_t bits = lookup_pairs(lut, in, cnt, pv, pq, &slow);
+        // the common case, every group of the round full and coded by the
+        // table, runs without a branch that splits the warp
+        const bool fast = __all_sync(~0u, !slow);
+        if (!fast && slow) {
+            bool nocode = false;
+            bits = exact_bits(in, cnt, job.cb, &nocode);
+            *bad |= nocode;
+        }
+        uint32_t incl = bits;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(~0u, incl, o);
+            incl += lane >= o ? y : 0u;
+        }
+        const uint32_t rtot = __shfl_sync(~0u, incl, 31);
+        // sub-block bit counts
+        if (tps <= 32) {
+            const uint32_t sb = __shfl_sync(~0u, incl, lane | (int)(tps - 1)) - (incl - bits);
+            if (cnt && (lane & (tps - 1)) == 0)
+                sub[my0 >> s_shift] = (uint16_t)sb;
+        } else {
+            if (((r0 - s0) / kRoundSyms) & 1) {
+                if (lane == 0)
+                    sub[(my0 - kRoundSyms) >> s_shift] = (uint16_t)(half + rtot);
+            } else if (r0 + kRoundSyms >= s1 && lane == 0) { // a final half sub-block
+                sub[my0 >> s_shift] = (uint16_t)rtot;
+            }
+            half = rtot;
+        }
+        room = room && run + rtot <= cap_bits;
+        if (room) {
+            const uint32_t pos = run + incl - bits;
+            // the word holding a lane's first bit may already hold bits of
+            // the previous round (merged there): every lane reads it before
+            // any lane of this round stores, so whichever lane completes it
+            // keeps those bits (the others merge them again, harmlessly)
+            const uint32_t cw = ld_shared_u32(region + (pos >> 5) * 4u);
+            const uint32_t c0 = (pos & 31u) ? cw : 0u;
+            __syncwarp();
+            if (fast) {
+                SegPacker pk;
+                pk.pack(region, pos, c0, pv, pq);
+                __syncwarp(); // every store of the round precedes every merge
+                red_or_shared(pk.addr, pk.cur);
+            } else {
+                uint32_t word = 0, wa = 0, nb = 0;
+                if (cnt) {
+                    if (!slow) {
+                        SegPacker pk;
+                        pk.pack(region, pos, c0, pv, pq);
+                        word = pk.cur;
+                        wa = pk.addr;
+                        nb = 1; // 1..32 bits: always a partial word to merge
+                    } else {
+                        const PackEnd e = seg_exact_pack(
+                            reinterpret_cast<uint32_t *>(__cvta_shared_to_generic(region)), pos, c0, in, cnt, job.cb);
+                        word = e.word;
+                        wa = region + e.wa * 4u;
+                        nb = e.nb;
+                    }
+                }
+                __syncwarp();
+                if (nb)
+                    red_or_shared(wa, word);
+            }
+            __syncwarp();
+        } else if (lane == 0) {
+            atomicOr(flag_word, 1u);
+        }
+        run += rtot;
+    }
+    return run;
+}
+
+// Copy region w of a finished chunk from its stage slot (shared-window
+// address `slot`, regions of region_words) to the chunk's payload at dst
+// (global, 16-byte aligned); one warp.  seg_bits[0..nseg) are the segments'
+// bit totals; the chunk's bitstream is their bits end to end.  Region w
+// supplies the output words whose first bit lies in its segment, shifted
+// from the region's word grid to the stream's; the last of them may also
+// take the first bits of the segments after it.  Region 0 also zeroes the
+// words up to the 16-byte boundary after the stream.  Each lane takes four
+// region words at a time (one 16-byte load).
+__device__ __forceinline__ void copy_region_out(uint32_t slot, uint32_t region_words, const uint32_t *seg_bits,
+                                                uint32_t nseg, uint32_t w, uint32_t *dst)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t P = 0, total = 0;
+    for (uint32_t u = 0; u < nseg; ++u) {
+        P += u < w ? seg_bits[u] : 0u;
+        total += seg_bits[u];
+    }
+    const uint32_t T = seg_bits[w];
+    const uint32_t j0 = (P + 31) >> 5, nw = ((P + T + 31) >> 5) - j0;
+    // nw = 0: the segment's bits all lie inside a word that starts in an
+    // earlier segment, whose last word takes them
+    if (nw) {
+        const uint32_t src = slot + w * region_words * 4u;
+        const uint32_t r = (0u - P) & 31u;
+        const uint32_t nlast = nw - 1; // words [0, nlast) here, the last one below
+        uint32_t *d = dst + j0;
+        // output word i takes region words i and i + 1 (i + 1 <= nw stays
+        // inside the region: nw <= its capacity in words + 1)
+#pragma unroll 2
+        for (uint32_t i0 = (uint32_t)lane * 4u; i0 < ((nlast + 127u) & ~127u); i0 += 128u) {
+            const uint4 v = i0 <= nw ? ld_shared_v4(src + i0 * 4u) : make_uint4(0, 0, 0, 0);
+            uint32_t nx = __shfl_down_sync(~0u, v.x, 1);
+            if (lane == 31)
+                nx = i0 + 4u <= nw ? ld_shared_u32(src + (i0 + 4u) * 4u) : 0u;
+            const uint32_t o[4] = {__funnelshift_l(v.y, v.x, r), __funnelshift_l(v.z, v.y, r),
+                                   __funnelshift_l(v.w, v.z, r), __funnelshift_l(nx, v.w, r)};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (i0 + (uint32_t)t < nlast)
+                    d[i0 + t] = bswap32(o[t]);
+        }
+        if (lane == 0) {
+            uint32_t val = __funnelshift_l(ld_shared_u32(src + nw * 4u), ld_shared_u32(src + nlast * 4u), r);
+            const uint32_t jj = j0 + nlast;
+            uint32_t Pv = P + T; // first bits of the following segments inside this word
+            for (uint32_t u = w + 1; u < nseg && Pv < 32 * jj + 32; ++u) {
+                if (seg_bits[u])
+                    val |= ld_shared_u32(slot + u * region_words * 4u) >> (Pv - 32 * jj);
+                Pv += seg_bits[u];
+            }
+            d[nlast] = bswap32(val);
+        }
+    }
+    if (w == 0) {
+        const uint32_t jend = (total + 31) >> 5, jpad = pad16((total + 7) >> 3) >> 2;
+        if (jend + (uint32_t)lane < jpad)
+            dst[jend + lane] = 0;
+    }
+}
+
+// Zero one warp's region (shared-window address, region_words words, a
+// multiple of 4).
+__device__ __forceinline__ void zero_region(uint32_t region, uint32_t region_words)
+{
+    const int lane = threadIdx.x & 31;
+    for (uint32_t i = (uint32_t)lane * 4u; i < region_words; i += 128u)
+        st_shared_v4_zero(region + i * 4u);
+}
+
 // ---------------------------------------------------------------- warp-specialised encoder
-// 8 compute warps encode chunk k into stage slot k % 2 and publish its
-// aggregate at once; one output warp resolves the chunk's offset (decoupled
-// look-back), writes the staged payload out and claims chunk k + 2 (ticket,
-// then a bulk copy of its input into the input buffer chunk k has just
-// released), while the compute warps already encode chunk k + 1.  Stage
-// slots are handed over with named barriers: kBarFull + slot (compute ->
-// output) and kBarEmpty + slot (output -> compute).  Claiming in the output
-// warp keeps the ticket's round trip off the compute warps' critical path.
+// 8 compute warps encode chunk k into stage slot k % 2 (one segment each)
+// and publish its aggregate at once; one output warp resolves the chunk's
+// offset (decoupled look-back), writes chunk_off/total_bits/status and
+// claims chunk k + 2 (ticket, then a bulk copy of its input into the input
+// buffer chunk k has just released), while the compute warps code chunk
+// k + 1 into the other slot; right after that they copy chunk k's regions
+// out to their places in its bitstream, so the look-back has a whole
+// chunk's time to resolve.  Named barriers: kBarFull + slot (compute ->
+// output: the chunk is coded) and kBarReady + slot (output -> compute: its
+// offset is known).  Claiming in the output warp keeps the ticket's round
+// trip off the compute warps' critical path.
 
 // Source of chunks of the many-tensor encoder: one ticket over the chunks of
 // all tensors (workspace order), item[t] = tensor << 32 | chunk.
@@ -789,24 +1136,26 @@ __device__ __forceinline__ void claim_batched(EncSlot &s, const EncBatch &bt)
     s.state = (cb->magic == ECC_CODEBOOK_MAGIC && cb->max_len <= ECC_MAX_CODE_LEN) ? kSlotChunk : kSlotBadCodebook;
 }
 
-// kBatched: chunks of many tensors from bt (each chunk's job in its slot);
-// else the chunks of `single`, claimed with `ticket`.  Shared memory: EncShared
-// | 2 input buffers of cmax bytes | 2 x (guard | stage slot of stage_bytes).
-__host__ __device__ constexpr size_t enc_ws_smem_bytes(uint32_t cmax, uint32_t stage_bytes)
+// Shared memory of the warp-specialised kernels: EncShared | 2 input buffers
+// of cmax bytes | 2 stage slots of slot_bytes (see enc_ws_slot_bytes).
+__host__ __device__ constexpr size_t enc_ws_smem_bytes(uint32_t cmax, uint32_t slot_bytes)
 {
-    return enc_shared_bytes() + 2 * (size_t)cmax + 2 * ((size_t)kStageLead + stage_bytes);
+    return enc_shared_bytes() + 2 * (size_t)cmax + 2 * (size_t)slot_bytes;
 }
 
+constexpr uint32_t kBarReady = 4; // + slot: the chunk's output offset is known (output warp -> compute)
+
+// kBatched: chunks of many tensors from bt (each chunk's job in its slot);
+// else the chunks of `single`, claimed with `ticket`.
 template <bool kBatched>
 __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_chunks, uint32_t *ticket,
-                                               const EncBatch &bt, uint32_t stage_bytes, uint32_t cmax,
+                                               const EncBatch &bt, uint32_t slot_bytes, uint32_t cmax,
                                                uint64_t timeout_ns)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
     uint8_t *inbuf = smem + enc_shared_bytes();
-    uint32_t *stage0 = reinterpret_cast<uint32_t *>(inbuf + 2 * (size_t)cmax + kStageLead);
-    const uint32_t slot_words = (kStageLead + stage_bytes) / 4;
+    const uint32_t stage0 = smem_u32(inbuf + 2 * (size_t)cmax);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (!kBatched && (single.cb->magic != ECC_CODEBOOK_MAGIC || single.cb->max_len > ECC_MAX_CODE_LEN)) {
         if (tid == 0 && blockIdx.x == 0)
@@ -819,14 +1168,12 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
         fence_mbar_init();
         sh.issued[0] = sh.issued[1] = 0;
         sh.nostage = 0;
+        sh.slot_flags[0] = sh.slot_flags[1] = 0;
     }
     if (!kBatched)
         load_encode_lut(sh, single.cb, kEncThreadsWS);
-    {
-        uint4 *st4 = reinterpret_cast<uint4 *>(inbuf + 2 * (size_t)cmax); // both slots with their guards
-        for (uint32_t i = tid; i < 2 * (kStageLead + stage_bytes) / 16; i += kEncThreadsWS)
-            st4[i] = make_uint4(0, 0, 0, 0);
-    }
+    for (uint32_t i = tid; i < 2 * slot_bytes / 16; i += kEncThreadsWS)
+        st_shared_v4_zero(stage0 + i * 16u);
     // one thread: claim the chunk of iteration k into slot k % 4 and, unless
     // staging was given up, bulk-copy its input into buffer k % 2
     auto claim = [&](uint32_t k) {
@@ -835,8 +1182,11 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             claim_batched(s, bt);
         else
             claim_single(s, ticket, n_chunks);
+        s.staged = 0;
         if (s.state != kSlotEnd && !sh.nostage) {
             issue_chunk_input(kBatched ? s.job : single, s.c, inbuf + (size_t)(k & 1) * cmax, &sh.bar[k & 1]);
+            s.parity = sh.issued[k & 1] & 1u;
+            s.staged = 1;
             ++sh.issued[k & 1];
         }
     };
@@ -849,7 +1199,6 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
     }
     __syncthreads(); // the last CTA-wide barrier before the warps split
 
-    uint32_t consumed[2] = {0, 0}; // compute warps: copies waited for, per input buffer
     if (warp == kEncWarps) { // ---------------- output warp
         for (uint32_t k = 0;; ++k) {
             const uint32_t b = k & 1;
@@ -871,6 +1220,7 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             bool to = false;
             const uint64_t prefix = c == 0 ? 0 : resolve_prefix(job.flags, c, bytes, timeout_ns, &to);
             const bool fits = prefix + bytes <= job.out_cap;
+            const bool write = fits && !to;
             if (lane == 0) {
                 job.chunk_off[c + 1] = prefix + bytes;
                 if (c == 0)
@@ -881,97 +1231,122 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 else if (!fits)
                     set_status(job.status, ECC_ERR_CAPACITY);
             }
-            uint4 *st4 = reinterpret_cast<uint4 *>(stage0 + b * slot_words);
-            const uint32_t nvec = (uint32_t)(bytes / 16);
-            const bool write = fits && !to;
-            if (!(fl & 1u)) {
-                uint4 *dst = reinterpret_cast<uint4 *>(job.out + prefix);
-#pragma unroll 4
-                for (uint32_t i = lane; i < nvec; i += 32) {
-                    const uint4 w = st4[i];
-                    st4[i] = make_uint4(0, 0, 0, 0);
-                    if (write)
-                        st_stream16(dst + i, w);
-                }
-            } else {
-                for (uint32_t i = lane; i < stage_bytes / 16; i += 32)
-                    st4[i] = make_uint4(0, 0, 0, 0);
-                if (write)
-                    encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + prefix), nvec * 4);
+            const bool copy = write && !(fl & 1u);
+            if (lane == 0) {
+                sh.out_prefix[b] = prefix;
+                sh.out_copy[b] = copy ? 1u : 0u;
             }
-            if (kBatched && s.t_done) {
-                __threadfence(); // this lane's payload stores before the completion count
+            if ((fl & 1u) && write) // a segment outgrew its region: code the chunk straight into the output
+                encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + prefix), (uint32_t)(bytes / 4));
+            if (kBatched && s.t_done && !copy) {
+                // completion counts one per segment: the copying warps count
+                // their own, else this warp counts the chunk's
+                __threadfence();
                 __syncwarp();
                 if (lane == 0) {
-                    const uint64_t nch = (job.n + job.C - 1) >> (31 - __clz(job.C));
-                    if (atomicAdd(bt.done + s.tensor, 1u) + 1u == nch)
+                    const uint32_t nseg = job.C / seg_symbols(job.C, job.S);
+                    const uint32_t want = nseg * (uint32_t)((job.n + job.C - 1) >> (31 - __clz(job.C)));
+                    if (atomicAdd(bt.done + s.tensor, nseg) + nseg == want)
                         *s.t_done = globaltimer();
                 }
             }
-            bar_arrive(kBarEmpty + b, kEncThreadsWS);
+            bar_arrive(kBarReady + b, kEncThreadsWS);
         }
     } else { // ---------------- compute warps
-        bool staging = true;
         const ecc_codebook *loaded = kBatched ? nullptr : single.cb;
+        // copy this warp's region of chunk j (slot j % 2) out once the
+        // output warp has resolved the chunk's offset
+        auto copy_out = [&](uint32_t j) {
+            const uint32_t pb = j & 1;
+            bar_sync(kBarReady + pb, kEncThreadsWS);
+            const EncSlot &ps = sh.slot[j % kEncSlots];
+            const EncJob &pjob = kBatched ? ps.job : single;
+            const uint32_t seg = seg_symbols(pjob.C, pjob.S);
+            const uint32_t nseg = pjob.C / seg;
+            if (sh.out_copy[pb] && (uint32_t)warp < nseg) {
+                copy_region_out(stage0 + pb * slot_bytes, region_bytes(seg) / 4u, sh.seg_bits[pb], nseg, warp,
+                                reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb]));
+                if (kBatched && ps.t_done) {
+                    __threadfence(); // this lane's payload stores before the completion count
+                    __syncwarp();
+                    const uint32_t want = nseg * (uint32_t)((pjob.n + pjob.C - 1) >> (31 - __clz(pjob.C)));
+                    if (lane == 0 && atomicAdd(bt.done + ps.tensor, 1u) + 1u == want)
+                        *ps.t_done = globaltimer();
+                }
+            }
+        };
         for (uint32_t k = 0;; ++k) {
             const uint32_t b = k & 1;
-            if (k >= 2)
-                bar_sync(kBarEmpty + b, kEncThreadsWS);
             const EncSlot &s = sh.slot[k % kEncSlots];
             const uint32_t state = s.state;
             if (state == kSlotEnd) {
                 bar_arrive(kBarFull + b, kEncThreadsWS);
                 if (k >= 1)
-                    bar_sync(kBarEmpty + (b ^ 1), kEncThreadsWS);
+                    copy_out(k - 1);
                 break;
             }
             const EncJob &job = kBatched ? s.job : single;
             const uint64_t c = s.c;
-            if (tid == 0)
-                sh.slot_flags[b] = 0;
+            const uint32_t seg = seg_symbols(job.C, job.S);
+            const uint32_t nseg = job.C / seg;
+            const uint32_t rwords = region_bytes(seg) / 4u;
+            // only warps below nseg own a region: the slot holds nseg of them
+            const uint32_t region = stage0 + b * slot_bytes + (uint32_t)warp * rwords * 4u;
+            if (k >= 2) {
+                // chunk k - 2 left this slot: every warp has copied its region
+                // out (after coding chunk k - 1) and is past its lookups
+                bar_sync(kBarCompute, kEncThreads);
+                if (tid == 0)
+                    sh.slot_flags[b] = 0; // the output warp has read it
+                if ((uint32_t)warp < nseg)
+                    zero_region(region, rwords);
+            }
             if (kBatched && state == kSlotChunk && job.cb != loaded) {
                 // every compute warp is past the last lookup of the previous
-                // chunk (its final tile barrier); the output warp's overflow
-                // path reads the codebook in global memory
+                // chunk (the chunk barrier); the output warp's overflow path
+                // reads the codebook in global memory
+                bar_sync(kBarCompute, kEncThreads);
                 load_encode_lut(sh, job.cb, kEncThreads);
                 loaded = job.cb;
                 bar_sync(kBarCompute, kEncThreads);
             }
-            bool ok = staging && mbar_wait(&sh.bar[b], consumed[b] & 1u, timeout_ns);
-            ok = bar_red_and(kBarCompute, kEncThreads, ok);
-            if (ok) {
-                ++consumed[b];
-            } else {
-                if (staging && tid == 0) {
-                    set_status(job.status, ECC_ERR_TIMEOUT);
-                    sh.nostage = 1;
-                }
-                staging = false;
-            }
-            uint32_t *stage = stage0 + b * slot_words;
             const uint64_t base = c * job.C;
             const uint32_t L = state == kSlotChunk ? (uint32_t)min((uint64_t)job.C, job.n - base) : 0u;
-            const uint8_t *src = inbuf + (size_t)b * cmax;
+            const uint32_t s0 = (uint32_t)warp * seg, s1 = min(s0 + seg, L);
             bool bad = state == kSlotBadCodebook;
-            uint32_t run = 0;
-            for (uint32_t t0 = 0; t0 < L; t0 += kTile) {
-                if (ok)
-                    run += encode_tile<true, true, true>(sh, job, src, base, L, t0, run, stage, stage_bytes * 8u, true,
-                                                         &bad, &sh.slot_flags[b]);
-                else
-                    run += encode_tile<true, false, true>(sh, job, nullptr, base, L, t0, run, stage, stage_bytes * 8u,
-                                                          true, &bad, &sh.slot_flags[b]);
+            uint32_t bits = 0;
+            if (s0 < s1) {
+                bool ok = false;
+                if (s.staged) {
+                    ok = __all_sync(~0u, mbar_wait(&sh.bar[b], s.parity, timeout_ns));
+                    if (!ok && lane == 0) { // never expected: the copy reads valid memory
+                        set_status(job.status, ECC_ERR_TIMEOUT);
+                        sh.nostage = 1;
+                    }
+                }
+                const uint8_t *src = inbuf + (size_t)b * cmax;
+                const uint32_t cap = region_cap_bytes(seg) * 8u;
+                bits = ok ? encode_segment<true>(sh, job, src, base, s0, s1, region, cap, &sh.slot_flags[b], &bad)
+                          : encode_segment<false>(sh, job, nullptr, base, s0, s1, region, cap, &sh.slot_flags[b],
+                                                  &bad);
             }
-            if (bad)
+            if (bad && lane == 0)
                 set_status(job.status, ECC_ERR_CODEBOOK);
+            if (lane == 0)
+                sh.seg_bits[b][warp] = bits;
+            bar_sync(kBarCompute, kEncThreads); // the chunk is coded
             if (tid == 0) {
+                uint32_t run = 0;
+                for (int w = 0; w < kEncWarps; ++w)
+                    run += (uint32_t)w < nseg ? sh.seg_bits[b][w] : 0u;
                 const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
                 st_relaxed(job.flags + c, (c == 0 ? kFlagPrefix : kFlagAggregate) | (bytes & kValueMask));
                 sh.slot_bits[b] = run;
             }
-            // each thread's packing writes precede its arrival; the output warp
-            // waits for all 256 arrivals
             bar_arrive(kBarFull + b, kEncThreadsWS);
+            // chunk k - 1's offset has had a whole chunk to resolve
+            if (k >= 1)
+                copy_out(k - 1);
         }
     }
     // never exit with a bulk copy still writing into this CTA's shared memory
@@ -979,11 +1354,8 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
     __syncthreads();
     if (tid == 0)
         for (uint32_t q = 0; q < 2; ++q)
-            while (consumed[q] < sh.issued[q]) {
-                if (!mbar_wait(&sh.bar[q], consumed[q] & 1u, timeout_ns))
-                    break;
-                ++consumed[q];
-            }
+            if (sh.issued[q])
+                (void)mbar_wait(&sh.bar[q], (sh.issued[q] - 1u) & 1u, timeout_ns);
 }
 
 // ---------------------------------------------------------------- decoder

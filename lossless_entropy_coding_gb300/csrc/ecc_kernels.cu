@@ -368,17 +368,20 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     const int sms = sm_count();
     if (sms <= 0)
         return ECC_ERR_CUDA;
-    // warp-specialised kernel (two input buffers, two stage slots) when it
-    // fits, else the single-slot kernel
+    // warp-specialised kernel (two input buffers, two stage slots of warp
+    // regions) when it fits, else the single-slot kernel
     {
-        const size_t smem = enc_ws_smem_bytes(C, p.stage_bytes);
+        const uint32_t slot = enc_ws_slot_bytes(C, S);
+        const size_t smem = enc_ws_smem_bytes(C, slot);
         const int occ = smem <= kMaxDynSmem - kStaticSmemReserve
                             ? occupancy((const void *)encode_ws_kernel, kEncThreadsWS, smem)
                             : 0;
         if (occ > 0) {
-            p.nbuf = 2;
+            EncParams q = p;
+            q.nbuf = 2;
+            q.stage_bytes = slot;
             const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
-            encode_ws_kernel<<<(unsigned)grid, kEncThreadsWS, smem, st>>>(p);
+            encode_ws_kernel<<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
             return launch_status(cudaGetLastError());
         }
     }

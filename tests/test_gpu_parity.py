@@ -184,6 +184,27 @@ def test_all_256_symbols_and_worst_case_qlc():
     check_against_oracle(x, ecc.qlc_build_tables(count), oracle.qlc_codebook(count), 16384, 256)
 
 
+@pytest.mark.parametrize("book", ["huffman", "qlc_adapted"])
+def test_runs_of_a_short_code(book):
+    """92% of the bytes are one value (a 1-bit Huffman code, a 3-bit adapted
+    QLC code): many 16-symbol groups take less than a 32-bit word, so
+    several coding lanes end inside one word, also across the rounds of a
+    warp's segment -- every bit of such shared words must survive."""
+    g = np.random.default_rng(17)
+    n = (1 << 21) + 4099
+    x = np.zeros(n, np.uint8)
+    m = g.random(n) < 0.08
+    x[m] = g.integers(1, 256, int(m.sum()))
+    count = oracle.histogram(x)
+    if book == "huffman":
+        cbb, ocb = ecc.huff_build_canonical(count + np.uint64(1)), oracle.huffman_codebook(count + np.uint64(1))
+    else:
+        w, _ = oracle.qlc_search(count)
+        cbb, ocb = ecc.qlc_build_tables(count, w), oracle.qlc_codebook(count, w)
+    for C, S in ((16384, 256), (4096, 1024), (1024, 64)):
+        check_against_oracle(x, cbb, ocb, C, S)
+
+
 def test_long_codes_take_the_slow_paths():
     # Fibonacci weights: codes up to 40 bits; a tensor of the rare symbols
     # expands ~5x, past the encoder's staging buffer and the decoder's
