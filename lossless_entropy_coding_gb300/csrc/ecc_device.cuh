@@ -1529,9 +1529,9 @@ __device__ __forceinline__ uint32_t step(Stream &s, const uint32_t *words, uint3
     return e;
 }
 
-// Stream of the hot loop, reading the staged chunk in shared memory: window
-// (hi, lo) in stream order, the following word nx still in memory byte
-// order, wa the shared-memory address of the word after nx.
+// Stream of the hot loop, reading the staged chunk in shared memory: the
+// next three words (hi, lo, nx) in stream order, o the bit offset in hi
+// (< 32), wa the shared-memory address of the word after nx.
 struct FastStream {
     uint32_t hi, lo, nx, o, wa;
 };
@@ -1551,22 +1551,32 @@ __device__ __forceinline__ void lds_u32_if(uint32_t &v, uint32_t addr, bool p)
                  : "r"(addr), "r"((uint32_t)p));
 }
 
-// Hot-loop step: codes the 14-bit table resolves.  An empty entry (a longer
-// or an invalid code) has length 0, so the stream stays where it is; emin
-// records it and the caller redoes the iteration with fstep_slow.
-__device__ __forceinline__ uint32_t fstep(FastStream &s, const uint16_t *dec, uint32_t &emin)
+// Hot-loop step: two codes the 14-bit table resolves, one window refill.
+// The first code starts at o < 32 and ends by bit 45, so the second one's
+// 14-bit peek lies in (hi, lo) or (lo, nx); after both the stream has moved
+// at most 59 bits, i.e. by at most one word.  An empty entry (a longer or an
+// invalid code) has length 0, so the stream stays where it is; emin records
+// it and the caller redoes the iteration with fstep_slow.  Returns the two
+// bytes in the low half (first code's in byte 0).
+__device__ __forceinline__ uint32_t fstep2(FastStream &s, const uint16_t *dec, uint32_t &emin)
 {
-    const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
-    const uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
-    emin = min(emin, e);
-    s.o += e >> 8;
-    const bool adv = s.o >= 32;
+    const uint32_t p1 = __funnelshift_l(s.lo, s.hi, s.o);
+    const uint32_t e1 = dec[p1 >> (32 - ECC_PEEK_BITS)];
+    const uint32_t o1 = s.o + (e1 >> 8);
+    const bool in2 = o1 >= 32;
+    const uint32_t p2 = __funnelshift_l(in2 ? s.nx : s.lo, in2 ? s.lo : s.hi, o1); // shift taken mod 32
+    const uint32_t e2 = dec[p2 >> (32 - ECC_PEEK_BITS)];
+    emin = min(emin, min(e1, e2));
+    const uint32_t o2 = o1 + (e2 >> 8);
+    const bool adv = o2 >= 32;
+    uint32_t w = 0;
+    lds_u32_if(w, s.wa, adv);
     s.hi = adv ? s.lo : s.hi;
-    s.lo = adv ? bswap32(s.nx) : s.lo;
-    lds_u32_if(s.nx, s.wa, adv);
+    s.lo = adv ? s.nx : s.lo;
+    s.nx = adv ? bswap32(w) : s.nx;
     s.wa += adv ? 4u : 0u;
-    s.o &= 31;
-    return e;
+    s.o = o2 & 31;
+    return __byte_perm(e1, e2, 0x0040);
 }
 
 // Any code, long ones through the canonical ranges; invalid codes set bad.
@@ -1575,7 +1585,7 @@ __device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *de
     const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
     uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
     if (e == 0) {
-        e = decode_long_at(s.hi, s.lo, bswap32(s.nx), s.o, lt);
+        e = decode_long_at(s.hi, s.lo, s.nx, s.o, lt);
         if (e == 0) {
             bad = true;
             e = 1u << 8; // consume one bit and go on; the chunk is flagged
@@ -1584,8 +1594,8 @@ __device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *de
     s.o += e >> 8;
     while (s.o >= 32) {
         s.hi = s.lo;
-        s.lo = bswap32(s.nx);
-        s.nx = lds_u32(s.wa);
+        s.lo = s.nx;
+        s.nx = bswap32(lds_u32(s.wa));
         s.wa += 4;
         s.o -= 32;
     }
@@ -1616,7 +1626,7 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
         s[r].o = st[r] & 31;
         s[r].hi = bswap32(words[w0]);
         s[r].lo = bswap32(words[w0 + 1]);
-        s[r].nx = words[w0 + 2];
+        s[r].nx = bswap32(words[w0 + 2]);
         s[r].wa = w_base + (w0 + 3) * 4;
         dst[r] = job.out + base + (uint64_t)(g0 + (uint32_t)(r * 32 + lane)) * job.S;
         q0[r] = q1[r] = 0;
@@ -1631,16 +1641,19 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
             a[r] = b[r] = 0;
             emin[r] = ~0u;
         }
+        {
+            uint32_t h[R][4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
+            for (int t = 0; t < 4; ++t)
 #pragma unroll
-            for (int r = 0; r < R; ++r)
-                a[r] = __byte_perm(a[r], fstep(s[r], dec, emin[r]), 0x4321);
+                for (int r = 0; r < R; ++r)
+                    h[r][t] = fstep2(s[r], dec, emin[r]);
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                b[r] = __byte_perm(b[r], fstep(s[r], dec, emin[r]), 0x4321);
+            for (int r = 0; r < R; ++r) {
+                a[r] = __byte_perm(h[r][0], h[r][1], 0x5410);
+                b[r] = __byte_perm(h[r][2], h[r][3], 0x5410);
+            }
+        }
         uint32_t esc = 0; // streams of this lane that met an unresolved code
 #pragma unroll
         for (int r = 0; r < R; ++r)
