@@ -325,10 +325,19 @@ struct BatchPlan {
     int R = 4; // decode: streams per lane, the smallest any tensor allows
 };
 
-uint32_t batch_decode_warps(uint32_t stage)
+const void *batch_decode_kernel(int R)
+{
+    return R == 4 ? (const void *)decode_batched_kernel<4>
+           : R == 2 ? (const void *)decode_batched_kernel<2>
+                    : (const void *)decode_batched_kernel<1>;
+}
+
+// as many warps as shared memory holds stages for, and registers allow
+uint32_t batch_decode_warps(uint32_t stage, int R)
 {
     int warps = decode_warps(stage);
-    while (warps > 1 && kDecHeadBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve)
+    while (warps > 1 && (kDecHeadBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve ||
+                         occupancy(batch_decode_kernel(R), warps * 32, kDecHeadBytes + (size_t)warps * stage) <= 0))
         --warps;
     return (uint32_t)warps;
 }
@@ -359,8 +368,8 @@ ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool c
             P->R = std::min<int>(P->R, (int)std::max<uint32_t>(1, d.C / d.S / 32));
     }
     P->stage = stage_bytes_for(P->max_C);
-    P->warps = batch_decode_warps(P->stage);
     P->R = P->R >= 4 ? 4 : P->R >= 2 ? 2 : 1;
+    P->warps = encode ? 1u : batch_decode_warps(P->stage, P->R);
     P->order.resize(count);
     std::iota(P->order.begin(), P->order.end(), 0u);
     std::stable_sort(P->order.begin(), P->order.end(), [&](uint32_t a, uint32_t b) {
@@ -450,9 +459,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
         return launch_status(cudaGetLastError());
     }
     const size_t smem = kDecHeadBytes + (size_t)P.warps * P.stage;
-    const void *kfn = P.R == 4 ? (const void *)decode_batched_kernel<4>
-                      : P.R == 2 ? (const void *)decode_batched_kernel<2>
-                                 : (const void *)decode_batched_kernel<1>;
+    const void *kfn = batch_decode_kernel(P.R);
     const int occ = occupancy(kfn, (int)P.warps * 32, smem);
     if (occ <= 0)
         return ECC_ERR_CUDA;

@@ -33,6 +33,19 @@ constexpr uint32_t kStageGuard = 96;
 // a zeroed guard so peeks past a payload's end read zeros.
 __host__ __device__ constexpr uint32_t stage_bytes_for(uint32_t C) { return pad16((C * 11u + 7u) / 8u) + kStageGuard; }
 
+// Decoder stage of one warp: a chunk at up to 9.25 bits a symbol (larger
+// chunks are staged 32 sub-blocks at a time), and never less than 32
+// sub-blocks at 11 bits; when a chunk has fewer than 32 sub-blocks, the whole
+// chunk at 11 bits.
+__host__ __device__ constexpr uint32_t dec_stage_bytes(uint32_t C, uint32_t S)
+{
+    return C / S < 32 ? stage_bytes_for(C)
+                      : (pad16((C * 37u + 31u) / 32u) > pad16((32u * S * 11u + 7u) / 8u) + 16u
+                             ? pad16((C * 37u + 31u) / 32u)
+                             : pad16((32u * S * 11u + 7u) / 8u) + 16u) +
+                            kStageGuard;
+}
+
 // ---------------------------------------------------------------- memory ops
 __device__ __forceinline__ uint64_t ld_relaxed(const uint64_t *p)
 {
@@ -1728,6 +1741,80 @@ __device__ __forceinline__ bool chunk_range_ok(const DecJob &job, uint64_t c, ui
     return b1 > b0 && b1 <= job.in_bytes && !((b0 | b1) & 15) && (b1 - b0) <= (uint64_t)job.C * 8;
 }
 
+// A chunk too big for the warp's stage: stage and decode it 32 sub-blocks at
+// a time (one stream per lane); each group's bytes fit, since a stage holds
+// at least 32 sub-blocks at the longest fast code lengths.
+static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, const uint16_t *dec,
+                                                           const LongTable &lt, WarpStage &ws, uint64_t base,
+                                                           uint32_t nsub, uint64_t sub0, uint64_t b0, uint32_t bytes)
+{
+    const int lane = threadIdx.x & 31;
+    bool bad = false;
+    uint32_t carry = 0; // bits of the chunk's earlier groups
+    for (uint32_t g0 = 0; g0 < nsub; g0 += 32) {
+        const uint32_t v = job.sub_bits[sub0 + g0 + lane];
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(~0u, incl, o);
+            incl += lane >= o ? y : 0u;
+        }
+        const uint32_t gbits = __shfl_sync(~0u, incl, 31);
+        // the group's bytes, widened to 16-byte boundaries of the chunk
+        const uint32_t s0 = (carry >> 3) & ~15u;
+        const uint32_t s1 = min(pad16((carry + gbits + 7) >> 3), bytes);
+        if (carry + gbits > bytes * 8u) { // sub_bits claim more bits than the chunk holds
+            bad = true;
+            break;
+        }
+        if (s1 - s0 + kStageGuard > ws.bytes) {
+            // long codes: the group does not fit either; read it from global memory
+            bad |= decode_stream_generic<false>(reinterpret_cast<const uint32_t *>(job.in + b0), bytes / 4 - 1,
+                                                carry + incl - v, job.S, v,
+                                                job.out + base + (uint64_t)(g0 + lane) * job.S, dec, lt);
+            carry += gbits;
+            continue;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_expect_tx(ws.bar, s1 - s0);
+            bulk_g2s(ws.buf, job.in + b0 + s0, s1 - s0, ws.bar);
+        }
+        bool ok = __all_sync(~0u, mbar_wait(ws.bar, ws.phase, kWaitLimitNs));
+        if (!ok) // never expected: the copy reads valid memory; wait once more
+            ok = __all_sync(~0u, mbar_wait(ws.bar, ws.phase, kWaitLimitNs));
+        ws.phase ^= 1;
+        if (!ok) {
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            ws.buf = nullptr; // the copy may still land: stop using this buffer
+            return;
+        }
+        if (lane < kStageGuard / 4)
+            ws.buf[(s1 - s0) / 4 + lane] = 0; // guard: reads past the end see 0
+        __syncwarp();
+        const uint32_t st[1] = {carry + incl - v - s0 * 8u}, nb[1] = {v};
+        decode_group_fast<1>(job, dec, lt, ws.buf, (s1 - s0) / 4 + 4, base, g0, st, nb, bad);
+        carry += gbits;
+    }
+    if (pad16((carry + 7) / 8) != bytes)
+        bad = true;
+    // the padding after the last code must be zero bits
+    if (!bad && lane == 0) {
+        const uint32_t *words = reinterpret_cast<const uint32_t *>(job.in + b0);
+        for (uint32_t wi = carry >> 5; wi < bytes / 4; ++wi) {
+            uint32_t w = bswap32(__ldg(words + wi));
+            if (wi == (carry >> 5))
+                w &= 0xFFFFFFFFu >> (carry & 31);
+            bad |= w != 0;
+        }
+    }
+    if (__any_sync(~0u, bad) && lane == 0)
+        set_status(job.status, ECC_ERR_CORRUPT);
+    __syncwarp();
+}
+
 // Decode chunk c with one warp.  The compressed chunk is staged into the
 // warp's shared buffer by one bulk copy (when it fits), while the lanes scan
 // sub_bits; next_c (if valid) is prefetched into L2 for the warp's next call.
@@ -1749,6 +1836,10 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
     }
     const uint32_t bytes = (uint32_t)(b1 - b0);
     const bool staged = ws.buf != nullptr && bytes + kStageGuard <= ws.bytes;
+    if (!staged && ws.buf != nullptr && L == job.C && nsub >= 32 && (nsub & 31) == 0) {
+        decode_chunk_in_groups(job, dec, lt, ws, base, nsub, sub0, b0, bytes);
+        return;
+    }
     if (staged) {
         __syncwarp();
         if (lane == 0) {

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "ecc_device.cuh"
@@ -226,7 +227,7 @@ namespace {
 
 struct DevInfo {
     int sms = 0;
-    std::map<std::pair<const void *, size_t>, int> occ; // (kernel, smem) -> blocks/SM
+    std::map<std::tuple<const void *, int, size_t>, int> occ; // (kernel, threads, smem) -> blocks/SM
 };
 
 std::mutex g_mu;
@@ -289,7 +290,7 @@ int occupancy(const void *kernel, int threads, size_t smem)
     if (!d)
         return 0;
     std::lock_guard<std::mutex> lk(g_mu);
-    auto key = std::make_pair(kernel, smem);
+    auto key = std::make_tuple(kernel, threads, smem);
     auto it = d->occ.find(key);
     if (it != d->occ.end())
         return it->second;
@@ -411,14 +412,17 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
     DecParams p;
     p.job = DecJob{in, in_bytes, chunk_off, sub_bits, n, C, S, cb, out, status};
     p.n_chunks = ecc_num_chunks(n, C);
-    p.stage_bytes = stage_bytes_for(C);
-    const int warps = decode_warps(p.stage_bytes);
-    const size_t smem = kDecHeadBytes + (size_t)warps * p.stage_bytes;
+    p.stage_bytes = dec_stage_bytes(C, S);
     // streams per lane: C/S sub-blocks per chunk over 32 lanes, at most 4
     const uint32_t per_lane = std::min<uint32_t>(4, std::max<uint32_t>(1, C / S / 32));
     const void *kfn = per_lane == 4 ? (const void *)decode_kernel<4>
                       : per_lane == 2 ? (const void *)decode_kernel<2>
                                       : (const void *)decode_kernel<1>;
+    // as many warps as shared memory holds stages for, and registers allow
+    int warps = decode_warps(p.stage_bytes);
+    while (warps > 1 && occupancy(kfn, warps * 32, kDecHeadBytes + (size_t)warps * p.stage_bytes) <= 0)
+        --warps;
+    const size_t smem = kDecHeadBytes + (size_t)warps * p.stage_bytes;
     const int occ = occupancy(kfn, warps * 32, smem);
     const int sms = sm_count();
     if (occ <= 0 || sms <= 0)

@@ -12,7 +12,7 @@ namespace ecc {
 
 constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit (static + dynamic)
 constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may add on top
-constexpr int kDecMaxWarps = 8;
+constexpr int kDecMaxWarps = 12;
 
 bool valid_sizes(uint32_t C, uint32_t S);
 // shared input buffers of the encoder (2 = the next chunk is prefetched)
