@@ -251,7 +251,8 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
     LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes);
+    QlcShared &qs = *reinterpret_cast<QlcShared *>(smem + kDecTableBytes + kLongTableBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes + kQlcSharedBytes);
     const BatchHeader *h = reinterpret_cast<const BatchHeader *>(ws);
     const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
     const uint64_t *item = reinterpret_cast<const uint64_t *>(ws + h->item_off);
@@ -270,7 +271,7 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
                   &bars[warp], 0};
     const uint64_t groups = h->n_items / W;
     const ecc_codebook *loaded = nullptr;
-    bool loaded_ok = false;
+    bool loaded_ok = false, loaded_qlc = false;
     for (uint64_t g = blockIdx.x; g < groups; g += gridDim.x) {
         const uint64_t m0 = item[g * W]; // a group never starts on padding
         const uint64_t m = item[g * W + warp];
@@ -279,7 +280,11 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
             __syncthreads(); // every warp is done with the previous tables
             loaded = cb;
             loaded_ok = cb->magic == ECC_CODEBOOK_MAGIC && cb->max_len <= ECC_MAX_CODE_LEN;
-            if (loaded_ok) {
+            loaded_qlc = loaded_ok && qlc_mode(cb);
+            if (loaded_qlc) {
+                load_qlc_tables(reinterpret_cast<uint32_t *>(smem), qs, cb, blockDim.x);
+                load_long_table(lt, cb);
+            } else if (loaded_ok) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(cb->dec);
                 uint4 *dst = reinterpret_cast<uint4 *>(dec);
                 for (int i = threadIdx.x; i < (int)(kDecTableBytes / 16); i += blockDim.x)
@@ -296,7 +301,16 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
         const uint64_t nch = chunks_of(d);
         if (loaded_ok) {
             const DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
-            decode_chunk<R>(job, dec, lt, wst, c, nch, nch); // next chunk is another tensor's: no L2 prefetch
+            // next chunk is another tensor's: no L2 prefetch
+            if (loaded_qlc) {
+                const DecTables T = qlc_tables(cb->dec, &lt, qs, reinterpret_cast<const uint32_t *>(smem));
+                decode_chunk<R, true>(job, T, wst, c, nch, nch);
+            } else {
+                DecTables T{};
+                T.dec = dec;
+                T.lt = &lt;
+                decode_chunk<R, false>(job, T, wst, c, nch, nch);
+            }
         } else if (lane == 0) {
             set_status(d.status, ECC_ERR_CODEBOOK);
         }

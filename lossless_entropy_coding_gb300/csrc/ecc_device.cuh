@@ -1615,6 +1615,99 @@ __device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *de
     return e;
 }
 
+// QLC codes need no first-level table: the 3-bit prefix fixes the code
+// length (a byte of two registers, selected by the prefix), and the rank is
+// the whole code plus a per-prefix offset (start of the area minus prefix <<
+// width).  The stream's next position then never waits for a shared-memory
+// load; the rank -> byte lookups run beside it, in a table with one replica
+// per lane (rank r of lane l at word r * 32 + l), free of bank conflicts.
+// A rank of 256 or more is no code (an empty area, or past the last rank).
+struct QlcShared {
+    int32_t off[8];
+    uint32_t len[2]; // code length of prefixes 0..3 and 4..7, one byte each
+};
+constexpr uint32_t kQlcNoCode = 0x10000;
+
+// The decoder's tables for one codebook.
+struct DecTables {
+    const uint16_t *dec; // 14-bit first-level table: shared, or (QLC mode) the codebook's own in global memory
+    const LongTable *lt; // shared
+    uint32_t len0, len1; // QLC: code length by prefix
+    const int32_t *off;  // QLC: shared, rank = code + off[prefix]
+    uint32_t rt;         // QLC: shared-window address of the rank table + lane * 4
+};
+
+// Whether the QLC path can decode with this codebook.
+__device__ __forceinline__ bool qlc_mode(const ecc_codebook *cb)
+{
+    return cb->family == ECC_FAMILY_QLC && cb->max_len <= 11;
+}
+
+// Fill the QLC tables from the codebook: the rank table over the 32 KB of
+// the first-level table (threads [0, nthreads)).
+__device__ __forceinline__ void load_qlc_tables(uint32_t *rt, QlcShared &q, const ecc_codebook *cb, uint32_t nthreads)
+{
+    const uint32_t t = threadIdx.x;
+    for (uint32_t i = t; i < 256 * 32; i += nthreads)
+        rt[i] = cb->by_rank[i >> 5];
+    if (t < 8) {
+        const uint32_t w = cb->width[t];
+        q.off[t] = cb->area_size[t] ? (int32_t)cb->area_start[t] - (int32_t)(t << w) : (int32_t)kQlcNoCode;
+    }
+    if (t == 0) {
+        uint32_t l0 = 0, l1 = 0;
+        for (int k = 0; k < 4; ++k) {
+            l0 |= (3u + cb->width[k]) << (8 * k);
+            l1 |= (3u + cb->width[k + 4]) << (8 * k);
+        }
+        q.len[0] = l0;
+        q.len[1] = l1;
+    }
+}
+
+__device__ __forceinline__ DecTables qlc_tables(const uint16_t *gdec, const LongTable *lt, const QlcShared &q,
+                                                const uint32_t *rt)
+{
+    DecTables T;
+    T.dec = gdec;
+    T.lt = lt;
+    T.len0 = q.len[0];
+    T.len1 = q.len[1];
+    T.off = q.off;
+    T.rt = smem_u32(rt) + (threadIdx.x & 31) * 4u;
+    return T;
+}
+
+// QLC hot-loop step: two codes, one window refill, as fstep2.  vmax collects
+// the ranks (one of 256 or more: no code, the chunk is corrupt).
+__device__ __forceinline__ uint32_t qstep2(FastStream &s, const DecTables &T, uint32_t &vmax)
+{
+    const uint32_t p1 = __funnelshift_l(s.lo, s.hi, s.o);
+    const uint32_t a1 = p1 >> 29;
+    const uint32_t l1 = __byte_perm(T.len0, T.len1, a1) & 0xFFu;
+    const uint32_t o1 = s.o + l1;
+    const bool in2 = o1 >= 32;
+    const uint32_t p2 = __funnelshift_l(in2 ? s.nx : s.lo, in2 ? s.lo : s.hi, o1); // shift taken mod 32
+    const uint32_t a2 = p2 >> 29;
+    const uint32_t l2 = __byte_perm(T.len0, T.len1, a2) & 0xFFu;
+    const uint32_t o2 = o1 + l2;
+    const bool adv = o2 >= 32;
+    uint32_t w = 0;
+    lds_u32_if(w, s.wa, adv);
+    s.hi = adv ? s.lo : s.hi;
+    s.lo = adv ? s.nx : s.lo;
+    s.nx = adv ? bswap32(w) : s.nx;
+    s.wa += adv ? 4u : 0u;
+    s.o = o2 & 31;
+    // beside the stream: ranks and bytes
+    const uint32_t r1 = __funnelshift_l(p1, 0u, l1) + (uint32_t)T.off[a1];
+    const uint32_t r2 = __funnelshift_l(p2, 0u, l2) + (uint32_t)T.off[a2];
+    vmax = max(vmax, max(r1, r2));
+    const uint32_t b1 = lds_u32(T.rt + min(r1, 255u) * 128u);
+    const uint32_t b2 = lds_u32(T.rt + min(r2, 255u) * 128u);
+    return __byte_perm(b1, b2, 0x0040);
+}
+
 // Hot loop: R full sub-blocks per lane from a staged chunk, 8 symbols per
 // stream per iteration, output as 16-byte stores every second iteration.
 // The loop body has no branch, so the R streams interleave; a lane that met
@@ -1622,11 +1715,14 @@ __device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *de
 // with fstep_slow (rare: codes longer than 14 bits, or corrupt data).
 // wmax: the highest word index a stream may reach at an iteration start; a
 // stream moves at most 16 words per iteration, into the zeroed guard.
-template <int R>
-__device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint16_t *dec, const LongTable &lt,
-                                                  const uint32_t *words, uint32_t wmax, uint64_t base, uint32_t g0,
+template <int R, bool kQlc>
+__device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTables &T, const uint32_t *words,
+                                                  uint32_t wmax, uint64_t base, uint32_t g0,
                                                   const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
 {
+    const uint16_t *dec = T.dec;
+    const LongTable &lt = *T.lt;
+    uint32_t vmax = 0;
     const int lane = threadIdx.x & 31;
     const uint32_t w_base = smem_u32(words);
     const uint32_t a_max = w_base + wmax * 4;
@@ -1660,7 +1756,7 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
             for (int t = 0; t < 4; ++t)
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    h[r][t] = fstep2(s[r], dec, emin[r]);
+                    h[r][t] = kQlc ? qstep2(s[r], T, vmax) : fstep2(s[r], dec, emin[r]);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 a[r] = __byte_perm(h[r][0], h[r][1], 0x5410);
@@ -1670,8 +1766,8 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
         uint32_t esc = 0; // streams of this lane that met an unresolved code
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            esc |= (emin[r] == 0) ? (1u << r) : 0u;
-        if (__any_sync(~0u, esc != 0)) {
+            esc |= (!kQlc && emin[r] == 0) ? (1u << r) : 0u;
+        if (!kQlc && __any_sync(~0u, esc != 0)) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (!(esc & (1u << r)))
@@ -1702,6 +1798,8 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const uint1
     for (int r = 0; r < R; ++r)
         if ((s[r].wa - w_base) / 4 * 32 - 96 + s[r].o - st[r] != nb[r]) // position = (word of hi) * 32 + o
             bad = true;
+    if (kQlc && vmax > 255)
+        bad = true;
 }
 
 // Any other sub-block (the tensor's last, partial chunk, or a chunk read
@@ -1724,7 +1822,8 @@ static __device__ __noinline__ bool decode_stream_generic(const uint32_t *words,
 constexpr uint32_t kDecTableBytes = sizeof(((ecc_codebook *)0)->dec);
 constexpr uint32_t kLongTableBytes = (sizeof(LongTable) + 15u) & ~15u;
 constexpr uint32_t kDecBarSlots = 16; // one mbarrier per warp
-constexpr uint32_t kDecHeadBytes = kDecTableBytes + kLongTableBytes + kDecBarSlots * 8;
+constexpr uint32_t kQlcSharedBytes = (sizeof(QlcShared) + 15u) & ~15u;
+constexpr uint32_t kDecHeadBytes = kDecTableBytes + kLongTableBytes + kQlcSharedBytes + kDecBarSlots * 8;
 
 // Per-warp staging state: the chunk buffer, its mbarrier and phase.
 struct WarpStage {
@@ -1744,10 +1843,13 @@ __device__ __forceinline__ bool chunk_range_ok(const DecJob &job, uint64_t c, ui
 // A chunk too big for the warp's stage: stage and decode it 32 sub-blocks at
 // a time (one stream per lane); each group's bytes fit, since a stage holds
 // at least 32 sub-blocks at the longest fast code lengths.
-static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, const uint16_t *dec,
-                                                           const LongTable &lt, WarpStage &ws, uint64_t base,
-                                                           uint32_t nsub, uint64_t sub0, uint64_t b0, uint32_t bytes)
+template <bool kQlc>
+static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, const DecTables &T, WarpStage &ws,
+                                                           uint64_t base, uint32_t nsub, uint64_t sub0, uint64_t b0,
+                                                           uint32_t bytes)
 {
+    const uint16_t *dec = T.dec;
+    const LongTable &lt = *T.lt;
     const int lane = threadIdx.x & 31;
     bool bad = false;
     uint32_t carry = 0; // bits of the chunk's earlier groups
@@ -1795,7 +1897,7 @@ static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, co
             ws.buf[(s1 - s0) / 4 + lane] = 0; // guard: reads past the end see 0
         __syncwarp();
         const uint32_t st[1] = {carry + incl - v - s0 * 8u}, nb[1] = {v};
-        decode_group_fast<1>(job, dec, lt, ws.buf, (s1 - s0) / 4 + 4, base, g0, st, nb, bad);
+        decode_group_fast<1, kQlc>(job, T, ws.buf, (s1 - s0) / 4 + 4, base, g0, st, nb, bad);
         carry += gbits;
     }
     if (pad16((carry + 7) / 8) != bytes)
@@ -1818,10 +1920,12 @@ static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, co
 // Decode chunk c with one warp.  The compressed chunk is staged into the
 // warp's shared buffer by one bulk copy (when it fits), while the lanes scan
 // sub_bits; next_c (if valid) is prefetched into L2 for the warp's next call.
-template <int R>
-__device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *dec, const LongTable &lt,
-                                             WarpStage &ws, uint64_t c, uint64_t next_c, uint64_t n_chunks)
+template <int R, bool kQlc>
+__device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables &T, WarpStage &ws, uint64_t c,
+                                             uint64_t next_c, uint64_t n_chunks)
 {
+    const uint16_t *dec = T.dec;
+    const LongTable &lt = *T.lt;
     const int lane = threadIdx.x & 31;
     const uint64_t base = c * job.C;
     const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
@@ -1837,7 +1941,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
     const uint32_t bytes = (uint32_t)(b1 - b0);
     const bool staged = ws.buf != nullptr && bytes + kStageGuard <= ws.bytes;
     if (!staged && ws.buf != nullptr && L == job.C && nsub >= 32 && (nsub & 31) == 0) {
-        decode_chunk_in_groups(job, dec, lt, ws, base, nsub, sub0, b0, bytes);
+        decode_chunk_in_groups<kQlc>(job, T, ws, base, nsub, sub0, b0, bytes);
         return;
     }
     if (staged) {
@@ -1898,7 +2002,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const uint16_t *
         // the hot loop needs every lane to own R full sub-blocks
         if (staged && L == job.C && nsub - g0 >= 32u * R) {
             const uint32_t wmax = bytes / 4 + 4; // + up to 2 words per step x 8 steps < guard
-            decode_group_fast<R>(job, dec, lt, words, wmax, base, g0, st, nb, bad);
+            decode_group_fast<R, kQlc>(job, T, words, wmax, base, g0, st, nb, bad);
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {

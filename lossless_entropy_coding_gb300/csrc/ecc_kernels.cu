@@ -184,20 +184,25 @@ __global__ void decode_kernel(DecParams p)
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
     LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes);
+    QlcShared &qs = *reinterpret_cast<QlcShared *>(smem + kDecTableBytes + kLongTableBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes + kQlcSharedBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = blockDim.x >> 5;
-    if (p.job.cb->magic != ECC_CODEBOOK_MAGIC || p.job.cb->max_len > ECC_MAX_CODE_LEN) {
+    const ecc_codebook *cb = p.job.cb;
+    if (cb->magic != ECC_CODEBOOK_MAGIC || cb->max_len > ECC_MAX_CODE_LEN) {
         if (threadIdx.x == 0 && blockIdx.x == 0)
             set_status(p.job.status, ECC_ERR_CODEBOOK);
         return;
     }
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.job.cb->dec);
+    const bool qlc = qlc_mode(cb);
+    if (qlc) {
+        load_qlc_tables(reinterpret_cast<uint32_t *>(smem), qs, cb, blockDim.x);
+    } else {
+        const uint4 *src = reinterpret_cast<const uint4 *>(cb->dec);
         uint4 *dst = reinterpret_cast<uint4 *>(dec);
         for (int i = threadIdx.x; i < (int)(kDecTableBytes / 16); i += blockDim.x)
             dst[i] = src[i];
     }
-    load_long_table(lt, p.job.cb);
+    load_long_table(lt, cb);
     if (lane == 0) {
         mbar_init(&bars[warp], 1);
         fence_mbar_init();
@@ -206,8 +211,17 @@ __global__ void decode_kernel(DecParams p)
     WarpStage ws{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * p.stage_bytes), p.stage_bytes,
                  &bars[warp], 0};
     const uint64_t stride = (uint64_t)gridDim.x * warps;
-    for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += stride)
-        decode_chunk<R>(p.job, dec, lt, ws, c, c + stride, p.n_chunks);
+    if (qlc) {
+        const DecTables T = qlc_tables(cb->dec, &lt, qs, reinterpret_cast<const uint32_t *>(smem));
+        for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += stride)
+            decode_chunk<R, true>(p.job, T, ws, c, c + stride, p.n_chunks);
+    } else {
+        DecTables T{};
+        T.dec = dec;
+        T.lt = &lt;
+        for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += stride)
+            decode_chunk<R, false>(p.job, T, ws, c, c + stride, p.n_chunks);
+    }
 }
 
 // ---------------------------------------------------------------- self-test

@@ -287,6 +287,29 @@ def test_corrupt_streams_are_flagged():
         assert int(st.item()) == ecc.ERR_CORRUPT
 
 
+def test_qlc_code_of_an_empty_area_is_corrupt():
+    """Widths (8, 0, ..., 0): area 0 holds every rank, areas 1..7 are empty,
+    so a code whose 3-bit prefix is not 000 is no code; planting one in a
+    sub-block must flag the stream, in every decoder path."""
+    g = np.random.default_rng(23)
+    x = g.integers(0, 256, 1 << 16).astype(np.uint8)
+    count = oracle.histogram(x)
+    cbb = ecc.qlc_build_tables(count, (8, 0, 0, 0, 0, 0, 0, 0))
+    ocb = oracle.qlc_codebook(count, (8, 0, 0, 0, 0, 0, 0, 0))
+    check_against_oracle(x, cbb, ocb, 16384, 256)
+    dcb = ecc.to_device(cbb)
+    for C, S in ((16384, 256), (4096, 64), (1024, 1024)):
+        enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), dcb, C, S, max_len=11)
+        torch.cuda.synchronize()
+        off = u64(enc.chunk_off)
+        bad = ecc.Encoded(enc.payload.clone(), enc.chunk_off, enc.sub_bits, enc.total_bits, enc.status,
+                          enc.n, enc.C, enc.S)
+        bad.payload[int(off[2])] |= 0x80  # chunk 2, sub-block 0: its first code now has prefix 1xx
+        out, st = ecc.ecc_decode(bad, dcb)
+        torch.cuda.synchronize()
+        assert int(st.item()) == ecc.ERR_CORRUPT
+
+
 def test_bounded_wait_times_out():
     """The look-back wait gives up and reports ECC_ERR_TIMEOUT when no
     predecessor ever publishes (nothing here sets the flags)."""
