@@ -350,8 +350,10 @@ const void *batch_decode_kernel(int R)
 uint32_t batch_decode_warps(uint32_t stage, int R)
 {
     int warps = decode_warps(stage);
-    while (warps > 1 && (kDecHeadBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve ||
-                         occupancy(batch_decode_kernel(R), warps * 32, kDecHeadBytes + (size_t)warps * stage) <= 0))
+    while (warps > 1 &&
+           (kDecHeadBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve ||
+            occupancy(batch_decode_kernel(R), warps * 32,
+                      std::max<size_t>(kDecMinSmem, kDecHeadBytes + (size_t)warps * stage)) <= 0))
         --warps;
     return (uint32_t)warps;
 }
@@ -472,7 +474,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
         encode_batched_kernel<<<(unsigned)grid, kEncThreads, smem, st>>>((uint8_t *)ws, t_start);
         return launch_status(cudaGetLastError());
     }
-    const size_t smem = kDecHeadBytes + (size_t)P.warps * P.stage;
+    const size_t smem = std::max<size_t>(kDecMinSmem, kDecHeadBytes + (size_t)P.warps * P.stage);
     const void *kfn = batch_decode_kernel(P.R);
     const int occ = occupancy(kfn, (int)P.warps * 32, smem);
     if (occ <= 0)

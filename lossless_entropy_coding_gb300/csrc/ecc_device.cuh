@@ -1622,11 +1622,15 @@ __device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *de
 // load; the rank -> byte lookups run beside it, in a table with one replica
 // per lane (rank r of lane l at word r * 32 + l), free of bank conflicts.
 // A rank of 256 or more is no code (an empty area, or past the last rank).
+// Ranks stay below 512 (an empty area's offset maps its codes to 256 +
+// suffix), so the lookup needs no clamp: it reads within the first 64 KiB
+// of the CTA's shared memory, which the launch always provides.
 struct QlcShared {
     int32_t off[8];
     uint32_t len[2]; // code length of prefixes 0..3 and 4..7, one byte each
 };
-constexpr uint32_t kQlcNoCode = 0x10000;
+// shared memory a decoder launch always provides, covering QLC rank lookups
+constexpr uint32_t kDecMinSmem = 64u * 1024u + 128u;
 
 // The decoder's tables for one codebook.
 struct DecTables {
@@ -1652,7 +1656,7 @@ __device__ __forceinline__ void load_qlc_tables(uint32_t *rt, QlcShared &q, cons
         rt[i] = cb->by_rank[i >> 5];
     if (t < 8) {
         const uint32_t w = cb->width[t];
-        q.off[t] = cb->area_size[t] ? (int32_t)cb->area_start[t] - (int32_t)(t << w) : (int32_t)kQlcNoCode;
+        q.off[t] = (cb->area_size[t] ? (int32_t)cb->area_start[t] : 256) - (int32_t)(t << w);
     }
     if (t == 0) {
         uint32_t l0 = 0, l1 = 0;
@@ -1703,8 +1707,8 @@ __device__ __forceinline__ uint32_t qstep2(FastStream &s, const DecTables &T, ui
     const uint32_t r1 = __funnelshift_l(p1, 0u, l1) + (uint32_t)T.off[a1];
     const uint32_t r2 = __funnelshift_l(p2, 0u, l2) + (uint32_t)T.off[a2];
     vmax = max(vmax, max(r1, r2));
-    const uint32_t b1 = lds_u32(T.rt + min(r1, 255u) * 128u);
-    const uint32_t b2 = lds_u32(T.rt + min(r2, 255u) * 128u);
+    const uint32_t b1 = lds_u32(T.rt + r1 * 128u);
+    const uint32_t b2 = lds_u32(T.rt + r2 * 128u);
     return __byte_perm(b1, b2, 0x0040);
 }
 

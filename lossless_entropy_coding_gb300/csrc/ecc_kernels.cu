@@ -434,9 +434,10 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
                                       : (const void *)decode_kernel<1>;
     // as many warps as shared memory holds stages for, and registers allow
     int warps = decode_warps(p.stage_bytes);
-    while (warps > 1 && occupancy(kfn, warps * 32, kDecHeadBytes + (size_t)warps * p.stage_bytes) <= 0)
+    auto smem_for = [&](int w) { return std::max<size_t>(kDecMinSmem, kDecHeadBytes + (size_t)w * p.stage_bytes); };
+    while (warps > 1 && occupancy(kfn, warps * 32, smem_for(warps)) <= 0)
         --warps;
-    const size_t smem = kDecHeadBytes + (size_t)warps * p.stage_bytes;
+    const size_t smem = smem_for(warps);
     const int occ = occupancy(kfn, warps * 32, smem);
     const int sms = sm_count();
     if (occ <= 0 || sms <= 0)
