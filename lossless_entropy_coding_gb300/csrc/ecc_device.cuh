@@ -1637,6 +1637,7 @@ struct DecTables {
     const uint16_t *dec; // 14-bit first-level table: shared, or (QLC mode) the codebook's own in global memory
     const LongTable *lt; // shared
     uint32_t len0, len1; // QLC: code length by prefix
+    uint32_t lg;         // QLC: the upper bytes a byte-permute of (len0, len1) by a prefix leaves (byte 0 of len0 in each)
     const int32_t *off;  // QLC: shared, rank = code + off[prefix]
     uint32_t rt;         // QLC: shared-window address of the rank table + lane * 4
 };
@@ -1677,6 +1678,7 @@ __device__ __forceinline__ DecTables qlc_tables(const uint16_t *gdec, const Long
     T.lt = lt;
     T.len0 = q.len[0];
     T.len1 = q.len[1];
+    T.lg = (q.len[0] & 0xFFu) * 0x01010100u;
     T.off = q.off;
     T.rt = smem_u32(rt) + (threadIdx.x & 31) * 4u;
     return T;
@@ -1686,15 +1688,17 @@ __device__ __forceinline__ DecTables qlc_tables(const uint16_t *gdec, const Long
 // the ranks (one of 256 or more: no code, the chunk is corrupt).
 __device__ __forceinline__ uint32_t qstep2(FastStream &s, const DecTables &T, uint32_t &vmax)
 {
+    // the permute leaves len[prefix] in byte 0 and byte 0 of len0 in bytes
+    // 1..3: lg removes those; a funnel shift only uses the low 5 bits anyway
     const uint32_t p1 = __funnelshift_l(s.lo, s.hi, s.o);
     const uint32_t a1 = p1 >> 29;
-    const uint32_t l1 = __byte_perm(T.len0, T.len1, a1) & 0xFFu;
-    const uint32_t o1 = s.o + l1;
+    const uint32_t l1 = __byte_perm(T.len0, T.len1, a1);
+    const uint32_t o1 = s.o + l1 - T.lg;
     const bool in2 = o1 >= 32;
     const uint32_t p2 = __funnelshift_l(in2 ? s.nx : s.lo, in2 ? s.lo : s.hi, o1); // shift taken mod 32
     const uint32_t a2 = p2 >> 29;
-    const uint32_t l2 = __byte_perm(T.len0, T.len1, a2) & 0xFFu;
-    const uint32_t o2 = o1 + l2;
+    const uint32_t l2 = __byte_perm(T.len0, T.len1, a2);
+    const uint32_t o2 = o1 + l2 - T.lg;
     const bool adv = o2 >= 32;
     uint32_t w = 0;
     lds_u32_if(w, s.wa, adv);
