@@ -206,6 +206,31 @@ size_t ecc_encode_workspace_bytes(size_t n, uint32_t C);
 ecc_status e4m3_histogram(const uint8_t *in, size_t n, uint64_t *count, void *stream);
 
 /*
+ * huff_build_device -- the canonical Huffman codebook built on the device,
+ * stream-ordered after e4m3_histogram, so that frequency analysis, codebook
+ * construction and encoding (the three stages a per-tensor Huffman pipeline
+ * runs, "Single-Stage Huffman Encoder for ML Compression", introduction)
+ * need no host round trip; also a codebook refresh from fresh counts when
+ * the data drift (same page, discussion).  One CTA, a few tens of
+ * microseconds.
+ *   count    device uint64[256] (e.g. the histogram); read only.
+ *   add      pseudocount added to every count: the weights are
+ *            count[b] + add, with the meaning huff_build_canonical gives
+ *            them; the output is byte-identical to that builder's.
+ *   max_len  1..ECC_MAX_CODE_LEN, as for huff_build_canonical.
+ *   out      device ecc_codebook, 16-byte aligned; always rewritten.  On a
+ *            device error it is left all zero (no magic word), so every call
+ *            that is handed it reports ECC_ERR_CODEBOOK.
+ *   status   device uint32[1]; ECC_OK, or ECC_ERR_ARG (a weight or the
+ *            weight sum does not fit 64 bits, all weights 0) or
+ *            ECC_ERR_CODEBOOK (tree deeper than max_len).
+ * Host errors: ECC_ERR_ARG (NULL, misaligned out, max_len out of range),
+ * ECC_ERR_CUDA.  Calls that read `out` must be ordered after this one.
+ */
+ecc_status huff_build_device(const uint64_t *count, uint64_t add, uint32_t max_len, ecc_codebook *out,
+                             uint32_t *status, void *stream);
+
+/*
  * ecc_encode -- single-stage encode with a fixed codebook ("Quad Length
  * Codes ...", section 2 "Codifica": the encoder looks the code up in the
  * LUT; "Single-Stage Huffman ...", Methodology step 4: encode with the

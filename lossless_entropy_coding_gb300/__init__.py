@@ -78,6 +78,7 @@ def _load():
             "ecc_max_encoded_bytes": (Z, [Z, U32, U32]),
             "ecc_encode_workspace_bytes": (Z, [Z, U32]),
             "e4m3_histogram": (I32, [P, Z, P, P]),
+            "huff_build_device": (I32, [P, U64, U32, P, P, P]),
             "ecc_encode": (I32, [P, Z, P, U32, U32, P, Z, P, P, P, P, Z, P, P]),
             "ecc_decode": (I32, [P, Z, P, P, Z, U32, U32, P, P, P, P]),
             "ecc_batched_workspace_bytes": (Z, [P, U32]),
@@ -227,6 +228,22 @@ def e4m3_histogram(x, count=None, stream=None):
         count = torch.zeros(256, dtype=torch.int64, device=x.device)
     _check(_load().e4m3_histogram(_dptr(x), x.numel(), _dptr(count), _stream_ptr(stream)), "e4m3_histogram")
     return count
+
+
+def huff_build_device(count, add: int = 1, max_len: int = MAX_CODE_LEN, out=None, status=None, stream=None):
+    """Build the canonical Huffman codebook of weights count + add on the
+    device (count: int64[256] device tensor, e.g. from e4m3_histogram).
+    Returns (codebook uint8 device tensor, status int32[1] device tensor);
+    nothing is synchronised, read status after the stream reaches the call."""
+    torch = _torch()
+    dev = count.device
+    if out is None:
+        out = torch.empty(codebook_bytes(), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(_load().huff_build_device(_dptr(count), int(add), int(max_len), _dptr(out), _dptr(status),
+                                     _stream_ptr(stream)), "huff_build_device")
+    return out, status
 
 
 @dataclass
