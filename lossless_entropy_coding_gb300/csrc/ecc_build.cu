@@ -26,9 +26,10 @@ constexpr int kBuildWarps = kBuildThreads / 32;
 constexpr int kMaxNodes = 511; // 256 leaves + 255 merges
 
 struct BuildShared {
-    uint64_t aw[256];     // leaves sorted by key: weight, or the packed key
+    uint64_t aw[257];     // leaves sorted by key: weight, or the packed key;
+                          // aw[256] = ~0 ends the queue when all 256 are leaves
     uint64_t bw[256];     // internal nodes in creation order: same
-    uint16_t ab[256];     // leaves: byte value (unpacked keys only)
+    uint16_t ab[257];     // leaves: byte value (unpacked keys only)
     uint16_t bb[256];     // internal nodes: smallest byte below (unpacked only)
     int16_t parent[512];  // node -> internal node index; leaves are nodes
                           // 0..255 (by byte), internal node k is 256 + k
@@ -38,9 +39,10 @@ struct BuildShared {
     uint64_t next[65];    // first canonical code of each length
     uint32_t index[65];   // position in sorted[] of the first code of each length
     uint32_t dec_lo[ECC_PEEK_BITS + 1], dec_hi[ECC_PEEK_BITS + 1]; // peek range of each length
+    uint64_t warp_sum[kBuildWarps]; // weight sum of each warp's bytes
+    uint32_t warp_wrap[kBuildWarps]; // ... did not fit 64 bits
     uint32_t warp_n[kBuildWarps];
     uint32_t err;
-    uint32_t packed;
 };
 
 constexpr size_t kBuildCbOffset = (sizeof(BuildShared) + 15) / 16 * 16;
@@ -100,14 +102,14 @@ __device__ __forceinline__ void bitonic(BuildShared &sh, uint64_t &kw, uint32_t 
 // internal nodes in creation order, therefore reproduce the heap exactly:
 // each pop takes the smaller head.  Each queue keeps its head and the next
 // node in registers plus a pending load of the node after that (index
-// clamped; a node not yet created reads as junk and is replaced when it is
+// clamped; a node not yet created reads as ~0 and is replaced when it is
 // created), so a pop consumes a load issued one pop earlier and the loop's
 // dependency chain holds compares and selects only.  Run by one thread.
 template <bool kPacked>
 __device__ __noinline__ void merge_queues(BuildShared &sh, uint32_t n)
 {
     uint32_t ia = 0, ib = 0, nb = 0;
-    uint64_t a0w = sh.aw[0], a1w = sh.aw[1], paw = sh.aw[2], b0w = 0, b1w = 0, pbw = 0;
+    uint64_t a0w = sh.aw[0], a1w = sh.aw[1], paw = sh.aw[2], b0w = ~0ull, b1w = ~0ull, pbw = ~0ull;
     uint32_t a0b = 0, a1b = 0, pab = 0, b0b = 0, b1b = 0, pbb = 0;
     if (!kPacked)
         a0b = sh.ab[0], a1b = sh.ab[1], pab = sh.ab[2];
@@ -116,8 +118,11 @@ __device__ __noinline__ void merge_queues(BuildShared &sh, uint32_t n)
         uint32_t b2[2], id2[2];
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            const bool lt = kPacked ? a0w < b0w : key_less(a0w, a0b, b0w, b0b);
-            const bool take_a = (ia < n) & ((ib == nb) | lt);
+            // packed: leaves past the last and internal nodes not yet
+            // created hold the key ~0, above every real key, so the compare
+            // alone decides
+            const bool take_a =
+                kPacked ? a0w < b0w : (ia < n) & ((ib == nb) | key_less(a0w, a0b, b0w, b0b));
             w2[p] = take_a ? a0w : b0w;
             b2[p] = take_a ? a0b : b0b;
             id2[p] = take_a ? (kPacked ? (uint32_t)(a0w & 255u) : a0b) : 256u + ib;
@@ -129,7 +134,7 @@ __device__ __noinline__ void merge_queues(BuildShared &sh, uint32_t n)
             }
             ia += take_a ? 1u : 0u;
             ib += take_a ? 0u : 1u;
-            const uint32_t ja = min(ia + 2, 255u), jb = min(ib + 2, 255u);
+            const uint32_t ja = min(ia + 2, 256u), jb = min(ib + 2, 255u);
             paw = sh.aw[ja];
             pbw = sh.bw[jb];
             if (!kPacked)
@@ -187,61 +192,65 @@ __global__ void __launch_bounds__(kBuildThreads) huff_build_kernel(const uint64_
     // ---- 1. weights; the codebook starts all zero, as the host builder's
     // (on an error it is copied out so, without its magic word, and every
     // call that is handed it rejects it)
+    const uint64_t c = count[t];
     {
         uint2 *z = reinterpret_cast<uint2 *>(cbs);
         for (uint32_t i = t; i < sizeof(ecc_codebook) / 8; i += kBuildThreads)
             z[i] = make_uint2(0, 0);
     }
-    const uint64_t c = count[t];
     const uint64_t wb = c + add;
     const bool present = wb != 0;
     const unsigned ball = __ballot_sync(~0u, present);
-    if (lane == 0)
-        sh.warp_n[warp] = __popc(ball);
+    // the total weight must fit 64 bits and be nonzero: a butterfly sum per
+    // warp that notes any wrap, then the eight warp sums
+    {
+        uint64_t sum = wb;
+        bool wrap = c > ~0ull - add;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const uint64_t s2 = __shfl_xor_sync(~0u, sum, o);
+            wrap = __shfl_xor_sync(~0u, (int)wrap, o) != 0 || wrap || s2 > ~0ull - sum;
+            sum += s2;
+        }
+        if (lane == 0) {
+            sh.warp_n[warp] = __popc(ball);
+            sh.warp_sum[warp] = sum;
+            sh.warp_wrap[warp] = wrap;
+        }
+    }
     if (t <= 64)
         sh.bl_count[t] = 0;
     for (int k = t; k < kBuildWarps * (ECC_MAX_CODE_LEN + 1); k += kBuildThreads)
         (&sh.warp_len[0][0])[k] = 0;
     sh.parent[t] = -1;
     sh.parent[t + 256] = -1;
-    sh.bw[t] = 0;
+    sh.bw[t] = ~0ull; // internal nodes not yet created: keys above every node's
     sh.bb[t] = 0;
-    // the total weight must fit 64 bits and be nonzero (warp 0: eight
-    // weights a lane, then a butterfly sum that notes any wrap)
-    if (warp == 0) {
-        uint64_t s = 0;
-        bool wrap = false;
-        for (int k = 0; k < 8; ++k) {
-            const uint64_t v0 = count[lane * 8 + k], v = v0 + add;
-            wrap |= (v0 > ~0ull - add) | (v > ~0ull - s);
-            s += v;
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const uint64_t s2 = __shfl_xor_sync(~0u, s, o);
-            wrap |= __shfl_xor_sync(~0u, (int)wrap, o) != 0;
-            wrap |= s2 > ~0ull - s;
-            s += s2;
-        }
-        if (lane == 0) {
-            sh.err = wrap || s == 0 ? (uint32_t)ECC_ERR_ARG : 0u;
-            sh.packed = (s >> 55) == 0;
-        }
+    if (t == 0) {
+        sh.err = 0;
+        sh.aw[256] = ~0ull;
+        sh.ab[256] = 0;
     }
     __syncthreads();
     uint32_t n_leaves = 0;
+    uint64_t total = 0;
+    bool bad = false;
 #pragma unroll
-    for (int k = 0; k < kBuildWarps; ++k)
+    for (int k = 0; k < kBuildWarps; ++k) {
         n_leaves += sh.warp_n[k];
-    if (sh.err) {
+        bad |= sh.warp_wrap[k] != 0 || sh.warp_sum[k] > ~0ull - total;
+        total += sh.warp_sum[k];
+    }
+    if (bad || total == 0) {
         copy_out(cbs, out);
         if (t == 0)
-            *status = sh.err;
+            *status = ECC_ERR_ARG;
         return;
     }
+    const bool packed = (total >> 55) == 0;
 
     // ---- 2-3. sorted leaves (absent bytes last), then the merges
-    if (sh.packed) {
+    if (packed) {
         uint64_t kw = present ? (wb << 8 | (uint32_t)t) : ~0ull;
         uint32_t kb = 0;
         bitonic<true>(sh, kw, kb);
@@ -303,13 +312,14 @@ __global__ void __launch_bounds__(kBuildThreads) huff_build_kernel(const uint64_
         const uint32_t k1 = lane + 1, k2 = lane + 33;
         uint64_t f1 = 0, f2 = 0;
         uint32_t i1 = 0, i2 = 0;
-        for (uint32_t j = 1; j < k2; ++j) {
+#pragma unroll
+        for (uint32_t j = 1; j < 64; ++j) {
             const uint32_t bl = sh.bl_count[j];
-            const bool below1 = j < k1;
-            f1 += below1 ? (uint64_t)bl << (k1 - j) : 0ull;
+            const bool below1 = j < k1, below2 = j < k2;
+            f1 += below1 ? (uint64_t)bl << ((k1 - j) & 63) : 0ull;
             i1 += below1 ? bl : 0u;
-            f2 += (uint64_t)bl << (k2 - j);
-            i2 += bl;
+            f2 += below2 ? (uint64_t)bl << ((k2 - j) & 63) : 0ull;
+            i2 += below2 ? bl : 0u;
         }
         sh.next[k1] = f1;
         sh.next[k2] = f2;
@@ -359,6 +369,7 @@ __global__ void __launch_bounds__(kBuildThreads) huff_build_kernel(const uint64_
     // under longer codes stay 0.
     for (uint32_t k = 1; k <= ECC_PEEK_BITS; ++k) {
         const uint32_t lo = sh.dec_lo[k], hi = sh.dec_hi[k], base = sh.index[k];
+#pragma unroll 4
         for (uint32_t i = lo + t; i < hi; i += kBuildThreads)
             cbs->dec[i] = (uint16_t)(sh.sorted[base + ((i - lo) >> (ECC_PEEK_BITS - k))] | (k << 8));
     }

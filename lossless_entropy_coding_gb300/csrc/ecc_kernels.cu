@@ -15,47 +15,111 @@
 namespace ecc {
 
 // ---------------------------------------------------------------- histogram
-// e4m3_histogram: per-warp sub-histograms in shared memory (privatised bins:
-// lanes of different warps never collide), 16-byte streaming loads, one
-// 64-bit global atomic per non-empty bin per CTA at the end.
-constexpr int kHistThreads = 512;
-constexpr int kHistWarps = kHistThreads / 32;
+// e4m3_histogram: lane-private counters in shared memory, counter b of lane
+// l at word b * 32 + l, so every lane of a shared atomic hits its own bank
+// and no two lanes of one instruction share an address (one pass per warp
+// instruction, whatever the byte distribution).  All 16 warps of a CTA
+// share the one 32 KB set: atomics of different instructions to one address
+// cost no extra pass.  Each warp streams 4 KB chunks (8 16-byte vectors a
+// lane, the next chunk's loads in flight while this one is counted) and asks
+// L2 for the chunk after that with a bulk prefetch.  At the end one warp per
+// bin sums the 32 lanes' counters and adds them to the 64-bit count with one
+// global atomic per non-empty bin per CTA.  A counter sums the bytes of one
+// lane position of 16 warps, about n / (CTAs x 32): it fits 32 bits while n
+// < 2^37 x CTAs, for any tensor that fits in device memory.
+constexpr int kHistWarps = 16;
+constexpr int kHistThreads = kHistWarps * 32;
+constexpr int kHistVec = 8;                                // 16-byte vectors a lane per chunk
+constexpr uint32_t kHistChunk = 32 * kHistVec * 16;        // bytes a warp counts per chunk
+constexpr size_t kHistSmem = 256 * 32 * 4;
 
-__global__ void __launch_bounds__(kHistThreads) hist_kernel(const uint8_t *in, uint64_t n, uint64_t head,
-                                                            unsigned long long *count)
+// L2 prefetch of the chunk at byte offset off of the body, if any
+__device__ __forceinline__ void prefetch_chunk(const uint8_t *body, uint64_t off, uint64_t body_bytes)
 {
-    __shared__ uint32_t h[kHistWarps][256];
-    const int tid = threadIdx.x, warp = tid >> 5;
-    for (int i = tid; i < kHistWarps * 256; i += kHistThreads)
-        (&h[0][0])[i] = 0;
+    if (off < body_bytes)
+        prefetch_l2(body + off, (uint32_t)(body_bytes - off < kHistChunk ? body_bytes - off : kHistChunk));
+}
+
+__device__ __forceinline__ void count_word(uint32_t *mine, uint32_t w)
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        atomicAdd(mine + (byte_of(w, k) << 5), 1u);
+}
+
+__global__ void __launch_bounds__(kHistThreads, 1) hist_kernel(const uint8_t *in, uint64_t n, uint64_t head,
+                                                              unsigned long long *count)
+{
+    extern __shared__ __align__(16) uint32_t hist_smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t *const mine = hist_smem + lane;
+    for (int i = tid; i < 256 * 32 / 4; i += kHistThreads)
+        reinterpret_cast<uint4 *>(hist_smem)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
-    uint32_t *mine = h[warp];
-    // unaligned head and the tail bytes: block 0
+    // unaligned head and the tail bytes: CTA 0
     const uint64_t nvec = (n - head) / 16;
     const uint64_t tail0 = head + nvec * 16;
     if (blockIdx.x == 0) {
         for (uint64_t i = tid; i < head; i += kHistThreads)
-            atomicAdd(&mine[in[i]], 1u);
+            atomicAdd(mine + ((uint32_t)in[i] << 5), 1u);
         for (uint64_t i = tail0 + tid; i < n; i += kHistThreads)
-            atomicAdd(&mine[in[i]], 1u);
+            atomicAdd(mine + ((uint32_t)in[i] << 5), 1u);
     }
-    const uint8_t *body = in + head;
-    const uint64_t stride = (uint64_t)gridDim.x * kHistThreads;
-    for (uint64_t i = (uint64_t)blockIdx.x * kHistThreads + tid; i < nvec; i += stride) {
-        const uint4 v = ld_stream16(body + i * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint4 *body = reinterpret_cast<const uint4 *>(in + head);
+    const uint64_t body_bytes = nvec * 16;
+    const uint64_t W = (uint64_t)gridDim.x * kHistWarps;
+    constexpr uint64_t kv = 32 * kHistVec; // vectors a chunk
+    uint64_t ch = (uint64_t)blockIdx.x * kHistWarps + warp;
+    if (lane == 0) {
+        prefetch_chunk((const uint8_t *)body, ch * kHistChunk, body_bytes);
+        prefetch_chunk((const uint8_t *)body, (ch + W) * kHistChunk, body_bytes);
+    }
+    uint4 cur[kHistVec];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            atomicAdd(&mine[byte_of(w[j >> 2], j & 3)], 1u);
+    for (int u = 0; u < kHistVec; ++u) {
+        const uint64_t v = ch * kv + u * 32 + lane;
+        cur[u] = v < nvec ? ld_stream16(body + v) : make_uint4(0, 0, 0, 0);
+    }
+    for (; ch * kv < nvec; ch += W) {
+        const uint64_t nx = ch + W;
+        if (lane == 0)
+            prefetch_chunk((const uint8_t *)body, (nx + W) * kHistChunk, body_bytes);
+        uint4 nxt[kHistVec];
+#pragma unroll
+        for (int u = 0; u < kHistVec; ++u) {
+            const uint64_t v = nx * kv + u * 32 + lane;
+            nxt[u] = v < nvec ? ld_stream16(body + v) : make_uint4(0, 0, 0, 0);
+        }
+        if (ch * kv + kv <= nvec) {
+#pragma unroll
+            for (int u = 0; u < kHistVec; ++u) {
+                count_word(mine, cur[u].x);
+                count_word(mine, cur[u].y);
+                count_word(mine, cur[u].z);
+                count_word(mine, cur[u].w);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kHistVec; ++u)
+                if (ch * kv + u * 32 + lane < nvec) {
+                    count_word(mine, cur[u].x);
+                    count_word(mine, cur[u].y);
+                    count_word(mine, cur[u].z);
+                    count_word(mine, cur[u].w);
+                }
+        }
+#pragma unroll
+        for (int u = 0; u < kHistVec; ++u)
+            cur[u] = nxt[u];
     }
     __syncthreads();
-    for (int b = tid; b < 256; b += kHistThreads) {
-        uint32_t s = 0;
+    for (int b = warp; b < 256; b += kHistWarps) {
+        uint32_t c = hist_smem[b * 32 + lane];
 #pragma unroll
-        for (int w = 0; w < kHistWarps; ++w)
-            s += h[w][b];
-        if (s)
-            atomicAdd(count + b, (unsigned long long)s);
+        for (int o = 16; o; o >>= 1)
+            c += __shfl_xor_sync(~0u, c, o);
+        if (lane == 0 && c)
+            atomicAdd(count + b, (unsigned long long)c);
     }
 }
 
@@ -345,11 +409,12 @@ ecc_status e4m3_histogram(const uint8_t *in, size_t n, uint64_t *count, void *st
         return ECC_ERR_CUDA;
     const uint64_t head = std::min<uint64_t>(n, (16 - ((uintptr_t)in & 15)) & 15);
     const uint64_t nvec = (n - head) / 16;
-    uint64_t blocks = (nvec + kHistThreads - 1) / kHistThreads;
-    const uint64_t cap = (uint64_t)sms * 4;
-    blocks = std::max<uint64_t>(1, std::min(blocks, cap));
-    hist_kernel<<<(unsigned)blocks, kHistThreads, 0, (cudaStream_t)stream>>>(in, n, head,
-                                                                              (unsigned long long *)count);
+    if (occupancy((const void *)hist_kernel, kHistThreads, kHistSmem) <= 0)
+        return launch_status(cudaErrorInvalidConfiguration);
+    const uint64_t chunks = (nvec + 32 * kHistVec - 1) / (32 * kHistVec);
+    const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((chunks + kHistWarps - 1) / kHistWarps, sms));
+    hist_kernel<<<(unsigned)blocks, kHistThreads, kHistSmem, (cudaStream_t)stream>>>(in, n, head,
+                                                                                      (unsigned long long *)count);
     return launch_status(cudaGetLastError());
 }
 

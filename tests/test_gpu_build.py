@@ -64,6 +64,17 @@ def test_random_histograms(seed):
     check_same(c, add=0)  # absent bytes get no code
 
 
+def test_weights_above_2_55():
+    """Weight sums of 2^55 and more take the two-word key path."""
+    g = np.random.default_rng(55)
+    c = g.integers(0, 1 << 55, 256, dtype=np.uint64)
+    check_same(c, add=1)
+    c[::2] = np.uint64(1 << 54)  # ties among large weights
+    c[1::4] = 0
+    check_same(c, add=0)
+    check_same(c, add=3)
+
+
 def test_workload_histograms():
     for x in (np_gauss(1 << 20, (3, 1))[0], np_gauss(1 << 20, (3, 2), 1.0)[0], np_zero_spike(1 << 20, (3, 3))):
         check_same(oracle.histogram(x), add=1)

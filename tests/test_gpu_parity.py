@@ -87,7 +87,8 @@ def codebooks(count):
 
 # ------------------------------------------------------------------ histogram
 
-@pytest.mark.parametrize("n,offset", [(1 << 20, 0), (1, 0), (17, 3), (123457, 5), ((1 << 22) + 9, 1)])
+@pytest.mark.parametrize("n,offset", [(1 << 20, 0), (1, 0), (17, 3), (123457, 5), ((1 << 22) + 9, 1),
+                                      (4111, 0), (4096 * 2 + 16, 7), (3 * 6 * 152 * 4096 + 4096 * 5 + 3, 2)])
 def test_histogram_matches_oracle(n, offset):
     x = np_grad(n + offset, (11, n))
     xd = torch.from_numpy(x).cuda()[offset:]            # misaligned start
@@ -95,6 +96,16 @@ def test_histogram_matches_oracle(n, offset):
     ecc.e4m3_histogram(xd, cnt)                         # accumulates
     torch.cuda.synchronize()
     want = oracle.histogram(x[offset:]) * np.uint64(2)
+    assert (cnt.cpu().numpy().view(np.uint64) == want).all()
+
+
+def test_histogram_one_byte_value():
+    """Every byte equal: all lanes of every counting step hit the same bin."""
+    x = np.full((1 << 26) + 5, 0x38, np.uint8)
+    cnt = ecc.e4m3_histogram(torch.from_numpy(x).cuda()[1:])
+    torch.cuda.synchronize()
+    want = np.zeros(256, np.uint64)
+    want[0x38] = x.size - 1
     assert (cnt.cpu().numpy().view(np.uint64) == want).all()
 
 
