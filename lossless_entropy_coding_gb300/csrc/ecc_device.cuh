@@ -411,6 +411,23 @@ __device__ __forceinline__ uint32_t lookup_pairs(const uint2 *lut, uint4 in, uin
     return zsum + 8;
 }
 
+// Bit total of the 16 symbols in `in` coded one by one from the table (a
+// group whose pairs do not all fit 32 bits); *exact when some byte has no
+// code of at most 31 bits (multiplier 0), which only the exact path codes.
+__device__ __forceinline__ uint32_t single_bits(const uint2 *lut, uint4 in, bool *exact)
+{
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    uint32_t zsum = 0, zor = 0;
+#pragma unroll
+    for (int j = 0; j < kSymPerThread; ++j) {
+        const uint32_t z = __clz(lut[byte_of(w[j >> 2], j & 3) * kLutReplicas].y); // length - 1
+        zsum += z;
+        zor |= z;
+    }
+    *exact = (zor & 32u) != 0;
+    return zsum + kSymPerThread;
+}
+
 // Predicated or-reduction into a shared word (addr: shared-window address):
 // done when `gate` is 0.  Written as one predicated instruction so that no
 // branch surrounds it.
@@ -883,6 +900,34 @@ struct SegPacker {
             K = yhi + ylo;
         }
     }
+    // the same for the 16 codes of `in` one by one (table entries of codes of
+    // at most 31 bits; a group with a longer pair)
+    __device__ __forceinline__ void pack_singles(const uint2 *lut, uint32_t region, uint32_t pos, uint32_t c0,
+                                                 uint4 in)
+    {
+        const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+        const uint32_t nb0 = pos & 31u;
+        addr = region + (pos >> 5) * 4u;
+        {
+            const uint2 e = lut[byte_of(w[0], 0) * kLutReplicas];
+            const uint32_t K0 = 1u << ((32u - nb0) & 31u);
+            const uint64_t x = (uint64_t)e.x * K0;
+            const uint64_t y = (uint64_t)K0 * e.y;
+            const uint32_t yhi = (uint32_t)(y >> 32), ylo = (uint32_t)y;
+            tail((uint32_t)(x >> 32) | c0, (uint32_t)x, nb0 ? yhi : 1u);
+            cur = nb0 ? cur : e.x;
+            K = nb0 ? yhi + ylo : e.y;
+        }
+#pragma unroll
+        for (int j = 1; j < kSymPerThread; ++j) {
+            const uint2 e = lut[byte_of(w[j >> 2], j & 3) * kLutReplicas];
+            const uint64_t x = (uint64_t)e.x * K;
+            const uint64_t y = (uint64_t)K * e.y;
+            const uint32_t yhi = (uint32_t)(y >> 32), ylo = (uint32_t)y;
+            tail((uint32_t)(x >> 32) | cur, (uint32_t)x, yhi);
+            K = yhi + ylo;
+        }
+    }
 };
 
 // Exact-path sink for one lane's group (rare: partial groups, long codes):
@@ -923,6 +968,33 @@ static __device__ __noinline__ PackEnd seg_exact_pack(uint32_t *region, uint32_t
     return PackEnd{nb ? shl_clamp(alo, 32u - nb) : 0u, wi, nb};
 }
 
+// Bit total of a slow group (bits 0-29), coded one code at a time from the
+// table when it is full and every code has at most 31 bits (bit 30), else by
+// the exact path from the codebook; bit 31: some byte has no code.
+static __device__ __noinline__ uint32_t slow_group_bits(const uint2 *lut, uint4 in, uint32_t cnt,
+                                                        const ecc_codebook *cb)
+{
+    bool exact = cnt < kSymPerThread;
+    if (!exact) {
+        const uint32_t bits = single_bits(lut, in, &exact);
+        if (!exact)
+            return bits | 1u << 30;
+    }
+    bool nocode = false;
+    const uint32_t bits = exact_bits(in, cnt, cb, &nocode);
+    return bits | (nocode ? 1u << 31 : 0u);
+}
+
+// Slow-group sink coded one code at a time from the table (SegPacker's
+// protocol); returns the final partial word and its shared-window address.
+static __device__ __noinline__ PackEnd seg_single_pack(const uint2 *lut, uint32_t region, uint32_t pos,
+                                                       uint32_t c0, uint4 in)
+{
+    SegPacker pk;
+    pk.pack_singles(lut, region, pos, c0, in);
+    return PackEnd{pk.cur, pk.addr, 1u};
+}
+
 // Code the rounds of one warp's segment [s0, s1) of chunk symbols (s1 > s0)
 // into its region (shared-window address `region`, cap_bits of room).
 // src: the chunk's staged input (kSharedSrc) else unused; the tensor's bytes
@@ -957,10 +1029,12 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
         // the common case, every group of the round full and coded by the
         // table, runs without a branch that splits the warp
         const bool fast = __all_sync(~0u, !slow);
+        bool single = false; // slow group coded one code at a time from the table
         if (!fast && slow) {
-            bool nocode = false;
-            bits = exact_bits(in, cnt, job.cb, &nocode);
-            *bad |= nocode;
+            const uint32_t r = slow_group_bits(lut, in, cnt, job.cb);
+            bits = r & 0x3FFFFFFFu;
+            single = (r >> 30) & 1u;
+            *bad |= (r >> 31) != 0;
         }
         uint32_t incl = bits;
 #pragma unroll
@@ -1007,6 +1081,11 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
                         word = pk.cur;
                         wa = pk.addr;
                         nb = 1; // 1..32 bits: always a partial word to merge
+                    } else if (single) {
+                        const PackEnd e = seg_single_pack(lut, region, pos, c0, in);
+                        word = e.word;
+                        wa = e.wa;
+                        nb = 1;
                     } else {
                         const PackEnd e = seg_exact_pack(
                             reinterpret_cast<uint32_t *>(__cvta_shared_to_generic(region)), pos, c0, in, cnt, job.cb);

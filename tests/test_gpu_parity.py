@@ -233,6 +233,28 @@ def test_long_codes_take_the_slow_paths():
         check_against_oracle(x, cbb, ocb, 4096, 64)
 
 
+def test_pairs_past_32_bits_with_codes_of_at_most_31():
+    """Fibonacci weights on 30 bytes: codes of 1..29 bits.  Rare bytes drawn
+    often enough that many 16-symbol groups hold a pair longer than 32 bits
+    (the table's pair join fails) while every single code fits 31 bits: such
+    groups are coded one code at a time from the table."""
+    w = np.zeros(256, np.uint64)
+    a, b = 1, 1
+    for s in range(30):
+        w[s] = a
+        a, b = b, a + b
+    cbb, ocb = ecc.huff_build_canonical(w), oracle.huffman_codebook(w)
+    assert ecc.codebook_view(cbb)["max_len"] == 29
+    g = np.random.default_rng(29)
+    p = 0.93 * (w[:30] / w[:30].sum()) + 0.07 / 30
+    x = g.choice(30, (1 << 20) + 333, p=p / p.sum()).astype(np.uint8)
+    L = ocb["len"][x].astype(np.int64)
+    pairs = L[: (x.size // 2) * 2].reshape(-1, 2).sum(axis=1)
+    assert (pairs > 32).mean() > 0.002
+    for C, S in ((16384, 256), (4096, 64), (1024, 64)):
+        check_against_oracle(x, cbb, ocb, C, S)
+
+
 # ------------------------------------------------------------------ errors
 
 def test_capacity_error_reports_needed_size():
