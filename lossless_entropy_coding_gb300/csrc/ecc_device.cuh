@@ -1685,6 +1685,58 @@ __device__ __forceinline__ uint32_t fstep_slow(FastStream &s, const uint16_t *de
     return e;
 }
 
+// A code of at most 32 bits longer than the first-level table, from the
+// next 32 stream bits p32; byte | len << 8, or 0 when the codebook has longer
+// codes or p32 starts no code.  The length is 15 plus the number of lengths
+// j in [15, max_len) whose canonical range lies below p32 (lim32 rises with
+// j), found by a binary search.
+__device__ __forceinline__ uint32_t decode_long32(uint32_t p32, const LongTable &lt)
+{
+    const uint32_t maxl = lt.max_len;
+    if (maxl > 32 || maxl <= ECC_PEEK_BITS || lt.family != ECC_FAMILY_HUFFMAN)
+        return 0;
+    const uint32_t n = maxl - (ECC_PEEK_BITS + 1); // candidates j = 15 .. maxl - 1
+    uint32_t c = 0;
+#pragma unroll
+    for (uint32_t step = 16; step; step >>= 1)
+        if (c + step <= n && (uint64_t)p32 >= lt.lim32[ECC_PEEK_BITS + c + step])
+            c += step;
+    const uint32_t L = ECC_PEEK_BITS + 1 + c;
+    const uint32_t v = L == 32 ? p32 : p32 >> (32 - L);
+    const uint64_t d = (uint64_t)v - lt.first[L];
+    if (d >= lt.count[L])
+        return 0;
+    const uint32_t at = lt.index[L] + (uint32_t)d;
+    return at < 256 ? (uint32_t)lt.sorted[at] | (L << 8) : 0u;
+}
+
+// The redo of an iteration that met a code the table does not resolve: one
+// code at a time, codes of up to 32 bits resolved in line, longer or invalid
+// ones by fstep_slow's out-of-line path.
+__device__ __forceinline__ uint32_t fstep_redo(FastStream &s, const uint16_t *dec, const LongTable &lt, bool &bad)
+{
+    const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
+    uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
+    if (e == 0)
+        e = decode_long32(p, lt);
+    if (e == 0) {
+        e = decode_long_at(s.hi, s.lo, s.nx, s.o, lt);
+        if (e == 0) {
+            bad = true;
+            e = 1u << 8; // consume one bit and go on; the chunk is flagged
+        }
+    }
+    s.o += e >> 8;
+    while (s.o >= 32) {
+        s.hi = s.lo;
+        s.lo = s.nx;
+        s.nx = bswap32(lds_u32(s.wa));
+        s.wa += 4;
+        s.o -= 32;
+    }
+    return e;
+}
+
 // QLC codes need no first-level table: the 3-bit prefix fixes the code
 // length (a byte of two registers, selected by the prefix), and the rank is
 // the whole code plus a per-prefix offset (start of the area minus prefix <<
@@ -1851,8 +1903,9 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
                     continue;
                 s[r] = s0[r];
                 a[r] = b[r] = 0;
+#pragma unroll 1
                 for (int t = 0; t < 8; ++t) {
-                    const uint32_t e = fstep_slow(s[r], dec, lt, bad);
+                    const uint32_t e = fstep_redo(s[r], dec, lt, bad);
                     if (t < 4)
                         a[r] = __byte_perm(a[r], e, 0x4321);
                     else

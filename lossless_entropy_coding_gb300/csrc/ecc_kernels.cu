@@ -250,7 +250,7 @@ __global__ void decode_kernel(DecParams p)
     LongTable &lt = *reinterpret_cast<LongTable *>(smem + kDecTableBytes);
     QlcShared &qs = *reinterpret_cast<QlcShared *>(smem + kDecTableBytes + kLongTableBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kDecTableBytes + kLongTableBytes + kQlcSharedBytes);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const ecc_codebook *cb = p.job.cb;
     if (cb->magic != ECC_CODEBOOK_MAGIC || cb->max_len > ECC_MAX_CODE_LEN) {
         if (threadIdx.x == 0 && blockIdx.x == 0)
@@ -267,24 +267,43 @@ __global__ void decode_kernel(DecParams p)
             dst[i] = src[i];
     }
     load_long_table(lt, cb);
+    __shared__ uint32_t next_item; // the CTA's chunks blockIdx.x + k * gridDim.x, claimed by k in turn
     if (lane == 0) {
         mbar_init(&bars[warp], 1);
         fence_mbar_init();
     }
+    if (threadIdx.x == 0)
+        next_item = 0;
     __syncthreads();
     WarpStage ws{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * p.stage_bytes), p.stage_bytes,
                  &bars[warp], 0};
-    const uint64_t stride = (uint64_t)gridDim.x * warps;
+    // The warps of a CTA claim its chunks one at a time, so a warp that
+    // drew chunks with many long codes does not hold up the CTA's end; a
+    // warp claims its next chunk before decoding the current one, so that
+    // the next one's L2 prefetch starts early.
+    auto claim = [&]() -> uint64_t {
+        uint32_t k = 0;
+        if (lane == 0)
+            k = atomicAdd(&next_item, 1u);
+        return blockIdx.x + (uint64_t)__shfl_sync(~0u, k, 0) * gridDim.x;
+    };
+    uint64_t c = claim();
     if (qlc) {
         const DecTables T = qlc_tables(cb->dec, &lt, qs, reinterpret_cast<const uint32_t *>(smem));
-        for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += stride)
-            decode_chunk<R, true>(p.job, T, ws, c, c + stride, p.n_chunks);
+        while (c < p.n_chunks) {
+            const uint64_t nc = claim();
+            decode_chunk<R, true>(p.job, T, ws, c, nc, p.n_chunks);
+            c = nc;
+        }
     } else {
         DecTables T{};
         T.dec = dec;
         T.lt = &lt;
-        for (uint64_t c = (uint64_t)blockIdx.x * warps + warp; c < p.n_chunks; c += stride)
-            decode_chunk<R, false>(p.job, T, ws, c, c + stride, p.n_chunks);
+        while (c < p.n_chunks) {
+            const uint64_t nc = claim();
+            decode_chunk<R, false>(p.job, T, ws, c, nc, p.n_chunks);
+            c = nc;
+        }
     }
 }
 
