@@ -70,6 +70,8 @@ def _load():
             "eo_encode": (I32, [P, U64, P, P, U32, U32, P, U64, P, P, P]),
             "eo_decode_qlc": (I32, [P, U64, P, P, U64, U32, U32, P, P, P]),
             "eo_decode_huffman": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
+            "eo_escape_codebook": (I32, [P, P, P, P]),
+            "eo_decode_escape": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
             "eo_entropy_bits": (ct.c_double, [P]),
             "eo_kl_bits": (ct.c_double, [P, P]),
             "eo_code_bits": (U64, [P, P]),
@@ -189,6 +191,21 @@ def huffman_codebook(weight) -> dict:
     return {"family": "huffman", "len": ln, "code": canonical_codes(ln)}
 
 
+# ---------------------------------------------------------------- escape code
+
+def escape_codebook(count) -> dict:
+    """ZipCCL-style escape code on the e4m3 exponent field (ZipCCL, section
+    2.B): the 7 most frequent exponents (summed counts, ties to the smaller)
+    coded 001..111, others 000 + the 4-bit exponent; sign and mantissa as
+    they are."""
+    count = _u64(count)
+    ln = np.zeros(256, np.uint8)
+    code = np.zeros(256, np.uint64)
+    top = np.zeros(7, np.uint8)
+    _check(_load().eo_escape_codebook(_p(count), _p(ln), _p(code), _p(top)), "escape_codebook")
+    return {"family": "escape", "len": ln, "code": code, "top": top}
+
+
 # ---------------------------------------------------------------- codec
 
 def max_encoded_bytes(n: int, C: int, max_len: int) -> int:
@@ -237,6 +254,9 @@ def decode(enc: dict, cb: dict) -> np.ndarray:
     if cb["family"] == "qlc":
         rc = lib.eo_decode_qlc(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
                                _p(_u8(cb["width"])), _p(_u8(cb["by_rank"])), _p(out))
+    elif cb["family"] == "escape":
+        rc = lib.eo_decode_escape(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
+                                  _p(_u8(cb["top"])), _p(out))
     else:
         rc = lib.eo_decode_huffman(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
                                    _p(_u8(cb["len"])), _p(out))

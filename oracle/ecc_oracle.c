@@ -22,6 +22,11 @@
  *          average PMF of earlier batches; compared with per-shard Huffman
  *          and the Shannon bound; KL divergence of Figure 3), and the
  *          euno.news summary, Methodology steps 1-4.
+ *   [ZIP]  "ZipCCL" (gist.science summary of arXiv 2604.27844), section 2.B
+ *          "Tecnica di Codifica degli Esponenti": sign and mantissa bits
+ *          kept as they are, the 7 most frequent exponents coded in 3 bits
+ *          (001-111), any other exponent as the code 000 plus the exponent
+ *          itself.
  *
  * Where the pages are silent the readings used are:
  *   - area k is named by the 3-bit prefix equal to k in binary, areas are
@@ -32,6 +37,14 @@
  *   - Huffman merges the two nodes with the smallest (weight, smallest byte
  *     in the subtree) keys; a lone symbol gets length 1; zero-weight bytes
  *     get no code; codes are canonical (sorted by length, then byte);
+ *   - escape code on e4m3 (sign bit 7, exponent bits 6-3, mantissa bits
+ *     2-0): the page codes BF16's 8-bit exponent and keeps escaped
+ *     exponents in a separate array; here the exponent field has 4 bits and
+ *     an escaped exponent follows its 000 code in the stream, so a byte's
+ *     codeword is [exponent code][4-bit exponent if escaped][sign]
+ *     [mantissa] (7 or 11 bits).  The top 7 are the exponents with the
+ *     largest summed counts, ties to the smaller exponent; the one ranked r
+ *     gets code r + 1.  000 followed by a top-7 exponent is no codeword;
  *   - codewords are written most significant bit first, bits are packed
  *     most significant bit first into bytes;
  *   - the container splits the tensor into chunks of C symbols, pads each
@@ -576,6 +589,84 @@ int eo_decode_huffman(const uint8_t *in, uint64_t in_bytes, const uint64_t *chun
         }
     }
     return decode_container(in, in_bytes, chunk_off, sub_bits, n, C, S, huff_symbol, &h, out);
+}
+
+/* ------------------------------------------------------------------ */
+/* Escape code on e4m3 exponents ([ZIP] section 2.B): top-7 exponents   */
+/* in 3 bits, others as 000 plus the 4-bit exponent; sign and mantissa  */
+/* follow as they are.                                                 */
+/* ------------------------------------------------------------------ */
+int eo_escape_codebook(const uint64_t *count, uint8_t *len, uint64_t *code, uint8_t *top)
+{
+    uint64_t ecount[16] = {0};
+    int taken[16] = {0};
+    for (int b = 0; b < 256; b++)
+        ecount[(b >> 3) & 15] += count[b];
+    int rank_of[16];
+    for (int e = 0; e < 16; e++)
+        rank_of[e] = -1;
+    for (int r = 0; r < 7; r++) { /* selection: largest count, then smaller exponent */
+        int best = -1;
+        for (int e = 0; e < 16; e++)
+            if (!taken[e] && (best < 0 || ecount[e] > ecount[best]))
+                best = e;
+        taken[best] = 1;
+        rank_of[best] = r;
+        top[r] = (uint8_t)best;
+    }
+    for (int b = 0; b < 256; b++) {
+        const int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+        const uint64_t sm = ((uint64_t)s << 3) | (uint64_t)m; /* 4 bits */
+        if (rank_of[e] >= 0) {
+            code[b] = ((uint64_t)(rank_of[e] + 1) << 4) | sm;
+            len[b] = 7;
+        } else {
+            code[b] = ((uint64_t)e << 4) | sm; /* 000 eeee s mmm */
+            len[b] = 11;
+        }
+    }
+    return EO_OK;
+}
+
+typedef struct {
+    int rank_of[16];
+    uint8_t top[7];
+} esc_ctx;
+
+static int escape_symbol(eo_reader *r, const void *vctx, uint8_t *sym)
+{
+    const esc_ctx *q = (const esc_ctx *)vctx;
+    uint64_t p, e, s, m;
+    if (read_bits(r, 3, &p))
+        return -1;
+    if (p == 0) {
+        if (read_bits(r, 4, &e))
+            return -1;
+        if (q->rank_of[e] >= 0)
+            return -1; /* a top-7 exponent has a short code: not a codeword */
+    } else {
+        e = q->top[p - 1];
+    }
+    if (read_bits(r, 1, &s) || read_bits(r, 3, &m))
+        return -1;
+    *sym = (uint8_t)((s << 7) | (e << 3) | m);
+    return 0;
+}
+
+int eo_decode_escape(const uint8_t *in, uint64_t in_bytes, const uint64_t *chunk_off,
+                     const uint16_t *sub_bits, uint64_t n, uint32_t C, uint32_t S,
+                     const uint8_t *top, uint8_t *out)
+{
+    esc_ctx q;
+    for (int e = 0; e < 16; e++)
+        q.rank_of[e] = -1;
+    for (int r = 0; r < 7; r++) {
+        if (top[r] > 15 || q.rank_of[top[r]] >= 0)
+            return EO_ARG;
+        q.rank_of[top[r]] = r;
+        q.top[r] = top[r];
+    }
+    return decode_container(in, in_bytes, chunk_off, sub_bits, n, C, S, escape_symbol, &q, out);
 }
 
 /* ------------------------------------------------------------------ */

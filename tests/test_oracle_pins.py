@@ -375,3 +375,86 @@ def test_pins_catch_planted_mistakes(spike_counts):
     assert spike_counts[a] > spike_counts[b]
     ln_q[a], ln_q[b] = ln_q[b], ln_q[a]
     assert oracle.code_bits(spike_counts, ln_q) > oracle.code_bits(spike_counts, base["len"])
+    # an escape code that numbers the top exponents from 0 collides with 000
+    esc = oracle.escape_codebook(spike_counts)
+    words = [bits_of(c, l) for c, l in zip(esc["code"], esc["len"])]
+    for b in range(256):
+        if ((b >> 3) & 15) == esc["top"][0]:
+            words[b] = "000" + words[b][3:]
+    assert not prefix_free(words)
+
+
+# --------------------------------------------------------------- escape code
+
+def exponent_counts(count):
+    """Summed counts of the 16 e4m3 exponent values (bits 6-3), test side."""
+    e = np.zeros(16, np.uint64)
+    for b in range(256):
+        e[(b >> 3) & 15] += np.uint64(count[b])
+    return e
+
+
+def test_escape_code_shape_and_kraft(gauss_counts):
+    """ZipCCL section 2.B on e4m3: 7 exponents x 16 (sign, mantissa) values
+    at 3 + 4 bits, the other 9 exponents at 3 + 4 + 4 bits.  Kraft sum
+    7*16/2^7 + 9*16/2^11 = 121/128, prefix-free."""
+    cb = oracle.escape_codebook(gauss_counts)
+    ln = cb["len"]
+    assert (np.bincount(ln, minlength=12)[[7, 11]] == [112, 144]).all()
+    assert kraft(ln) == Fraction(7 * 16, 2 ** 7) + Fraction(9 * 16, 2 ** 11) == Fraction(121, 128)
+    assert prefix_free([bits_of(c, l) for c, l in zip(cb["code"], ln)])
+
+
+def test_escape_code_fields(spike_counts):
+    """Top 7 = exponents with the largest summed counts (ties to the smaller
+    exponent, checked against a sort); a byte's codeword is its exponent's
+    code (rank + 1, or 000 and the exponent) then sign then mantissa."""
+    cb = oracle.escape_codebook(spike_counts)
+    ec = exponent_counts(spike_counts)
+    want = sorted(range(16), key=lambda e: (-int(ec[e]), e))[:7]
+    assert list(cb["top"]) == want
+    for b in range(256):
+        s, e, m = b >> 7, (b >> 3) & 15, b & 7
+        tail = format(s, "b") + format(m, "03b")
+        word = bits_of(cb["code"][b], cb["len"][b])
+        if e in want:
+            assert word == format(want.index(e) + 1, "03b") + tail
+        else:
+            assert word == "000" + format(e, "04b") + tail
+
+
+def test_escape_code_ties_and_round_trip():
+    """Equal exponent counts rank by exponent value; round trip and bit count
+    7 x (top-7 bytes) + 11 x (others) on a tensor with escapes."""
+    count = np.ones(256, np.uint64)                      # all exponents tie
+    cb = oracle.escape_codebook(count)
+    assert list(cb["top"]) == list(range(7))
+    x = np_grad(50000, (21, 1))
+    cb = oracle.escape_codebook(oracle.histogram(np_gauss(1 << 16, (21, 2))[0]))
+    e = (x >> 3) & 15
+    n_top = int(np.isin(e, cb["top"]).sum())
+    assert 0 < n_top < x.size
+    for C, S in ((1024, 64), (16384, 256)):
+        enc = oracle.encode(x, cb, C, S)
+        assert enc["total_bits"] == 7 * n_top + 11 * (x.size - n_top)
+        assert (oracle.decode(enc, cb) == x).all()
+
+
+def test_escape_of_a_top_exponent_is_corrupt():
+    """000 followed by a top-7 exponent codes nothing (that byte has a short
+    code): a stream holding it is corrupt."""
+    cb = oracle.escape_codebook(np.ones(256, np.uint64))  # top 7 = exponents 0..6
+    stream = "000" + "0011" + "0" + "101"                  # escape of exponent 3
+    payload = pack_bits(stream)
+    payload = np.concatenate([payload, np.zeros((-payload.size) % 16, np.uint8)])
+    enc = {"payload": payload, "chunk_off": np.array([0, 16], np.uint64),
+           "sub_bits": np.array([11], np.uint16), "n": 1, "C": 1024, "S": 64}
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.decode(enc, cb)
+    assert ei.value.code == oracle.CORRUPT
+    # the same byte through its short code decodes
+    ok = "100" + "0" + "101"                               # exponent 3 has rank 3 -> code 100
+    payload = pack_bits(ok)
+    payload = np.concatenate([payload, np.zeros((-payload.size) % 16, np.uint8)])
+    enc.update(payload=payload, sub_bits=np.array([7], np.uint16))
+    assert list(oracle.decode(enc, cb)) == [(3 << 3) | 5]
