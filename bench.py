@@ -349,6 +349,38 @@ def three_stage_latency(ecc, x, fixed_cb, b, C, S, stream, reps=8):
     return out
 
 
+def escape_code_timing(ecc, x, pooled_h, b, C, S, stream, reps=8):
+    """The ZipCCL-style exponent escape code as a third fixed codebook (from
+    the same warm-up counts) on the same tensor: encode and decode times
+    (device events, medians) and compressibility; informational, outside the
+    headline step."""
+    import torch
+
+    EV = torch.cuda.Event
+    n = x.numel()
+    dcb = ecc.to_device(ecc.escape_build_tables(pooled_h), x.device)
+    enc_ms, dec_ms = [], []
+    for rep in range(reps + 1):
+        e0, e1, e2 = EV(enable_timing=True), EV(enable_timing=True), EV(enable_timing=True)
+        e0.record(stream)
+        enc = ecc.ecc_encode(x, dcb, C, S, out=b["out"], chunk_off=b["chunk_off"], sub_bits=b["sub_bits"],
+                             total_bits=b["total_bits"], ws=b["ws"], status=b["status"])
+        e1.record(stream)
+        ecc.ecc_decode(enc, dcb, out=b["y"], status=b["dstatus"])
+        e2.record(stream)
+        torch.cuda.synchronize()
+        if rep:
+            enc_ms.append(e0.elapsed_time(e1))
+            dec_ms.append(e1.elapsed_time(e2))
+    if int(b["status"].item()) or int(b["dstatus"].item()) or not torch.equal(b["y"], x):
+        raise SystemExit("escape code: status or round trip failed")
+    bits = int(b["total_bits"].item())
+    em, dm = statistics.median(enc_ms), statistics.median(dec_ms)
+    return {"encode_ms": em, "decode_ms": dm, "encode_gbs": n / em / 1e6, "decode_gbs": n / dm / 1e6,
+            "compressibility_pct": 100.0 * (1.0 - bits / (8.0 * n)),
+            "payload_bytes": int(b["chunk_off"][-1].item())}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -540,6 +572,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         extra["histogram_gbs"] = 5 * n / h0.elapsed_time(h1) / 1e6
         extra["three_stage"] = three_stage_latency(ecc, x, dcbs["huffman"], bufs["huffman"], C, S, stream)
+        extra["escape_code"] = escape_code_timing(ecc, x, pooled_h, bufs["qlc"], C, S, stream)
         if not args.no_sweep:
             sweep = {}
             for Cs in (4096, 16384, 65536):

@@ -2,7 +2,7 @@
  * ecc.h -- C ABI of the GB300 library for lossless fixed-codebook coding of
  * e4m3 byte tensors.
  *
- * Two codebook families, both fixed before the data is seen:
+ * Three codebook families, all fixed before the data is seen:
  *
  *  - the Quad Length Code (QLC) of "Quad Length Codes for Lossless
  *    Compression of e4m3" (gist.science summary of arXiv 2602.17849),
@@ -14,7 +14,10 @@
  *    Encoder for ML Compression" (arXiv 2601.10673), abstract and TL;DR: one
  *    codebook built from the average symbol distribution of earlier batches
  *    and reused for every later tensor, with no per-tensor frequency
- *    analysis and no codebook sent with the data.
+ *    analysis and no codebook sent with the data;
+ *  - the exponent escape code of ZipCCL (gist.science summary of arXiv
+ *    2604.27844), section 2.B, on the e4m3 exponent field (see
+ *    escape_build_tables).
  *
  * Conventions (all entry points):
  *  - Every function returns an ecc_status.  A host-side return value reports
@@ -70,7 +73,7 @@ enum {
     ECC_ERR_CUDA = 6      /* a CUDA runtime call failed */
 };
 
-enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2 };
+enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2, ECC_FAMILY_ESCAPE = 3 };
 
 #define ECC_CODEBOOK_MAGIC 0x45434342u /* "ECCB" */
 #define ECC_MAX_CODE_LEN 48            /* longest code the device path accepts */
@@ -78,14 +81,15 @@ enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2 };
 
 /*
  * Codebook: a fixed-size, pointer-free record built on the host by
- * qlc_build_tables or huff_build_canonical and copied as raw bytes to the
+ * qlc_build_tables, huff_build_canonical or escape_build_tables (or on the
+ * device by huff_build_device) and copied as raw bytes to the
  * device (cudaMemcpy of ecc_codebook_bytes()).  Serialising it is a memcpy.
  * Fields marked "derived" are lookup tables the kernels stage in shared
  * memory; they follow from len/code and are filled by the builders.
  */
 typedef struct ecc_codebook {
     uint32_t magic;       /* ECC_CODEBOOK_MAGIC */
-    uint32_t family;      /* ECC_FAMILY_QLC or ECC_FAMILY_HUFFMAN */
+    uint32_t family;      /* ECC_FAMILY_QLC, ECC_FAMILY_HUFFMAN or ECC_FAMILY_ESCAPE */
     uint32_t max_len;     /* longest code length in bits */
     uint32_t min_len;     /* shortest code length in bits */
     uint32_t n_coded;     /* number of byte values that have a code */
@@ -103,7 +107,7 @@ typedef struct ecc_codebook {
     uint8_t width[8];     /* QLC: suffix width of each area, 0..8 */
     uint8_t len[256];     /* code length of each byte value, 0 = no code */
     uint8_t rank[256];    /* QLC: rank of each byte value */
-    uint8_t by_rank[256]; /* QLC: byte value holding each rank */
+    uint8_t by_rank[256]; /* QLC: byte value holding each rank; escape code: the 7 exponents by rank */
     uint8_t sorted[256];  /* Huffman: coded byte values sorted by (length, value) */
 } ecc_codebook;
 
@@ -162,6 +166,22 @@ ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, u
  * whose sum overflows 64 bits), ECC_ERR_CODEBOOK (tree deeper than max_len).
  */
 ecc_status huff_build_canonical(const uint64_t weight[256], uint32_t max_len, ecc_codebook *out);
+
+/*
+ * escape_build_tables -- the exponent escape code of ZipCCL (gist.science
+ * summary of arXiv 2604.27844, section 2.B "Tecnica di Codifica degli
+ * Esponenti") as a fixed codebook for e4m3 bytes (sign bit 7, exponent bits
+ * 6-3, mantissa bits 2-0): the 7 exponents with the largest summed counts
+ * (ties to the smaller exponent) get the 3-bit codes 001..111 by rank; any
+ * other exponent is coded 000 followed by its 4 bits (the page keeps such
+ * exponents in a separate array; here they stay in the stream).  Sign and
+ * mantissa follow as they are, so every byte has a 7- or 11-bit code.
+ *   count[256]  byte counts (e.g. pooled warm-up histograms).
+ *   out         filled codebook (family ECC_FAMILY_ESCAPE); by_rank[0..6]
+ *               holds the 7 exponents in rank order.
+ * Errors: ECC_ERR_ARG for NULL pointers.
+ */
+ecc_status escape_build_tables(const uint64_t count[256], ecc_codebook *out);
 
 /* ------------------------------------------------------------------------
  * Host figures in float64 ("Single-Stage Huffman ...", TL;DR: compressibility

@@ -21,7 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libecc_gb300.so")
 
 OK, ERR_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_CODEBOOK, ERR_TIMEOUT, ERR_CUDA = range(7)
-FAMILY_QLC, FAMILY_HUFFMAN = 1, 2
+FAMILY_QLC, FAMILY_HUFFMAN, FAMILY_ESCAPE = 1, 2, 3
 MAX_CODE_LEN = 48
 BASE_WIDTHS = (3, 3, 3, 3, 3, 4, 5, 8)
 
@@ -70,6 +70,7 @@ def _load():
             "qlc_build_tables": (I32, [P, P, P]),
             "qlc_search_widths": (I32, [P, U32, U32, P, P]),
             "huff_build_canonical": (I32, [P, U32, P]),
+            "escape_build_tables": (I32, [P, P]),
             "ecc_entropy_bits": (D, [P]),
             "ecc_kl_bits": (D, [P, P]),
             "ecc_code_bits": (I32, [P, P, P]),
@@ -212,6 +213,15 @@ def _stream_ptr(stream):
 
 def _dptr(t):
     return ct.c_void_p(t.data_ptr()) if t is not None else ct.c_void_p(0)
+
+
+def escape_build_tables(count) -> np.ndarray:
+    """Host escape-code codebook (raw ecc_codebook bytes): top-7 e4m3
+    exponents in 3 bits, others 000 + exponent, sign and mantissa kept."""
+    count = _u64(count)
+    out = np.zeros(codebook_bytes(), np.uint8)
+    _check(_load().escape_build_tables(_np_ptr(count), _np_ptr(out)), "escape_build_tables")
+    return out
 
 
 def to_device(cb: np.ndarray, device="cuda"):

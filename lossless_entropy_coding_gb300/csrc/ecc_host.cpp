@@ -297,6 +297,40 @@ ecc_status huff_build_canonical(const uint64_t weight[256], uint32_t max_len, ec
     return ECC_OK;
 }
 
+ecc_status escape_build_tables(const uint64_t count[256], ecc_codebook *out)
+{
+    if (!count || !out)
+        return ECC_ERR_ARG;
+    uint64_t ecount[16] = {0};
+    for (int b = 0; b < 256; ++b)
+        ecount[(b >> 3) & 15] += count[b];
+    int order[16];
+    for (int e = 0; e < 16; ++e)
+        order[e] = e;
+    std::stable_sort(order, order + 16, [&](int a, int b) { return ecount[a] > ecount[b]; });
+    int code_of[16]; // 1..7 for the top exponents, 0 for the escaped ones
+    for (int e = 0; e < 16; ++e)
+        code_of[e] = 0;
+    clear(out, ECC_FAMILY_ESCAPE);
+    for (int r = 0; r < 7; ++r) {
+        code_of[order[r]] = r + 1;
+        out->by_rank[r] = (uint8_t)order[r];
+    }
+    for (int b = 0; b < 256; ++b) {
+        const int e = (b >> 3) & 15;
+        const uint64_t tail = (uint64_t)(b >> 7) << 3 | (uint64_t)(b & 7); // sign, mantissa
+        if (code_of[e]) {
+            out->len[b] = 7;
+            out->code[b] = (uint64_t)code_of[e] << 4 | tail;
+        } else {
+            out->len[b] = 11;
+            out->code[b] = (uint64_t)e << 4 | tail; // 000, exponent, sign, mantissa
+        }
+    }
+    fill_derived(out);
+    return ECC_OK;
+}
+
 double ecc_entropy_bits(const uint64_t count[256])
 {
     if (!count)

@@ -343,6 +343,47 @@ def test_qlc_code_of_an_empty_area_is_corrupt():
         assert int(st.item()) == ecc.ERR_CORRUPT
 
 
+@pytest.mark.parametrize("law", ["gauss", "spike", "grad"])
+def test_escape_code_workloads(law):
+    """The ZipCCL-style escape code (7- and 11-bit codes from the e4m3
+    exponent) through the same encoder and the table decoder, with the
+    codebook fixed from a warm-up tensor of the same law, so that the tensor
+    coded also holds escaped exponents."""
+    n = (1 << 20) + 777
+    if law == "gauss":
+        warm, x = np_gauss(1 << 18, (31, 1))[0], np_gauss(n, (31, 2))[0]
+    elif law == "spike":
+        warm, x = np_zero_spike(1 << 18, (31, 3)), np_zero_spike(n, (31, 4))
+    else:
+        warm, x = np_grad(1 << 18, (31, 5)), np_grad(n, (31, 6))
+    count = oracle.histogram(warm)
+    cbb, ocb = ecc.escape_build_tables(count), oracle.escape_codebook(count)
+    assert not np.isin((x >> 3) & 15, ocb["top"]).all()
+    for C, S in ((16384, 256), (4096, 64), (1024, 1024)):
+        check_against_oracle(x, cbb, ocb, C, S)
+
+
+def test_escape_of_a_top_exponent_is_corrupt():
+    """000 followed by a top-7 exponent is no codeword: planting one at the
+    start of a sub-block flags the stream."""
+    g = np.random.default_rng(41)
+    x = g.integers(0, 256, 1 << 16).astype(np.uint8)
+    count = np.ones(256, np.uint64)                        # top 7 = exponents 0..6
+    cbb, ocb = ecc.escape_build_tables(count), oracle.escape_codebook(count)
+    check_against_oracle(x, cbb, ocb, 16384, 256)
+    dcb = ecc.to_device(cbb)
+    for C, S in ((16384, 256), (4096, 64)):
+        enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), dcb, C, S, max_len=11)
+        torch.cuda.synchronize()
+        off = u64(enc.chunk_off)
+        bad = ecc.Encoded(enc.payload.clone(), enc.chunk_off, enc.sub_bits, enc.total_bits, enc.status,
+                          enc.n, enc.C, enc.S)
+        bad.payload[int(off[1])] = 0b00000110              # chunk 1 starts 000 0011 0..: escape of exponent 3
+        out, st = ecc.ecc_decode(bad, dcb)
+        torch.cuda.synchronize()
+        assert int(st.item()) == ecc.ERR_CORRUPT
+
+
 def test_bounded_wait_times_out():
     """The look-back wait gives up and reports ECC_ERR_TIMEOUT when no
     predecessor ever publishes (nothing here sets the flags)."""

@@ -102,6 +102,18 @@ def test_huffman_matches_oracle(name):
     assert (cb2["len"] == oracle.huffman_lengths(fixed)).all()
 
 
+@pytest.mark.parametrize("name", list(pmfs().keys()))
+def test_escape_code_matches_oracle(name):
+    count = pmfs()[name]
+    cb = ecc.codebook_view(ecc.escape_build_tables(count))
+    ref = oracle.escape_codebook(count)
+    assert cb["family"] == ecc.FAMILY_ESCAPE
+    assert (cb["len"] == ref["len"]).all()
+    assert (cb["code"] == ref["code"]).all()
+    assert (cb["by_rank"][:7] == ref["top"]).all()
+    assert int(cb["max_len"]) == 11 and int(cb["min_len"]) == 7 and int(cb["n_coded"]) == 256
+
+
 def test_huffman_length_limit_is_an_error():
     w = np.zeros(256, np.uint64)
     a, b = 1, 1
@@ -119,7 +131,8 @@ def test_huffman_length_limit_is_an_error():
 def test_derived_decode_table():
     # every 14-bit index resolves to the code that prefixes it, or is 0 when
     # no code of <= 14 bits does
-    for cbb in (ecc.qlc_build_tables(pmfs()["gauss"]), ecc.huff_build_canonical(pmfs()["spike"] + 1)):
+    for cbb in (ecc.qlc_build_tables(pmfs()["gauss"]), ecc.huff_build_canonical(pmfs()["spike"] + 1),
+                ecc.escape_build_tables(pmfs()["grad"])):
         cb = ecc.codebook_view(cbb)
         want = np.zeros(1 << 14, np.uint16)
         for b in range(256):
