@@ -71,6 +71,7 @@ def _load():
             "eo_decode_qlc": (I32, [P, U64, P, P, U64, U32, U32, P, P, P]),
             "eo_decode_huffman": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
             "eo_escape_codebook": (I32, [P, P, P, P]),
+            "eo_huffman_limited": (I32, [P, I32, P]),
             "eo_decode_escape": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
             "eo_entropy_bits": (ct.c_double, [P]),
             "eo_kl_bits": (ct.c_double, [P, P]),
@@ -188,6 +189,20 @@ def huffman_codebook(weight) -> dict:
     """Canonical Huffman code of a weight vector (Single-Stage Huffman,
     Methodology step 3)."""
     ln = huffman_lengths(weight)
+    return {"family": "huffman", "len": ln, "code": canonical_codes(ln)}
+
+
+def huffman_limited_lengths(weight, max_len: int) -> np.ndarray:
+    """Optimal code lengths of at most max_len bits (package-merge)."""
+    weight = _u64(weight)
+    ln = np.zeros(256, np.uint8)
+    _check(_load().eo_huffman_limited(_p(weight), int(max_len), _p(ln)), "huffman_limited")
+    return ln
+
+
+def huffman_limited_codebook(weight, max_len: int) -> dict:
+    """Canonical code of the length-limited Huffman lengths."""
+    ln = huffman_limited_lengths(weight, max_len)
     return {"family": "huffman", "len": ln, "code": canonical_codes(ln)}
 
 

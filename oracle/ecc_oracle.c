@@ -22,6 +22,11 @@
  *          average PMF of earlier batches; compared with per-shard Huffman
  *          and the Shannon bound; KL divergence of Figure 3), and the
  *          euno.news summary, Methodology steps 1-4.
+ *   [LLH]  length-limited Huffman, to bound decode tables ([QLC] section 5
+ *          "Future Directions" asks for the lengths to be optimised under the
+ *          speed constraint): the package-merge algorithm of Larmore and
+ *          Hirschberg (J. ACM 37(3), 1990), whose result is an optimal code
+ *          among those with no length above the limit.
  *   [ZIP]  "ZipCCL" (gist.science summary of arXiv 2604.27844), section 2.B
  *          "Tecnica di Codifica degli Esponenti": sign and mantissa bits
  *          kept as they are, the 7 most frequent exponents coded in 3 bits
@@ -37,6 +42,9 @@
  *   - Huffman merges the two nodes with the smallest (weight, smallest byte
  *     in the subtree) keys; a lone symbol gets length 1; zero-weight bytes
  *     get no code; codes are canonical (sorted by length, then byte);
+ *   - package-merge ties: leaves sort by (weight, byte); when a leaf and a
+ *     package weigh the same, the leaf comes first; packages pair items
+ *     0-1, 2-3, ... of the previous list; a lone symbol gets length 1;
  *   - escape code on e4m3 (sign bit 7, exponent bits 6-3, mantissa bits
  *     2-0): the page codes BF16's 8-bit exponent and keeps escaped
  *     exponents in a separate array; here the exponent field has 4 bits and
@@ -589,6 +597,101 @@ int eo_decode_huffman(const uint8_t *in, uint64_t in_bytes, const uint64_t *chun
         }
     }
     return decode_container(in, in_bytes, chunk_off, sub_bits, n, C, S, huff_symbol, &h, out);
+}
+
+/* ------------------------------------------------------------------ */
+/* Length-limited Huffman by package-merge ([LLH]).  List 1 holds the   */
+/* leaves sorted by weight; list d merges the leaves with the packages  */
+/* of list d-1 (pairs of consecutive items).  The first 2n-2 items of   */
+/* list max_len are selected; a symbol's length is the number of times */
+/* it occurs in them, counting inside packages.                        */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    uint64_t w;
+    int sym;  /* >= 0: a leaf */
+    int a, b; /* package: items a and b of the previous list */
+} llh_item;
+
+static void llh_count(llh_item **lists, int level, int i, uint8_t *len)
+{
+    const llh_item *it = &lists[level][i];
+    if (it->sym >= 0) {
+        len[it->sym]++;
+        return;
+    }
+    llh_count(lists, level - 1, it->a, len);
+    llh_count(lists, level - 1, it->b, len);
+}
+
+int eo_huffman_limited(const uint64_t *weight, int max_len, uint8_t *len)
+{
+    int leaf_sym[256], n = 0;
+    uint64_t total = 0;
+    for (int b = 0; b < 256; b++) {
+        len[b] = 0;
+        if (weight[b]) {
+            if (weight[b] >= ((uint64_t)1 << 62) - total)
+                return EO_ARG; /* sums of packages must fit 64 bits */
+            total += weight[b];
+            leaf_sym[n++] = b;
+        }
+    }
+    if (n == 0 || max_len < 1 || max_len > 64)
+        return EO_ARG;
+    if (n == 1) {
+        len[leaf_sym[0]] = 1;
+        return EO_OK;
+    }
+    if (max_len < 63 && ((uint64_t)1 << max_len) < (uint64_t)n)
+        return EO_CODEBOOK; /* no prefix code of n words fits max_len bits */
+    /* leaves by (weight, byte): selection sort */
+    for (int i = 0; i < n; i++) {
+        int m = i;
+        for (int j = i + 1; j < n; j++) {
+            const uint64_t wj = weight[leaf_sym[j]], wm = weight[leaf_sym[m]];
+            if (wj < wm || (wj == wm && leaf_sym[j] < leaf_sym[m]))
+                m = j;
+        }
+        const int t = leaf_sym[i];
+        leaf_sym[i] = leaf_sym[m];
+        leaf_sym[m] = t;
+    }
+    llh_item *lists[65];
+    int cnt[65];
+    for (int d = 1; d <= max_len; d++)
+        lists[d] = (llh_item *)malloc(sizeof(llh_item) * 2 * 256);
+    for (int i = 0; i < n; i++) {
+        lists[1][i].w = weight[leaf_sym[i]];
+        lists[1][i].sym = leaf_sym[i];
+        lists[1][i].a = lists[1][i].b = -1;
+    }
+    cnt[1] = n;
+    for (int d = 2; d <= max_len; d++) {
+        const int npk = cnt[d - 1] / 2;
+        int i = 0, j = 0, k = 0;
+        while (i < n || j < npk) {
+            const uint64_t pw = j < npk ? lists[d - 1][2 * j].w + lists[d - 1][2 * j + 1].w : 0;
+            if (i < n && (j >= npk || weight[leaf_sym[i]] <= pw)) { /* leaf first on a tie */
+                lists[d][k].w = weight[leaf_sym[i]];
+                lists[d][k].sym = leaf_sym[i];
+                lists[d][k].a = lists[d][k].b = -1;
+                i++;
+            } else {
+                lists[d][k].w = pw;
+                lists[d][k].sym = -1;
+                lists[d][k].a = 2 * j;
+                lists[d][k].b = 2 * j + 1;
+                j++;
+            }
+            k++;
+        }
+        cnt[d] = k;
+    }
+    for (int i = 0; i < 2 * n - 2; i++)
+        llh_count(lists, max_len, i, len);
+    for (int d = 1; d <= max_len; d++)
+        free(lists[d]);
+    return EO_OK;
 }
 
 /* ------------------------------------------------------------------ */

@@ -458,3 +458,62 @@ def test_escape_of_a_top_exponent_is_corrupt():
     payload = np.concatenate([payload, np.zeros((-payload.size) % 16, np.uint8)])
     enc.update(payload=payload, sub_bits=np.array([7], np.uint16))
     assert list(oracle.decode(enc, cb)) == [(3 << 3) | 5]
+
+
+# --------------------------------------------------------------- length-limited Huffman
+
+def brute_min_cost(w, L):
+    """Minimum sum(w x len) over all length vectors in [1, L]^n with Kraft <= 1."""
+    best = None
+    for ls in itertools.product(range(1, L + 1), repeat=len(w)):
+        if sum(Fraction(1, 2 ** l) for l in ls) <= 1:
+            c = sum(int(a) * b for a, b in zip(w, ls))
+            best = c if best is None or c < best else best
+    return best
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 6])
+def test_limited_huffman_optimal_against_brute_force(n):
+    g = np.random.default_rng(100 + n)
+    for trial in range(6):
+        w = np.zeros(256, np.uint64)
+        syms = g.choice(256, n, replace=False)
+        w[syms] = g.integers(1, [2, 10, 1000][trial % 3] + 1, n)
+        lo = max(1, int(np.ceil(np.log2(n))))
+        for L in range(lo, 6):
+            ln = oracle.huffman_limited_lengths(w, L)
+            assert ln.max() <= L and (ln[w == 0] == 0).all()
+            assert oracle.code_bits(w, ln) == brute_min_cost(w[syms], L)
+
+
+def test_limited_huffman_properties(spike_counts):
+    w = spike_counts + np.uint64(1)
+    full = oracle.huffman_lengths(w)
+    prev = None
+    for L in range(8, int(full.max()) + 3):
+        ln = oracle.huffman_limited_lengths(w, L)
+        assert ln.max() <= L and kraft(ln) == 1
+        cost = oracle.code_bits(w, ln)
+        assert prev is None or cost <= prev                    # a looser limit never costs more
+        prev = cost
+        if L >= full.max():
+            assert cost == oracle.code_bits(w, full)           # no binding limit: Huffman's cost
+    # 2^k equal weights under limit k: every length k
+    assert (oracle.huffman_limited_lengths(np.full(256, 3, np.uint64), 8) == 8).all()
+    # lone symbol: length 1; more symbols than 2^L: no code
+    one = np.zeros(256, np.uint64)
+    one[9] = 4
+    assert oracle.huffman_limited_lengths(one, 3)[9] == 1
+    with pytest.raises(oracle.OracleError) as ei:
+        oracle.huffman_limited_lengths(np.ones(256, np.uint64), 7)
+    assert ei.value.code == oracle.CODEBOOK
+
+
+def test_limited_huffman_round_trip():
+    x = np_grad(60000, (22, 1))
+    w = oracle.histogram(x) + np.uint64(1)
+    cb = oracle.huffman_limited_codebook(w, 11)
+    assert cb["len"].max() <= 11
+    enc = oracle.encode(x, cb, 4096, 64)
+    assert (oracle.decode(enc, cb) == x).all()
+    assert enc["total_bits"] == oracle.code_bits(oracle.histogram(x), cb["len"])
