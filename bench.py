@@ -349,16 +349,14 @@ def three_stage_latency(ecc, x, fixed_cb, b, C, S, stream, reps=8):
     return out
 
 
-def escape_code_timing(ecc, x, pooled_h, b, C, S, stream, reps=8):
-    """The ZipCCL-style exponent escape code as a third fixed codebook (from
-    the same warm-up counts) on the same tensor: encode and decode times
-    (device events, medians) and compressibility; informational, outside the
-    headline step."""
+def codebook_timing(ecc, x, dcb, b, C, S, stream, reps=8):
+    """Encode and decode times (device events, medians) and compressibility
+    of one more fixed codebook on the same tensor; informational, outside the
+    headline step.  b: output buffers sized for the codebook's longest code."""
     import torch
 
     EV = torch.cuda.Event
     n = x.numel()
-    dcb = ecc.to_device(ecc.escape_build_tables(pooled_h), x.device)
     enc_ms, dec_ms = [], []
     for rep in range(reps + 1):
         e0, e1, e2 = EV(enable_timing=True), EV(enable_timing=True), EV(enable_timing=True)
@@ -373,7 +371,7 @@ def escape_code_timing(ecc, x, pooled_h, b, C, S, stream, reps=8):
             enc_ms.append(e0.elapsed_time(e1))
             dec_ms.append(e1.elapsed_time(e2))
     if int(b["status"].item()) or int(b["dstatus"].item()) or not torch.equal(b["y"], x):
-        raise SystemExit("escape code: status or round trip failed")
+        raise SystemExit("extra codebook: status or round trip failed")
     bits = int(b["total_bits"].item())
     em, dm = statistics.median(enc_ms), statistics.median(dec_ms)
     return {"encode_ms": em, "decode_ms": dm, "encode_gbs": n / em / 1e6, "decode_gbs": n / dm / 1e6,
@@ -572,7 +570,14 @@ def run_ours(args):
         torch.cuda.synchronize()
         extra["histogram_gbs"] = 5 * n / h0.elapsed_time(h1) / 1e6
         extra["three_stage"] = three_stage_latency(ecc, x, dcbs["huffman"], bufs["huffman"], C, S, stream)
-        extra["escape_code"] = escape_code_timing(ecc, x, pooled_h, bufs["qlc"], C, S, stream)
+        # the other fixed codebooks, from the same warm-up counts (buffers
+        # sized for 11-bit and 14-bit codes: those of the QLC, and of the
+        # Huffman code, whose longest code is longer)
+        extra["escape_code"] = codebook_timing(ecc, x, ecc.to_device(ecc.escape_build_tables(pooled_h), dev),
+                                               bufs["qlc"], C, S, stream)
+        extra["huffman_limited_14"] = codebook_timing(
+            ecc, x, ecc.to_device(ecc.huff_build_limited(pooled_h + np.uint64(1), 14), dev), bufs["huffman"], C, S,
+            stream)
         if not args.no_sweep:
             sweep = {}
             for Cs in (4096, 16384, 65536):

@@ -168,6 +168,22 @@ ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, u
 ecc_status huff_build_canonical(const uint64_t weight[256], uint32_t max_len, ecc_codebook *out);
 
 /*
+ * huff_build_limited -- canonical Huffman code with no length above max_len
+ * (the decode tables stay bounded: "Quad Length Codes ...", section 5
+ * "Future Directions", asks for code lengths optimised under the decoder's
+ * constraints), from the package-merge algorithm of Larmore and Hirschberg
+ * (J. ACM 37(3), 1990): optimal among codes within the limit.  Leaves sort
+ * by (weight, byte value); a package and a leaf of equal weight: the leaf
+ * first.  With max_len at least the unlimited tree's depth the cost equals
+ * huff_build_canonical's (the lengths may differ on ties).
+ *   weight[256], out  as for huff_build_canonical (family ECC_FAMILY_HUFFMAN);
+ *   max_len   1..ECC_MAX_CODE_LEN.
+ * Errors: ECC_ERR_ARG (NULL, max_len out of range, all weights 0, a weight
+ * sum of 2^62 or more), ECC_ERR_CODEBOOK (more coded bytes than 2^max_len).
+ */
+ecc_status huff_build_limited(const uint64_t weight[256], uint32_t max_len, ecc_codebook *out);
+
+/*
  * escape_build_tables -- the exponent escape code of ZipCCL (gist.science
  * summary of arXiv 2604.27844, section 2.B "Tecnica di Codifica degli
  * Esponenti") as a fixed codebook for e4m3 bytes (sign bit 7, exponent bits

@@ -71,6 +71,7 @@ def _load():
             "qlc_search_widths": (I32, [P, U32, U32, P, P]),
             "huff_build_canonical": (I32, [P, U32, P]),
             "escape_build_tables": (I32, [P, P]),
+            "huff_build_limited": (I32, [P, U32, P]),
             "ecc_entropy_bits": (D, [P]),
             "ecc_kl_bits": (D, [P, P]),
             "ecc_code_bits": (I32, [P, P, P]),
@@ -213,6 +214,15 @@ def _stream_ptr(stream):
 
 def _dptr(t):
     return ct.c_void_p(t.data_ptr()) if t is not None else ct.c_void_p(0)
+
+
+def huff_build_limited(weight, max_len: int) -> np.ndarray:
+    """Host canonical Huffman codebook with lengths of at most max_len
+    (package-merge; raw ecc_codebook bytes)."""
+    weight = _u64(weight)
+    out = np.zeros(codebook_bytes(), np.uint8)
+    _check(_load().huff_build_limited(_np_ptr(weight), int(max_len), _np_ptr(out)), "huff_build_limited")
+    return out
 
 
 def escape_build_tables(count) -> np.ndarray:

@@ -95,6 +95,38 @@ void order_by_count(const uint64_t *count, uint8_t by_rank[256])
         by_rank[r] = (uint8_t)idx[r];
 }
 
+// Canonical Huffman codebook from code lengths (RFC 1951 section 3.2.2):
+// codes of one length are consecutive in byte order, the first code of each
+// length follows the last of the shorter ones, shifted.
+void canonical_fill(const uint8_t len[256], ecc_codebook *out)
+{
+    clear(out, ECC_FAMILY_HUFFMAN);
+    uint32_t bl_count[65] = {0};
+    for (int b = 0; b < 256; ++b)
+        if (len[b])
+            ++bl_count[len[b]];
+    // first code of each length: first[1] = 0, first[L] = (first[L-1] + count[L-1]) << 1
+    uint64_t next[65] = {0};
+    for (int L = 2; L <= 64; ++L)
+        next[L] = (next[L - 1] + bl_count[L - 1]) << 1;
+    int pos = 0;
+    for (int L = 1; L <= (int)ECC_MAX_CODE_LEN; ++L) {
+        out->index[L] = (uint16_t)pos;
+        out->count[L] = (uint16_t)bl_count[L];
+        out->first[L] = next[L];
+        for (int b = 0; b < 256; ++b)
+            if (len[b] == L)
+                out->sorted[pos++] = (uint8_t)b;
+    }
+    for (int b = 0; b < 256; ++b) {
+        if (!len[b])
+            continue;
+        out->len[b] = len[b];
+        out->code[b] = next[len[b]]++;
+    }
+    fill_derived(out);
+}
+
 } // namespace
 
 extern "C" {
@@ -268,32 +300,79 @@ ecc_status huff_build_canonical(const uint64_t weight[256], uint32_t max_len, ec
         }
     }
 
-    clear(out, ECC_FAMILY_HUFFMAN);
-    // canonical assignment by counting (RFC 1951 section 3.2.2)
-    uint32_t bl_count[65] = {0};
+    canonical_fill(len, out);
+    return ECC_OK;
+}
+
+ecc_status huff_build_limited(const uint64_t weight[256], uint32_t max_len, ecc_codebook *out)
+{
+    if (!weight || !out || max_len < 1 || max_len > ECC_MAX_CODE_LEN)
+        return ECC_ERR_ARG;
+    std::vector<int> leaves;
+    uint64_t total = 0;
     for (int b = 0; b < 256; ++b)
-        if (len[b])
-            ++bl_count[len[b]];
-    // first code of each length: first[1] = 0, first[L] = (first[L-1] + count[L-1]) << 1
-    uint64_t next[65] = {0};
-    for (int L = 2; L <= 64; ++L)
-        next[L] = (next[L - 1] + bl_count[L - 1]) << 1;
-    int pos = 0;
-    for (int L = 1; L <= (int)ECC_MAX_CODE_LEN; ++L) {
-        out->index[L] = (uint16_t)pos;
-        out->count[L] = (uint16_t)bl_count[L];
-        out->first[L] = next[L];
-        for (int b = 0; b < 256; ++b)
-            if (len[b] == L)
-                out->sorted[pos++] = (uint8_t)b;
+        if (weight[b]) {
+            if (weight[b] >= (1ull << 62) - total)
+                return ECC_ERR_ARG; // package sums must fit 64 bits
+            total += weight[b];
+            leaves.push_back(b);
+        }
+    const int n = (int)leaves.size();
+    if (n == 0)
+        return ECC_ERR_ARG;
+    uint8_t len[256] = {0};
+    if (n == 1) {
+        len[leaves[0]] = 1;
+        canonical_fill(len, out);
+        return ECC_OK;
     }
-    for (int b = 0; b < 256; ++b) {
-        if (!len[b])
-            continue;
-        out->len[b] = len[b];
-        out->code[b] = next[len[b]]++;
+    if (max_len < 63 && (1ull << max_len) < (uint64_t)n)
+        return ECC_ERR_CODEBOOK; // n codewords need more than max_len bits
+    std::stable_sort(leaves.begin(), leaves.end(), [&](int a, int b) { return weight[a] < weight[b]; });
+    // Package-merge (Larmore and Hirschberg): list d merges the leaves with
+    // the packages (consecutive pairs) of list d - 1, a leaf first on equal
+    // weight; a symbol's length is its number of occurrences among the
+    // first 2n - 2 items of the last list.
+    struct Item {
+        uint64_t w;
+        int sym;  // >= 0: leaf
+        int a, b; // package of items a, b of the previous list
+    };
+    std::vector<std::vector<Item>> lists(max_len + 1);
+    for (int b : leaves)
+        lists[1].push_back({weight[b], b, -1, -1});
+    for (uint32_t d = 2; d <= max_len; ++d) {
+        const std::vector<Item> &prev = lists[d - 1];
+        std::vector<Item> &cur = lists[d];
+        const size_t npk = prev.size() / 2;
+        size_t i = 0, j = 0;
+        while (i < leaves.size() || j < npk) {
+            const uint64_t pw = j < npk ? prev[2 * j].w + prev[2 * j + 1].w : 0;
+            if (i < leaves.size() && (j >= npk || weight[leaves[i]] <= pw)) {
+                cur.push_back({weight[leaves[i]], leaves[i], -1, -1});
+                ++i;
+            } else {
+                cur.push_back({pw, -1, (int)(2 * j), (int)(2 * j + 1)});
+                ++j;
+            }
+        }
     }
-    fill_derived(out);
+    // count occurrences: an explicit stack of (list, item)
+    std::vector<std::pair<uint32_t, int>> stack;
+    for (int i = 0; i < 2 * n - 2; ++i)
+        stack.push_back({max_len, i});
+    while (!stack.empty()) {
+        const auto [d, i] = stack.back();
+        stack.pop_back();
+        const Item &it = lists[d][i];
+        if (it.sym >= 0) {
+            ++len[it.sym];
+        } else {
+            stack.push_back({d - 1, it.a});
+            stack.push_back({d - 1, it.b});
+        }
+    }
+    canonical_fill(len, out);
     return ECC_OK;
 }
 

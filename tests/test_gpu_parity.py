@@ -363,6 +363,21 @@ def test_escape_code_workloads(law):
         check_against_oracle(x, cbb, ocb, C, S)
 
 
+@pytest.mark.parametrize("L", [11, 14])
+def test_limited_huffman_workloads(L):
+    """Length-limited canonical Huffman (package-merge) through the same
+    encoder and the table decoder: with L = 14 every code resolves from the
+    first-level table."""
+    n = (1 << 20) + 4099
+    for warm, x in ((np_grad(1 << 20, (32, 1)), np_grad(n, (32, 2))),
+                    (np_zero_spike(1 << 18, (32, 3)), np_zero_spike(n, (32, 4)))):
+        w = oracle.histogram(warm) + np.uint64(1)
+        cbb, ocb = ecc.huff_build_limited(w, L), oracle.huffman_limited_codebook(w, L)
+        assert int(ecc.codebook_view(cbb)["max_len"]) <= L
+        for C, S in ((16384, 256), (4096, 64)):
+            check_against_oracle(x, cbb, ocb, C, S)
+
+
 def test_escape_of_a_top_exponent_is_corrupt():
     """000 followed by a top-7 exponent is no codeword: planting one at the
     start of a sub-block flags the stream."""

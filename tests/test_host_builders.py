@@ -103,6 +103,24 @@ def test_huffman_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", list(pmfs().keys()))
+def test_limited_huffman_matches_oracle(name):
+    weight = pmfs()[name]
+    nz = int((weight > 0).sum())
+    for L in (8, 10, 11, 14, 20, 48):
+        if nz > (1 << L):
+            continue
+        cb = ecc.codebook_view(ecc.huff_build_limited(weight, L))
+        ref = oracle.huffman_limited_codebook(weight, L)
+        assert cb["family"] == ecc.FAMILY_HUFFMAN
+        assert (cb["len"] == ref["len"]).all(), L
+        assert (cb["code"] == ref["code"]).all(), L
+        assert int(cb["max_len"]) <= L
+    with pytest.raises(ecc.EccError) as ei:
+        ecc.huff_build_limited(np.ones(256, np.uint64), 7)
+    assert ei.value.code == ecc.ERR_CODEBOOK
+
+
+@pytest.mark.parametrize("name", list(pmfs().keys()))
 def test_escape_code_matches_oracle(name):
     count = pmfs()[name]
     cb = ecc.codebook_view(ecc.escape_build_tables(count))
