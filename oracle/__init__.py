@@ -71,6 +71,10 @@ def _load():
             "eo_decode_qlc": (I32, [P, U64, P, P, U64, U32, U32, P, P, P]),
             "eo_decode_huffman": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
             "eo_escape_codebook": (I32, [P, P, P, P]),
+            "eo_gqlc_layout": (I32, [I32, P, P, P]),
+            "eo_gqlc_codebook": (I32, [P, I32, P, P, P, P]),
+            "eo_gqlc_search": (I32, [P, I32, I32, I32, I32, P, P]),
+            "eo_decode_gqlc": (I32, [P, U64, P, P, U64, U32, U32, I32, P, P, P]),
             "eo_huffman_limited": (I32, [P, I32, P]),
             "eo_decode_escape": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
             "eo_entropy_bits": (ct.c_double, [P]),
@@ -139,34 +143,40 @@ def rank(count):
 BASE_WIDTHS = (3, 3, 3, 3, 3, 4, 5, 8)
 
 
-def qlc_layout(width):
-    """(start, size, covered) of the 8 areas filled in rank order."""
-    w = _u8(width)
+def qlc_layout(width, prefix_bits: int = 3):
+    """(start, size, covered) of the 2^prefix_bits areas filled in rank order."""
+    w = np.zeros(8, np.uint8)
+    w[:len(width)] = _u8(width)
     start = np.zeros(8, np.int32)
     size = np.zeros(8, np.int32)
-    covered = _load().eo_qlc_layout(_p(w), _p(start), _p(size))
-    return start, size, covered
+    covered = _load().eo_gqlc_layout(int(prefix_bits), _p(w), _p(start), _p(size))
+    A = 1 << prefix_bits
+    return start[:A], size[:A], covered
 
 
-def qlc_codebook(count, width=BASE_WIDTHS) -> dict:
-    """Per-byte QLC code (len, code) plus by_rank, for the given widths."""
+def qlc_codebook(count, width=BASE_WIDTHS, prefix_bits: int = 3) -> dict:
+    """Per-byte QLC code (len, code) plus by_rank, for the widths of the
+    2^prefix_bits areas (the page's code: 3 prefix bits, 8 areas)."""
     count = _u64(count)
-    w = _u8(width)
+    w = np.zeros(8, np.uint8)
+    w[:len(width)] = _u8(width)
     ln = np.zeros(256, np.uint8)
     code = np.zeros(256, np.uint64)
     br = np.zeros(256, np.uint8)
-    _check(_load().eo_qlc_codebook(_p(count), _p(w), _p(ln), _p(code), _p(br)), "qlc_codebook")
-    return {"family": "qlc", "width": w.copy(), "len": ln, "code": code, "by_rank": br}
+    _check(_load().eo_gqlc_codebook(_p(count), int(prefix_bits), _p(w), _p(ln), _p(code), _p(br)), "qlc_codebook")
+    return {"family": "qlc", "prefix_bits": int(prefix_bits), "width": w[:1 << prefix_bits].copy(), "len": ln,
+            "code": code, "by_rank": br}
 
 
-def qlc_search(count, max_distinct=4, require_full=False, nondecreasing_only=True):
-    """Adapted-QLC widths by exhaustive search; returns (width, cost_bits)."""
+def qlc_search(count, max_distinct=4, require_full=False, nondecreasing_only=True, prefix_bits: int = 3):
+    """Adapted-QLC widths of the 2^prefix_bits areas by exhaustive search;
+    returns (width, cost_bits)."""
     count = _u64(count)
     w = np.zeros(8, np.uint8)
     cost = np.zeros(1, np.uint64)
-    _check(_load().eo_qlc_search(_p(count), int(max_distinct), int(bool(require_full)),
-                                 int(bool(nondecreasing_only)), _p(w), _p(cost)), "qlc_search")
-    return w, int(cost[0])
+    _check(_load().eo_gqlc_search(_p(count), int(prefix_bits), int(max_distinct), int(bool(require_full)),
+                                  int(bool(nondecreasing_only)), _p(w), _p(cost)), "qlc_search")
+    return w[:1 << prefix_bits].copy(), int(cost[0])
 
 
 # ---------------------------------------------------------------- Huffman
@@ -267,8 +277,10 @@ def decode(enc: dict, cb: dict) -> np.ndarray:
     buf = payload if payload.size else np.zeros(1, np.uint8)
     lib = _load()
     if cb["family"] == "qlc":
-        rc = lib.eo_decode_qlc(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
-                               _p(_u8(cb["width"])), _p(_u8(cb["by_rank"])), _p(out))
+        w = np.zeros(8, np.uint8)
+        w[:len(cb["width"])] = _u8(cb["width"])
+        rc = lib.eo_decode_gqlc(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
+                                int(cb.get("prefix_bits", 3)), _p(w), _p(_u8(cb["by_rank"])), _p(out))
     elif cb["family"] == "escape":
         rc = lib.eo_decode_escape(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
                                   _p(_u8(cb["top"])), _p(out))

@@ -114,13 +114,15 @@ void eo_rank(const uint64_t *count, uint8_t *rank, uint8_t *by_rank)
 /* ------------------------------------------------------------------ */
 /* Area layout ([QLC] section 2, "Partizionamento in Aree" and the     */
 /* base example: five areas of 8, one of 16, one of 32, the remaining  */
-/* 168).  Area k can hold 2^width[k] ranks; areas are filled in order. */
-/* Returns the number of ranks the areas can hold, capped at 256.      */
+/* 168).  With p prefix bits there are 2^p areas ([QLC] section 5:     */
+/* optimise the number of areas; the page's code has p = 3).  Area k   */
+/* can hold 2^width[k] ranks; areas are filled in order.  Returns the   */
+/* number of ranks the areas can hold, capped at 256.                  */
 /* ------------------------------------------------------------------ */
-int eo_qlc_layout(const uint8_t *width, int32_t *start, int32_t *size)
+int eo_gqlc_layout(int p, const uint8_t *width, int32_t *start, int32_t *size)
 {
     int next = 0;
-    for (int k = 0; k < 8; k++) {
+    for (int k = 0; k < (1 << p); k++) {
         int cap = 1 << width[k];
         int left = 256 - next;
         int take = cap < left ? cap : left;
@@ -133,17 +135,24 @@ int eo_qlc_layout(const uint8_t *width, int32_t *start, int32_t *size)
     return next;
 }
 
-/* Code of every byte under QLC widths: rank r in area k gets the code
- * (k << width[k]) | (r - start[k]) of length 3 + width[k]. */
-int eo_qlc_codebook(const uint64_t *count, const uint8_t *width, uint8_t *len,
-                    uint64_t *code, uint8_t *by_rank)
+int eo_qlc_layout(const uint8_t *width, int32_t *start, int32_t *size)
+{
+    return eo_gqlc_layout(3, width, start, size);
+}
+
+/* Code of every byte under widths of 2^p areas: rank r in area k gets the
+ * code (k << width[k]) | (r - start[k]) of length p + width[k]. */
+int eo_gqlc_codebook(const uint64_t *count, int p, const uint8_t *width, uint8_t *len,
+                     uint64_t *code, uint8_t *by_rank)
 {
     int32_t start[8], size[8];
     uint8_t rank[256];
-    for (int k = 0; k < 8; k++)
+    if (p < 1 || p > 3)
+        return EO_ARG;
+    for (int k = 0; k < (1 << p); k++)
         if (width[k] > 8)
             return EO_ARG;
-    if (eo_qlc_layout(width, start, size) < 256)
+    if (eo_gqlc_layout(p, width, start, size) < 256)
         return EO_ARG;
     eo_rank(count, rank, by_rank);
     for (int b = 0; b < 256; b++) {
@@ -151,30 +160,37 @@ int eo_qlc_codebook(const uint64_t *count, const uint8_t *width, uint8_t *len,
         int k = 0;
         while (!(r >= start[k] && r < start[k] + size[k]))
             k++;
-        len[b] = (uint8_t)(3 + width[k]);
+        len[b] = (uint8_t)(p + width[k]);
         code[b] = ((uint64_t)k << width[k]) | (uint64_t)(r - start[k]);
     }
     return EO_OK;
 }
 
-/* Expected-length cost (integer sum of count x length) of widths b when
- * ranks are filled in order; counts_by_rank is sorted descending.  Also
- * reports how many distinct lengths the non-empty areas use. */
-static uint64_t qlc_cost(const uint64_t *counts_by_rank, const uint8_t *b, int *distinct, int *capacity)
+int eo_qlc_codebook(const uint64_t *count, const uint8_t *width, uint8_t *len,
+                    uint64_t *code, uint8_t *by_rank)
+{
+    return eo_gqlc_codebook(count, 3, width, len, code, by_rank);
+}
+
+/* Expected-length cost (integer sum of count x length) of widths b of the
+ * 2^p areas when ranks are filled in order; counts_by_rank is sorted
+ * descending.  Also reports how many distinct lengths the non-empty areas
+ * use. */
+static uint64_t qlc_cost(int p, const uint64_t *counts_by_rank, const uint8_t *b, int *distinct, int *capacity)
 {
     int32_t start[8], size[8];
     int cap = 0;
-    for (int k = 0; k < 8; k++)
+    for (int k = 0; k < (1 << p); k++)
         cap += 1 << b[k];
     *capacity = cap;
-    eo_qlc_layout(b, start, size);
+    eo_gqlc_layout(p, b, start, size);
     uint64_t cost = 0;
     int seen[12] = {0};
     int nd = 0;
-    for (int k = 0; k < 8; k++) {
+    for (int k = 0; k < (1 << p); k++) {
         if (size[k] == 0)
             continue;
-        int L = 3 + b[k];
+        int L = p + b[k];
         if (!seen[L]) {
             seen[L] = 1;
             nd++;
@@ -188,17 +204,20 @@ static uint64_t qlc_cost(const uint64_t *counts_by_rank, const uint8_t *b, int *
 
 /* Adapted QLC ([QLC] section 2 "Adattabilita": change the symbols per area
  * and the lengths, keep 4 distinct lengths; section 5: optimise the areas
- * and lengths).  Exhaustive search over widths in 0..8 for the 8 areas with
- * capacity >= 256 (require_full: capacity == 256) and at most max_distinct
- * distinct lengths, minimising the integer cost; ties go to the
+ * and lengths).  Exhaustive search over widths in 0..8 for the 2^p areas
+ * with capacity >= 256 (require_full: capacity == 256) and at most
+ * max_distinct distinct lengths, minimising the integer cost; ties go to the
  * lexicographically smallest width vector.  nondecreasing_only restricts the
- * search to b0 <= b1 <= ... <= b7 (12870 vectors); 0 tries all 9^8.
- * Returns EO_ARG if no vector qualifies. */
-int eo_qlc_search(const uint64_t *count, int max_distinct, int require_full,
-                  int nondecreasing_only, uint8_t *width_out, uint64_t *cost_out)
+ * search to b0 <= b1 <= ...; 0 tries all 9^(2^p).  Returns EO_ARG if no
+ * vector qualifies. */
+int eo_gqlc_search(const uint64_t *count, int p, int max_distinct, int require_full,
+                   int nondecreasing_only, uint8_t *width_out, uint64_t *cost_out)
 {
     uint8_t rank[256], by_rank[256];
     uint64_t sorted[256];
+    if (p < 1 || p > 3)
+        return EO_ARG;
+    const int A = 1 << p;
     eo_rank(count, rank, by_rank);
     for (int r = 0; r < 256; r++)
         sorted[r] = count[by_rank[r]];
@@ -206,19 +225,17 @@ int eo_qlc_search(const uint64_t *count, int max_distinct, int require_full,
     int found = 0;
     uint64_t best = 0;
     uint8_t bestb[8] = {0};
-    uint8_t b[8];
-    /* odometer over 9^8 width vectors in lexicographic order */
-    for (int k = 0; k < 8; k++)
-        b[k] = 0;
+    uint8_t b[8] = {0};
+    /* odometer over 9^A width vectors in lexicographic order */
     for (;;) {
         int ok = 1;
         if (nondecreasing_only)
-            for (int k = 1; k < 8; k++)
+            for (int k = 1; k < A; k++)
                 if (b[k] < b[k - 1])
                     ok = 0;
         if (ok) {
             int nd, cap;
-            uint64_t c = qlc_cost(sorted, b, &nd, &cap);
+            uint64_t c = qlc_cost(p, sorted, b, &nd, &cap);
             int cap_ok = require_full ? (cap == 256) : (cap >= 256);
             if (cap_ok && nd <= max_distinct && (!found || c < best)) {
                 found = 1;
@@ -226,7 +243,7 @@ int eo_qlc_search(const uint64_t *count, int max_distinct, int require_full,
                 memcpy(bestb, b, 8);
             }
         }
-        int k = 7;
+        int k = A - 1;
         while (k >= 0 && b[k] == 8) {
             b[k] = 0;
             k--;
@@ -237,9 +254,17 @@ int eo_qlc_search(const uint64_t *count, int max_distinct, int require_full,
     }
     if (!found)
         return EO_ARG;
-    memcpy(width_out, bestb, 8);
+    memcpy(width_out, bestb, (size_t)A);
+    for (int k = A; k < 8; k++)
+        width_out[k] = 0;
     *cost_out = best;
     return EO_OK;
+}
+
+int eo_qlc_search(const uint64_t *count, int max_distinct, int require_full,
+                  int nondecreasing_only, uint8_t *width_out, uint64_t *cost_out)
+{
+    return eo_gqlc_search(count, 3, max_distinct, require_full, nondecreasing_only, width_out, cost_out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -508,6 +533,7 @@ static int decode_container(const uint8_t *in, uint64_t in_bytes, const uint64_t
 /* second LUT maps the rank back to the symbol).                       */
 /* ------------------------------------------------------------------ */
 typedef struct {
+    int p;
     uint8_t width[8];
     int32_t start[8], size[8];
     const uint8_t *by_rank;
@@ -517,7 +543,7 @@ static int qlc_symbol(eo_reader *r, const void *vctx, uint8_t *sym)
 {
     const qlc_ctx *q = (const qlc_ctx *)vctx;
     uint64_t k, v;
-    if (read_bits(r, 3, &k))
+    if (read_bits(r, q->p, &k))
         return -1;
     if (read_bits(r, q->width[k], &v))
         return -1;
@@ -527,20 +553,30 @@ static int qlc_symbol(eo_reader *r, const void *vctx, uint8_t *sym)
     return 0;
 }
 
-int eo_decode_qlc(const uint8_t *in, uint64_t in_bytes, const uint64_t *chunk_off,
-                  const uint16_t *sub_bits, uint64_t n, uint32_t C, uint32_t S,
-                  const uint8_t *width, const uint8_t *by_rank, uint8_t *out)
+int eo_decode_gqlc(const uint8_t *in, uint64_t in_bytes, const uint64_t *chunk_off,
+                   const uint16_t *sub_bits, uint64_t n, uint32_t C, uint32_t S,
+                   int p, const uint8_t *width, const uint8_t *by_rank, uint8_t *out)
 {
     qlc_ctx q;
-    for (int k = 0; k < 8; k++) {
+    if (p < 1 || p > 3)
+        return EO_ARG;
+    q.p = p;
+    for (int k = 0; k < (1 << p); k++) {
         if (width[k] > 8)
             return EO_ARG;
         q.width[k] = width[k];
     }
-    if (eo_qlc_layout(width, q.start, q.size) < 256)
+    if (eo_gqlc_layout(p, width, q.start, q.size) < 256)
         return EO_ARG;
     q.by_rank = by_rank;
     return decode_container(in, in_bytes, chunk_off, sub_bits, n, C, S, qlc_symbol, &q, out);
+}
+
+int eo_decode_qlc(const uint8_t *in, uint64_t in_bytes, const uint64_t *chunk_off,
+                  const uint16_t *sub_bits, uint64_t n, uint32_t C, uint32_t S,
+                  const uint8_t *width, const uint8_t *by_rank, uint8_t *out)
+{
+    return eo_decode_gqlc(in, in_bytes, chunk_off, sub_bits, n, C, S, 3, width, by_rank, out);
 }
 
 /* ------------------------------------------------------------------ */

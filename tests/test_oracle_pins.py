@@ -517,3 +517,59 @@ def test_limited_huffman_round_trip():
     enc = oracle.encode(x, cb, 4096, 64)
     assert (oracle.decode(enc, cb) == x).all()
     assert enc["total_bits"] == oracle.code_bits(oracle.histogram(x), cb["len"])
+
+
+# --------------------------------------------------------------- QLC with 1-3 prefix bits
+
+def qlc_cost_py(sorted_counts, p, widths):
+    """Test-side cost of widths for 2^p areas filled in rank order, and its
+    capacity and distinct lengths (non-empty areas)."""
+    nxt, cost, lens = 0, 0, set()
+    for w in widths:
+        take = max(0, min(1 << w, 256 - nxt))
+        if take:
+            lens.add(p + w)
+            cost += int(sorted_counts[nxt:nxt + take].sum()) * (p + w)
+        nxt += take
+    return cost, sum(1 << w for w in widths), len(lens)
+
+
+@pytest.mark.parametrize("p", [1, 2])
+def test_fewer_prefix_bits_search_against_all_vectors(p, spike_counts, gauss_counts):
+    """With 2 or 4 areas every width vector can be tried in the test: the
+    oracle's non-decreasing search reaches the optimum over all orderings,
+    and returns the lexicographically smallest optimal non-decreasing one."""
+    A = 1 << p
+    for counts in (spike_counts, gauss_counts):
+        sc = np.sort(counts.astype(np.int64))[::-1]
+        for md in (2, 4):
+            allv = [(qlc_cost_py(sc, p, v), v) for v in itertools.product(range(9), repeat=A)]
+            ok = [(c, v) for (c, cap, nd), v in allv if cap >= 256 and nd <= md]
+            best = min(c for c, _ in ok)
+            nd_ok = sorted(v for c, v in ok if c == best and list(v) == sorted(v))
+            w, cost = oracle.qlc_search(counts, md, prefix_bits=p)
+            assert cost == best
+            assert tuple(int(x) for x in w) == nd_ok[0]
+
+
+@pytest.mark.parametrize("p", [1, 2, 3])
+def test_prefix_bits_codes_kraft_and_round_trip(p, gauss_counts):
+    w, _ = oracle.qlc_search(gauss_counts, 4, prefix_bits=p)
+    cb = oracle.qlc_codebook(gauss_counts, w, prefix_bits=p)
+    start, size, covered = oracle.qlc_layout(w, prefix_bits=p)
+    assert covered == 256
+    assert kraft(cb["len"]) == sum(Fraction(int(z), 2 ** (p + int(x))) for z, x in zip(size, w))
+    assert prefix_free([bits_of(c, l) for c, l in zip(cb["code"], cb["len"])])
+    # the code of rank r in area k is k's p-bit prefix then r - start[k]
+    r, br = oracle.rank(gauss_counts)
+    for b in range(256):
+        k = int(np.searchsorted(start, r[b], side="right")) - 1
+        while size[k] == 0:
+            k -= 1
+        assert bits_of(cb["code"][b], cb["len"][b]) == format(k, f"0{p}b") + (
+            format(int(r[b] - start[k]), f"0{int(w[k])}b") if w[k] else "")
+    x = qlc_base_tensor()[:50000]
+    enc = oracle.encode(x, cb, 4096, 64)
+    assert (oracle.decode(enc, cb) == x).all()
+    if p == 3:
+        assert (cb["len"] == oracle.qlc_codebook(gauss_counts, w)["len"]).all()
