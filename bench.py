@@ -575,6 +575,18 @@ def run_ours(args):
         # Huffman code, whose longest code is longer)
         extra["escape_code"] = codebook_timing(ecc, x, ecc.to_device(ecc.escape_build_tables(pooled_h), dev),
                                                bufs["qlc"], C, S, stream)
+        # QLC with 2, 4 or 8 areas (searched widths, at most 4 lengths): code
+        # bits from the counts; the best layout timed
+        qa = {}
+        for pb in (1, 2, 3):
+            wq, cost = ecc.gqlc_search_widths(pooled_h, pb, 4)
+            qa[f"prefix_bits_{pb}"] = {"widths": [int(v) for v in wq],
+                                       "bits_per_byte_warmup": cost / float(pooled_h.sum())}
+        best = min((1, 2, 3), key=lambda pb: qa[f"prefix_bits_{pb}"]["bits_per_byte_warmup"])
+        wq = qa[f"prefix_bits_{best}"]["widths"]
+        qa["best"] = {"prefix_bits": best, **codebook_timing(
+            ecc, x, ecc.to_device(ecc.gqlc_build_tables(pooled_h, wq, best), dev), bufs["qlc"], C, S, stream)}
+        extra["qlc_adapted"] = qa
         extra["huffman_limited_14"] = codebook_timing(
             ecc, x, ecc.to_device(ecc.huff_build_limited(pooled_h + np.uint64(1), 14), dev), bufs["huffman"], C, S,
             stream)

@@ -93,7 +93,8 @@ typedef struct ecc_codebook {
     uint32_t max_len;     /* longest code length in bits */
     uint32_t min_len;     /* shortest code length in bits */
     uint32_t n_coded;     /* number of byte values that have a code */
-    uint32_t reserved[3];
+    uint32_t prefix_bits; /* QLC: prefix bits p, 2^p areas (the page's code: 3); 0 for other families */
+    uint32_t reserved[2];
     uint64_t code[256];   /* code of each byte value, right-aligned */
     uint64_t first[64];   /* Huffman: first canonical code of each length */
     uint32_t enc_code[256]; /* derived: code << (32 - len) (first bit in bit 31) if 1 <= len <= 31, else 0 */
@@ -147,6 +148,21 @@ ecc_status qlc_build_tables(const uint64_t count[256], const uint8_t width[8], e
  */
 ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, uint32_t require_full,
                              uint8_t width_out[8], uint64_t *cost_bits);
+
+/*
+ * gqlc_build_tables, gqlc_search_widths -- QLC with p = 1, 2 or 3 prefix
+ * bits, i.e. 2, 4 or 8 areas ("Quad Length Codes ...", section 5 "Future
+ * Directions": optimise the number of areas and the code lengths).  As
+ * qlc_build_tables / qlc_search_widths (which are the p = 3 case) with
+ * lengths p + width[k] over the first 2^p entries of width (the rest are
+ * ignored on input, 0 on output).  The decoder's QLC fast path serves
+ * p = 3; other codebooks decode through the first-level table.
+ * Errors: as for the p = 3 calls, and ECC_ERR_ARG for p outside 1..3.
+ */
+ecc_status gqlc_build_tables(const uint64_t count[256], uint32_t prefix_bits, const uint8_t width[8],
+                             ecc_codebook *out);
+ecc_status gqlc_search_widths(const uint64_t count[256], uint32_t prefix_bits, uint32_t max_distinct,
+                              uint32_t require_full, uint8_t width_out[8], uint64_t *cost_bits);
 
 /*
  * huff_build_canonical -- the fixed Huffman codebook of the single-stage

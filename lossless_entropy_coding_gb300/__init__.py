@@ -28,7 +28,7 @@ BASE_WIDTHS = (3, 3, 3, 3, 3, 4, 5, 8)
 # Layout of ecc_codebook (C struct in include/ecc.h), naturally aligned.
 CODEBOOK_DTYPE = np.dtype([
     ("magic", "<u4"), ("family", "<u4"), ("max_len", "<u4"), ("min_len", "<u4"),
-    ("n_coded", "<u4"), ("reserved", "<u4", (3,)),
+    ("n_coded", "<u4"), ("prefix_bits", "<u4"), ("reserved", "<u4", (2,)),
     ("code", "<u8", (256,)), ("first", "<u8", (64,)),
     ("enc_code", "<u4", (256,)), ("enc_mul", "<u4", (256,)), ("area", "<u4", (8,)), ("dec", "<u2", (16384,)),
     ("count", "<u2", (64,)), ("index", "<u2", (64,)),
@@ -71,6 +71,8 @@ def _load():
             "qlc_search_widths": (I32, [P, U32, U32, P, P]),
             "huff_build_canonical": (I32, [P, U32, P]),
             "escape_build_tables": (I32, [P, P]),
+            "gqlc_build_tables": (I32, [P, U32, P, P]),
+            "gqlc_search_widths": (I32, [P, U32, U32, U32, P, P]),
             "huff_build_limited": (I32, [P, U32, P]),
             "ecc_entropy_bits": (D, [P]),
             "ecc_kl_bits": (D, [P, P]),
@@ -214,6 +216,27 @@ def _stream_ptr(stream):
 
 def _dptr(t):
     return ct.c_void_p(t.data_ptr()) if t is not None else ct.c_void_p(0)
+
+
+def gqlc_build_tables(count, width, prefix_bits: int) -> np.ndarray:
+    """Host QLC codebook with 2^prefix_bits areas (raw ecc_codebook bytes)."""
+    count = _u64(count)
+    w = np.zeros(8, np.uint8)
+    w[:len(width)] = _u8(width)
+    out = np.zeros(codebook_bytes(), np.uint8)
+    _check(_load().gqlc_build_tables(_np_ptr(count), int(prefix_bits), _np_ptr(w), _np_ptr(out)),
+           "gqlc_build_tables")
+    return out
+
+
+def gqlc_search_widths(count, prefix_bits: int, max_distinct: int = 4, require_full: bool = False):
+    """Best widths of the 2^prefix_bits areas; returns (width, cost_bits)."""
+    count = _u64(count)
+    w = np.zeros(8, np.uint8)
+    cost = np.zeros(1, np.uint64)
+    _check(_load().gqlc_search_widths(_np_ptr(count), int(prefix_bits), int(max_distinct), int(bool(require_full)),
+                                      _np_ptr(w), _np_ptr(cost)), "gqlc_search_widths")
+    return w[:1 << prefix_bits].copy(), int(cost[0])
 
 
 def huff_build_limited(weight, max_len: int) -> np.ndarray:

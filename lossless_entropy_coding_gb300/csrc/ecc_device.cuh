@@ -1767,7 +1767,7 @@ struct DecTables {
 // Whether the QLC path can decode with this codebook.
 __device__ __forceinline__ bool qlc_mode(const ecc_codebook *cb)
 {
-    return cb->family == ECC_FAMILY_QLC && cb->max_len <= 11;
+    return cb->family == ECC_FAMILY_QLC && cb->prefix_bits == 3 && cb->max_len <= 11;
 }
 
 // Fill the QLC tables from the codebook: the rank table over the 32 KB of

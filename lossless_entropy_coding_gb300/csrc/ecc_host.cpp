@@ -61,19 +61,19 @@ void fill_derived(ecc_codebook *cb)
     cb->n_coded = nc;
 }
 
-bool valid_widths(const uint8_t *width)
+bool valid_widths(const uint8_t *width, int areas)
 {
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < areas; ++k)
         if (width[k] > 8)
             return false;
     return true;
 }
 
-// Ranks held by areas filled in order, capped at 256.
-int layout(const uint8_t *width, int start[8], int size[8])
+// Ranks held by the first `areas` areas filled in order, capped at 256.
+int layout(const uint8_t *width, int areas, int start[8], int size[8])
 {
     int used = 0;
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < areas; ++k) {
         int room = 256 - used;
         int n = std::min(1 << width[k], room);
         start[k] = used;
@@ -133,20 +133,25 @@ extern "C" {
 
 size_t ecc_codebook_bytes(void) { return sizeof(ecc_codebook); }
 
-ecc_status qlc_build_tables(const uint64_t count[256], const uint8_t width[8], ecc_codebook *out)
+ecc_status gqlc_build_tables(const uint64_t count[256], uint32_t prefix_bits, const uint8_t width[8],
+                             ecc_codebook *out)
 {
-    if (!count || !width || !out || !valid_widths(width))
+    if (!count || !width || !out || prefix_bits < 1 || prefix_bits > 3)
+        return ECC_ERR_ARG;
+    const int areas = 1 << prefix_bits;
+    if (!valid_widths(width, areas))
         return ECC_ERR_ARG;
     int start[8], size[8];
-    if (layout(width, start, size) < 256)
+    if (layout(width, areas, start, size) < 256)
         return ECC_ERR_ARG;
     clear(out, ECC_FAMILY_QLC);
+    out->prefix_bits = prefix_bits;
     order_by_count(count, out->by_rank);
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < areas; ++k) {
         out->width[k] = width[k];
         out->area_start[k] = (uint16_t)start[k];
         out->area_size[k] = (uint16_t)size[k];
-        uint32_t L = 3u + width[k];
+        uint32_t L = prefix_bits + width[k];
         out->area[k] = (uint32_t)start[k] | (L << 16) | ((uint32_t)width[k] << 24);
         for (int v = 0; v < size[k]; ++v) {
             int r = start[k] + v;
@@ -160,10 +165,16 @@ ecc_status qlc_build_tables(const uint64_t count[256], const uint8_t width[8], e
     return ECC_OK;
 }
 
+ecc_status qlc_build_tables(const uint64_t count[256], const uint8_t width[8], ecc_codebook *out)
+{
+    return gqlc_build_tables(count, 3, width, out);
+}
+
 namespace {
 
 struct Search {
     uint64_t sorted[257]; // prefix sums of counts in rank order
+    uint32_t p;           // prefix bits: 2^p areas
     uint32_t max_distinct;
     bool full;
     bool found = false;
@@ -174,17 +185,18 @@ struct Search {
     // cost of the current w, or false if it does not qualify
     bool evaluate(uint64_t &cost) const
     {
+        const int areas = 1 << p;
         uint32_t cap = 0;
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < areas; ++k)
             cap += 1u << w[k];
         if (full ? cap != 256 : cap < 256)
             return false;
         uint32_t lengths_used = 0; // bit L set if some non-empty area uses length L
         uint64_t c = 0;
         int at = 0;
-        for (int k = 0; k < 8 && at < 256; ++k) {
+        for (int k = 0; k < areas && at < 256; ++k) {
             int take = std::min(1 << w[k], 256 - at);
-            uint32_t L = 3u + w[k];
+            uint32_t L = p + w[k];
             lengths_used |= 1u << L;
             c += (sorted[at + take] - sorted[at]) * L;
             at += take;
@@ -198,7 +210,7 @@ struct Search {
     // widths non-decreasing, generated in lexicographic order
     void walk(int k, int lo)
     {
-        if (k == 8) {
+        if (k == (1 << p)) {
             uint64_t c;
             if (evaluate(c) && (!found || c < best)) {
                 found = true;
@@ -216,10 +228,10 @@ struct Search {
 
 } // namespace
 
-ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, uint32_t require_full,
-                             uint8_t width_out[8], uint64_t *cost_bits)
+ecc_status gqlc_search_widths(const uint64_t count[256], uint32_t prefix_bits, uint32_t max_distinct,
+                              uint32_t require_full, uint8_t width_out[8], uint64_t *cost_bits)
 {
-    if (!count || !width_out || max_distinct == 0)
+    if (!count || !width_out || max_distinct == 0 || prefix_bits < 1 || prefix_bits > 3)
         return ECC_ERR_ARG;
     Search s;
     uint8_t by_rank[256];
@@ -227,8 +239,10 @@ ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, u
     s.sorted[0] = 0;
     for (int r = 0; r < 256; ++r)
         s.sorted[r + 1] = s.sorted[r] + count[by_rank[r]];
+    s.p = prefix_bits;
     s.max_distinct = max_distinct;
     s.full = require_full != 0;
+    std::memset(s.w, 0, 8);
     s.walk(0, 0);
     if (!s.found)
         return ECC_ERR_ARG;
@@ -236,6 +250,12 @@ ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, u
     if (cost_bits)
         *cost_bits = s.best;
     return ECC_OK;
+}
+
+ecc_status qlc_search_widths(const uint64_t count[256], uint32_t max_distinct, uint32_t require_full,
+                             uint8_t width_out[8], uint64_t *cost_bits)
+{
+    return gqlc_search_widths(count, 3, max_distinct, require_full, width_out, cost_bits);
 }
 
 ecc_status huff_build_canonical(const uint64_t weight[256], uint32_t max_len, ecc_codebook *out)

@@ -378,6 +378,20 @@ def test_limited_huffman_workloads(L):
             check_against_oracle(x, cbb, ocb, C, S)
 
 
+@pytest.mark.parametrize("p", [1, 2])
+def test_prefix_bits_qlc_workloads(p):
+    """QLC with 2 or 4 areas (searched widths, at most 4 lengths) through the
+    same encoder and the table decoder."""
+    n = (1 << 20) + 12345
+    for warm, x in ((np_grad(1 << 20, (33, 1)), np_grad(n, (33, 2))),
+                    (np_zero_spike(1 << 18, (33, 3)), np_zero_spike(n, (33, 4)))):
+        count = oracle.histogram(warm)
+        w, _ = oracle.qlc_search(count, 4, prefix_bits=p)
+        cbb, ocb = ecc.gqlc_build_tables(count, w, p), oracle.qlc_codebook(count, w, prefix_bits=p)
+        for C, S in ((16384, 256), (4096, 64)):
+            check_against_oracle(x, cbb, ocb, C, S)
+
+
 def test_escape_of_a_top_exponent_is_corrupt():
     """000 followed by a top-7 exponent is no codeword: planting one at the
     start of a sub-block flags the stream."""

@@ -102,6 +102,24 @@ def test_huffman_matches_oracle(name):
     assert (cb2["len"] == oracle.huffman_lengths(fixed)).all()
 
 
+@pytest.mark.parametrize("name", ["gauss", "spike", "grad", "ties", "random"])
+@pytest.mark.parametrize("p", [1, 2, 3])
+def test_prefix_bits_qlc_matches_oracle(name, p):
+    count = pmfs()[name]
+    for md in (2, 4):
+        w, cost = ecc.gqlc_search_widths(count, p, md)
+        ow, ocost = oracle.qlc_search(count, md, prefix_bits=p)
+        assert (w == ow).all() and cost == ocost
+        cb = ecc.codebook_view(ecc.gqlc_build_tables(count, w, p))
+        ref = oracle.qlc_codebook(count, w, prefix_bits=p)
+        assert cb["family"] == ecc.FAMILY_QLC and int(cb["prefix_bits"]) == p
+        assert (cb["len"] == ref["len"]).all() and (cb["code"] == ref["code"]).all()
+    if p == 3:
+        assert (ecc.gqlc_build_tables(count, ecc.BASE_WIDTHS, 3) == ecc.qlc_build_tables(count)).all()
+    with pytest.raises(ecc.EccError):
+        ecc.gqlc_build_tables(count, (8, 8), 4)
+
+
 @pytest.mark.parametrize("name", list(pmfs().keys()))
 def test_limited_huffman_matches_oracle(name):
     weight = pmfs()[name]
