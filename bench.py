@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the informational timings after the timed region (three-stage, other codebooks)")
     p.add_argument("--tensors", type=int, default=4096, help="batched workload: number of tensors")
     p.add_argument("--workload", choices=["gradient", "batched"], default="gradient",
                    help="gradient: the 2^30-byte tensor (default); batched: 4096 tensors in one launch each way")
@@ -380,6 +382,36 @@ def codebook_timing(ecc, x, dcb, b, C, S, stream, reps=8):
             "payload_bytes": int(b["chunk_off"][-1].item())}
 
 
+def other_timings(ecc, x, pooled_h, dcbs, bufs, C, S, stream, dev):
+    """Informational timings after the timed region: the three-stage
+    pipeline, and the other fixed codebooks on the same tensor."""
+    import numpy as np
+
+    out = {}
+    out["three_stage"] = three_stage_latency(ecc, x, dcbs["huffman"], bufs["huffman"], C, S, stream)
+    # the other fixed codebooks, from the same warm-up counts (buffers
+    # sized for 11-bit and 14-bit codes: those of the QLC, and of the
+    # Huffman code, whose longest code is longer)
+    out["escape_code"] = codebook_timing(ecc, x, ecc.to_device(ecc.escape_build_tables(pooled_h), dev),
+                                         bufs["qlc"], C, S, stream)
+    # QLC with 2, 4 or 8 areas (searched widths, at most 4 lengths): code
+    # bits from the counts; the best layout timed
+    qa = {}
+    for pb in (1, 2, 3):
+        wq, cost = ecc.gqlc_search_widths(pooled_h, pb, 4)
+        qa[f"prefix_bits_{pb}"] = {"widths": [int(v) for v in wq],
+                                   "bits_per_byte_warmup": cost / float(pooled_h.sum())}
+    best = min((1, 2, 3), key=lambda pb: qa[f"prefix_bits_{pb}"]["bits_per_byte_warmup"])
+    wq = qa[f"prefix_bits_{best}"]["widths"]
+    qa["best"] = {"prefix_bits": best, **codebook_timing(
+        ecc, x, ecc.to_device(ecc.gqlc_build_tables(pooled_h, wq, best), dev), bufs["qlc"], C, S, stream)}
+    out["qlc_adapted"] = qa
+    out["huffman_limited_14"] = codebook_timing(
+        ecc, x, ecc.to_device(ecc.huff_build_limited(pooled_h + np.uint64(1), 14), dev), bufs["huffman"], C, S,
+        stream)
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -628,27 +660,8 @@ def run_ours(args):
         h1.record(stream)
         torch.cuda.synchronize()
         extra["histogram_gbs"] = 5 * n / h0.elapsed_time(h1) / 1e6
-        extra["three_stage"] = three_stage_latency(ecc, x, dcbs["huffman"], bufs["huffman"], C, S, stream)
-        # the other fixed codebooks, from the same warm-up counts (buffers
-        # sized for 11-bit and 14-bit codes: those of the QLC, and of the
-        # Huffman code, whose longest code is longer)
-        extra["escape_code"] = codebook_timing(ecc, x, ecc.to_device(ecc.escape_build_tables(pooled_h), dev),
-                                               bufs["qlc"], C, S, stream)
-        # QLC with 2, 4 or 8 areas (searched widths, at most 4 lengths): code
-        # bits from the counts; the best layout timed
-        qa = {}
-        for pb in (1, 2, 3):
-            wq, cost = ecc.gqlc_search_widths(pooled_h, pb, 4)
-            qa[f"prefix_bits_{pb}"] = {"widths": [int(v) for v in wq],
-                                       "bits_per_byte_warmup": cost / float(pooled_h.sum())}
-        best = min((1, 2, 3), key=lambda pb: qa[f"prefix_bits_{pb}"]["bits_per_byte_warmup"])
-        wq = qa[f"prefix_bits_{best}"]["widths"]
-        qa["best"] = {"prefix_bits": best, **codebook_timing(
-            ecc, x, ecc.to_device(ecc.gqlc_build_tables(pooled_h, wq, best), dev), bufs["qlc"], C, S, stream)}
-        extra["qlc_adapted"] = qa
-        extra["huffman_limited_14"] = codebook_timing(
-            ecc, x, ecc.to_device(ecc.huff_build_limited(pooled_h + np.uint64(1), 14), dev), bufs["huffman"], C, S,
-            stream)
+        if not args.no_extras:
+            extra.update(other_timings(ecc, x, pooled_h, dcbs, bufs, C, S, stream, dev))
         if not args.no_sweep:
             sweep = {}
             for Cs in (4096, 16384, 65536):
