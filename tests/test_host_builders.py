@@ -207,3 +207,28 @@ def test_sizes():
             assert ecc.num_chunks(n, C) == -(-n // C)
             for L in (11, 48):
                 assert ecc.max_encoded_bytes(n, C, L) == oracle.max_encoded_bytes(n, C, L)
+
+
+def test_new_builders_reject_bad_arguments():
+    """Argument checks of the later builders, through the C ABI (no GPU)."""
+    lib = ecc.lib()
+    cnt = np.ones(256, np.uint64)
+    out = np.zeros(ecc.codebook_bytes(), np.uint8)
+    w = np.zeros(8, np.uint8)
+    cost = np.zeros(1, np.uint64)
+    p = lambda a: a.ctypes.data_as(ct.c_void_p)
+    assert lib.escape_build_tables(None, p(out)) == ecc.ERR_ARG
+    assert lib.escape_build_tables(p(cnt), None) == ecc.ERR_ARG
+    assert lib.huff_build_limited(p(cnt), 0, p(out)) == ecc.ERR_ARG
+    assert lib.huff_build_limited(p(cnt), 49, p(out)) == ecc.ERR_ARG
+    assert lib.huff_build_limited(p(np.zeros(256, np.uint64)), 14, p(out)) == ecc.ERR_ARG
+    assert lib.huff_build_limited(p(np.full(256, 1 << 60, np.uint64)), 14, p(out)) == ecc.ERR_ARG  # sum >= 2^62
+    assert lib.gqlc_build_tables(p(cnt), 0, p(w), p(out)) == ecc.ERR_ARG
+    assert lib.gqlc_build_tables(p(cnt), 4, p(w), p(out)) == ecc.ERR_ARG
+    assert lib.gqlc_build_tables(p(cnt), 2, p(w), p(out)) == ecc.ERR_ARG  # 4 areas of 1 rank: < 256
+    assert lib.gqlc_search_widths(p(cnt), 2, 0, 0, p(w), p(cost)) == ecc.ERR_ARG
+    # the device builder checks its pointers before any CUDA call
+    dummy = ct.c_void_p(16)
+    assert lib.huff_build_device(dummy, 1, 48, ct.c_void_p(24), dummy, None) == ecc.ERR_ARG  # misaligned
+    assert lib.huff_build_device(None, 1, 48, dummy, dummy, None) == ecc.ERR_ARG
+    assert lib.huff_build_device(dummy, 1, 0, dummy, dummy, None) == ecc.ERR_ARG
