@@ -70,7 +70,9 @@ enum {
     ECC_ERR_CORRUPT = 3,  /* stream, offsets or sub-block bits inconsistent */
     ECC_ERR_CODEBOOK = 4, /* bad codebook, or a byte the codebook does not code */
     ECC_ERR_TIMEOUT = 5,  /* a bounded device wait ran out (the kernel returned) */
-    ECC_ERR_CUDA = 6      /* a CUDA runtime call failed */
+    ECC_ERR_CUDA = 6,     /* a CUDA runtime call failed */
+    ECC_ERR_CHECK = 7     /* index-checked builds only (-DECC_CHECKED): a kernel index was out of
+                             range; the access was skipped */
 };
 
 enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2, ECC_FAMILY_ESCAPE = 3 };

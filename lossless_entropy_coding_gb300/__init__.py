@@ -20,7 +20,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libecc_gb300.so")
 
-OK, ERR_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_CODEBOOK, ERR_TIMEOUT, ERR_CUDA = range(7)
+OK, ERR_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_CODEBOOK, ERR_TIMEOUT, ERR_CUDA, ERR_CHECK = range(8)
 FAMILY_QLC, FAMILY_HUFFMAN, FAMILY_ESCAPE = 1, 2, 3
 MAX_CODE_LEN = 48
 BASE_WIDTHS = (3, 3, 3, 3, 3, 4, 5, 8)

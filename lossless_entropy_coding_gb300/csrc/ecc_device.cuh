@@ -862,12 +862,24 @@ __host__ __device__ constexpr uint32_t enc_ws_slot_bytes(uint32_t C, uint32_t S)
 // by the next lane.
 struct SegPacker {
     uint32_t addr, cur, K; // addr: shared-window address of the word holding cur
+#ifdef ECC_CHECKED
+    uint32_t lim = ~0u;  // index-checked builds: stores must end at or below lim
+    bool bad_index = false;
+#endif
 
     // one append's tail: store w at addr when gate == 0 (the word filled up),
     // then take xlo (the code's remaining bits) as the partial word and move
     // to the next word; else w stays the partial word
     __device__ __forceinline__ void tail(uint32_t w, uint32_t xlo, uint32_t gate)
     {
+#ifdef ECC_CHECKED
+        if (gate == 0 && addr + 4u > lim) { // skip the store, keep the stream going
+            bad_index = true;
+            cur = xlo;
+            addr += 4u;
+            return;
+        }
+#endif
         asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %4, 0;\n\t@p st.shared.b32 [%0], %2;\n\t"
                      "selp.b32 %1, %3, %2, p;\n\t@p add.u32 %0, %0, 4;\n\t}"
                      : "+r"(addr), "=r"(cur)
@@ -988,10 +1000,17 @@ static __device__ __noinline__ uint32_t slow_group_bits(const uint2 *lut, uint4 
 // Slow-group sink coded one code at a time from the table (SegPacker's
 // protocol); returns the final partial word and its shared-window address.
 static __device__ __noinline__ PackEnd seg_single_pack(const uint2 *lut, uint32_t region, uint32_t pos,
-                                                       uint32_t c0, uint4 in)
+                                                       uint32_t c0, uint4 in, uint32_t lim)
 {
     SegPacker pk;
+#ifdef ECC_CHECKED
+    pk.lim = lim;
+#endif
     pk.pack_singles(lut, region, pos, c0, in);
+#ifdef ECC_CHECKED
+    if (pk.bad_index)
+        return PackEnd{pk.cur, pk.addr, 0xFFFFFFFFu};
+#endif
     return PackEnd{pk.cur, pk.addr, 1u};
 }
 
@@ -1064,25 +1083,47 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
             // the previous round (merged there): every lane reads it before
             // any lane of this round stores, so whichever lane completes it
             // keeps those bits (the others merge them again, harmlessly)
+            const uint32_t lim = region + cap_bits / 8u + 16u; // the region's end (capacity + slack)
+#ifdef ECC_CHECKED
+            bool bad_index = region + (pos >> 5) * 4u + 4u > lim;
+            const uint32_t cw = bad_index ? 0u : ld_shared_u32(region + (pos >> 5) * 4u);
+#else
             const uint32_t cw = ld_shared_u32(region + (pos >> 5) * 4u);
+#endif
             const uint32_t c0 = (pos & 31u) ? cw : 0u;
             __syncwarp();
             if (fast) {
                 SegPacker pk;
+#ifdef ECC_CHECKED
+                pk.lim = lim;
+#endif
                 pk.pack(region, pos, c0, pv, pq);
                 __syncwarp(); // every store of the round precedes every merge
-                red_or_shared(pk.addr, pk.cur);
+#ifdef ECC_CHECKED
+                bad_index |= pk.bad_index || pk.addr + 4u > lim;
+                if (pk.addr + 4u <= lim)
+#endif
+                    red_or_shared(pk.addr, pk.cur);
             } else {
                 uint32_t word = 0, wa = 0, nb = 0;
                 if (cnt) {
                     if (!slow) {
                         SegPacker pk;
+#ifdef ECC_CHECKED
+                        pk.lim = lim;
+#endif
                         pk.pack(region, pos, c0, pv, pq);
+#ifdef ECC_CHECKED
+                        bad_index |= pk.bad_index;
+#endif
                         word = pk.cur;
                         wa = pk.addr;
                         nb = 1; // 1..32 bits: always a partial word to merge
                     } else if (single) {
-                        const PackEnd e = seg_single_pack(lut, region, pos, c0, in);
+                        const PackEnd e = seg_single_pack(lut, region, pos, c0, in, lim);
+#ifdef ECC_CHECKED
+                        bad_index |= e.nb != 1u;
+#endif
                         word = e.word;
                         wa = e.wa;
                         nb = 1;
@@ -1092,12 +1133,24 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
                         word = e.word;
                         wa = region + e.wa * 4u;
                         nb = e.nb;
+#ifdef ECC_CHECKED
+                        bad_index |= wa > lim; // its stores ended below wa
+#endif
                     }
                 }
                 __syncwarp();
+#ifdef ECC_CHECKED
+                bad_index |= nb && wa + 4u > lim;
+                if (nb && wa + 4u <= lim)
+#else
                 if (nb)
+#endif
                     red_or_shared(wa, word);
             }
+#ifdef ECC_CHECKED
+            if (bad_index)
+                set_status(job.status, ECC_ERR_CHECK);
+#endif
             __syncwarp();
         } else if (lane == 0) {
             atomicOr(flag_word, 1u);
@@ -1116,7 +1169,9 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
 // take the first bits of the segments after it.  Region 0 also zeroes the
 // words up to the 16-byte boundary after the stream.  Each lane takes four
 // region words at a time (one 16-byte load).
-__device__ __forceinline__ void copy_region_out(uint32_t slot, uint32_t region_words, const uint32_t *seg_bits,
+// Returns true (index-checked builds only) if the region or the chunk's
+// padded payload would be overrun; nothing is copied then.
+__device__ __forceinline__ bool copy_region_out(uint32_t slot, uint32_t region_words, const uint32_t *seg_bits,
                                                 uint32_t nseg, uint32_t w, uint32_t *dst)
 {
     const int lane = threadIdx.x & 31;
@@ -1127,6 +1182,10 @@ __device__ __forceinline__ void copy_region_out(uint32_t slot, uint32_t region_w
     }
     const uint32_t T = seg_bits[w];
     const uint32_t j0 = (P + 31) >> 5, nw = ((P + T + 31) >> 5) - j0;
+#ifdef ECC_CHECKED
+    if (nw && (nw >= region_words || j0 + nw > (pad16((total + 7) >> 3) >> 2)))
+        return true;
+#endif
     // nw = 0: the segment's bits all lie inside a word that starts in an
     // earlier segment, whose last word takes them
     if (nw) {
@@ -1166,6 +1225,7 @@ __device__ __forceinline__ void copy_region_out(uint32_t slot, uint32_t region_w
         if (jend + (uint32_t)lane < jpad)
             dst[jend + lane] = 0;
     }
+    return false;
 }
 
 // Zero one warp's region (shared-window address, region_words words, a
@@ -1356,8 +1416,11 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             const uint32_t seg = seg_symbols(pjob.C, pjob.S);
             const uint32_t nseg = pjob.C / seg;
             if (sh.out_copy[pb] && (uint32_t)warp < nseg) {
-                copy_region_out(stage0 + pb * slot_bytes, region_bytes(seg) / 4u, sh.seg_bits[pb], nseg, warp,
-                                reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb]));
+                const bool bad_index =
+                    copy_region_out(stage0 + pb * slot_bytes, region_bytes(seg) / 4u, sh.seg_bits[pb], nseg, warp,
+                                    reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb]));
+                if (bad_index && lane == 0)
+                    set_status(pjob.status, ECC_ERR_CHECK);
                 if (kBatched && ps.t_done) {
                     __threadfence(); // this lane's payload stores before the completion count
                     __syncwarp();
@@ -1913,10 +1976,23 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
                 }
             }
         }
+#ifdef ECC_CHECKED
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (s[r].wa > a_max + 16u * 4u) // past the guard the stage keeps after wmax
+                set_status(job.status, ECC_ERR_CHECK);
+#endif
         if (i & 8) {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
+            for (int r = 0; r < R; ++r) {
+#ifdef ECC_CHECKED
+                if (dst[r] + i + 8 > job.out + job.n) {
+                    set_status(job.status, ECC_ERR_CHECK);
+                    continue;
+                }
+#endif
                 st_stream16(dst[r] + i - 8, make_uint4(q0[r], q1[r], a[r], b[r]));
+            }
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {

@@ -508,6 +508,7 @@ const char *ecc_status_string(ecc_status s)
     case ECC_ERR_CODEBOOK: return "codebook error";
     case ECC_ERR_TIMEOUT: return "device wait timed out";
     case ECC_ERR_CUDA: return "CUDA error";
+    case ECC_ERR_CHECK: return "kernel index out of range (checked build)";
     default: return "unknown status";
     }
 }

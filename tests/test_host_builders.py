@@ -232,3 +232,12 @@ def test_new_builders_reject_bad_arguments():
     assert lib.huff_build_device(dummy, 1, 48, ct.c_void_p(24), dummy, None) == ecc.ERR_ARG  # misaligned
     assert lib.huff_build_device(None, 1, 48, dummy, dummy, None) == ecc.ERR_ARG
     assert lib.huff_build_device(dummy, 1, 0, dummy, dummy, None) == ecc.ERR_ARG
+
+
+def test_checked_build_compiles_and_exports():
+    """The index-checked variant (-DECC_CHECKED) builds for sm_103a and
+    exports the same C ABI (its kernels run in tests/test_gpu_checked.py)."""
+    path = ecc_build.build(checked=True)
+    lib = ct.CDLL(path)
+    for name in header_functions():
+        assert hasattr(lib, name), name
