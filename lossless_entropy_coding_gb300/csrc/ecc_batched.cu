@@ -335,7 +335,7 @@ struct BatchPlan {
     std::vector<uint32_t> order; // workspace position -> caller's index
     std::vector<uint64_t> prefix;
     uint64_t n_items = 0, total_chunks = 0;
-    uint32_t max_C = 1024, warps = 1, stage = 0, ws_slot = 0;
+    uint32_t max_C = 1024, warps = 1, stage = 0, ws_slot = 0, dec_stage = 0;
     int R = 4; // decode: streams per lane, the smallest any tensor allows
 };
 
@@ -380,10 +380,13 @@ ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool c
         P->total_chunks += nc;
         P->max_C = std::max(P->max_C, d.C);
         P->ws_slot = std::max(P->ws_slot, enc_ws_slot_bytes(d.C, d.S));
+        // decode stage: the single-tensor decoder's (a chunk at up to 9.25
+        // bits a symbol, larger ones 32 sub-blocks at a time), for every shape
+        P->dec_stage = std::max(P->dec_stage, dec_stage_bytes(d.C, d.S));
         if (d.n)
             P->R = std::min<int>(P->R, (int)std::max<uint32_t>(1, d.C / d.S / 32));
     }
-    P->stage = stage_bytes_for(P->max_C);
+    P->stage = encode ? stage_bytes_for(P->max_C) : P->dec_stage;
     P->R = P->R >= 4 ? 4 : P->R >= 2 ? 2 : 1;
     P->warps = encode ? 1u : batch_decode_warps(P->stage, P->R);
     P->order.resize(count);
