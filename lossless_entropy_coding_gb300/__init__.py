@@ -197,8 +197,11 @@ def encode_workspace_bytes(n: int, C: int) -> int:
 
 
 def default_subblock(C: int) -> int:
-    """Sub-block size used when none is given: C/64, clamped to [64, 1024]."""
-    return int(min(1024, max(64, C // 64)))
+    """Sub-block size used when none is given: C/64, clamped to [64, 256].
+
+    Larger sub-blocks cost the decoder occupancy: a warp stages 32 sub-blocks
+    or more, so with S > 256 fewer warps fit an SM."""
+    return int(min(256, max(64, C // 64)))
 
 
 # ------------------------------------------------------------------ device calls

@@ -314,6 +314,11 @@ constexpr uint32_t kEncSlots = 4; // claimed two chunks ahead: slots k .. k + 2 
 // time, and the 16 lanes of each half read 16 different bank pairs whatever
 // bytes they look up.
 constexpr uint32_t kLutReplicas = 16;
+// The warp-segmented encoder takes chunks smaller than kGroupSyms symbols in
+// groups of consecutive chunks and codes and places a group as one unit of
+// kEncWarps segments (one a compute warp): at most kMaxGroup chunks.
+constexpr uint32_t kGroupSyms = 16384;
+constexpr uint32_t kMaxGroup = kEncWarps;
 struct EncShared {
     uint2 lut[kLutRows * kLutReplicas];
     alignas(16) uint32_t warp_tot[2][kEncWarps]; // per tile parity: one barrier per tile suffices
@@ -328,8 +333,9 @@ struct EncShared {
     uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
     EncSlot slot[kEncSlots];
     uint32_t seg_bits[2][kEncWarps]; // warp-segmented encoder: payload bits of each warp's segment, per slot
-    uint64_t out_prefix[2];          // byte offset of the slot's chunk in the output (resolved look-back)
+    uint64_t out_prefix[2];          // byte offset of the slot's chunk or group in the output (resolved look-back)
     uint32_t out_copy[2];            // 1: the compute warps copy the slot out to the output
+    uint32_t chunk_rel[2][kMaxGroup + 1]; // byte offsets of a group's chunks in its output (last: the group's bytes)
 };
 
 __host__ __device__ constexpr uint32_t enc_shared_bytes() { return (sizeof(EncShared) + 15u) & ~15u; }
@@ -810,13 +816,15 @@ static __device__ __noinline__ void encode_chunk_warp(const EncJob &job, uint64_
     }
 }
 
-// Bulk-copy the whole 16-byte groups of chunk c's input into buf (thread 0);
-// completion arrives on bar.  The last chunk's trailing bytes (fewer than
-// 16) are read from global memory by the thread that owns them.
-__device__ __forceinline__ void issue_chunk_input(const EncJob &job, uint64_t c, uint8_t *buf, uint64_t *bar)
+// Bulk-copy the whole 16-byte groups of the input of chunks c .. c + g - 1
+// into buf (thread 0); completion arrives on bar.  The last chunk's trailing
+// bytes (fewer than 16) are read from global memory by the thread that owns
+// them.
+__device__ __forceinline__ void issue_chunk_input(const EncJob &job, uint64_t c, uint8_t *buf, uint64_t *bar,
+                                                  uint32_t g = 1)
 {
     const uint64_t base = c * job.C;
-    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
+    const uint32_t L = (uint32_t)min((uint64_t)job.C * g, job.n - base);
     const uint32_t whole = L & ~15u;
     fence_proxy_async();
     mbar_expect_tx(bar, whole);
@@ -849,6 +857,27 @@ __host__ __device__ constexpr uint32_t region_bytes(uint32_t seg) { return regio
 __host__ __device__ constexpr uint32_t enc_ws_slot_bytes(uint32_t C, uint32_t S)
 {
     return (C / seg_symbols(C, S)) * region_bytes(seg_symbols(C, S));
+}
+// Segments of chunks coded in groups (chunks of fewer than kGroupSyms
+// symbols): kGroupSyms / kEncWarps symbols, or the whole chunk when it is
+// smaller (and at least one sub-block and one round); a group holds
+// kEncWarps of them, one a compute warp.
+__host__ __device__ constexpr uint32_t seg_symbols_grouped(uint32_t C, uint32_t S)
+{
+    if (C >= kGroupSyms)
+        return seg_symbols(C, S);
+    uint32_t seg = C < kGroupSyms / kEncWarps ? C : kGroupSyms / kEncWarps;
+    seg = seg > S ? seg : S;
+    return seg > kRoundSyms ? seg : kRoundSyms;
+}
+// Chunks of a group, and the stage slot of a group.
+__host__ __device__ constexpr uint32_t enc_group_chunks(uint32_t C, uint32_t S)
+{
+    return C >= kGroupSyms ? 1u : kEncWarps / (C / seg_symbols_grouped(C, S));
+}
+__host__ __device__ constexpr uint32_t enc_ws_group_slot_bytes(uint32_t C, uint32_t S)
+{
+    return kEncWarps * region_bytes(seg_symbols_grouped(C, S));
 }
 
 // Fast-path sink for one lane's group: the multiplying packer with plain
@@ -1298,17 +1327,23 @@ __host__ __device__ constexpr size_t enc_ws_smem_bytes(uint32_t cmax, uint32_t s
 constexpr uint32_t kBarReady = 4; // + slot: the chunk's output offset is known (output warp -> compute)
 
 // kBatched: chunks of many tensors from bt (each chunk's job in its slot);
-// else the chunks of `single`, claimed with `ticket`.
-template <bool kBatched>
+// else the chunks of `single`, one at a time or (kGrouped) in groups of gsz
+// consecutive chunks, claimed with `ticket` (one ticket a group).  A group is coded
+// as one unit: its chunks' segments spread over the compute warps (segment q
+// of the group to warp q % kEncWarps), one look-back word and one output
+// offset for the group, its chunks placed back to back from that offset.
+template <bool kBatched, bool kGrouped = false>
 __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_chunks, uint32_t *ticket,
                                                const EncBatch &bt, uint32_t slot_bytes, uint32_t cmax,
-                                               uint64_t timeout_ns)
+                                               uint64_t timeout_ns, uint32_t gsz = 1)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     EncShared &sh = *reinterpret_cast<EncShared *>(smem);
     uint8_t *inbuf = smem + enc_shared_bytes();
     const uint32_t stage0 = smem_u32(inbuf + 2 * (size_t)cmax);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t G = kGrouped && !kBatched ? gsz : 1u;
+    const uint64_t n_units = kBatched ? 0 : (n_chunks + G - 1) / G; // groups
     if (!kBatched && (single.cb->magic != ECC_CODEBOOK_MAGIC || single.cb->max_len > ECC_MAX_CODE_LEN)) {
         if (tid == 0 && blockIdx.x == 0)
             set_status(single.status, ECC_ERR_CODEBOOK);
@@ -1326,17 +1361,19 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
         load_encode_lut(sh, single.cb, kEncThreadsWS);
     for (uint32_t i = tid; i < 2 * slot_bytes / 16; i += kEncThreadsWS)
         st_shared_v4_zero(stage0 + i * 16u);
-    // one thread: claim the chunk of iteration k into slot k % 4 and, unless
-    // staging was given up, bulk-copy its input into buffer k % 2
+    // one thread: claim the unit (group or chunk) of iteration k into slot
+    // k % 4 and, unless staging was given up, bulk-copy its input into buffer
+    // k % 2
     auto claim = [&](uint32_t k) {
         EncSlot &s = sh.slot[k % kEncSlots];
         if (kBatched)
             claim_batched(s, bt);
         else
-            claim_single(s, ticket, n_chunks);
+            claim_single(s, ticket, n_units);
         s.staged = 0;
         if (s.state != kSlotEnd && !sh.nostage) {
-            issue_chunk_input(kBatched ? s.job : single, s.c, inbuf + (size_t)(k & 1) * cmax, &sh.bar[k & 1]);
+            issue_chunk_input(kBatched ? s.job : single, s.c * G, inbuf + (size_t)(k & 1) * cmax, &sh.bar[k & 1],
+                              G);
             s.parity = sh.issued[k & 1] & 1u;
             s.staged = 1;
             ++sh.issued[k & 1];
@@ -1358,24 +1395,29 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             const EncSlot &s = sh.slot[k % kEncSlots];
             if (s.state == kSlotEnd)
                 break;
-            if (lane == 0) { // chunk k's input buffer is free: claim chunk k + 2 into it
+            if (lane == 0) { // unit k's input buffer is free: claim unit k + 2 into it
                 if (sh.slot[(k + 1) % kEncSlots].state != kSlotEnd)
                     claim(k + 2);
                 else
                     sh.slot[(k + 2) % kEncSlots].state = kSlotEnd;
             }
             const EncJob &job = kBatched ? s.job : single;
-            const uint64_t c = s.c;
+            const uint64_t u = s.c;
+            const uint64_t c0 = u * G;
+            const uint32_t gc = kGrouped ? (uint32_t)min((uint64_t)G, n_chunks - c0) : 1u; // chunks in the unit
             const uint32_t run = sh.slot_bits[b];
             const uint32_t fl = sh.slot_flags[b];
-            const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
+            const uint64_t bytes = kGrouped ? (uint64_t)sh.chunk_rel[b][gc] : ((uint64_t)run + 127u) / 128u * 16u;
             bool to = false;
-            const uint64_t prefix = c == 0 ? 0 : resolve_prefix(job.flags, c, bytes, timeout_ns, &to);
+            const uint64_t prefix = u == 0 ? 0 : resolve_prefix(job.flags, u, bytes, timeout_ns, &to);
             const bool fits = prefix + bytes <= job.out_cap;
             const bool write = fits && !to;
+            if (kGrouped && (uint32_t)lane < gc)
+                job.chunk_off[c0 + lane + 1] = prefix + sh.chunk_rel[b][lane + 1];
             if (lane == 0) {
-                job.chunk_off[c + 1] = prefix + bytes;
-                if (c == 0)
+                if (!kGrouped)
+                    job.chunk_off[u + 1] = prefix + bytes;
+                if (u == 0)
                     job.chunk_off[0] = 0;
                 atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)run);
                 if (to)
@@ -1388,8 +1430,15 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 sh.out_prefix[b] = prefix;
                 sh.out_copy[b] = copy ? 1u : 0u;
             }
-            if ((fl & 1u) && write) // a segment outgrew its region: code the chunk straight into the output
-                encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + prefix), (uint32_t)(bytes / 4));
+            if ((fl & 1u) && write) { // a segment outgrew its region: code the unit straight into the output
+                if (kGrouped)
+                    for (uint32_t i = 0; i < gc; ++i)
+                        encode_chunk_warp(job, c0 + i,
+                                          reinterpret_cast<uint32_t *>(job.out + prefix + sh.chunk_rel[b][i]),
+                                          (sh.chunk_rel[b][i + 1] - sh.chunk_rel[b][i]) / 4u);
+                else
+                    encode_chunk_warp(job, u, reinterpret_cast<uint32_t *>(job.out + prefix), (uint32_t)(bytes / 4));
+            }
             if (kBatched && s.t_done && !copy) {
                 // completion counts one per segment: the copying warps count
                 // their own, else this warp counts the chunk's
@@ -1406,19 +1455,23 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
         }
     } else { // ---------------- compute warps
         const ecc_codebook *loaded = kBatched ? nullptr : single.cb;
-        // copy this warp's region of chunk j (slot j % 2) out once the
-        // output warp has resolved the chunk's offset
+        // copy this warp's regions of unit j (slot j % 2) out once the output
+        // warp has resolved the unit's offset
         auto copy_out = [&](uint32_t j) {
             const uint32_t pb = j & 1;
             bar_sync(kBarReady + pb, kEncThreadsWS);
             const EncSlot &ps = sh.slot[j % kEncSlots];
             const EncJob &pjob = kBatched ? ps.job : single;
-            const uint32_t seg = seg_symbols(pjob.C, pjob.S);
+            const uint32_t seg = kGrouped ? seg_symbols_grouped(pjob.C, pjob.S) : seg_symbols(pjob.C, pjob.S);
             const uint32_t nseg = pjob.C / seg;
-            if (sh.out_copy[pb] && (uint32_t)warp < nseg) {
-                const bool bad_index =
-                    copy_region_out(stage0 + pb * slot_bytes, region_bytes(seg) / 4u, sh.seg_bits[pb], nseg, warp,
-                                    reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb]));
+            const uint32_t gc = kGrouped ? (uint32_t)min((uint64_t)G, n_chunks - ps.c * G) : 1u;
+            const uint32_t rwords = region_bytes(seg) / 4u;
+            const uint32_t q = (uint32_t)warp; // the unit's segment q: chunk i, segment w of the chunk
+            if (sh.out_copy[pb] && q < gc * nseg) {
+                const uint32_t i = kGrouped ? q >> (31 - __clz(nseg)) : 0u, w = q - i * nseg; // nseg: a power of 2
+                const bool bad_index = copy_region_out(
+                    stage0 + pb * slot_bytes + i * nseg * rwords * 4u, rwords, sh.seg_bits[pb] + i * nseg, nseg, w,
+                    reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb] + (kGrouped ? sh.chunk_rel[pb][i] : 0u)));
                 if (bad_index && lane == 0)
                     set_status(pjob.status, ECC_ERR_CHECK);
                 if (kBatched && ps.t_done) {
@@ -1441,19 +1494,24 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 break;
             }
             const EncJob &job = kBatched ? s.job : single;
-            const uint64_t c = s.c;
-            const uint32_t seg = seg_symbols(job.C, job.S);
+            const uint64_t u = s.c;
+            const uint64_t c0 = u * G;
+            const uint32_t gc = kGrouped ? (uint32_t)min((uint64_t)G, n_chunks - c0) : 1u;
+            const uint32_t seg = kGrouped ? seg_symbols_grouped(job.C, job.S) : seg_symbols(job.C, job.S);
             const uint32_t nseg = job.C / seg;
             const uint32_t rwords = region_bytes(seg) / 4u;
-            // only warps below nseg own a region: the slot holds nseg of them
+            // this warp's segment: segment w of the unit's chunk i (i = 0 unless
+            // grouped; nseg is a power of two)
+            const uint32_t i = kGrouped ? (uint32_t)warp >> (31 - __clz(nseg)) : 0u;
+            const uint32_t w = (uint32_t)warp - i * nseg;
             const uint32_t region = stage0 + b * slot_bytes + (uint32_t)warp * rwords * 4u;
             if (k >= 2) {
-                // chunk k - 2 left this slot: every warp has copied its region
-                // out (after coding chunk k - 1) and is past its lookups
+                // unit k - 2 left this slot: every warp has copied its region
+                // out (after coding unit k - 1) and is past its lookups
                 bar_sync(kBarCompute, kEncThreads);
                 if (tid == 0)
                     sh.slot_flags[b] = 0; // the output warp has read it
-                if ((uint32_t)warp < nseg)
+                if ((uint32_t)warp < G * nseg)
                     zero_region(region, rwords);
             }
             if (kBatched && state == kSlotChunk && job.cb != loaded) {
@@ -1465,9 +1523,10 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 loaded = job.cb;
                 bar_sync(kBarCompute, kEncThreads);
             }
-            const uint64_t base = c * job.C;
-            const uint32_t L = state == kSlotChunk ? (uint32_t)min((uint64_t)job.C, job.n - base) : 0u;
-            const uint32_t s0 = (uint32_t)warp * seg, s1 = min(s0 + seg, L);
+            const uint64_t base = (c0 + i) * job.C;
+            const uint32_t L =
+                state == kSlotChunk && i < gc ? (uint32_t)min((uint64_t)job.C, job.n - base) : 0u;
+            const uint32_t s0 = w * seg, s1 = min(s0 + seg, L);
             bool bad = state == kSlotBadCodebook;
             uint32_t bits = 0;
             if (s0 < s1) {
@@ -1479,27 +1538,43 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                         sh.nostage = 1;
                     }
                 }
-                const uint8_t *src = inbuf + (size_t)b * cmax;
+                const uint8_t *src = inbuf + (size_t)b * cmax + (size_t)i * job.C;
                 const uint32_t cap = region_cap_bytes(seg) * 8u;
                 bits = ok ? encode_segment<true>(sh, job, src, base, s0, s1, region, cap, &sh.slot_flags[b], &bad)
                           : encode_segment<false>(sh, job, nullptr, base, s0, s1, region, cap, &sh.slot_flags[b],
                                                   &bad);
             }
-            if (bad && lane == 0)
-                set_status(job.status, ECC_ERR_CODEBOOK);
             if (lane == 0)
                 sh.seg_bits[b][warp] = bits;
-            bar_sync(kBarCompute, kEncThreads); // the chunk is coded
+            if (bad && lane == 0)
+                set_status(job.status, ECC_ERR_CODEBOOK);
+            bar_sync(kBarCompute, kEncThreads); // the unit is coded
             if (tid == 0) {
                 uint32_t run = 0;
-                for (int w = 0; w < kEncWarps; ++w)
-                    run += (uint32_t)w < nseg ? sh.seg_bits[b][w] : 0u;
-                const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
-                st_relaxed(job.flags + c, (c == 0 ? kFlagPrefix : kFlagAggregate) | (bytes & kValueMask));
+                uint64_t bytes;
+                if (kGrouped) { // the chunks' padded offsets in the group
+                    uint32_t rel = 0;
+                    sh.chunk_rel[b][0] = 0;
+                    for (uint32_t i = 0; i < gc; ++i) {
+                        uint32_t r = 0;
+                        for (uint32_t w = 0; w < nseg; ++w)
+                            r += sh.seg_bits[b][i * nseg + w];
+                        run += r;
+                        rel += (r + 127u) / 128u * 16u;
+                        sh.chunk_rel[b][i + 1] = rel;
+                    }
+                    bytes = rel;
+                } else {
+#pragma unroll
+                    for (uint32_t w = 0; w < kEncWarps; ++w)
+                        run += w < nseg ? sh.seg_bits[b][w] : 0u;
+                    bytes = ((uint64_t)run + 127u) / 128u * 16u;
+                }
+                st_relaxed(job.flags + u, (u == 0 ? kFlagPrefix : kFlagAggregate) | (bytes & kValueMask));
                 sh.slot_bits[b] = run;
             }
             bar_arrive(kBarFull + b, kEncThreadsWS);
-            // chunk k - 1's offset has had a whole chunk to resolve
+            // unit k - 1's offset has had a whole unit to resolve
             if (k >= 1)
                 copy_out(k - 1);
         }
@@ -2046,20 +2121,44 @@ __device__ __forceinline__ bool chunk_range_ok(const DecJob &job, uint64_t c, ui
     return b1 > b0 && b1 <= job.in_bytes && !((b0 | b1) & 15) && (b1 - b0) <= (uint64_t)job.C * 8;
 }
 
-// A chunk too big for the warp's stage: stage and decode it 32 sub-blocks at
-// a time (one stream per lane); each group's bytes fit, since a stage holds
-// at least 32 sub-blocks at the longest fast code lengths.
+// End of a chunk's stream after its last code at bit `carry`: the chunk's
+// size must be the stream padded to 16 bytes, and the padding zero bits (read
+// from global memory by lane 0).  Returns true if not (lane 0's answer;
+// skipped when the stream is already known bad).
+__device__ __forceinline__ bool chunk_tail_bad(const DecJob &job, uint64_t b0, uint32_t bytes, uint32_t carry,
+                                               bool known_bad)
+{
+    bool bad = pad16((carry + 7) / 8) != bytes;
+    if (!bad && !known_bad && (threadIdx.x & 31) == 0) {
+        const uint32_t *words = reinterpret_cast<const uint32_t *>(job.in + b0);
+        for (uint32_t wi = carry >> 5; wi < bytes / 4; ++wi) {
+            uint32_t w = bswap32(__ldg(words + wi));
+            if (wi == (carry >> 5))
+                w &= 0xFFFFFFFFu >> (carry & 31);
+            bad |= w != 0;
+        }
+    }
+    return bad;
+}
+
+// Sub-blocks [g_begin, g_end) of a chunk (a multiple of 32, all full) too big
+// for the warp's stage: stage and decode them 32 sub-blocks at a time (one
+// stream per lane); each group's bytes fit, since a stage holds at least 32
+// sub-blocks at the longest fast code lengths.  carry0: the chunk's bits
+// before g_begin; `last`: the range ends the chunk, so its end is checked
+// against the chunk's size and zero padding.
 template <bool kQlc>
 static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, const DecTables &T, WarpStage &ws,
-                                                           uint64_t base, uint32_t nsub, uint64_t sub0, uint64_t b0,
-                                                           uint32_t bytes)
+                                                           uint64_t base, uint32_t g_begin, uint32_t g_end,
+                                                           uint64_t sub0, uint64_t b0, uint32_t bytes,
+                                                           uint32_t carry0, bool last)
 {
     const uint16_t *dec = T.dec;
     const LongTable &lt = *T.lt;
     const int lane = threadIdx.x & 31;
     bool bad = false;
-    uint32_t carry = 0; // bits of the chunk's earlier groups
-    for (uint32_t g0 = 0; g0 < nsub; g0 += 32) {
+    uint32_t carry = carry0; // bits of the chunk's earlier groups
+    for (uint32_t g0 = g_begin; g0 < g_end; g0 += 32) {
         const uint32_t v = job.sub_bits[sub0 + g0 + lane];
         uint32_t incl = v;
 #pragma unroll
@@ -2071,7 +2170,7 @@ static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, co
         // the group's bytes, widened to 16-byte boundaries of the chunk
         const uint32_t s0 = (carry >> 3) & ~15u;
         const uint32_t s1 = min(pad16((carry + gbits + 7) >> 3), bytes);
-        if (carry + gbits > bytes * 8u) { // sub_bits claim more bits than the chunk holds
+        if (carry + gbits > bytes * 8u || gbits == 0) { // sub_bits claim more bits than the chunk holds, or none
             bad = true;
             break;
         }
@@ -2106,18 +2205,8 @@ static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, co
         decode_group_fast<1, kQlc>(job, T, ws.buf, (s1 - s0) / 4 + 4, base, g0, st, nb, bad);
         carry += gbits;
     }
-    if (pad16((carry + 7) / 8) != bytes)
-        bad = true;
-    // the padding after the last code must be zero bits
-    if (!bad && lane == 0) {
-        const uint32_t *words = reinterpret_cast<const uint32_t *>(job.in + b0);
-        for (uint32_t wi = carry >> 5; wi < bytes / 4; ++wi) {
-            uint32_t w = bswap32(__ldg(words + wi));
-            if (wi == (carry >> 5))
-                w &= 0xFFFFFFFFu >> (carry & 31);
-            bad |= w != 0;
-        }
-    }
+    if (last)
+        bad |= chunk_tail_bad(job, b0, bytes, carry, bad);
     if (__any_sync(~0u, bad) && lane == 0)
         set_status(job.status, ECC_ERR_CORRUPT);
     __syncwarp();
@@ -2147,7 +2236,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables 
     const uint32_t bytes = (uint32_t)(b1 - b0);
     const bool staged = ws.buf != nullptr && bytes + kStageGuard <= ws.bytes;
     if (!staged && ws.buf != nullptr && L == job.C && nsub >= 32 && (nsub & 31) == 0) {
-        decode_chunk_in_groups<kQlc>(job, T, ws, base, nsub, sub0, b0, bytes);
+        decode_chunk_in_groups<kQlc>(job, T, ws, base, 0, nsub, sub0, b0, bytes, 0, true);
         return;
     }
     if (staged) {
@@ -2233,6 +2322,144 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables 
             bad |= w != 0;
         }
     }
+    if (__any_sync(~0u, bad) && lane == 0)
+        set_status(job.status, ECC_ERR_CORRUPT);
+    __syncwarp();
+}
+
+// Decode piece `piece` of chunk c with one warp: the sub-blocks [piece * ps,
+// (piece + 1) * ps) of the chunk, ps = (C / S) >> pshift (32 * R of them in a
+// full piece).  Splitting a large chunk into pieces lets each warp stage
+// only a piece, so that as many warps fit an SM as for a small chunk.  The
+// piece starts at the sum of the chunk's sub_bits before it; its bytes,
+// widened to 16-byte boundaries of the chunk, are staged by one bulk copy
+// when they fit.  The piece that ends the chunk also checks the chunk's size
+// and zero padding.  next_c / next_piece (if valid) is prefetched into L2.
+template <int R, bool kQlc>
+__device__ __forceinline__ void decode_piece(const DecJob &job, const DecTables &T, WarpStage &ws, uint64_t c,
+                                             uint32_t piece, uint32_t pshift, uint64_t next_c, uint32_t next_piece,
+                                             uint64_t n_chunks)
+{
+    const uint16_t *dec = T.dec;
+    const LongTable &lt = *T.lt;
+    const int lane = threadIdx.x & 31;
+    const uint64_t base = c * job.C;
+    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - base);
+    const uint32_t s_shift = 31 - __clz(job.S); // S is a power of two
+    const uint32_t nsub = (L + job.S - 1) >> s_shift;
+    const uint32_t ps = (job.C >> s_shift) >> pshift;
+    const uint32_t g_begin = piece * ps;
+    if (g_begin >= nsub) // past the end of the tensor's last, partial chunk
+        return;
+    const uint32_t g_end = min(g_begin + ps, nsub);
+    const bool last = g_end == nsub;
+    const uint64_t sub0 = base >> s_shift;
+    uint64_t b0, b1;
+    if (!chunk_range_ok(job, c, b0, b1)) {
+        if (lane == 0)
+            set_status(job.status, ECC_ERR_CORRUPT);
+        return;
+    }
+    const uint32_t bytes = (uint32_t)(b1 - b0);
+    if (lane == 0 && next_c < n_chunks) { // the next piece's share of its chunk, roughly
+        uint64_t n0, n1;
+        if (chunk_range_ok(job, next_c, n0, n1)) {
+            const uint64_t nbytes = n1 - n0;
+            const uint64_t lo = ((nbytes * next_piece) >> pshift) & ~15ull;
+            const uint64_t e = (((nbytes * (next_piece + 1)) >> pshift) + 15) & ~15ull;
+            const uint64_t hi = e < nbytes ? e : nbytes;
+            if (hi > lo)
+                prefetch_l2(job.in + n0 + lo, (uint32_t)(hi - lo));
+        }
+    }
+    // the chunk's bits before the piece
+    uint32_t carry0 = 0;
+    for (uint32_t k = (uint32_t)lane; k < g_begin; k += 32)
+        carry0 += job.sub_bits[sub0 + k];
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        carry0 += __shfl_xor_sync(~0u, carry0, o);
+    // the piece's streams: lane l runs sub-blocks g_begin + r * 32 + l
+    uint32_t st[R], nb[R];
+    uint32_t carry = carry0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t k = g_begin + (uint32_t)(r * 32 + lane);
+        const uint32_t v = k < g_end ? job.sub_bits[sub0 + k] : 0u;
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(~0u, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        st[r] = carry + incl - v;
+        nb[r] = v;
+        carry += __shfl_sync(~0u, incl, 31);
+    }
+    if ((uint64_t)carry > (uint64_t)bytes * 8u || carry == carry0) { // more bits than the chunk holds, or none
+        if (lane == 0)
+            set_status(job.status, ECC_ERR_CORRUPT);
+        return;
+    }
+    // every stream of a full piece is a full sub-block
+    const bool full = g_end - g_begin == 32u * R && g_end * job.S <= L;
+    const uint32_t s0 = (carry0 >> 3) & ~15u;
+    const uint32_t s1 = min(pad16((carry + 7) >> 3), bytes);
+    const bool staged = ws.buf != nullptr && s1 - s0 + kStageGuard <= ws.bytes;
+    if (!staged && ws.buf != nullptr && full && ((g_end - g_begin) & 31) == 0) {
+        decode_chunk_in_groups<kQlc>(job, T, ws, base, g_begin, g_end, sub0, b0, bytes, carry0, last);
+        return;
+    }
+    const uint32_t *words;
+    uint32_t wlast, off = 0; // off: the stage's first bit in the chunk
+    if (staged) {
+        __syncwarp();
+        if (lane == 0) {
+            fence_proxy_async();
+            mbar_expect_tx(ws.bar, s1 - s0);
+            bulk_g2s(ws.buf, job.in + b0 + s0, s1 - s0, ws.bar);
+        }
+        bool ok = __all_sync(~0u, mbar_wait(ws.bar, ws.phase, kWaitLimitNs));
+        if (!ok) // never expected: the copy reads valid memory; wait once more
+            ok = __all_sync(~0u, mbar_wait(ws.bar, ws.phase, kWaitLimitNs));
+        ws.phase ^= 1;
+        if (!ok) {
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            ws.buf = nullptr; // the copy may still land: stop using this buffer
+            return;
+        }
+        if (lane < kStageGuard / 4)
+            ws.buf[(s1 - s0) / 4 + lane] = 0; // guard: reads past the end see 0
+        __syncwarp();
+        words = ws.buf;
+        wlast = (s1 - s0) / 4 + kStageGuard / 4 - 1;
+        off = s0 * 8u;
+    } else {
+        words = reinterpret_cast<const uint32_t *>(job.in + b0);
+        wlast = bytes / 4 - 1;
+    }
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        st[r] -= off;
+    if (staged && full) {
+        decode_group_fast<R, kQlc>(job, T, words, (s1 - s0) / 4 + 4, base, g_begin, st, nb, bad);
+    } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t k = g_begin + (uint32_t)(r * 32 + lane);
+            if (k >= g_end)
+                continue;
+            const uint32_t cnt = min(job.S, L - k * job.S);
+            uint8_t *dst = job.out + base + (uint64_t)k * job.S;
+            bad |= staged ? decode_stream_generic<true>(words, wlast, st[r], cnt, nb[r], dst, dec, lt)
+                          : decode_stream_generic<false>(words, wlast, st[r], cnt, nb[r], dst, dec, lt);
+        }
+    }
+    if (last)
+        bad |= chunk_tail_bad(job, b0, bytes, carry, bad);
     if (__any_sync(~0u, bad) && lane == 0)
         set_status(job.status, ECC_ERR_CORRUPT);
     __syncwarp();

@@ -131,6 +131,7 @@ struct EncParams {
     uint32_t stage_bytes;
     uint32_t nbuf; // shared input buffers of C bytes: 2 = next chunk prefetched
     uint64_t timeout_ns;
+    uint32_t group; // warp-specialised kernel: chunks coded as one unit
 };
 
 // zero the look-back flags, the ticket and the outputs the kernel accumulates
@@ -229,10 +230,12 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_kernel(EncParams p)
 
 // Warp-specialised encoder over one tensor: see encode_ws_body.  At most 96
 // registers a thread, so that two 288-thread CTAs fit one SM.
+template <bool kGrouped>
 __global__ void __maxnreg__(96) encode_ws_kernel(EncParams p)
 {
     const EncBatch none{};
-    encode_ws_body<false>(p.job, p.n_chunks, p.ticket, none, p.stage_bytes, p.job.C, p.timeout_ns);
+    encode_ws_body<false, kGrouped>(p.job, p.n_chunks, p.ticket, none, p.stage_bytes, p.job.C * p.group,
+                                    p.timeout_ns, p.group);
 }
 
 // ---------------------------------------------------------------- decode
@@ -240,9 +243,11 @@ struct DecParams {
     DecJob job;
     uint64_t n_chunks;
     uint32_t stage_bytes;
+    uint32_t pshift; // log2(pieces per chunk): warps take chunks (0) or pieces of chunks
 };
 
-template <int R>
+// kPieces: the warps take pieces of chunks (p.pshift > 0), else chunks.
+template <int R, bool kPieces>
 __global__ void decode_kernel(DecParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -288,21 +293,41 @@ __global__ void decode_kernel(DecParams p)
         return blockIdx.x + (uint64_t)__shfl_sync(~0u, k, 0) * gridDim.x;
     };
     uint64_t c = claim();
+    const uint32_t ps = p.pshift, pm = (1u << ps) - 1u;
+    const uint64_t n_items = p.n_chunks << ps;
     if (qlc) {
         const DecTables T = qlc_tables(cb->dec, &lt, qs, reinterpret_cast<const uint32_t *>(smem));
-        while (c < p.n_chunks) {
-            const uint64_t nc = claim();
-            decode_chunk<R, true>(p.job, T, ws, c, nc, p.n_chunks);
-            c = nc;
+        if constexpr (kPieces) {
+            while (c < n_items) {
+                const uint64_t nc = claim();
+                decode_piece<R, true>(p.job, T, ws, c >> ps, (uint32_t)c & pm, ps, nc >> ps, (uint32_t)nc & pm,
+                                      p.n_chunks);
+                c = nc;
+            }
+        } else {
+            while (c < p.n_chunks) {
+                const uint64_t nc = claim();
+                decode_chunk<R, true>(p.job, T, ws, c, nc, p.n_chunks);
+                c = nc;
+            }
         }
     } else {
         DecTables T{};
         T.dec = dec;
         T.lt = &lt;
-        while (c < p.n_chunks) {
-            const uint64_t nc = claim();
-            decode_chunk<R, false>(p.job, T, ws, c, nc, p.n_chunks);
-            c = nc;
+        if constexpr (kPieces) {
+            while (c < n_items) {
+                const uint64_t nc = claim();
+                decode_piece<R, false>(p.job, T, ws, c >> ps, (uint32_t)c & pm, ps, nc >> ps, (uint32_t)nc & pm,
+                                       p.n_chunks);
+                c = nc;
+            }
+        } else {
+            while (c < p.n_chunks) {
+                const uint64_t nc = claim();
+                decode_chunk<R, false>(p.job, T, ws, c, nc, p.n_chunks);
+                c = nc;
+            }
         }
     }
 }
@@ -464,23 +489,29 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     p.ticket = ticket;
     p.stage_bytes = stage_bytes_for(C);
     p.timeout_ns = kWaitLimitNs;
+    p.group = 1;
     const int sms = sm_count();
     if (sms <= 0)
         return ECC_ERR_CUDA;
     // warp-specialised kernel (two input buffers, two stage slots of warp
-    // regions) when it fits, else the single-slot kernel
+    // regions) when it fits, else the single-slot kernel; chunks smaller
+    // than kGroupSyms symbols are coded in groups of consecutive chunks
     {
-        const uint32_t slot = enc_ws_slot_bytes(C, S);
-        const size_t smem = enc_ws_smem_bytes(C, slot);
-        const int occ = smem <= kMaxDynSmem - kStaticSmemReserve
-                            ? occupancy((const void *)encode_ws_kernel, kEncThreadsWS, smem)
-                            : 0;
+        const uint32_t G = enc_group_chunks(C, S);
+        const uint32_t slot = G > 1 ? enc_ws_group_slot_bytes(C, S) : enc_ws_slot_bytes(C, S);
+        const size_t smem = enc_ws_smem_bytes(C * G, slot);
+        const void *kfn = G > 1 ? (const void *)encode_ws_kernel<true> : (const void *)encode_ws_kernel<false>;
+        const int occ = smem <= kMaxDynSmem - kStaticSmemReserve ? occupancy(kfn, kEncThreadsWS, smem) : 0;
         if (occ > 0) {
             EncParams q = p;
             q.nbuf = 2;
             q.stage_bytes = slot;
-            const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
-            encode_ws_kernel<<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
+            q.group = G;
+            const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, (n_chunks + G - 1) / G);
+            if (G > 1)
+                encode_ws_kernel<true><<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
+            else
+                encode_ws_kernel<false><<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
             return launch_status(cudaGetLastError());
         }
     }
@@ -510,12 +541,21 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
     DecParams p;
     p.job = DecJob{in, in_bytes, chunk_off, sub_bits, n, C, S, cb, out, status};
     p.n_chunks = ecc_num_chunks(n, C);
-    p.stage_bytes = dec_stage_bytes(C, S);
-    // streams per lane: C/S sub-blocks per chunk over 32 lanes, at most 4
-    const uint32_t per_lane = std::min<uint32_t>(4, std::max<uint32_t>(1, C / S / 32));
-    const void *kfn = per_lane == 4 ? (const void *)decode_kernel<4>
-                      : per_lane == 2 ? (const void *)decode_kernel<2>
-                                      : (const void *)decode_kernel<1>;
+    // streams per lane: C/S sub-blocks per chunk over 32 lanes, at most 4,
+    // and a warp's 32 x per_lane sub-blocks at most kDecPieceSyms symbols; a
+    // chunk of more sub-blocks is decoded in pieces of that many, one warp
+    // each, so that the stages stay as small as for a chunk of that size
+    uint32_t per_lane = std::min<uint32_t>(4, std::max<uint32_t>(1, C / S / 32));
+    while (per_lane > 1 && 32u * per_lane * S > kDecPieceSyms)
+        per_lane >>= 1;
+    p.pshift = 0;
+    while ((C / S >> p.pshift) > 32u * per_lane)
+        ++p.pshift;
+    p.stage_bytes = dec_stage_bytes(C >> p.pshift, S);
+    const bool pieces = p.pshift > 0;
+    const void *kfn = per_lane == 4   ? (pieces ? (const void *)decode_kernel<4, true> : (const void *)decode_kernel<4, false>)
+                      : per_lane == 2 ? (pieces ? (const void *)decode_kernel<2, true> : (const void *)decode_kernel<2, false>)
+                                      : (pieces ? (const void *)decode_kernel<1, true> : (const void *)decode_kernel<1, false>);
     // as many warps as shared memory holds stages for, and registers allow
     int warps = decode_warps(p.stage_bytes);
     auto smem_for = [&](int w) { return std::max<size_t>(kDecMinSmem, kDecHeadBytes + (size_t)w * p.stage_bytes); };
@@ -526,14 +566,20 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
     const int sms = sm_count();
     if (occ <= 0 || sms <= 0)
         return ECC_ERR_CUDA;
-    const uint64_t need = (p.n_chunks + warps - 1) / warps;
+    const uint64_t need = ((p.n_chunks << p.pshift) + warps - 1) / warps;
     const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, need);
-    if (per_lane == 4)
-        decode_kernel<4><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    if (per_lane == 4 && pieces)
+        decode_kernel<4, true><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    else if (per_lane == 4)
+        decode_kernel<4, false><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    else if (per_lane == 2 && pieces)
+        decode_kernel<2, true><<<(unsigned)grid, warps * 32, smem, st>>>(p);
     else if (per_lane == 2)
-        decode_kernel<2><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+        decode_kernel<2, false><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+    else if (pieces)
+        decode_kernel<1, true><<<(unsigned)grid, warps * 32, smem, st>>>(p);
     else
-        decode_kernel<1><<<(unsigned)grid, warps * 32, smem, st>>>(p);
+        decode_kernel<1, false><<<(unsigned)grid, warps * 32, smem, st>>>(p);
     return launch_status(cudaGetLastError());
 }
 

@@ -91,7 +91,7 @@ def round_trip(e, x, cbb, ocb, C, S):
 
 
 @pytest.mark.parametrize("C,S", [(1024, 64), (4096, 64), (4096, 128), (16384, 256), (16384, 1024),
-                                 (65536, 1024)])
+                                 (65536, 1024), (65536, 256), (32768, 64)])
 def test_checked_edges(eck, C, S):
     for name, cbb, ocb in books(eck):
         for k, n in enumerate((1, 17, C - 1, C, C + 1, 3 * C + 5)):

@@ -168,6 +168,76 @@ def test_chunk_and_subblock_shapes(C, S):
         check_against_oracle(x, cbb, ocb, C, S)
 
 
+@pytest.mark.parametrize("C,S", [(65536, 256), (65536, 128), (65536, 512), (65536, 1024), (32768, 64),
+                                 (16384, 64)])
+def test_decode_in_pieces(C, S):
+    """A chunk of more sub-blocks than one warp stages (32 x streams per
+    lane, at most 16384 symbols) is decoded in pieces, one warp each.  Last
+    chunks end inside the first piece, on a piece boundary and inside a later
+    piece (with a partial sub-block); uniform bytes under a Huffman code fitted
+    to a Gaussian give pieces too long for the stage (decoded 32 sub-blocks at
+    a time, or from global memory)."""
+    x = np_gauss(3 * C, (15, C), 1.0)[0]
+    count = oracle.histogram(x)
+    books = [(ecc.qlc_build_tables(count), oracle.qlc_codebook(count)),
+             (ecc.huff_build_canonical(count + np.uint64(1)), oracle.huffman_codebook(count + np.uint64(1)))]
+    g = np.random.default_rng(C + S)
+    for n in (C - 1, 2 * C + C // 2, 2 * C + C // 4 + 5, 2 * C + 3 * C // 4 + S // 2 + 1):
+        y = x[:n].copy()
+        for cbb, ocb in books:
+            check_against_oracle(y, cbb, ocb, C, S)
+    u = g.integers(0, 256, 2 * C + 3 * C // 4 + 7).astype(np.uint8)
+    check_against_oracle(u, *books[1], C, S)
+
+
+@pytest.mark.parametrize("C,S", [(1024, 64), (1024, 1024), (2048, 128), (4096, 64), (4096, 1024), (8192, 256)])
+def test_encode_in_groups(C, S):
+    """Chunks smaller than 16384 symbols are encoded in groups of
+    consecutive chunks (one look-back word and one output offset a group):
+    tensors ending in a group's first chunk, on a group boundary, one chunk
+    short of it and in a partial chunk of a partial group; a rare-byte mix so
+    that some segments take the one-by-one and exact paths."""
+    seg = max(min(C, 2048), S, 512)    # a group: 8 segments of this many symbols
+    G = 8 // (C // seg)                 # chunks a group
+    x = np_gauss(5 * 16384, (17, C), 1.0)[0]
+    g = np.random.default_rng(C + S)
+    m = g.random(x.size) < 0.02
+    x[m] = g.integers(0, 256, int(m.sum()))
+    count = oracle.histogram(x)
+    books = [(ecc.qlc_build_tables(count), oracle.qlc_codebook(count)),
+             (ecc.huff_build_canonical(count + np.uint64(1)), oracle.huffman_codebook(count + np.uint64(1)))]
+    for n in (C // 2 + 3, 2 * G * C, (3 * G - 1) * C, 3 * G * C + 2 * C + 77):
+        for cbb, ocb in books:
+            check_against_oracle(x[:n].copy(), cbb, ocb, C, S)
+
+
+def test_corrupt_pieces_are_flagged():
+    """Pieces of a 64 KiB chunk: a sub-block count raised in one piece, or
+    moved from one piece to the next, is corrupt (the streams no longer end
+    where their counts say)."""
+    x = np_gauss(3 * 65536, (16, 0), 1.0)[0]
+    count = oracle.histogram(x)
+    for cbb in (ecc.qlc_build_tables(count), ecc.huff_build_canonical(count + 1)):
+        dcb = ecc.to_device(cbb)
+        enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), dcb, 65536, 256)
+        torch.cuda.synchronize()
+        assert int(enc.status.item()) == ecc.OK
+        for j, d in ((70, 1), (255, -1), (300, 3)):
+            sb = enc.sub_bits.clone()
+            sb[j] += d
+            out, st = ecc.ecc_decode(ecc.Encoded(enc.payload, enc.chunk_off, sb, enc.total_bits, enc.status,
+                                                 enc.n, enc.C, enc.S), dcb)
+            torch.cuda.synchronize()
+            assert int(st.item()) == ecc.ERR_CORRUPT, (j, d)
+        sb = enc.sub_bits.clone()
+        sb[63] -= 2
+        sb[64] += 2
+        out, st = ecc.ecc_decode(ecc.Encoded(enc.payload, enc.chunk_off, sb, enc.total_bits, enc.status,
+                                             enc.n, enc.C, enc.S), dcb)
+        torch.cuda.synchronize()
+        assert int(st.item()) == ecc.ERR_CORRUPT
+
+
 # ------------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("n", [0, 1, 15, 16, 17, 63, 64, 65, 4095, 4096, 4097, 16383, 16385])
