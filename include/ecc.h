@@ -71,8 +71,10 @@ enum {
     ECC_ERR_CODEBOOK = 4, /* bad codebook, or a byte the codebook does not code */
     ECC_ERR_TIMEOUT = 5,  /* a bounded device wait ran out (the kernel returned) */
     ECC_ERR_CUDA = 6,     /* a CUDA runtime call failed */
-    ECC_ERR_CHECK = 7     /* index-checked builds only (-DECC_CHECKED): a kernel index was out of
-                             range; the access was skipped */
+    ECC_ERR_CHECK = 7     /* an internal check failed: in index-checked builds (-DECC_CHECKED) a
+                             kernel index was out of range and the access skipped; in any build,
+                             chunks of more than 16384 symbols coded to other sizes than their
+                             length pass counted (nothing is written for such a chunk) */
 };
 
 enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2, ECC_FAMILY_ESCAPE = 3 };
@@ -306,6 +308,10 @@ ecc_status huff_build_device(const uint64_t *count, uint64_t add, uint32_t max_l
  * chunk-offset look-back waited more than about a second).
  * Host errors: ECC_ERR_ARG (sizes, alignment, NULL, small workspace),
  * ECC_ERR_CUDA.  n = 0 writes chunk_off[0] = 0 and total_bits = 0.
+ * Launches: chunks of at most 16384 symbols are coded and placed in one
+ * kernel (decoupled look-back over chunks, or over groups of consecutive
+ * chunks of 16384 symbols); larger chunks take a length pass, a scan of the
+ * offsets and a coding kernel (ECC_ERR_CHECK if the two ever disagree).
  */
 ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S,
                       uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,

@@ -1198,13 +1198,19 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
 // take the first bits of the segments after it.  Region 0 also zeroes the
 // words up to the 16-byte boundary after the stream.  Each lane takes four
 // region words at a time (one 16-byte load).
+// A pass of a larger chunk (P0 > 0: the slot's segments are the chunk's bits
+// from bit P0 on): the word holding bit P0 was stored by the previous pass,
+// with zeros for this pass's bits, and region 0 or-s its first bits into it
+// (the caller orders the two); `pad`: the slot ends the chunk, so region 0
+// zeroes the padding.
 // Returns true (index-checked builds only) if the region or the chunk's
 // padded payload would be overrun; nothing is copied then.
 __device__ __forceinline__ bool copy_region_out(uint32_t slot, uint32_t region_words, const uint32_t *seg_bits,
-                                                uint32_t nseg, uint32_t w, uint32_t *dst)
+                                                uint32_t nseg, uint32_t w, uint32_t *dst, uint32_t P0 = 0,
+                                                bool pad = true)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t P = 0, total = 0;
+    uint32_t P = P0, total = P0;
     for (uint32_t u = 0; u < nseg; ++u) {
         P += u < w ? seg_bits[u] : 0u;
         total += seg_bits[u];
@@ -1215,6 +1221,8 @@ __device__ __forceinline__ bool copy_region_out(uint32_t slot, uint32_t region_w
     if (nw && (nw >= region_words || j0 + nw > (pad16((total + 7) >> 3) >> 2)))
         return true;
 #endif
+    if (w == 0 && (P0 & 31u) && T && lane == 0) // the first word, shared with the previous pass
+        atomicOr(dst + (P0 >> 5), bswap32(ld_shared_u32(slot) >> (P0 & 31u)));
     // nw = 0: the segment's bits all lie inside a word that starts in an
     // earlier segment, whose last word takes them
     if (nw) {
@@ -1249,7 +1257,7 @@ __device__ __forceinline__ bool copy_region_out(uint32_t slot, uint32_t region_w
             d[nlast] = bswap32(val);
         }
     }
-    if (w == 0) {
+    if (w == 0 && pad) {
         const uint32_t jend = (total + 31) >> 5, jpad = pad16((total + 7) >> 3) >> 2;
         if (jend + (uint32_t)lane < jpad)
             dst[jend + lane] = 0;
@@ -1575,6 +1583,241 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             }
             bar_arrive(kBarFull + b, kEncThreadsWS);
             // unit k - 1's offset has had a whole unit to resolve
+            if (k >= 1)
+                copy_out(k - 1);
+        }
+    }
+    // never exit with a bulk copy still writing into this CTA's shared memory
+    // (only after a timed-out wait can an issued copy be left unconsumed)
+    __syncthreads();
+    if (tid == 0)
+        for (uint32_t q = 0; q < 2; ++q)
+            if (sh.issued[q])
+                (void)mbar_wait(&sh.bar[q], (sh.issued[q] - 1u) & 1u, timeout_ns);
+}
+
+// ---------------------------------------------------------------- chunks of more than kGroupSyms symbols
+// Three launches: a length pass writes each chunk's payload bits into the
+// look-back words (flags[c], bit 63 set when a segment of the chunk needs
+// more than its stage region), a scan turns them into chunk_off and
+// total_bits, and then encode_pass_body codes each chunk in passes of
+// kGroupSyms symbols (kEncWarps segments of kPassSeg, one a compute warp)
+// into a stage slot and copies every pass out at its place in the chunk's
+// bitstream, which is known before the pass is coded: no pass waits for a
+// look-back, and a stage slot holds one pass instead of a whole chunk.  A
+// chunk's passes go to one CTA in order, so the word that two passes share
+// is stored by the earlier pass and or-ed into by the later one after a CTA
+// barrier.  A flagged chunk is coded by the output warp straight into the
+// output.
+constexpr uint32_t kPassSeg = kGroupSyms / kEncWarps;
+constexpr uint32_t kSlotDirect = 3; // a chunk the output warp codes straight into the output
+constexpr uint64_t kLenOverflow = 1ull << 63;
+
+// Bulk-copy the whole 16-byte groups of the L input bytes at src into buf
+// (thread 0); completion arrives on bar.  Trailing bytes (fewer than 16, the
+// tensor's end) are read from global memory by the thread that owns them.
+__device__ __forceinline__ void issue_input(const uint8_t *src, uint32_t L, uint8_t *buf, uint64_t *bar)
+{
+    const uint32_t whole = L & ~15u;
+    fence_proxy_async();
+    mbar_expect_tx(bar, whole);
+    if (whole)
+        bulk_g2s(buf, src, whole, bar);
+}
+
+// Passes of chunk c.
+__device__ __forceinline__ uint32_t chunk_passes(const EncJob &job, uint64_t c)
+{
+    const uint32_t L = (uint32_t)min((uint64_t)job.C, job.n - c * job.C);
+    return (L + kGroupSyms - 1) / kGroupSyms;
+}
+
+// The pass encoder (C > kGroupSyms): slots and barriers as in
+// encode_ws_body, a unit being one pass (EncSlot::c the chunk,
+// EncSlot::tensor the pass) or one flagged chunk (kSlotDirect).
+// chunk_rel[b][0] / [1] hold the slot's bit offset in its chunk and whether
+// it ends the chunk.
+__device__ __forceinline__ void encode_pass_body(const EncJob &job, uint64_t n_chunks, uint32_t *ticket,
+                                                 uint32_t slot_bytes, uint64_t timeout_ns)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    EncShared &sh = *reinterpret_cast<EncShared *>(smem);
+    uint8_t *inbuf = smem + enc_shared_bytes();
+    constexpr uint32_t cmax = kGroupSyms;
+    const uint32_t stage0 = smem_u32(inbuf + 2 * (size_t)cmax);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (job.cb->magic != ECC_CODEBOOK_MAGIC || job.cb->max_len > ECC_MAX_CODE_LEN) {
+        if (tid == 0 && blockIdx.x == 0)
+            set_status(job.status, ECC_ERR_CODEBOOK);
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(&sh.bar[0], 1);
+        mbar_init(&sh.bar[1], 1);
+        fence_mbar_init();
+        sh.issued[0] = sh.issued[1] = 0;
+        sh.nostage = 0;
+        sh.slot_flags[0] = sh.slot_flags[1] = 0;
+    }
+    load_encode_lut(sh, job.cb, kEncThreadsWS);
+    for (uint32_t i = tid; i < 2 * slot_bytes / 16; i += kEncThreadsWS)
+        st_shared_v4_zero(stage0 + i * 16u);
+    // one thread: the unit of iteration k into slot k % 4 -- the next pass
+    // of iteration k - 1's chunk, else a new chunk by ticket -- and, unless
+    // staging was given up, its input into buffer k % 2
+    auto claim = [&](uint32_t k) {
+        EncSlot &s = sh.slot[k % kEncSlots];
+        const EncSlot &prev = sh.slot[(k + kEncSlots - 1) % kEncSlots];
+        if (k > 0 && prev.state == kSlotChunk && prev.tensor + 1 < chunk_passes(job, prev.c)) {
+            s.c = prev.c;
+            s.tensor = prev.tensor + 1;
+            s.state = kSlotChunk;
+        } else {
+            claim_single(s, ticket, n_chunks);
+            s.tensor = 0;
+            if (s.state == kSlotChunk && (ld_relaxed(job.flags + s.c) & kLenOverflow))
+                s.state = kSlotDirect;
+        }
+        s.staged = 0;
+        if (s.state == kSlotChunk && !sh.nostage) {
+            const uint64_t base = s.c * job.C + (uint64_t)s.tensor * kGroupSyms;
+            issue_input(job.in + base, (uint32_t)min((uint64_t)kGroupSyms, job.n - base),
+                        inbuf + (size_t)(k & 1) * cmax, &sh.bar[k & 1]);
+            s.parity = sh.issued[k & 1] & 1u;
+            s.staged = 1;
+            ++sh.issued[k & 1];
+        }
+    };
+    if (tid == 0) {
+        claim(0);
+        if (sh.slot[0].state != kSlotEnd)
+            claim(1);
+        else
+            sh.slot[1].state = kSlotEnd;
+    }
+    __syncthreads(); // the last CTA-wide barrier before the warps split
+
+    const uint32_t seg = kPassSeg;
+    const uint32_t rwords = region_bytes(seg) / 4u;
+    if (warp == kEncWarps) { // ---------------- output warp
+        uint32_t pos = 0; // bits of the current chunk's earlier passes
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t b = k & 1;
+            bar_sync(kBarFull + b, kEncThreadsWS);
+            const EncSlot &s = sh.slot[k % kEncSlots];
+            if (s.state == kSlotEnd)
+                break;
+            if (lane == 0) { // unit k's input buffer is free: claim unit k + 2 into it
+                if (sh.slot[(k + 1) % kEncSlots].state != kSlotEnd)
+                    claim(k + 2);
+                else
+                    sh.slot[(k + 2) % kEncSlots].state = kSlotEnd;
+            }
+            const uint64_t c = s.c;
+            const uint64_t prefix = job.chunk_off[c], end = job.chunk_off[c + 1]; // written by the scan
+            const bool write = end <= job.out_cap;
+            bool copy = false;
+            if (s.state == kSlotDirect) {
+                if (write)
+                    encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + prefix),
+                                      (uint32_t)((end - prefix) / 4));
+            } else {
+                const uint32_t run = sh.slot_bits[b];
+                if (s.tensor == 0)
+                    pos = 0;
+                const uint32_t P0 = pos;
+                pos += run;
+                const bool last = s.tensor + 1 == chunk_passes(job, c);
+                // the coded bits must be the length pass's (the same lookups)
+                const bool mismatch = (sh.slot_flags[b] & 1u) ||
+                                      (last && (uint64_t)pos != (ld_relaxed(job.flags + c) & ~kLenOverflow));
+                if (mismatch && lane == 0)
+                    set_status(job.status, ECC_ERR_CHECK);
+                copy = write && !mismatch;
+                if (lane == 0) {
+                    sh.chunk_rel[b][0] = P0;
+                    sh.chunk_rel[b][1] = last ? 1u : 0u;
+                    sh.out_prefix[b] = prefix;
+                }
+            }
+            if (lane == 0)
+                sh.out_copy[b] = copy ? 1u : 0u;
+            bar_arrive(kBarReady + b, kEncThreadsWS);
+        }
+    } else { // ---------------- compute warps
+        // copy this warp's region of unit j (slot j % 2) out
+        auto copy_out = [&](uint32_t j) {
+            const uint32_t pb = j & 1;
+            bar_sync(kBarReady + pb, kEncThreadsWS);
+            if (sh.out_copy[pb]) {
+                const bool bad_index = copy_region_out(
+                    stage0 + pb * slot_bytes, rwords, sh.seg_bits[pb], kEncWarps, (uint32_t)warp,
+                    reinterpret_cast<uint32_t *>(job.out + sh.out_prefix[pb]), sh.chunk_rel[pb][0],
+                    sh.chunk_rel[pb][1] != 0);
+                if (bad_index && lane == 0)
+                    set_status(job.status, ECC_ERR_CHECK);
+            }
+        };
+        for (uint32_t k = 0;; ++k) {
+            const uint32_t b = k & 1;
+            const EncSlot &s = sh.slot[k % kEncSlots];
+            const uint32_t state = s.state;
+            if (state == kSlotEnd) {
+                bar_arrive(kBarFull + b, kEncThreadsWS);
+                if (k >= 1)
+                    copy_out(k - 1);
+                break;
+            }
+            const uint32_t region = stage0 + b * slot_bytes + (uint32_t)warp * rwords * 4u;
+            if (k >= 2) {
+                // unit k - 2 left this slot: every warp has copied its region
+                // out (after coding unit k - 1) and is past its lookups; the
+                // barrier also orders the copies of consecutive passes
+                bar_sync(kBarCompute, kEncThreads);
+                if (tid == 0)
+                    sh.slot_flags[b] = 0; // the output warp has read it
+                zero_region(region, rwords);
+            }
+            // a flagged chunk (the output warp codes it): this warp's eighth of
+            // the chunk, for its sub-block counts only (a region of no room
+            // packs nothing)
+            const bool direct = state == kSlotDirect;
+            const uint64_t base = s.c * job.C + (direct ? 0ull : (uint64_t)s.tensor * kGroupSyms);
+            const uint32_t span = direct ? job.C / kEncWarps : seg;
+            const uint32_t L = (uint32_t)min((uint64_t)(direct ? job.C : kGroupSyms), job.n - base);
+            const uint32_t s0 = (uint32_t)warp * span, s1 = min(s0 + span, L);
+            bool bad = false;
+            uint32_t bits = 0;
+            if (direct && s0 < s1) {
+                (void)encode_segment<false>(sh, job, nullptr, base, s0, s1, region, 0u, &sh.slot_flags[b], &bad);
+            } else if (s0 < s1) {
+                bool ok = false;
+                if (s.staged) {
+                    ok = __all_sync(~0u, mbar_wait(&sh.bar[b], s.parity, timeout_ns));
+                    if (!ok && lane == 0) { // never expected: the copy reads valid memory
+                        set_status(job.status, ECC_ERR_TIMEOUT);
+                        sh.nostage = 1;
+                    }
+                }
+                const uint8_t *src = inbuf + (size_t)b * cmax;
+                const uint32_t cap = region_cap_bytes(seg) * 8u;
+                bits = ok ? encode_segment<true>(sh, job, src, base, s0, s1, region, cap, &sh.slot_flags[b], &bad)
+                          : encode_segment<false>(sh, job, nullptr, base, s0, s1, region, cap, &sh.slot_flags[b],
+                                                  &bad);
+            }
+            if (bad && lane == 0)
+                set_status(job.status, ECC_ERR_CODEBOOK);
+            if (lane == 0)
+                sh.seg_bits[b][warp] = bits;
+            bar_sync(kBarCompute, kEncThreads); // the unit is coded
+            if (tid == 0) {
+                uint32_t run = 0;
+#pragma unroll
+                for (uint32_t w = 0; w < kEncWarps; ++w)
+                    run += sh.seg_bits[b][w];
+                sh.slot_bits[b] = run;
+            }
+            bar_arrive(kBarFull + b, kEncThreadsWS);
             if (k >= 1)
                 copy_out(k - 1);
         }

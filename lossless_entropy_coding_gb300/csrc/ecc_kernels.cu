@@ -238,6 +238,135 @@ __global__ void __maxnreg__(96) encode_ws_kernel(EncParams p)
                                     p.timeout_ns, p.group);
 }
 
+// ---------------------------------------------------------------- chunks of more than kGroupSyms symbols
+// Length pass: flags[c] = the payload bits of chunk c (the same table
+// lookups as the encoder's), bit 63 set when one of its segments of kPassSeg
+// symbols needs more than its stage region.  A CTA takes one chunk at a
+// time; warp w sums segments w, w + 8, ... reading the input straight from
+// global memory, a segment's four 16-byte loads a lane issued together.
+__global__ void __launch_bounds__(kEncThreads) enc_len_kernel(const uint8_t *in, uint64_t n, const ecc_codebook *cb,
+                                                              uint32_t C, uint64_t n_chunks, uint64_t *flags)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    EncShared &sh = *reinterpret_cast<EncShared *>(smem);
+    __shared__ uint32_t wbits[kEncWarps], wover[kEncWarps];
+    if (cb->magic != ECC_CODEBOOK_MAGIC || cb->max_len > ECC_MAX_CODE_LEN)
+        return; // the encoder reports it
+    load_encode_lut(sh, cb, kEncThreads);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint2 *lut = sh.lut + (lane & (kLutReplicas - 1));
+    const uint32_t cap = region_cap_bytes(kPassSeg) * 8u;
+    for (uint64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const uint64_t base = c * C;
+        const uint32_t L = (uint32_t)min((uint64_t)C, n - base);
+        uint32_t bits = 0, over = 0;
+        for (uint32_t s0 = (uint32_t)warp * kPassSeg; s0 < L; s0 += kEncWarps * kPassSeg) {
+            const uint32_t s1 = min(s0 + kPassSeg, L);
+            uint4 v[kPassSeg / kRoundSyms];
+            uint32_t cnt[kPassSeg / kRoundSyms];
+#pragma unroll
+            for (uint32_t r = 0; r < kPassSeg / kRoundSyms; ++r) {
+                const uint32_t my0 = s0 + r * kRoundSyms + (uint32_t)lane * kSymPerThread;
+                cnt[r] = my0 < s1 ? min((uint32_t)kSymPerThread, s1 - my0) : 0u;
+                v[r] = cnt[r] ? load_symbols<false>(nullptr, in + base + my0, cnt[r]) : make_uint4(0, 0, 0, 0);
+            }
+            uint32_t sb = 0;
+#pragma unroll
+            for (uint32_t r = 0; r < kPassSeg / kRoundSyms; ++r) {
+                uint32_t pv[8], pq[8];
+                bool slow;
+                uint32_t g = lookup_pairs(lut, v[r], cnt[r], pv, pq, &slow);
+                if (slow)
+                    g = cnt[r] ? slow_group_bits(lut, v[r], cnt[r], cb) & 0x3FFFFFFFu : 0u;
+                sb += g;
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1)
+                sb += __shfl_xor_sync(~0u, sb, o);
+            bits += sb;
+            over |= sb > cap ? 1u : 0u;
+        }
+        if (lane == 0) {
+            wbits[warp] = bits;
+            wover[warp] = over;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint64_t t = 0;
+            uint32_t o = 0;
+            for (int w = 0; w < kEncWarps; ++w) {
+                t += wbits[w];
+                o |= wover[w];
+            }
+            flags[c] = t | (o ? kLenOverflow : 0ull);
+        }
+        __syncthreads();
+    }
+}
+
+// Scan of the length pass (one CTA of 1024 threads, 1024 chunks a step):
+// chunk_off[c + 1] = the padded bytes of chunks 0 .. c, total_bits, and
+// ECC_ERR_CAPACITY when the payload exceeds out_cap.
+__global__ void __launch_bounds__(1024) enc_scan_kernel(const uint64_t *flags, uint64_t n_chunks, uint64_t *chunk_off,
+                                                        uint64_t *total_bits, uint64_t out_cap, uint32_t *status)
+{
+    __shared__ uint64_t wsum[32];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    uint64_t carry = 0, tbits = 0;
+    for (uint64_t t0 = 0; t0 < n_chunks; t0 += 1024) {
+        const uint64_t c = t0 + (uint64_t)t;
+        const uint64_t bits = c < n_chunks ? flags[c] & ~kLenOverflow : 0ull;
+        tbits += bits;
+        uint64_t incl = (bits + 127u) / 128u * 16u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(~0u, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        if (lane == 31)
+            wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            uint64_t v = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t y = __shfl_up_sync(~0u, v, o);
+                if (lane >= o)
+                    v += y;
+            }
+            wsum[lane] = v;
+        }
+        __syncthreads();
+        if (c < n_chunks)
+            chunk_off[c + 1] = carry + (warp ? wsum[warp - 1] : 0ull) + incl;
+        carry += wsum[31];
+        __syncthreads(); // wsum is rewritten by the next step
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        tbits += __shfl_xor_sync(~0u, tbits, o);
+    if (lane == 0)
+        wsum[warp] = tbits;
+    __syncthreads();
+    if (t == 0) {
+        uint64_t sum = 0;
+        for (int w = 0; w < 32; ++w)
+            sum += wsum[w];
+        *total_bits = sum;
+        chunk_off[0] = 0;
+        if (carry > out_cap)
+            set_status(status, ECC_ERR_CAPACITY);
+    }
+}
+
+// Pass encoder over one tensor (C > kGroupSyms): see encode_pass_body.
+__global__ void __maxnreg__(96) encode_pass_kernel(EncParams p)
+{
+    encode_pass_body(p.job, p.n_chunks, p.ticket, p.stage_bytes, p.timeout_ns);
+}
+
 // ---------------------------------------------------------------- decode
 struct DecParams {
     DecJob job;
@@ -493,6 +622,26 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     const int sms = sm_count();
     if (sms <= 0)
         return ECC_ERR_CUDA;
+    // chunks of more than kGroupSyms symbols: length pass, scan, pass encoder
+    if (C > kGroupSyms) {
+        const uint32_t slot = enc_ws_slot_bytes(kGroupSyms, S);
+        const size_t smem = enc_ws_smem_bytes(kGroupSyms, slot);
+        const int occ = smem <= kMaxDynSmem - kStaticSmemReserve
+                            ? occupancy((const void *)encode_pass_kernel, kEncThreadsWS, smem)
+                            : 0;
+        const int occ_len = occupancy((const void *)enc_len_kernel, kEncThreads, enc_shared_bytes());
+        if (occ > 0 && occ_len > 0) {
+            const uint64_t grid_len = std::min<uint64_t>((uint64_t)occ_len * sms, n_chunks);
+            enc_len_kernel<<<(unsigned)grid_len, kEncThreads, enc_shared_bytes(), st>>>(in, n, cb, C, n_chunks, flags);
+            enc_scan_kernel<<<1, 1024, 0, st>>>(flags, n_chunks, chunk_off, total_bits, out_cap, status);
+            EncParams q = p;
+            q.nbuf = 2;
+            q.stage_bytes = slot;
+            const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
+            encode_pass_kernel<<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
+            return launch_status(cudaGetLastError());
+        }
+    }
     // warp-specialised kernel (two input buffers, two stage slots of warp
     // regions) when it fits, else the single-slot kernel; chunks smaller
     // than kGroupSyms symbols are coded in groups of consecutive chunks

@@ -211,6 +211,30 @@ def test_encode_in_groups(C, S):
             check_against_oracle(x[:n].copy(), cbb, ocb, C, S)
 
 
+@pytest.mark.parametrize("C,S", [(32768, 64), (32768, 1024), (65536, 256), (65536, 1024)])
+def test_encode_in_passes(C, S):
+    """Chunks of more than 16384 symbols: a length pass and a scan place the
+    chunks, then each chunk is coded in passes of 16384 symbols whose shared
+    boundary words are merged.  Tensors ending inside a pass, on a pass
+    boundary and one symbol past it; a chunk of rare bytes whose segments
+    outgrow their stage regions (coded straight into the output) between
+    ordinary chunks."""
+    x = np_gauss(3 * C, (18, C), 1.0)[0]
+    count = oracle.histogram(x)
+    w = count + np.uint64(1)
+    books = [(ecc.qlc_build_tables(count), oracle.qlc_codebook(count)),
+             (ecc.huff_build_canonical(w), oracle.huffman_codebook(w))]
+    for n in (16384 + 5, 16384, 16385, C + 3 * 16384 - 1, 2 * C + 16384 + 1, 3 * C):
+        for cbb, ocb in books:
+            check_against_oracle(x[:n].copy(), cbb, ocb, C, S)
+    rare = np.argsort(w)[:8].astype(np.uint8)        # the longest Huffman codes
+    y = x.copy()
+    y[C:2 * C] = np.random.default_rng(C).choice(rare, C)
+    assert ecc.codebook_view(books[1][0])["len"][rare].astype(int).min() > 11
+    check_against_oracle(y, *books[1], C, S)
+    check_against_oracle(y[:C + 777].copy(), *books[1], C, S)
+
+
 def test_corrupt_pieces_are_flagged():
     """Pieces of a 64 KiB chunk: a sub-block count raised in one piece, or
     moved from one piece to the next, is corrupt (the streams no longer end
