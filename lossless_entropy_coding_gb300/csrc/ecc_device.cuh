@@ -2345,7 +2345,7 @@ static __device__ __noinline__ bool decode_stream_generic(const uint32_t *words,
 
 constexpr uint32_t kDecTableBytes = sizeof(((ecc_codebook *)0)->dec);
 constexpr uint32_t kLongTableBytes = (sizeof(LongTable) + 15u) & ~15u;
-constexpr uint32_t kDecBarSlots = 16; // one mbarrier per warp
+constexpr uint32_t kDecBarSlots = 24; // one mbarrier per warp
 constexpr uint32_t kQlcSharedBytes = (sizeof(QlcShared) + 15u) & ~15u;
 constexpr uint32_t kDecHeadBytes = kDecTableBytes + kLongTableBytes + kQlcSharedBytes + kDecBarSlots * 8;
 

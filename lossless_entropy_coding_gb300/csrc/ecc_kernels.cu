@@ -513,6 +513,8 @@ uint32_t enc_input_buffers(uint32_t C)
     return two <= kMaxDynSmem / 2 - kStaticSmemReserve ? 2u : 1u;
 }
 
+static_assert(kDecMaxWarps <= (int)kDecBarSlots, "one stage mbarrier per decoding warp");
+
 int decode_warps(uint32_t stage_bytes)
 {
     const size_t room = kMaxDynSmem - kStaticSmemReserve - kDecHeadBytes;

@@ -12,8 +12,8 @@ namespace ecc {
 
 constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit (static + dynamic)
 constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may add on top
-constexpr int kDecMaxWarps = 12;
-constexpr uint32_t kDecPieceSyms = 16384; // symbols one decoding warp stages at most (but 32 sub-blocks)
+constexpr int kDecMaxWarps = 18;
+constexpr uint32_t kDecPieceSyms = 8192; // symbols one decoding warp stages at most (but 32 sub-blocks)
 
 bool valid_sizes(uint32_t C, uint32_t S);
 // shared input buffers of the encoder (2 = the next chunk is prefetched)
