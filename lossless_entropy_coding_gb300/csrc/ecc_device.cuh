@@ -332,7 +332,12 @@ struct EncShared {
     uint32_t ticket;
     uint32_t flags; // bit 0: staging overflow, bit 1: skip the write
     EncSlot slot[kEncSlots];
-    uint32_t seg_bits[2][kEncWarps]; // warp-segmented encoder: payload bits of each warp's segment, per slot
+    // warp-segmented encoder: each warp's segment of unit k, its payload
+    // bits and the first word of its region, in entry k % 4 (two units are
+    // in flight, and a warp may code the next one while another still
+    // copies the one before)
+    uint32_t seg_bits[4][kEncWarps];
+    uint32_t seg_first[4][kEncWarps];
     uint64_t out_prefix[2];          // byte offset of the slot's chunk or group in the output (resolved look-back)
     uint32_t out_copy[2];            // 1: the compute warps copy the slot out to the output
     uint32_t chunk_rel[2][kMaxGroup + 1]; // byte offsets of a group's chunks in its output (last: the group's bytes)
@@ -1195,7 +1200,9 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
 // bit totals; the chunk's bitstream is their bits end to end.  Region w
 // supplies the output words whose first bit lies in its segment, shifted
 // from the region's word grid to the stream's; the last of them may also
-// take the first bits of the segments after it.  Region 0 also zeroes the
+// take the first bits of the segments after it (the first words of their
+// regions, or seg_first[u] when given, which leaves the other regions free
+// for reuse).  Region 0 also zeroes the
 // words up to the 16-byte boundary after the stream.  Each lane takes four
 // region words at a time (one 16-byte load).
 // A pass of a larger chunk (P0 > 0: the slot's segments are the chunk's bits
@@ -1207,7 +1214,7 @@ __device__ __forceinline__ uint32_t encode_segment(EncShared &sh, const EncJob &
 // padded payload would be overrun; nothing is copied then.
 __device__ __forceinline__ bool copy_region_out(uint32_t slot, uint32_t region_words, const uint32_t *seg_bits,
                                                 uint32_t nseg, uint32_t w, uint32_t *dst, uint32_t P0 = 0,
-                                                bool pad = true)
+                                                bool pad = true, const uint32_t *seg_first = nullptr)
 {
     const int lane = threadIdx.x & 31;
     uint32_t P = P0, total = P0;
@@ -1251,7 +1258,7 @@ __device__ __forceinline__ bool copy_region_out(uint32_t slot, uint32_t region_w
             uint32_t Pv = P + T; // first bits of the following segments inside this word
             for (uint32_t u = w + 1; u < nseg && Pv < 32 * jj + 32; ++u) {
                 if (seg_bits[u])
-                    val |= ld_shared_u32(slot + u * region_words * 4u) >> (Pv - 32 * jj);
+                    val |= (seg_first ? seg_first[u] : ld_shared_u32(slot + u * region_words * 4u)) >> (Pv - 32 * jj);
                 Pv += seg_bits[u];
             }
             d[nlast] = bswap32(val);
@@ -1415,6 +1422,9 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             const uint32_t gc = kGrouped ? (uint32_t)min((uint64_t)G, n_chunks - c0) : 1u; // chunks in the unit
             const uint32_t run = sh.slot_bits[b];
             const uint32_t fl = sh.slot_flags[b];
+            __syncwarp();
+            if (lane == 0)
+                sh.slot_flags[b] = 0; // read; unit k + 2 is coded after this warp's arrival below
             const uint64_t bytes = kGrouped ? (uint64_t)sh.chunk_rel[b][gc] : ((uint64_t)run + 127u) / 128u * 16u;
             bool to = false;
             const uint64_t prefix = u == 0 ? 0 : resolve_prefix(job.flags, u, bytes, timeout_ns, &to);
@@ -1478,8 +1488,9 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             if (sh.out_copy[pb] && q < gc * nseg) {
                 const uint32_t i = kGrouped ? q >> (31 - __clz(nseg)) : 0u, w = q - i * nseg; // nseg: a power of 2
                 const bool bad_index = copy_region_out(
-                    stage0 + pb * slot_bytes + i * nseg * rwords * 4u, rwords, sh.seg_bits[pb] + i * nseg, nseg, w,
-                    reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb] + (kGrouped ? sh.chunk_rel[pb][i] : 0u)));
+                    stage0 + pb * slot_bytes + i * nseg * rwords * 4u, rwords, sh.seg_bits[j & 3u] + i * nseg, nseg, w,
+                    reinterpret_cast<uint32_t *>(pjob.out + sh.out_prefix[pb] + (kGrouped ? sh.chunk_rel[pb][i] : 0u)),
+                    0u, true, sh.seg_first[j & 3u] + i * nseg);
                 if (bad_index && lane == 0)
                     set_status(pjob.status, ECC_ERR_CHECK);
                 if (kBatched && ps.t_done) {
@@ -1514,11 +1525,13 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             const uint32_t w = (uint32_t)warp - i * nseg;
             const uint32_t region = stage0 + b * slot_bytes + (uint32_t)warp * rwords * 4u;
             if (k >= 2) {
-                // unit k - 2 left this slot: every warp has copied its region
-                // out (after coding unit k - 1) and is past its lookups
-                bar_sync(kBarCompute, kEncThreads);
-                if (tid == 0)
-                    sh.slot_flags[b] = 0; // the output warp has read it
+                // unit k - 2 left this slot: this warp has copied its region
+                // out (after coding unit k - 1), and the others' copies read
+                // only their own regions and seg_first, so the region is free.
+                // The many-tensor kernel also keeps every warp past its
+                // lookups before a codebook change.
+                if (kBatched)
+                    bar_sync(kBarCompute, kEncThreads);
                 if ((uint32_t)warp < G * nseg)
                     zero_region(region, rwords);
             }
@@ -1552,8 +1565,10 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                           : encode_segment<false>(sh, job, nullptr, base, s0, s1, region, cap, &sh.slot_flags[b],
                                                   &bad);
             }
-            if (lane == 0)
-                sh.seg_bits[b][warp] = bits;
+            if (lane == 0) {
+                sh.seg_bits[k & 3u][warp] = bits;
+                sh.seg_first[k & 3u][warp] = bits ? ld_shared_u32(region) : 0u;
+            }
             if (bad && lane == 0)
                 set_status(job.status, ECC_ERR_CODEBOOK);
             bar_sync(kBarCompute, kEncThreads); // the unit is coded
@@ -1566,7 +1581,7 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                     for (uint32_t i = 0; i < gc; ++i) {
                         uint32_t r = 0;
                         for (uint32_t w = 0; w < nseg; ++w)
-                            r += sh.seg_bits[b][i * nseg + w];
+                            r += sh.seg_bits[k & 3u][i * nseg + w];
                         run += r;
                         rel += (r + 127u) / 128u * 16u;
                         sh.chunk_rel[b][i + 1] = rel;
@@ -1575,7 +1590,7 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 } else {
 #pragma unroll
                     for (uint32_t w = 0; w < kEncWarps; ++w)
-                        run += w < nseg ? sh.seg_bits[b][w] : 0u;
+                        run += w < nseg ? sh.seg_bits[k & 3u][w] : 0u;
                     bytes = ((uint64_t)run + 127u) / 128u * 16u;
                 }
                 st_relaxed(job.flags + u, (u == 0 ? kFlagPrefix : kFlagAggregate) | (bytes & kValueMask));
