@@ -241,3 +241,13 @@ def test_checked_build_compiles_and_exports():
     lib = ct.CDLL(path)
     for name in header_functions():
         assert hasattr(lib, name), name
+
+
+def test_default_subblock_rule():
+    """The sub-block size the binding picks when none is given: C/64 clamped
+    to [64, 256], a power of two dividing C (valid for every chunk size)."""
+    for k in range(7):
+        C = 1024 << k
+        S = ecc.default_subblock(C)
+        assert S == min(256, max(64, C // 64))
+        assert S & (S - 1) == 0 and C % S == 0 and 64 <= S <= min(C, 1024)
