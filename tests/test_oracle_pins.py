@@ -252,6 +252,67 @@ def test_entropy_and_kl_closed_forms(gauss_counts):
     assert oracle.kl_bits(two, one) == float("inf")
 
 
+# --------------------------------------------------------------- fixed codebook weights
+
+def _golden_shards():
+    rows = golden("fixed_codebook_weights.txt")
+    weights = {int(r[0]): int(r[1]) for r in rows if r[0] != "shard"}
+    shards = [np.array([int(v) for v in r[1:]], np.uint8) for r in rows if r[0] == "shard"]
+    return weights, shards
+
+
+def _shard_counts(shards):
+    return [np.bincount(s, minlength=256).astype(np.uint64) for s in shards]
+
+
+def test_fixed_codebook_weights_worked_example():
+    # hand-worked weights of three 8-byte shards (tests/golden): the average
+    # PMF times the pooled size, plus one pseudocount per byte value
+    weights, shards = _golden_shards()
+    expect = np.ones(256, np.uint64)
+    for b, w in weights.items():
+        expect[b] = w
+    got = oracle.fixed_codebook_weights(_shard_counts(shards))
+    assert got.dtype == np.uint64 and got.shape == (256,)
+    assert (got == expect).all()
+
+
+def test_fixed_codebook_weights_are_the_average_pmf():
+    # Equal-size shards: weight - 1 equals (mean of the shard PMFs) x (total
+    # bytes), exactly, for every byte value.  The mean is taken here in
+    # rational arithmetic straight from the definition (a PMF per shard, then
+    # their average), not by pooling counts.
+    g = np.random.default_rng(31)
+    shards = [g.integers(0, 256, 4096).astype(np.uint8) for _ in range(5)]
+    shards.append(np.full(4096, 7, np.uint8))  # a shard of one repeated byte
+    counts = _shard_counts(shards)
+    got = oracle.fixed_codebook_weights(counts)
+    total = sum(s.size for s in shards)
+    for b in range(256):
+        mean_pmf = sum(Fraction(int(c[b]), s.size) for c, s in zip(counts, shards)) / len(shards)
+        assert Fraction(int(got[b]) - 1) == mean_pmf * total
+    # no warm-up data at all: the pseudocount alone, a uniform codebook
+    assert (oracle.fixed_codebook_weights([]) == 1).all()
+
+
+def test_fixed_codebook_weights_catch_planted_slips():
+    # the plausible misreadings of the pseudocount and of the averaging give
+    # other weights than the worked example, so the two pins above fail on them
+    weights, shards = _golden_shards()
+    counts = _shard_counts(shards)
+    expect = np.ones(256, np.uint64)
+    for b, w in weights.items():
+        expect[b] = w
+    per_shard = sum(c + 1 for c in counts)                             # +1 per shard
+    only_absent = np.where(sum(counts) == 0, 1, sum(counts)).astype(np.uint64)  # +1 only to absent bytes
+    float_mean = np.floor(sum(c.astype(np.float64) / 8 for c in counts) / 3 * 256 + 1)  # PMFs averaged as floats
+    for slip in (per_shard, only_absent, float_mean):
+        assert not (np.asarray(slip, np.uint64) == expect).all()
+    # and the codebooks differ too: a slip changes the code lengths
+    good = oracle.huffman_codebook(expect)["len"]
+    assert not (oracle.huffman_codebook(np.asarray(per_shard, np.uint64))["len"] == good).all()
+
+
 # --------------------------------------------------------------- adapted QLC
 
 def test_search_space_reduction_matches_all_orderings(spike_counts):
