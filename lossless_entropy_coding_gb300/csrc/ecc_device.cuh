@@ -808,6 +808,8 @@ static __device__ __noinline__ void encode_chunk_warp(const EncJob &job, uint64_
         const uint4 v = cnt ? load_symbols<false>(nullptr, job.in + base + my0, cnt) : make_uint4(0, 0, 0, 0);
         bool bad;
         const uint32_t bits = exact_bits(v, cnt, job.cb, &bad);
+        if (bad)
+            set_status(job.status, ECC_ERR_CODEBOOK);
         uint32_t incl = bits;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {

@@ -644,9 +644,13 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
             return launch_status(cudaGetLastError());
         }
     }
-    // warp-specialised kernel (two input buffers, two stage slots of warp
-    // regions) when it fits, else the single-slot kernel; chunks smaller
-    // than kGroupSyms symbols are coded in groups of consecutive chunks
+    // chunks of at most 16384 symbols: the unit encoder (ecc_units.cu)
+    if (launch_unit_encoder(p.job, ticket, st) == ECC_OK)
+        return ECC_OK;
+    // a device where it cannot run: the warp-specialised kernel (two input
+    // buffers, two stage slots of warp regions) when it fits, else the
+    // single-slot kernel; chunks smaller than kGroupSyms symbols are coded in
+    // groups of consecutive chunks
     {
         const uint32_t G = enc_group_chunks(C, S);
         const uint32_t slot = G > 1 ? enc_ws_group_slot_bytes(C, S) : enc_ws_slot_bytes(C, S);

@@ -10,6 +10,8 @@
 
 namespace ecc {
 
+struct EncJob;
+
 constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit (static + dynamic)
 constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may add on top
 constexpr int kDecMaxWarps = 18;
@@ -26,5 +28,7 @@ int sm_count();
 // CTAs of `kernel` that fit on one SM (raises the kernel's dynamic shared
 // memory limit on first use on the current device).
 int occupancy(const void *kernel, int threads, size_t smem);
+// The unit encoder for chunks of at most 16384 symbols (ecc_units.cu).
+ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st);
 
 } // namespace ecc

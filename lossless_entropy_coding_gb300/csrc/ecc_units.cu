@@ -1,0 +1,907 @@
+// ecc_units.cu -- the unit encoder: chunks of at most 16384 symbols coded in
+// units of 16384 consecutive symbols (one chunk of 16384, or 2..16 whole
+// smaller chunks), the codewords of each chunk packed at their final places
+// in a shared stage and the unit's payload written with one bulk copy.
+//
+// The coding follows "Quad Length Codes for Lossless Compression of e4m3",
+// section 2 "Codifica" (a table gives each byte its code; codes are written
+// one after the other), and "Single-Stage Huffman Encoder for ML
+// Compression", Methodology step 4 (the precomputed codebook is applied with
+// no analysis of the tensor).  Chunk offsets, sub-block bit counts and the
+// padding are the library's container (include/ecc.h).
+//
+// A CTA is one pipeline: 16 compute warps, a loader warp and a storer warp;
+// two CTAs run on an SM.
+//  * compute thread t of a unit owns symbols [32 t, 32 t + 32).  Phase A sums
+//    its 32 code lengths from a 256-byte shared length table (one byte-sized
+//    load a symbol, the byte value being the address).
+//  * phase B: a warp scan of the counts and one barrier over the compute
+//    warps give every thread its bit position inside its chunk, every chunk
+//    its padded place in the unit, and the unit its padded size, which is
+//    published at once for the decoupled look-back over units; sub-block bit
+//    counts are written here.
+//  * phase C: each thread reads its 32 bytes again, looks them up in a
+//    16-way replicated shared table of {code << (32 - len), 2^(32 - len)},
+//    joins them into 16 code pairs (v1 + hi32(v2 * q1), hi32(q1 * q2)) and
+//    appends the pairs at their final bit positions in the stage (two wide
+//    multiplies an append, a predicated store of each completed word,
+//    byte-swapped to memory order).  A word two threads share
+//    is stored by the later one: the earlier passes its last partial word on
+//    with a shuffle (across warps, through the storer).
+//  * the loader warp claims units in ticket order as phase C frees an input
+//    buffer and bulk-copies their input; the storer warp resolves each unit's
+//    offset from its predecessors' published sizes while the compute warps
+//    pack it, writes chunk_off and total_bits, finishes the words shared
+//    across warps and the chunks' zero padding, and stores the stage to the
+//    output with one cp.async.bulk shared -> global copy.
+// A unit whose payload outgrows the stage (long codes only) is coded by the
+// storer straight into the output, one chunk at a time, from the codebook in
+// global memory.
+
+#include <algorithm>
+
+#include "ecc_device.cuh"
+#include "ecc_launch.h"
+
+namespace ecc {
+
+constexpr uint32_t kUSyms = 16384;                   // symbols of a unit
+constexpr uint32_t kUThr = 32;                       // symbols of a compute thread
+constexpr uint32_t kUWarps = kUSyms / (32 * kUThr);  // compute warps (16)
+constexpr uint32_t kUCompute = 32 * kUWarps;         // compute threads (512)
+constexpr uint32_t kUThreads = kUCompute + 64;       // + the loader and the storer
+constexpr uint64_t kUEnd = ~0ull;                    // slot holds no unit: the pipeline ends
+constexpr uint32_t kULutBytes = kLutRows * kLutReplicas * 8u;
+constexpr uint32_t kUBarCompute = 1;                 // named barrier of the compute warps
+static_assert(kUWarps == 16, "phase B scans the warp totals over the lanes of one half-warp");
+
+// Shared state of the pipeline.  Slot s = k % 2 of the CTA's k-th unit holds
+// its input buffer and its stage; the per-unit records the storer reads are
+// kept four deep (k % 4).
+struct UPipe {
+    uint64_t full[2];      // input buffer s filled: one arrival (loader) + the copy's bytes
+    uint64_t st_free[2];   // stage s read by its bulk store: one arrival (storer)
+    uint64_t agg[2];       // unit of slot s sized and published: one arrival (compute thread 0)
+    uint64_t done[2];      // unit of slot s packed (its input read, its stage written): one arrival per compute thread
+    uint64_t unit[2];      // loader -> compute: unit of slot s, or kUEnd
+    uint64_t sunit[4];     // compute -> storer: unit k, or kUEnd
+    uint32_t wtot[4][kUWarps];  // compute -> storer: bit totals of the compute warps of unit k
+    uint32_t wtail[2][kUWarps]; // lane 31's last partial word (memory order) when the next warp continues its chunk
+};
+static_assert(sizeof(UPipe) % 16 == 0, "buffers stay 16-byte aligned");
+
+struct UnitParams {
+    EncJob job;
+    uint64_t n_units;
+    uint32_t *ticket;
+    uint32_t stage_bytes; // payload bytes a stage holds (multiple of 16)
+    uint64_t timeout_ns;
+};
+
+__host__ __device__ constexpr size_t unit_smem_bytes(uint32_t stage_bytes)
+{
+    return kULutBytes + sizeof(UPipe) + 2u * kUSyms + 2u * (size_t)stage_bytes;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// the stage may be reused once every bulk store has read it
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// predicated shared store (one instruction, no branch)
+__device__ __forceinline__ void st_shared_pred(uint32_t addr, uint32_t v, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.b32 [%0], %1;\n\t}" ::"r"(addr), "r"(v),
+                 "r"((uint32_t)p)
+                 : "memory");
+}
+
+// predicated shared or-reduction
+__device__ __forceinline__ void red_or_pred(uint32_t addr, uint32_t v, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q red.shared.or.b32 [%0], %1;\n\t}" ::"r"(addr),
+                 "r"(v), "r"((uint32_t)p)
+                 : "memory");
+}
+
+// index of the highest set bit, 0xFFFFFFFF for 0
+__device__ __forceinline__ uint32_t bfind(uint32_t x)
+{
+    uint32_t r;
+    asm("bfind.u32 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// inclusive scan over the 32 lanes (shfl.up with its in-range predicate)
+__device__ __forceinline__ uint32_t warp_incl(uint32_t x)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y;
+        asm volatile("{\n\t.reg .pred p;\n\tshfl.sync.up.b32 %0|p, %1, %2, 0, -1;\n\t@!p mov.b32 %0, 0;\n\t}"
+                     : "=r"(y)
+                     : "r"(x), "r"(o));
+        x += y;
+    }
+    return x;
+}
+
+// inclusive scan over lanes 0..15 (lanes 16..31 get sums of their own half)
+__device__ __forceinline__ uint32_t half_incl(uint32_t x)
+{
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+        uint32_t y;
+        asm volatile("{\n\t.reg .pred p;\n\tshfl.sync.up.b32 %0|p, %1, %2, 0, -1;\n\t@!p mov.b32 %0, 0;\n\t}"
+                     : "=r"(y)
+                     : "r"(x), "r"(o));
+        x += y;
+    }
+    return x;
+}
+
+// barrier over the compute warps that also returns the OR of p over them
+__device__ __forceinline__ bool compute_bar_or(bool p)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred a, b;\n\tsetp.ne.u32 a, %1, 0;\n\tbar.red.or.pred b, %2, %3, a;\n\t"
+                 "selp.u32 %0, 1, 0, b;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)p), "n"(kUBarCompute), "n"(kUCompute)
+                 : "memory");
+    return r != 0;
+}
+
+// Exact bit count of the cnt bytes of (a, b) from the codebook in global
+// memory (a partial thread, or a code longer than 31 bits); *bad when a byte
+// has no code.
+static __device__ __noinline__ uint32_t unit_bits_slow(uint4 a, uint4 b, uint32_t cnt, const ecc_codebook *cb,
+                                                       bool *bad)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t bits = 0;
+    bool nocode = false;
+    for (uint32_t j = 0; j < cnt; ++j) {
+        const uint32_t L = min((uint32_t)cb->len[byte_of(w[j >> 2], j & 3)], (uint32_t)ECC_MAX_CODE_LEN);
+        nocode |= L == 0;
+        bits += L;
+    }
+    *bad = nocode;
+    return bits;
+}
+
+// Bit count of the 32 bytes of (a, b) coded one code at a time from the
+// lane's table replica (a thread with a pair longer than 32 bits); bit 31 set
+// when some byte has no code of at most 31 bits in the table (the exact path
+// from the codebook must code the thread).
+static __device__ __noinline__ uint32_t unit_bits_single(const uint2 *lt, uint4 a, uint4 b)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t f = 0, fo = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t ff = bfind(lt[byte_of(w[j >> 2], j & 3) * kLutReplicas].y); // 32 - length, or ~0
+        f += ff;
+        fo |= ff;
+    }
+    return (fo >> 31) ? 1u << 31 : 32u * 32u - f;
+}
+
+// End state of a thread's packing: its last partial word (register order,
+// first bit in bit 31; 0 when the thread ended on a word boundary) and the
+// shared-window address of the word that holds it (else of the next word).
+struct UEnd {
+    uint32_t tail, addr;
+    bool partial; // tail holds 1..31 bits (it may still be all zeros)
+};
+
+#ifdef ECC_CHECKED
+// index-checked builds: a stage store at or past lim is skipped and reported
+__device__ __forceinline__ void ust(uint32_t addr, uint32_t v, uint32_t lim, bool &bad)
+{
+    if (addr + 4u > lim) {
+        bad = true;
+        return;
+    }
+    st_shared_u32(addr, v);
+}
+#endif
+
+// Packer of codes given as (v, q): v = code << (32 - l) (first bit in bit
+// 31), q = 2^(32 - l), l <= 32.  State: the partial word cur (its first nb
+// bits used, 1 <= nb <= 32, first bit in bit 31) at shared address addr, K =
+// 2^(32 - nb).  Appending (v, q): v * K + (cur << 32) holds cur completed by
+// v's leading bits in its high word and v's remaining bits in its low word;
+// K * q = 2^(64 - nb - l) has a zero high word exactly when the word filled
+// up (it is then stored, byte-swapped to memory order, and the low word
+// becomes the partial one) and holds the next K in whichever word is
+// non-zero.  The store, the select and the address step are one predicated
+// block (no branch).
+struct UPacker {
+    uint32_t addr, cur, K, nb0;
+#ifdef ECC_CHECKED
+    uint32_t lim;
+    bool bad = false;
+#endif
+
+    // position at bit pos of the stage; the first code follows with
+    // start_pending: when pos is inside a word, its first nb0 bits belong to
+    // an earlier thread (zeros here) and the code is appended to them; when
+    // pos starts a word, the code is the partial word
+    __device__ __forceinline__ void begin(uint32_t stage, uint32_t pos)
+    {
+        nb0 = pos & 31u;
+        addr = stage + (pos >> 5) * 4u;
+        cur = 0;
+        K = 1u << ((32u - nb0) & 31u); // nb0 = 0: 1, as if a full word came first
+    }
+    __device__ __forceinline__ void start_pending(uint32_t v0, uint32_t q0)
+    {
+        const uint64_t x = (uint64_t)v0 * K;
+        const uint64_t y = (uint64_t)K * q0;
+        const uint32_t xhi = (uint32_t)(x >> 32), xlo = (uint32_t)x;
+        const uint32_t yhi = (uint32_t)(y >> 32), ylo = (uint32_t)y;
+        emit(xhi, xlo, nb0 ? yhi : 1u); // nb0 = 0: nothing to store, the word is v0
+        cur = nb0 ? cur : v0;
+        K = nb0 ? yhi + ylo : q0;
+    }
+    // begin + start_pending
+    __device__ __forceinline__ void start(uint32_t stage, uint32_t pos, uint32_t v0, uint32_t q0)
+    {
+        begin(stage, pos);
+        start_pending(v0, q0);
+    }
+    // the append's tail: the word w = cur completed by the code's leading
+    // bits is stored when gate == 0 (it filled up), and the code's remaining
+    // bits xlo become the partial word; else w stays the partial word
+    __device__ __forceinline__ void emit(uint32_t xhi, uint32_t xlo, uint32_t gate)
+    {
+        const uint32_t w = xhi | cur;
+#ifdef ECC_CHECKED
+        if (gate == 0)
+            ust(addr, bswap32(w), lim, bad);
+        cur = gate == 0 ? xlo : w;
+        addr += gate == 0 ? 4u : 0u;
+#else
+        asm volatile("{\n\t.reg .pred p;\n\t.reg .b32 s;\n\tsetp.eq.u32 p, %3, 0;\n\tprmt.b32 s, %2, 0, 0x0123;\n\t"
+                     "@p st.shared.b32 [%0], s;\n\tselp.b32 %1, %4, %2, p;\n\t@p add.u32 %0, %0, 4;\n\t}"
+                     : "+r"(addr), "=r"(cur)
+                     : "r"(w), "r"(gate), "r"(xlo)
+                     : "memory");
+#endif
+    }
+    __device__ __forceinline__ void put(uint32_t v, uint32_t q)
+    {
+        const uint64_t x = (uint64_t)v * K;
+        const uint64_t y = (uint64_t)K * q;
+        emit((uint32_t)(x >> 32), (uint32_t)x, (uint32_t)(y >> 32));
+        K = (uint32_t)(y >> 32) + (uint32_t)y;
+    }
+    // store a completed last word; the end state
+    __device__ __forceinline__ UEnd finish()
+    {
+        const bool complete = K == 1u;
+#ifdef ECC_CHECKED
+        if (complete)
+            ust(addr, bswap32(cur), lim, bad);
+#else
+        st_shared_pred(addr, bswap32(cur), complete);
+#endif
+        return complete ? UEnd{0u, addr + 4u, false} : UEnd{cur, addr, true};
+    }
+};
+
+// The 32 bytes of (a, b) packed one code at a time from the lane's table
+// replica (every code at most 31 bits).
+static __device__ __noinline__ UEnd unit_pack_single(const uint2 *lt, uint32_t stage, uint32_t pos, uint4 a, uint4 b,
+                                                     uint32_t lim, uint32_t *status)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    UPacker pk;
+#ifdef ECC_CHECKED
+    pk.lim = lim;
+#endif
+    const uint2 e0 = lt[byte_of(w[0], 0) * kLutReplicas];
+    pk.start(stage, pos, e0.x, e0.y);
+#pragma unroll
+    for (int j = 1; j < 32; ++j) {
+        const uint2 e = lt[byte_of(w[j >> 2], j & 3) * kLutReplicas];
+        pk.put(e.x, e.y);
+    }
+    const UEnd e = pk.finish();
+#ifdef ECC_CHECKED
+    if (pk.bad)
+        set_status(status, ECC_ERR_CHECK);
+#endif
+    return e;
+}
+
+// Slow-path packing of the cnt bytes of (a, b) at bit pos of the stage (codes
+// from the codebook in global memory, up to ECC_MAX_CODE_LEN bits): the same
+// word protocol.
+static __device__ __noinline__ UEnd unit_pack_slow(uint32_t stage, uint32_t pos, uint4 a, uint4 b, uint32_t cnt,
+                                                   const ecc_codebook *cb, uint32_t lim, uint32_t *status)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t addr = stage + (pos >> 5) * 4u;
+    uint32_t nb = pos & 31u; // bits of the current word already used (by an earlier thread: zeros here)
+    uint64_t acc = 0;        // the current word in bits 63..32, first bit in bit 63
+    bool bad = false;
+    auto put = [&](uint32_t code, uint32_t len) { // len <= 24
+        acc |= (uint64_t)code << (64u - nb - len);
+        nb += len;
+        if (nb >= 32u) {
+#ifdef ECC_CHECKED
+            ust(addr, bswap32((uint32_t)(acc >> 32)), lim, bad);
+#else
+            st_shared_u32(addr, bswap32((uint32_t)(acc >> 32)));
+#endif
+            addr += 4u;
+            acc <<= 32;
+            nb -= 32u;
+        }
+    };
+    bool nocode = false;
+    for (uint32_t j = 0; j < cnt; ++j) {
+        const uint32_t b8 = byte_of(w[j >> 2], j & 3);
+        const uint32_t L = min((uint32_t)cb->len[b8], (uint32_t)ECC_MAX_CODE_LEN);
+        if (!L) { // a byte the codebook does not code (its length counted 0 bits)
+            nocode = true;
+            continue;
+        }
+        const uint64_t code = cb->code[b8] & ((1ull << L) - 1);
+        if (L > 24) {
+            put((uint32_t)(code >> 24), L - 24);
+            put((uint32_t)(code & 0xFFFFFFu), 24);
+        } else {
+            put((uint32_t)code, L);
+        }
+    }
+    if (nocode)
+        set_status(status, ECC_ERR_CODEBOOK);
+    if (bad)
+        set_status(status, ECC_ERR_CHECK);
+    return UEnd{nb ? (uint32_t)(acc >> 32) : 0u, addr, nb != 0};
+}
+
+// Chunk layout of a unit from the compute warps' bit totals (x = total of
+// warp `lane`, lanes 0..15; wpc warps per chunk): for lane l, E = bits of
+// its chunk before warp l, base = byte offset of its chunk in the unit's
+// stage, cbits = its chunk's bits (valid on the chunk's last lane), Y =
+// inclusive sum of padded chunk sizes (lane 15: the unit's bytes).
+struct ULayout {
+    uint32_t E, base, cbits, Y;
+};
+template <bool kOne>
+__device__ __forceinline__ ULayout unit_layout(uint32_t x, uint32_t lane, uint32_t wpc)
+{
+    ULayout o;
+    const uint32_t X = half_incl(x);
+    if (kOne) {
+        o.E = X - x;
+        o.base = 0;
+        o.cbits = X;
+        o.Y = (X + 127u) / 128u * 16u;
+        return o;
+    }
+    const uint32_t sl = lane & ~(wpc - 1u);                    // first lane of this lane's chunk
+    const uint32_t xp = __shfl_sync(~0u, X, (sl + 31u) & 31u); // inclusive total before the chunk
+    const uint32_t before = sl ? xp : 0u;
+    o.E = X - x - before;
+    o.cbits = X - before;
+    const bool last = (lane & (wpc - 1u)) == wpc - 1u && lane < kUWarps;
+    o.Y = half_incl(last ? (o.cbits + 127u) / 128u * 16u : 0u);
+    const uint32_t yp = __shfl_sync(~0u, o.Y, (sl + 31u) & 31u);
+    o.base = sl ? yp : 0u;
+    return o;
+}
+
+// Exclusive prefix (bytes) of unit u from its predecessors' published sizes
+// (decoupled look-back over units, one warp, 8 flags a lane per step, so a
+// step spans 256 predecessors), then u's inclusive prefix is published.  The
+// look-back stops at the first inclusive prefix it meets, or at unit `known`
+// (< u, or -1 for none) whose inclusive prefix known_incl the caller already
+// holds (the CTA's previous unit, about one ticket round back): it never
+// depends on how far other CTAs have got with their own look-backs.  Waits
+// for a predecessor that has published nothing yet, at most timeout_ns in all
+// (then *timed_out; u's prefix is still published, so that successors
+// finish).
+__device__ __forceinline__ uint64_t unit_resolve(uint64_t *flags, uint64_t u, uint64_t aggregate, int64_t known,
+                                                 uint64_t known_incl, uint64_t timeout_ns, bool *timed_out)
+{
+    constexpr int kPer = 8;
+    const uint32_t lane = threadIdx.x & 31;
+    uint64_t prefix = 0;
+    int64_t j = (int64_t)u - 1; // highest unit this step reads
+    uint64_t t0 = 0;
+    bool expired = false;
+    while (j >= 0) {
+        uint64_t f[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int64_t idx = j - kPer * (int64_t)lane - i;
+            // before unit 0: a prefix of 0; the known unit: its inclusive prefix
+            f[i] = idx < 0 ? kFlagPrefix
+                           : idx == known ? (kFlagPrefix | known_incl) : (idx < known ? kFlagPrefix : ld_relaxed(flags + idx));
+        }
+        // this lane's flags, newest first, up to and including the first prefix
+        bool have = false, zero = false;
+        uint64_t sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (!have) {
+                const uint32_t state = (uint32_t)(f[i] >> 62);
+                zero |= state == 0;
+                sum += f[i] & kValueMask;
+                have = state == 2;
+            }
+        }
+        const unsigned pmask = __ballot_sync(~0u, have);
+        const int fp = pmask ? __ffs(pmask) - 1 : 32; // first lane holding a prefix
+        const bool need = (int)lane <= fp;
+        if (__any_sync(~0u, need && zero)) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0)
+                t0 = now;
+            if (__any_sync(~0u, now - t0 > timeout_ns)) {
+                expired = true;
+                break;
+            }
+            __nanosleep(32);
+            continue;
+        }
+        uint64_t v = need ? sum : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            v += __shfl_xor_sync(~0u, v, o);
+        prefix += v;
+        if (fp < 32)
+            break;
+        j -= 32 * kPer;
+    }
+    if (lane == 0)
+        st_relaxed(flags + u, kFlagPrefix | ((prefix + aggregate) & kValueMask));
+    *timed_out = expired;
+    return prefix;
+}
+
+// ---------------------------------------------------------------- compute warps
+// The 4 bytes of w as two code pairs (v, q) from the lane's table replica;
+// qm tracks the smallest pair multiplier (0: some pair longer than 32 bits,
+// or a byte without a table code).
+__device__ __forceinline__ void unit_join(const uint2 *lt, uint32_t w, uint32_t &v0, uint32_t &q0, uint32_t &v1,
+                                          uint32_t &q1, uint32_t &qm)
+{
+    const uint2 e0 = lt[byte_of(w, 0) * kLutReplicas];
+    const uint2 e1 = lt[byte_of(w, 1) * kLutReplicas];
+    const uint2 e2 = lt[byte_of(w, 2) * kLutReplicas];
+    const uint2 e3 = lt[byte_of(w, 3) * kLutReplicas];
+    v0 = mad_hi(e1.x, e0.y, e0.x);
+    q0 = __umulhi(e0.y, e1.y);
+    v1 = mad_hi(e3.x, e2.y, e2.x);
+    q1 = __umulhi(e2.y, e3.y);
+    qm = min(qm, min(q0, q1));
+}
+
+// sum of the 4 code lengths of the bytes of w (len: the shared length table)
+__device__ __forceinline__ uint32_t len4(const uint8_t *len, uint32_t w)
+{
+    return (uint32_t)len[byte_of(w, 0)] + len[byte_of(w, 1)] + len[byte_of(w, 2)] + len[byte_of(w, 3)];
+}
+
+// the 16 bytes of x as 8 pairs appended to pk, or nothing (false) if some
+// pair has no fast code
+__device__ __forceinline__ bool unit_half(const uint2 *lt, uint4 x, UPacker &pk, bool first)
+{
+    uint32_t v[8], q[8], qm = 0xFFFFFFFFu;
+    unit_join(lt, x.x, v[0], q[0], v[1], q[1], qm);
+    unit_join(lt, x.y, v[2], q[2], v[3], q[3], qm);
+    unit_join(lt, x.z, v[4], q[4], v[5], q[5], qm);
+    unit_join(lt, x.w, v[6], q[6], v[7], q[7], qm);
+    if (qm == 0)
+        return false;
+    if (first)
+        pk.start_pending(v[0], q[0]);
+    else
+        pk.put(v[0], q[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        pk.put(v[i], q[i]);
+    return true;
+}
+
+template <bool kOne>
+__device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, const uint2 *lut, const uint8_t *len,
+                                             uint32_t in0, uint32_t st0, uint32_t w, uint32_t lane)
+{
+    const EncJob &job = p.job;
+    const uint2 *lt = lut + (lane & (kLutReplicas - 1u));
+    const uint32_t s_shift = 31u - __clz(job.S);
+    const uint32_t tps = job.S / kUThr;                          // threads per sub-block: 2..32
+    const uint32_t wpc = kOne ? kUWarps : job.C / (32u * kUThr); // warps per chunk: 1..16
+    const uint32_t t = w * 32u + lane;
+    const uint32_t s0 = t * kUThr;
+    const uint64_t n_sub = (job.n + job.S - 1) >> s_shift;
+    for (uint64_t k = 0; k <= p.n_units; ++k) {
+        const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r = (uint32_t)k & 3u;
+        const bool ok = mbar_wait(&P.full[slot], par, p.timeout_ns);
+        if (!ok)
+            set_status(job.status, ECC_ERR_TIMEOUT);
+        const uint64_t u = ok ? (uint64_t)*(volatile uint64_t *)&P.unit[slot] : (uint64_t)kUEnd;
+        const bool end = u == kUEnd;
+        const uint64_t ubase = end ? 0 : u * kUSyms;
+        const uint32_t L = end ? 0u : (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
+        const uint32_t cnt = s0 < L ? min(kUThr, L - s0) : 0u;
+        const uint32_t src = in0 + slot * kUSyms + s0;
+
+        // ---- phase A: the thread's bit count from the length table
+        uint32_t B;
+        {
+            const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16u);
+            if (cnt == kUThr) {
+                B = len4(len, a.x) + len4(len, a.y) + len4(len, a.z) + len4(len, a.w) + len4(len, b.x) +
+                    len4(len, b.y) + len4(len, b.z) + len4(len, b.w);
+            } else {
+                const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                B = 0;
+#pragma unroll
+                for (uint32_t j = 0; j < kUThr; ++j)
+                    B += j < cnt ? (uint32_t)len[byte_of(wd[j >> 2], j & 3)] : 0u;
+            }
+        }
+
+        // ---- phase B: positions, sub-block counts, the unit's size
+        const uint32_t incl = warp_incl(B);
+        if (lane == 31)
+            P.wtot[r][w] = incl;
+        if (compute_bar_or(end)) { // the pipeline ends (the same decision in every compute warp)
+            if (t == 0) {
+                P.sunit[r] = kUEnd;
+                mbar_arrive(&P.agg[slot]);
+            }
+            break;
+        }
+        const uint32_t x = lane < kUWarps ? P.wtot[r][lane] : 0u;
+        const ULayout lay = unit_layout<kOne>(x, lane, wpc);
+        const uint32_t wE = __shfl_sync(~0u, lay.E, w);
+        const uint32_t cbase = kOne ? 0u : __shfl_sync(~0u, lay.base, w);
+        const uint32_t ubytes = __shfl_sync(~0u, lay.Y, kUWarps - 1u);
+        if (t == 0) { // publish the unit's size for the look-back; hand the unit to the storer
+            if (u != 0)
+                st_relaxed(job.flags + u, kFlagAggregate | ubytes);
+            P.sunit[r] = u;
+            mbar_arrive(&P.agg[slot]);
+        }
+        {
+            const uint32_t sb = __shfl_sync(~0u, incl, lane | (tps - 1u)) - (incl - B);
+            const uint64_t sidx = (ubase + s0) >> s_shift;
+            if (cnt && (lane & (tps - 1u)) == 0 && sidx < n_sub)
+                job.sub_bits[sidx] = (uint16_t)sb;
+        }
+        const bool over = ubytes > p.stage_bytes;
+        // the stage of this slot is free once the unit two back has been stored
+        if (!mbar_wait(&P.st_free[slot], par ^ 1u, p.timeout_ns))
+            set_status(job.status, ECC_ERR_TIMEOUT);
+
+        // ---- phase C: codes at their final places in the stage
+        const uint32_t pos = cbase * 8u + wE + incl - B;
+        const uint32_t st = st0 + slot * p.stage_bytes;
+        const uint32_t lim = st + p.stage_bytes;
+        UEnd e{0u, 0u, false};
+        bool bad_index = false;
+        if (!over && cnt) {
+            // the pairs of both halves: a half with a pair the table cannot
+            // code sends the whole thread to the paths below, which rewrite
+            // every word of its range
+            UPacker pk;
+#ifdef ECC_CHECKED
+            pk.lim = lim;
+#endif
+            pk.begin(st, pos);
+            bool fast = cnt == kUThr;
+            if (fast)
+                fast = unit_half(lt, ld_shared_v4(src), pk, true);
+            if (fast)
+                fast = unit_half(lt, ld_shared_v4(src + 16u), pk, false);
+            if (fast) {
+                e = pk.finish();
+#ifdef ECC_CHECKED
+                bad_index = pk.bad;
+#endif
+            } else {
+                const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16u);
+                const uint32_t bs = cnt == kUThr ? unit_bits_single(lt, a, b) : 1u << 31;
+                if (!(bs >> 31))
+                    e = unit_pack_single(lt, st, pos, a, b, lim, job.status);
+                else
+                    e = unit_pack_slow(st, pos, a, b, cnt, job.cb, lim, job.status);
+            }
+        }
+        // The thread's last partial word: the next lane or-s it into its first
+        // word; lane 31 leaves it to the storer; the chunk's last thread
+        // stores it (the storer writes the zero padding after it).
+        const uint32_t cend = kOne ? L : min(L, (w / wpc + 1u) * wpc * 32u * kUThr); // this chunk's end in the unit
+        const bool clast = cnt && s0 + cnt == cend;
+        const uint32_t prev = __shfl_up_sync(~0u, clast ? 0u : e.tail, 1);
+        if (!over) {
+#ifdef ECC_CHECKED
+            if (clast && e.partial)
+                ust(e.addr, bswap32(e.tail), lim, bad_index);
+#else
+            st_shared_pred(e.addr, bswap32(e.tail), clast && e.partial);
+#endif
+            if (lane == 31 && !clast)
+                P.wtail[slot][w] = bswap32(e.tail);
+            red_or_pred(st + (pos >> 5) * 4u, bswap32(prev), cnt && lane && (pos & 31u));
+        }
+#ifdef ECC_CHECKED
+        if (bad_index)
+            set_status(job.status, ECC_ERR_CHECK);
+#endif
+        fence_proxy_async(); // this thread's stage stores before the bulk store that reads them
+        mbar_arrive(&P.done[slot]); // also: this thread has read the input buffer
+    }
+}
+
+// ---------------------------------------------------------------- loader warp
+// Claims units in ticket order, one slot at a time as the compute warps finish
+// the unit in it (phase C reads the input again) and size the next one, and
+// bulk-copies each unit's input (lane 0 alone).
+__device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8_t *in0, uint32_t lane)
+{
+    if (lane != 0)
+        return;
+    const EncJob &job = p.job;
+    for (uint64_t k = 0; k <= p.n_units; ++k) {
+        const uint32_t slot = (uint32_t)k & 1u;
+        bool stop = false;
+        if (k >= 2 && !mbar_wait(&P.done[slot], (uint32_t)((k - 2) >> 1) & 1u, p.timeout_ns)) {
+            set_status(job.status, ECC_ERR_TIMEOUT);
+            stop = true;
+        }
+        // claim late, once the compute warps have sized the unit in the other
+        // slot: a unit is then sized soon after its ticket, and the
+        // look-backs of later units wait less for it
+        if (k >= 2 && !stop && !mbar_wait(&P.agg[slot ^ 1u], (uint32_t)((k - 1) >> 1) & 1u, p.timeout_ns)) {
+            set_status(job.status, ECC_ERR_TIMEOUT);
+            stop = true;
+        }
+        const uint32_t tk = stop ? 0xFFFFFFFFu : atomicAdd(p.ticket, 1u);
+        if (tk >= p.n_units) {
+            P.unit[slot] = kUEnd;
+            mbar_arrive(&P.full[slot]);
+            return;
+        }
+        const uint64_t u = tk;
+        P.unit[slot] = u;
+        uint8_t *buf = in0 + slot * kUSyms;
+        const uint64_t ubase = u * kUSyms;
+        const uint32_t L = (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
+        const uint32_t whole = L & ~15u;
+        for (uint32_t i = whole; i < L; ++i) // the tensor's last bytes (fewer than 16)
+            buf[i] = job.in[ubase + i];
+        fence_proxy_async();
+        mbar_expect_tx(&P.full[slot], whole);
+        if (whole)
+            bulk_g2s(buf, job.in + ubase, whole, &P.full[slot]);
+    }
+}
+
+// ---------------------------------------------------------------- storer warp
+// For each unit: its offset (look-back, while the compute warps pack it),
+// chunk_off, total_bits, then the stage to the output with one bulk copy.
+template <bool kOne>
+__device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint32_t st0, uint32_t lane)
+{
+    const EncJob &job = p.job;
+    const uint32_t G = kOne ? 1u : kUSyms / job.C;
+    const uint32_t wpc = kOne ? kUWarps : job.C / (32u * kUThr);
+    const uint64_t n_chunks = (job.n + job.C - 1) / job.C;
+    int64_t known = -1; // the CTA's previous unit, whose inclusive prefix is known_incl
+    uint64_t known_incl = 0;
+    for (uint64_t k = 0; k <= p.n_units; ++k) {
+        const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r = (uint32_t)k & 3u;
+        if (!mbar_wait(&P.agg[slot], par, p.timeout_ns)) {
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            break;
+        }
+        const uint64_t u = *(volatile uint64_t *)&P.sunit[r];
+        const uint32_t x = lane < kUWarps ? P.wtot[r][lane] : 0u;
+        __syncwarp();
+        // The previous unit's stage is free again once its bulk store has
+        // read it.  Released only now that unit k's records are read: the
+        // compute warps cannot hand over unit k + 2 (same slot, same records)
+        // before they have packed unit k + 1 into that stage.
+        if (k > 0 && lane == 0) {
+            bulk_wait_read();
+            mbar_arrive(&P.st_free[slot ^ 1u]);
+        }
+        if (u == kUEnd)
+            break;
+        const uint64_t ubase = u * kUSyms;
+        const uint32_t L = (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
+        const ULayout lay = unit_layout<kOne>(x, lane, wpc);
+        const uint32_t ubytes = __shfl_sync(~0u, lay.Y, kUWarps - 1u);
+        uint32_t ubits = x;
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            ubits += __shfl_xor_sync(~0u, ubits, o);
+        bool to = false;
+        const uint64_t prefix = unit_resolve(job.flags, u, ubytes, known, known_incl, p.timeout_ns, &to);
+        known = (int64_t)u;
+        known_incl = prefix + ubytes;
+        const uint64_t c0 = u * G;
+        const bool chunk_end = lane < kUWarps && (lane & (wpc - 1u)) == wpc - 1u; // a chunk's last lane
+        const bool chunk_real = chunk_end && c0 + lane / wpc < n_chunks;
+        if (chunk_real)
+            job.chunk_off[c0 + lane / wpc + 1] = prefix + lay.Y;
+        if (lane == 0) {
+            if (u == 0)
+                job.chunk_off[0] = 0;
+            atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)ubits);
+            if (to)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+        }
+        const bool fits = prefix + ubytes <= job.out_cap;
+        if (!fits && !to && lane == 0)
+            set_status(job.status, ECC_ERR_CAPACITY);
+        const bool write = fits && !to;
+        if (!mbar_wait(&P.done[slot], par, p.timeout_ns)) { // the compute warps have packed the unit
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            break;
+        }
+        if (ubytes > p.stage_bytes) {
+            // the unit outgrew the stage: code its chunks straight into the output
+            if (write)
+                for (uint32_t j = 0; j < G && c0 + j < n_chunks; ++j) {
+                    const uint32_t jb = __shfl_sync(~0u, lay.base, j * wpc);
+                    const uint32_t je = __shfl_sync(~0u, lay.Y, j * wpc + wpc - 1u);
+                    encode_chunk_warp(job, c0 + j, reinterpret_cast<uint32_t *>(job.out + prefix + jb), (je - jb) / 4u);
+                }
+        } else if (write) {
+            const uint32_t st = st0 + slot * p.stage_bytes;
+            // words shared across warps: warp `lane`'s first word takes the
+            // previous warp's last partial word
+            if (lane > 0 && lane < kUWarps && (lane & (wpc - 1u)) != 0 && lane * 32u * kUThr < L) {
+                const uint32_t bit = lay.base * 8u + lay.E;
+                if (bit & 31u)
+                    red_or_shared(st + (bit >> 5) * 4u, P.wtail[slot][lane - 1]);
+            }
+            // each chunk's zero padding: from the word after its last bit to its 16-byte end
+            if (chunk_real) {
+                const uint32_t cb0 = lay.Y - (lay.cbits + 127u) / 128u * 16u; // the chunk's base
+                for (uint32_t a2 = cb0 + (lay.cbits + 31u) / 32u * 4u; a2 < lay.Y; a2 += 4u)
+                    st_shared_u32(st + a2, 0u);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                bulk_s2g(job.out + prefix, st, ubytes);
+        }
+        __syncwarp();
+    }
+    if (lane == 0)
+        bulk_wait_all();
+}
+
+// Two CTAs an SM (56 registers a thread): one CTA's barrier waits and
+// pipeline stalls are covered by the other's warps.
+template <bool kOne>
+__global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
+{
+    extern __shared__ __align__(128) uint8_t unit_smem[];
+    __shared__ uint8_t len_table[kLutRows]; // code length of each byte (at most ECC_MAX_CODE_LEN; 0: no code)
+    uint2 *lut = reinterpret_cast<uint2 *>(unit_smem);
+    UPipe &P = *reinterpret_cast<UPipe *>(unit_smem + kULutBytes);
+    uint8_t *const base = unit_smem + kULutBytes + sizeof(UPipe);
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const ecc_codebook *cb = p.job.cb;
+    if (cb->magic != ECC_CODEBOOK_MAGIC || cb->max_len > ECC_MAX_CODE_LEN) {
+        if (threadIdx.x == 0 && blockIdx.x == 0)
+            set_status(p.job.status, ECC_ERR_CODEBOOK);
+        return;
+    }
+#ifdef ECC_CHECKED
+    {   // the layout must lie inside the dynamic shared memory the launch gave
+        uint32_t dyn;
+        asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        if (unit_smem_bytes(p.stage_bytes) > dyn) {
+            if (threadIdx.x == 0)
+                set_status(p.job.status, ECC_ERR_CHECK);
+            return;
+        }
+    }
+#endif
+    for (uint32_t i = threadIdx.x; i < kLutRows * kLutReplicas; i += blockDim.x) {
+        const uint32_t s = i / kLutReplicas;
+        lut[i] = make_uint2(cb->enc_code[s], cb->enc_mul[s]);
+    }
+    for (uint32_t i = threadIdx.x; i < kLutRows; i += blockDim.x)
+        len_table[i] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&P.full[s], 1);
+            mbar_init(&P.st_free[s], 1);
+            mbar_init(&P.agg[s], 1);
+            mbar_init(&P.done[s], kUCompute);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint32_t st0 = smem_u32(base + 2 * kUSyms);
+    if (warp < kUWarps)
+        unit_compute<kOne>(p, P, lut, len_table, smem_u32(base), st0, warp, lane);
+    else if (warp == kUWarps)
+        unit_loader(p, P, base, lane);
+    else
+        unit_storer<kOne>(p, P, st0, lane);
+}
+
+// ---------------------------------------------------------------- host side
+// Largest stage (multiple of 16, at most 32 KiB: 16 bits a symbol) with
+// which two CTAs fit one SM; 0 if none.
+uint32_t unit_stage_bytes()
+{
+    int dev = 0, per_sm = 0, reserved = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const int64_t per_cta = std::min<int64_t>(per_sm / 2 - reserved, (int64_t)kMaxDynSmem) - 512; // static shared bytes
+    const int64_t room = per_cta - (int64_t)unit_smem_bytes(0);
+    if (room < 2 * 16)
+        return 0;
+    return (uint32_t)std::min<int64_t>(room / 2 / 16 * 16, 2 * kUSyms);
+}
+
+// Launch the unit encoder for chunks of C <= kUSyms symbols (the prologue
+// has cleared the flags, the ticket and the outputs).  Returns ECC_ERR_CUDA
+// if it cannot run on this device.
+ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st)
+{
+    UnitParams p;
+    p.job = job;
+    p.n_units = (job.n + kUSyms - 1) / kUSyms;
+    p.ticket = ticket;
+    p.timeout_ns = kWaitLimitNs;
+    p.stage_bytes = unit_stage_bytes();
+    if (p.stage_bytes < 16u)
+        return ECC_ERR_CUDA;
+    const bool one = job.C == kUSyms;
+    const void *kfn = one ? (const void *)encode_unit_kernel<true> : (const void *)encode_unit_kernel<false>;
+    const size_t smem = unit_smem_bytes(p.stage_bytes);
+    const int occ = occupancy(kfn, kUThreads, smem);
+    const int sms = sm_count();
+    if (occ <= 0 || sms <= 0)
+        return ECC_ERR_CUDA;
+    // persistent: every CTA resident, so a unit's predecessors are always being coded
+    const uint64_t need = (p.n_units + 1) / 2;
+    const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)occ * sms, need));
+    if (one)
+        encode_unit_kernel<true><<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    else
+        encode_unit_kernel<false><<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    return launch_status(cudaGetLastError());
+}
+
+} // namespace ecc

@@ -364,13 +364,18 @@ def test_capacity_error_reports_needed_size():
     assert (u64(enc.chunk_off) == ref["chunk_off"]).all()
 
 
-def test_uncoded_byte_is_a_codebook_error():
+@pytest.mark.parametrize("n,where", [(20, 12), (40000, 20000), (1 << 20, (1 << 20) - 5)])
+def test_uncoded_byte_is_a_codebook_error(n, where):
+    """A byte the codebook does not code is reported, whether it falls in a
+    partial last group, in the middle of full groups, or near the end."""
     w = np.zeros(256, np.uint64)
     w[:10] = 1
-    x = np.arange(20, dtype=np.uint8)
-    enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), ecc.to_device(ecc.huff_build_canonical(w)), 1024, 64)
-    torch.cuda.synchronize()
-    assert int(enc.status.item()) == ecc.ERR_CODEBOOK
+    x = (np.arange(n) % 10).astype(np.uint8)
+    x[where] = 200
+    for C in (1024, 16384):
+        enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), ecc.to_device(ecc.huff_build_canonical(w)), C, 64)
+        torch.cuda.synchronize()
+        assert int(enc.status.item()) == ecc.ERR_CODEBOOK
 
 
 def test_bad_codebook_magic():
