@@ -686,12 +686,10 @@ def run_ours(args):
                                            "payload_bytes": int(enc.chunk_off[-1].item())}
                     del out, enc
             extra["chunk_sweep"] = sweep
-        import oracle
         extra["figures"] = {
             "shannon_compressibility_pct": 100.0 * (1.0 - ecc.entropy_bits(xcount_h) / 8.0),
             "kl_tensor_vs_warmup_bits": ecc.kl_bits(xcount_h, pooled_h + np.uint64(1)),
         }
-        del oracle
 
     clocks.stop()
     ck = clocks.summary(t_warm, t_end)

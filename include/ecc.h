@@ -400,9 +400,11 @@ ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate
  *   every GPU loading the library holds until the process exits; the call
  *   allocates and frees nothing.  Inputs with more than ECC_STATIC_MAX_CHUNKS
  *   chunks (n > 65536 * C) are rejected with ECC_ERR_ARG.
- *   The first call on each device resolves the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  Every call clears the scratch words it uses
+ *   Every call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress, with that device current), so a context reset
+ *   that reloads the library's module does not leave a stale address; the
+ *   first call on a device may load the module, so make it before any stream
+ *   capture.  Every call clears the scratch words it uses
  *   before use, but all calls share the one array: calls that can overlap on
  *   the GPU (other streams, other host threads) race and must be ordered by
  *   the caller.

@@ -1526,6 +1526,17 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
             const uint32_t i = kGrouped ? (uint32_t)warp >> (31 - __clz(nseg)) : 0u;
             const uint32_t w = (uint32_t)warp - i * nseg;
             const uint32_t region = stage0 + b * slot_bytes + (uint32_t)warp * rwords * 4u;
+#ifdef ECC_CHECKED
+            // index-checked builds: the warp's region must lie inside its
+            // stage slot (a slot sized for another layout would run past the
+            // shared memory the launch gave); otherwise nothing is staged and
+            // the chunk takes the output warp's direct path
+            const bool region_ok = (uint32_t)(warp + 1) * rwords * 4u <= slot_bytes;
+            if (!region_ok && lane == 0)
+                set_status(job.status, ECC_ERR_CHECK);
+#else
+            constexpr bool region_ok = true;
+#endif
             if (k >= 2) {
                 // unit k - 2 left this slot: this warp has copied its region
                 // out (after coding unit k - 1), and the others' copies read
@@ -1534,7 +1545,7 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 // lookups before a codebook change.
                 if (kBatched)
                     bar_sync(kBarCompute, kEncThreads);
-                if ((uint32_t)warp < G * nseg)
+                if ((uint32_t)warp < G * nseg && region_ok)
                     zero_region(region, rwords);
             }
             if (kBatched && state == kSlotChunk && job.cb != loaded) {
@@ -1562,14 +1573,14 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                     }
                 }
                 const uint8_t *src = inbuf + (size_t)b * cmax + (size_t)i * job.C;
-                const uint32_t cap = region_cap_bytes(seg) * 8u;
+                const uint32_t cap = region_ok ? region_cap_bytes(seg) * 8u : 0u;
                 bits = ok ? encode_segment<true>(sh, job, src, base, s0, s1, region, cap, &sh.slot_flags[b], &bad)
                           : encode_segment<false>(sh, job, nullptr, base, s0, s1, region, cap, &sh.slot_flags[b],
                                                   &bad);
             }
             if (lane == 0) {
                 sh.seg_bits[k & 3u][warp] = bits;
-                sh.seg_first[k & 3u][warp] = bits ? ld_shared_u32(region) : 0u;
+                sh.seg_first[k & 3u][warp] = bits && region_ok ? ld_shared_u32(region) : 0u;
             }
             if (bad && lane == 0)
                 set_status(job.status, ECC_ERR_CODEBOOK);

@@ -764,31 +764,19 @@ constexpr uint64_t kStaticScratchWords = 256 / sizeof(uint64_t) + kStaticMaxChun
 static __device__ __align__(256) uint64_t g_encode_scratch[kStaticScratchWords];
 
 namespace {
-std::mutex g_scratch_mu;
-std::map<int, void *> g_scratch_addr; // device ordinal -> device address of g_encode_scratch
-
-// Resolve the array's device address once per device, with that device
-// current (the first ecc_encode_static call on a device does this).
+// The array's device address on the current device, resolved on every call
+// with that device current: a host-side lookup, cheap once the module is
+// loaded, and never stale (a context reset reloads the module elsewhere).
+// The first call on a device may load the module; make it before any stream
+// capture.
 ecc_status static_scratch(void **out)
 {
-    int dev;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return ECC_ERR_CUDA;
-    }
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    auto it = g_scratch_addr.find(dev);
-    if (it != g_scratch_addr.end()) {
-        *out = it->second;
-        return ECC_OK;
-    }
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_encode_scratch);
     if (e != cudaSuccess || p == nullptr) {
         (void)cudaGetLastError();
         return ECC_ERR_CUDA;
     }
-    g_scratch_addr[dev] = p;
     *out = p;
     return ECC_OK;
 }

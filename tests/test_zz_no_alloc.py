@@ -13,7 +13,8 @@ import ctypes as ct
 import numpy as np
 import pytest
 
-from workloads import np_gauss, np_zero_spike
+import oracle
+from workloads import np_gauss, np_grad, np_zero_spike
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -68,6 +69,52 @@ def test_static_encode_matches_workspace_encode_twice():
     u1 = _same_as_workspace_encode(x1, ecc.qlc_build_tables(c1), 16384, 256)
     u2 = _same_as_workspace_encode(x2, ecc.huff_build_canonical(c2 + np.uint64(1)), 4096, 64)
     assert u1 > 0 and u2 > 0
+
+
+def test_static_encode_matches_oracle():
+    """Against the bit-serial oracle: the container (offsets, payload,
+    sub-block bits, total) of a gradient-like tensor with a Huffman code."""
+    xh = np_grad((1 << 20) + 77, (31, 3))
+    count = oracle.histogram(xh)
+    weights = oracle.fixed_codebook_weights([count])
+    cbb, ocb = ecc.huff_build_canonical(weights), oracle.huffman_codebook(weights)
+    x = torch.from_numpy(xh).cuda()
+    dcb = ecc.to_device(cbb)
+    C, S = 16384, 256
+    rc, out, off, sub, tot, st = _encode_static_c_abi(
+        x, dcb, C, S, ecc.max_encoded_bytes(x.numel(), C, int(ecc.codebook_view(cbb)["max_len"])))
+    torch.cuda.synchronize()
+    assert rc == ecc.OK and int(st.item()) == ecc.OK
+    ref = oracle.encode(xh, ocb, C, S)
+    o = off.cpu().numpy().view(np.uint64)
+    assert (o == ref["chunk_off"]).all()
+    assert (out[: int(o[-1])].cpu().numpy() == ref["payload"]).all()
+    assert (sub.cpu().numpy().view(np.uint16) == ref["sub_bits"]).all()
+    assert int(tot.item()) == ref["total_bits"]
+
+
+def test_static_encode_large_chunks_and_python_wrapper():
+    """Chunks of 65536 symbols take the length pass and the offset scan,
+    whose words also live in the static array; the Python wrapper
+    ecc.ecc_encode_static is called twice in a row and must equal
+    ecc_encode."""
+    xh = np_grad((1 << 22) + 1234, (31, 4))
+    x = torch.from_numpy(xh).cuda()
+    count = ecc.e4m3_histogram(x).cpu().numpy().view(np.uint64)
+    for cbb in (ecc.qlc_build_tables(count), ecc.huff_build_canonical(count + np.uint64(1))):
+        _same_as_workspace_encode(x, cbb, 65536, 256)
+        dcb = ecc.to_device(cbb)
+        max_len = int(ecc.codebook_view(cbb)["max_len"])
+        ref = ecc.ecc_encode(x, dcb, 65536, 1024, max_len=max_len)
+        for _ in range(2):
+            got = ecc.ecc_encode_static(x, dcb, 65536, 1024, max_len=max_len)
+            torch.cuda.synchronize()
+            assert int(got.status.item()) == ecc.OK and int(ref.status.item()) == ecc.OK
+            assert torch.equal(got.chunk_off, ref.chunk_off)
+            used = int(ref.chunk_off[-1].item())
+            assert torch.equal(got.payload[:used], ref.payload[:used])
+            assert torch.equal(got.sub_bits, ref.sub_bits)
+            assert int(got.total_bits.item()) == int(ref.total_bits.item())
 
 
 def test_static_encode_rejects_too_many_chunks():
