@@ -80,6 +80,12 @@ def _load():
             "eo_entropy_bits": (ct.c_double, [P]),
             "eo_kl_bits": (ct.c_double, [P, P]),
             "eo_code_bits": (U64, [P, P]),
+            "eo_bf16_exponent_counts": (I32, [P, U64, P]),
+            "eo_bf16_top7_from_counts": (I32, [P, P]),
+            "eo_bf16_exponent_probs": (I32, [ct.c_double, P]),
+            "eo_bf16_top7_from_sigma": (I32, [ct.c_double, P]),
+            "eo_bf16_escape_encode": (I32, [P, U64, P, U32, U32, P, U64, P, P, P]),
+            "eo_bf16_escape_decode": (I32, [P, U64, P, P, U64, U32, U32, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -319,3 +325,79 @@ def compressibility(bits: int, n: int) -> float:
 
 def shannon_compressibility(count) -> float:
     return 1.0 - entropy_bits(count) / 8.0
+
+
+# ---------------------------------------------------------------- BF16 escape code
+
+def _u16(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def bf16_exponent_counts(x) -> np.ndarray:
+    """count[e] = number of BF16 values (uint16 bit patterns) whose exponent
+    field (bits 14-7) is e."""
+    x = _u16(x)
+    out = np.zeros(256, np.uint64)
+    _check(_load().eo_bf16_exponent_counts(_p(x), x.size, _p(out)), "bf16_exponent_counts")
+    return out
+
+
+def bf16_top7_from_counts(count) -> np.ndarray:
+    """The 7 most frequent exponents, in rank order (ZipCCL, section 2.A;
+    count descending, ties to the smaller exponent)."""
+    count = _u64(count)
+    top = np.zeros(7, np.uint8)
+    _check(_load().eo_bf16_top7_from_counts(_p(count), _p(top)), "bf16_top7_from_counts")
+    return top
+
+
+def bf16_exponent_probs(sigma: float) -> np.ndarray:
+    """P(exponent field = e) for N(0, sigma^2) rounded to BF16 (ZipCCL,
+    section 2.A: the exponent table follows from sigma)."""
+    out = np.zeros(256, np.float64)
+    _check(_load().eo_bf16_exponent_probs(float(sigma), _p(out)), "bf16_exponent_probs")
+    return out
+
+
+def bf16_top7_from_sigma(sigma: float) -> np.ndarray:
+    """The 7 most probable exponents of N(0, sigma^2) in BF16, in rank order
+    (ties to the smaller exponent)."""
+    top = np.zeros(7, np.uint8)
+    _check(_load().eo_bf16_top7_from_sigma(float(sigma), _p(top)), "bf16_top7_from_sigma")
+    return top
+
+
+def bf16_escape_encode(x, top, C: int, S: int, cap: int | None = None) -> dict:
+    """Bit-serial encode of BF16 values (uint16 bit patterns) with the
+    exponent escape code (ZipCCL, section 2.B) into the chunked container."""
+    x = _u16(x)
+    top = _u8(top)
+    n = x.size
+    if cap is None:
+        full, tail = divmod(n, C)
+        cap = full * ((C * 19 + 7) // 8 + 15) // 16 * 16 + (((tail * 19 + 7) // 8 + 15) // 16 * 16 if tail else 0)
+    out = np.zeros(max(cap, 1), np.uint8)
+    n_chunks = -(-n // C)
+    chunk_off = np.zeros(n_chunks + 1, np.uint64)
+    sub_bits = np.zeros(max(-(-n // S), 1), np.uint16)
+    total = np.zeros(1, np.uint64)
+    _check(_load().eo_bf16_escape_encode(_p(x), n, _p(top), C, S, _p(out), cap, _p(chunk_off), _p(sub_bits),
+                                         _p(total)), "bf16_escape_encode")
+    used = int(chunk_off[-1])
+    return {"payload": out[:used].copy(), "chunk_off": chunk_off, "sub_bits": sub_bits[:-(-n // S)].copy(),
+            "total_bits": int(total[0]), "n": n, "C": C, "S": S}
+
+
+def bf16_escape_decode(enc: dict, top) -> np.ndarray:
+    """Bit-serial decode of a container produced by bf16_escape_encode()."""
+    payload = _u8(enc["payload"])
+    n, C, S = enc["n"], enc["C"], enc["S"]
+    chunk_off = _u64(enc["chunk_off"])
+    sub_bits = np.ascontiguousarray(enc["sub_bits"], dtype=np.uint16)
+    if sub_bits.size == 0:
+        sub_bits = np.zeros(1, np.uint16)
+    out = np.zeros(max(n, 1), np.uint16)
+    buf = payload if payload.size else np.zeros(1, np.uint8)
+    _check(_load().eo_bf16_escape_decode(_p(buf), payload.size, _p(chunk_off), _p(sub_bits), n, C, S,
+                                         _p(_u8(top)), _p(out)), "bf16_escape_decode")
+    return out[:n]

@@ -866,3 +866,222 @@ uint64_t eo_code_bits(const uint64_t *count, const uint8_t *len)
     }
     return bits;
 }
+
+/* ------------------------------------------------------------------ */
+/* Escape code on BF16 exponents ([ZIP] section 2.A and 2.B).  A BF16   */
+/* value is sign (bit 15), exponent (bits 14-7, bias 127) and mantissa   */
+/* (bits 6-0).  The 7 exponents of the table get the 3-bit codes        */
+/* 001-111 by rank; any other exponent is coded 000 followed by its 8    */
+/* bits (the page moves escaped exponents to a separate array; here     */
+/* they follow their 000 code in the stream, as in the e4m3 variant).   */
+/* Sign and mantissa follow as they are: a value's codeword is          */
+/* [code][exponent if escaped][sign][mantissa], 11 or 19 bits.  The      */
+/* container is the byte container's, with 16-bit symbols.              */
+/* ------------------------------------------------------------------ */
+
+/* Histogram of the exponent field. */
+int eo_bf16_exponent_counts(const uint16_t *x, uint64_t n, uint64_t *count)
+{
+    for (int e = 0; e < 256; e++)
+        count[e] = 0;
+    for (uint64_t i = 0; i < n; i++)
+        count[(x[i] >> 7) & 0xFF]++;
+    return EO_OK;
+}
+
+/* Top 7 exponents by count ([ZIP] 2.A: the 7 most frequent exponents):
+ * selection, largest count first, ties to the smaller exponent. */
+int eo_bf16_top7_from_counts(const uint64_t *count, uint8_t *top)
+{
+    int taken[256] = {0};
+    for (int r = 0; r < 7; r++) {
+        int best = -1;
+        for (int e = 0; e < 256; e++)
+            if (!taken[e] && (best < 0 || count[e] > count[best]))
+                best = e;
+        taken[best] = 1;
+        top[r] = (uint8_t)best;
+    }
+    return EO_OK;
+}
+
+/* Probability that x ~ N(0, sigma^2), rounded to BF16 (round to nearest,
+ * ties to even), has exponent field e ([ZIP] 2.A: the table follows from
+ * the standard deviation alone).  A BF16 value with exponent field e
+ * (1..254) has magnitude in [2^(e-127), 2^(e-126)); rounding moves each
+ * boundary 2^k down to the midpoint 2^k (1 - 2^-9) between 2^k and the
+ * largest BF16 below it (the tie goes to 2^k, whose mantissa is even).
+ * Field 0 holds zero and the subnormals (|x| below 2^-126 (1 - 2^-9)); field
+ * 255 the values that round past the largest finite BF16 (not reached by
+ * any sigma a tensor has).  P(|x| >= a) = erfc(a / (sigma sqrt 2)). */
+static double bf16_tail(double a, double sigma)
+{
+    return erfc(a / (sigma * sqrt(2.0)));
+}
+
+int eo_bf16_exponent_probs(double sigma, double *prob)
+{
+    if (!(sigma > 0.0))
+        return EO_ARG;
+    const double shrink = 1.0 - ldexp(1.0, -9);
+    for (int e = 0; e < 256; e++) {
+        double lo, hi;
+        if (e == 0) {
+            lo = 0.0;
+            hi = ldexp(1.0, -126) * shrink;
+        } else if (e == 255) {
+            lo = ldexp(1.0, 128) * shrink;
+            hi = INFINITY;
+        } else {
+            lo = ldexp(1.0, e - 127) * shrink;
+            hi = ldexp(1.0, e - 126) * shrink;
+        }
+        prob[e] = bf16_tail(lo, sigma) - (isinf(hi) ? 0.0 : bf16_tail(hi, sigma));
+    }
+    return EO_OK;
+}
+
+/* Top 7 exponents of N(0, sigma^2): the 7 largest probabilities, ties to
+ * the smaller exponent. */
+int eo_bf16_top7_from_sigma(double sigma, uint8_t *top)
+{
+    double prob[256];
+    if (eo_bf16_exponent_probs(sigma, prob))
+        return EO_ARG;
+    int taken[256] = {0};
+    for (int r = 0; r < 7; r++) {
+        int best = -1;
+        for (int e = 0; e < 256; e++)
+            if (!taken[e] && (best < 0 || prob[e] > prob[best]))
+                best = e;
+        taken[best] = 1;
+        top[r] = (uint8_t)best;
+    }
+    return EO_OK;
+}
+
+static int bf16_rank_table(const uint8_t *top, int *rank_of)
+{
+    for (int e = 0; e < 256; e++)
+        rank_of[e] = -1;
+    for (int r = 0; r < 7; r++) {
+        if (rank_of[top[r]] >= 0)
+            return EO_ARG; /* an exponent listed twice */
+        rank_of[top[r]] = r;
+    }
+    return EO_OK;
+}
+
+/* Code and length of one BF16 value. */
+static void bf16_code(uint16_t v, const int *rank_of, uint64_t *code, int *len)
+{
+    const uint64_t s = (v >> 15) & 1, e = (v >> 7) & 0xFF, m = v & 0x7F;
+    const uint64_t sm = (s << 7) | m; /* 8 bits */
+    if (rank_of[e] >= 0) {
+        *code = ((uint64_t)(rank_of[e] + 1) << 8) | sm; /* ccc s mmmmmmm */
+        *len = 11;
+    } else {
+        *code = (e << 8) | sm; /* 000 eeeeeeee s mmmmmmm */
+        *len = 19;
+    }
+}
+
+/* Encode n BF16 values into the container, one bit at a time. */
+int eo_bf16_escape_encode(const uint16_t *x, uint64_t n, const uint8_t *top, uint32_t C, uint32_t S,
+                          uint8_t *out, uint64_t cap, uint64_t *chunk_off, uint16_t *sub_bits,
+                          uint64_t *total_bits)
+{
+    int rank_of[256];
+    if (!container_args(C, S) || bf16_rank_table(top, rank_of))
+        return EO_ARG;
+    for (uint64_t i = 0; i < cap; i++)
+        out[i] = 0;
+    uint64_t n_chunks = (n + C - 1) / C;
+    uint64_t pos = 0, total = 0;
+    int err = EO_OK;
+    chunk_off[0] = 0;
+    for (uint64_t c = 0; c < n_chunks; c++) {
+        uint64_t lo = c * C, hi = lo + C < n ? lo + C : n;
+        uint64_t bit = 0, sub_start = 0;
+        for (uint64_t i = lo; i < hi; i++) {
+            uint64_t code;
+            int len;
+            bf16_code(x[i], rank_of, &code, &len);
+            if (i % S == 0)
+                sub_start = bit;
+            for (int t = len - 1; t >= 0; t--) {
+                uint64_t at = pos * 8 + bit;
+                if (at / 8 < cap) {
+                    if ((code >> t) & 1)
+                        out[at / 8] |= (uint8_t)(0x80u >> (at % 8));
+                } else {
+                    err = EO_CAPACITY;
+                }
+                bit++;
+            }
+            if ((i + 1) % S == 0 || i + 1 == hi)
+                sub_bits[i / S] = (uint16_t)(bit - sub_start);
+        }
+        uint64_t bytes = pad16((bit + 7) / 8);
+        if (pos + bytes > cap)
+            err = EO_CAPACITY;
+        pos += bytes;
+        chunk_off[c + 1] = pos;
+        total += bit;
+    }
+    *total_bits = total;
+    return err;
+}
+
+/* Decode the container back to BF16 values, one bit at a time, with the
+ * same checks as the byte container (offsets, sub-block bit counts, zero
+ * padding); 000 followed by an exponent of the table is no codeword. */
+int eo_bf16_escape_decode(const uint8_t *in, uint64_t in_bytes, const uint64_t *chunk_off,
+                          const uint16_t *sub_bits, uint64_t n, uint32_t C, uint32_t S, const uint8_t *top,
+                          uint16_t *out)
+{
+    int rank_of[256];
+    if (!container_args(C, S) || bf16_rank_table(top, rank_of))
+        return EO_ARG;
+    uint64_t n_chunks = (n + C - 1) / C;
+    if (chunk_off[0] != 0)
+        return EO_CORRUPT;
+    for (uint64_t c = 0; c < n_chunks; c++) {
+        uint64_t b0 = chunk_off[c], b1 = chunk_off[c + 1];
+        if (b1 < b0 || b1 > in_bytes || (b0 % 16) || (b1 % 16))
+            return EO_CORRUPT;
+        eo_reader r = {in, b0 * 8, b1 * 8};
+        uint64_t lo = c * C, hi = lo + C < n ? lo + C : n;
+        uint64_t sub_start = r.at;
+        for (uint64_t i = lo; i < hi; i++) {
+            uint64_t p, e, s, m;
+            if (i % S == 0)
+                sub_start = r.at;
+            if (read_bits(&r, 3, &p))
+                return EO_CORRUPT;
+            if (p == 0) {
+                if (read_bits(&r, 8, &e))
+                    return EO_CORRUPT;
+                if (rank_of[e] >= 0)
+                    return EO_CORRUPT;
+            } else {
+                e = top[p - 1];
+            }
+            if (read_bits(&r, 1, &s) || read_bits(&r, 7, &m))
+                return EO_CORRUPT;
+            out[i] = (uint16_t)((s << 15) | (e << 7) | m);
+            if ((i + 1) % S == 0 || i + 1 == hi)
+                if (r.at - sub_start != sub_bits[i / S])
+                    return EO_CORRUPT;
+        }
+        if (pad16((r.at - b0 * 8 + 7) / 8) != b1 - b0)
+            return EO_CORRUPT;
+        while (r.at < r.limit) {
+            int v;
+            read_bit(&r, &v);
+            if (v)
+                return EO_CORRUPT;
+        }
+    }
+    return EO_OK;
+}

@@ -634,3 +634,89 @@ def test_prefix_bits_codes_kraft_and_round_trip(p, gauss_counts):
     assert (oracle.decode(enc, cb) == x).all()
     if p == 3:
         assert (cb["len"] == oracle.qlc_codebook(gauss_counts, w)["len"]).all()
+
+
+# --------------------------------------------------------------- BF16 exponent escape code
+
+def _bf16_from_f64(x):
+    """Test-side cast float64 -> float32 -> BF16 bit patterns, round to
+    nearest even on the float32 bits (finite inputs)."""
+    f = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (f >> np.uint64(16)) & np.uint64(1)
+    return ((f + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+
+
+def test_bf16_escape_golden_stream():
+    rows = {r[0]: r[1:] for r in golden("bf16_escape_example.txt")}
+    top = np.array([int(v) for v in rows["top"]], np.uint8)
+    vals = np.array([int(v, 16) for v in rows["values"]], np.uint16)
+    expect = np.array([int(v, 16) for v in rows["bytes"]], np.uint8)
+    enc = oracle.bf16_escape_encode(vals, top, 1024, 64)
+    assert enc["total_bits"] == int(rows["bits"][0])
+    assert (enc["payload"] == expect).all()
+    assert list(enc["chunk_off"]) == [0, 16] and list(enc["sub_bits"]) == [41]
+    assert (oracle.bf16_escape_decode(enc, top) == vals).all()
+
+
+@pytest.mark.parametrize("sigma", [1.0, 0.02, 3.7e-3, 0.75, 40.0])
+def test_bf16_exponent_probs_match_a_sample(sigma):
+    # the closed form against the exponent frequencies of 2^22 draws of
+    # N(0, sigma^2) rounded to BF16 (five binomial standard errors)
+    g = np.random.default_rng(int(sigma * 1e4) + 7)
+    x = _bf16_from_f64(sigma * g.standard_normal(1 << 22))
+    freq = oracle.bf16_exponent_counts(x).astype(np.float64) / x.size
+    p = oracle.bf16_exponent_probs(sigma)
+    assert abs(p.sum() - 1.0) < 1e-12
+    tol = 5 * np.sqrt(np.maximum(p, 1e-7) * (1 - p) / x.size) + 1e-7
+    assert (np.abs(freq - p) <= tol).all()
+    # and the sigma table is the sample's top 7 where the ranks are clear
+    top_s, top_c = oracle.bf16_top7_from_sigma(sigma), oracle.bf16_top7_from_counts(oracle.bf16_exponent_counts(x))
+    assert set(top_s[:5].tolist()) == set(top_c[:5].tolist())
+    assert set(top_s.tolist()) == set(top_c.tolist())
+
+
+def test_bf16_top7_covers_97_percent():
+    # the page: the 7 most frequent exponents hold more than 97% of the data;
+    # for a Gaussian that holds at every scale (the top 7 from sigma)
+    for sigma in 2.0 ** np.linspace(-14, 6, 97):
+        p = oracle.bf16_exponent_probs(sigma)
+        top = oracle.bf16_top7_from_sigma(sigma)
+        assert len(set(top.tolist())) == 7
+        assert p[top].sum() > 0.97
+        assert p[top[0]] >= p[top[1]] >= p[top[6]]             # rank order
+        assert p[top].sum() >= np.sort(p)[-7:].sum() - 1e-15   # the 7 largest
+        assert 0 < p[top].sum() - np.sort(p)[-6:].sum()        # a 7th matters
+
+
+def test_bf16_escape_closed_form_and_round_trip():
+    # 16 -> 11 bits for exponents of the table, 19 bits for the others; every
+    # one of the 65536 bit patterns round-trips
+    top = oracle.bf16_top7_from_sigma(1.0)
+    allv = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    g = np.random.default_rng(3)
+    x = allv[g.permutation(allv.size)]
+    for C, S in ((1024, 64), (16384, 1024)):
+        enc = oracle.bf16_escape_encode(x, top, C, S)
+        in_top = np.isin((x >> 7) & 0xFF, top)
+        assert enc["total_bits"] == 11 * int(in_top.sum()) + 19 * int((~in_top).sum())
+        assert (oracle.bf16_escape_decode(enc, top) == x).all()
+    # a Gaussian tensor: about 31% smaller (16 -> 11 bits for > 97% of values)
+    v = _bf16_from_f64(0.02 * g.standard_normal(1 << 18))
+    enc = oracle.bf16_escape_encode(v, oracle.bf16_top7_from_sigma(0.02), 4096, 256)
+    bits = enc["total_bits"] / v.size
+    assert 11.0 < bits < 11.0 + 8 * 0.03 and 1 - bits / 16 > 0.29
+
+
+def test_bf16_escaped_table_exponent_is_corrupt():
+    top = oracle.bf16_top7_from_sigma(1.0)
+    # 000 followed by exponent 127 (in the table) is not a codeword
+    s = "000" + format(127, "08b") + "0" + "0000000"
+    buf = np.zeros(16, np.uint8)
+    buf[:3] = [int((s + "0" * 5)[i:i + 8], 2) for i in range(0, 24, 8)]
+    enc = {"payload": buf, "chunk_off": np.array([0, 16], np.uint64), "sub_bits": np.array([19], np.uint16),
+           "n": 1, "C": 1024, "S": 64}
+    with pytest.raises(oracle.OracleError):
+        oracle.bf16_escape_decode(enc, top)
+    enc["payload"] = oracle.bf16_escape_encode(np.array([0x3F80], np.uint16), top, 1024, 64)["payload"]
+    enc["sub_bits"] = np.array([11], np.uint16)
+    assert oracle.bf16_escape_decode(enc, top)[0] == 0x3F80

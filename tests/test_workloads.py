@@ -73,8 +73,14 @@ def test_generators_are_seeded_and_shaped():
     assert 0.40 < frac0 < 0.45         # 40% forced zeros plus GELU underflow
     g = np_grad(3 * 4096, (4, 2))
     assert g.dtype == np.uint8 and g.size == 3 * 4096
-    plan = batch_plan(64)
+    plan = batch_plan(4096)
     assert all(4096 <= s < 8 * 2 ** 20 for s, _, _ in plan)
-    assert {law for _, law, _ in plan} <= {0, 1, 2} and {t for _, _, t in plan} <= {0, 1, 2, 3}
-    # each law is coded with a codebook fitted to that law
-    assert all(t in ((0,), (2,), (1, 3))[law] for _, law, t in plan)
+    assert {law for _, law, _ in plan} == {0, 1, 2} and {t for _, _, t in plan} == {0, 1, 2, 3}
+    # laws uniform over 3, tags uniform over 4, drawn independently: every
+    # (law, tag) pair occurs about 4096/12 times
+    pairs = np.zeros((3, 4), np.int64)
+    for _, law, t in plan:
+        pairs[law, t] += 1
+    assert pairs.min() > 4096 / 12 * 0.75 and pairs.max() < 4096 / 12 * 1.25
+    sizes = np.log2([s for s, _, _ in plan])
+    assert abs(sizes.mean() - 17.5) < 0.15   # log2 size uniform on [12, 23]

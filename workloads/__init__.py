@@ -210,20 +210,22 @@ def grad_warmup(i: int, n: int = 1 << 24) -> np.ndarray:
 def batch_plan(count: int = 4096, key: tuple = (5,), lo_log2: float = 12.0, hi_log2: float = 23.0):
     """Plan of the batched workload: per tensor (size, law, codebook tag).
 
-    law: 0 = gauss N(0,1), 1 = gauss with sigma log-uniform, 2 = zero spike.
-    tag: which of four precomputed codebooks encodes it, each fitted to
-    warm-up data of one law (as a sender fits a codebook to the traffic it
-    codes): 0 = base QLC of N(0,1), 1 = adapted QLC of the zero spike,
-    2 = Huffman of pooled N(0, sigma) shards, 3 = Huffman of the zero spike.
-    Law 0 takes tag 0, law 1 tag 2, law 2 tag 1 or 3 (even odds).
+    size: floor(2^U(lo_log2, hi_log2)) bytes (4 KiB .. 8 MiB by default).
+    law: the generator of workload 1, 2 or 3, drawn uniformly:
+    0 = gauss N(0,1), 1 = gauss with sigma log-uniform, 2 = zero spike.
+    tag: one of the four precomputed codebooks, drawn uniformly and
+    independently of the law: 0 = base QLC of N(0,1) warm-up data,
+    1 = adapted QLC of zero-spike warm-up data, 2 = Huffman of pooled
+    N(0, sigma) shards, 3 = Huffman of zero-spike warm-up data.  A tensor is
+    therefore often coded with a codebook fitted to another law (longer codes,
+    even expansion), as happens when one codebook serves mixed traffic.
     """
     plan = []
     for i in range(count):
         g = rng(*key, i)
         size = int(math.floor(2.0 ** g.uniform(lo_log2, hi_log2)))
         law = int(g.integers(0, 3))
-        pick = int(g.integers(0, 2))
-        tag = (0, 2, 1 + 2 * pick)[law]
+        tag = int(g.integers(0, 4))
         plan.append((size, law, tag))
     return plan
 
