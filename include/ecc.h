@@ -340,6 +340,76 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
                       const ecc_codebook *cb, uint8_t *out, uint32_t *status, void *stream);
 
 /* ------------------------------------------------------------------------
+ * The exponent escape code on BF16 tensors (ZipCCL, gist.science summary of
+ * arXiv 2604.27844, section 2.B "Tecnica di Codifica degli Esponenti"; the
+ * exponent table of section 2.A).  Values are BF16 bit patterns (uint16:
+ * sign bit 15, exponent bits 14-7, mantissa bits 6-0).  A value whose
+ * exponent is one of the 7 of the table is written as the 3-bit code r + 1
+ * (its rank r in the table), any other as 000 followed by its 8-bit
+ * exponent; the sign bit and the 7 mantissa bits follow as they are: 11 or 19
+ * bits a value, most significant bit first (the page keeps escaped exponents
+ * in a separate array; here they stay in the stream).  The container is the
+ * byte container above with BF16 values as the symbols: chunks of C values
+ * (1024 <= C <= 16384), sub_bits per S values, chunk payloads padded to 16
+ * bytes.
+ * ---------------------------------------------------------------------- */
+
+/*
+ * bf16_escape_table_sigma -- the table from the layer's standard deviation
+ * alone (section 2.A: no statistics of the data): the 7 exponent fields of
+ * largest probability under N(0, sigma^2) rounded to BF16 (round to nearest
+ * even: a field's magnitude range [2^(e-127), 2^(e-126)) has its edges at the
+ * rounding midpoints 2^k (1 - 2^-9)), in decreasing probability, ties to the
+ * smaller field.
+ *   sigma  > 0, finite.   top7  host uint8[7], written.
+ * Errors: ECC_ERR_ARG.
+ */
+ecc_status bf16_escape_table_sigma(double sigma, uint8_t top7[7]);
+
+/*
+ * bf16_escape_table_counts -- the table from exponent counts (section 2.A:
+ * the 7 most frequent exponents): count descending, ties to the smaller
+ * field.   count  host uint64[256] (e.g. from bf16_exponent_histogram).
+ * Errors: ECC_ERR_ARG.
+ */
+ecc_status bf16_escape_table_counts(const uint64_t count[256], uint8_t top7[7]);
+
+/*
+ * bf16_exponent_histogram -- count of each exponent field, ADDED to count.
+ *   in  device uint16[n], 16-byte aligned;  count  device uint64[256].
+ * Errors: ECC_ERR_ARG (NULL, misaligned), ECC_ERR_CUDA.
+ */
+ecc_status bf16_exponent_histogram(const uint16_t *in, size_t n, uint64_t *count, void *stream);
+
+/* Payload bytes that always suffice for n values in chunks of C: 19 bits a
+ * value, each chunk padded to 16 bytes. */
+size_t bf16_escape_max_encoded_bytes(size_t n, uint32_t C);
+
+/*
+ * bf16_escape_encode -- code n BF16 values with the table top7 (host array
+ * of 7 distinct exponent fields, rank order).  Arguments, outputs, workspace
+ * (ecc_encode_workspace_bytes(n, C)) and device errors as for ecc_encode;
+ * out_cap: bf16_escape_max_encoded_bytes() always suffices.
+ * Host errors: ECC_ERR_ARG (sizes, C above 16384, alignment, NULL, a table
+ * exponent listed twice, small workspace), ECC_ERR_CUDA.
+ */
+ecc_status bf16_escape_encode(const uint16_t *in, size_t n, const uint8_t top7[7], uint32_t C, uint32_t S,
+                              uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,
+                              uint64_t *total_bits, void *ws, size_t ws_bytes, uint32_t *status, void *stream);
+
+/*
+ * bf16_escape_decode -- the inverse: out (device uint16[n]) from the
+ * container written with the same table, C and S.  Device errors:
+ * ECC_ERR_CORRUPT (offsets, a sub-block whose bit count differs from
+ * sub_bits, 000 followed by a table exponent, a chunk whose padded size or
+ * zero padding is wrong); nothing is read outside each chunk's payload.
+ * Host errors as for ecc_decode.
+ */
+ecc_status bf16_escape_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_off,
+                              const uint16_t *sub_bits, size_t n, uint32_t C, uint32_t S, const uint8_t top7[7],
+                              uint16_t *out, uint32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Batched calls: many tensors, one kernel launch for encode and one for
  * decode (each tensor an independent container, each with its own codebook)
  * ---------------------------------------------------------------------- */

@@ -91,6 +91,12 @@ def _load():
             "ecc_selftest_wait": (I32, [P, U64, U64, U64, P, P, P]),
             "ecc_encode_static": (I32, [P, Z, P, U32, U32, P, Z, P, P, P, P, P]),
             "ecc_status_string": (ct.c_char_p, [I32]),
+            "bf16_escape_table_sigma": (I32, [ct.c_double, P]),
+            "bf16_escape_table_counts": (I32, [P, P]),
+            "bf16_exponent_histogram": (I32, [P, Z, P, P]),
+            "bf16_escape_max_encoded_bytes": (Z, [Z, U32]),
+            "bf16_escape_encode": (I32, [P, Z, P, U32, U32, P, Z, P, P, P, P, Z, P, P]),
+            "bf16_escape_decode": (I32, [P, Z, P, P, Z, U32, U32, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -413,3 +419,77 @@ def ecc_encode_static(x, dev_cb, C: int = 16384, S: int | None = None, max_len: 
                                      _dptr(sub_bits), _dptr(total_bits), _dptr(status), _stream_ptr(stream)),
            "ecc_encode_static")
     return Encoded(out, chunk_off, sub_bits, total_bits, status, n, C, S)
+
+
+# ---------------------------------------------------------------- BF16 exponent escape code
+
+def bf16_escape_table_sigma(sigma: float) -> np.ndarray:
+    """The 7-exponent table of N(0, sigma^2) in BF16 (uint8[7], rank order)."""
+    top = np.zeros(7, np.uint8)
+    _check(_load().bf16_escape_table_sigma(float(sigma), _np_ptr(top)), "bf16_escape_table_sigma")
+    return top
+
+
+def bf16_escape_table_counts(count) -> np.ndarray:
+    """The 7 most frequent exponent fields of a count vector (uint8[7])."""
+    count = _u64(count)
+    top = np.zeros(7, np.uint8)
+    _check(_load().bf16_escape_table_counts(_np_ptr(count), _np_ptr(top)), "bf16_escape_table_counts")
+    return top
+
+
+def bf16_exponent_histogram(x, count=None, stream=None):
+    """Device exponent-field counts of BF16 values (x: uint16/int16/bfloat16
+    device tensor), added to count (int64[256], allocated if None)."""
+    torch = _torch()
+    if count is None:
+        count = torch.zeros(256, dtype=torch.int64, device=x.device)
+    _check(_load().bf16_exponent_histogram(_dptr(x), x.numel(), _dptr(count), _stream_ptr(stream)),
+           "bf16_exponent_histogram")
+    return count
+
+
+def bf16_escape_max_encoded_bytes(n: int, C: int) -> int:
+    return int(_load().bf16_escape_max_encoded_bytes(n, C))
+
+
+def bf16_escape_encode(x, top7, C: int = 4096, S: int | None = None, out=None, chunk_off=None, sub_bits=None,
+                       total_bits=None, ws=None, status=None, stream=None) -> Encoded:
+    """Encode device BF16 values (2-byte elements) with the escape code and
+    the host table top7."""
+    torch = _torch()
+    dev = x.device
+    n = x.numel()
+    S = default_subblock(C) if S is None else S
+    top7 = np.ascontiguousarray(top7, dtype=np.uint8)
+    if out is None:
+        out = torch.empty(max(16, bf16_escape_max_encoded_bytes(n, C)), dtype=torch.uint8, device=dev)
+    if chunk_off is None:
+        chunk_off = torch.empty(num_chunks(n, C) + 1, dtype=torch.int64, device=dev)
+    if sub_bits is None:
+        sub_bits = torch.empty(max(1, num_subblocks(n, S)), dtype=torch.int16, device=dev)
+    if total_bits is None:
+        total_bits = torch.empty(1, dtype=torch.int64, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = torch.empty(encode_workspace_bytes(n, C), dtype=torch.uint8, device=dev)
+    _check(_load().bf16_escape_encode(_dptr(x), n, _np_ptr(top7), C, S, _dptr(out), out.numel(), _dptr(chunk_off),
+                                      _dptr(sub_bits), _dptr(total_bits), _dptr(ws), ws.numel(), _dptr(status),
+                                      _stream_ptr(stream)), "bf16_escape_encode")
+    return Encoded(out, chunk_off, sub_bits, total_bits, status, n, C, S)
+
+
+def bf16_escape_decode(enc: Encoded, top7, out=None, status=None, stream=None):
+    """Decode a BF16 escape-code container (returns (values int16, status))."""
+    torch = _torch()
+    dev = enc.payload.device
+    top7 = np.ascontiguousarray(top7, dtype=np.uint8)
+    if out is None:
+        out = torch.empty(max(8, enc.n), dtype=torch.int16, device=dev)
+    if status is None:
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(_load().bf16_escape_decode(_dptr(enc.payload), enc.payload.numel(), _dptr(enc.chunk_off),
+                                      _dptr(enc.sub_bits), enc.n, enc.C, enc.S, _np_ptr(top7), _dptr(out),
+                                      _dptr(status), _stream_ptr(stream)), "bf16_escape_decode")
+    return out, status

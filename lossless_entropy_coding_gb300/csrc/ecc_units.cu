@@ -168,24 +168,6 @@ __device__ __forceinline__ bool compute_bar_or(bool p)
     return r != 0;
 }
 
-// Exact bit count of the cnt bytes of (a, b) from the codebook in global
-// memory (a partial thread, or a code longer than 31 bits); *bad when a byte
-// has no code.
-static __device__ __noinline__ uint32_t unit_bits_slow(uint4 a, uint4 b, uint32_t cnt, const ecc_codebook *cb,
-                                                       bool *bad)
-{
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t bits = 0;
-    bool nocode = false;
-    for (uint32_t j = 0; j < cnt; ++j) {
-        const uint32_t L = min((uint32_t)cb->len[byte_of(w[j >> 2], j & 3)], (uint32_t)ECC_MAX_CODE_LEN);
-        nocode |= L == 0;
-        bits += L;
-    }
-    *bad = nocode;
-    return bits;
-}
-
 // Bit count of the 32 bytes of (a, b) coded one code at a time from the
 // lane's table replica (a thread with a pair longer than 32 bits); bit 31 set
 // when some byte has no code of at most 31 bits in the table (the exact path
@@ -604,7 +586,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
         const uint32_t st = st0 + slot * p.stage_bytes;
         const uint32_t lim = st + p.stage_bytes;
         UEnd e{0u, 0u, false};
-        bool bad_index = false;
+        [[maybe_unused]] bool bad_index = false;
         if (!over && cnt) {
             // the pairs of both halves: a half with a pair the table cannot
             // code sends the whole thread to the paths below, which rewrite

@@ -251,3 +251,16 @@ def test_default_subblock_rule():
         S = ecc.default_subblock(C)
         assert S == min(256, max(64, C // 64))
         assert S & (S - 1) == 0 and C % S == 0 and 64 <= S <= min(C, 1024)
+
+
+def test_bf16_escape_tables_match_oracle():
+    """The library's BF16 exponent tables (from sigma and from counts) equal
+    the oracle's (ZipCCL, section 2.A)."""
+    for sigma in 2.0 ** np.linspace(-20, 10, 61):
+        assert (ecc.bf16_escape_table_sigma(sigma) == oracle.bf16_top7_from_sigma(sigma)).all()
+    g = np.random.default_rng(12)
+    for trial in range(20):
+        count = g.integers(0, 5, 256).astype(np.uint64) * g.integers(0, 1000, 256).astype(np.uint64)
+        assert (ecc.bf16_escape_table_counts(count) == oracle.bf16_top7_from_counts(count)).all()
+    with pytest.raises(ecc.EccError):
+        ecc.bf16_escape_table_sigma(0.0)

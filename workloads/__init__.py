@@ -239,6 +239,30 @@ def np_batch_tensor(size: int, law: int, key: tuple) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# BF16 tensors (the exponent escape code of ZipCCL works on BF16 values)
+# --------------------------------------------------------------------------
+
+def bf16_from_f32(x: np.ndarray) -> np.ndarray:
+    """Cast float32 values to BF16 bit patterns (uint16): round to nearest
+    even on the float32 bits (finite values)."""
+    f = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (f >> np.uint64(16)) & np.uint64(1)
+    return ((f + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+
+
+def np_bf16_gauss(n: int, key: tuple, sigma: float) -> np.ndarray:
+    """n BF16 values of N(0, sigma^2) (drawn in float64, rounded to float32,
+    then to BF16), as uint16 bit patterns: the near-Gaussian layer data the
+    ZipCCL page codes."""
+    g = rng(*key)
+    out = np.empty(n, dtype=np.uint16)
+    for i in range(0, n, _BATCH):
+        k = min(_BATCH, n - i)
+        out[i:i + k] = bf16_from_f32((sigma * g.standard_normal(k)).astype(np.float32))
+    return out
+
+
+# --------------------------------------------------------------------------
 # PyTorch (device) laws: same recipes, device random streams
 # --------------------------------------------------------------------------
 
@@ -315,3 +339,16 @@ def dev_batch_tensor(size: int, law: int, key: tuple, device="cuda", out=None):
     if law == 1:
         return dev_gauss(size, key, device, out=out)[0]
     return dev_zero_spike(size, key, device, out=out)
+
+
+def dev_bf16_gauss(n: int, key: tuple, sigma: float, device="cuda"):
+    """Device BF16 values of N(0, sigma^2) (float64 draw -> float32 -> BF16,
+    round to nearest even), returned as an int16 tensor of bit patterns."""
+    torch = _torch()
+    g = _dev_gen(device, key)
+    out = torch.empty(n, dtype=torch.int16, device=device)
+    for i in range(0, n, _DEV_BATCH):
+        k = min(_DEV_BATCH, n - i)
+        z = torch.randn(k, generator=g, device=device, dtype=torch.float64)
+        out[i:i + k] = (sigma * z).float().to(torch.bfloat16).view(torch.int16)
+    return out
