@@ -56,12 +56,15 @@ constexpr uint32_t kUBarCompute = 1;                 // named barrier of the com
 static_assert(kUWarps == 16, "phase B scans the warp totals over the lanes of one half-warp");
 
 // Shared state of the pipeline.  Slot s = k % 2 of the CTA's k-th unit holds
-// its input buffer and its stage; the per-unit records the storer reads are
-// kept four deep (k % 4).
+// its input buffer and its stage; the per-unit records the storer reads, and
+// the mbarrier that hands them over, are kept four deep (k % 4): the compute
+// warps may size unit k + 2 before the storer, busy with unit k's look-back,
+// has taken unit k's records (at the start, when both stages are free), but
+// never unit k + 4.
 struct UPipe {
     uint64_t full[2];      // input buffer s filled: one arrival (loader) + the copy's bytes
     uint64_t st_free[2];   // stage s read by its bulk store: one arrival (storer)
-    uint64_t agg[2];       // unit of slot s sized and published: one arrival (compute thread 0)
+    uint64_t agg[4];       // unit k sized and published: one arrival (compute thread 0), in agg[k % 4]
     uint64_t done[2];      // unit of slot s packed (its input read, its stage written): one arrival per compute thread
     uint64_t unit[2];      // loader -> compute: unit of slot s, or kUEnd
     uint64_t sunit[4];     // compute -> storer: unit k, or kUEnd
@@ -117,6 +120,34 @@ __device__ __forceinline__ void red_or_pred(uint32_t addr, uint32_t v, bool p)
 {
     asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q red.shared.or.b32 [%0], %1;\n\t}" ::"r"(addr),
                  "r"(v), "r"((uint32_t)p)
+                 : "memory");
+}
+
+// predicated shared 64-bit store, mbarrier arrival, relaxed global store and
+// 16-bit global store (single instructions under a predicate, no branch)
+__device__ __forceinline__ void st_shared_u64_pred(void *addr, uint64_t v, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.u64 [%0], %1;\n\t}" ::"r"(smem_u32(addr)),
+                 "l"(v), "r"((uint32_t)p)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_pred(uint64_t *bar, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(
+                     smem_u32(bar)),
+                 "r"((uint32_t)p)
+                 : "memory");
+}
+__device__ __forceinline__ void st_relaxed_pred(uint64_t *addr, uint64_t v, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.relaxed.gpu.global.u64 [%0], %1;\n\t}" ::"l"(addr),
+                 "l"(v), "r"((uint32_t)p)
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_u16_pred(uint16_t *addr, uint32_t v, bool p)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.u16 [%0], %1;\n\t}" ::"l"(addr),
+                 "h"((uint16_t)v), "r"((uint32_t)p)
                  : "memory");
 }
 
@@ -396,16 +427,15 @@ __device__ __forceinline__ ULayout unit_layout(uint32_t x, uint32_t lane, uint32
 
 // Exclusive prefix (bytes) of unit u from its predecessors' published sizes
 // (decoupled look-back over units, one warp, 8 flags a lane per step, so a
-// step spans 256 predecessors), then u's inclusive prefix is published.  The
-// look-back stops at the first inclusive prefix it meets, or at unit `known`
-// (< u, or -1 for none) whose inclusive prefix known_incl the caller already
-// holds (the CTA's previous unit, about one ticket round back): it never
-// depends on how far other CTAs have got with their own look-backs.  Waits
-// for a predecessor that has published nothing yet, at most timeout_ns in all
-// (then *timed_out; u's prefix is still published, so that successors
-// finish).
-__device__ __forceinline__ uint64_t unit_resolve(uint64_t *flags, uint64_t u, uint64_t aggregate, int64_t known,
-                                                 uint64_t known_incl, uint64_t timeout_ns, bool *timed_out)
+// step spans 256 predecessors); the caller then publishes u's inclusive
+// prefix.  The look-back stops at the first
+// inclusive prefix it meets, or at unit `known` (< u, or -1 for none) whose
+// inclusive prefix known_incl the caller already holds (the CTA's previous
+// unit, about one ticket round back): it never depends on how far other CTAs
+// have got with their own look-backs.  Waits for a predecessor that has
+// published nothing yet, at most timeout_ns in all (then *timed_out).
+__device__ __forceinline__ uint64_t unit_lookback(const uint64_t *flags, uint64_t u, int64_t known,
+                                                  uint64_t known_incl, uint64_t timeout_ns, bool *timed_out)
 {
     constexpr int kPer = 8;
     const uint32_t lane = threadIdx.x & 31;
@@ -420,7 +450,8 @@ __device__ __forceinline__ uint64_t unit_resolve(uint64_t *flags, uint64_t u, ui
             const int64_t idx = j - kPer * (int64_t)lane - i;
             // before unit 0: a prefix of 0; the known unit: its inclusive prefix
             f[i] = idx < 0 ? kFlagPrefix
-                           : idx == known ? (kFlagPrefix | known_incl) : (idx < known ? kFlagPrefix : ld_relaxed(flags + idx));
+                           : idx == known ? (kFlagPrefix | known_incl)
+                                          : (idx < known ? kFlagPrefix : ld_relaxed(const_cast<uint64_t *>(flags) + idx));
         }
         // this lane's flags, newest first, up to and including the first prefix
         bool have = false, zero = false;
@@ -457,8 +488,6 @@ __device__ __forceinline__ uint64_t unit_resolve(uint64_t *flags, uint64_t u, ui
             break;
         j -= 32 * kPer;
     }
-    if (lane == 0)
-        st_relaxed(flags + u, kFlagPrefix | ((prefix + aggregate) & kValueMask));
     *timed_out = expired;
     return prefix;
 }
@@ -485,27 +514,6 @@ __device__ __forceinline__ void unit_join(const uint2 *lt, uint32_t w, uint32_t 
 __device__ __forceinline__ uint32_t len4(const uint8_t *len, uint32_t w)
 {
     return (uint32_t)len[byte_of(w, 0)] + len[byte_of(w, 1)] + len[byte_of(w, 2)] + len[byte_of(w, 3)];
-}
-
-// the 16 bytes of x as 8 pairs appended to pk, or nothing (false) if some
-// pair has no fast code
-__device__ __forceinline__ bool unit_half(const uint2 *lt, uint4 x, UPacker &pk, bool first)
-{
-    uint32_t v[8], q[8], qm = 0xFFFFFFFFu;
-    unit_join(lt, x.x, v[0], q[0], v[1], q[1], qm);
-    unit_join(lt, x.y, v[2], q[2], v[3], q[3], qm);
-    unit_join(lt, x.z, v[4], q[4], v[5], q[5], qm);
-    unit_join(lt, x.w, v[6], q[6], v[7], q[7], qm);
-    if (qm == 0)
-        return false;
-    if (first)
-        pk.start_pending(v[0], q[0]);
-    else
-        pk.put(v[0], q[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i)
-        pk.put(v[i], q[i]);
-    return true;
 }
 
 template <bool kOne>
@@ -550,12 +558,11 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
 
         // ---- phase B: positions, sub-block counts, the unit's size
         const uint32_t incl = warp_incl(B);
-        if (lane == 31)
-            P.wtot[r][w] = incl;
+        st_shared_pred(smem_u32(&P.wtot[r][w]), incl, lane == 31);
         if (compute_bar_or(end)) { // the pipeline ends (the same decision in every compute warp)
             if (t == 0) {
                 P.sunit[r] = kUEnd;
-                mbar_arrive(&P.agg[slot]);
+                mbar_arrive(&P.agg[r]);
             }
             break;
         }
@@ -564,17 +571,14 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
         const uint32_t wE = __shfl_sync(~0u, lay.E, w);
         const uint32_t cbase = kOne ? 0u : __shfl_sync(~0u, lay.base, w);
         const uint32_t ubytes = __shfl_sync(~0u, lay.Y, kUWarps - 1u);
-        if (t == 0) { // publish the unit's size for the look-back; hand the unit to the storer
-            if (u != 0)
-                st_relaxed(job.flags + u, kFlagAggregate | ubytes);
-            P.sunit[r] = u;
-            mbar_arrive(&P.agg[slot]);
-        }
+        // publish the unit's size for the look-back; hand the unit to the storer
+        st_relaxed_pred(job.flags + u, kFlagAggregate | ubytes, t == 0 && u != 0);
+        st_shared_u64_pred(&P.sunit[r], u, t == 0);
+        mbar_arrive_pred(&P.agg[r], t == 0);
         {
             const uint32_t sb = __shfl_sync(~0u, incl, lane | (tps - 1u)) - (incl - B);
             const uint64_t sidx = (ubase + s0) >> s_shift;
-            if (cnt && (lane & (tps - 1u)) == 0 && sidx < n_sub)
-                job.sub_bits[sidx] = (uint16_t)sb;
+            st_global_u16_pred(job.sub_bits + sidx, sb, cnt && (lane & (tps - 1u)) == 0 && sidx < n_sub);
         }
         const bool over = ubytes > p.stage_bytes;
         // the stage of this slot is free once the unit two back has been stored
@@ -587,33 +591,59 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
         const uint32_t lim = st + p.stage_bytes;
         UEnd e{0u, 0u, false};
         [[maybe_unused]] bool bad_index = false;
-        if (!over && cnt) {
-            // the pairs of both halves: a half with a pair the table cannot
-            // code sends the whole thread to the paths below, which rewrite
-            // every word of its range
-            UPacker pk;
+        // the code pairs, 8 at a time (16 bytes); a partial thread, or one
+        // with a pair the table cannot code, takes the paths below, which
+        // rewrite every word of its range
+        UPacker pk;
 #ifdef ECC_CHECKED
-            pk.lim = lim;
+        pk.lim = lim;
 #endif
-            pk.begin(st, pos);
-            bool fast = cnt == kUThr;
-            if (fast)
-                fast = unit_half(lt, ld_shared_v4(src), pk, true);
-            if (fast)
-                fast = unit_half(lt, ld_shared_v4(src + 16u), pk, false);
-            if (fast) {
-                e = pk.finish();
-#ifdef ECC_CHECKED
-                bad_index = pk.bad;
-#endif
-            } else {
-                const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16u);
-                const uint32_t bs = cnt == kUThr ? unit_bits_single(lt, a, b) : 1u << 31;
-                if (!(bs >> 31))
-                    e = unit_pack_single(lt, st, pos, a, b, lim, job.status);
+        pk.begin(st, pos);
+        bool fast = !over && cnt == kUThr;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t v[8], q[8], qm = 0xFFFFFFFFu;
+            const uint4 x = ld_shared_v4(src + 16u * h);
+            unit_join(lt, x.x, v[0], q[0], v[1], q[1], qm);
+            unit_join(lt, x.y, v[2], q[2], v[3], q[3], qm);
+            unit_join(lt, x.z, v[4], q[4], v[5], q[5], qm);
+            unit_join(lt, x.w, v[6], q[6], v[7], q[7], qm);
+            fast = fast && qm != 0;
+            if (__all_sync(~0u, fast)) { // the common case: straight-line appends
+                if (h == 0)
+                    pk.start_pending(v[0], q[0]);
                 else
-                    e = unit_pack_slow(st, pos, a, b, cnt, job.cb, lim, job.status);
+                    pk.put(v[0], q[0]);
+#pragma unroll
+                for (int i = 1; i < 8; ++i)
+                    pk.put(v[i], q[i]);
+            } else if (fast) {
+                if (h == 0)
+                    pk.start_pending(v[0], q[0]);
+                else
+                    pk.put(v[0], q[0]);
+#pragma unroll
+                for (int i = 1; i < 8; ++i)
+                    pk.put(v[i], q[i]);
             }
+        }
+        if (__all_sync(~0u, fast)) {
+            e = pk.finish();
+#ifdef ECC_CHECKED
+            bad_index = pk.bad;
+#endif
+        } else if (fast) {
+            e = pk.finish();
+#ifdef ECC_CHECKED
+            bad_index = pk.bad;
+#endif
+        } else if (!over && cnt) {
+            const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16u);
+            const uint32_t bs = cnt == kUThr ? unit_bits_single(lt, a, b) : 1u << 31;
+            if (!(bs >> 31))
+                e = unit_pack_single(lt, st, pos, a, b, lim, job.status);
+            else
+                e = unit_pack_slow(st, pos, a, b, cnt, job.cb, lim, job.status);
         }
         // The thread's last partial word: the next lane or-s it into its first
         // word; lane 31 leaves it to the storer; the chunk's last thread
@@ -628,8 +658,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
 #else
             st_shared_pred(e.addr, bswap32(e.tail), clast && e.partial);
 #endif
-            if (lane == 31 && !clast)
-                P.wtail[slot][w] = bswap32(e.tail);
+            st_shared_pred(smem_u32(&P.wtail[slot][w]), bswap32(e.tail), lane == 31 && !clast);
             red_or_pred(st + (pos >> 5) * 4u, bswap32(prev), cnt && lane && (pos & 31u));
         }
 #ifdef ECC_CHECKED
@@ -660,7 +689,7 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
         // claim late, once the compute warps have sized the unit in the other
         // slot: a unit is then sized soon after its ticket, and the
         // look-backs of later units wait less for it
-        if (k >= 2 && !stop && !mbar_wait(&P.agg[slot ^ 1u], (uint32_t)((k - 1) >> 1) & 1u, p.timeout_ns)) {
+        if (k >= 2 && !stop && !mbar_wait(&P.agg[(k - 1) & 3u], (uint32_t)((k - 1) >> 2) & 1u, p.timeout_ns)) {
             set_status(job.status, ECC_ERR_TIMEOUT);
             stop = true;
         }
@@ -699,7 +728,7 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
     uint64_t known_incl = 0;
     for (uint64_t k = 0; k <= p.n_units; ++k) {
         const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r = (uint32_t)k & 3u;
-        if (!mbar_wait(&P.agg[slot], par, p.timeout_ns)) {
+        if (!mbar_wait(&P.agg[r], (uint32_t)(k >> 2) & 1u, p.timeout_ns)) {
             if (lane == 0)
                 set_status(job.status, ECC_ERR_TIMEOUT);
             break;
@@ -709,8 +738,8 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         __syncwarp();
         // The previous unit's stage is free again once its bulk store has
         // read it.  Released only now that unit k's records are read: the
-        // compute warps cannot hand over unit k + 2 (same slot, same records)
-        // before they have packed unit k + 1 into that stage.
+        // compute warps cannot hand over unit k + 4 (same records) before
+        // they have packed unit k + 3, whose stage this releases.
         if (k > 0 && lane == 0) {
             bulk_wait_read();
             mbar_arrive(&P.st_free[slot ^ 1u]);
@@ -726,7 +755,9 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         for (int o = 16; o; o >>= 1)
             ubits += __shfl_xor_sync(~0u, ubits, o);
         bool to = false;
-        const uint64_t prefix = unit_resolve(job.flags, u, ubytes, known, known_incl, p.timeout_ns, &to);
+        const uint64_t prefix = unit_lookback(job.flags, u, known, known_incl, p.timeout_ns, &to);
+        if (lane == 0) // u's inclusive prefix, for the look-backs of later units
+            st_relaxed(job.flags + u, kFlagPrefix | ((prefix + ubytes) & kValueMask));
         known = (int64_t)u;
         known_incl = prefix + ubytes;
         const uint64_t c0 = u * G;
@@ -819,10 +850,11 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
     for (uint32_t i = threadIdx.x; i < kLutRows; i += blockDim.x)
         len_table[i] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
     if (threadIdx.x == 0) {
+        for (int s = 0; s < 4; ++s)
+            mbar_init(&P.agg[s], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&P.full[s], 1);
             mbar_init(&P.st_free[s], 1);
-            mbar_init(&P.agg[s], 1);
             mbar_init(&P.done[s], kUCompute);
         }
         fence_mbar_init();
