@@ -426,9 +426,11 @@ __device__ __forceinline__ ULayout unit_layout(uint32_t x, uint32_t lane, uint32
 }
 
 // Exclusive prefix (bytes) of unit u from its predecessors' published sizes
-// (decoupled look-back over units, one warp, 8 flags a lane per step, so a
-// step spans 256 predecessors); the caller then publishes u's inclusive
-// prefix.  The look-back stops at the first
+// (decoupled look-back over units, one warp, one flag a lane per step, so a
+// step spans 32 predecessors: the nearest published inclusive prefix is
+// usually that close, and a poll that reads fewer flags adds less traffic to
+// the cache lines every storer is polling); the caller then publishes u's
+// inclusive prefix.  The look-back stops at the first
 // inclusive prefix it meets, or at unit `known` (< u, or -1 for none) whose
 // inclusive prefix known_incl the caller already holds (the CTA's previous
 // unit, about one ticket round back): it never depends on how far other CTAs
@@ -437,7 +439,7 @@ __device__ __forceinline__ ULayout unit_layout(uint32_t x, uint32_t lane, uint32
 __device__ __forceinline__ uint64_t unit_lookback(const uint64_t *flags, uint64_t u, int64_t known,
                                                   uint64_t known_incl, uint64_t timeout_ns, bool *timed_out)
 {
-    constexpr int kPer = 8;
+    constexpr int kPer = 1;
     const uint32_t lane = threadIdx.x & 31;
     uint64_t prefix = 0;
     int64_t j = (int64_t)u - 1; // highest unit this step reads
