@@ -164,6 +164,7 @@ def hbm_peak():
 # sources of the kernels the main bench line times (single-tensor encode and
 # decode); a recorded ncu traffic figure is only reported for these exact sources
 TIMED_KERNEL_SOURCES = ("lossless_entropy_coding_gb300/csrc/ecc_kernels.cu",
+                        "lossless_entropy_coding_gb300/csrc/ecc_units.cu",
                         "lossless_entropy_coding_gb300/csrc/ecc_device.cuh",
                         "lossless_entropy_coding_gb300/csrc/ecc_launch.h", "include/ecc.h")
 

@@ -14,7 +14,7 @@
 // two CTAs run on an SM.
 //  * compute thread t of a unit owns symbols [32 t, 32 t + 32).  Phase A sums
 //    its 32 code lengths from a 256-byte shared length table (one byte-sized
-//    load a symbol, the byte value being the address).
+//    load a symbol, at the byte value rotated by one bit).
 //  * phase B: a warp scan of the counts and one barrier over the compute
 //    warps give every thread its bit position inside its chunk, every chunk
 //    its padded place in the unit, and the unit its padded size, which is
@@ -512,9 +512,20 @@ __device__ __forceinline__ void unit_join(const uint2 *lt, uint32_t w, uint32_t 
     qm = min(qm, min(q0, q1));
 }
 
+// The length table is indexed by each byte rotated left by one bit
+// (len_rot), which puts a byte's sign bit beside its lowest bit: a value and
+// its negation, equally frequent in these tensors, then share one word of
+// the table instead of two words of one bank.  A byte's bank is set by bits
+// 1..5, and only bit 6 (the exponent's top bit, rarely set in a gradient or
+// an activation) splits a bank's bytes over two words.
+__host__ __device__ constexpr uint32_t len_rot(uint32_t b) { return ((b << 1) | (b >> 7)) & 0xFFu; }
+// the four bytes of w rotated alike (three instructions for four bytes)
+__device__ __forceinline__ uint32_t len_rot4(uint32_t w) { return ((w << 1) & 0xFEFEFEFEu) | ((w >> 7) & 0x01010101u); }
+
 // sum of the 4 code lengths of the bytes of w (len: the shared length table)
 __device__ __forceinline__ uint32_t len4(const uint8_t *len, uint32_t w)
 {
+    w = len_rot4(w);
     return (uint32_t)len[byte_of(w, 0)] + len[byte_of(w, 1)] + len[byte_of(w, 2)] + len[byte_of(w, 3)];
 }
 
@@ -554,7 +565,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
                 B = 0;
 #pragma unroll
                 for (uint32_t j = 0; j < kUThr; ++j)
-                    B += j < cnt ? (uint32_t)len[byte_of(wd[j >> 2], j & 3)] : 0u;
+                    B += j < cnt ? (uint32_t)len[byte_of(len_rot4(wd[j >> 2]), j & 3)] : 0u;
             }
         }
 
@@ -823,7 +834,7 @@ template <bool kOne>
 __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
 {
     extern __shared__ __align__(128) uint8_t unit_smem[];
-    __shared__ uint8_t len_table[kLutRows]; // code length of each byte (at most ECC_MAX_CODE_LEN; 0: no code)
+    __shared__ uint8_t len_table[kLutRows]; // code length of byte b at len_rot(b) (at most ECC_MAX_CODE_LEN; 0: no code)
     uint2 *lut = reinterpret_cast<uint2 *>(unit_smem);
     UPipe &P = *reinterpret_cast<UPipe *>(unit_smem + kULutBytes);
     uint8_t *const base = unit_smem + kULutBytes + sizeof(UPipe);
@@ -850,7 +861,7 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
         lut[i] = make_uint2(cb->enc_code[s], cb->enc_mul[s]);
     }
     for (uint32_t i = threadIdx.x; i < kLutRows; i += blockDim.x)
-        len_table[i] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
+        len_table[len_rot(i)] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s)
             mbar_init(&P.agg[s], 1);
