@@ -376,8 +376,10 @@ struct DecParams {
 };
 
 // kPieces: the warps take pieces of chunks (p.pshift > 0), else chunks.
+// One or two streams a lane: at most 96 registers, so that up to 21 warps
+// fit an SM where the stages allow (smaller chunks); four: at most 136.
 template <int R, bool kPieces>
-__global__ void decode_kernel(DecParams p)
+__global__ void __maxnreg__(R >= 4 ? 136 : 96) decode_kernel(DecParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);

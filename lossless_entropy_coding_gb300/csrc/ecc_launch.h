@@ -14,7 +14,7 @@ struct EncJob;
 
 constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit (static + dynamic)
 constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may add on top
-constexpr int kDecMaxWarps = 18;
+constexpr int kDecMaxWarps = 22;
 constexpr uint32_t kDecPieceSyms = 8192; // symbols one decoding warp stages at most (but 32 sub-blocks)
 
 bool valid_sizes(uint32_t C, uint32_t S);
