@@ -203,9 +203,11 @@ def oracle_round_trip_rate(x_chunks, codebooks, C, S, seconds_target=10.0, threa
 
     threads = threads or os.cpu_count() or 1
 
+    Ss = list(S) if isinstance(S, (list, tuple)) else [S] * len(codebooks)
+
     def work(chunk):
-        for ocb in codebooks:
-            e = oracle.encode(chunk, ocb, C, S)
+        for ocb, s_ in zip(codebooks, Ss):
+            e = oracle.encode(chunk, ocb, C, s_)
             y = oracle.decode(e, ocb)
             assert (y == chunk).all()
         return chunk.size * len(codebooks)
@@ -233,8 +235,16 @@ def cpu_sample(n_chunks, C, key=(4, 0)):
     return [x[i * C:(i + 1) * C] for i in range(n_chunks)]
 
 
+def default_subblocks(C):
+    """The library's default sub-block sizes of the two codebooks (Huffman:
+    table-decoded, C/128; base QLC: register-decoded, C/64; both clamped to
+    [64, 256]), restated so that the reference arm needs no library."""
+    return [min(256, max(64, C // 128)), min(256, max(64, C // 64))]
+
+
 def host_codebooks(C):
-    """Oracle codebooks from a host-generated warm-up of the same law."""
+    """Oracle codebooks (Huffman, base QLC) from a host-generated warm-up of
+    the same law."""
     import oracle
     from workloads import grad_warmup
     counts = [oracle.histogram(grad_warmup(i, 1 << 22)) for i in range(2)]
@@ -247,7 +257,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     C = args.chunk
-    S = min(1024, max(64, C // 64))
+    S = [args.subblock] * 2 if args.subblock else default_subblocks(C)
     cbs = host_codebooks(C)
     threads = os.cpu_count() or 1
     # per-step sample sized so that warm-up + timed steps take ~90 s
@@ -261,8 +271,8 @@ def run_reference(args):
     def step():
         def work(chunk):
             import oracle
-            for ocb in cbs:
-                e = oracle.encode(chunk, ocb, C, S)
+            for ocb, s_ in zip(cbs, S):
+                e = oracle.encode(chunk, ocb, C, s_)
                 oracle.decode(e, ocb)
             return chunk.size * len(cbs)
         with cf.ThreadPoolExecutor(threads) as ex:
@@ -282,8 +292,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "chunk": C, "subblock": S, "codebooks": ["fixed Huffman", "base QLC"],
-                   "oracle": "bit-serial C, host threads over chunks"},
+        "config": {"workload": WORKLOAD, "chunk": C, "subblock": {"huffman": S[0], "qlc": S[1]},
+                   "codebooks": ["fixed Huffman", "base QLC"], "oracle": "bit-serial C, host threads over chunks"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -426,7 +436,6 @@ def cfg2_row(ecc, dev, stream, peak, oracle_s):
     from workloads import dev_gauss, np_gauss
     EV = torch.cuda.Event
     n, C = 1 << 22, CHUNK
-    S = ecc.default_subblock(C)
     pooled = torch.zeros(256, dtype=torch.int64, device=dev)
     for i in range(16):
         ecc.e4m3_histogram(dev_gauss(n, (2, i), dev)[0], pooled)
@@ -435,6 +444,7 @@ def cfg2_row(ecc, dev, stream, peak, oracle_s):
     cbb = ecc.huff_build_canonical(weights)
     dcb = ecc.to_device(cbb, dev)
     max_len = int(ecc.codebook_view(cbb)["max_len"])
+    S = ecc.default_subblock(C, cbb)
     shards, sig, counts = [], [], []
     for i in range(64):
         xs, sg = dev_gauss(n, (2, 100 + i), dev)
@@ -529,7 +539,6 @@ def cfg3_row(ecc, dev, stream, peak, oracle_s):
     import torch
     from workloads import dev_zero_spike, np_zero_spike
     n, C = 1 << 28, CHUNK
-    S = ecc.default_subblock(C)
     x = dev_zero_spike(n, (3, 0), dev)
     counts = ecc.e4m3_histogram(x)
     torch.cuda.synchronize()
@@ -538,7 +547,9 @@ def cfg3_row(ecc, dev, stream, peak, oracle_s):
     books = {"adapted_qlc": ecc.qlc_build_tables(counts, w), "base_qlc": ecc.qlc_build_tables(counts),
              "huffman": ecc.huff_build_canonical(counts + np.uint64(1))}
     res = {}
+    Sb = {k: ecc.default_subblock(C, cbb) for k, cbb in books.items()}
     for k, cbb in books.items():
+        S = Sb[k]
         t = _code_times(ecc, x, ecc.to_device(cbb, dev), C, S, int(ecc.codebook_view(cbb)["max_len"]), stream)
         algo = _algo_bytes(ecc, n, t["payload"], C, S)
         res[k] = _rates(n, t, algo, peak) | {"compressibility_pct": 100 * (1 - t["bits"] / (8.0 * n)),
@@ -557,7 +568,8 @@ def cfg3_row(ecc, dev, stream, peak, oracle_s):
         "huffman_minus_adapted_pp": res["huffman"]["compressibility_pct"] - res["adapted_qlc"]["compressibility_pct"],
         "shannon_pct": 100 * (1 - ecc.entropy_bits(counts) / 8.0),
         "pages_context": "FFN2: adapted QLC +2.3 pp over base, about 4 pp below Huffman",
-        "cpu_baseline": _oracle_rates_lazy(sample, C, S, oracle_s),
+        "subblock": Sb,
+        "cpu_baseline": _oracle_rates_lazy(sample, C, [Sb["adapted_qlc"], Sb["base_qlc"], Sb["huffman"]], oracle_s),
     }
 
 
@@ -658,18 +670,23 @@ def codebook_timing(ecc, x, dcb, b, C, S, stream, reps=8):
             "payload_bytes": int(b["chunk_off"][-1].item())}
 
 
-def other_timings(ecc, x, pooled_h, dcbs, bufs, C, S, stream, dev):
+def other_timings(ecc, x, pooled_h, dcbs, bufs, C, Sk, max_len, stream, dev, S_arg=None):
     """Informational timings after the timed region: the three-stage
-    pipeline, and the other fixed codebooks on the same tensor."""
+    pipeline, and the other fixed codebooks on the same tensor, each at its
+    own default sub-block size (in the buffers of the timed codebook with the
+    same sub-block size and long enough codes)."""
     import numpy as np
 
+    def timing(cb):
+        S = S_arg or ecc.default_subblock(C, cb)
+        ml = int(ecc.codebook_view(cb)["max_len"])
+        k = next(k for k in ("qlc", "huffman") if Sk[k] == S and max_len[k] >= ml)
+        return {"subblock": S, **codebook_timing(ecc, x, ecc.to_device(cb, dev), bufs[k], C, S, stream)}
+
     out = {}
-    out["three_stage"] = three_stage_latency(ecc, x, dcbs["huffman"], bufs["huffman"], C, S, stream)
-    # the other fixed codebooks, from the same warm-up counts (buffers
-    # sized for 11-bit and 14-bit codes: those of the QLC, and of the
-    # Huffman code, whose longest code is longer)
-    out["escape_code"] = codebook_timing(ecc, x, ecc.to_device(ecc.escape_build_tables(pooled_h), dev),
-                                         bufs["qlc"], C, S, stream)
+    out["three_stage"] = three_stage_latency(ecc, x, dcbs["huffman"], bufs["huffman"], C, Sk["huffman"], stream)
+    # the other fixed codebooks, from the same warm-up counts
+    out["escape_code"] = timing(ecc.escape_build_tables(pooled_h))
     # QLC with 2, 4 or 8 areas (searched widths, at most 4 lengths): code
     # bits from the counts; the best layout timed
     qa = {}
@@ -679,12 +696,9 @@ def other_timings(ecc, x, pooled_h, dcbs, bufs, C, S, stream, dev):
                                    "bits_per_byte_warmup": cost / float(pooled_h.sum())}
     best = min((1, 2, 3), key=lambda pb: qa[f"prefix_bits_{pb}"]["bits_per_byte_warmup"])
     wq = qa[f"prefix_bits_{best}"]["widths"]
-    qa["best"] = {"prefix_bits": best, **codebook_timing(
-        ecc, x, ecc.to_device(ecc.gqlc_build_tables(pooled_h, wq, best), dev), bufs["qlc"], C, S, stream)}
+    qa["best"] = {"prefix_bits": best, **timing(ecc.gqlc_build_tables(pooled_h, wq, best))}
     out["qlc_adapted"] = qa
-    out["huffman_limited_14"] = codebook_timing(
-        ecc, x, ecc.to_device(ecc.huff_build_limited(pooled_h + np.uint64(1), 14), dev), bufs["huffman"], C, S,
-        stream)
+    out["huffman_limited_14"] = timing(ecc.huff_build_limited(pooled_h + np.uint64(1), 14))
     return out
 
 
@@ -707,7 +721,6 @@ def run_ours(args):
     clocks.start()
 
     n, C = args.n, args.chunk
-    S = args.subblock or ecc.default_subblock(C)
     stream = torch.cuda.current_stream()
 
     # warm-up stage of the single-stage method: pooled histogram -> codebooks
@@ -721,6 +734,9 @@ def run_ours(args):
            "qlc": ecc.qlc_build_tables(pooled_h)}
     dcbs = {k: ecc.to_device(v, dev) for k, v in cbs.items()}
     max_len = {k: int(ecc.codebook_view(v)["max_len"]) for k, v in cbs.items()}
+    # each codebook at its default sub-block size (Huffman: C/128, read by
+    # the decoder's table path; QLC: C/64, its register path)
+    Sk = {k: args.subblock or ecc.default_subblock(C, v) for k, v in cbs.items()}
 
     x = dev_grad(n, (4, rank), device=dev)
     xcount = ecc.e4m3_histogram(x)
@@ -732,7 +748,7 @@ def run_ours(args):
         bufs[k] = {
             "out": torch.empty(ecc.max_encoded_bytes(n, C, max_len[k]), dtype=torch.uint8, device=dev),
             "chunk_off": torch.empty(ecc.num_chunks(n, C) + 1, dtype=torch.int64, device=dev),
-            "sub_bits": torch.empty(ecc.num_subblocks(n, S), dtype=torch.int16, device=dev),
+            "sub_bits": torch.empty(ecc.num_subblocks(n, Sk[k]), dtype=torch.int16, device=dev),
             "total_bits": torch.empty(1, dtype=torch.int64, device=dev),
             "status": torch.empty(1, dtype=torch.int32, device=dev),
             "dstatus": torch.empty(1, dtype=torch.int32, device=dev),
@@ -742,7 +758,7 @@ def run_ours(args):
 
     def encode(k, src):
         b = bufs[k]
-        return ecc.ecc_encode(src, dcbs[k], C, S, out=b["out"], chunk_off=b["chunk_off"], sub_bits=b["sub_bits"],
+        return ecc.ecc_encode(src, dcbs[k], C, Sk[k], out=b["out"], chunk_off=b["chunk_off"], sub_bits=b["sub_bits"],
                               total_bits=b["total_bits"], ws=b["ws"], status=b["status"])
 
     def decode(k, enc):
@@ -799,7 +815,7 @@ def run_ours(args):
         dec_ms = [a.elapsed_time(c) for a, c in zip(rec[k][1], rec[k][2])]
         payload = int(b["chunk_off"][-1].item())
         bits = int(b["total_bits"].item())
-        side = 8 * (ecc.num_chunks(n, C) + 1) + 2 * ecc.num_subblocks(n, S)
+        side = 8 * (ecc.num_chunks(n, C) + 1) + 2 * ecc.num_subblocks(n, Sk[k])
         algo = n + payload + side          # bytes read + written by one encode or one decode
         stats[k] = {
             "encode_ms": statistics.mean(enc_ms), "decode_ms": statistics.mean(dec_ms),
@@ -847,7 +863,7 @@ def run_ours(args):
             nch = ecc.num_chunks(P, C)
             return {"out": torch.empty(ecc.max_encoded_bytes(P, C, max_len[k]), dtype=torch.uint8, device=dev),
                     "chunk_off": torch.empty(nch + 1, dtype=torch.int64, device=dev),
-                    "sub_bits": torch.empty(ecc.num_subblocks(P, S), dtype=torch.int16, device=dev),
+                    "sub_bits": torch.empty(ecc.num_subblocks(P, Sk[k]), dtype=torch.int16, device=dev),
                     "total_bits": torch.empty(1, dtype=torch.int64, device=dev),
                     "status": torch.empty(1, dtype=torch.int32, device=dev),
                     "dstatus": torch.empty(1, dtype=torch.int32, device=dev)}
@@ -858,8 +874,8 @@ def run_ours(args):
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
         def code_piece(k, b, src, dst, L):
-            nch, nsub = ecc.num_chunks(L, C), ecc.num_subblocks(L, S)
-            enc = ecc.ecc_encode(src, dcbs[k], C, S, out=b["out"], chunk_off=b["chunk_off"][:nch + 1],
+            nch, nsub = ecc.num_chunks(L, C), ecc.num_subblocks(L, Sk[k])
+            enc = ecc.ecc_encode(src, dcbs[k], C, Sk[k], out=b["out"], chunk_off=b["chunk_off"][:nch + 1],
                                  sub_bits=b["sub_bits"][:nsub], total_bits=b["total_bits"], ws=pws,
                                  status=b["status"])
             ecc.ecc_decode(enc, dcbs[k], out=dst, status=b["dstatus"])
@@ -937,12 +953,12 @@ def run_ours(args):
         torch.cuda.synchronize()
         extra["histogram_gbs"] = 5 * n / h0.elapsed_time(h1) / 1e6
         if not args.no_extras:
-            extra.update(other_timings(ecc, x, pooled_h, dcbs, bufs, C, S, stream, dev))
+            extra.update(other_timings(ecc, x, pooled_h, dcbs, bufs, C, Sk, max_len, stream, dev, args.subblock))
         if not args.no_sweep:
             sweep = {}
             for Cs in (4096, 16384, 65536):
-                Ss = ecc.default_subblock(Cs)
                 for k in kinds:
+                    Ss = args.subblock or ecc.default_subblock(Cs, cbs[k])
                     out = torch.empty(ecc.max_encoded_bytes(n, Cs, max_len[k]), dtype=torch.uint8, device=dev)
                     res = []
                     for rep in range(4):
@@ -986,8 +1002,9 @@ def run_ours(args):
         C_ = C
         cbo = host_codebooks(C_)
         chunks = cpu_sample(256, C_)
-        rate, cores, desc = oracle_round_trip_rate(chunks, cbo, C_, S, seconds_target=12.0)
-        rate1, _, desc1 = oracle_round_trip_rate(chunks, cbo, C_, S, seconds_target=4.0, threads=1)
+        So = [Sk["huffman"], Sk["qlc"]]  # host_codebooks order
+        rate, cores, desc = oracle_round_trip_rate(chunks, cbo, C_, So, seconds_target=12.0)
+        rate1, _, desc1 = oracle_round_trip_rate(chunks, cbo, C_, So, seconds_target=4.0, threads=1)
         cpu = {"value": rate, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc,
                "value_1_thread": rate1, "sample_1_thread": desc1}
 
@@ -997,7 +1014,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "bytes": n, "chunk": C, "subblock": S,
+            "config": {"workload": WORKLOAD, "bytes": n, "chunk": C, "subblock": dict(Sk),
                        "codebooks": ["fixed canonical Huffman (8 x 2^24 B warm-up, +1)", "base QLC (same counts)"],
                        "step": "encode + decode with each codebook", "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}"},
@@ -1027,7 +1044,6 @@ def batched_row(ecc, dev, stream, peak, tensors, steps, warmup, oracle_s=None):
     import torch
     from workloads import batch_plan, dev_batch_tensor, dev_gauss, dev_zero_spike, np_batch_tensor
     C = CHUNK
-    S = ecc.default_subblock(C)
     plan = batch_plan(tensors)
 
     def counts(x):
@@ -1045,6 +1061,7 @@ def batched_row(ecc, dev, stream, peak, tensors, steps, warmup, oracle_s=None):
              ecc.huff_build_canonical(c2 + np.uint64(1)), ecc.huff_build_canonical(c3 + np.uint64(1))]
     dcbs = [ecc.to_device(b, dev) for b in books]
     max_len = [int(ecc.codebook_view(b)["max_len"]) for b in books]
+    Sb = [ecc.default_subblock(C, b) for b in books]  # each codebook at its default sub-block size
     total = sum(sz for sz, _, _ in plan)
     xin = torch.empty(total + 16 * len(plan), dtype=torch.uint8, device=dev)
     enc_items, dec_items, off = [], [], 0
@@ -1053,9 +1070,9 @@ def batched_row(ecc, dev, stream, peak, tensors, steps, warmup, oracle_s=None):
         dev_batch_tensor(size, law, (5, i), device=dev, out=x)
         off += (size + 15) // 16 * 16
         cap = ecc.max_encoded_bytes(size, C, max_len[tag])
-        common = {"n": size, "cap": cap, "cb": dcbs[tag], "C": C, "S": S,
+        common = {"n": size, "cap": cap, "cb": dcbs[tag], "C": C, "S": Sb[tag],
                   "chunk_off": torch.empty(ecc.num_chunks(size, C) + 1, dtype=torch.int64, device=dev),
-                  "sub_bits": torch.empty(ecc.num_subblocks(size, S), dtype=torch.int16, device=dev)}
+                  "sub_bits": torch.empty(ecc.num_subblocks(size, Sb[tag]), dtype=torch.int16, device=dev)}
         payload = torch.empty(cap, dtype=torch.uint8, device=dev)
         enc_items.append(dict(common, **{"in": x, "out": payload,
                                          "total_bits": torch.empty(1, dtype=torch.int64, device=dev),
@@ -1104,7 +1121,7 @@ def batched_row(ecc, dev, stream, peak, tensors, steps, warmup, oracle_s=None):
     done_d = (torch.cat([it["t_done_ns"] for it in dec_items]) - t_dec).cpu().numpy() / 1e3
     payload = sum(int(it["chunk_off"][-1].item()) for it in enc_items)
     bits = sum(int(it["total_bits"].item()) for it in enc_items)
-    side = sum(8 * (ecc.num_chunks(sz, C) + 1) + 2 * ecc.num_subblocks(sz, S) for sz, _, _ in plan)
+    side = sum(8 * (ecc.num_chunks(sz, C) + 1) + 2 * ecc.num_subblocks(sz, Sb[tag]) for sz, _, tag in plan)
     algo = total + payload + side
     tags = np.array([t for _, _, t in plan])
     names = ["base_qlc", "adapted_qlc", "huffman_gauss", "huffman_zero_spike"]
@@ -1121,7 +1138,7 @@ def batched_row(ecc, dev, stream, peak, tensors, steps, warmup, oracle_s=None):
         "workload": f"{len(plan)} tensors, sizes 2^U(12,23) B, laws {{N(0,1), N(0,sigma), zero spike}} uniform, "
                     "codebook uniform over {base QLC, adapted QLC, Huffman of N(0,sigma), Huffman of zero spike} "
                     "independently of the law",
-        "bytes": total, "chunk": C, "subblock": S, "steps": steps, "warmup": warmup,
+        "bytes": total, "chunk": C, "subblock": dict(zip(names, Sb)), "steps": steps, "warmup": warmup,
         "value_gbs": 2.0 * total * steps / total_ms / 1e6, "ms_per_step": total_ms / steps,
         "encode_gbs": total / enc_ms / 1e6, "decode_gbs": total / dec_ms / 1e6,
         "encode_frac": algo / enc_ms / 1e6 / peak, "decode_frac": algo / dec_ms / 1e6 / peak,
@@ -1140,7 +1157,7 @@ def batched_row(ecc, dev, stream, peak, tensors, steps, warmup, oracle_s=None):
 
         def work(item):
             xt, tag = item
-            e = oracle.encode(xt, ocbs[tag], C, S)
+            e = oracle.encode(xt, ocbs[tag], C, Sb[tag])
             oracle.decode(e, ocbs[tag])
             return xt.size
 

@@ -202,12 +202,38 @@ def encode_workspace_bytes(n: int, C: int) -> int:
     return int(_load().ecc_encode_workspace_bytes(n, C))
 
 
-def default_subblock(C: int) -> int:
-    """Sub-block size used when none is given: C/64, clamped to [64, 256].
+def _register_path(cb) -> bool:
+    """Whether the decoder reads codes of codebook cb through its prefix
+    register path (QLC with a 3-bit prefix and codes of at most 11 bits)
+    rather than through its first-level table.  cb: host codebook bytes, a
+    device codebook made by to_device, or None (taken as the register
+    path)."""
+    if cb is None:
+        return True
+    tag = getattr(cb, "_ecc_register_path", None)
+    if tag is not None:
+        return bool(tag)
+    if not isinstance(cb, np.ndarray):  # a device tensor of unknown origin
+        return True
+    v = codebook_view(cb)
+    return int(v["family"]) == FAMILY_QLC and int(v["prefix_bits"]) == 3 and int(v["max_len"]) <= 11
 
-    Larger sub-blocks cost the decoder occupancy: a warp stages 32 sub-blocks
-    or more, so with S > 256 fewer warps fit an SM."""
-    return int(min(256, max(64, C // 64)))
+
+def default_subblock(C: int, cb=None) -> int:
+    """Sub-block size used when none is given.
+
+    A QLC codebook the decoder reads through its prefix registers (or no
+    codebook given): C/64, clamped to [64, 256].  Any other codebook (Huffman,
+    the escape code, a length-limited Huffman or a QLC of fewer areas):
+    C/128, clamped to [64, 256].  Its decoder waits on dependent table
+    lookups, and 16 KiB chunks of 128 sub-blocks give each lane two
+    independent streams at the same number of warps (1 GiB gradient tensor:
+    Huffman decode 1.14 -> 1.03 ms, for 1/64 byte a symbol more of sub-block
+    counts); the QLC decoder is issue-bound and gains nothing.  Larger
+    sub-blocks cost the decoder occupancy: a warp stages 32 sub-blocks or
+    more, so with S > 256 fewer warps fit an SM."""
+    d = 64 if _register_path(cb) else 128
+    return int(min(256, max(64, C // d)))
 
 
 # ------------------------------------------------------------------ device calls
@@ -267,9 +293,13 @@ def escape_build_tables(count) -> np.ndarray:
 
 
 def to_device(cb: np.ndarray, device="cuda"):
-    """Copy raw codebook bytes to a device tensor (what the kernels read)."""
+    """Copy raw codebook bytes to a device tensor (what the kernels read).
+    The tensor remembers which decoder path the codebook takes, for
+    default_subblock."""
     torch = _torch()
-    return torch.from_numpy(np.ascontiguousarray(cb, np.uint8)).to(device)
+    t = torch.from_numpy(np.ascontiguousarray(cb, np.uint8)).to(device)
+    t._ecc_register_path = _register_path(cb)
+    return t
 
 
 def e4m3_histogram(x, count=None, stream=None):
@@ -319,7 +349,7 @@ def ecc_encode(x, dev_cb, C: int = 16384, S: int | None = None, max_len: int = M
     torch = _torch()
     dev = x.device
     n = x.numel()
-    S = default_subblock(C) if S is None else S
+    S = default_subblock(C, dev_cb) if S is None else S
     if out is None:
         out = torch.empty(max(16, max_encoded_bytes(n, C, max_len)), dtype=torch.uint8, device=dev)
     nch = num_chunks(n, C)
@@ -404,7 +434,7 @@ def ecc_encode_static(x, dev_cb, C: int = 16384, S: int | None = None, max_len: 
     torch = _torch()
     dev = x.device
     n = x.numel()
-    S = default_subblock(C) if S is None else S
+    S = default_subblock(C, dev_cb) if S is None else S
     if out is None:
         out = torch.empty(max(16, max_encoded_bytes(n, C, max_len)), dtype=torch.uint8, device=dev)
     if chunk_off is None:

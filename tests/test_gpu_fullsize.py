@@ -64,7 +64,6 @@ def test_zero_spike_full_size():
     device histogram) against base QLC and the Huffman code of the same
     PMF."""
     n = 1 << 28
-    S = ecc.default_subblock(C)
     x = dev_zero_spike(n, (3, 0))
     xh = x.cpu().numpy()
     count = device_counts(x)
@@ -79,6 +78,7 @@ def test_zero_spike_full_size():
     bits = {}
     g = np.random.default_rng(3)
     for name, cbb, ocb in books:
+        S = ecc.default_subblock(C, cbb)  # each codebook at the size the benchmark codes it with
         enc = round_trip(x, cbb, S)
         bits[name] = int(u64(enc.total_bits)[0])
         assert bits[name] == oracle.code_bits(count, ocb["len"])
@@ -96,7 +96,6 @@ def test_single_stage_huffman_full_size():
     Huffman codebook, applied to 64 fresh shards; per shard the fixed code,
     the shard's own Huffman code and the Shannon bound, and D(shard || avg)."""
     n = 1 << 22
-    S = ecc.default_subblock(C)
     pooled = torch.zeros(256, dtype=torch.int64, device="cuda")
     for i in range(16):
         x, _ = dev_gauss(n, (2, i))
@@ -108,6 +107,7 @@ def test_single_stage_huffman_full_size():
     ocb = oracle.huffman_codebook(weights)
     dcb = ecc.to_device(cbb)
     max_len = int(ecc.codebook_view(cbb)["max_len"])
+    S = ecc.default_subblock(C, cbb)
     g = np.random.default_rng(2)
     for i in range(64):
         x, sigma = dev_gauss(n, (2, 100 + i))
@@ -156,7 +156,7 @@ def test_batched_full_size():
              (ecc.huff_build_canonical(c3 + np.uint64(1)), oracle.huffman_codebook(c3 + np.uint64(1)))]
     dcbs = [ecc.to_device(b) for b, _ in books]
     max_len = [int(ecc.codebook_view(b)["max_len"]) for b, _ in books]
-    S = ecc.default_subblock(C)
+    Sb = [ecc.default_subblock(C, b) for b, _ in books]
     total = sum(s for s, _, _ in plan)
     xin = torch.empty(total + 16 * len(plan), dtype=torch.uint8, device="cuda")
     items, views, off = [], [], 0
@@ -166,10 +166,10 @@ def test_batched_full_size():
         cap = ecc.max_encoded_bytes(size, C, max_len[tag])
         items.append({"in": x, "out": torch.empty(cap, dtype=torch.uint8, device="cuda"), "n": size, "cap": cap,
                       "chunk_off": torch.empty(ecc.num_chunks(size, C) + 1, dtype=torch.int64, device="cuda"),
-                      "sub_bits": torch.empty(ecc.num_subblocks(size, S), dtype=torch.int16, device="cuda"),
+                      "sub_bits": torch.empty(ecc.num_subblocks(size, Sb[tag]), dtype=torch.int16, device="cuda"),
                       "total_bits": torch.empty(1, dtype=torch.int64, device="cuda"), "cb": dcbs[tag],
                       "status": torch.full((1,), 99, dtype=torch.int32, device="cuda"),
-                      "t_done_ns": torch.zeros(1, dtype=torch.int64, device="cuda"), "C": C, "S": S})
+                      "t_done_ns": torch.zeros(1, dtype=torch.int64, device="cuda"), "C": C, "S": Sb[tag]})
         views.append(tag)
         off += (size + 15) // 16 * 16
     descs = ecc.make_descs(items)
@@ -202,5 +202,5 @@ def test_batched_full_size():
         assert int(u64(it["total_bits"])[0]) == oracle.code_bits(oracle.histogram(xh), ocb["len"])
         nch = ecc.num_chunks(it["n"], C)
         enc = ecc.Encoded(it["out"], it["chunk_off"], it["sub_bits"], it["total_bits"], it["status"],
-                          it["n"], C, S)
-        sampled_parity(xh, enc, ocb, S, sorted({0, nch - 1, int(g.integers(0, nch))}))
+                          it["n"], C, it["S"])
+        sampled_parity(xh, enc, ocb, it["S"], sorted({0, nch - 1, int(g.integers(0, nch))}))

@@ -614,7 +614,6 @@ def test_gradient_gib_sampled_parity():
     round trip on the device."""
     n = 1 << 30
     C = 16384
-    S = ecc.default_subblock(C)
     x = dev_grad(n, (4, 0))
     warm = [oracle.histogram(grad_warmup(i, 1 << 22)) for i in range(2)]
     pooled = oracle.fixed_codebook_weights(warm)
@@ -627,6 +626,7 @@ def test_gradient_gib_sampled_parity():
     for cbb, ocb in [(ecc.qlc_build_tables(pooled), oracle.qlc_codebook(pooled)),
                      (ecc.huff_build_canonical(pooled), oracle.huffman_codebook(pooled))]:
         dcb = ecc.to_device(cbb)
+        S = ecc.default_subblock(C, cbb)  # the benchmark's size for this codebook
         enc = ecc.ecc_encode(x, dcb, C, S, max_len=int(ecc.codebook_view(cbb)["max_len"]))
         out, st = ecc.ecc_decode(enc, dcb)
         torch.cuda.synchronize()
