@@ -398,8 +398,9 @@ ecc_status bf16_escape_encode(const uint16_t *in, size_t n, const uint8_t top7[7
                               uint64_t *total_bits, void *ws, size_t ws_bytes, uint32_t *status, void *stream);
 
 /*
- * bf16_escape_decode -- the inverse: out (device uint16[n]) from the
- * container written with the same table, C and S.  Device errors:
+ * bf16_escape_decode -- the inverse: out (device uint16[n], 16-byte
+ * aligned) from the container written with the same table, C and S; in
+ * (the payload) 16-byte aligned.  Device errors:
  * ECC_ERR_CORRUPT (offsets, a sub-block whose bit count differs from
  * sub_bits, 000 followed by a table exponent, a chunk whose padded size or
  * zero padding is wrong); nothing is read outside each chunk's payload.

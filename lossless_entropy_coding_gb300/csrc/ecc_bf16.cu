@@ -14,7 +14,8 @@
 // and tile; block scan of the code lengths; codes packed into a zeroed shared
 // stage; chunk offsets by decoupled look-back; the stage written out
 // byte-swapped with 16-byte stores); the decoder (a warp per chunk, a lane per
-// sub-block, codes read through a 64-bit window).
+// sub-block, codes read through a three-word window, eight values a 16-byte
+// store).
 
 #include <algorithm>
 #include <cmath>
@@ -237,17 +238,36 @@ struct BfDecParams {
     uint64_t n_chunks;
 };
 
-// big-endian 32-bit word at byte offset b of the chunk [c0, c1) (zeros past it)
-__device__ __forceinline__ uint32_t bf_word(const uint8_t *in, uint64_t c0, uint64_t c1, uint64_t b)
+// One value of a lane's stream: the window (hi, lo, nx) holds the next 96
+// bits from bit o of hi (o < 32); w is the stream's word after nx, loaded
+// ahead.  A value takes 11 or 19 bits, so the window moves by at most one
+// word.  tA/tB: the table's exponents 0-3 and 4-6, one a byte.  Returns the
+// BF16 value; sets bad for 000 followed by a table exponent.
+__device__ __forceinline__ uint32_t bf_step(uint32_t &hi, uint32_t &lo, uint32_t &nx, uint32_t &o, uint32_t &wi,
+                                            uint32_t w, uint32_t tA, uint32_t tB, const uint8_t *rank, bool &bad)
 {
-    if (c0 + b + 4 <= c1)
-        return bswap32(*reinterpret_cast<const uint32_t *>(in + c0 + b));
-    uint32_t w = 0;
-    for (int k = 0; k < 4; ++k)
-        w = (w << 8) | (c0 + b + k < c1 ? (uint32_t)in[c0 + b + k] : 0u);
-    return w;
+    const uint32_t top = __funnelshift_l(lo, hi, o);
+    const uint32_t code = top >> 29;
+    const bool esc = code == 0;
+    const uint32_t et = __byte_perm(tA, tB, (code - 1u) & 7u) & 0xFFu; // code - 1 = 7 for an escape (unused byte)
+    const uint32_t e = esc ? (top >> 21) & 0xFFu : et;
+    const uint32_t tail = esc ? (top >> 13) & 0xFFu : (top >> 21) & 0xFFu;
+    if (esc)
+        bad |= rank[e] != 0; // a table exponent has a short code
+    o += esc ? 19u : 11u;
+    const bool adv = o >= 32u;
+    hi = adv ? lo : hi;
+    lo = adv ? nx : lo;
+    nx = adv ? w : nx;
+    wi += adv ? 1u : 0u;
+    o &= 31u;
+    return ((tail & 0x80u) << 8) | (e << 7) | (tail & 0x7Fu);
 }
 
+// A warp per chunk, a lane per sub-block (rounds of 32 sub-blocks): each lane
+// decodes its sub-block from a three-word window over the chunk's words
+// (read through the read-only path, clamped to the chunk), eight values at a
+// time, written as one 16-byte store.
 __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
 {
     __shared__ uint8_t rank[256];
@@ -258,6 +278,9 @@ __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
     if (tid < 7)
         rank[p.tab.top[tid]] = (uint8_t)(tid + 1);
     __syncthreads();
+    const uint32_t tA = p.tab.top[0] | (uint32_t)p.tab.top[1] << 8 | (uint32_t)p.tab.top[2] << 16 |
+                        (uint32_t)p.tab.top[3] << 24;
+    const uint32_t tB = p.tab.top[4] | (uint32_t)p.tab.top[5] << 8 | (uint32_t)p.tab.top[6] << 16;
     const uint64_t gw = (uint64_t)blockIdx.x * (blockDim.x / 32) + (tid >> 5);
     const uint64_t nw = (uint64_t)gridDim.x * (blockDim.x / 32);
     const uint32_t s_shift = 31u - __clz(p.S);
@@ -266,12 +289,16 @@ __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
         const uint64_t base = c * p.C;
         const uint32_t L = (uint32_t)min((uint64_t)p.C, p.n - base);
         const uint32_t nsub = (L + p.S - 1) >> s_shift;
-        bool bad = c1 < c0 || c1 > p.in_bytes || (c0 & 15) || (c1 & 15) || (c == 0 && c0 != 0);
+        // a chunk of at least one value holds at least 16 bytes
+        bool bad = c1 < c0 + 16 || c1 > p.in_bytes || (c0 & 15) || (c1 & 15) || (c == 0 && c0 != 0);
         if (__any_sync(~0u, bad)) {
             if (lane == 0)
                 set_status(p.status, ECC_ERR_CORRUPT);
             continue;
         }
+        const uint32_t *words = reinterpret_cast<const uint32_t *>(p.in + c0);
+        const uint32_t wlast = (uint32_t)((c1 - c0) / 4) - 1u;
+        auto word = [&](uint32_t k) { return bswap32(__ldg(words + min(k, wlast))); };
         uint64_t run = 0; // bits of the sub-blocks before this round
         for (uint32_t r0 = 0; r0 < nsub; r0 += 32) {
             const uint32_t j = r0 + lane;
@@ -283,42 +310,50 @@ __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
                 if (lane >= o)
                     incl += y;
             }
-            uint64_t pos = run + incl - sb; // bit offset in the chunk
-            const uint64_t start = pos;
-            if (j < nsub) {
-                const uint32_t v0 = j << s_shift, v1 = min(v0 + p.S, L);
-                for (uint32_t v = v0; v < v1; ++v) {
-                    const uint64_t b = (pos >> 5) * 4;
-                    const uint64_t win = ((uint64_t)bf_word(p.in, c0, c1, b) << 32 | bf_word(p.in, c0, c1, b + 4))
-                                         << (pos & 31);
-                    const uint32_t top = (uint32_t)(win >> 32);
-                    const uint32_t code = top >> 29;
-                    uint32_t e, tail;
-                    if (code) {
-                        e = p.tab.top[code - 1];
-                        tail = (top >> 21) & 0xFFu;
-                        pos += 11;
-                    } else {
-                        e = (top >> 21) & 0xFFu;
-                        tail = (top >> 13) & 0xFFu;
-                        bad |= rank[e] != 0; // a table exponent has a short code
-                        pos += 19;
-                    }
-                    p.out[base + v] = (uint16_t)(((tail & 0x80u) << 8) | (e << 7) | (tail & 0x7Fu));
-                }
-                bad |= pos - start != sb;
-            }
+            const uint64_t start = run + incl - sb; // bit offset in the chunk
             run += __shfl_sync(~0u, incl, 31);
+            if (j >= nsub)
+                continue;
+            if (start + sb > (uint64_t)(wlast + 1u) * 32u) { // more bits than the chunk holds
+                bad = true;
+                continue;
+            }
+            const uint32_t v0 = j << s_shift, v1 = min(v0 + p.S, L);
+            uint32_t wi = (uint32_t)(start >> 5), o = (uint32_t)start & 31u;
+            uint32_t hi = word(wi), lo = word(wi + 1), nx = word(wi + 2);
+            wi += 3; // the next word to load
+            uint16_t *dst = p.out + base;
+            uint32_t v = v0;
+            for (; v + 8 <= v1; v += 8) { // p.out + base + v is 16-byte aligned (C, S multiples of 8)
+                uint32_t q[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t a = bf_step(hi, lo, nx, o, wi, word(wi), tA, tB, rank, bad);
+                    const uint32_t b = bf_step(hi, lo, nx, o, wi, word(wi), tA, tB, rank, bad);
+                    q[h] = a | b << 16;
+                }
+#ifdef ECC_CHECKED
+                if (base + v + 8 > p.n) {
+                    set_status(p.status, ECC_ERR_CHECK);
+                    break;
+                }
+#endif
+                *reinterpret_cast<uint4 *>(dst + v) = make_uint4(q[0], q[1], q[2], q[3]);
+            }
+            for (; v < v1; ++v)
+                dst[v] = (uint16_t)bf_step(hi, lo, nx, o, wi, word(wi), tA, tB, rank, bad);
+            // consumed bits: (words loaded - 3) * 32 + o
+            bad |= (uint64_t)(wi - 3u) * 32u + o - start != sb;
         }
         // the chunk ends at its padded size, and the padding is zero
         if (lane == 0) {
             bad |= ((run + 127) / 128) * 16 != c1 - c0;
             if (!bad) {
-                uint64_t wi = run >> 5;
+                uint64_t wk = run >> 5;
                 if (run & 31)
-                    bad |= (bf_word(p.in, c0, c1, (wi++) * 4) << (run & 31)) != 0;
-                for (; wi < (c1 - c0) / 4; ++wi)
-                    bad |= bf_word(p.in, c0, c1, wi * 4) != 0;
+                    bad |= (word((uint32_t)(wk++)) << (run & 31)) != 0;
+                for (; wk <= wlast; ++wk)
+                    bad |= word((uint32_t)wk) != 0;
             }
         }
         if (__any_sync(~0u, bad) && lane == 0)
@@ -462,7 +497,7 @@ ecc_status bf16_escape_decode(const uint8_t *in, size_t in_bytes, const uint64_t
 {
     if (!top7 || !bf_table_ok(top7) || !status || !chunk_off || !valid_sizes(C, S) || C > kBfMaxC)
         return ECC_ERR_ARG;
-    if (n && (!in || !out || !sub_bits || !aligned16(in)))
+    if (n && (!in || !out || !sub_bits || !aligned16(in) || !aligned16(out)))
         return ECC_ERR_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess)

@@ -98,3 +98,17 @@ def test_bf16_corruption_is_flagged():
     _, st = ecc.bf16_escape_decode(one, top)
     torch.cuda.synchronize()
     assert int(st.item()) == ecc.ERR_CORRUPT
+
+
+def test_decode_needs_aligned_output():
+    """The decoder writes eight values at a time with 16-byte stores: an
+    output that is not 16-byte aligned is a host error (nothing launched)."""
+    xh = np_bf16_gauss(4096, (9, 3), 0.02)
+    top = oracle.bf16_top7_from_sigma(0.02)
+    enc = ecc.bf16_escape_encode(_dev(xh), top, 4096, 64)
+    out = torch.empty(4096 + 8, dtype=torch.int16, device="cuda")
+    with pytest.raises(ecc.EccError):
+        ecc.bf16_escape_decode(enc, top, out=out[1:])
+    y, st = ecc.bf16_escape_decode(enc, top, out=out[8:])
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and (y[:4096].cpu().numpy().view(np.uint16) == xh).all()
