@@ -2605,11 +2605,10 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables 
 // piece starts at the sum of the chunk's sub_bits before it; its bytes,
 // widened to 16-byte boundaries of the chunk, are staged by one bulk copy
 // when they fit.  The piece that ends the chunk also checks the chunk's size
-// and zero padding.  next_c / next_piece (if valid) is prefetched into L2.
+// and zero padding.
 template <int R, bool kQlc>
 __device__ __forceinline__ void decode_piece(const DecJob &job, const DecTables &T, WarpStage &ws, uint64_t c,
-                                             uint32_t piece, uint32_t pshift, uint64_t next_c, uint32_t next_piece,
-                                             uint64_t n_chunks)
+                                             uint32_t piece, uint32_t pshift)
 {
     const uint16_t *dec = T.dec;
     const LongTable &lt = *T.lt;
@@ -2632,17 +2631,8 @@ __device__ __forceinline__ void decode_piece(const DecJob &job, const DecTables 
         return;
     }
     const uint32_t bytes = (uint32_t)(b1 - b0);
-    if (lane == 0 && next_c < n_chunks) { // the next piece's share of its chunk, roughly
-        uint64_t n0, n1;
-        if (chunk_range_ok(job, next_c, n0, n1)) {
-            const uint64_t nbytes = n1 - n0;
-            const uint64_t lo = ((nbytes * next_piece) >> pshift) & ~15ull;
-            const uint64_t e = (((nbytes * (next_piece + 1)) >> pshift) + 15) & ~15ull;
-            const uint64_t hi = e < nbytes ? e : nbytes;
-            if (hi > lo)
-                prefetch_l2(job.in + n0 + lo, (uint32_t)(hi - lo));
-        }
-    }
+    // (no L2 prefetch of the next piece: estimated from the chunk's size, it
+    // fetched about a sixth of the payload twice and saved no time)
     // the chunk's bits before the piece
     uint32_t carry0 = 0;
     for (uint32_t k = (uint32_t)lane; k < g_begin; k += 32)

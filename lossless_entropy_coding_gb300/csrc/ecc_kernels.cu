@@ -416,7 +416,7 @@ __global__ void __maxnreg__(R >= 4 ? 136 : 96) decode_kernel(DecParams p)
     // The warps of a CTA claim its chunks one at a time, so a warp that
     // drew chunks with many long codes does not hold up the CTA's end; a
     // warp claims its next chunk before decoding the current one, so that
-    // the next one's L2 prefetch starts early.
+    // (whole chunks) the next one's L2 prefetch starts early.
     auto claim = [&]() -> uint64_t {
         uint32_t k = 0;
         if (lane == 0)
@@ -431,8 +431,7 @@ __global__ void __maxnreg__(R >= 4 ? 136 : 96) decode_kernel(DecParams p)
         if constexpr (kPieces) {
             while (c < n_items) {
                 const uint64_t nc = claim();
-                decode_piece<R, true>(p.job, T, ws, c >> ps, (uint32_t)c & pm, ps, nc >> ps, (uint32_t)nc & pm,
-                                      p.n_chunks);
+                decode_piece<R, true>(p.job, T, ws, c >> ps, (uint32_t)c & pm, ps);
                 c = nc;
             }
         } else {
@@ -449,8 +448,7 @@ __global__ void __maxnreg__(R >= 4 ? 136 : 96) decode_kernel(DecParams p)
         if constexpr (kPieces) {
             while (c < n_items) {
                 const uint64_t nc = claim();
-                decode_piece<R, false>(p.job, T, ws, c >> ps, (uint32_t)c & pm, ps, nc >> ps, (uint32_t)nc & pm,
-                                       p.n_chunks);
+                decode_piece<R, false>(p.job, T, ws, c >> ps, (uint32_t)c & pm, ps);
                 c = nc;
             }
         } else {
