@@ -120,6 +120,50 @@ __global__ void __maxnreg__(96) encode_batched_ws_kernel(uint8_t *ws, uint64_t *
     encode_ws_body<true>(none, 0, nullptr, bt, h->ws_slot_bytes, h->max_C, kWaitLimitNs);
 }
 
+// The deferred pass of the many-tensor encoder: every warp scans 32
+// look-back words (one per chunk position) at a time and codes the chunks
+// the encoder marked (long codes), then counts their segments toward the
+// tensor's completion stamp as the encoder would have.
+__global__ void __launch_bounds__(256) encode_batched_deferred_kernel(uint8_t *ws)
+{
+    const BatchHeader *h = reinterpret_cast<const BatchHeader *>(ws);
+    const uint64_t *item = reinterpret_cast<const uint64_t *>(ws + h->item_off);
+    const ecc_desc *descs = reinterpret_cast<const ecc_desc *>(ws + h->desc_off);
+    uint64_t *flags = reinterpret_cast<uint64_t *>(ws + h->flags_off);
+    uint32_t *done = reinterpret_cast<uint32_t *>(ws + h->done_off);
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t total = h->total_chunks;
+    const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t b = w0 * 32; b < total; b += nw * 32) {
+        const uint64_t i = b + lane;
+        unsigned m = __ballot_sync(~0u, i < total && is_deferred(flags[i]));
+        while (m) {
+            const uint64_t pos = b + (uint64_t)(__ffs(m) - 1);
+            m &= m - 1;
+            const uint64_t it = item[pos];
+            if (it == kNoItem)
+                continue;
+            const uint32_t t = (uint32_t)(it >> 32);
+            const uint64_t c = it & 0xFFFFFFFFull;
+            const ecc_desc &d = descs[t];
+            const EncJob job{d.in, d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits, d.total_bits,
+                             flags + (pos - c), d.status};
+            code_deferred_unit(job, c, 1, chunks_of(d));
+            if (d.t_done_ns) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t nseg = d.C / seg_symbols(d.C, d.S);
+                    const uint32_t want = nseg * (uint32_t)chunks_of(d);
+                    if (atomicAdd(done + t, nseg) + nseg == want)
+                        *d.t_done_ns = globaltimer();
+                }
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void stamp_done(const ecc_desc &d, uint32_t *done, uint32_t k)
 {
     if (!d.t_done_ns)
@@ -467,6 +511,11 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
         if (occ_ws > 0) {
             const uint64_t grid = std::min<uint64_t>((uint64_t)occ_ws * sms, P.n_items);
             encode_batched_ws_kernel<<<(unsigned)grid, kEncThreadsWS, ws_smem, st>>>((uint8_t *)ws, t_start);
+            if ((e = launch_status(cudaGetLastError())) != ECC_OK)
+                return e;
+            // the chunks it left to the deferred pass (long codes)
+            const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((P.n_items + 255) / 256, (uint64_t)sms * 8));
+            encode_batched_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>((uint8_t *)ws);
             return launch_status(cudaGetLastError());
         }
         const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)P.max_C + kStageLead + P.stage;

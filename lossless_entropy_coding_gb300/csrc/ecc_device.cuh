@@ -20,7 +20,8 @@ constexpr int kTile = kEncThreads * kSymPerThread;    // symbols per tile
 constexpr uint32_t kLutRows = 256;                    // byte values
 constexpr uint64_t kFlagAggregate = 1ull << 62;       // look-back states
 constexpr uint64_t kFlagPrefix = 2ull << 62;
-constexpr uint64_t kValueMask = (1ull << 62) - 1;
+constexpr uint64_t kFlagDeferred = 1ull << 61;        // with kFlagPrefix: the deferred pass codes the unit's payload
+constexpr uint64_t kValueMask = (1ull << 61) - 1;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;      // bounded waits: 1 s
 
 __host__ __device__ constexpr uint32_t pad16(uint32_t b) { return (b + 15u) & ~15u; }
@@ -823,6 +824,26 @@ static __device__ __noinline__ void encode_chunk_warp(const EncJob &job, uint64_
     }
 }
 
+// The deferred pass: units an encoder could not stage (long codes) were
+// sized, their offsets resolved and their flag word marked kFlagPrefix |
+// kFlagDeferred; here one warp codes each chunk of such a unit straight into
+// the output at chunk_off (the encoder checked the capacity before marking).
+// Unit u holds chunks [u * G, u * G + G).  Returns the chunks it coded.
+__device__ __forceinline__ uint32_t code_deferred_unit(const EncJob &job, uint64_t u, uint32_t G, uint64_t n_chunks)
+{
+    uint32_t k = 0;
+    for (uint64_t c = u * G; c < n_chunks && c < (u + 1) * G; ++c, ++k) {
+        const uint64_t o0 = job.chunk_off[c], o1 = job.chunk_off[c + 1];
+        encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + o0), (uint32_t)((o1 - o0) / 4u));
+    }
+    return k;
+}
+
+__device__ __forceinline__ bool is_deferred(uint64_t f)
+{
+    return (f & (3ull << 62)) == kFlagPrefix && (f & kFlagDeferred);
+}
+
 // Bulk-copy the whole 16-byte groups of the input of chunks c .. c + g - 1
 // into buf (thread 0); completion arrives on bar.  The last chunk's trailing
 // bytes (fewer than 16) are read from global memory by the thread that owns
@@ -1450,16 +1471,13 @@ __device__ __forceinline__ void encode_ws_body(const EncJob &single, uint64_t n_
                 sh.out_prefix[b] = prefix;
                 sh.out_copy[b] = copy ? 1u : 0u;
             }
-            if ((fl & 1u) && write) { // a segment outgrew its region: code the unit straight into the output
-                if (kGrouped)
-                    for (uint32_t i = 0; i < gc; ++i)
-                        encode_chunk_warp(job, c0 + i,
-                                          reinterpret_cast<uint32_t *>(job.out + prefix + sh.chunk_rel[b][i]),
-                                          (sh.chunk_rel[b][i + 1] - sh.chunk_rel[b][i]) / 4u);
-                else
-                    encode_chunk_warp(job, u, reinterpret_cast<uint32_t *>(job.out + prefix), (uint32_t)(bytes / 4));
-            }
-            if (kBatched && s.t_done && !copy) {
+            // a segment outgrew its region (long codes): the unit is left to
+            // the deferred pass (a warp a unit over the whole GPU, after this
+            // kernel), so this warp's pipeline does not stall on it
+            const bool deferred = (fl & 1u) && write;
+            if (deferred && lane == 0)
+                st_relaxed(job.flags + u, kFlagPrefix | kFlagDeferred | ((prefix + bytes) & kValueMask));
+            if (kBatched && s.t_done && !copy && !deferred) {
                 // completion counts one per segment: the copying warps count
                 // their own, else this warp counts the chunk's
                 __threadfence();

@@ -560,6 +560,37 @@ int occupancy(const void *kernel, int threads, size_t smem)
     return nb;
 }
 
+// The deferred pass (code_deferred_unit): every warp scans 32 look-back
+// words at a time and codes the marked units among them.  A launch over a
+// tensor with no marked unit only reads its look-back words.
+__global__ void __launch_bounds__(256) encode_deferred_kernel(EncJob job, uint64_t n_chunks, uint32_t G)
+{
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t n_units = (n_chunks + G - 1) / G;
+    const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t b = w0 * 32; b < n_units; b += nw * 32) {
+        const uint64_t u = b + lane;
+        unsigned m = __ballot_sync(~0u, u < n_units && is_deferred(job.flags[u]));
+        while (m) {
+            const int i = __ffs(m) - 1;
+            m &= m - 1;
+            code_deferred_unit(job, b + (uint64_t)i, G, n_chunks);
+        }
+    }
+}
+
+ecc_status launch_deferred(const EncJob &job, uint64_t n_chunks, uint32_t G, cudaStream_t st)
+{
+    const int sms = sm_count();
+    if (sms <= 0)
+        return ECC_ERR_CUDA;
+    const uint64_t n_units = (n_chunks + G - 1) / G;
+    const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((n_units + 255) / 256, (uint64_t)sms * 8));
+    encode_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>(job, n_chunks, G);
+    return launch_status(cudaGetLastError());
+}
+
 } // namespace ecc
 
 using namespace ecc;
@@ -644,9 +675,11 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
             return launch_status(cudaGetLastError());
         }
     }
-    // chunks of at most 16384 symbols: the unit encoder (ecc_units.cu)
-    if (launch_unit_encoder(p.job, ticket, st) == ECC_OK)
-        return ECC_OK;
+    // chunks of at most 16384 symbols: the unit encoder (ecc_units.cu), then
+    // the deferred pass over the units it could not stage
+    uint32_t unit_chunks = 1;
+    if (launch_unit_encoder(p.job, ticket, st, &unit_chunks) == ECC_OK)
+        return launch_deferred(p.job, n_chunks, unit_chunks, st);
     // a device where it cannot run: the warp-specialised kernel (two input
     // buffers, two stage slots of warp regions) when it fits, else the
     // single-slot kernel; chunks smaller than kGroupSyms symbols are coded in
@@ -667,7 +700,8 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
                 encode_ws_kernel<true><<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
             else
                 encode_ws_kernel<false><<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
-            return launch_status(cudaGetLastError());
+            const ecc_status e = launch_status(cudaGetLastError());
+            return e != ECC_OK ? e : launch_deferred(p.job, n_chunks, G, st);
         }
     }
     p.nbuf = enc_input_buffers(C);

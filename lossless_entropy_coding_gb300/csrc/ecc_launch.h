@@ -29,6 +29,7 @@ int sm_count();
 // memory limit on first use on the current device).
 int occupancy(const void *kernel, int threads, size_t smem);
 // The unit encoder for chunks of at most 16384 symbols (ecc_units.cu).
-ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st);
+// (unit_chunks: the chunks of a unit, for the deferred pass)
+ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st, uint32_t *unit_chunks);
 
 } // namespace ecc

@@ -34,9 +34,10 @@
 //    pack it, writes chunk_off and total_bits, finishes the words shared
 //    across warps and the chunks' zero padding, and stores the stage to the
 //    output with one cp.async.bulk shared -> global copy.
-// A unit whose payload outgrows the stage (long codes only) is coded by the
-// storer straight into the output, one chunk at a time, from the codebook in
-// global memory.
+// A unit whose payload outgrows the stage (long codes only) is sized and
+// placed like any other and marked in its look-back word; a second kernel
+// (the deferred pass) codes it, a warp a unit, from the codebook in global
+// memory.
 
 #include <algorithm>
 
@@ -795,13 +796,10 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
             break;
         }
         if (ubytes > p.stage_bytes) {
-            // the unit outgrew the stage: code its chunks straight into the output
-            if (write)
-                for (uint32_t j = 0; j < G && c0 + j < n_chunks; ++j) {
-                    const uint32_t jb = __shfl_sync(~0u, lay.base, j * wpc);
-                    const uint32_t je = __shfl_sync(~0u, lay.Y, j * wpc + wpc - 1u);
-                    encode_chunk_warp(job, c0 + j, reinterpret_cast<uint32_t *>(job.out + prefix + jb), (je - jb) / 4u);
-                }
+            // the unit outgrew the stage (long codes): left to the deferred
+            // pass, a warp a unit over the whole GPU after this kernel
+            if (write && lane == 0)
+                st_relaxed(job.flags + u, kFlagPrefix | kFlagDeferred | ((prefix + ubytes) & kValueMask));
         } else if (write) {
             const uint32_t st = st0 + slot * p.stage_bytes;
             // words shared across warps: warp `lane`'s first word takes the
@@ -904,7 +902,7 @@ uint32_t unit_stage_bytes()
 // Launch the unit encoder for chunks of C <= kUSyms symbols (the prologue
 // has cleared the flags, the ticket and the outputs).  Returns ECC_ERR_CUDA
 // if it cannot run on this device.
-ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st)
+ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st, uint32_t *unit_chunks)
 {
     UnitParams p;
     p.job = job;
@@ -928,6 +926,7 @@ ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t
         encode_unit_kernel<true><<<(unsigned)grid, kUThreads, smem, st>>>(p);
     else
         encode_unit_kernel<false><<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    *unit_chunks = kUSyms / job.C;
     return launch_status(cudaGetLastError());
 }
 
