@@ -120,10 +120,11 @@ __global__ void __maxnreg__(96) encode_batched_ws_kernel(uint8_t *ws, uint64_t *
     encode_ws_body<true>(none, 0, nullptr, bt, h->ws_slot_bytes, h->max_C, kWaitLimitNs);
 }
 
-// The deferred pass of the many-tensor encoder: every warp scans 32
-// look-back words (one per chunk position) at a time and codes the chunks
-// the encoder marked (long codes), then counts their segments toward the
-// tensor's completion stamp as the encoder would have.
+// The deferred pass of the many-tensor encoder: warp w takes chunk positions
+// w, w + W, ... (the marked chunks come in runs: the tensors are grouped by
+// codebook, and long codes are a codebook's), codes each chunk the encoder
+// marked (long codes), then counts its segments toward the tensor's
+// completion stamp as the encoder would have.
 __global__ void __launch_bounds__(256) encode_batched_deferred_kernel(uint8_t *ws)
 {
     const BatchHeader *h = reinterpret_cast<const BatchHeader *>(ws);
@@ -135,12 +136,9 @@ __global__ void __launch_bounds__(256) encode_batched_deferred_kernel(uint8_t *w
     const uint64_t total = h->total_chunks;
     const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    for (uint64_t b = w0 * 32; b < total; b += nw * 32) {
-        const uint64_t i = b + lane;
-        unsigned m = __ballot_sync(~0u, i < total && is_deferred(flags[i]));
-        while (m) {
-            const uint64_t pos = b + (uint64_t)(__ffs(m) - 1);
-            m &= m - 1;
+    for (uint64_t pos = w0; pos < total; pos += nw) {
+        const uint64_t f = lane == 0 ? flags[pos] : 0;
+        if (__shfl_sync(~0u, is_deferred(f) ? 1u : 0u, 0)) {
             const uint64_t it = item[pos];
             if (it == kNoItem)
                 continue;
@@ -514,7 +512,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
             if ((e = launch_status(cudaGetLastError())) != ECC_OK)
                 return e;
             // the chunks it left to the deferred pass (long codes)
-            const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((P.n_items + 255) / 256, (uint64_t)sms * 8));
+            const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((P.n_items + 7) / 8, (uint64_t)sms * 8));
             encode_batched_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>((uint8_t *)ws);
             return launch_status(cudaGetLastError());
         }

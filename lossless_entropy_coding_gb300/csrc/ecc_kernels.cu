@@ -560,23 +560,20 @@ int occupancy(const void *kernel, int threads, size_t smem)
     return nb;
 }
 
-// The deferred pass (code_deferred_unit): every warp scans 32 look-back
-// words at a time and codes the marked units among them.  A launch over a
-// tensor with no marked unit only reads its look-back words.
+// The deferred pass (code_deferred_unit): warp w takes units w, w + W, ...
+// (marked units come in runs: the long codes of one part of a tensor), reads
+// each one's look-back word and codes it if marked.  A launch over a tensor
+// with no marked unit only reads its look-back words.
 __global__ void __launch_bounds__(256) encode_deferred_kernel(EncJob job, uint64_t n_chunks, uint32_t G)
 {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t n_units = (n_chunks + G - 1) / G;
     const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    for (uint64_t b = w0 * 32; b < n_units; b += nw * 32) {
-        const uint64_t u = b + lane;
-        unsigned m = __ballot_sync(~0u, u < n_units && is_deferred(job.flags[u]));
-        while (m) {
-            const int i = __ffs(m) - 1;
-            m &= m - 1;
-            code_deferred_unit(job, b + (uint64_t)i, G, n_chunks);
-        }
+    for (uint64_t u = w0; u < n_units; u += nw) {
+        const uint64_t f = lane == 0 ? job.flags[u] : 0;
+        if (__shfl_sync(~0u, is_deferred(f) ? 1u : 0u, 0))
+            code_deferred_unit(job, u, G, n_chunks);
     }
 }
 
@@ -586,7 +583,8 @@ ecc_status launch_deferred(const EncJob &job, uint64_t n_chunks, uint32_t G, cud
     if (sms <= 0)
         return ECC_ERR_CUDA;
     const uint64_t n_units = (n_chunks + G - 1) / G;
-    const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((n_units + 255) / 256, (uint64_t)sms * 8));
+    // a warp a unit, up to 8 CTAs of 8 warps an SM
+    const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((n_units + 7) / 8, (uint64_t)sms * 8));
     encode_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>(job, n_chunks, G);
     return launch_status(cudaGetLastError());
 }
