@@ -308,10 +308,13 @@ ecc_status huff_build_device(const uint64_t *count, uint64_t add, uint32_t max_l
  * chunk-offset look-back waited more than about a second).
  * Host errors: ECC_ERR_ARG (sizes, alignment, NULL, small workspace),
  * ECC_ERR_CUDA.  n = 0 writes chunk_off[0] = 0 and total_bits = 0.
- * Launches: chunks of at most 16384 symbols are coded and placed in one
- * kernel (decoupled look-back over chunks, or over groups of consecutive
- * chunks of 16384 symbols); larger chunks take a length pass, a scan of the
- * offsets and a coding kernel (ECC_ERR_CHECK if the two ever disagree).
+ * Launches (all on `stream`, after a prologue that clears the workspace):
+ * chunks of at most 16384 symbols are coded and placed by one kernel in
+ * units of 16384 symbols (decoupled look-back over units), followed by a
+ * deferred pass that codes the units whose codes were too long to stage
+ * (it only reads the look-back words when there are none); larger chunks
+ * take a length pass, a scan of the offsets and a coding kernel
+ * (ECC_ERR_CHECK if the two ever disagree).
  */
 ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S,
                       uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,
@@ -411,8 +414,8 @@ ecc_status bf16_escape_decode(const uint8_t *in, size_t in_bytes, const uint64_t
                               uint16_t *out, uint32_t *status, void *stream);
 
 /* ------------------------------------------------------------------------
- * Batched calls: many tensors, one kernel launch for encode and one for
- * decode (each tensor an independent container, each with its own codebook)
+ * Batched calls: many tensors, one call for encode and one for decode (each
+ * tensor an independent container, each with its own codebook)
  * ---------------------------------------------------------------------- */
 typedef struct ecc_desc {
     const uint8_t *in;     /* encode: symbols [n]; decode: payload [in_bytes] */
@@ -434,12 +437,16 @@ size_t ecc_batched_workspace_bytes(const ecc_desc *descs, uint32_t count);
 
 /*
  * ecc_encode_batched / ecc_decode_batched -- the calls above over `count`
- * tensors in one launch.  `descs` is a host array; the call copies it and a
+ * tensors in one coding launch over all of them (after a prologue; the
+ * encode adds the deferred pass for chunks whose codes were too long to
+ * stage, and a tensor's t_done_ns is stamped by whichever launch finishes
+ * its last chunk).  `descs` is a host array; the call copies it and a
  * chunk prefix table into `ws` with one asynchronous host-to-device copy,
  * so `descs` may be reused once the call returns.  Every tensor obeys the
  * rules of ecc_encode / ecc_decode; its errors go to its own status word.
  * Optionally `t_start_ns` (device word, may be NULL) receives %globaltimer
- * at kernel start, for per-tensor latency = t_done_ns - t_start_ns.
+ * at the coding kernel's start, for per-tensor latency = t_done_ns -
+ * t_start_ns.
  * Host errors: ECC_ERR_ARG (bad descriptor, small workspace), ECC_ERR_CUDA.
  */
 ecc_status ecc_encode_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t ws_bytes,
