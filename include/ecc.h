@@ -243,7 +243,8 @@ size_t ecc_num_subblocks(size_t n, uint32_t S);  /* ceil(n / S) */
 /* Payload bytes that always suffice: every symbol at max_len bits, every
  * chunk padded to 16 bytes. */
 size_t ecc_max_encoded_bytes(size_t n, uint32_t C, uint32_t max_len);
-/* Device workspace ecc_encode needs for n symbols in chunks of C. */
+/* Device workspace ecc_encode needs for n symbols in chunks of C: 256 bytes,
+ * 8 a chunk and, when C > 16384, 8 per 16384 symbols. */
 size_t ecc_encode_workspace_bytes(size_t n, uint32_t C);
 
 /* ------------------------------------------------------------------------
@@ -309,12 +310,13 @@ ecc_status huff_build_device(const uint64_t *count, uint64_t add, uint32_t max_l
  * Host errors: ECC_ERR_ARG (sizes, alignment, NULL, small workspace),
  * ECC_ERR_CUDA.  n = 0 writes chunk_off[0] = 0 and total_bits = 0.
  * Launches (all on `stream`, after a prologue that clears the workspace):
- * chunks of at most 16384 symbols are coded and placed by one kernel in
- * units of 16384 symbols (decoupled look-back over units), followed by a
- * deferred pass that codes the units whose codes were too long to stage
- * (it only reads the look-back words when there are none); larger chunks
- * take a length pass, a scan of the offsets and a coding kernel
- * (ECC_ERR_CHECK if the two ever disagree).
+ * one kernel codes and places the symbols in units of 16384 (a chunk,
+ * whole smaller chunks, or part of a larger chunk; decoupled look-back over
+ * units, or over chunks when a chunk spans units), followed by a deferred
+ * pass that codes the units (or chunks) whose codes were too long to stage
+ * (it only reads the look-back words when there are none).  On a device
+ * where that kernel cannot run, larger chunks take a length pass, a scan of
+ * the offsets and a coding kernel (ECC_ERR_CHECK if the two ever disagree).
  */
 ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint32_t C, uint32_t S,
                       uint8_t *out, size_t out_cap, uint64_t *chunk_off, uint16_t *sub_bits,
@@ -473,8 +475,9 @@ ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate
  * embedded in a framework whose allocator owns all device memory.  The pages
  * have no counterpart; this is a property of the library, not of the method.
  *   Arguments, outputs and errors are those of ecc_encode.  The scratch
- *   space (a ticket and one 64-bit look-back word per chunk) is a file-scope
- *   device array of ECC_STATIC_MAX_CHUNKS + 32 words (about 512 KiB) that
+ *   space (a ticket, one 64-bit look-back word per chunk and, for chunks of
+ *   more than 16384 symbols, one per 16384 symbols) is a file-scope device
+ *   array of 5 x ECC_STATIC_MAX_CHUNKS + 32 words (about 2.5 MiB) that
  *   every GPU loading the library holds until the process exits; the call
  *   allocates and frees nothing.  Inputs with more than ECC_STATIC_MAX_CHUNKS
  *   chunks (n > 65536 * C) are rejected with ECC_ERR_ARG.

@@ -834,6 +834,8 @@ __device__ __forceinline__ uint32_t code_deferred_unit(const EncJob &job, uint64
     uint32_t k = 0;
     for (uint64_t c = u * G; c < n_chunks && c < (u + 1) * G; ++c, ++k) {
         const uint64_t o0 = job.chunk_off[c], o1 = job.chunk_off[c + 1];
+        if (o0 > o1 || o1 > job.out_cap) // offsets not published (an error status is set)
+            continue;
         encode_chunk_warp(job, c, reinterpret_cast<uint32_t *>(job.out + o0), (uint32_t)((o1 - o0) / 4u));
     }
     return k;

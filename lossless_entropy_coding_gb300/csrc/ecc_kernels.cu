@@ -562,22 +562,33 @@ int occupancy(const void *kernel, int threads, size_t smem)
 
 // The deferred pass (code_deferred_unit): warp w takes units w, w + W, ...
 // (marked units come in runs: the long codes of one part of a tensor), reads
-// each one's look-back word and codes it if marked.  A launch over a tensor
-// with no marked unit only reads its look-back words.
-__global__ void __launch_bounds__(256) encode_deferred_kernel(EncJob job, uint64_t n_chunks, uint32_t G)
+// each one's look-back word and codes it if marked.  Chunks coded in parts
+// (marks != NULL: chunks of 2^mlog parts, n_parts in all) are also coded
+// when the mark word of the chunk (the word of its last part) is set and
+// the chunk's offsets are published within the output.  A launch over a
+// tensor with no marked unit only reads its look-back (and mark) words.
+__global__ void __launch_bounds__(256) encode_deferred_kernel(EncJob job, uint64_t n_chunks, uint32_t G,
+                                                               const uint64_t *marks, uint32_t mlog, uint64_t n_parts)
 {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t n_units = (n_chunks + G - 1) / G;
     const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
     for (uint64_t u = w0; u < n_units; u += nw) {
-        const uint64_t f = lane == 0 ? job.flags[u] : 0;
-        if (__shfl_sync(~0u, is_deferred(f) ? 1u : 0u, 0))
+        bool d = false;
+        if (lane == 0) {
+            const uint64_t f = job.flags[u];
+            d = is_deferred(f);
+            if (!d && marks && (marks[min(((u + 1) << mlog) - 1u, n_parts - 1u)] & 1u) && (f >> 62) == 2u)
+                d = job.chunk_off[u] <= job.chunk_off[u + 1] && job.chunk_off[u + 1] <= job.out_cap;
+        }
+        if (__shfl_sync(~0u, d ? 1u : 0u, 0))
             code_deferred_unit(job, u, G, n_chunks);
     }
 }
 
-ecc_status launch_deferred(const EncJob &job, uint64_t n_chunks, uint32_t G, cudaStream_t st)
+ecc_status launch_deferred(const EncJob &job, uint64_t n_chunks, uint32_t G, cudaStream_t st, const uint64_t *marks,
+                           uint32_t mlog, uint64_t n_parts)
 {
     const int sms = sm_count();
     if (sms <= 0)
@@ -585,7 +596,7 @@ ecc_status launch_deferred(const EncJob &job, uint64_t n_chunks, uint32_t G, cud
     const uint64_t n_units = (n_chunks + G - 1) / G;
     // a warp a unit, up to 8 CTAs of 8 warps an SM
     const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((n_units + 7) / 8, (uint64_t)sms * 8));
-    encode_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>(job, n_chunks, G);
+    encode_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>(job, n_chunks, G, marks, mlog, n_parts);
     return launch_status(cudaGetLastError());
 }
 
@@ -599,7 +610,10 @@ size_t ecc_encode_workspace_bytes(size_t n, uint32_t C)
 {
     if (!C)
         return 0;
-    return 256 + ecc_num_chunks(n, C) * sizeof(uint64_t);
+    // a ticket; a look-back word per chunk; for chunks of more than kGroupSyms
+    // symbols, also a word per kGroupSyms symbols (the unit encoder's units)
+    const uint64_t units = C > kGroupSyms ? ecc_num_chunks(n, kGroupSyms) : 0;
+    return 256 + (ecc_num_chunks(n, C) + units) * sizeof(uint64_t);
 }
 
 ecc_status e4m3_histogram(const uint8_t *in, size_t n, uint64_t *count, void *stream)
@@ -637,8 +651,9 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     uint32_t *ticket = (uint32_t *)ws;
     uint64_t *flags = (uint64_t *)((uint8_t *)ws + 256);
     {
-        const uint64_t nb = std::max<uint64_t>(1, std::min<uint64_t>((n_chunks + 255) / 256, 1024));
-        enc_prologue_kernel<<<(unsigned)nb, 256, 0, st>>>(flags, n_chunks, ticket, total_bits, chunk_off, status);
+        const uint64_t n_flags = (ecc_encode_workspace_bytes(n, C) - 256) / sizeof(uint64_t);
+        const uint64_t nb = std::max<uint64_t>(1, std::min<uint64_t>((n_flags + 255) / 256, 1024));
+        enc_prologue_kernel<<<(unsigned)nb, 256, 0, st>>>(flags, n_flags, ticket, total_bits, chunk_off, status);
         ecc_status e = launch_status(cudaGetLastError());
         if (e != ECC_OK || !n)
             return e;
@@ -653,7 +668,18 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
     const int sms = sm_count();
     if (sms <= 0)
         return ECC_ERR_CUDA;
-    // chunks of more than kGroupSyms symbols: length pass, scan, pass encoder
+    // the unit encoder (ecc_units.cu), then the deferred pass over the units
+    // (or split chunks) it could not stage
+    uint32_t unit_chunks = 1;
+    if (launch_unit_encoder(p.job, ticket, st, &unit_chunks) == ECC_OK) {
+        if (C <= kGroupSyms)
+            return launch_deferred(p.job, n_chunks, unit_chunks, st, nullptr, 0, 0);
+        // chunks coded in parts of kGroupSyms symbols: their mark words follow the chunks' words
+        return launch_deferred(p.job, n_chunks, 1, st, flags + n_chunks, 31u - __builtin_clz(C / kGroupSyms),
+                               ecc_num_chunks(n, kGroupSyms));
+    }
+    // a device where it cannot run.  Chunks of more than kGroupSyms symbols:
+    // length pass, scan, pass encoder
     if (C > kGroupSyms) {
         const uint32_t slot = enc_ws_slot_bytes(kGroupSyms, S);
         const size_t smem = enc_ws_smem_bytes(kGroupSyms, slot);
@@ -673,15 +699,10 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
             return launch_status(cudaGetLastError());
         }
     }
-    // chunks of at most 16384 symbols: the unit encoder (ecc_units.cu), then
-    // the deferred pass over the units it could not stage
-    uint32_t unit_chunks = 1;
-    if (launch_unit_encoder(p.job, ticket, st, &unit_chunks) == ECC_OK)
-        return launch_deferred(p.job, n_chunks, unit_chunks, st);
-    // a device where it cannot run: the warp-specialised kernel (two input
-    // buffers, two stage slots of warp regions) when it fits, else the
-    // single-slot kernel; chunks smaller than kGroupSyms symbols are coded in
-    // groups of consecutive chunks
+    // Smaller chunks: the warp-specialised kernel (two input buffers, two
+    // stage slots of warp regions) when it fits, else the single-slot kernel;
+    // chunks smaller than kGroupSyms symbols are coded in groups of
+    // consecutive chunks
     {
         const uint32_t G = enc_group_chunks(C, S);
         const uint32_t slot = G > 1 ? enc_ws_group_slot_bytes(C, S) : enc_ws_slot_bytes(C, S);
@@ -699,7 +720,7 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
             else
                 encode_ws_kernel<false><<<(unsigned)grid, kEncThreadsWS, smem, st>>>(q);
             const ecc_status e = launch_status(cudaGetLastError());
-            return e != ECC_OK ? e : launch_deferred(p.job, n_chunks, G, st);
+            return e != ECC_OK ? e : launch_deferred(p.job, n_chunks, G, st, nullptr, 0, 0);
         }
     }
     p.nbuf = enc_input_buffers(C);
@@ -784,11 +805,13 @@ ecc_status ecc_selftest_wait(uint64_t *flags, uint64_t chunk, uint64_t aggregate
 // ---------------------------------------------------------------- encode without allocation
 // ecc_encode_static: ecc_encode for callers that cannot allocate device
 // memory on their call path.  Its workspace (ticket + one look-back word per
-// chunk) is a file-scope device array instead of a caller buffer.
+// chunk, and one per 16384 symbols for larger chunks) is a file-scope
+// device array instead of a caller buffer.
 namespace ecc {
 
 constexpr uint64_t kStaticMaxChunks = ECC_STATIC_MAX_CHUNKS;
-constexpr uint64_t kStaticScratchWords = 256 / sizeof(uint64_t) + kStaticMaxChunks;
+// a ticket, a word per chunk and, for chunks of 65536 symbols, 4 per chunk
+constexpr uint64_t kStaticScratchWords = 256 / sizeof(uint64_t) + kStaticMaxChunks * (1 + 65536 / kGroupSyms);
 
 // Held by every GPU that loads the library until the process exits.  Host
 // code must not pass this name to a kernel: on the host it is only a

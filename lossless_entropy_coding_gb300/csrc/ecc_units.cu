@@ -1,7 +1,8 @@
-// ecc_units.cu -- the unit encoder: chunks of at most 16384 symbols coded in
-// units of 16384 consecutive symbols (one chunk of 16384, or 2..16 whole
-// smaller chunks), the codewords of each chunk packed at their final places
-// in a shared stage and the unit's payload written with one bulk copy.
+// ecc_units.cu -- the unit encoder: a tensor coded in units of 16384
+// consecutive symbols (one chunk of 16384, 2..16 whole smaller chunks, or a
+// quarter or half of a chunk of 65536 or 32768), the codewords of each chunk
+// packed at their final places in a shared stage and the unit's payload
+// written with one bulk copy.
 //
 // The coding follows "Quad Length Codes for Lossless Compression of e4m3",
 // section 2 "Codifica" (a table gives each byte its code; codes are written
@@ -38,6 +39,21 @@
 // placed like any other and marked in its look-back word; a second kernel
 // (the deferred pass) codes it, a warp a unit, from the codebook in global
 // memory.
+//
+// Chunks of more than 16384 symbols (split chunks) are coded a unit at a
+// time, units of one chunk running on different CTAs at once.  The look-back
+// runs over chunks: each unit adds its bit count to its chunk's word in
+// phase B, and the unit that completes the count publishes the chunk's
+// padded size there.  Inside a chunk a unit starts at any bit.  Its compute
+// warps pack it from bit 0 of the stage, without waiting for anything; its
+// storer learns the bit counts of the chunk's earlier units (published in
+// their phase B, a word a unit) and writes the stage shifted to that bit:
+// the words that are wholly the unit's (16-byte stores in the middle, single
+// words at either end).  Two consecutive units of a chunk share a word (the
+// earlier one's last bits, the later one's first): each ors its part into
+// the earlier unit's word with one atomic, and the one that comes second
+// writes the whole word.  The chunk's last unit pads the chunk; a chunk with
+// a unit too long to stage is marked and left whole to the deferred pass.
 
 #include <algorithm>
 
@@ -54,6 +70,29 @@ constexpr uint32_t kUThreads = kUCompute + 64;       // + the loader and the sto
 constexpr uint64_t kUEnd = ~0ull;                    // slot holds no unit: the pipeline ends
 constexpr uint32_t kULutBytes = kLutRows * kLutReplicas * 8u;
 constexpr uint32_t kUBarCompute = 1;                 // named barrier of the compute warps
+// what a unit holds: a whole chunk, whole smaller chunks, or part of a chunk
+constexpr int kUnitOne = 0, kUnitGroup = 1, kUnitSplit = 2;
+// Word of a unit of a split chunk that is not the chunk's last: kFlagAggregate
+// | bits once sized (bits 0..20); then the word the unit shares with the
+// next one (memory order, bits 21..52), or-ed in by both, with a bit for
+// each that has (kHandPrev: this unit, kHandNext: the next).  The word of a
+// chunk's last unit is the chunk's deferred mark (kMarkDeferred: some unit
+// of the chunk could not be staged).
+constexpr uint32_t kUBitsShift = 21;
+constexpr uint64_t kUBitsMask = (1ull << kUBitsShift) - 1;
+constexpr uint64_t kHandPrev = 1ull << 53, kHandNext = 1ull << 54;
+constexpr uint64_t kMarkDeferred = 1;
+// A split chunk's look-back word before it is published (state 0): the
+// units sized so far (<< kUCountShift) and their bits.  Every later change
+// of the word raises it (atomicMax): published size, inclusive prefix, the
+// deferred mark.
+constexpr uint32_t kUCountShift = 32;
+static_assert((uint64_t)kUSyms * ECC_MAX_CODE_LEN <= kUBitsMask, "a unit's bit count fits its field");
+// Stage bytes a unit of a split chunk needs: its words from bit 0, and 8
+// words more that the storer clears and reads past them when it shifts the
+// unit to its bit in the output (the shifted unit spans at most 4 words more,
+// and its 16-byte blocks are read whole).
+__host__ __device__ constexpr uint32_t split_stage_bytes(uint32_t bits) { return (bits + 31u) / 32u * 4u + 32u; }
 static_assert(kUWarps == 16, "phase B scans the warp totals over the lanes of one half-warp");
 
 // Shared state of the pipeline.  Slot s = k % 2 of the CTA's k-th unit holds
@@ -77,6 +116,8 @@ static_assert(sizeof(UPipe) % 16 == 0, "buffers stay 16-byte aligned");
 struct UnitParams {
     EncJob job;
     uint64_t n_units;
+    uint64_t *uflags;     // split chunks: a word per unit (job.flags holds a word per chunk)
+    uint32_t mlog;        // split chunks: log2 of the units of a chunk
     uint32_t *ticket;
     uint32_t stage_bytes; // payload bytes a stage holds (multiple of 16)
     uint64_t timeout_ns;
@@ -495,6 +536,28 @@ __device__ __forceinline__ uint64_t unit_lookback(const uint64_t *flags, uint64_
     return prefix;
 }
 
+// The word of a unit of a split chunk once its state is at least `state` (1:
+// the unit is sized, 2: its tail word is published), polled by the calling
+// lane; 0 after timeout_ns (ECC_ERR_TIMEOUT).
+__device__ __forceinline__ uint64_t unit_wait_word(const uint64_t *f, uint32_t state, uint64_t timeout_ns,
+                                                   uint32_t *status)
+{
+    uint64_t v = ld_relaxed(f);
+    if ((uint32_t)(v >> 62) >= state)
+        return v;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        __nanosleep(32);
+        v = ld_relaxed(f);
+        if ((uint32_t)(v >> 62) >= state)
+            return v;
+        if (globaltimer() - t0 > timeout_ns) {
+            set_status(status, ECC_ERR_TIMEOUT);
+            return 0;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- compute warps
 // The 4 bytes of w as two code pairs (v, q) from the lane's table replica;
 // qm tracks the smallest pair multiplier (0: some pair longer than 32 bits,
@@ -530,10 +593,11 @@ __device__ __forceinline__ uint32_t len4(const uint8_t *len, uint32_t w)
     return (uint32_t)len[byte_of(w, 0)] + len[byte_of(w, 1)] + len[byte_of(w, 2)] + len[byte_of(w, 3)];
 }
 
-template <bool kOne>
+template <int kMode>
 __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, const uint2 *lut, const uint8_t *len,
                                              uint32_t in0, uint32_t st0, uint32_t w, uint32_t lane)
 {
+    constexpr bool kOne = kMode != kUnitGroup; // the unit's codes are one run (one chunk, or part of one)
     const EncJob &job = p.job;
     const uint2 *lt = lut + (lane & (kLutReplicas - 1u));
     const uint32_t s_shift = 31u - __clz(job.S);
@@ -584,9 +648,34 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
         const ULayout lay = unit_layout<kOne>(x, lane, wpc);
         const uint32_t wE = __shfl_sync(~0u, lay.E, w);
         const uint32_t cbase = kOne ? 0u : __shfl_sync(~0u, lay.base, w);
-        const uint32_t ubytes = __shfl_sync(~0u, lay.Y, kUWarps - 1u);
-        // publish the unit's size for the look-back; hand the unit to the storer
-        st_relaxed_pred(job.flags + u, kFlagAggregate | ubytes, t == 0 && u != 0);
+        const uint32_t utot = __shfl_sync(~0u, lay.cbits, kUWarps - 1u); // the unit's bits (kOne)
+        // stage bytes the unit needs (split chunks: its words and the storer's 8)
+        const uint32_t ubytes = kMode == kUnitSplit ? split_stage_bytes(utot) : __shfl_sync(~0u, lay.Y, kUWarps - 1u);
+        // publish the unit's size for the look-back (split chunks: its bits,
+        // for the chunk's later units, unless it is the chunk's last); hand
+        // the unit to the storer
+        if (kMode == kUnitSplit) {
+            if (t == 0) {
+                const uint32_t m1 = (1u << p.mlog) - 1u;
+                const uint64_t c = u >> p.mlog;
+                const bool clast = ((uint32_t)u & m1) == m1 || u + 1 == p.n_units;
+                const uint64_t units = min((uint64_t)m1 + 1u, p.n_units - (c << p.mlog)); // units of chunk c
+                // count the unit into its chunk's word; the last one counted publishes the chunk's size
+                const uint64_t old = atomicAdd((unsigned long long *)(job.flags + c),
+                                               (1ull << kUCountShift) | (uint64_t)utot);
+                if ((old >> kUCountShift) + 1u == units) {
+                    const uint64_t cb = ((old & ((1ull << kUCountShift) - 1u)) + utot + 127u) / 128u * 16u;
+                    atomicMax((unsigned long long *)(job.flags + c), (c ? kFlagAggregate : kFlagPrefix) | cb);
+                }
+                // the unit's bits for the chunk's later units, published after
+                // the count (whoever reads them may then raise the chunk's word)
+                __threadfence();
+                if (!clast)
+                    st_relaxed(p.uflags + u, kFlagAggregate | utot);
+            }
+        } else {
+            st_relaxed_pred(job.flags + u, kFlagAggregate | ubytes, t == 0 && u != 0);
+        }
         st_shared_u64_pred(&P.sunit[r], u, t == 0);
         mbar_arrive_pred(&P.agg[r], t == 0);
         {
@@ -826,9 +915,199 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         bulk_wait_all();
 }
 
+__device__ __forceinline__ void st_global_u32(uint8_t *addr, uint32_t v)
+{
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_v4(uint8_t *addr, uint4 v)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// The output word whose first r bits are the last r bits of hi and whose
+// other 32 - r bits are the first bits of lo (all words in memory order).
+__device__ __forceinline__ uint32_t shift_word(uint32_t hi, uint32_t lo, uint32_t r)
+{
+    return bswap32(__funnelshift_r(bswap32(lo), bswap32(hi), r));
+}
+
+// Output blocks [b_first, b_end) (16 bytes each, relative to g0) of a unit
+// of a split chunk whose stage holds its bits from bit 0 and whose first bit
+// is bit s = 32 Q + r of block 0: block b takes stage words 4b - Q - 1 ..
+// 4b - Q + 3, read as the two aligned 16-byte groups around them.  A lane a
+// block; b_first >= 1.
+template <int Q>
+__device__ __forceinline__ void split_blocks(uint8_t *g0, uint32_t st, uint32_t r, uint32_t b_first, uint32_t b_end,
+                                             uint32_t lane)
+{
+#pragma unroll 4
+    for (uint32_t b = b_first + lane; b < b_end; b += 32u) {
+        const uint4 A = ld_shared_v4(st + 16u * (b - 1u)), B = ld_shared_v4(st + 16u * b);
+        const uint32_t w[8] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w};
+        uint32_t v[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i)
+            v[i] = bswap32(w[i + 3 - Q]);
+        uint4 o;
+        o.x = bswap32(__funnelshift_r(v[1], v[0], r));
+        o.y = bswap32(__funnelshift_r(v[2], v[1], r));
+        o.z = bswap32(__funnelshift_r(v[3], v[2], r));
+        o.w = bswap32(__funnelshift_r(v[4], v[3], r));
+        st_global_v4(g0 + 16u * b, o);
+    }
+}
+
+// Storer of split chunks.  For unit u (the j-th of chunk c): the bits of the
+// chunk's earlier units, the chunk's offset (look-back over chunks), then the
+// unit's stage shifted to its bit in the output: the words that are wholly
+// the unit's, and its part of each word it shares with a neighbour.  The
+// chunk's last unit also publishes the chunk's inclusive prefix, writes
+// chunk_off and pads the chunk.  A unit that could not be staged marks its
+// chunk for the deferred pass.
+__device__ __forceinline__ void unit_storer_split(const UnitParams &p, UPipe &P, uint32_t st0, uint32_t lane)
+{
+    const EncJob &job = p.job;
+    const uint32_t m1 = (1u << p.mlog) - 1u;
+    int64_t known = -1; // a chunk whose inclusive prefix known_incl the CTA holds
+    uint64_t known_incl = 0;
+    for (uint64_t k = 0; k <= p.n_units; ++k) {
+        const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r4 = (uint32_t)k & 3u;
+        if (!mbar_wait(&P.agg[r4], (uint32_t)(k >> 2) & 1u, p.timeout_ns)) {
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            break;
+        }
+        const uint64_t u = *(volatile uint64_t *)&P.sunit[r4];
+        const uint32_t x = lane < kUWarps ? P.wtot[r4][lane] : 0u;
+        __syncwarp();
+        if (k > 0 && lane == 0) { // as in unit_storer
+            bulk_wait_read();
+            mbar_arrive(&P.st_free[slot ^ 1u]);
+        }
+        if (u == kUEnd)
+            break;
+        const uint64_t c = u >> p.mlog;
+        const uint32_t j = (uint32_t)u & m1;
+        const bool clast = j == m1 || u + 1 == p.n_units;
+        const uint32_t L = (uint32_t)min((uint64_t)kUSyms, job.n - u * kUSyms);
+        const ULayout lay = unit_layout<true>(x, lane, kUWarps);
+        const uint32_t ubits = __shfl_sync(~0u, lay.cbits, kUWarps - 1u);
+        // the bits of the chunk's earlier units (lane i waits for the i-th)
+        const uint64_t fb = lane < j ? unit_wait_word(p.uflags + (u - j + lane), 1, p.timeout_ns, job.status) : 0;
+        const uint32_t intra = __reduce_add_sync(~0u, (uint32_t)(fb & kUBitsMask));
+        const uint32_t cbytes = (intra + ubits + 127u) / 128u * 16u; // the chunk's size (its last unit)
+        bool to = false;
+        const uint64_t prefix = unit_lookback(job.flags, c, known, known_incl, p.timeout_ns, &to);
+        if (clast) {
+            if (lane == 0) {
+                // every unit of the chunk has been counted into its word (their
+                // bits were read above): raise it to the inclusive prefix
+                __threadfence();
+                atomicMax((unsigned long long *)(job.flags + c), kFlagPrefix | ((prefix + cbytes) & kValueMask));
+                job.chunk_off[c + 1] = prefix + cbytes;
+            }
+            known = (int64_t)c;
+            known_incl = prefix + cbytes;
+        } else {
+            known = (int64_t)c - 1;
+            known_incl = prefix;
+        }
+        if (lane == 0) {
+            if (u == 0)
+                job.chunk_off[0] = 0;
+            atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)ubits);
+            if (to)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+        }
+        // the unit's first bit is bit s = 32 q + r of output block g0
+        const uint32_t s = intra & 127u, q = s >> 5, r = s & 31u, e = s + ubits;
+        uint8_t *const g0 = job.out + prefix + (intra >> 7) * 16u;
+        // output words (from g0) the unit writes, from word q: every word
+        // through the chunk's padding (last unit), else its complete words
+        // (the partial last one, word e / 32, is shared with the next unit)
+        const uint32_t nwe = clast ? (e + 127u) / 128u * 4u : e / 32u;
+        const bool fits = prefix + (intra >> 7) * 16u + 4ull * nwe <= job.out_cap;
+        if (!fits && !to && lane == 0)
+            set_status(job.status, ECC_ERR_CAPACITY);
+        const bool write = fits && !to;
+        if (!mbar_wait(&P.done[slot], par, p.timeout_ns)) { // the compute warps have packed the unit
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            break;
+        }
+        const uint32_t st = st0 + slot * p.stage_bytes;
+        const uint32_t nst = (ubits + 31u) / 32u; // stage words holding the unit's bits
+        if (split_stage_bytes(ubits) > p.stage_bytes) {
+            // not staged: the deferred pass codes the whole chunk (the chunk's
+            // last unit marks the chunk's word, once the chunk fits; the
+            // others the mark word)
+            if (lane == 0) {
+                if (!clast)
+                    atomicOr((unsigned long long *)(p.uflags + min(((c + 1) << p.mlog) - 1u, p.n_units - 1u)),
+                             (unsigned long long)kMarkDeferred);
+                else if (write)
+                    atomicMax((unsigned long long *)(job.flags + c),
+                              kFlagPrefix | kFlagDeferred | ((prefix + cbytes) & kValueMask));
+            }
+            __syncwarp();
+            continue;
+        }
+        // words shared across warps (as in unit_storer; the unit starts at stage bit 0)
+        if (lane > 0 && lane < kUWarps && lane * 32u * kUThr < L && (lay.E & 31u))
+            red_or_shared(st + (lay.E >> 5) * 4u, P.wtail[slot][lane - 1]);
+        // zeros after the unit's last word: the shifted unit reads up to 4
+        // words past it (its last partial word, the chunk's padding)
+        if (lane < 4u)
+            st_shared_u32(st + 4u * (nst + lane), 0u);
+        __syncwarp();
+        if (!write)
+            continue;
+        // output word W (q <= W, W - q <= nst + 3): the unit's bits that
+        // fall in it, shifted from the stage (word q: zeros in the first r bits)
+        auto out_word = [&](uint32_t W) -> uint32_t {
+            const uint32_t lo = ld_shared_u32(st + 4u * (W - q));
+            const uint32_t hi = W > q ? ld_shared_u32(st + 4u * (W - q - 1u)) : 0u;
+            return shift_word(hi, lo, r);
+        };
+        // whole 16-byte blocks after block 0 (a lane a block)
+        const uint32_t b_end = nwe / 4u;
+        switch (q) {
+        case 0: split_blocks<0>(g0, st, r, 1u, b_end, lane); break;
+        case 1: split_blocks<1>(g0, st, r, 1u, b_end, lane); break;
+        case 2: split_blocks<2>(g0, st, r, 1u, b_end, lane); break;
+        default: split_blocks<3>(g0, st, r, 1u, b_end, lane); break;
+        }
+        // single words: block 0 after word q (from word q when r = 0: nothing
+        // of the previous unit's in it), and the complete words of a last
+        // partial block
+        const uint32_t hw = q + (r ? 1u : 0u) + lane;          // lanes 0..3
+        const uint32_t tw = max(4u, 4u * b_end) + (lane - 4u); // lanes 4..7
+        if (lane < 4u && hw < min(4u, nwe))
+            st_global_u32(g0 + 4u * hw, out_word(hw));
+        if (lane >= 4u && lane < 8u && tw < nwe)
+            st_global_u32(g0 + 4u * tw, out_word(tw));
+        // the words shared with the previous unit of the chunk (word q, lane
+        // 8) and with the next (word e / 32, lane 9): or this unit's part into
+        // the earlier unit's word; the second to do so writes the word
+        const bool head = lane == 8u && j > 0 && r;
+        const bool tail = lane == 9u && !clast && (e & 31u);
+        if (head || tail) {
+            const uint32_t W = head ? q : e >> 5;
+            const uint32_t part = out_word(W);
+            const uint64_t old = atomicOr((unsigned long long *)(p.uflags + (head ? u - 1 : u)),
+                                          (unsigned long long)((head ? kHandNext : kHandPrev) |
+                                                               ((uint64_t)part << kUBitsShift)));
+            if (old & (head ? kHandPrev : kHandNext))
+                st_global_u32(g0 + 4u * W, part | (uint32_t)(old >> kUBitsShift));
+        }
+        __syncwarp();
+    }
+}
+
 // Two CTAs an SM (56 registers a thread): one CTA's barrier waits and
 // pipeline stalls are covered by the other's warps.
-template <bool kOne>
+template <int kMode>
 __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
 {
     extern __shared__ __align__(128) uint8_t unit_smem[];
@@ -873,11 +1152,13 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
     __syncthreads();
     const uint32_t st0 = smem_u32(base + 2 * kUSyms);
     if (warp < kUWarps)
-        unit_compute<kOne>(p, P, lut, len_table, smem_u32(base), st0, warp, lane);
+        unit_compute<kMode>(p, P, lut, len_table, smem_u32(base), st0, warp, lane);
     else if (warp == kUWarps)
         unit_loader(p, P, base, lane);
+    else if (kMode == kUnitSplit)
+        unit_storer_split(p, P, st0, lane);
     else
-        unit_storer<kOne>(p, P, st0, lane);
+        unit_storer<kMode == kUnitOne>(p, P, st0, lane);
 }
 
 // ---------------------------------------------------------------- host side
@@ -899,21 +1180,27 @@ uint32_t unit_stage_bytes()
     return (uint32_t)std::min<int64_t>(room / 2 / 16 * 16, 2 * kUSyms);
 }
 
-// Launch the unit encoder for chunks of C <= kUSyms symbols (the prologue
-// has cleared the flags, the ticket and the outputs).  Returns ECC_ERR_CUDA
-// if it cannot run on this device.
+// Launch the unit encoder (the prologue has cleared the flags, the ticket
+// and the outputs; for chunks of more than kUSyms symbols job.flags holds a
+// word per chunk and then a word per unit).  *unit_chunks: the chunks of a
+// unit of the deferred pass.  Returns ECC_ERR_CUDA if it cannot run on this
+// device.
 ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st, uint32_t *unit_chunks)
 {
     UnitParams p;
     p.job = job;
     p.n_units = (job.n + kUSyms - 1) / kUSyms;
+    p.uflags = job.flags + (job.n + job.C - 1) / job.C;
+    p.mlog = job.C > kUSyms ? 31u - __builtin_clz(job.C / kUSyms) : 0u;
     p.ticket = ticket;
     p.timeout_ns = kWaitLimitNs;
     p.stage_bytes = unit_stage_bytes();
     if (p.stage_bytes < 16u)
         return ECC_ERR_CUDA;
-    const bool one = job.C == kUSyms;
-    const void *kfn = one ? (const void *)encode_unit_kernel<true> : (const void *)encode_unit_kernel<false>;
+    const int mode = job.C == kUSyms ? kUnitOne : job.C < kUSyms ? kUnitGroup : kUnitSplit;
+    const void *kfn = mode == kUnitOne     ? (const void *)encode_unit_kernel<kUnitOne>
+                      : mode == kUnitGroup ? (const void *)encode_unit_kernel<kUnitGroup>
+                                           : (const void *)encode_unit_kernel<kUnitSplit>;
     const size_t smem = unit_smem_bytes(p.stage_bytes);
     const int occ = occupancy(kfn, kUThreads, smem);
     const int sms = sm_count();
@@ -922,11 +1209,13 @@ ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t
     // persistent: every CTA resident, so a unit's predecessors are always being coded
     const uint64_t need = (p.n_units + 1) / 2;
     const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)occ * sms, need));
-    if (one)
-        encode_unit_kernel<true><<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    if (mode == kUnitOne)
+        encode_unit_kernel<kUnitOne><<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    else if (mode == kUnitGroup)
+        encode_unit_kernel<kUnitGroup><<<(unsigned)grid, kUThreads, smem, st>>>(p);
     else
-        encode_unit_kernel<false><<<(unsigned)grid, kUThreads, smem, st>>>(p);
-    *unit_chunks = kUSyms / job.C;
+        encode_unit_kernel<kUnitSplit><<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    *unit_chunks = mode == kUnitSplit ? 1u : kUSyms / job.C;
     return launch_status(cudaGetLastError());
 }
 

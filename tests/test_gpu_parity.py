@@ -212,13 +212,14 @@ def test_encode_in_groups(C, S):
 
 
 @pytest.mark.parametrize("C,S", [(32768, 64), (32768, 1024), (65536, 256), (65536, 1024)])
-def test_encode_in_passes(C, S):
-    """Chunks of more than 16384 symbols: a length pass and a scan place the
-    chunks, then each chunk is coded in passes of 16384 symbols whose shared
-    boundary words are merged.  Tensors ending inside a pass, on a pass
-    boundary and one symbol past it; a chunk of rare bytes whose segments
-    outgrow their stage regions (coded straight into the output) between
-    ordinary chunks."""
+def test_encode_split_chunks(C, S):
+    """Chunks of more than 16384 symbols are coded in units of 16384 symbols
+    on different CTAs: each unit starts at the bit where the chunk's earlier
+    units end, and the word two units share is handed from one to the next.
+    Tensors ending inside a unit, on a unit boundary and one symbol past it;
+    a chunk of rare bytes whose units outgrow the stage (the whole chunk is
+    left to the deferred pass) between ordinary chunks, and ending inside
+    that chunk."""
     x = np_gauss(3 * C, (18, C), 1.0)[0]
     count = oracle.histogram(x)
     w = count + np.uint64(1)
@@ -233,6 +234,11 @@ def test_encode_in_passes(C, S):
     assert ecc.codebook_view(books[1][0])["len"][rare].astype(int).min() > 11
     check_against_oracle(y, *books[1], C, S)
     check_against_oracle(y[:C + 777].copy(), *books[1], C, S)
+    # one unit of rare bytes: the chunk's first unit, or its last
+    for lo in (C, 2 * C - 16384):
+        z = x.copy()
+        z[lo:lo + 16384] = np.random.default_rng(lo).choice(rare, 16384)
+        check_against_oracle(z, *books[1], C, S)
 
 
 def test_corrupt_pieces_are_flagged():

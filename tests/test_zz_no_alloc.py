@@ -94,8 +94,9 @@ def test_static_encode_matches_oracle():
 
 
 def test_static_encode_large_chunks_and_python_wrapper():
-    """Chunks of 65536 symbols take the length pass and the offset scan,
-    whose words also live in the static array; the Python wrapper
+    """Chunks of 65536 symbols are coded in units of 16384 symbols, whose
+    words (one per unit, after the chunks' words) also live in the static
+    array; the Python wrapper
     ecc.ecc_encode_static is called twice in a row and must equal
     ecc_encode."""
     xh = np_grad((1 << 22) + 1234, (31, 4))
