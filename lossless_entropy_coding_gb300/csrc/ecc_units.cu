@@ -84,8 +84,9 @@ constexpr uint64_t kHandPrev = 1ull << 53, kHandNext = 1ull << 54;
 constexpr uint64_t kMarkDeferred = 1;
 // A split chunk's look-back word before it is published (state 0): the
 // units sized so far (<< kUCountShift) and their bits.  Every later change
-// of the word raises it (atomicMax): published size, inclusive prefix, the
-// deferred mark.
+// of the word raises it (atomicMax): the size (by the unit counted last,
+// after its count, so a published size means every unit is counted), the
+// inclusive prefix, the deferred mark.
 constexpr uint32_t kUCountShift = 32;
 static_assert((uint64_t)kUSyms * ECC_MAX_CODE_LEN <= kUBitsMask, "a unit's bit count fits its field");
 // Stage bytes a unit of a split chunk needs: its words from bit 0, and 8
@@ -109,7 +110,7 @@ struct UPipe {
     uint64_t unit[2];      // loader -> compute: unit of slot s, or kUEnd
     uint64_t sunit[4];     // compute -> storer: unit k, or kUEnd
     uint32_t wtot[4][kUWarps];  // compute -> storer: bit totals of the compute warps of unit k
-    uint32_t wtail[2][kUWarps]; // lane 31's last partial word (memory order) when the next warp continues its chunk
+    uint32_t wtail[2][kUWarps]; // lane 31's last partial word (stage word order) when the next warp continues its chunk
 };
 static_assert(sizeof(UPipe) % 16 == 0, "buffers stay 16-byte aligned");
 
@@ -284,10 +285,14 @@ __device__ __forceinline__ void ust(uint32_t addr, uint32_t v, uint32_t lim, boo
 // 2^(32 - nb).  Appending (v, q): v * K + (cur << 32) holds cur completed by
 // v's leading bits in its high word and v's remaining bits in its low word;
 // K * q = 2^(64 - nb - l) has a zero high word exactly when the word filled
-// up (it is then stored, byte-swapped to memory order, and the low word
-// becomes the partial one) and holds the next K in whichever word is
-// non-zero.  The store, the select and the address step are one predicated
-// block (no branch).
+// up (it is then stored, byte-swapped to memory order unless kSwap is
+// false, and the low word becomes the partial one) and holds the next K in
+// whichever word is non-zero.  The store, the select and the address step
+// are one predicated block (no branch).
+template <bool kSwap>
+__device__ __forceinline__ uint32_t word_order(uint32_t w) { return kSwap ? bswap32(w) : w; }
+
+template <bool kSwap>
 struct UPacker {
     uint32_t addr, cur, K, nb0;
 #ifdef ECC_CHECKED
@@ -330,15 +335,22 @@ struct UPacker {
         const uint32_t w = xhi | cur;
 #ifdef ECC_CHECKED
         if (gate == 0)
-            ust(addr, bswap32(w), lim, bad);
+            ust(addr, word_order<kSwap>(w), lim, bad);
         cur = gate == 0 ? xlo : w;
         addr += gate == 0 ? 4u : 0u;
 #else
-        asm volatile("{\n\t.reg .pred p;\n\t.reg .b32 s;\n\tsetp.eq.u32 p, %3, 0;\n\tprmt.b32 s, %2, 0, 0x0123;\n\t"
-                     "@p st.shared.b32 [%0], s;\n\tselp.b32 %1, %4, %2, p;\n\t@p add.u32 %0, %0, 4;\n\t}"
-                     : "+r"(addr), "=r"(cur)
-                     : "r"(w), "r"(gate), "r"(xlo)
-                     : "memory");
+        if (kSwap)
+            asm volatile("{\n\t.reg .pred p;\n\t.reg .b32 s;\n\tsetp.eq.u32 p, %3, 0;\n\tprmt.b32 s, %2, 0, 0x0123;\n\t"
+                         "@p st.shared.b32 [%0], s;\n\tselp.b32 %1, %4, %2, p;\n\t@p add.u32 %0, %0, 4;\n\t}"
+                         : "+r"(addr), "=r"(cur)
+                         : "r"(w), "r"(gate), "r"(xlo)
+                         : "memory");
+        else
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %3, 0;\n\t"
+                         "@p st.shared.b32 [%0], %2;\n\tselp.b32 %1, %4, %2, p;\n\t@p add.u32 %0, %0, 4;\n\t}"
+                         : "+r"(addr), "=r"(cur)
+                         : "r"(w), "r"(gate), "r"(xlo)
+                         : "memory");
 #endif
     }
     __device__ __forceinline__ void put(uint32_t v, uint32_t q)
@@ -354,9 +366,9 @@ struct UPacker {
         const bool complete = K == 1u;
 #ifdef ECC_CHECKED
         if (complete)
-            ust(addr, bswap32(cur), lim, bad);
+            ust(addr, word_order<kSwap>(cur), lim, bad);
 #else
-        st_shared_pred(addr, bswap32(cur), complete);
+        st_shared_pred(addr, word_order<kSwap>(cur), complete);
 #endif
         return complete ? UEnd{0u, addr + 4u, false} : UEnd{cur, addr, true};
     }
@@ -364,11 +376,12 @@ struct UPacker {
 
 // The 32 bytes of (a, b) packed one code at a time from the lane's table
 // replica (every code at most 31 bits).
+template <bool kSwap>
 static __device__ __noinline__ UEnd unit_pack_single(const uint2 *lt, uint32_t stage, uint32_t pos, uint4 a, uint4 b,
                                                      uint32_t lim, uint32_t *status)
 {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    UPacker pk;
+    UPacker<kSwap> pk;
 #ifdef ECC_CHECKED
     pk.lim = lim;
 #endif
@@ -390,6 +403,7 @@ static __device__ __noinline__ UEnd unit_pack_single(const uint2 *lt, uint32_t s
 // Slow-path packing of the cnt bytes of (a, b) at bit pos of the stage (codes
 // from the codebook in global memory, up to ECC_MAX_CODE_LEN bits): the same
 // word protocol.
+template <bool kSwap>
 static __device__ __noinline__ UEnd unit_pack_slow(uint32_t stage, uint32_t pos, uint4 a, uint4 b, uint32_t cnt,
                                                    const ecc_codebook *cb, uint32_t lim, uint32_t *status)
 {
@@ -403,9 +417,9 @@ static __device__ __noinline__ UEnd unit_pack_slow(uint32_t stage, uint32_t pos,
         nb += len;
         if (nb >= 32u) {
 #ifdef ECC_CHECKED
-            ust(addr, bswap32((uint32_t)(acc >> 32)), lim, bad);
+            ust(addr, word_order<kSwap>((uint32_t)(acc >> 32)), lim, bad);
 #else
-            st_shared_u32(addr, bswap32((uint32_t)(acc >> 32)));
+            st_shared_u32(addr, word_order<kSwap>((uint32_t)(acc >> 32)));
 #endif
             addr += 4u;
             acc <<= 32;
@@ -598,6 +612,9 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
                                              uint32_t in0, uint32_t st0, uint32_t w, uint32_t lane)
 {
     constexpr bool kOne = kMode != kUnitGroup; // the unit's codes are one run (one chunk, or part of one)
+    // stage words in memory order (the storer copies them out as they are),
+    // or in register order (split chunks: the storer shifts them first)
+    constexpr bool kSwap = kMode != kUnitSplit;
     const EncJob &job = p.job;
     const uint2 *lt = lut + (lane & (kLutReplicas - 1u));
     const uint32_t s_shift = 31u - __clz(job.S);
@@ -667,9 +684,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
                     const uint64_t cb = ((old & ((1ull << kUCountShift) - 1u)) + utot + 127u) / 128u * 16u;
                     atomicMax((unsigned long long *)(job.flags + c), (c ? kFlagAggregate : kFlagPrefix) | cb);
                 }
-                // the unit's bits for the chunk's later units, published after
-                // the count (whoever reads them may then raise the chunk's word)
-                __threadfence();
+                // the unit's bits, for the chunk's later units
                 if (!clast)
                     st_relaxed(p.uflags + u, kFlagAggregate | utot);
             }
@@ -697,7 +712,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
         // the code pairs, 8 at a time (16 bytes); a partial thread, or one
         // with a pair the table cannot code, takes the paths below, which
         // rewrite every word of its range
-        UPacker pk;
+        UPacker<kSwap> pk;
 #ifdef ECC_CHECKED
         pk.lim = lim;
 #endif
@@ -744,9 +759,9 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
             const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16u);
             const uint32_t bs = cnt == kUThr ? unit_bits_single(lt, a, b) : 1u << 31;
             if (!(bs >> 31))
-                e = unit_pack_single(lt, st, pos, a, b, lim, job.status);
+                e = unit_pack_single<kSwap>(lt, st, pos, a, b, lim, job.status);
             else
-                e = unit_pack_slow(st, pos, a, b, cnt, job.cb, lim, job.status);
+                e = unit_pack_slow<kSwap>(st, pos, a, b, cnt, job.cb, lim, job.status);
         }
         // The thread's last partial word: the next lane or-s it into its first
         // word; lane 31 leaves it to the storer; the chunk's last thread
@@ -757,12 +772,12 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
         if (!over) {
 #ifdef ECC_CHECKED
             if (clast && e.partial)
-                ust(e.addr, bswap32(e.tail), lim, bad_index);
+                ust(e.addr, word_order<kSwap>(e.tail), lim, bad_index);
 #else
-            st_shared_pred(e.addr, bswap32(e.tail), clast && e.partial);
+            st_shared_pred(e.addr, word_order<kSwap>(e.tail), clast && e.partial);
 #endif
-            st_shared_pred(smem_u32(&P.wtail[slot][w]), bswap32(e.tail), lane == 31 && !clast);
-            red_or_pred(st + (pos >> 5) * 4u, bswap32(prev), cnt && lane && (pos & 31u));
+            st_shared_pred(smem_u32(&P.wtail[slot][w]), word_order<kSwap>(e.tail), lane == 31 && !clast);
+            red_or_pred(st + (pos >> 5) * 4u, word_order<kSwap>(prev), cnt && lane && (pos & 31u));
         }
 #ifdef ECC_CHECKED
         if (bad_index)
@@ -925,18 +940,19 @@ __device__ __forceinline__ void st_global_v4(uint8_t *addr, uint4 v)
                  : "memory");
 }
 
-// The output word whose first r bits are the last r bits of hi and whose
-// other 32 - r bits are the first bits of lo (all words in memory order).
+// The output word (memory order) whose first r bits are the last r bits of
+// hi and whose other 32 - r bits are the first bits of lo (stage words, in
+// register order: first bit in bit 31).
 __device__ __forceinline__ uint32_t shift_word(uint32_t hi, uint32_t lo, uint32_t r)
 {
-    return bswap32(__funnelshift_r(bswap32(lo), bswap32(hi), r));
+    return bswap32(__funnelshift_r(lo, hi, r));
 }
 
 // Output blocks [b_first, b_end) (16 bytes each, relative to g0) of a unit
-// of a split chunk whose stage holds its bits from bit 0 and whose first bit
-// is bit s = 32 Q + r of block 0: block b takes stage words 4b - Q - 1 ..
-// 4b - Q + 3, read as the two aligned 16-byte groups around them.  A lane a
-// block; b_first >= 1.
+// of a split chunk whose stage holds its bits from bit 0 (register-order
+// words) and whose first bit is bit s = 32 Q + r of block 0: block b takes
+// stage words 4b - Q - 1 .. 4b - Q + 3, read as the two aligned 16-byte
+// groups around them.  A lane a block; b_first >= 1.
 template <int Q>
 __device__ __forceinline__ void split_blocks(uint8_t *g0, uint32_t st, uint32_t r, uint32_t b_first, uint32_t b_end,
                                              uint32_t lane)
@@ -948,7 +964,7 @@ __device__ __forceinline__ void split_blocks(uint8_t *g0, uint32_t st, uint32_t 
         uint32_t v[5];
 #pragma unroll
         for (int i = 0; i < 5; ++i)
-            v[i] = bswap32(w[i + 3 - Q]);
+            v[i] = w[i + 3 - Q];
         uint4 o;
         o.x = bswap32(__funnelshift_r(v[1], v[0], r));
         o.y = bswap32(__funnelshift_r(v[2], v[1], r));
@@ -1001,9 +1017,9 @@ __device__ __forceinline__ void unit_storer_split(const UnitParams &p, UPipe &P,
         const uint64_t prefix = unit_lookback(job.flags, c, known, known_incl, p.timeout_ns, &to);
         if (clast) {
             if (lane == 0) {
-                // every unit of the chunk has been counted into its word (their
-                // bits were read above): raise it to the inclusive prefix
-                __threadfence();
+                // raise the chunk's word to the inclusive prefix once every
+                // unit has been counted into it (it holds the chunk's size)
+                unit_wait_word(job.flags + c, 1, p.timeout_ns, job.status);
                 atomicMax((unsigned long long *)(job.flags + c), kFlagPrefix | ((prefix + cbytes) & kValueMask));
                 job.chunk_off[c + 1] = prefix + cbytes;
             }
