@@ -238,9 +238,10 @@ def cpu_sample(n_chunks, C, key=(4, 0)):
 
 def default_subblocks(C):
     """The library's default sub-block sizes of the two codebooks (Huffman:
-    table-decoded, C/128; base QLC: register-decoded, C/64; both clamped to
-    [64, 256]), restated so that the reference arm needs no library."""
-    return [min(256, max(64, C // 128)), min(256, max(64, C // 64))]
+    table-decoded, C/128 clamped to [64, 128]; base QLC: register-decoded,
+    C/64 clamped to [64, 256]), restated so that the reference arm needs no
+    library."""
+    return [min(128, max(64, C // 128)), min(256, max(64, C // 64))]
 
 
 def host_codebooks(C):
@@ -735,8 +736,8 @@ def run_ours(args):
            "qlc": ecc.qlc_build_tables(pooled_h)}
     dcbs = {k: ecc.to_device(v, dev) for k, v in cbs.items()}
     max_len = {k: int(ecc.codebook_view(v)["max_len"]) for k, v in cbs.items()}
-    # each codebook at its default sub-block size (Huffman: C/128, read by
-    # the decoder's table path; QLC: C/64, its register path)
+    # each codebook at its default sub-block size (Huffman: C/128 up to 128,
+    # read by the decoder's table path; QLC: C/64 up to 256, its register path)
     Sk = {k: args.subblock or ecc.default_subblock(C, v) for k, v in cbs.items()}
 
     x = dev_grad(n, (4, rank), device=dev)

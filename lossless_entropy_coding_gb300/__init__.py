@@ -225,15 +225,17 @@ def default_subblock(C: int, cb=None) -> int:
     A QLC codebook the decoder reads through its prefix registers (or no
     codebook given): C/64, clamped to [64, 256].  Any other codebook (Huffman,
     the escape code, a length-limited Huffman or a QLC of fewer areas):
-    C/128, clamped to [64, 256].  Its decoder waits on dependent table
-    lookups, and 16 KiB chunks of 128 sub-blocks give each lane two
-    independent streams at the same number of warps (1 GiB gradient tensor:
-    Huffman decode 1.14 -> 1.03 ms, for 1/64 byte a symbol more of sub-block
-    counts); the QLC decoder is issue-bound and gains nothing.  Larger
-    sub-blocks cost the decoder occupancy: a warp stages 32 sub-blocks or
-    more, so with S > 256 fewer warps fit an SM."""
-    d = 64 if _register_path(cb) else 128
-    return int(min(256, max(64, C // d)))
+    C/128, clamped to [64, 128].  Its decoder waits on dependent table
+    lookups, and sub-blocks of 128 symbols give each lane two independent
+    streams at the same number of warps (1 GiB gradient tensor, Huffman
+    decode: 1.14 -> 1.03 ms at 16 KiB chunks, 1.15 -> 1.04 ms at 64 KiB,
+    for 1/64 byte a symbol more of sub-block counts); the QLC decoder is
+    issue-bound and gains nothing.  Larger sub-blocks cost the decoder
+    occupancy: a warp stages 32 sub-blocks or more, so with S > 256 fewer
+    warps fit an SM."""
+    if _register_path(cb):
+        return int(min(256, max(64, C // 64)))
+    return int(min(128, max(64, C // 128)))
 
 
 # ------------------------------------------------------------------ device calls

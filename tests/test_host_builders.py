@@ -246,7 +246,7 @@ def test_checked_build_compiles_and_exports():
 def test_default_subblock_rule():
     """The sub-block size the binding picks when none is given: C/64 clamped
     to [64, 256] for the base QLC (and when no codebook is named), C/128
-    clamped to [64, 256] for codes the decoder reads through its table
+    clamped to [64, 128] for codes the decoder reads through its table
     (Huffman, the escape code, a QLC of fewer areas); always a power of two
     dividing C (valid for every chunk size)."""
     counts = np.random.default_rng(3).integers(1, 1000, 256).astype(np.uint64)
@@ -255,9 +255,9 @@ def test_default_subblock_rule():
                    ecc.gqlc_build_tables(counts, [4, 4, 7, 8], 2)]
     for k in range(7):
         C = 1024 << k
-        for S, d in [(ecc.default_subblock(C), 64), (ecc.default_subblock(C, qlc), 64)] + \
-                [(ecc.default_subblock(C, cb), 128) for cb in table_coded]:
-            assert S == min(256, max(64, C // d))
+        for S, d, hi in [(ecc.default_subblock(C), 64, 256), (ecc.default_subblock(C, qlc), 64, 256)] + \
+                [(ecc.default_subblock(C, cb), 128, 128) for cb in table_coded]:
+            assert S == min(hi, max(64, C // d))
             assert S & (S - 1) == 0 and C % S == 0 and 64 <= S <= min(C, 1024)
 
 
