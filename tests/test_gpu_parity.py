@@ -613,13 +613,14 @@ def test_batched_matches_single():
 
 # ------------------------------------------------------------------ full size
 
-def test_gradient_gib_sampled_parity():
-    """The 2^30-byte gradient-like tensor in the benchmark's launch setup:
-    sampled chunks bit-exact to the oracle, offsets consistent, GPU counts
-    equal to the oracle's, total bits == sum(count x len), and a lossless
-    round trip on the device."""
+@pytest.mark.parametrize("C", [16384, 4096, 65536])
+def test_gradient_gib_sampled_parity(C):
+    """The 2^30-byte gradient-like tensor in the benchmark's launch setup, at
+    each chunk size of its sweep (4 KiB: groups of chunks a unit; 64 KiB: a
+    chunk in four units): sampled chunks bit-exact to the oracle, offsets
+    consistent, GPU counts equal to the oracle's, total bits == sum(count x
+    len), and a lossless round trip on the device."""
     n = 1 << 30
-    C = 16384
     x = dev_grad(n, (4, 0))
     warm = [oracle.histogram(grad_warmup(i, 1 << 22)) for i in range(2)]
     pooled = oracle.fixed_codebook_weights(warm)
