@@ -120,10 +120,11 @@ __global__ void __maxnreg__(96) encode_batched_ws_kernel(uint8_t *ws, uint64_t *
     encode_ws_body<true>(none, 0, nullptr, bt, h->ws_slot_bytes, h->max_C, kWaitLimitNs);
 }
 
-// The deferred pass of the many-tensor encoder: warp w takes chunk positions
-// w, w + W, ... (the marked chunks come in runs: the tensors are grouped by
-// codebook, and long codes are a codebook's), codes each chunk the encoder
-// marked (long codes), then counts its segments toward the tensor's
+// The deferred pass of the many-tensor encoder: warp w of W takes chunk
+// positions w, w + W, w + 2W, ... (the marked chunks come in runs: the
+// tensors are grouped by codebook, and long codes are a codebook's), 32 at a
+// time, a lane each reading a look-back word; it codes each chunk the
+// encoder marked (long codes), then counts its segments toward the tensor's
 // completion stamp as the encoder would have.
 __global__ void __launch_bounds__(256) encode_batched_deferred_kernel(uint8_t *ws)
 {
@@ -136,9 +137,11 @@ __global__ void __launch_bounds__(256) encode_batched_deferred_kernel(uint8_t *w
     const uint64_t total = h->total_chunks;
     const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    for (uint64_t pos = w0; pos < total; pos += nw) {
-        const uint64_t f = lane == 0 ? flags[pos] : 0;
-        if (__shfl_sync(~0u, is_deferred(f) ? 1u : 0u, 0)) {
+    for (uint64_t p0 = w0; p0 < total; p0 += 32 * nw) {
+        const uint64_t mine = p0 + lane * nw;
+        const bool marked = mine < total && is_deferred(flags[mine]);
+        for (uint32_t m = __ballot_sync(~0u, marked); m; m &= m - 1) {
+            const uint64_t pos = p0 + (uint64_t)(__ffs(m) - 1) * nw;
             const uint64_t it = item[pos];
             if (it == kNoItem)
                 continue;

@@ -560,13 +560,14 @@ int occupancy(const void *kernel, int threads, size_t smem)
     return nb;
 }
 
-// The deferred pass (code_deferred_unit): warp w takes units w, w + W, ...
-// (marked units come in runs: the long codes of one part of a tensor), reads
-// each one's look-back word and codes it if marked.  Chunks coded in parts
-// (marks != NULL: chunks of 2^mlog parts, n_parts in all) are also coded
-// when the mark word of the chunk (the word of its last part) is set and
-// the chunk's offsets are published within the output.  A launch over a
-// tensor with no marked unit only reads its look-back (and mark) words.
+// The deferred pass (code_deferred_unit): warp w of W takes units w, w + W,
+// w + 2W, ... (marked units come in runs: the long codes of one part of a
+// tensor), 32 at a time, a lane each reading a look-back word, and codes the
+// marked ones.  Chunks coded in parts (marks != NULL: chunks of 2^mlog parts,
+// n_parts in all) are also coded when the mark word of the chunk (the word
+// of its last part) is set and the chunk's offsets are published within the
+// output.  A launch over a tensor with no marked unit only reads its
+// look-back (and mark) words, all of a warp's at once.
 __global__ void __launch_bounds__(256) encode_deferred_kernel(EncJob job, uint64_t n_chunks, uint32_t G,
                                                                const uint64_t *marks, uint32_t mlog, uint64_t n_parts)
 {
@@ -574,16 +575,17 @@ __global__ void __launch_bounds__(256) encode_deferred_kernel(EncJob job, uint64
     const uint64_t n_units = (n_chunks + G - 1) / G;
     const uint64_t w0 = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint64_t nw = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-    for (uint64_t u = w0; u < n_units; u += nw) {
+    for (uint64_t u0 = w0; u0 < n_units; u0 += 32 * nw) {
+        const uint64_t u = u0 + lane * nw;
         bool d = false;
-        if (lane == 0) {
+        if (u < n_units) {
             const uint64_t f = job.flags[u];
             d = is_deferred(f);
             if (!d && marks && (marks[min(((u + 1) << mlog) - 1u, n_parts - 1u)] & 1u) && (f >> 62) == 2u)
                 d = job.chunk_off[u] <= job.chunk_off[u + 1] && job.chunk_off[u + 1] <= job.out_cap;
         }
-        if (__shfl_sync(~0u, d ? 1u : 0u, 0))
-            code_deferred_unit(job, u, G, n_chunks);
+        for (uint32_t m = __ballot_sync(~0u, d); m; m &= m - 1)
+            code_deferred_unit(job, u0 + (uint64_t)(__ffs(m) - 1) * nw, G, n_chunks);
     }
 }
 
