@@ -534,7 +534,7 @@ __device__ __forceinline__ uint64_t unit_lookback(const uint64_t *flags, uint64_
                 expired = true;
                 break;
             }
-            __nanosleep(32);
+            __nanosleep(128); // polls compete with the compute warps for issue slots
             continue;
         }
         uint64_t v = need ? sum : 0;
