@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 N_DEFAULT = 1 << 30
 CHUNK = 16384
 WARM_TENSORS, WARM_BYTES = 8, 1 << 24
-E2E_PIECE = 64 << 20
+E2E_PIECE = 128 << 20
 METRIC = "encode/decode GB/s of e4m3 input on 1 GB300, % of HBM roofline; compressibility %"
 WORKLOAD = "gradient-like e4m3 tensor, 2^30 B (s_b * t_4, s_b = 2^U(-4,4) per 4096 elements)"
 FALLBACK_HBM_GBS = 6800.0
@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-piece", type=int, default=E2E_PIECE,
+                   help="end-to-end run: bytes of input coded as one container (whole chunks)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the informational timings after the timed region (three-stage, other codebooks)")
     p.add_argument("--tensors", type=int, default=4096, help="batched workload: number of tensors")
@@ -844,14 +846,14 @@ def run_ours(args):
 
     # End to end through the Python API from pinned host memory: the step's
     # work (encode + decode with both codebooks) in chunk-aligned pieces of
-    # E2E_PIECE bytes, each piece coded as a container of its own (the same
+    # --e2e-piece bytes (128 MiB), each piece coded as a container of its own (the same
     # chunk payloads), so that the host-to-device copy of piece i + 1, the
     # coding of piece i and the device-to-host copy of piece i - 1's Huffman
     # payload overlap on three streams.  The host reads each piece's payload
     # size (8 bytes) once the piece is coded, then issues its copy.
     e2e = None
     if not args.no_e2e:
-        P = max(C, (E2E_PIECE // C) * C)
+        P = max(C, (args.e2e_piece // C) * C)
         K = (n + P - 1) // P
         xh = torch.empty(n, dtype=torch.uint8, pin_memory=True)
         xh.copy_(x)
