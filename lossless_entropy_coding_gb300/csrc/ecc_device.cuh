@@ -2064,16 +2064,28 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
     return v;
 }
 
+// predicated shared load: v when p is false
+__device__ __forceinline__ uint32_t lds_u32_if(uint32_t addr, bool p, uint32_t v)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.shared.u32 %0, [%1];\n\t}"
+                 : "+r"(v)
+                 : "r"(addr), "r"((uint32_t)p));
+    return v;
+}
+
 // Hot-loop step: two codes the 14-bit table resolves, one window refill.
 // The first code starts at o < 32 and ends by bit 45, so the second one's
 // 14-bit peek lies in (hi, lo) or (lo, nx); after both the stream has moved
-// at most 59 bits, i.e. by at most one word.  An empty entry (a longer or an
+// at most 59 bits, i.e. by at most one word.  Only a stream that moved on
+// loads the refill word, after the lookups: the next step's first lookup
+// reads (hi, lo) alone and hides the load, and the lanes that stay add no
+// bank conflicts to the load (QLC steps, with no lookup on the stream's
+// path, load first instead).  An empty entry (a longer or an
 // invalid code) has length 0, so the stream stays where it is; emin records
 // it and the caller redoes the iteration with fstep_slow.  Returns the two
 // bytes in the low half (first code's in byte 0).
 __device__ __forceinline__ uint32_t fstep2(FastStream &s, const uint16_t *dec, uint32_t &emin)
 {
-    const uint32_t w = lds_u32(s.wa); // the refill word, loaded before the lookups so that they hide its latency
     const uint32_t p1 = __funnelshift_l(s.lo, s.hi, s.o);
     const uint32_t e1 = dec[p1 >> (32 - ECC_PEEK_BITS)];
     const uint32_t o1 = s.o + (e1 >> 8);
@@ -2083,6 +2095,7 @@ __device__ __forceinline__ uint32_t fstep2(FastStream &s, const uint16_t *dec, u
     emin = min(emin, min(e1, e2));
     const uint32_t o2 = o1 + (e2 >> 8);
     const bool adv = o2 >= 32;
+    const uint32_t w = lds_u32_if(s.wa, adv, 0u);
     s.hi = adv ? s.lo : s.hi;
     s.lo = adv ? s.nx : s.lo;
     s.nx = adv ? bswap32(w) : s.nx;
@@ -2239,7 +2252,7 @@ __device__ __forceinline__ DecTables qlc_tables(const uint16_t *gdec, const Long
 // the ranks (one of 256 or more: no code, the chunk is corrupt).
 __device__ __forceinline__ uint32_t qstep2(FastStream &s, const DecTables &T, uint32_t &vmax)
 {
-    const uint32_t w = lds_u32(s.wa); // the refill word, loaded first (see fstep2)
+    const uint32_t w = lds_u32(s.wa); // the refill word, loaded first: nothing else hides its latency here
     // the permute leaves len[prefix] in byte 0 and byte 0 of len0 in bytes
     // 1..3: lg removes those; a funnel shift only uses the low 5 bits anyway
     const uint32_t p1 = __funnelshift_l(s.lo, s.hi, s.o);
