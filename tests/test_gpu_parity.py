@@ -357,17 +357,25 @@ def test_pairs_past_32_bits_with_codes_of_at_most_31():
 
 # ------------------------------------------------------------------ errors
 
-def test_capacity_error_reports_needed_size():
-    x = np_gauss(100000, (13, 0), 1.0)[0]
+@pytest.mark.parametrize("C", [4096, 16384, 65536])
+def test_capacity_error_reports_needed_size(C):
+    """A payload buffer too small: ECC_ERR_CAPACITY, chunk_off still holds
+    the sizes the payload needs, and no byte past out_cap is written (the
+    buffer is a view of a larger one whose tail is a canary), whether the
+    buffer is far too small or 16 bytes short."""
+    x = np_gauss(3 * 65536 + 12345, (13, 0), 1.0)[0]
     count = oracle.histogram(x)
     cbb = ecc.qlc_build_tables(count)
     dcb = ecc.to_device(cbb)
-    small = torch.empty(4096, dtype=torch.uint8, device="cuda")
-    enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), dcb, 16384, 256, out=small)
-    torch.cuda.synchronize()
-    assert int(enc.status.item()) == ecc.ERR_CAPACITY
-    ref = oracle.encode(x, oracle.qlc_codebook(count), 16384, 256)
-    assert (u64(enc.chunk_off) == ref["chunk_off"]).all()
+    ref = oracle.encode(x, oracle.qlc_codebook(count), C, 256)
+    need = int(ref["chunk_off"][-1])
+    for cap in (4096, need - 16):
+        big = torch.full((need + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+        enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), dcb, C, 256, out=big[:cap])
+        torch.cuda.synchronize()
+        assert int(enc.status.item()) == ecc.ERR_CAPACITY, cap
+        assert (u64(enc.chunk_off) == ref["chunk_off"]).all()
+        assert bool((big[cap:] == 0xA5).all()), cap
 
 
 @pytest.mark.parametrize("n,where", [(20, 12), (40000, 20000), (1 << 20, (1 << 20) - 5)])
@@ -378,10 +386,36 @@ def test_uncoded_byte_is_a_codebook_error(n, where):
     w[:10] = 1
     x = (np.arange(n) % 10).astype(np.uint8)
     x[where] = 200
-    for C in (1024, 16384):
+    for C in (1024, 16384, 65536):
         enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), ecc.to_device(ecc.huff_build_canonical(w)), C, 64)
         torch.cuda.synchronize()
         assert int(enc.status.item()) == ecc.ERR_CODEBOOK
+
+
+def test_unit_of_uncoded_bytes_is_a_codebook_error():
+    """A whole unit of 16384 bytes the codebook does not code (zero bits:
+    the unit shares its one word with both neighbours) inside a chunk of
+    65536 symbols, or as a whole chunk of 16384: reported, and the other
+    chunks are still placed as the oracle places them."""
+    w = np.zeros(256, np.uint64)
+    w[:10] = 1
+    x = (np.arange(4 * 65536 + 77) % 10).astype(np.uint8)
+    x[65536 + 16384:65536 + 32768] = 200
+    cbb = ecc.huff_build_canonical(w)
+    for C in (16384, 65536):
+        enc = ecc.ecc_encode(torch.from_numpy(x).cuda(), ecc.to_device(cbb), C, 64)
+        torch.cuda.synchronize()
+        assert int(enc.status.item()) == ecc.ERR_CODEBOOK
+        y = x.copy()
+        y[65536 + 16384:65536 + 32768] = 0
+        ref = oracle.encode(y, oracle.huffman_codebook(w), C, 64)
+        off = u64(enc.chunk_off)
+        lens = np.diff(off)
+        rl = np.diff(ref["chunk_off"])
+        bad = (65536 + 16384) // C
+        # chunks without the uncoded bytes keep their sizes
+        keep = [c for c in range(lens.size) if not (bad <= c < bad + max(1, 16384 // C))]
+        assert (lens[keep] == rl[keep]).all()
 
 
 def test_bad_codebook_magic():
