@@ -10,10 +10,11 @@
 // values, 16-byte padded payloads, chunk_off, sub_bits per S values).
 //
 // Kernels: an exponent histogram (lane-private shared counters); the encoder
-// (persistent CTAs of 256 threads claim chunks by ticket; 16 values a thread
-// and tile; block scan of the code lengths; codes packed into a zeroed shared
-// stage; chunk offsets by decoupled look-back; the stage written out
-// byte-swapped with 16-byte stores); the decoder (a warp per chunk, a lane per
+// (chunks of at most 4096 values: a warp a chunk, claimed by ticket, coded in
+// rounds of 16 values a lane placed by a warp scan, packed into the warp's
+// zeroed shared stage, placed by decoupled look-back and written out
+// byte-swapped with 16-byte stores; larger chunks: the same with a CTA of 256
+// threads a chunk and block scans); the decoder (a warp per chunk, a lane per
 // sub-block, codes read through a three-word window, eight values a 16-byte
 // store).
 
@@ -110,8 +111,10 @@ __global__ void __launch_bounds__(kBfThreads) bf16_encode_kernel(BfEncParams p)
     for (int e = tid; e < 256; e += kBfThreads)
         rank[e] = 0;
     __syncthreads();
-    if (tid < 7)
-        rank[p.tab.top[tid]] = (uint8_t)(tid + 1);
+#pragma unroll
+    for (int r = 0; r < 7; ++r) // static indices: the parameter block stays out of local memory
+        if (tid == r)
+            rank[p.tab.top[r]] = (uint8_t)(r + 1);
     for (uint32_t i = tid; i < p.stage_bytes / 16; i += kBfThreads)
         reinterpret_cast<uint4 *>(stage)[i] = make_uint4(0, 0, 0, 0);
     const uint32_t s_shift = 31u - __clz(p.S);
@@ -224,6 +227,126 @@ __global__ void __launch_bounds__(kBfThreads) bf16_encode_kernel(BfEncParams p)
     }
 }
 
+// ---------------------------------------------------------------- warp encoder
+// Chunks of at most kBfWarpC values, a warp a chunk: rounds of 512 values
+// (16 a lane) placed by a warp scan of the code lengths and packed into the
+// warp's own zeroed stage; the chunk's sub-block counts from the bit
+// positions where its sub-blocks start; then its offset by the look-back, and
+// the stage written out and cleared.  After the start no CTA barrier: a warp
+// waiting on its look-back holds up no other warp.
+constexpr uint32_t kBfWarpC = 4096;
+constexpr int kBfWarpThreads = 128;
+constexpr uint32_t kBfRound = 32 * kBfPerThread;   // 512 values
+constexpr uint32_t kBfSubMax = kBfWarpC / 64 + 1;  // sub-blocks of a chunk (S >= 64)
+
+__global__ void __launch_bounds__(kBfWarpThreads) bf16_encode_warp_kernel(BfEncParams p)
+{
+    extern __shared__ __align__(16) uint8_t bfw_smem[];
+    __shared__ uint8_t rank[256];
+    __shared__ uint32_t subpos[kBfWarpThreads / 32][kBfSubMax]; // bit where each sub-block starts
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < 256; e += kBfWarpThreads)
+        rank[e] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 7; ++r) // static indices: the parameter block stays out of local memory
+        if (tid == r)
+            rank[p.tab.top[r]] = (uint8_t)(r + 1);
+    __syncthreads();
+    uint32_t *stage = reinterpret_cast<uint32_t *>(bfw_smem + (size_t)warp * p.stage_bytes);
+    uint4 *st4 = reinterpret_cast<uint4 *>(stage);
+    for (uint32_t i = lane; i < p.stage_bytes / 16; i += 32)
+        st4[i] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    const uint32_t s_shift = 31u - __clz(p.S);
+    uint32_t *sp = subpos[warp];
+    for (;;) {
+        uint32_t tk = 0;
+        if (lane == 0)
+            tk = atomicAdd(p.ticket, 1u);
+        const uint64_t c = __shfl_sync(~0u, tk, 0);
+        if (c >= p.n_chunks)
+            break;
+        const uint64_t base = c * p.C;
+        const uint32_t L = (uint32_t)min((uint64_t)p.C, p.n - base);
+        uint32_t run = 0; // bits of the chunk's earlier rounds
+        for (uint32_t t0 = 0; t0 < L; t0 += kBfRound) {
+            const uint32_t my0 = t0 + (uint32_t)lane * kBfPerThread;
+            const uint32_t cnt = my0 < L ? min(kBfPerThread, L - my0) : 0u;
+            uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (cnt == kBfPerThread) {
+                const uint4 a = ld_stream16(p.in + base + my0), b = ld_stream16(p.in + base + my0 + 8);
+                w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+            } else {
+#pragma unroll
+                for (uint32_t j = 0; j < kBfPerThread; ++j) // unrolled: w stays in registers
+                    if (j < cnt)
+                        w[j >> 1] |= (uint32_t)p.in[base + my0 + j] << (16 * (j & 1));
+            }
+            uint32_t bits = 0;
+#pragma unroll
+            for (uint32_t j = 0; j < kBfPerThread; ++j) {
+                uint32_t len;
+                (void)bf_code((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, rank, len);
+                bits += j < cnt ? len : 0u;
+            }
+            uint32_t incl = bits;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(~0u, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            const uint32_t pos = run + incl - bits;
+            if (cnt && (my0 & (p.S - 1u)) == 0)
+                sp[my0 >> s_shift] = pos;
+            if (cnt) {
+                Packer<false> pk;
+                pk.start(stage, pos);
+#pragma unroll
+                for (uint32_t j = 0; j < kBfPerThread; ++j) {
+                    if (j < cnt) {
+                        uint32_t len;
+                        const uint32_t code = bf_code((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, rank, len);
+                        pk.put(code, len);
+                    }
+                }
+                pk.finish();
+            }
+            run += __shfl_sync(~0u, incl, 31);
+        }
+        __syncwarp(); // the stage and the sub-block starts are complete
+        const uint32_t nsub = (L + p.S - 1u) >> s_shift;
+        for (uint32_t k = lane; k < nsub; k += 32) {
+            const uint32_t e = k + 1 < nsub ? sp[k + 1] : run;
+            p.sub_bits[(base >> s_shift) + k] = (uint16_t)(e - sp[k]);
+        }
+        const uint64_t bytes = ((uint64_t)run + 127u) / 128u * 16u;
+        bool to;
+        const uint64_t prefix = lookback(p.flags, c, bytes, p.timeout_ns, &to);
+        if (lane == 0) {
+            if (to)
+                set_status(p.status, ECC_ERR_TIMEOUT);
+            p.chunk_off[c + 1] = prefix + bytes;
+            if (c == 0)
+                p.chunk_off[0] = 0;
+            atomicAdd((unsigned long long *)p.total_bits, (unsigned long long)run);
+        }
+        const bool fits = prefix + bytes <= p.out_cap;
+        if (!fits && !to && lane == 0)
+            set_status(p.status, ECC_ERR_CAPACITY);
+        const bool write = fits && !to;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + prefix);
+        for (uint32_t i = lane; i < (uint32_t)(bytes / 16); i += 32) {
+            const uint4 v = st4[i];
+            st4[i] = make_uint4(0, 0, 0, 0);
+            if (write)
+                st_stream16(dst + i, bswap4(v));
+        }
+        __syncwarp(); // the stage is clear and the sub-block starts are read
+    }
+}
+
 // ---------------------------------------------------------------- decoder
 struct BfDecParams {
     const uint8_t *in;
@@ -275,8 +398,10 @@ __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
     for (int e = tid; e < 256; e += 256)
         rank[e] = 0;
     __syncthreads();
-    if (tid < 7)
-        rank[p.tab.top[tid]] = (uint8_t)(tid + 1);
+#pragma unroll
+    for (int r = 0; r < 7; ++r) // static indices: the parameter block stays out of local memory
+        if (tid == r)
+            rank[p.tab.top[r]] = (uint8_t)(r + 1);
     __syncthreads();
     const uint32_t tA = p.tab.top[0] | (uint32_t)p.tab.top[1] << 8 | (uint32_t)p.tab.top[2] << 16 |
                         (uint32_t)p.tab.top[3] << 24;
@@ -480,11 +605,23 @@ ecc_status bf16_escape_encode(const uint16_t *in, size_t n, const uint8_t top7[7
     p.ticket = ticket;
     p.status = status;
     p.n_chunks = n_chunks;
-    p.stage_bytes = pad16((C * 19u + 7u) / 8u) + 16u;
+    p.stage_bytes = pad16((C * 19u + 7u) / 8u) + 16u; // C values at 19 bits
     p.timeout_ns = kWaitLimitNs;
-    const int occ = occupancy((const void *)bf16_encode_kernel, kBfThreads, p.stage_bytes);
     const int sms = sm_count();
-    if (occ <= 0 || sms <= 0)
+    if (sms <= 0)
+        return ECC_ERR_CUDA;
+    if (C <= kBfWarpC) { // a warp a chunk, persistent
+        const size_t smem = (size_t)(kBfWarpThreads / 32) * p.stage_bytes;
+        const int occ = occupancy((const void *)bf16_encode_warp_kernel, kBfWarpThreads, smem);
+        if (occ <= 0)
+            return ECC_ERR_CUDA;
+        const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, (n_chunks + kBfWarpThreads / 32 - 1) /
+                                                                          (kBfWarpThreads / 32));
+        bf16_encode_warp_kernel<<<(unsigned)grid, kBfWarpThreads, smem, st>>>(p);
+        return launch_status(cudaGetLastError());
+    }
+    const int occ = occupancy((const void *)bf16_encode_kernel, kBfThreads, p.stage_bytes);
+    if (occ <= 0)
         return ECC_ERR_CUDA;
     const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, n_chunks);
     bf16_encode_kernel<<<(unsigned)grid, kBfThreads, p.stage_bytes, st>>>(p);

@@ -38,7 +38,7 @@ def _check(xh, top, C, S):
 
 
 @pytest.mark.parametrize("sigma", [0.02, 1.0, 37.0])
-@pytest.mark.parametrize("C,S", [(1024, 64), (4096, 256), (16384, 1024)])
+@pytest.mark.parametrize("C,S", [(1024, 64), (4096, 256), (4096, 1024), (16384, 1024)])
 def test_bf16_escape_matches_oracle(sigma, C, S):
     top = ecc.bf16_escape_table_sigma(sigma)
     assert (top == oracle.bf16_top7_from_sigma(sigma)).all()
