@@ -269,11 +269,13 @@ __global__ void __launch_bounds__(kBfWarpThreads) bf16_encode_warp_kernel(BfEncP
             break;
         const uint64_t base = c * p.C;
         const uint32_t L = (uint32_t)min((uint64_t)p.C, p.n - base);
-        uint32_t run = 0; // bits of the chunk's earlier rounds
-        for (uint32_t t0 = 0; t0 < L; t0 += kBfRound) {
+        // the lane's 16 values of the round starting at t0 (zeros past the chunk)
+        auto load_round = [&](uint32_t t0, uint32_t (&w)[8]) {
             const uint32_t my0 = t0 + (uint32_t)lane * kBfPerThread;
             const uint32_t cnt = my0 < L ? min(kBfPerThread, L - my0) : 0u;
-            uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                w[k] = 0;
             if (cnt == kBfPerThread) {
                 const uint4 a = ld_stream16(p.in + base + my0), b = ld_stream16(p.in + base + my0 + 8);
                 w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
@@ -283,6 +285,19 @@ __global__ void __launch_bounds__(kBfWarpThreads) bf16_encode_warp_kernel(BfEncP
                     if (j < cnt)
                         w[j >> 1] |= (uint32_t)p.in[base + my0 + j] << (16 * (j & 1));
             }
+        };
+        uint32_t wn[8]; // the next round's values, loaded one round ahead
+        load_round(0, wn);
+        uint32_t run = 0; // bits of the chunk's earlier rounds
+        for (uint32_t t0 = 0; t0 < L; t0 += kBfRound) {
+            const uint32_t my0 = t0 + (uint32_t)lane * kBfPerThread;
+            const uint32_t cnt = my0 < L ? min(kBfPerThread, L - my0) : 0u;
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                w[k] = wn[k];
+            if (t0 + kBfRound < L)
+                load_round(t0 + kBfRound, wn);
             uint32_t bits = 0;
 #pragma unroll
             for (uint32_t j = 0; j < kBfPerThread; ++j) {
