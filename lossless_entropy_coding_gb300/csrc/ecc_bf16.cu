@@ -376,13 +376,17 @@ struct BfDecParams {
     uint64_t n_chunks;
 };
 
-// One value of a lane's stream: the window (hi, lo, nx) holds the next 96
-// bits from bit o of hi (o < 32); w is the stream's word after nx, loaded
-// ahead.  A value takes 11 or 19 bits, so the window moves by at most one
-// word.  tA/tB: the table's exponents 0-3 and 4-6, one a byte.  Returns the
-// BF16 value; sets bad for 000 followed by a table exponent.
-__device__ __forceinline__ uint32_t bf_step(uint32_t &hi, uint32_t &lo, uint32_t &nx, uint32_t &o, uint32_t &wi,
-                                            uint32_t w, uint32_t tA, uint32_t tB, const uint8_t *rank, bool &bad)
+// One value of a lane's stream: the window (hi, lo, nx, nn) holds the next
+// 128 bits from bit o of hi (o < 32), wi is the index of the word after nn.
+// A value takes 11 or 19 bits, so the window moves by at most one word; when
+// it does, the word after nn is loaded (word(wi)), and its value is needed
+// only at a later move, two or more values on, which hides the load.
+// tA/tB: the table's exponents 0-3 and 4-6, one a byte.  Returns the BF16
+// value; sets bad for 000 followed by a table exponent.
+template <typename WordFn>
+__device__ __forceinline__ uint32_t bf_step(uint32_t &hi, uint32_t &lo, uint32_t &nx, uint32_t &nn, uint32_t &o,
+                                            uint32_t &wi, const WordFn &word, uint32_t tA, uint32_t tB,
+                                            const uint8_t *rank, bool &bad)
 {
     const uint32_t top = __funnelshift_l(lo, hi, o);
     const uint32_t code = top >> 29;
@@ -396,8 +400,11 @@ __device__ __forceinline__ uint32_t bf_step(uint32_t &hi, uint32_t &lo, uint32_t
     const bool adv = o >= 32u;
     hi = adv ? lo : hi;
     lo = adv ? nx : lo;
-    nx = adv ? w : nx;
-    wi += adv ? 1u : 0u;
+    nx = adv ? nn : nx;
+    if (adv) {
+        nn = word(wi);
+        ++wi;
+    }
     o &= 31u;
     return ((tail & 0x80u) << 8) | (e << 7) | (tail & 0x7Fu);
 }
@@ -460,16 +467,16 @@ __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
             }
             const uint32_t v0 = j << s_shift, v1 = min(v0 + p.S, L);
             uint32_t wi = (uint32_t)(start >> 5), o = (uint32_t)start & 31u;
-            uint32_t hi = word(wi), lo = word(wi + 1), nx = word(wi + 2);
-            wi += 3; // the next word to load
+            uint32_t hi = word(wi), lo = word(wi + 1), nx = word(wi + 2), nn = word(wi + 3);
+            wi += 4; // the next word to load
             uint16_t *dst = p.out + base;
             uint32_t v = v0;
             for (; v + 8 <= v1; v += 8) { // p.out + base + v is 16-byte aligned (C, S multiples of 8)
                 uint32_t q[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const uint32_t a = bf_step(hi, lo, nx, o, wi, word(wi), tA, tB, rank, bad);
-                    const uint32_t b = bf_step(hi, lo, nx, o, wi, word(wi), tA, tB, rank, bad);
+                    const uint32_t a = bf_step(hi, lo, nx, nn, o, wi, word, tA, tB, rank, bad);
+                    const uint32_t b = bf_step(hi, lo, nx, nn, o, wi, word, tA, tB, rank, bad);
                     q[h] = a | b << 16;
                 }
 #ifdef ECC_CHECKED
@@ -481,9 +488,9 @@ __global__ void __launch_bounds__(256) bf16_decode_kernel(BfDecParams p)
                 *reinterpret_cast<uint4 *>(dst + v) = make_uint4(q[0], q[1], q[2], q[3]);
             }
             for (; v < v1; ++v)
-                dst[v] = (uint16_t)bf_step(hi, lo, nx, o, wi, word(wi), tA, tB, rank, bad);
-            // consumed bits: (words loaded - 3) * 32 + o
-            bad |= (uint64_t)(wi - 3u) * 32u + o - start != sb;
+                dst[v] = (uint16_t)bf_step(hi, lo, nx, nn, o, wi, word, tA, tB, rank, bad);
+            // consumed bits: (words loaded - 4) * 32 + o
+            bad |= (uint64_t)(wi - 4u) * 32u + o - start != sb;
         }
         // the chunk ends at its padded size, and the padding is zero
         if (lane == 0) {
