@@ -3,11 +3,12 @@
 // communication: many tensors of very different sizes).  See ecc.h.
 //
 // The host orders the tensors by codebook (stable: equal codebooks keep the
-// caller's order) and lays their chunks end to end in that order.  A
-// prologue kernel writes item[i] = tensor << 32 | chunk for every position,
-// so a kernel finds its work with one load instead of a search, and a CTA
-// reloads its shared code tables only where the codebook changes (a few
-// times per launch) instead of at almost every chunk.
+// caller's order) and lays their chunks (decode: the pieces of their chunks,
+// as the single-tensor decoder splits them) end to end in that order.  A
+// prologue kernel writes item[i] = tensor << 32 | chunk (or piece) for every
+// position, so a kernel finds its work with one load instead of a search,
+// and a CTA reloads its shared code tables only where the codebook changes
+// (a few times per launch) instead of at almost every chunk.
 
 #include <algorithm>
 #include <cstdint>
@@ -33,7 +34,7 @@ struct BatchHeader {
     uint32_t encode;
     uint32_t ws_slot_bytes; // encode: stage slot of the warp-specialised kernel (largest over the tensors)
     uint32_t pad;
-    uint64_t n_items;     // encode: chunks; decode: chunks, each codebook run padded to a multiple of warps
+    uint64_t n_items;     // encode: chunks; decode: pieces, each codebook run padded to a multiple of warps
     uint64_t total_chunks;
     uint64_t desc_off, prefix_off, done_off, item_off, flags_off;
 };
@@ -59,6 +60,10 @@ static BatchLayout layout_for(uint32_t count, uint64_t n_items, uint64_t flag_wo
 }
 
 __device__ __forceinline__ uint64_t chunks_of(const ecc_desc &d) { return (d.n + d.C - 1) >> (31 - __clz(d.C)); }
+
+// The batched decoder's split of a tensor's chunks: one or two streams a
+// lane, pieces of at most kDecPieceSyms symbols.
+__host__ __device__ inline DecSplit batch_split(const ecc_desc &d) { return dec_split(d.C, d.S, 2); }
 
 __global__ void batch_prologue_kernel(uint8_t *ws)
 {
@@ -93,8 +98,9 @@ __global__ void batch_prologue_kernel(uint8_t *ws)
             else
                 hi = mid;
         }
-        const uint64_t c = i - prefix[lo];
-        item[i] = c < chunks_of(descs[lo]) ? ((uint64_t)lo << 32 | c) : kNoItem;
+        const uint64_t c = i - prefix[lo]; // the chunk (decode: the piece) within its tensor
+        const uint32_t ps = h->encode ? 0u : batch_split(descs[lo]).ps;
+        item[i] = c < (chunks_of(descs[lo]) << ps) ? ((uint64_t)lo << 32 | c) : kNoItem;
     }
     if (h->encode)
         for (uint64_t i = i0; i < h->total_chunks; i += stride)
@@ -290,8 +296,11 @@ __global__ void __launch_bounds__(kEncThreads) encode_batched_kernel(uint8_t *ws
 // (warp w the group's item w), the schedule of the single-tensor decoder.
 // Codebook runs are padded to whole groups, so a group has one codebook and
 // every warp of a CTA meets the codebook changes at the same groups.
-template <int R>
-__global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
+// An item is a piece of a chunk (dec_split with at most 2 streams a lane,
+// per tensor): the warp decodes it with its own streams a lane.  At most 128
+// registers (batched message workload, decode GB/s: 417 at 96, 430 at 112,
+// 437 at 128, 358 at 144 and 363 uncapped at 168, with fewer warps).
+__global__ void __maxnreg__(128) decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
 {
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t *dec = reinterpret_cast<uint16_t *>(smem);
@@ -341,20 +350,35 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
         if (m == kNoItem)
             continue;
         const uint32_t k = (uint32_t)(m >> 32);
-        const uint64_t c = m & 0xFFFFFFFFull;
+        const uint64_t local = m & 0xFFFFFFFFull;
         const ecc_desc &d = descs[k];
         const uint64_t nch = chunks_of(d);
+        const DecSplit sp = batch_split(d);
+        const uint64_t c = local >> sp.ps;
+        const uint32_t piece = (uint32_t)local & ((1u << sp.ps) - 1u);
         if (loaded_ok) {
             const DecJob job{d.in, d.cap, d.chunk_off, d.sub_bits, d.n, d.C, d.S, d.cb, d.out, d.status};
-            // next chunk is another tensor's: no L2 prefetch
+            // (the next item is another warp's: no L2 prefetch)
+            auto run = [&](const DecTables &T, auto qlc) {
+                constexpr bool kQ = decltype(qlc)::value;
+                if (sp.ps == 0) {
+                    if (sp.R == 2)
+                        decode_chunk<2, kQ>(job, T, wst, c, nch, nch);
+                    else
+                        decode_chunk<1, kQ>(job, T, wst, c, nch, nch);
+                } else if (sp.R == 2) {
+                    decode_piece<2, kQ>(job, T, wst, c, piece, sp.ps);
+                } else {
+                    decode_piece<1, kQ>(job, T, wst, c, piece, sp.ps);
+                }
+            };
             if (loaded_qlc) {
-                const DecTables T = qlc_tables(cb->dec, &lt, qs, reinterpret_cast<const uint32_t *>(smem));
-                decode_chunk<R, true>(job, T, wst, c, nch, nch);
+                run(qlc_tables(cb->dec, &lt, qs, reinterpret_cast<const uint32_t *>(smem)), std::true_type{});
             } else {
                 DecTables T{};
                 T.dec = dec;
                 T.lt = &lt;
-                decode_chunk<R, false>(job, T, wst, c, nch, nch);
+                run(T, std::false_type{});
             }
         } else if (lane == 0) {
             set_status(d.status, ECC_ERR_CODEBOOK);
@@ -362,7 +386,7 @@ __global__ void decode_batched_kernel(uint8_t *ws, uint64_t *t_start)
         if (d.t_done_ns) {
             __threadfence(); // this lane's output stores before the completion count
             __syncwarp();
-            if (lane == 0 && atomicAdd(done + k, 1u) + 1u == nch)
+            if (lane == 0 && atomicAdd(done + k, 1u) + 1u == (uint32_t)(nch << sp.ps))
                 *d.t_done_ns = globaltimer();
         }
     }
@@ -381,23 +405,15 @@ struct BatchPlan {
     std::vector<uint64_t> prefix;
     uint64_t n_items = 0, total_chunks = 0;
     uint32_t max_C = 1024, warps = 1, stage = 0, ws_slot = 0, dec_stage = 0;
-    int R = 4; // decode: streams per lane, the smallest any tensor allows
 };
 
-const void *batch_decode_kernel(int R)
-{
-    return R == 4 ? (const void *)decode_batched_kernel<4>
-           : R == 2 ? (const void *)decode_batched_kernel<2>
-                    : (const void *)decode_batched_kernel<1>;
-}
-
 // as many warps as shared memory holds stages for, and registers allow
-uint32_t batch_decode_warps(uint32_t stage, int R)
+uint32_t batch_decode_warps(uint32_t stage)
 {
     int warps = decode_warps(stage);
     while (warps > 1 &&
            (kDecHeadBytes + (size_t)warps * stage > kMaxDynSmem - kStaticSmemReserve ||
-            occupancy(batch_decode_kernel(R), warps * 32,
+            occupancy((const void *)decode_batched_kernel, warps * 32,
                       std::max<size_t>(kDecMinSmem, kDecHeadBytes + (size_t)warps * stage)) <= 0))
         --warps;
     return (uint32_t)warps;
@@ -425,15 +441,12 @@ ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool c
         P->total_chunks += nc;
         P->max_C = std::max(P->max_C, d.C);
         P->ws_slot = std::max(P->ws_slot, enc_ws_slot_bytes(d.C, d.S));
-        // decode stage: the single-tensor decoder's (a chunk at up to 9.25
+        // decode stage: the single-tensor decoder's for a piece (at up to 9.25
         // bits a symbol, larger ones 32 sub-blocks at a time), for every shape
-        P->dec_stage = std::max(P->dec_stage, dec_stage_bytes(d.C, d.S));
-        if (d.n)
-            P->R = std::min<int>(P->R, (int)std::max<uint32_t>(1, d.C / d.S / 32));
+        P->dec_stage = std::max(P->dec_stage, dec_stage_bytes(d.C >> batch_split(d).ps, d.S));
     }
     P->stage = encode ? stage_bytes_for(P->max_C) : P->dec_stage;
-    P->R = P->R >= 4 ? 4 : P->R >= 2 ? 2 : 1;
-    P->warps = encode ? 1u : batch_decode_warps(P->stage, P->R);
+    P->warps = encode ? 1u : batch_decode_warps(P->stage);
     P->order.resize(count);
     std::iota(P->order.begin(), P->order.end(), 0u);
     std::stable_sort(P->order.begin(), P->order.end(), [&](uint32_t a, uint32_t b) {
@@ -447,7 +460,7 @@ ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool c
         if (!encode && j > 0 && d.cb != descs[P->order[j - 1]].cb)
             acc = (acc + P->warps - 1) / P->warps * P->warps;
         P->prefix[j] = acc;
-        acc += valid_sizes(d.C, d.S) ? ecc_num_chunks(d.n, d.C) : 0;
+        acc += valid_sizes(d.C, d.S) ? ecc_num_chunks(d.n, d.C) << (encode ? 0u : batch_split(d).ps) : 0;
     }
     if (!encode)
         acc = (acc + P->warps - 1) / P->warps * P->warps;
@@ -528,18 +541,11 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
         return launch_status(cudaGetLastError());
     }
     const size_t smem = std::max<size_t>(kDecMinSmem, kDecHeadBytes + (size_t)P.warps * P.stage);
-    const void *kfn = batch_decode_kernel(P.R);
-    const int occ = occupancy(kfn, (int)P.warps * 32, smem);
+    const int occ = occupancy((const void *)decode_batched_kernel, (int)P.warps * 32, smem);
     if (occ <= 0)
         return ECC_ERR_CUDA;
     const uint64_t grid = std::min<uint64_t>((uint64_t)occ * sms, P.n_items / P.warps);
-    const unsigned threads = P.warps * 32;
-    if (P.R == 4)
-        decode_batched_kernel<4><<<(unsigned)grid, threads, smem, st>>>((uint8_t *)ws, t_start);
-    else if (P.R == 2)
-        decode_batched_kernel<2><<<(unsigned)grid, threads, smem, st>>>((uint8_t *)ws, t_start);
-    else
-        decode_batched_kernel<1><<<(unsigned)grid, threads, smem, st>>>((uint8_t *)ws, t_start);
+    decode_batched_kernel<<<(unsigned)grid, P.warps * 32, smem, st>>>((uint8_t *)ws, t_start);
     return launch_status(cudaGetLastError());
 }
 

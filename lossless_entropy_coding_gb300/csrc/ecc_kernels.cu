@@ -751,16 +751,10 @@ ecc_status ecc_decode(const uint8_t *in, size_t in_bytes, const uint64_t *chunk_
     DecParams p;
     p.job = DecJob{in, in_bytes, chunk_off, sub_bits, n, C, S, cb, out, status};
     p.n_chunks = ecc_num_chunks(n, C);
-    // streams per lane: C/S sub-blocks per chunk over 32 lanes, at most 4,
-    // and a warp's 32 x per_lane sub-blocks at most kDecPieceSyms symbols; a
-    // chunk of more sub-blocks is decoded in pieces of that many, one warp
-    // each, so that the stages stay as small as for a chunk of that size
-    uint32_t per_lane = std::min<uint32_t>(4, std::max<uint32_t>(1, C / S / 32));
-    while (per_lane > 1 && 32u * per_lane * S > kDecPieceSyms)
-        per_lane >>= 1;
-    p.pshift = 0;
-    while ((C / S >> p.pshift) > 32u * per_lane)
-        ++p.pshift;
+    // streams per lane and pieces of a chunk (up to 4 streams)
+    const DecSplit split = dec_split(C, S, 4);
+    const uint32_t per_lane = split.R;
+    p.pshift = split.ps;
     p.stage_bytes = dec_stage_bytes(C >> p.pshift, S);
     const bool pieces = p.pshift > 0;
     const void *kfn = per_lane == 4   ? (pieces ? (const void *)decode_kernel<4, true> : (const void *)decode_kernel<4, false>)

@@ -17,6 +17,26 @@ constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may a
 constexpr int kDecMaxWarps = 22;
 constexpr uint32_t kDecPieceSyms = 8192; // symbols one decoding warp stages at most (but 32 sub-blocks)
 
+// How a decoding warp splits a chunk of C symbols in sub-blocks of S: R
+// streams a lane (C / S sub-blocks over 32 lanes, at most rmax, with a
+// warp's 32 R sub-blocks at most kDecPieceSyms symbols), and chunks of more
+// than 32 R sub-blocks in 2^ps pieces of 32 R sub-blocks, one warp a piece,
+// so that a warp's stage stays as small as for a chunk of that size.
+struct DecSplit {
+    uint32_t R, ps;
+};
+__host__ __device__ inline DecSplit dec_split(uint32_t C, uint32_t S, uint32_t rmax)
+{
+    uint32_t R = C / S / 32u;
+    R = R < 1u ? 1u : (R > rmax ? rmax : R);
+    while (R > 1u && 32u * R * S > kDecPieceSyms)
+        R >>= 1;
+    uint32_t ps = 0;
+    while ((C / S >> ps) > 32u * R)
+        ++ps;
+    return DecSplit{R, ps};
+}
+
 bool valid_sizes(uint32_t C, uint32_t S);
 // shared input buffers of the encoder (2 = the next chunk is prefetched)
 uint32_t enc_input_buffers(uint32_t C);
