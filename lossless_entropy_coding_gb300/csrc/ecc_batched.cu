@@ -405,6 +405,7 @@ struct BatchPlan {
     std::vector<uint64_t> prefix;
     uint64_t n_items = 0, total_chunks = 0;
     uint32_t max_C = 1024, warps = 1, stage = 0, ws_slot = 0, dec_stage = 0;
+    bool units = true; // every tensor's chunks are of kUnitSyms symbols: the unit encoder codes the batch
 };
 
 // as many warps as shared memory holds stages for, and registers allow
@@ -439,6 +440,7 @@ ecc_status plan_batch(const ecc_desc *descs, uint32_t count, bool encode, bool c
         if (nc >= kMaxItems)
             return ECC_ERR_ARG;
         P->total_chunks += nc;
+        P->units = P->units && (d.n == 0 || d.C == kUnitSyms);
         P->max_C = std::max(P->max_C, d.C);
         P->ws_slot = std::max(P->ws_slot, enc_ws_slot_bytes(d.C, d.S));
         // decode stage: the single-tensor decoder's for a piece (at up to 9.25
@@ -518,6 +520,25 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     if (P.n_items == 0)
         return ECC_OK;
     if (encode) {
+        // the chunks it leaves to the deferred pass (long codes)
+        auto deferred = [&]() {
+            const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((P.n_items + 7) / 8, (uint64_t)sms * 8));
+            encode_batched_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>((uint8_t *)ws);
+            return launch_status(cudaGetLastError());
+        };
+        if (P.units) {
+            uint8_t *w = (uint8_t *)ws;
+            const UnitBatch ub{reinterpret_cast<const uint64_t *>(w + L.item_off),
+                               reinterpret_cast<const ecc_desc *>(w + L.desc_off),
+                               reinterpret_cast<uint64_t *>(w + L.flags_off),
+                               reinterpret_cast<uint32_t *>(w + L.done_off),
+                               &reinterpret_cast<BatchHeader *>(w)->ticket,
+                               sorted[0].status,
+                               t_start,
+                               P.total_chunks};
+            if (launch_unit_encoder_batched(ub, st) == ECC_OK)
+                return deferred();
+        }
         const size_t ws_smem = enc_ws_smem_bytes(P.max_C, P.ws_slot);
         const int occ_ws = ws_smem <= kMaxDynSmem - kStaticSmemReserve
                                ? occupancy((const void *)encode_batched_ws_kernel, kEncThreadsWS, ws_smem)
@@ -527,10 +548,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
             encode_batched_ws_kernel<<<(unsigned)grid, kEncThreadsWS, ws_smem, st>>>((uint8_t *)ws, t_start);
             if ((e = launch_status(cudaGetLastError())) != ECC_OK)
                 return e;
-            // the chunks it left to the deferred pass (long codes)
-            const uint64_t blocks = std::max<uint64_t>(1, std::min<uint64_t>((P.n_items + 7) / 8, (uint64_t)sms * 8));
-            encode_batched_deferred_kernel<<<(unsigned)blocks, 256, 0, st>>>((uint8_t *)ws);
-            return launch_status(cudaGetLastError());
+            return deferred();
         }
         const size_t smem = enc_shared_bytes() + kBatchSlotBytes + (size_t)P.max_C + kStageLead + P.stage;
         const int occ = occupancy((const void *)encode_batched_kernel, kEncThreads, smem);

@@ -16,6 +16,7 @@ constexpr size_t kMaxDynSmem = 227 * 1024; // per-CTA shared memory opt-in limit
 constexpr size_t kStaticSmemReserve = 64;  // static shared bytes a kernel may add on top
 constexpr int kDecMaxWarps = 22;
 constexpr uint32_t kDecPieceSyms = 8192; // symbols one decoding warp stages at most (but 32 sub-blocks)
+constexpr uint32_t kUnitSyms = 16384;    // symbols of a unit of the unit encoder
 
 // How a decoding warp splits a chunk of C symbols in sub-blocks of S: R
 // streams a lane (C / S sub-blocks over 32 lanes, at most rmax, with a
@@ -51,5 +52,21 @@ int occupancy(const void *kernel, int threads, size_t smem);
 // The unit encoder for chunks of at most 16384 symbols (ecc_units.cu).
 // (unit_chunks: the chunks of a unit, for the deferred pass)
 ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st, uint32_t *unit_chunks);
+// The unit encoder over many tensors whose chunks are all of 16384 symbols,
+// a chunk a unit (ecc_units.cu): unit k is chunk items[k] & 0xFFFFFFFF of
+// tensor descs[items[k] >> 32]; flags: a look-back word per unit (zeroed);
+// done: a counter per tensor (zeroed) for the completion stamps; status:
+// where waits that end before their unit is known report.
+struct UnitBatch {
+    const uint64_t *items;
+    const ecc_desc *descs;
+    uint64_t *flags;
+    uint32_t *done;
+    uint32_t *ticket;
+    uint32_t *status;
+    uint64_t *t_start;
+    uint64_t n_units;
+};
+ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st);
 
 } // namespace ecc

@@ -62,7 +62,7 @@
 
 namespace ecc {
 
-constexpr uint32_t kUSyms = 16384;                   // symbols of a unit
+constexpr uint32_t kUSyms = kUnitSyms;               // symbols of a unit
 constexpr uint32_t kUThr = 32;                       // symbols of a compute thread
 constexpr uint32_t kUWarps = kUSyms / (32 * kUThr);  // compute warps (16)
 constexpr uint32_t kUCompute = 32 * kUWarps;         // compute threads (512)
@@ -70,6 +70,7 @@ constexpr uint32_t kUThreads = kUCompute + 64;       // + the loader and the sto
 constexpr uint64_t kUEnd = ~0ull;                    // slot holds no unit: the pipeline ends
 constexpr uint32_t kULutBytes = kLutRows * kLutReplicas * 8u;
 constexpr uint32_t kUBarCompute = 1;                 // named barrier of the compute warps
+constexpr uint32_t kUBarTables = 2;                  // ... around a reload of the code tables
 // what a unit holds: a whole chunk, whole smaller chunks, or part of a chunk
 constexpr int kUnitOne = 0, kUnitGroup = 1, kUnitSplit = 2;
 // Word of a unit of a split chunk that is not the chunk's last: kFlagAggregate
@@ -122,7 +123,41 @@ struct UnitParams {
     uint32_t *ticket;
     uint32_t stage_bytes; // payload bytes a stage holds (multiple of 16)
     uint64_t timeout_ns;
+    // Many-tensor launch (chunks of kUSyms symbols, a unit each): unit k is
+    // chunk items[k] & 0xFFFFFFFF of tensor items[k] >> 32; job.flags holds
+    // a look-back word per unit, job.status receives the errors of waits
+    // that end before their unit is known; done counts each tensor's coded
+    // segments for its completion stamp; *t_start (may be null) is stamped
+    // at the start.
+    const uint64_t *items;
+    const ecc_desc *descs;
+    uint32_t *done;
+    uint64_t *t_start;
 };
+
+// Unit k of a many-tensor launch: its chunk as a job of its own (look-back
+// words offset to its tensor's), the chunk's index in its tensor, and the
+// tensor's.
+struct UItem {
+    EncJob job;
+    uint64_t c;
+    uint32_t tensor;
+};
+__device__ __forceinline__ UItem unit_item(const UnitParams &p, uint64_t k)
+{
+    const uint64_t it = p.items[k];
+    const uint32_t t = (uint32_t)(it >> 32);
+    const uint64_t c = it & 0xFFFFFFFFull;
+    const ecc_desc &d = p.descs[t];
+    return UItem{EncJob{d.in, d.n, d.cb, d.C, d.S, d.out, d.cap, d.chunk_off, d.sub_bits, d.total_bits,
+                        p.job.flags + (k - c), d.status},
+                 c, t};
+}
+
+__device__ __forceinline__ bool codebook_ok(const ecc_codebook *cb)
+{
+    return cb->magic == ECC_CODEBOOK_MAGIC && cb->max_len <= ECC_MAX_CODE_LEN;
+}
 
 __host__ __device__ constexpr size_t unit_smem_bytes(uint32_t stage_bytes)
 {
@@ -607,31 +642,57 @@ __device__ __forceinline__ uint32_t len4(const uint8_t *len, uint32_t w)
     return (uint32_t)len[byte_of(w, 0)] + len[byte_of(w, 1)] + len[byte_of(w, 2)] + len[byte_of(w, 3)];
 }
 
-template <int kMode>
-__device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, const uint2 *lut, const uint8_t *len,
+// The shared tables of codebook cb (valid), filled by the threads i0,
+// i0 + stride, ...: the code table (each code replicated kLutReplicas
+// times) and the length table (at the rotated byte values).
+__device__ __forceinline__ void unit_load_lut(const ecc_codebook *cb, uint2 *lut, uint32_t i0, uint32_t stride)
+{
+    for (uint32_t i = i0; i < kLutRows * kLutReplicas; i += stride) {
+        const uint32_t s = i / kLutReplicas;
+        lut[i] = make_uint2(cb->enc_code[s], cb->enc_mul[s]);
+    }
+}
+__device__ __forceinline__ void unit_load_len(const ecc_codebook *cb, uint8_t *len, uint32_t i0, uint32_t stride)
+{
+    for (uint32_t i = i0; i < kLutRows; i += stride)
+        len[len_rot(i)] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
+}
+
+// (lens: the length table; a many-tensor launch: one a slot)
+template <int kMode, bool kBatch = false>
+__device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint2 *lut, const uint8_t *lens,
                                              uint32_t in0, uint32_t st0, uint32_t w, uint32_t lane)
 {
+    static_assert(!kBatch || kMode == kUnitOne, "a many-tensor launch codes a chunk a unit");
     constexpr bool kOne = kMode != kUnitGroup; // the unit's codes are one run (one chunk, or part of one)
     // stage words in memory order (the storer copies them out as they are),
     // or in register order (split chunks: the storer shifts them first)
     constexpr bool kSwap = kMode != kUnitSplit;
-    const EncJob &job = p.job;
     const uint2 *lt = lut + (lane & (kLutReplicas - 1u));
-    const uint32_t s_shift = 31u - __clz(job.S);
-    const uint32_t tps = job.S / kUThr;                          // threads per sub-block: 2..32
-    const uint32_t wpc = kOne ? kUWarps : job.C / (32u * kUThr); // warps per chunk: 1..16
+    const uint32_t wpc = kOne ? kUWarps : p.job.C / (32u * kUThr); // warps per chunk: 1..16
     const uint32_t t = w * 32u + lane;
     const uint32_t s0 = t * kUThr;
-    const uint64_t n_sub = (job.n + job.S - 1) >> s_shift;
+    [[maybe_unused]] const ecc_codebook *loaded = nullptr; // many-tensor launch: the code table's codebook
     for (uint64_t k = 0; k <= p.n_units; ++k) {
         const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r = (uint32_t)k & 3u;
         const bool ok = mbar_wait(&P.full[slot], par, p.timeout_ns);
         if (!ok)
-            set_status(job.status, ECC_ERR_TIMEOUT);
+            set_status(p.job.status, ECC_ERR_TIMEOUT);
         const uint64_t u = ok ? (uint64_t)*(volatile uint64_t *)&P.unit[slot] : (uint64_t)kUEnd;
         const bool end = u == kUEnd;
-        const uint64_t ubase = end ? 0 : u * kUSyms;
-        const uint32_t L = end ? 0u : (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
+        // the unit's job, and the unit's index in it (a many-tensor launch:
+        // its chunk of its tensor)
+        const UItem I = kBatch && !end ? unit_item(p, u) : UItem{p.job, u, 0u};
+        const EncJob &job = I.job;
+        const uint64_t uc = I.c;
+        const uint32_t s_shift = 31u - __clz(job.S);
+        const uint32_t tps = job.S / kUThr; // threads per sub-block: 2..32
+        // a many-tensor launch: a broken codebook codes nothing; the length
+        // table is the slot's (the loader fills it with the input)
+        const bool cb_ok = !kBatch || end || codebook_ok(job.cb);
+        const uint8_t *len = kBatch ? lens + slot * kLutRows : lens;
+        const uint64_t ubase = end ? 0 : uc * kUSyms;
+        const uint32_t L = end || !cb_ok ? 0u : (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
         const uint32_t cnt = s0 < L ? min(kUThr, L - s0) : 0u;
         const uint32_t src = in0 + slot * kUSyms + s0;
 
@@ -661,6 +722,17 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
             }
             break;
         }
+        if constexpr (kBatch) {
+            // A codebook other than the code table's: every compute warp is
+            // past the last unit's phase C (and holds this unit: none has
+            // ended), so the table is reloaded here, the same decision in
+            // every compute warp, before this unit's phase C reads it.
+            if (cb_ok && job.cb != loaded) {
+                unit_load_lut(job.cb, lut, t, kUCompute);
+                bar_sync(kUBarTables, kUCompute);
+                loaded = job.cb;
+            }
+        }
         const uint32_t x = lane < kUWarps ? P.wtot[r][lane] : 0u;
         const ULayout lay = unit_layout<kOne>(x, lane, wpc);
         const uint32_t wE = __shfl_sync(~0u, lay.E, w);
@@ -689,13 +761,14 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
                     st_relaxed(p.uflags + u, kFlagAggregate | utot);
             }
         } else {
-            st_relaxed_pred(job.flags + u, kFlagAggregate | ubytes, t == 0 && u != 0);
+            st_relaxed_pred(job.flags + uc, kFlagAggregate | ubytes, t == 0 && uc != 0);
         }
         st_shared_u64_pred(&P.sunit[r], u, t == 0);
         mbar_arrive_pred(&P.agg[r], t == 0);
         {
             const uint32_t sb = __shfl_sync(~0u, incl, lane | (tps - 1u)) - (incl - B);
             const uint64_t sidx = (ubase + s0) >> s_shift;
+            const uint64_t n_sub = (job.n + job.S - 1) >> s_shift;
             st_global_u16_pred(job.sub_bits + sidx, sb, cnt && (lane & (tps - 1u)) == 0 && sidx < n_sub);
         }
         const bool over = ubytes > p.stage_bytes;
@@ -792,23 +865,28 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, cons
 // Claims units in ticket order, one slot at a time as the compute warps finish
 // the unit in it (phase C reads the input again) and size the next one, and
 // bulk-copies each unit's input (lane 0 alone).
-__device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8_t *in0, uint32_t lane)
+// A many-tensor launch: the loader also fills the slot's length table for
+// the unit's codebook (when it is not the one the slot's table holds) before
+// the slot's arrival, as it does the input bytes it copies itself.
+template <bool kBatch = false>
+__device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8_t *in0,
+                                            [[maybe_unused]] uint8_t *lens, uint32_t lane)
 {
     if (lane != 0)
         return;
-    const EncJob &job = p.job;
+    [[maybe_unused]] const ecc_codebook *held0 = nullptr, *held1 = nullptr; // codebooks of the slots' length tables
     for (uint64_t k = 0; k <= p.n_units; ++k) {
         const uint32_t slot = (uint32_t)k & 1u;
         bool stop = false;
         if (k >= 2 && !mbar_wait(&P.done[slot], (uint32_t)((k - 2) >> 1) & 1u, p.timeout_ns)) {
-            set_status(job.status, ECC_ERR_TIMEOUT);
+            set_status(p.job.status, ECC_ERR_TIMEOUT);
             stop = true;
         }
         // claim late, once the compute warps have sized the unit in the other
         // slot: a unit is then sized soon after its ticket, and the
         // look-backs of later units wait less for it
         if (k >= 2 && !stop && !mbar_wait(&P.agg[(k - 1) & 3u], (uint32_t)((k - 1) >> 2) & 1u, p.timeout_ns)) {
-            set_status(job.status, ECC_ERR_TIMEOUT);
+            set_status(p.job.status, ECC_ERR_TIMEOUT);
             stop = true;
         }
         const uint32_t tk = stop ? 0xFFFFFFFFu : atomicAdd(p.ticket, 1u);
@@ -819,12 +897,23 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
         }
         const uint64_t u = tk;
         P.unit[slot] = u;
+        const UItem I = kBatch ? unit_item(p, u) : UItem{p.job, u, 0u};
+        const EncJob &job = I.job;
         uint8_t *buf = in0 + slot * kUSyms;
-        const uint64_t ubase = u * kUSyms;
+        const uint64_t ubase = I.c * kUSyms;
         const uint32_t L = (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
         const uint32_t whole = L & ~15u;
         for (uint32_t i = whole; i < L; ++i) // the tensor's last bytes (fewer than 16)
             buf[i] = job.in[ubase + i];
+        if constexpr (kBatch) {
+            if (job.cb != (slot ? held1 : held0) && codebook_ok(job.cb)) {
+                unit_load_len(job.cb, lens + slot * kLutRows, 0u, 1u);
+                if (slot)
+                    held1 = job.cb;
+                else
+                    held0 = job.cb;
+            }
+        }
         fence_proxy_async();
         mbar_expect_tx(&P.full[slot], whole);
         if (whole)
@@ -835,20 +924,19 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
 // ---------------------------------------------------------------- storer warp
 // For each unit: its offset (look-back, while the compute warps pack it),
 // chunk_off, total_bits, then the stage to the output with one bulk copy.
-template <bool kOne>
+template <bool kOne, bool kBatch = false>
 __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint32_t st0, uint32_t lane)
 {
-    const EncJob &job = p.job;
-    const uint32_t G = kOne ? 1u : kUSyms / job.C;
-    const uint32_t wpc = kOne ? kUWarps : job.C / (32u * kUThr);
-    const uint64_t n_chunks = (job.n + job.C - 1) / job.C;
+    const uint32_t G = kOne ? 1u : kUSyms / p.job.C;
+    const uint32_t wpc = kOne ? kUWarps : p.job.C / (32u * kUThr);
     int64_t known = -1; // the CTA's previous unit, whose inclusive prefix is known_incl
     uint64_t known_incl = 0;
+    [[maybe_unused]] uint32_t known_t = 0xFFFFFFFFu; // many-tensor launch: the previous unit's tensor
     for (uint64_t k = 0; k <= p.n_units; ++k) {
         const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r = (uint32_t)k & 3u;
         if (!mbar_wait(&P.agg[r], (uint32_t)(k >> 2) & 1u, p.timeout_ns)) {
             if (lane == 0)
-                set_status(job.status, ECC_ERR_TIMEOUT);
+                set_status(p.job.status, ECC_ERR_TIMEOUT);
             break;
         }
         const uint64_t u = *(volatile uint64_t *)&P.sunit[r];
@@ -864,8 +952,15 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         }
         if (u == kUEnd)
             break;
-        const uint64_t ubase = u * kUSyms;
-        const uint32_t L = (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
+        // the unit's job, and the unit's index in it (a many-tensor launch:
+        // its chunk of its tensor, whose look-back it runs)
+        const UItem I = kBatch ? unit_item(p, u) : UItem{p.job, u, 0u};
+        const EncJob &job = I.job;
+        const uint64_t uc = I.c;
+        const uint64_t n_chunks = (job.n + job.C - 1) / job.C;
+        const bool cb_ok = !kBatch || codebook_ok(job.cb); // else the compute warps coded nothing
+        const uint64_t ubase = uc * kUSyms;
+        const uint32_t L = cb_ok ? (uint32_t)min((uint64_t)kUSyms, job.n - ubase) : 0u;
         const ULayout lay = unit_layout<kOne>(x, lane, wpc);
         const uint32_t ubytes = __shfl_sync(~0u, lay.Y, kUWarps - 1u);
         uint32_t ubits = x;
@@ -873,22 +968,27 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         for (int o = 16; o; o >>= 1)
             ubits += __shfl_xor_sync(~0u, ubits, o);
         bool to = false;
-        const uint64_t prefix = unit_lookback(job.flags, u, known, known_incl, p.timeout_ns, &to);
-        if (lane == 0) // u's inclusive prefix, for the look-backs of later units
-            st_relaxed(job.flags + u, kFlagPrefix | ((prefix + ubytes) & kValueMask));
-        known = (int64_t)u;
+        const int64_t kn = kBatch && known_t != I.tensor ? -1 : known;
+        const uint64_t prefix = unit_lookback(job.flags, uc, kn, known_incl, p.timeout_ns, &to);
+        if (lane == 0) // the unit's inclusive prefix, for the look-backs of later units
+            st_relaxed(job.flags + uc, kFlagPrefix | ((prefix + ubytes) & kValueMask));
+        known = (int64_t)uc;
         known_incl = prefix + ubytes;
-        const uint64_t c0 = u * G;
+        if constexpr (kBatch)
+            known_t = I.tensor;
+        const uint64_t c0 = uc * G;
         const bool chunk_end = lane < kUWarps && (lane & (wpc - 1u)) == wpc - 1u; // a chunk's last lane
         const bool chunk_real = chunk_end && c0 + lane / wpc < n_chunks;
         if (chunk_real)
             job.chunk_off[c0 + lane / wpc + 1] = prefix + lay.Y;
         if (lane == 0) {
-            if (u == 0)
+            if (uc == 0)
                 job.chunk_off[0] = 0;
             atomicAdd((unsigned long long *)job.total_bits, (unsigned long long)ubits);
             if (to)
                 set_status(job.status, ECC_ERR_TIMEOUT);
+            if (!cb_ok)
+                set_status(job.status, ECC_ERR_CODEBOOK);
         }
         const bool fits = prefix + ubytes <= job.out_cap;
         if (!fits && !to && lane == 0)
@@ -899,11 +999,12 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
                 set_status(job.status, ECC_ERR_TIMEOUT);
             break;
         }
-        if (ubytes > p.stage_bytes) {
+        const bool deferred = ubytes > p.stage_bytes;
+        if (deferred) {
             // the unit outgrew the stage (long codes): left to the deferred
             // pass, a warp a unit over the whole GPU after this kernel
             if (write && lane == 0)
-                st_relaxed(job.flags + u, kFlagPrefix | kFlagDeferred | ((prefix + ubytes) & kValueMask));
+                st_relaxed(job.flags + uc, kFlagPrefix | kFlagDeferred | ((prefix + ubytes) & kValueMask));
         } else if (write) {
             const uint32_t st = st0 + slot * p.stage_bytes;
             // words shared across warps: warp `lane`'s first word takes the
@@ -921,8 +1022,19 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0 && (!kBatch || ubytes)) // (a broken codebook's chunk has no bytes)
                 bulk_s2g(job.out + prefix, st, ubytes);
+        }
+        if constexpr (kBatch) {
+            // the tensor's completion stamp: its segments counted as the
+            // deferred pass counts them, by whichever launch codes the chunk
+            uint64_t *t_done = p.descs[I.tensor].t_done_ns;
+            if (lane == 0 && t_done && !(deferred && write)) {
+                __threadfence();
+                const uint32_t nseg = job.C / seg_symbols(job.C, job.S);
+                if (atomicAdd(p.done + I.tensor, nseg) + nseg == nseg * (uint32_t)n_chunks)
+                    *t_done = globaltimer();
+            }
         }
         __syncwarp();
     }
@@ -1121,22 +1233,26 @@ __device__ __forceinline__ void unit_storer_split(const UnitParams &p, UPipe &P,
     }
 }
 
-// Two CTAs an SM (56 registers a thread): one CTA's barrier waits and
-// pipeline stalls are covered by the other's warps.
-template <int kMode>
-__global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
+// The pipeline of one CTA: tables, barriers, then the warps' roles.  A
+// many-tensor launch loads the code tables at each unit whose codebook is
+// not the last one's (the units come sorted by codebook).
+template <int kMode, bool kBatch>
+__device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit_smem, uint8_t *len_table)
 {
-    extern __shared__ __align__(128) uint8_t unit_smem[];
-    __shared__ uint8_t len_table[kLutRows]; // code length of byte b at len_rot(b) (at most ECC_MAX_CODE_LEN; 0: no code)
     uint2 *lut = reinterpret_cast<uint2 *>(unit_smem);
     UPipe &P = *reinterpret_cast<UPipe *>(unit_smem + kULutBytes);
     uint8_t *const base = unit_smem + kULutBytes + sizeof(UPipe);
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const ecc_codebook *cb = p.job.cb;
-    if (cb->magic != ECC_CODEBOOK_MAGIC || cb->max_len > ECC_MAX_CODE_LEN) {
-        if (threadIdx.x == 0 && blockIdx.x == 0)
-            set_status(p.job.status, ECC_ERR_CODEBOOK);
-        return;
+    if constexpr (kBatch) {
+        if (p.t_start && blockIdx.x == 0 && threadIdx.x == 0)
+            *p.t_start = globaltimer();
+    } else {
+        const ecc_codebook *cb = p.job.cb;
+        if (!codebook_ok(cb)) {
+            if (threadIdx.x == 0 && blockIdx.x == 0)
+                set_status(p.job.status, ECC_ERR_CODEBOOK);
+            return;
+        }
     }
 #ifdef ECC_CHECKED
     {   // the layout must lie inside the dynamic shared memory the launch gave
@@ -1149,12 +1265,10 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
         }
     }
 #endif
-    for (uint32_t i = threadIdx.x; i < kLutRows * kLutReplicas; i += blockDim.x) {
-        const uint32_t s = i / kLutReplicas;
-        lut[i] = make_uint2(cb->enc_code[s], cb->enc_mul[s]);
+    if constexpr (!kBatch) {
+        unit_load_lut(p.job.cb, lut, threadIdx.x, blockDim.x);
+        unit_load_len(p.job.cb, len_table, threadIdx.x, blockDim.x);
     }
-    for (uint32_t i = threadIdx.x; i < kLutRows; i += blockDim.x)
-        len_table[len_rot(i)] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
     if (threadIdx.x == 0) {
         for (int s = 0; s < 4; ++s)
             mbar_init(&P.agg[s], 1);
@@ -1168,13 +1282,32 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
     __syncthreads();
     const uint32_t st0 = smem_u32(base + 2 * kUSyms);
     if (warp < kUWarps)
-        unit_compute<kMode>(p, P, lut, len_table, smem_u32(base), st0, warp, lane);
+        unit_compute<kMode, kBatch>(p, P, lut, len_table, smem_u32(base), st0, warp, lane);
     else if (warp == kUWarps)
-        unit_loader(p, P, base, lane);
-    else if (kMode == kUnitSplit)
+        unit_loader<kBatch>(p, P, base, len_table, lane);
+    else if constexpr (kMode == kUnitSplit)
         unit_storer_split(p, P, st0, lane);
     else
-        unit_storer<kMode == kUnitOne>(p, P, st0, lane);
+        unit_storer<kMode == kUnitOne, kBatch>(p, P, st0, lane);
+}
+
+// Two CTAs an SM (56 registers a thread): one CTA's barrier waits and
+// pipeline stalls are covered by the other's warps.
+template <int kMode>
+__global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
+{
+    extern __shared__ __align__(128) uint8_t unit_smem[];
+    __shared__ uint8_t len_table[kLutRows]; // code length of byte b at len_rot(b) (at most ECC_MAX_CODE_LEN; 0: no code)
+    unit_pipeline<kMode, false>(p, unit_smem, len_table);
+}
+
+// The many-tensor launch: tensors of chunks of kUSyms symbols, a chunk a
+// unit, in the order of the item map.
+__global__ void __launch_bounds__(kUThreads, 2) encode_unit_batched_kernel(UnitParams p)
+{
+    extern __shared__ __align__(128) uint8_t unit_smem[];
+    __shared__ uint8_t len_table[2 * kLutRows]; // a length table for each input slot
+    unit_pipeline<kUnitOne, true>(p, unit_smem, len_table);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1203,7 +1336,7 @@ uint32_t unit_stage_bytes()
 // device.
 ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st, uint32_t *unit_chunks)
 {
-    UnitParams p;
+    UnitParams p{};
     p.job = job;
     p.n_units = (job.n + kUSyms - 1) / kUSyms;
     p.uflags = job.flags + (job.n + job.C - 1) / job.C;
@@ -1232,6 +1365,39 @@ ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t
     else
         encode_unit_kernel<kUnitSplit><<<(unsigned)grid, kUThreads, smem, st>>>(p);
     *unit_chunks = mode == kUnitSplit ? 1u : kUSyms / job.C;
+    return launch_status(cudaGetLastError());
+}
+
+// The many-tensor launch over n_units chunks of kUSyms symbols (the prologue
+// has cleared flags, done and the tensors' outputs; *ticket is 0).  Returns
+// ECC_ERR_CUDA, having launched nothing, if it cannot run on this device.
+ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st)
+{
+    UnitParams p{};
+    // only its look-back words and status are read (the waits that end
+    // before their unit is known report there)
+    p.job.flags = b.flags;
+    p.job.status = b.status;
+    p.job.C = kUSyms;
+    p.job.S = kUSyms;
+    p.n_units = b.n_units;
+    p.ticket = b.ticket;
+    p.timeout_ns = kWaitLimitNs;
+    p.stage_bytes = unit_stage_bytes();
+    p.items = b.items;
+    p.descs = b.descs;
+    p.done = b.done;
+    p.t_start = b.t_start;
+    if (p.stage_bytes < 16u || b.n_units == 0)
+        return ECC_ERR_CUDA;
+    const size_t smem = unit_smem_bytes(p.stage_bytes);
+    const int occ = occupancy((const void *)encode_unit_batched_kernel, kUThreads, smem);
+    const int sms = sm_count();
+    if (occ <= 0 || sms <= 0)
+        return ECC_ERR_CUDA;
+    const uint64_t need = (p.n_units + 1) / 2;
+    const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)occ * sms, need));
+    encode_unit_batched_kernel<<<(unsigned)grid, kUThreads, smem, st>>>(p);
     return launch_status(cudaGetLastError());
 }
 

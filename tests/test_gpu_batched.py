@@ -156,3 +156,16 @@ def test_batched_one_codebook_many_small(books):
     """Hundreds of small tensors sharing one codebook (a message-sized batch)."""
     spec = [(int(s), 0, 0, 4096, 64) for s in np.random.default_rng(9).integers(1, 20000, 300)]
     run_batch(books, spec)
+
+
+def test_batched_long_codes(books):
+    """N(0, 1) tensors coded with the zero-spike Huffman code (about 12.4 bits
+    a symbol, more than a chunk's stage holds at 16 KiB chunks) beside tensors
+    with short codes: their chunks are sized and placed by the encoder and
+    coded by the deferred pass, and the look-back runs across them."""
+    g = np.random.default_rng(23)
+    spec = []
+    for i in range(24):
+        size = int(g.integers(1, 5 * 16384))
+        spec.append((size, 0, 3 if i % 2 == 0 else int(g.integers(0, 3)), 16384, 256 if i % 3 else 128))
+    run_batch(books, spec)
