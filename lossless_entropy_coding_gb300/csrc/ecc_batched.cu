@@ -346,6 +346,10 @@ __global__ void __maxnreg__(128) decode_batched_kernel(uint8_t *ws, uint64_t *t_
                 load_long_table(lt, cb);
             }
             __syncthreads();
+            if (loaded_ok && lt.sub_np) { // the long codes' second level (the same decision in every thread)
+                fill_long_sub(lt, threadIdx.x, blockDim.x);
+                __syncthreads();
+            }
         }
         if (m == kNoItem)
             continue;

@@ -1902,6 +1902,18 @@ struct DecJob {
 // prefix v of the stream is a code of length L exactly when v < first[L] +
 // count[L] and no shorter length matched; the test is monotone in L, so the
 // code length is the number of lengths that fail plus the first length tried.
+//
+// Second level: a canonical code's longer codes are its numerically largest,
+// so the codes longer than the first-level table start with the few 14-bit
+// prefixes from first[14] + count[14] up (about 2^14 times their share of
+// the code space: two or three for a code whose long codes are rare under
+// its own statistics, however often the data meets them).  For those
+// sub_np prefixes, each followed by sub_kb more bits, sub[] holds
+// byte | length << 8 of the code those 14 + sub_kb bits start, or 0 when
+// the code is longer (or there is none): one lookup in place of the search
+// over the ranges.  sub_np = 0: no second level (a QLC codebook, codes
+// longer than 32 bits, or too many prefixes for kLongSubEntries).
+constexpr uint32_t kLongSubEntries = 2048;
 struct LongTable {
     uint64_t lim32[33];    // (first[L] + count[L]) << (32 - L), L <= 32
     uint64_t first[ECC_MAX_CODE_LEN + 1];
@@ -1910,6 +1922,8 @@ struct LongTable {
     uint8_t sorted[256];
     uint32_t max_len;
     uint32_t family;
+    uint32_t sub_p0, sub_np, sub_kb;
+    uint16_t sub[kLongSubEntries];
 };
 
 __device__ __forceinline__ void load_long_table(LongTable &lt, const ecc_codebook *cb)
@@ -1930,7 +1944,51 @@ __device__ __forceinline__ void load_long_table(LongTable &lt, const ecc_codeboo
     if (t == 0) {
         lt.max_len = maxl;
         lt.family = cb->family;
+        // the second level's extent (its entries: fill_long_sub, once the
+        // ranges above are in place)
+        uint32_t np = 0, kb = 0;
+        const uint64_t p0 = cb->first[ECC_PEEK_BITS] + (ECC_PEEK_BITS <= maxl ? cb->count[ECC_PEEK_BITS] : 0u);
+        if (cb->family == ECC_FAMILY_HUFFMAN && maxl > ECC_PEEK_BITS && maxl <= 32 && p0 < (1u << ECC_PEEK_BITS)) {
+            const uint64_t end = (cb->first[maxl] + cb->count[maxl]) << (32 - maxl); // past the last long code
+            const uint64_t lo = p0 << (32 - ECC_PEEK_BITS);
+            if (end > lo && end <= (1ull << 32)) {
+                np = (uint32_t)(((end - 1) >> (32 - ECC_PEEK_BITS)) - p0 + 1);
+                while (kb < maxl - ECC_PEEK_BITS && ((uint64_t)np << (kb + 1)) <= kLongSubEntries)
+                    ++kb;
+                if (kb == 0)
+                    np = 0;
+            }
+        }
+        lt.sub_p0 = (uint32_t)p0;
+        lt.sub_np = np;
+        lt.sub_kb = kb;
     }
+}
+
+// The second level's entries from the ranges (threads i0, i0 + stride, ...,
+// after a barrier that follows load_long_table; a barrier follows before
+// any lookup).
+__device__ __forceinline__ uint32_t decode_long32(uint32_t p32, const LongTable &lt);
+__device__ __forceinline__ void fill_long_sub(LongTable &lt, uint32_t i0, uint32_t stride)
+{
+    const uint32_t kb = lt.sub_kb, n = lt.sub_np << kb;
+    for (uint32_t j = i0; j < n; j += stride) {
+        // the 32-bit window of prefix sub_p0 + (j >> kb), then j's low kb bits, then zeros
+        const uint32_t v = ((lt.sub_p0 + (j >> kb)) << (32 - ECC_PEEK_BITS)) |
+                           ((j & ((1u << kb) - 1u)) << (32 - ECC_PEEK_BITS - kb));
+        const uint32_t e = decode_long32(v, lt);
+        lt.sub[j] = (uint16_t)((e >> 8) <= ECC_PEEK_BITS + kb ? e : 0u);
+    }
+}
+
+// A long code from the second level (p32: the next 32 stream bits), or 0.
+__device__ __forceinline__ uint32_t decode_sub(uint32_t p32, const LongTable &lt)
+{
+    const uint32_t j = (p32 >> (32 - ECC_PEEK_BITS)) - lt.sub_p0;
+    if (j >= lt.sub_np)
+        return 0;
+    const uint32_t kb = lt.sub_kb;
+    return lt.sub[(j << kb) | ((p32 << ECC_PEEK_BITS) >> (32 - kb))];
 }
 
 // Resolve a code longer than the first-level table.  p32 holds the next 32
@@ -2159,6 +2217,8 @@ __device__ __forceinline__ uint32_t fstep_redo(FastStream &s, const uint16_t *de
 {
     const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
     uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
+    if (e == 0)
+        e = decode_sub(p, lt);
     if (e == 0)
         e = decode_long32(p, lt);
     if (e == 0) {

@@ -411,6 +411,10 @@ __global__ void __maxnreg__(R >= 4 ? 136 : 96) decode_kernel(DecParams p)
     if (threadIdx.x == 0)
         next_item = 0;
     __syncthreads();
+    if (lt.sub_np) { // the long codes' second level (the same decision in every thread)
+        fill_long_sub(lt, threadIdx.x, blockDim.x);
+        __syncthreads();
+    }
     WarpStage ws{reinterpret_cast<uint32_t *>(smem + kDecHeadBytes + (size_t)warp * p.stage_bytes), p.stage_bytes,
                  &bars[warp], 0};
     // The warps of a CTA claim its chunks one at a time, so a warp that
