@@ -1981,16 +1981,6 @@ __device__ __forceinline__ void fill_long_sub(LongTable &lt, uint32_t i0, uint32
     }
 }
 
-// A long code from the second level (p32: the next 32 stream bits), or 0.
-__device__ __forceinline__ uint32_t decode_sub(uint32_t p32, const LongTable &lt)
-{
-    const uint32_t j = (p32 >> (32 - ECC_PEEK_BITS)) - lt.sub_p0;
-    if (j >= lt.sub_np)
-        return 0;
-    const uint32_t kb = lt.sub_kb;
-    return lt.sub[(j << kb) | ((p32 << ECC_PEEK_BITS) >> (32 - kb))];
-}
-
 // Resolve a code longer than the first-level table.  p32 holds the next 32
 // stream bits and win the next 64, MSB first.  Returns byte | len << 8, or 0
 // for a code the codebook lacks.
@@ -2210,23 +2200,39 @@ __device__ __forceinline__ uint32_t decode_long32(uint32_t p32, const LongTable 
     return at < 256 ? (uint32_t)lt.sorted[at] | (L << 8) : 0u;
 }
 
-// The redo of an iteration that met a code the table does not resolve: one
-// code at a time, codes of up to 32 bits resolved in line, longer or invalid
-// ones by fstep_slow's out-of-line path.
-__device__ __forceinline__ uint32_t fstep_redo(FastStream &s, const uint16_t *dec, const LongTable &lt, bool &bad)
+// The second level's extent, read once per redo.
+struct SubHdr {
+    uint32_t p0, np, kb;
+};
+
+// A code the two table levels do not resolve: longer ones through the
+// canonical ranges, byte | length << 8; an invalid code gives a one-bit step
+// with bit 16 set (the chunk is flagged).
+static __device__ __noinline__ uint32_t redo_long(uint32_t hi, uint32_t lo, uint32_t nx, uint32_t o, uint32_t p,
+                                                  const LongTable &lt)
+{
+    uint32_t e = decode_long32(p, lt);
+    if (e == 0)
+        e = decode_long_at(hi, lo, nx, o, lt);
+    return e ? e : (1u << 16) | (1u << 8);
+}
+
+// The redo of an iteration that met a code the first-level table does not
+// resolve: one code at a time; the second level resolves most long codes in
+// line, the rest go out of line.
+__device__ __forceinline__ uint32_t fstep_redo(FastStream &s, const uint16_t *dec, const LongTable &lt,
+                                               const SubHdr &h, bool &bad)
 {
     const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
-    uint32_t e = dec[p >> (32 - ECC_PEEK_BITS)];
-    if (e == 0)
-        e = decode_sub(p, lt);
-    if (e == 0)
-        e = decode_long32(p, lt);
+    const uint32_t top = p >> (32 - ECC_PEEK_BITS);
+    uint32_t e = dec[top];
+    const uint32_t j = top - h.p0;
+    if (e == 0 && j < h.np)
+        e = lt.sub[(j << h.kb) | ((p << ECC_PEEK_BITS) >> (32 - h.kb))];
     if (e == 0) {
-        e = decode_long_at(s.hi, s.lo, s.nx, s.o, lt);
-        if (e == 0) {
-            bad = true;
-            e = 1u << 8; // consume one bit and go on; the chunk is flagged
-        }
+        e = redo_long(s.hi, s.lo, s.nx, s.o, p, lt);
+        bad |= (e >> 16) != 0;
+        e &= 0xFFFFu;
     }
     s.o += e >> 8;
     while (s.o >= 32) {
@@ -2399,6 +2405,10 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
         for (int r = 0; r < R; ++r)
             esc |= (!kQlc && emin[r] == 0) ? (1u << r) : 0u;
         if (!kQlc && __any_sync(~0u, esc != 0)) {
+            // the lane's streams that met one, from their saved states, a
+            // code at a time (one stream after the other: interleaving the
+            // streams was slower, for the long-code chunks and the rest)
+            const SubHdr sh{lt.sub_p0, lt.sub_np, lt.sub_kb};
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (!(esc & (1u << r)))
@@ -2407,7 +2417,7 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
                 a[r] = b[r] = 0;
 #pragma unroll 1
                 for (int t = 0; t < 8; ++t) {
-                    const uint32_t e = fstep_redo(s[r], dec, lt, bad);
+                    const uint32_t e = fstep_redo(s[r], dec, lt, sh, bad);
                     if (t < 4)
                         a[r] = __byte_perm(a[r], e, 0x4321);
                     else

@@ -154,6 +154,31 @@ __device__ __forceinline__ UItem unit_item(const UnitParams &p, uint64_t k)
                  c, t};
 }
 
+// A many-tensor launch's unit as the loader resolves it when it claims the
+// unit (the CTA's k-th unit in recs[k % 4], the depth of the storer's
+// records): the compute warps and the storer then start the unit without
+// dependent global loads.  The loader claims unit k + 4 only once the
+// storer is past unit k (see the UPipe records).
+struct UUnitRec {
+    EncJob job;
+    uint64_t c;        // the unit's chunk in its tensor
+    uint64_t *t_done;  // the tensor's completion stamp (may be null)
+    uint32_t tensor;
+    uint32_t cb_ok;    // the codebook is valid
+};
+constexpr uint32_t kURecs = 4;
+
+// The job of the CTA's unit with record slot r: the launch's, or (a
+// many-tensor launch) the record's in shared memory.
+template <bool kBatch>
+__device__ __forceinline__ const EncJob &unit_job(const UnitParams &p, const UUnitRec *recs, uint32_t r)
+{
+    if constexpr (kBatch)
+        return recs[r].job;
+    else
+        return p.job;
+}
+
 __device__ __forceinline__ bool codebook_ok(const ecc_codebook *cb)
 {
     return cb->magic == ECC_CODEBOOK_MAGIC && cb->max_len <= ECC_MAX_CODE_LEN;
@@ -167,6 +192,13 @@ __host__ __device__ constexpr size_t unit_smem_bytes(uint32_t stage_bytes)
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// expected transaction bytes without an arrival (the arrival follows)
+__device__ __forceinline__ void mbar_expect_tx_only(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t bytes)
@@ -658,10 +690,12 @@ __device__ __forceinline__ void unit_load_len(const ecc_codebook *cb, uint8_t *l
         len[len_rot(i)] = (uint8_t)min((uint32_t)cb->len[i], (uint32_t)ECC_MAX_CODE_LEN);
 }
 
-// (lens: the length table; a many-tensor launch: one a slot)
+// (lens: the length table; a many-tensor launch: one a slot, and the unit
+// records recs)
 template <int kMode, bool kBatch = false>
 __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint2 *lut, const uint8_t *lens,
-                                             uint32_t in0, uint32_t st0, uint32_t w, uint32_t lane)
+                                             [[maybe_unused]] const UUnitRec *recs, uint32_t in0, uint32_t st0,
+                                             uint32_t w, uint32_t lane)
 {
     static_assert(!kBatch || kMode == kUnitOne, "a many-tensor launch codes a chunk a unit");
     constexpr bool kOne = kMode != kUnitGroup; // the unit's codes are one run (one chunk, or part of one)
@@ -682,15 +716,15 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint
         const bool end = u == kUEnd;
         // the unit's job, and the unit's index in it (a many-tensor launch:
         // its chunk of its tensor)
-        const UItem I = kBatch && !end ? unit_item(p, u) : UItem{p.job, u, 0u};
-        const EncJob &job = I.job;
-        const uint64_t uc = I.c;
+        // (a many-tensor launch reads its record even at the end, stale or
+        // never written: no address in it is used before the pipeline ends)
+        const EncJob &job = unit_job<kBatch>(p, recs, r);
+        const uint64_t uc = kBatch ? recs[r].c : u;
         const uint32_t s_shift = 31u - __clz(job.S);
         const uint32_t tps = job.S / kUThr; // threads per sub-block: 2..32
         // a many-tensor launch: a broken codebook codes nothing; the length
         // table is the slot's (the loader fills it with the input)
-        const bool cb_ok = !kBatch || end || codebook_ok(job.cb);
-        const uint8_t *len = kBatch ? lens + slot * kLutRows : lens;
+        const bool cb_ok = !kBatch || recs[r].cb_ok;
         const uint64_t ubase = end ? 0 : uc * kUSyms;
         const uint32_t L = end || !cb_ok ? 0u : (uint32_t)min((uint64_t)kUSyms, job.n - ubase);
         const uint32_t cnt = s0 < L ? min(kUThr, L - s0) : 0u;
@@ -700,16 +734,23 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint
         uint32_t B;
         {
             const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16u);
-            if (cnt == kUThr) {
-                B = len4(len, a.x) + len4(len, a.y) + len4(len, a.z) + len4(len, a.w) + len4(len, b.x) +
-                    len4(len, b.y) + len4(len, b.z) + len4(len, b.w);
-            } else {
+            auto count = [&](const uint8_t *len) {
+                if (cnt == kUThr)
+                    return len4(len, a.x) + len4(len, a.y) + len4(len, a.z) + len4(len, a.w) + len4(len, b.x) +
+                           len4(len, b.y) + len4(len, b.z) + len4(len, b.w);
                 const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                B = 0;
+                uint32_t n = 0;
 #pragma unroll
                 for (uint32_t j = 0; j < kUThr; ++j)
-                    B += j < cnt ? (uint32_t)len[byte_of(len_rot4(wd[j >> 2]), j & 3)] : 0u;
-            }
+                    n += j < cnt ? (uint32_t)len[byte_of(len_rot4(wd[j >> 2]), j & 3)] : 0u;
+                return n;
+            };
+            // (a many-tensor launch: the slot's table, each at a fixed
+            // address, so that the lookups take it as an immediate offset)
+            if constexpr (kBatch)
+                B = slot ? count(lens + kLutRows) : count(lens);
+            else
+                B = count(lens);
         }
 
         // ---- phase B: positions, sub-block counts, the unit's size
@@ -865,12 +906,14 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint
 // Claims units in ticket order, one slot at a time as the compute warps finish
 // the unit in it (phase C reads the input again) and size the next one, and
 // bulk-copies each unit's input (lane 0 alone).
-// A many-tensor launch: the loader also fills the slot's length table for
-// the unit's codebook (when it is not the one the slot's table holds) before
-// the slot's arrival, as it does the input bytes it copies itself.
+// A many-tensor launch: the loader also writes the unit's record and fills
+// the slot's length table for the unit's codebook (when it is not the one
+// the slot's table holds) before the slot's arrival, as it does the input
+// bytes it copies itself.
 template <bool kBatch = false>
 __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8_t *in0,
-                                            [[maybe_unused]] uint8_t *lens, uint32_t lane)
+                                            [[maybe_unused]] uint8_t *lens, [[maybe_unused]] UUnitRec *recs,
+                                            uint32_t lane)
 {
     if (lane != 0)
         return;
@@ -905,19 +948,28 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
         const uint32_t whole = L & ~15u;
         for (uint32_t i = whole; i < L; ++i) // the tensor's last bytes (fewer than 16)
             buf[i] = job.in[ubase + i];
+        fence_proxy_async();
         if constexpr (kBatch) {
-            if (job.cb != (slot ? held1 : held0) && codebook_ok(job.cb)) {
+            // the input copy first; the record and the length table (more
+            // dependent loads) while it runs, published by the arrival
+            mbar_expect_tx_only(&P.full[slot], whole);
+            if (whole)
+                bulk_g2s(buf, job.in + ubase, whole, &P.full[slot]);
+            const bool ok = codebook_ok(job.cb);
+            recs[k & (kURecs - 1u)] = UUnitRec{job, I.c, p.descs[I.tensor].t_done_ns, I.tensor, ok ? 1u : 0u};
+            if (job.cb != (slot ? held1 : held0) && ok) {
                 unit_load_len(job.cb, lens + slot * kLutRows, 0u, 1u);
                 if (slot)
                     held1 = job.cb;
                 else
                     held0 = job.cb;
             }
+            mbar_arrive(&P.full[slot]);
+        } else {
+            mbar_expect_tx(&P.full[slot], whole);
+            if (whole)
+                bulk_g2s(buf, job.in + ubase, whole, &P.full[slot]);
         }
-        fence_proxy_async();
-        mbar_expect_tx(&P.full[slot], whole);
-        if (whole)
-            bulk_g2s(buf, job.in + ubase, whole, &P.full[slot]);
     }
 }
 
@@ -925,7 +977,8 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
 // For each unit: its offset (look-back, while the compute warps pack it),
 // chunk_off, total_bits, then the stage to the output with one bulk copy.
 template <bool kOne, bool kBatch = false>
-__device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint32_t st0, uint32_t lane)
+__device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, [[maybe_unused]] const UUnitRec *recs,
+                                            uint32_t st0, uint32_t lane)
 {
     const uint32_t G = kOne ? 1u : kUSyms / p.job.C;
     const uint32_t wpc = kOne ? kUWarps : p.job.C / (32u * kUThr);
@@ -954,11 +1007,10 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
             break;
         // the unit's job, and the unit's index in it (a many-tensor launch:
         // its chunk of its tensor, whose look-back it runs)
-        const UItem I = kBatch ? unit_item(p, u) : UItem{p.job, u, 0u};
-        const EncJob &job = I.job;
-        const uint64_t uc = I.c;
+        const EncJob &job = unit_job<kBatch>(p, recs, r);
+        const uint64_t uc = kBatch ? recs[r].c : u;
         const uint64_t n_chunks = (job.n + job.C - 1) / job.C;
-        const bool cb_ok = !kBatch || codebook_ok(job.cb); // else the compute warps coded nothing
+        const bool cb_ok = !kBatch || recs[r].cb_ok; // else the compute warps coded nothing
         const uint64_t ubase = uc * kUSyms;
         const uint32_t L = cb_ok ? (uint32_t)min((uint64_t)kUSyms, job.n - ubase) : 0u;
         const ULayout lay = unit_layout<kOne>(x, lane, wpc);
@@ -968,14 +1020,15 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         for (int o = 16; o; o >>= 1)
             ubits += __shfl_xor_sync(~0u, ubits, o);
         bool to = false;
-        const int64_t kn = kBatch && known_t != I.tensor ? -1 : known;
+        const uint32_t tensor = kBatch ? recs[r].tensor : 0u;
+        const int64_t kn = kBatch && known_t != tensor ? -1 : known;
         const uint64_t prefix = unit_lookback(job.flags, uc, kn, known_incl, p.timeout_ns, &to);
         if (lane == 0) // the unit's inclusive prefix, for the look-backs of later units
             st_relaxed(job.flags + uc, kFlagPrefix | ((prefix + ubytes) & kValueMask));
         known = (int64_t)uc;
         known_incl = prefix + ubytes;
         if constexpr (kBatch)
-            known_t = I.tensor;
+            known_t = tensor;
         const uint64_t c0 = uc * G;
         const bool chunk_end = lane < kUWarps && (lane & (wpc - 1u)) == wpc - 1u; // a chunk's last lane
         const bool chunk_real = chunk_end && c0 + lane / wpc < n_chunks;
@@ -1028,11 +1081,11 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, uint3
         if constexpr (kBatch) {
             // the tensor's completion stamp: its segments counted as the
             // deferred pass counts them, by whichever launch codes the chunk
-            uint64_t *t_done = p.descs[I.tensor].t_done_ns;
+            uint64_t *t_done = recs[r].t_done;
             if (lane == 0 && t_done && !(deferred && write)) {
                 __threadfence();
                 const uint32_t nseg = job.C / seg_symbols(job.C, job.S);
-                if (atomicAdd(p.done + I.tensor, nseg) + nseg == nseg * (uint32_t)n_chunks)
+                if (atomicAdd(p.done + tensor, nseg) + nseg == nseg * (uint32_t)n_chunks)
                     *t_done = globaltimer();
             }
         }
@@ -1237,7 +1290,8 @@ __device__ __forceinline__ void unit_storer_split(const UnitParams &p, UPipe &P,
 // many-tensor launch loads the code tables at each unit whose codebook is
 // not the last one's (the units come sorted by codebook).
 template <int kMode, bool kBatch>
-__device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit_smem, uint8_t *len_table)
+__device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit_smem, uint8_t *len_table,
+                                              UUnitRec *recs)
 {
     uint2 *lut = reinterpret_cast<uint2 *>(unit_smem);
     UPipe &P = *reinterpret_cast<UPipe *>(unit_smem + kULutBytes);
@@ -1282,13 +1336,13 @@ __device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit
     __syncthreads();
     const uint32_t st0 = smem_u32(base + 2 * kUSyms);
     if (warp < kUWarps)
-        unit_compute<kMode, kBatch>(p, P, lut, len_table, smem_u32(base), st0, warp, lane);
+        unit_compute<kMode, kBatch>(p, P, lut, len_table, recs, smem_u32(base), st0, warp, lane);
     else if (warp == kUWarps)
-        unit_loader<kBatch>(p, P, base, len_table, lane);
+        unit_loader<kBatch>(p, P, base, len_table, recs, lane);
     else if constexpr (kMode == kUnitSplit)
         unit_storer_split(p, P, st0, lane);
     else
-        unit_storer<kMode == kUnitOne, kBatch>(p, P, st0, lane);
+        unit_storer<kMode == kUnitOne, kBatch>(p, P, recs, st0, lane);
 }
 
 // Two CTAs an SM (56 registers a thread): one CTA's barrier waits and
@@ -1298,7 +1352,7 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_kernel(UnitParams p)
 {
     extern __shared__ __align__(128) uint8_t unit_smem[];
     __shared__ uint8_t len_table[kLutRows]; // code length of byte b at len_rot(b) (at most ECC_MAX_CODE_LEN; 0: no code)
-    unit_pipeline<kMode, false>(p, unit_smem, len_table);
+    unit_pipeline<kMode, false>(p, unit_smem, len_table, nullptr);
 }
 
 // The many-tensor launch: tensors of chunks of kUSyms symbols, a chunk a
@@ -1307,13 +1361,20 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_batched_kernel(UnitP
 {
     extern __shared__ __align__(128) uint8_t unit_smem[];
     __shared__ uint8_t len_table[2 * kLutRows]; // a length table for each input slot
-    unit_pipeline<kUnitOne, true>(p, unit_smem, len_table);
+    __shared__ UUnitRec recs[kURecs];           // the records of the units in flight
+    unit_pipeline<kUnitOne, true>(p, unit_smem, len_table, recs);
 }
 
 // ---------------------------------------------------------------- host side
+// static shared bytes of the kernels, rounded up (the length tables, the
+// unit records)
+constexpr uint32_t kUStaticOne = 512, kUStaticBatch = 1024;
+static_assert(kLutRows <= kUStaticOne && 2 * kLutRows + kURecs * sizeof(UUnitRec) <= kUStaticBatch,
+              "static shared bytes");
 // Largest stage (multiple of 16, at most 32 KiB: 16 bits a symbol) with
-// which two CTAs fit one SM; 0 if none.
-uint32_t unit_stage_bytes()
+// which two CTAs fit one SM beside static_bytes of static shared memory
+// each; 0 if none.
+uint32_t unit_stage_bytes(uint32_t static_bytes)
 {
     int dev = 0, per_sm = 0, reserved = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1322,7 +1383,7 @@ uint32_t unit_stage_bytes()
         (void)cudaGetLastError();
         return 0;
     }
-    const int64_t per_cta = std::min<int64_t>(per_sm / 2 - reserved, (int64_t)kMaxDynSmem) - 512; // static shared bytes
+    const int64_t per_cta = std::min<int64_t>(per_sm / 2 - reserved, (int64_t)kMaxDynSmem) - static_bytes;
     const int64_t room = per_cta - (int64_t)unit_smem_bytes(0);
     if (room < 2 * 16)
         return 0;
@@ -1343,7 +1404,7 @@ ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t
     p.mlog = job.C > kUSyms ? 31u - __builtin_clz(job.C / kUSyms) : 0u;
     p.ticket = ticket;
     p.timeout_ns = kWaitLimitNs;
-    p.stage_bytes = unit_stage_bytes();
+    p.stage_bytes = unit_stage_bytes(kUStaticOne);
     if (p.stage_bytes < 16u)
         return ECC_ERR_CUDA;
     const int mode = job.C == kUSyms ? kUnitOne : job.C < kUSyms ? kUnitGroup : kUnitSplit;
@@ -1383,7 +1444,7 @@ ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st)
     p.n_units = b.n_units;
     p.ticket = b.ticket;
     p.timeout_ns = kWaitLimitNs;
-    p.stage_bytes = unit_stage_bytes();
+    p.stage_bytes = unit_stage_bytes(kUStaticBatch);
     p.items = b.items;
     p.descs = b.descs;
     p.done = b.done;
