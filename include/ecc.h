@@ -74,7 +74,9 @@ enum {
     ECC_ERR_CHECK = 7     /* an internal check failed: in index-checked builds (-DECC_CHECKED) a
                              kernel index was out of range and the access skipped; in any build,
                              chunks of more than 16384 symbols coded to other sizes than their
-                             length pass counted (nothing is written for such a chunk) */
+                             length pass counted, or a batched encode's second pass (chunks
+                             with long codes) sizing a chunk otherwise than its first pass
+                             placed it (nothing is written for such a chunk) */
 };
 
 enum { ECC_FAMILY_QLC = 1, ECC_FAMILY_HUFFMAN = 2, ECC_FAMILY_ESCAPE = 3 };

@@ -23,8 +23,10 @@ namespace ecc {
 
 // Workspace layout (all offsets 16-byte aligned):
 //   header | descs[count] | prefix[count + 1] | done[count] | item[n_items] | flags[total_chunks]
+//   | deferred[total_chunks]
 // descs are in workspace order (sorted by codebook); prefix[d] = first item
-// of tensor d; flags = look-back words (encode only).
+// of tensor d; flags = look-back words, deferred = the positions of the
+// chunks the unit encoder left to its second pass (encode only).
 struct BatchHeader {
     uint32_t ticket;
     uint32_t count;
@@ -33,16 +35,18 @@ struct BatchHeader {
     uint32_t max_C;
     uint32_t encode;
     uint32_t ws_slot_bytes; // encode: stage slot of the warp-specialised kernel (largest over the tensors)
+    uint32_t n_deferred;    // encode: entries of deferred[]
+    uint32_t ticket2;       // encode: the unit encoder's second pass
     uint32_t pad;
     uint64_t n_items;     // encode: chunks; decode: pieces, each codebook run padded to a multiple of warps
     uint64_t total_chunks;
-    uint64_t desc_off, prefix_off, done_off, item_off, flags_off;
+    uint64_t desc_off, prefix_off, done_off, item_off, flags_off, deferred_off;
 };
 
 constexpr uint64_t kNoItem = ~0ull; // item of a padding position
 
 struct BatchLayout {
-    size_t desc_off, prefix_off, done_off, item_off, flags_off, bytes;
+    size_t desc_off, prefix_off, done_off, item_off, flags_off, deferred_off, bytes;
 };
 
 static size_t up16(size_t v) { return (v + 15) & ~size_t(15); }
@@ -55,7 +59,8 @@ static BatchLayout layout_for(uint32_t count, uint64_t n_items, uint64_t flag_wo
     L.done_off = up16(L.prefix_off + ((size_t)count + 1) * sizeof(uint64_t));
     L.item_off = up16(L.done_off + (size_t)count * sizeof(uint32_t));
     L.flags_off = up16(L.item_off + n_items * sizeof(uint64_t));
-    L.bytes = up16(L.flags_off + flag_words * sizeof(uint64_t));
+    L.deferred_off = up16(L.flags_off + flag_words * sizeof(uint64_t));
+    L.bytes = up16(L.deferred_off + flag_words * sizeof(uint32_t));
     return L;
 }
 
@@ -504,6 +509,7 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
     h->done_off = L.done_off;
     h->item_off = L.item_off;
     h->flags_off = L.flags_off;
+    h->deferred_off = L.deferred_off;
     ecc_desc *sorted = reinterpret_cast<ecc_desc *>(img.data() + L.desc_off);
     for (uint32_t j = 0; j < count; ++j)
         sorted[j] = descs[P.order[j]];
@@ -532,16 +538,21 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
         };
         if (P.units) {
             uint8_t *w = (uint8_t *)ws;
+            BatchHeader *wh = reinterpret_cast<BatchHeader *>(w);
             const UnitBatch ub{reinterpret_cast<const uint64_t *>(w + L.item_off),
                                reinterpret_cast<const ecc_desc *>(w + L.desc_off),
                                reinterpret_cast<uint64_t *>(w + L.flags_off),
                                reinterpret_cast<uint32_t *>(w + L.done_off),
-                               &reinterpret_cast<BatchHeader *>(w)->ticket,
+                               &wh->ticket,
                                sorted[0].status,
                                t_start,
-                               P.total_chunks};
+                               P.total_chunks,
+                               reinterpret_cast<uint32_t *>(w + L.deferred_off),
+                               &wh->n_deferred,
+                               &wh->ticket2};
+            // (its second pass codes the chunks it could not stage)
             if (launch_unit_encoder_batched(ub, st) == ECC_OK)
-                return deferred();
+                return ECC_OK;
         }
         const size_t ws_smem = enc_ws_smem_bytes(P.max_C, P.ws_slot);
         const int occ_ws = ws_smem <= kMaxDynSmem - kStaticSmemReserve

@@ -53,10 +53,13 @@ int occupancy(const void *kernel, int threads, size_t smem);
 // (unit_chunks: the chunks of a unit, for the deferred pass)
 ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t st, uint32_t *unit_chunks);
 // The unit encoder over many tensors whose chunks are all of 16384 symbols,
-// a chunk a unit (ecc_units.cu): unit k is chunk items[k] & 0xFFFFFFFF of
-// tensor descs[items[k] >> 32]; flags: a look-back word per unit (zeroed);
-// done: a counter per tensor (zeroed) for the completion stamps; status:
-// where waits that end before their unit is known report.
+// a chunk a unit (ecc_units.cu), in two launches: unit k is chunk items[k] &
+// 0xFFFFFFFF of tensor descs[items[k] >> 32]; flags: a look-back word per
+// unit (zeroed); done: a counter per tensor (zeroed) for the completion
+// stamps; status: where waits that end before their unit is known report;
+// deferred[*n_deferred] (zeroed count): the units the first launch sized
+// and placed but could not stage, which the second one codes (its tickets
+// from *ticket2, zeroed).
 struct UnitBatch {
     const uint64_t *items;
     const ecc_desc *descs;
@@ -66,6 +69,9 @@ struct UnitBatch {
     uint32_t *status;
     uint64_t *t_start;
     uint64_t n_units;
+    uint32_t *deferred;
+    uint32_t *n_deferred;
+    uint32_t *ticket2;
 };
 ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st);
 

@@ -133,6 +133,10 @@ struct UnitParams {
     const ecc_desc *descs;
     uint32_t *done;
     uint64_t *t_start;
+    // the units the first pass sized and placed but could not stage (their
+    // positions, *n_deferred of them), coded by the second pass
+    uint32_t *deferred;
+    uint32_t *n_deferred;
 };
 
 // Unit k of a many-tensor launch: its chunk as a job of its own (look-back
@@ -692,12 +696,13 @@ __device__ __forceinline__ void unit_load_len(const ecc_codebook *cb, uint8_t *l
 
 // (lens: the length table; a many-tensor launch: one a slot, and the unit
 // records recs)
-template <int kMode, bool kBatch = false>
+template <int kMode, bool kBatch = false, bool kFixed = false>
 __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint2 *lut, const uint8_t *lens,
                                              [[maybe_unused]] const UUnitRec *recs, uint32_t in0, uint32_t st0,
                                              uint32_t w, uint32_t lane)
 {
     static_assert(!kBatch || kMode == kUnitOne, "a many-tensor launch codes a chunk a unit");
+    static_assert(!kFixed || kBatch, "the second pass is a many-tensor launch's");
     constexpr bool kOne = kMode != kUnitGroup; // the unit's codes are one run (one chunk, or part of one)
     // stage words in memory order (the storer copies them out as they are),
     // or in register order (split chunks: the storer shifts them first)
@@ -801,7 +806,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint
                 if (!clast)
                     st_relaxed(p.uflags + u, kFlagAggregate | utot);
             }
-        } else {
+        } else if (!kFixed) { // (the second pass: the first published it)
             st_relaxed_pred(job.flags + uc, kFlagAggregate | ubytes, t == 0 && uc != 0);
         }
         st_shared_u64_pred(&P.sunit[r], u, t == 0);
@@ -810,7 +815,8 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint
             const uint32_t sb = __shfl_sync(~0u, incl, lane | (tps - 1u)) - (incl - B);
             const uint64_t sidx = (ubase + s0) >> s_shift;
             const uint64_t n_sub = (job.n + job.S - 1) >> s_shift;
-            st_global_u16_pred(job.sub_bits + sidx, sb, cnt && (lane & (tps - 1u)) == 0 && sidx < n_sub);
+            st_global_u16_pred(job.sub_bits + sidx, sb,
+                               !kFixed && cnt && (lane & (tps - 1u)) == 0 && sidx < n_sub);
         }
         const bool over = ubytes > p.stage_bytes;
         // the stage of this slot is free once the unit two back has been stored
@@ -910,7 +916,7 @@ __device__ __forceinline__ void unit_compute(const UnitParams &p, UPipe &P, uint
 // the slot's length table for the unit's codebook (when it is not the one
 // the slot's table holds) before the slot's arrival, as it does the input
 // bytes it copies itself.
-template <bool kBatch = false>
+template <bool kBatch = false, bool kFixed = false>
 __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8_t *in0,
                                             [[maybe_unused]] uint8_t *lens, [[maybe_unused]] UUnitRec *recs,
                                             uint32_t lane)
@@ -918,6 +924,9 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
     if (lane != 0)
         return;
     [[maybe_unused]] const ecc_codebook *held0 = nullptr, *held1 = nullptr; // codebooks of the slots' length tables
+    // the second pass: its units are the first pass's deferred list (written
+    // by the previous launch)
+    const uint64_t n_claims = kFixed ? (uint64_t)*(volatile uint32_t *)p.n_deferred : p.n_units;
     for (uint64_t k = 0; k <= p.n_units; ++k) {
         const uint32_t slot = (uint32_t)k & 1u;
         bool stop = false;
@@ -933,12 +942,12 @@ __device__ __forceinline__ void unit_loader(const UnitParams &p, UPipe &P, uint8
             stop = true;
         }
         const uint32_t tk = stop ? 0xFFFFFFFFu : atomicAdd(p.ticket, 1u);
-        if (tk >= p.n_units) {
+        if (tk >= n_claims) {
             P.unit[slot] = kUEnd;
             mbar_arrive(&P.full[slot]);
             return;
         }
-        const uint64_t u = tk;
+        const uint64_t u = kFixed ? (uint64_t)p.deferred[tk] : (uint64_t)tk;
         P.unit[slot] = u;
         const UItem I = kBatch ? unit_item(p, u) : UItem{p.job, u, 0u};
         const EncJob &job = I.job;
@@ -1056,8 +1065,11 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, [[may
         if (deferred) {
             // the unit outgrew the stage (long codes): left to the deferred
             // pass, a warp a unit over the whole GPU after this kernel
-            if (write && lane == 0)
+            if (write && lane == 0) {
                 st_relaxed(job.flags + uc, kFlagPrefix | kFlagDeferred | ((prefix + ubytes) & kValueMask));
+                if constexpr (kBatch) // for the second pass
+                    p.deferred[atomicAdd(p.n_deferred, 1u)] = (uint32_t)u;
+            }
         } else if (write) {
             const uint32_t st = st0 + slot * p.stage_bytes;
             // words shared across warps: warp `lane`'s first word takes the
@@ -1088,6 +1100,80 @@ __device__ __forceinline__ void unit_storer(const UnitParams &p, UPipe &P, [[may
                 if (atomicAdd(p.done + tensor, nseg) + nseg == nseg * (uint32_t)n_chunks)
                     *t_done = globaltimer();
             }
+        }
+        __syncwarp();
+    }
+    if (lane == 0)
+        bulk_wait_all();
+}
+
+// The second pass's storer (many-tensor launch): its units are chunks the
+// first pass sized and placed at chunk_off but could not stage; with the
+// larger stage of one CTA an SM they are staged and stored like any other
+// (a unit still too long, more than 32 bits a symbol, is coded by this warp
+// into the output directly).  No look-back: the places are known.
+__device__ __forceinline__ void unit_storer_fixed(const UnitParams &p, UPipe &P, const UUnitRec *recs, uint32_t st0,
+                                                  uint32_t lane)
+{
+    for (uint64_t k = 0; k <= p.n_units; ++k) {
+        const uint32_t slot = (uint32_t)k & 1u, par = (uint32_t)(k >> 1) & 1u, r = (uint32_t)k & 3u;
+        if (!mbar_wait(&P.agg[r], (uint32_t)(k >> 2) & 1u, p.timeout_ns)) {
+            if (lane == 0)
+                set_status(p.job.status, ECC_ERR_TIMEOUT);
+            break;
+        }
+        const uint64_t u = *(volatile uint64_t *)&P.sunit[r];
+        const uint32_t x = lane < kUWarps ? P.wtot[r][lane] : 0u;
+        __syncwarp();
+        if (k > 0 && lane == 0) { // the previous unit's stage is free again (as unit_storer)
+            bulk_wait_read();
+            mbar_arrive(&P.st_free[slot ^ 1u]);
+        }
+        if (u == kUEnd)
+            break;
+        const UUnitRec &R = recs[r];
+        const EncJob &job = R.job;
+        const uint64_t uc = R.c;
+        const uint64_t n_chunks = (job.n + job.C - 1) / job.C;
+        const uint32_t L = (uint32_t)min((uint64_t)kUSyms, job.n - uc * kUSyms);
+        const ULayout lay = unit_layout<true>(x, lane, kUWarps);
+        const uint32_t ubytes = __shfl_sync(~0u, lay.Y, kUWarps - 1u);
+        const uint64_t o0 = job.chunk_off[uc], o1 = job.chunk_off[uc + 1];
+        const bool placed = o0 + ubytes == o1 && o1 <= job.out_cap; // where the first pass put it
+        if (!placed && lane == 0)
+            set_status(job.status, ECC_ERR_CHECK);
+        if (!mbar_wait(&P.done[slot], par, p.timeout_ns)) { // the compute warps have packed the unit
+            if (lane == 0)
+                set_status(job.status, ECC_ERR_TIMEOUT);
+            break;
+        }
+        if (ubytes > p.stage_bytes) {
+            if (placed)
+                encode_chunk_warp(job, uc, reinterpret_cast<uint32_t *>(job.out + o0), (uint32_t)((o1 - o0) / 4u));
+        } else if (placed) {
+            const uint32_t st = st0 + slot * p.stage_bytes;
+            // words shared across warps, then the chunk's zero padding (as unit_storer)
+            if (lane > 0 && lane < kUWarps && lane * 32u * kUThr < L) {
+                const uint32_t bit = lay.base * 8u + lay.E;
+                if (bit & 31u)
+                    red_or_shared(st + (bit >> 5) * 4u, P.wtail[slot][lane - 1]);
+            }
+            if (lane == kUWarps - 1u) {
+                const uint32_t cb0 = lay.Y - (lay.cbits + 127u) / 128u * 16u;
+                for (uint32_t a2 = cb0 + (lay.cbits + 31u) / 32u * 4u; a2 < lay.Y; a2 += 4u)
+                    st_shared_u32(st + a2, 0u);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0 && ubytes)
+                bulk_s2g(job.out + o0, st, ubytes);
+        }
+        // the tensor's completion stamp (the first pass left these chunks' segments to be counted here)
+        if (lane == 0 && R.t_done) {
+            __threadfence();
+            const uint32_t nseg = job.C / seg_symbols(job.C, job.S);
+            if (atomicAdd(p.done + R.tensor, nseg) + nseg == nseg * (uint32_t)n_chunks)
+                *R.t_done = globaltimer();
         }
         __syncwarp();
     }
@@ -1289,7 +1375,7 @@ __device__ __forceinline__ void unit_storer_split(const UnitParams &p, UPipe &P,
 // The pipeline of one CTA: tables, barriers, then the warps' roles.  A
 // many-tensor launch loads the code tables at each unit whose codebook is
 // not the last one's (the units come sorted by codebook).
-template <int kMode, bool kBatch>
+template <int kMode, bool kBatch, bool kFixed = false>
 __device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit_smem, uint8_t *len_table,
                                               UUnitRec *recs)
 {
@@ -1298,7 +1384,7 @@ __device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit
     uint8_t *const base = unit_smem + kULutBytes + sizeof(UPipe);
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if constexpr (kBatch) {
-        if (p.t_start && blockIdx.x == 0 && threadIdx.x == 0)
+        if (!kFixed && p.t_start && blockIdx.x == 0 && threadIdx.x == 0)
             *p.t_start = globaltimer();
     } else {
         const ecc_codebook *cb = p.job.cb;
@@ -1336,11 +1422,13 @@ __device__ __forceinline__ void unit_pipeline(const UnitParams &p, uint8_t *unit
     __syncthreads();
     const uint32_t st0 = smem_u32(base + 2 * kUSyms);
     if (warp < kUWarps)
-        unit_compute<kMode, kBatch>(p, P, lut, len_table, recs, smem_u32(base), st0, warp, lane);
+        unit_compute<kMode, kBatch, kFixed>(p, P, lut, len_table, recs, smem_u32(base), st0, warp, lane);
     else if (warp == kUWarps)
-        unit_loader<kBatch>(p, P, base, len_table, recs, lane);
+        unit_loader<kBatch, kFixed>(p, P, base, len_table, recs, lane);
     else if constexpr (kMode == kUnitSplit)
         unit_storer_split(p, P, st0, lane);
+    else if constexpr (kFixed)
+        unit_storer_fixed(p, P, recs, st0, lane);
     else
         unit_storer<kMode == kUnitOne, kBatch>(p, P, recs, st0, lane);
 }
@@ -1365,16 +1453,26 @@ __global__ void __launch_bounds__(kUThreads, 2) encode_unit_batched_kernel(UnitP
     unit_pipeline<kUnitOne, true>(p, unit_smem, len_table, recs);
 }
 
+// Its second pass: the units the first could not stage, with the stage of
+// one CTA an SM.
+__global__ void __launch_bounds__(kUThreads, 1) encode_unit_fixed_kernel(UnitParams p)
+{
+    extern __shared__ __align__(128) uint8_t unit_smem[];
+    __shared__ uint8_t len_table[2 * kLutRows];
+    __shared__ UUnitRec recs[kURecs];
+    unit_pipeline<kUnitOne, true, true>(p, unit_smem, len_table, recs);
+}
+
 // ---------------------------------------------------------------- host side
 // static shared bytes of the kernels, rounded up (the length tables, the
 // unit records)
 constexpr uint32_t kUStaticOne = 512, kUStaticBatch = 1024;
 static_assert(kLutRows <= kUStaticOne && 2 * kLutRows + kURecs * sizeof(UUnitRec) <= kUStaticBatch,
               "static shared bytes");
-// Largest stage (multiple of 16, at most 32 KiB: 16 bits a symbol) with
-// which two CTAs fit one SM beside static_bytes of static shared memory
-// each; 0 if none.
-uint32_t unit_stage_bytes(uint32_t static_bytes)
+// Largest stage (multiple of 16; at most 16 bits a symbol for two CTAs an
+// SM, 32 for one) with which `ctas` CTAs fit one SM beside static_bytes of
+// static shared memory each; 0 if none.
+uint32_t unit_stage_bytes(uint32_t static_bytes, int ctas = 2)
 {
     int dev = 0, per_sm = 0, reserved = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1383,11 +1481,11 @@ uint32_t unit_stage_bytes(uint32_t static_bytes)
         (void)cudaGetLastError();
         return 0;
     }
-    const int64_t per_cta = std::min<int64_t>(per_sm / 2 - reserved, (int64_t)kMaxDynSmem) - static_bytes;
+    const int64_t per_cta = std::min<int64_t>(per_sm / ctas - reserved, (int64_t)kMaxDynSmem) - static_bytes;
     const int64_t room = per_cta - (int64_t)unit_smem_bytes(0);
     if (room < 2 * 16)
         return 0;
-    return (uint32_t)std::min<int64_t>(room / 2 / 16 * 16, 2 * kUSyms);
+    return (uint32_t)std::min<int64_t>(room / 2 / 16 * 16, (ctas == 1 ? 4 : 2) * kUSyms);
 }
 
 // Launch the unit encoder (the prologue has cleared the flags, the ticket
@@ -1458,7 +1556,22 @@ ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st)
         return ECC_ERR_CUDA;
     const uint64_t need = (p.n_units + 1) / 2;
     const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)occ * sms, need));
+    p.deferred = b.deferred;
+    p.n_deferred = b.n_deferred;
     encode_unit_batched_kernel<<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    ecc_status e = launch_status(cudaGetLastError());
+    if (e != ECC_OK)
+        return e;
+    // the second pass: a CTA an SM, each with stages of up to 32 bits a symbol
+    UnitParams q = p;
+    q.ticket = b.ticket2;
+    q.stage_bytes = unit_stage_bytes(kUStaticBatch, 1);
+    q.t_start = nullptr;
+    const size_t smem2 = unit_smem_bytes(q.stage_bytes);
+    const int occ2 = occupancy((const void *)encode_unit_fixed_kernel, kUThreads, smem2);
+    if (q.stage_bytes < 16u || occ2 <= 0)
+        return ECC_ERR_CUDA;
+    encode_unit_fixed_kernel<<<(unsigned)(occ2 * sms), kUThreads, smem2, st>>>(q);
     return launch_status(cudaGetLastError());
 }
 
