@@ -51,13 +51,14 @@ def tensor(size, law, key):
     return np_zero_spike(size, key)
 
 
-def run_batch(books, spec, broken=()):
+def run_batch(books, spec, broken=(), data=None):
     """spec: list of (size, law, tag, C, S).  Tensors listed in `broken` get a
-    copy of their codebook with a wrong magic word."""
+    copy of their codebook with a wrong magic word; data (optional) gives
+    the tensors themselves."""
     host, dcbs, ocbs = books
     items, xs, tags = [], [], []
     for i, (size, law, tag, C, S) in enumerate(spec):
-        x = tensor(size, law, (41, i))
+        x = data[i] if data is not None else tensor(size, law, (41, i))
         cb = dcbs[tag]
         if i in broken:
             bad = host[tag].copy()
@@ -169,3 +170,24 @@ def test_batched_long_codes(books):
         size = int(g.integers(1, 5 * 16384))
         spec.append((size, 0, 3 if i % 2 == 0 else int(g.integers(0, 3)), 16384, 256 if i % 3 else 128))
     run_batch(books, spec)
+
+
+def test_batched_codes_past_the_second_stage():
+    """Fibonacci weights: codes of up to 40 bits.  Chunks of the rarest bytes
+    average about 34 bits a symbol, more than the second pass's stages hold
+    (32 bits a symbol): its storer warp codes them; chunks of about 20 bits a
+    symbol are staged by the second pass; chunks of the common bytes by the
+    first."""
+    w = np.zeros(256, np.uint64)
+    a, b = 1, 1
+    for s in range(41):
+        w[s] = a
+        a, b = b, a + b
+    host = [ecc.huff_build_canonical(w)]
+    fib = (host, [ecc.to_device(host[0])], [oracle.huffman_codebook(w)])
+    g = np.random.default_rng(31)
+    rare = g.integers(0, 12, 3 * 16384 + 77).astype(np.uint8)       # lengths 29..40
+    middle = g.integers(16, 24, 2 * 16384 + 5).astype(np.uint8)     # lengths 17..24
+    common = g.choice(41, 3 * 16384, p=w[:41] / w[:41].sum()).astype(np.uint8)
+    data = [common, rare, middle, np.concatenate([middle[:20000], rare[:30000]]), common[:5000]]
+    run_batch(fib, [(x.size, 0, 0, 16384, 256) for x in data], data=data)
