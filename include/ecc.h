@@ -328,8 +328,9 @@ ecc_status ecc_encode(const uint8_t *in, size_t n, const ecc_codebook *cb, uint3
  * ecc_decode -- chunk-parallel decode ("Quad Length Codes ...", section 2
  * "Decodifica": read 3 bits -> area -> length, read the suffix, add the
  * area's offset, a second LUT gives the byte; section 4 items 2-3; Huffman
- * codes resolve through a 14-bit first-level table and canonical per-length
- * ranges for longer codes).
+ * codes resolve through a 14-bit first-level table, then a second-level
+ * table over the few 14-bit prefixes longer codes start with, then the
+ * canonical per-length ranges).
  *   in, in_bytes device payload [in_bytes], 16-byte aligned.
  *   chunk_off    device uint64[ceil(n/C) + 1] and sub_bits device
  *                uint16[ceil(n/S)] as written by ecc_encode.
@@ -442,9 +443,10 @@ size_t ecc_batched_workspace_bytes(const ecc_desc *descs, uint32_t count);
 /*
  * ecc_encode_batched / ecc_decode_batched -- the calls above over `count`
  * tensors in one coding launch over all of them (after a prologue; the
- * encode adds the deferred pass for chunks whose codes were too long to
- * stage, and a tensor's t_done_ns is stamped by whichever launch finishes
- * its last chunk).  `descs` is a host array; the call copies it and a
+ * encode adds a second launch for the chunks whose codes were too long to
+ * stage -- when every tensor has 16 KiB chunks, the unit encoder again with
+ * larger stages, else a deferred pass of a warp a chunk -- and a tensor's
+ * t_done_ns is stamped by whichever launch finishes its last chunk).  `descs` is a host array; the call copies it and a
  * chunk prefix table into `ws` with one asynchronous host-to-device copy,
  * so `descs` may be reused once the call returns.  Every tensor obeys the
  * rules of ecc_encode / ecc_decode; its errors go to its own status word.
