@@ -372,13 +372,13 @@ __global__ void __maxnreg__(128) decode_batched_kernel(uint8_t *ws, uint64_t *t_
                 constexpr bool kQ = decltype(qlc)::value;
                 if (sp.ps == 0) {
                     if (sp.R == 2)
-                        decode_chunk<2, kQ>(job, T, wst, c, nch, nch);
+                        decode_chunk<2, kQ, true>(job, T, wst, c, nch, nch);
                     else
-                        decode_chunk<1, kQ>(job, T, wst, c, nch, nch);
+                        decode_chunk<1, kQ, true>(job, T, wst, c, nch, nch);
                 } else if (sp.R == 2) {
-                    decode_piece<2, kQ>(job, T, wst, c, piece, sp.ps);
+                    decode_piece<2, kQ, true>(job, T, wst, c, piece, sp.ps);
                 } else {
-                    decode_piece<1, kQ>(job, T, wst, c, piece, sp.ps);
+                    decode_piece<1, kQ, true>(job, T, wst, c, piece, sp.ps);
                 }
             };
             if (loaded_qlc) {

@@ -2121,6 +2121,15 @@ __device__ __forceinline__ uint32_t lds_u32_if(uint32_t addr, bool p, uint32_t v
     return v;
 }
 
+// predicated 16-bit shared load (zero-extended): v when p is false
+__device__ __forceinline__ uint32_t lds_u16_if(uint32_t addr, bool p, uint32_t v)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.shared.u16 %0, [%1];\n\t}"
+                 : "+r"(v)
+                 : "r"(addr), "r"((uint32_t)p));
+    return v;
+}
+
 // Hot-loop step: two codes the 14-bit table resolves, one window refill.
 // The first code starts at o < 32 and ends by bit 45, so the second one's
 // 14-bit peek lies in (hi, lo) or (lo, nx); after both the stream has moved
@@ -2228,7 +2237,7 @@ __device__ __forceinline__ uint32_t fstep_redo(FastStream &s, const uint16_t *de
     uint32_t e = dec[top];
     const uint32_t j = top - h.p0;
     if (e == 0 && j < h.np)
-        e = lt.sub[(j << h.kb) | ((p << ECC_PEEK_BITS) >> (32 - h.kb))];
+        e = lt.sub[(j << h.kb) | ((p << ECC_PEEK_BITS) >> (31u - h.kb) >> 1)];
     if (e == 0) {
         e = redo_long(s.hi, s.lo, s.nx, s.o, p, lt);
         bad |= (e >> 16) != 0;
@@ -2242,6 +2251,36 @@ __device__ __forceinline__ uint32_t fstep_redo(FastStream &s, const uint16_t *de
         s.wa += 4;
         s.o -= 32;
     }
+    return e;
+}
+
+// Step of an iteration in long-code mode: one code through both table
+// levels, the second-level load predicated on the first missing (no
+// branch, so the R streams interleave).  A code either level resolves has
+// at most 32 bits, so the window moves by at most one word; an unresolved
+// one has length 0 (the stream stays) and sets emin to 0 for the redo.
+// long2 records that some code took the second level.
+__device__ __forceinline__ uint32_t fstep_long(FastStream &s, const uint16_t *dec, const LongTable &lt,
+                                               const SubHdr &h, uint32_t &emin, bool &long2)
+{
+    const uint32_t p = __funnelshift_l(s.lo, s.hi, s.o);
+    const uint32_t top = p >> (32 - ECC_PEEK_BITS);
+    uint32_t e = dec[top];
+    const uint32_t j = top - h.p0;
+    const bool use2 = e == 0 && j < h.np;
+    // (kb = 0 when there is no second level: the shifts stay below 32)
+    const uint32_t idx = (j << h.kb) | ((p << ECC_PEEK_BITS) >> (31u - h.kb) >> 1);
+    e = lds_u16_if(smem_u32(lt.sub) + 2u * idx, use2, e);
+    long2 |= use2;
+    emin = min(emin, e);
+    const uint32_t o = s.o + (e >> 8);
+    const bool adv = o >= 32;
+    const uint32_t w = lds_u32_if(s.wa, adv, 0u);
+    s.hi = adv ? s.lo : s.hi;
+    s.lo = adv ? s.nx : s.lo;
+    s.nx = adv ? bswap32(w) : s.nx;
+    s.wa += adv ? 4u : 0u;
+    s.o = o & 31;
     return e;
 }
 
@@ -2352,7 +2391,7 @@ __device__ __forceinline__ uint32_t qstep2(FastStream &s, const DecTables &T, ui
 // with fstep_slow (rare: codes longer than 14 bits, or corrupt data).
 // wmax: the highest word index a stream may reach at an iteration start; a
 // stream moves at most 16 words per iteration, into the zeroed guard.
-template <int R, bool kQlc>
+template <int R, bool kQlc, bool kLong = false>
 __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTables &T, const uint32_t *words,
                                                   uint32_t wmax, uint64_t base, uint32_t g0,
                                                   const uint32_t (&st)[R], const uint32_t (&nb)[R], bool &bad)
@@ -2377,6 +2416,14 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
         dst[r] = job.out + base + (uint64_t)(g0 + (uint32_t)(r * 32 + lane)) * job.S;
         q0[r] = q1[r] = 0;
     }
+    // Long-code mode (table-decoded codes; the same in every lane of the
+    // warp): after an iteration in which some lane met a code longer than
+    // the first-level table, the next one decodes a code at a time through
+    // both table levels instead of two codes a step through the first,
+    // until an iteration takes no code from the second level.  Chunks whose
+    // data meets a codebook's long codes often (a codebook fitted to other
+    // data) then skip the fast attempt that the redo would discard.
+    bool lmode = false;
     for (uint32_t i = 0; i < job.S; i += 8) {
         FastStream s0[R];
         uint32_t a[R], b[R], emin[R];
@@ -2387,7 +2434,21 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
             a[r] = b[r] = 0;
             emin[r] = ~0u;
         }
-        {
+        bool long2 = false; // some code of this lane took the second level
+        const bool was_long = !kQlc && kLong && lmode;
+        if (was_long) {
+            const SubHdr sh{lt.sub_p0, lt.sub_np, lt.sub_kb};
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t e = fstep_long(s[r], dec, lt, sh, emin[r], long2);
+                    if (t < 4)
+                        a[r] = __byte_perm(a[r], e, 0x4321);
+                    else
+                        b[r] = __byte_perm(b[r], e, 0x4321);
+                }
+        } else {
             uint32_t h[R][4];
 #pragma unroll
             for (int t = 0; t < 4; ++t)
@@ -2404,7 +2465,11 @@ __device__ __forceinline__ void decode_group_fast(const DecJob &job, const DecTa
 #pragma unroll
         for (int r = 0; r < R; ++r)
             esc |= (!kQlc && emin[r] == 0) ? (1u << r) : 0u;
-        if (!kQlc && __any_sync(~0u, esc != 0)) {
+        // (fast mode: the one vote, as before long-code mode existed)
+        const bool any_esc = !kQlc && __any_sync(~0u, esc != 0);
+        if (!kQlc && kLong)
+            lmode = was_long ? __any_sync(~0u, esc != 0 || long2) : any_esc;
+        if (any_esc) {
             // the lane's streams that met one, from their saved states, a
             // code at a time (one stream after the other: interleaving the
             // streams was slower, for the long-code chunks and the rest)
@@ -2521,7 +2586,7 @@ __device__ __forceinline__ bool chunk_tail_bad(const DecJob &job, uint64_t b0, u
 // sub-blocks at the longest fast code lengths.  carry0: the chunk's bits
 // before g_begin; `last`: the range ends the chunk, so its end is checked
 // against the chunk's size and zero padding.
-template <bool kQlc>
+template <bool kQlc, bool kLong = false>
 static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, const DecTables &T, WarpStage &ws,
                                                            uint64_t base, uint32_t g_begin, uint32_t g_end,
                                                            uint64_t sub0, uint64_t b0, uint32_t bytes,
@@ -2576,7 +2641,7 @@ static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, co
             ws.buf[(s1 - s0) / 4 + lane] = 0; // guard: reads past the end see 0
         __syncwarp();
         const uint32_t st[1] = {carry + incl - v - s0 * 8u}, nb[1] = {v};
-        decode_group_fast<1, kQlc>(job, T, ws.buf, (s1 - s0) / 4 + 4, base, g0, st, nb, bad);
+        decode_group_fast<1, kQlc, kLong>(job, T, ws.buf, (s1 - s0) / 4 + 4, base, g0, st, nb, bad);
         carry += gbits;
     }
     if (last)
@@ -2589,7 +2654,7 @@ static __device__ __noinline__ void decode_chunk_in_groups(const DecJob &job, co
 // Decode chunk c with one warp.  The compressed chunk is staged into the
 // warp's shared buffer by one bulk copy (when it fits), while the lanes scan
 // sub_bits; next_c (if valid) is prefetched into L2 for the warp's next call.
-template <int R, bool kQlc>
+template <int R, bool kQlc, bool kLong = false>
 __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables &T, WarpStage &ws, uint64_t c,
                                              uint64_t next_c, uint64_t n_chunks)
 {
@@ -2610,7 +2675,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables 
     const uint32_t bytes = (uint32_t)(b1 - b0);
     const bool staged = ws.buf != nullptr && bytes + kStageGuard <= ws.bytes;
     if (!staged && ws.buf != nullptr && L == job.C && nsub >= 32 && (nsub & 31) == 0) {
-        decode_chunk_in_groups<kQlc>(job, T, ws, base, 0, nsub, sub0, b0, bytes, 0, true);
+        decode_chunk_in_groups<kQlc, kLong>(job, T, ws, base, 0, nsub, sub0, b0, bytes, 0, true);
         return;
     }
     if (staged) {
@@ -2671,7 +2736,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables 
         // the hot loop needs every lane to own R full sub-blocks
         if (staged && L == job.C && nsub - g0 >= 32u * R) {
             const uint32_t wmax = bytes / 4 + 4; // + up to 2 words per step x 8 steps < guard
-            decode_group_fast<R, kQlc>(job, T, words, wmax, base, g0, st, nb, bad);
+            decode_group_fast<R, kQlc, kLong>(job, T, words, wmax, base, g0, st, nb, bad);
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -2709,7 +2774,7 @@ __device__ __forceinline__ void decode_chunk(const DecJob &job, const DecTables 
 // widened to 16-byte boundaries of the chunk, are staged by one bulk copy
 // when they fit.  The piece that ends the chunk also checks the chunk's size
 // and zero padding.
-template <int R, bool kQlc>
+template <int R, bool kQlc, bool kLong = false>
 __device__ __forceinline__ void decode_piece(const DecJob &job, const DecTables &T, WarpStage &ws, uint64_t c,
                                              uint32_t piece, uint32_t pshift)
 {
@@ -2772,7 +2837,7 @@ __device__ __forceinline__ void decode_piece(const DecJob &job, const DecTables 
     const uint32_t s1 = min(pad16((carry + 7) >> 3), bytes);
     const bool staged = ws.buf != nullptr && s1 - s0 + kStageGuard <= ws.bytes;
     if (!staged && ws.buf != nullptr && full && ((g_end - g_begin) & 31) == 0) {
-        decode_chunk_in_groups<kQlc>(job, T, ws, base, g_begin, g_end, sub0, b0, bytes, carry0, last);
+        decode_chunk_in_groups<kQlc, kLong>(job, T, ws, base, g_begin, g_end, sub0, b0, bytes, carry0, last);
         return;
     }
     const uint32_t *words;
@@ -2809,7 +2874,7 @@ __device__ __forceinline__ void decode_piece(const DecJob &job, const DecTables 
     for (int r = 0; r < R; ++r)
         st[r] -= off;
     if (staged && full) {
-        decode_group_fast<R, kQlc>(job, T, words, (s1 - s0) / 4 + 4, base, g_begin, st, nb, bad);
+        decode_group_fast<R, kQlc, kLong>(job, T, words, (s1 - s0) / 4 + 4, base, g_begin, st, nb, bad);
     } else {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
