@@ -54,6 +54,16 @@
 // the earlier unit's word with one atomic, and the one that comes second
 // writes the whole word.  The chunk's last unit pads the chunk; a chunk with
 // a unit too long to stage is marked and left whole to the deferred pass.
+//
+// Many tensors at once (every tensor with chunks of 16384 symbols): the same
+// pipeline over an item map, a chunk a unit.  The loader resolves each unit
+// it claims into a shared record (its tensor's job, its chunk, the codebook
+// check, the completion stamp) and fills the slot's length table; the
+// compute warps reload the code table after the phase-B barrier of a unit
+// whose codebook differs; the look-back runs over the unit's tensor.  The
+// units too long to stage are listed, and a second launch of the pipeline,
+// one CTA an SM with stages of up to 32 bits a symbol, codes them at the
+// places the first gave them.
 
 #include <algorithm>
 
