@@ -550,9 +550,12 @@ ecc_status run_batched(const ecc_desc *descs, uint32_t count, void *ws, size_t w
                                reinterpret_cast<uint32_t *>(w + L.deferred_off),
                                &wh->n_deferred,
                                &wh->ticket2};
-            // (its second pass codes the chunks it could not stage)
-            if (launch_unit_encoder_batched(ub, st) == ECC_OK)
-                return ECC_OK;
+            // (its second pass codes the chunks it could not stage); the
+            // warp-segmented route below only if it launched nothing
+            bool launched = false;
+            const ecc_status ue = launch_unit_encoder_batched(ub, st, &launched);
+            if (ue == ECC_OK || launched)
+                return ue;
         }
         const size_t ws_smem = enc_ws_smem_bytes(P.max_C, P.ws_slot);
         const int occ_ws = ws_smem <= kMaxDynSmem - kStaticSmemReserve

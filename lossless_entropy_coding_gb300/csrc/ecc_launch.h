@@ -73,6 +73,6 @@ struct UnitBatch {
     uint32_t *n_deferred;
     uint32_t *ticket2;
 };
-ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st);
+ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st, bool *launched);
 
 } // namespace ecc

@@ -1539,9 +1539,11 @@ ecc_status launch_unit_encoder(const EncJob &job, uint32_t *ticket, cudaStream_t
 
 // The many-tensor launch over n_units chunks of kUSyms symbols (the prologue
 // has cleared flags, done and the tensors' outputs; *ticket is 0).  Returns
-// ECC_ERR_CUDA, having launched nothing, if it cannot run on this device.
-ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st)
+// ECC_ERR_CUDA with *launched false, having launched nothing, if it cannot
+// run on this device; *launched true once its first kernel is launched.
+ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st, bool *launched)
 {
+    *launched = false;
     UnitParams p{};
     // only its look-back words and status are read (the waits that end
     // before their unit is known report there)
@@ -1568,19 +1570,22 @@ ecc_status launch_unit_encoder_batched(const UnitBatch &b, cudaStream_t st)
     const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)occ * sms, need));
     p.deferred = b.deferred;
     p.n_deferred = b.n_deferred;
-    encode_unit_batched_kernel<<<(unsigned)grid, kUThreads, smem, st>>>(p);
-    ecc_status e = launch_status(cudaGetLastError());
-    if (e != ECC_OK)
-        return e;
-    // the second pass: a CTA an SM, each with stages of up to 32 bits a symbol
+    // the second pass: a CTA an SM, each with stages of up to 32 bits a
+    // symbol (checked before the first launches: the caller's other route
+    // must find the workspace untouched)
     UnitParams q = p;
     q.ticket = b.ticket2;
     q.stage_bytes = unit_stage_bytes(kUStaticBatch, 1);
     q.t_start = nullptr;
     const size_t smem2 = unit_smem_bytes(q.stage_bytes);
-    const int occ2 = occupancy((const void *)encode_unit_fixed_kernel, kUThreads, smem2);
-    if (q.stage_bytes < 16u || occ2 <= 0)
+    const int occ2 = q.stage_bytes < 16u ? 0 : occupancy((const void *)encode_unit_fixed_kernel, kUThreads, smem2);
+    if (occ2 <= 0)
         return ECC_ERR_CUDA;
+    encode_unit_batched_kernel<<<(unsigned)grid, kUThreads, smem, st>>>(p);
+    const ecc_status e = launch_status(cudaGetLastError());
+    if (e != ECC_OK)
+        return e;
+    *launched = true; // from here on an error is the call's: no other route may follow
     encode_unit_fixed_kernel<<<(unsigned)(occ2 * sms), kUThreads, smem2, st>>>(q);
     return launch_status(cudaGetLastError());
 }
